@@ -1,0 +1,268 @@
+"""CPU oracle for the fused collective + GEMM ops -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import or call this module.  The
+product path (the CUDA library and its Python binding) never does, and shares
+no code with it.
+
+What it computes is the plain definition of each fused op, written out with
+numpy in float64:
+
+* bf16 inputs are widened exactly to float64 (a bf16 value has 8 significant
+  bits, so every product of two of them is exact in float64 and every sum
+  used here carries at most float64 rounding, ~1e-16 relative);
+* contractions use ``np.matmul`` on float64 as the one library step;
+* the result is rounded ONCE to the output type: round-to-nearest-even to bf16
+  (``f64_to_bf16_bits``) or to fp32 (numpy's IEEE cast).
+
+The ops (mKernel write-up, news.chathome.org, "五种融合内核" table):
+
+* AllGather + GEMM (table row "AllGather + GEMM"): each rank holds one row
+  shard of A; the gathered A is the shards stacked in rank order and
+  C = gather(A) @ B.
+* GEMM + ReduceScatter (row "GEMM + ReduceScatter"): S = sum_r A_r @ B_r;
+  row block o of S (rows [o*m/R, (o+1)*m/R)) belongs to rank o.
+* GEMM + AllReduce (row "GEMM + AllReduce"): S as above, and every rank ends
+  with all of S.
+* MoE Dispatch + GEMM (row "MoE Dispatch + GEMM"): route each token to its
+  top-k experts, move each (token, expert) row to the rank that holds the
+  expert, then multiply the rows of each expert by that expert's weight.
+  The pages leave the gating, tie-breaking and row order open; the readings
+  used here are: top-k on the raw logits (largest first, ties to the lower
+  expert id), expert e lives on rank e // E_loc, and the rows that rank d
+  receives are ordered by (local expert, global token id g = r*T + t).
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against
+brute force on tiny inputs, closed forms, invariants, and special cases that
+reduce to a library routine.  Nothing in this file is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# bf16 <-> float64
+# ----------------------------------------------------------------------------
+
+
+def bf16_to_f64(b: np.ndarray) -> np.ndarray:
+    """Exact widening of raw bf16 bit patterns (uint16) to float64.
+
+    A bf16 value is the top half of an IEEE binary32 value, so shifting the
+    16 bits up by 16 gives that binary32 exactly; binary32 -> binary64 is exact.
+    """
+    b = np.asarray(b, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+_BF16_MIN_QUANTUM_EXP = -133   # bf16 subnormal spacing 2**-133 (2**-126 * 2**-7)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 with round-to-nearest, ties-to-even, once.
+
+    bf16 keeps 8 significant bits.  For |x| in [2**(e-1), 2**e) the spacing of
+    bf16 values is 2**(e-8); below the normal range (2**-126) the spacing stays
+    2**-133.  Dividing by the spacing, rounding to the nearest integer with
+    ties to even (``np.rint``) and scaling back is the textbook definition.
+    Results at or beyond 2**128 overflow to +-inf; NaN stays NaN.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        _, e = np.frexp(x)
+        q = np.maximum(e.astype(np.int64) - 8, _BF16_MIN_QUANTUM_EXP)
+        r = np.ldexp(np.rint(np.ldexp(x, -q)), q)
+        r = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, x), r)
+        r = np.where(np.isnan(x), np.nan, r)
+        f32 = r.astype(np.float32)            # exact: r has <= 8 significant bits
+    return (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def round_out(x: np.ndarray, out: str) -> np.ndarray:
+    """Round an exact float64 result to the output dtype: 'bf16' -> uint16
+    bit patterns, 'f32' -> float32 values."""
+    if out == "bf16":
+        return f64_to_bf16_bits(x)
+    if out == "f32":
+        return np.asarray(x, dtype=np.float64).astype(np.float32)
+    raise ValueError(f"unknown output dtype {out!r}")
+
+
+# ----------------------------------------------------------------------------
+# AllGather + GEMM
+# ----------------------------------------------------------------------------
+
+
+def allgather_rows(a_shards) -> np.ndarray:
+    """The gathered A: the row shards stacked in rank order r = 0..R-1
+    (a bit copy; the order in which shards travel does not change it)."""
+    return np.concatenate([np.asarray(a, dtype=np.uint16) for a in a_shards], axis=0)
+
+
+def ag_gemm(a_shards, b, out: str = "bf16", rows=None):
+    """C = gather_r(A_r) @ B.
+
+    a_shards: R arrays of bf16 bits, each [m_r x k]; b: [k x n] bf16 bits.
+    rows: optional index array of gathered rows to compute (row sample).
+    Returns (gathered A bits [R*m_r x k], C rounded to `out` [len(rows) x n]).
+    """
+    gathered = allgather_rows(a_shards)
+    a_sel = gathered if rows is None else gathered[np.asarray(rows)]
+    c = bf16_to_f64(a_sel) @ bf16_to_f64(b)
+    return gathered, round_out(c, out)
+
+
+# ----------------------------------------------------------------------------
+# GEMM + ReduceScatter / GEMM + AllReduce
+# ----------------------------------------------------------------------------
+
+
+def sum_over_ranks(a_list, b_list, rows=None) -> np.ndarray:
+    """S = sum_r A_r @ B_r in float64 (rows: optional sample of S's rows)."""
+    assert len(a_list) == len(b_list) and len(a_list) >= 1
+    s = None
+    for a, b in zip(a_list, b_list):
+        a_sel = np.asarray(a) if rows is None else np.asarray(a)[np.asarray(rows)]
+        p = bf16_to_f64(a_sel) @ bf16_to_f64(b)
+        s = p if s is None else s + p
+    return s
+
+
+def owner_rows(m: int, R: int, o: int) -> range:
+    """Rows of S owned by rank o after the reduce-scatter: the o-th of R
+    contiguous row blocks (m must be a multiple of R)."""
+    if m % R:
+        raise ValueError("m must be a multiple of R for a row-block reduce-scatter")
+    h = m // R
+    return range(o * h, (o + 1) * h)
+
+
+def gemm_rs(a_list, b_list, out: str = "bf16"):
+    """GEMM + ReduceScatter: returns R row blocks; block o = rows owner_rows(o) of S."""
+    s = sum_over_ranks(a_list, b_list)
+    R, m = len(a_list), s.shape[0]
+    blocks = []
+    for o in range(R):
+        rr = owner_rows(m, R, o)
+        blocks.append(round_out(s[rr.start:rr.stop], out))
+    return blocks
+
+
+def gemm_ar(a_list, b_list, out: str = "bf16"):
+    """GEMM + AllReduce: returns R replicas, each equal to all of S."""
+    c = round_out(sum_over_ranks(a_list, b_list), out)
+    return [c.copy() for _ in range(len(a_list))]
+
+
+# ----------------------------------------------------------------------------
+# MoE dispatch + grouped GEMM
+# ----------------------------------------------------------------------------
+
+
+def moe_route(logits: np.ndarray, topk: int) -> np.ndarray:
+    """Top-k experts of each token: largest logit first, ties to the lower
+    expert id.  logits: [T x E] float32 (no NaN).  Returns int32 [T x topk].
+
+    Written as k rounds of "take the best expert not taken yet": each round
+    scans the experts in id order and replaces the running best only on a
+    strictly larger value, so the lower id wins a tie (a -inf logit is still
+    a valid pick when nothing larger is left).
+    """
+    work = np.asarray(logits, dtype=np.float64)
+    T, E = work.shape
+    if not 1 <= topk <= E:
+        raise ValueError("need 1 <= topk <= E")
+    taken = np.zeros((T, E), dtype=bool)
+    out = np.empty((T, topk), dtype=np.int32)
+    rows = np.arange(T)
+    for j in range(topk):
+        best_idx = np.full(T, -1, dtype=np.int64)
+        best_val = np.zeros(T, dtype=np.float64)
+        for e in range(E):
+            better = ~taken[:, e] & ((best_idx < 0) | (work[:, e] > best_val))
+            best_val = np.where(better, work[:, e], best_val)
+            best_idx = np.where(better, e, best_idx)
+        out[:, j] = best_idx
+        taken[rows, best_idx] = True
+    return out
+
+
+def moe_counts(topk_idx_list, E: int) -> np.ndarray:
+    """counts[r][e] = number of (token, slot) pairs of source rank r routed to e."""
+    counts = np.zeros((len(topk_idx_list), E), dtype=np.int64)
+    for r, idx in enumerate(topk_idx_list):
+        for e in np.asarray(idx).reshape(-1):
+            counts[r, int(e)] += 1
+    return counts
+
+
+def moe_dispatch(topk_idx_list, E_loc: int):
+    """The all-to-all token permutation.
+
+    topk_idx_list: R arrays [T x topk] (expert ids of rank r's tokens).
+    Expert e is held by rank e // E_loc.  Rank d receives every (token, slot)
+    pair routed to one of its experts, ordered by local expert, then by global
+    token id g = r*T + t.  Returns (recv_src, seg) where recv_src[d] is an
+    int64 array of g*topk + slot per received row, and seg[d][l] is the number
+    of rows of local expert l on rank d.
+    """
+    R = len(topk_idx_list)
+    idx_all = np.concatenate([np.asarray(i) for i in topk_idx_list], axis=0)   # [R*T x topk]
+    topk = idx_all.shape[1]
+    recv_src, seg = [], []
+    for d in range(R):
+        src_d, seg_d = [], []
+        for l in range(E_loc):
+            e = d * E_loc + l
+            g, j = np.nonzero(idx_all == e)      # row-major: g ascending
+            src_d.append(g.astype(np.int64) * topk + j)
+            seg_d.append(len(g))
+        recv_src.append(np.concatenate(src_d) if src_d else np.zeros(0, np.int64))
+        seg.append(np.asarray(seg_d, dtype=np.int64))
+    return recv_src, seg
+
+
+def moe_gather_rows(x_list, recv_src_d, topk: int) -> np.ndarray:
+    """recv_x rows of one destination rank: bit copies of the source token rows."""
+    x_all = np.concatenate([np.asarray(x, dtype=np.uint16) for x in x_list], axis=0)
+    g = np.asarray(recv_src_d, dtype=np.int64) // topk
+    return x_all[g]
+
+
+def moe_expert_gemm(recv_x_d, seg_d, w_d, out: str = "bf16", rows=None):
+    """Grouped GEMM of one destination rank: the rows of local expert l
+    (the l-th segment) times W_l.  w_d: [E_loc x H x N] bf16 bits.
+    rows: optional sample of received row indices.  Returns rounded [rows x N]."""
+    seg_d = np.asarray(seg_d, dtype=np.int64)
+    starts = np.concatenate([[0], np.cumsum(seg_d)])
+    nrows = int(starts[-1])
+    sel = np.arange(nrows) if rows is None else np.asarray(rows, dtype=np.int64)
+    N = np.asarray(w_d).shape[2]
+    y = np.zeros((len(sel), N), dtype=np.float64)
+    expert_of = np.searchsorted(starts, sel, side="right") - 1
+    for l in range(len(seg_d)):
+        pick = np.nonzero(expert_of == l)[0]
+        if len(pick):
+            y[pick] = bf16_to_f64(np.asarray(recv_x_d)[sel[pick]]) @ bf16_to_f64(np.asarray(w_d)[l])
+    return round_out(y, out)
+
+
+def moe_dispatch_gemm(x_list, logits_list, w_list, E_loc: int, topk: int, out: str = "bf16"):
+    """The whole MoE path for all ranks: route, count, dispatch, grouped GEMM."""
+    topk_idx = [moe_route(lg, topk) for lg in logits_list]
+    counts = moe_counts(topk_idx, len(x_list) * E_loc)
+    recv_src, seg = moe_dispatch(topk_idx, E_loc)
+    recv_x = [moe_gather_rows(x_list, recv_src[d], topk) for d in range(len(x_list))]
+    y = [moe_expert_gemm(recv_x[d], seg[d], w_list[d], out) for d in range(len(x_list))]
+    return dict(topk_idx=topk_idx, counts=counts, recv_src=recv_src, seg=seg, recv_x=recv_x, y=y)
+
+
+# ----------------------------------------------------------------------------
+# tolerance used for float parity
+# ----------------------------------------------------------------------------
+
+
+def norm_scale(K: int, a_absmax: float, b_absmax: float) -> float:
+    """Error normaliser sqrt(K) * max|a| * max|b| (K = contraction length)."""
+    return float(np.sqrt(K) * a_absmax * b_absmax)

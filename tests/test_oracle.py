@@ -1,0 +1,371 @@
+"""Pins for the CPU oracle (CPU only).
+
+Each check ties the oracle to something other than itself: the IEEE
+definition of round-to-nearest-even, brute-force loops on tiny inputs, closed
+forms, invariants of the collectives, and special cases that reduce to a
+library routine (torch's fp32->bf16 cast, numpy's stable argsort).  The cases
+are chosen so that a dropped term, a wrong sign or index, a transposed
+operand, a wrong gather order or a wrong owner block fails at least one.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from comm_gemm_tile_gb300 import inputs as I
+
+
+def bf(x):
+    """float values -> bf16 bits via torch (inputs only; exact for small ints)."""
+    return I.bits(torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def rand_int_bits(shape, seed, lo=-3, hi=3):
+    g = np.random.default_rng(seed)
+    return bf(g.integers(lo, hi + 1, size=shape).astype(np.float32))
+
+
+def brute_matmul(a, b):
+    """Pure-Python triple loop on float64 values."""
+    m, k = a.shape
+    k2, n = b.shape
+    assert k == k2
+    c = np.zeros((m, n))
+    for i in range(m):
+        for j in range(n):
+            s = 0.0
+            for t in range(k):
+                s += float(a[i, t]) * float(b[t, j])
+            c[i, j] = s
+    return c
+
+
+# ---------------------------------------------------------------- rounding
+
+@pytest.mark.parametrize("x,expect", [
+    (1.0, 0x3F80),
+    (-1.5, 0xBFC0),
+    (1.0 + 2.0 ** -8, 0x3F80),                 # tie -> even (mantissa 0)
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),             # tie -> even (mantissa 2)
+    (1.0 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),    # just above the tie -> up
+    (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),    # single rounding (via fp32 would give 0x3F80)
+    (-(1.0 + 2.0 ** -8 + 2.0 ** -20), 0xBF81),
+    (0.0, 0x0000),
+    (-0.0, 0x8000),
+    (2.0 ** -133, 0x0001),                     # smallest subnormal
+    (2.0 ** -134, 0x0000),                     # tie with 0 -> even (0)
+    (3 * 2.0 ** -134, 0x0002),                 # 1.5 quanta: tie -> 2
+    (2.0 ** -126, 0x0080),                     # smallest normal
+    ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),    # largest finite
+    ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),    # tie between max and 2^128 -> even -> inf
+    (-1e39, 0xFF80),
+    (float("inf"), 0x7F80),
+    (65536.0 + 256.0, 0x4780),                 # 65792 = 2^16(1+2^-8): tie -> 65536
+    (65536.0 + 257.0, 0x4781),
+])
+def test_bf16_rne_closed_forms(x, expect):
+    assert int(O.f64_to_bf16_bits(np.array([x]))[0]) == expect
+
+
+def test_bf16_rne_nan():
+    b = int(O.f64_to_bf16_bits(np.array([np.nan]))[0])
+    assert (b & 0x7F80) == 0x7F80 and (b & 0x7F) != 0
+
+
+def test_bf16_rne_matches_torch_on_fp32_values():
+    # For values that are exactly fp32, single RNE to bf16 equals torch's cast.
+    g = np.random.default_rng(7)
+    x = np.concatenate([
+        g.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        (g.standard_normal(2000) * 1e-39).astype(np.float32),    # fp32 subnormals
+        g.integers(-70000, 70000, 5000).astype(np.float32),
+    ])
+    want = I.bits(torch.from_numpy(x).to(torch.bfloat16))
+    got = O.f64_to_bf16_bits(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("b,val", [(0x3F80, 1.0), (0xC000, -2.0), (0x0001, 2.0 ** -133),
+                                   (0x7F80, np.inf), (0x4049, 3.140625)])
+def test_bf16_widen_closed_forms(b, val):
+    assert O.bf16_to_f64(np.array([b], np.uint16))[0] == val
+
+
+def test_bf16_roundtrip_all_finite_patterns():
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = O.bf16_to_f64(allb)
+    fin = np.isfinite(v)
+    back = O.f64_to_bf16_bits(v[fin])
+    # -0.0 and +0.0 keep their sign
+    np.testing.assert_array_equal(back, allb[fin])
+
+
+def test_f32_output_rounding():
+    x = np.array([1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 0.1])
+    got = O.round_out(x, "f32")
+    assert got[0] == np.float32(1.0)                      # tie -> even
+    assert got[1] == np.float32(1.0 + 2.0 ** -22)         # tie -> even (up)
+    assert got.dtype == np.float32
+
+
+# ---------------------------------------------------------------- AllGather + GEMM
+
+def test_ag_brute_force_tiny():
+    R, mr, k, n = 3, 2, 5, 4
+    shards = [rand_int_bits((mr, k), 10 + r) for r in range(R)]
+    b = rand_int_bits((k, n), 99)
+    gathered, c = O.ag_gemm(shards, b, out="f32")
+    A = np.concatenate([O.bf16_to_f64(s) for s in shards], 0)
+    want = brute_matmul(A, O.bf16_to_f64(b))
+    np.testing.assert_array_equal(c, want.astype(np.float32))
+    assert gathered.shape == (R * mr, k)
+
+
+def test_ag_gather_order_closed_form():
+    # shard r is all (r+1): block r of C must be (r+1) * column sums of B.
+    R, mr, k, n = 4, 3, 6, 5
+    shards = [bf(np.full((mr, k), r + 1.0)) for r in range(R)]
+    b = rand_int_bits((k, n), 5)
+    gathered, c = O.ag_gemm(shards, b, out="f32")
+    colsum = O.bf16_to_f64(b).sum(0)
+    for r in range(R):
+        np.testing.assert_array_equal(c[r * mr:(r + 1) * mr], np.tile((r + 1) * colsum, (mr, 1)))
+        np.testing.assert_array_equal(gathered[r * mr:(r + 1) * mr], shards[r])
+
+
+def test_ag_row_sample_matches_full():
+    R, mr, k, n = 2, 8, 16, 8
+    shards = [rand_int_bits((mr, k), 20 + r) for r in range(R)]
+    b = rand_int_bits((k, n), 30)
+    _, full = O.ag_gemm(shards, b)
+    rows = np.array([0, 5, 9, 15])
+    _, part = O.ag_gemm(shards, b, rows=rows)
+    np.testing.assert_array_equal(part, full[rows])
+
+
+# ---------------------------------------------------------------- GEMM + RS / AR
+
+def test_rs_brute_force_tiny():
+    R, m, k, n = 2, 4, 3, 5
+    a = [rand_int_bits((m, k), 40 + r) for r in range(R)]
+    b = [rand_int_bits((k, n), 50 + r) for r in range(R)]
+    blocks = O.gemm_rs(a, b, out="f32")
+    want = sum(brute_matmul(O.bf16_to_f64(a[r]), O.bf16_to_f64(b[r])) for r in range(R))
+    np.testing.assert_array_equal(np.concatenate(blocks, 0), want.astype(np.float32))
+    assert [blk.shape for blk in blocks] == [(2, 5), (2, 5)]
+
+
+def test_rs_closed_form_constant():
+    # A_r = 1, B_r = (r+1): S = k * R(R+1)/2 everywhere.
+    R, m, k, n = 4, 8, 7, 3
+    a = [bf(np.ones((m, k))) for _ in range(R)]
+    b = [bf(np.full((k, n), r + 1.0)) for r in range(R)]
+    for blk in O.gemm_rs(a, b, out="f32"):
+        assert np.all(blk == k * R * (R + 1) / 2)
+
+
+def test_rs_owner_blocks_closed_form():
+    # Row i of every A_r is (i+1) e_0, row 0 of B_r is r+1: S[i, j] = (i+1) * R(R+1)/2.
+    R, m, k, n = 4, 16, 3, 2
+    a_np = np.zeros((m, k))
+    a_np[:, 0] = np.arange(1, m + 1)
+    a = [bf(a_np) for _ in range(R)]
+    b = []
+    for r in range(R):
+        bb = np.zeros((k, n))
+        bb[0, :] = r + 1
+        b.append(bf(bb))
+    blocks = O.gemm_rs(a, b, out="f32")
+    h = m // R
+    for o, blk in enumerate(blocks):
+        rows = np.arange(o * h, (o + 1) * h)
+        np.testing.assert_array_equal(blk[:, 0], (rows + 1) * R * (R + 1) / 2)
+        assert list(O.owner_rows(m, R, o)) == rows.tolist()
+
+
+def test_rs_rank_sum_not_product_and_all_terms():
+    # Dropping any rank's term changes the result (each rank contributes a distinct power of 2).
+    R, m, k, n = 3, 3, 2, 2
+    a = [bf(np.full((m, k), 2.0 ** r)) for r in range(R)]
+    b = [bf(np.ones((k, n))) for _ in range(R)]
+    s = np.concatenate(O.gemm_rs(a, b, out="f32"), 0)
+    assert np.all(s == k * (2 ** R - 1))
+
+
+def test_rs_requires_divisible_m():
+    a = [bf(np.ones((5, 2)))] * 2
+    b = [bf(np.ones((2, 2)))] * 2
+    with pytest.raises(ValueError):
+        O.gemm_rs(a, b)
+
+
+def test_r1_is_plain_gemm_brute_force():
+    a = [rand_int_bits((3, 4), 61)]
+    b = [rand_int_bits((4, 6), 62)]
+    want = brute_matmul(O.bf16_to_f64(a[0]), O.bf16_to_f64(b[0])).astype(np.float32)
+    np.testing.assert_array_equal(O.gemm_rs(a, b, "f32")[0], want)
+    np.testing.assert_array_equal(O.gemm_ar(a, b, "f32")[0], want)
+    np.testing.assert_array_equal(O.ag_gemm(a, b[0], "f32")[1], want)
+
+
+def test_ar_replicas_equal_rs_blocks_union():
+    R, m, k, n = 4, 8, 16, 8
+    g = np.random.default_rng(3)
+    a = [bf(g.standard_normal((m, k))) for _ in range(R)]
+    b = [bf(g.standard_normal((k, n)) * 0.02) for _ in range(R)]
+    reps = O.gemm_ar(a, b, "bf16")
+    rs = np.concatenate(O.gemm_rs(a, b, "bf16"), 0)
+    for rep in reps:
+        np.testing.assert_array_equal(rep, reps[0])
+    np.testing.assert_array_equal(reps[0], rs)
+
+
+def test_rs_rank_permutation_invariant_integers():
+    R, m, k, n = 3, 6, 5, 4
+    a = [rand_int_bits((m, k), 70 + r) for r in range(R)]
+    b = [rand_int_bits((k, n), 80 + r) for r in range(R)]
+    base = np.concatenate(O.gemm_rs(a, b, "f32"), 0)
+    for perm in itertools.permutations(range(R)):
+        s = np.concatenate(O.gemm_rs([a[p] for p in perm], [b[p] for p in perm], "f32"), 0)
+        np.testing.assert_array_equal(s, base)
+    assert np.all(base == np.round(base))
+
+
+def test_integer_config_sums_are_exact_in_fp32():
+    # The tiny bit-exact workload: |S| <= 2*2*256*2 < 2**24, so any fp32 summation order is exact.
+    w = I.RS_R2_256_INT
+    a, b = I.gemm_inputs(w)
+    s = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
+    assert np.abs(s).max() < 2 ** 24
+    assert np.all(s == np.round(s))
+
+
+# ---------------------------------------------------------------- MoE
+
+def test_route_matches_stable_argsort():
+    g = np.random.default_rng(11)
+    lg = np.round(g.standard_normal((500, 16)) * 2) / 2      # many ties
+    lg = lg.astype(np.float32)
+    want = np.argsort(-lg, axis=1, kind="stable")[:, :3]
+    np.testing.assert_array_equal(O.moe_route(lg, 3), want)
+
+
+@pytest.mark.parametrize("row,k,expect", [
+    ([1.0, 3.0, 3.0, 2.0], 2, [1, 2]),
+    ([5.0, 5.0, 5.0, 5.0], 2, [0, 1]),
+    ([-1.0, -3.0, 7.0, 0.0], 1, [2]),
+    ([0.5, -0.5, 0.25, 0.75], 4, [3, 0, 2, 1]),
+    ([-np.inf, -np.inf, -1.0], 3, [2, 0, 1]),
+])
+def test_route_hand_cases(row, k, expect):
+    got = O.moe_route(np.array([row], dtype=np.float32), k)
+    assert got[0].tolist() == expect
+
+
+def test_route_rejects_topk_above_E():
+    with pytest.raises(ValueError):
+        O.moe_route(np.zeros((2, 3), np.float32), 4)
+
+
+def test_dispatch_hand_worked_example():
+    # R=2 ranks, 2 experts each (E=4), T=2 tokens per rank, top-2.
+    idx0 = np.array([[3, 0], [1, 2]])      # rank 0: g=0 -> {3,0}, g=1 -> {1,2}
+    idx1 = np.array([[0, 1], [2, 3]])      # rank 1: g=2 -> {0,1}, g=3 -> {2,3}
+    recv_src, seg = O.moe_dispatch([idx0, idx1], E_loc=2)
+    # rank 0 (experts 0,1): e0 <- (g0,slot1)=1, (g2,slot0)=4 ; e1 <- (g1,slot0)=2, (g2,slot1)=5
+    assert recv_src[0].tolist() == [1, 4, 2, 5]
+    assert seg[0].tolist() == [2, 2]
+    # rank 1 (experts 2,3): e2 <- (g1,slot1)=3, (g3,slot0)=6 ; e3 <- (g0,slot0)=0, (g3,slot1)=7
+    assert recv_src[1].tolist() == [3, 6, 0, 7]
+    assert seg[1].tolist() == [2, 2]
+    counts = O.moe_counts([idx0, idx1], 4)
+    assert counts.tolist() == [[1, 1, 1, 1], [1, 1, 1, 1]]
+
+
+def test_dispatch_invariants_random():
+    R, E_loc, T, topk = 4, 3, 50, 2
+    logits = [I.zipf_logits(T, R * E_loc, 900 + r).numpy() for r in range(R)]
+    idx = [O.moe_route(lg, topk) for lg in logits]
+    counts = O.moe_counts(idx, R * E_loc)
+    recv_src, seg = O.moe_dispatch(idx, E_loc)
+    assert counts.sum() == R * T * topk
+    allsrc = np.concatenate(recv_src)
+    assert sorted(allsrc.tolist()) == list(range(R * T * topk))      # bijection onto (g, slot)
+    idx_all = np.concatenate(idx, 0)
+    for d in range(R):
+        assert seg[d].sum() == len(recv_src[d])
+        start = 0
+        for l in range(E_loc):
+            e = d * E_loc + l
+            part = recv_src[d][start:start + seg[d][l]]
+            g = part // topk
+            assert np.all(np.diff(g) > 0)                               # token order
+            assert np.all(idx_all[g, part % topk] == e)                 # right expert
+            assert seg[d][l] == counts[:, e].sum()
+            start += seg[d][l]
+
+
+def test_dispatch_single_expert_is_identity():
+    T = 17
+    idx = [np.zeros((T, 1), np.int64)]
+    recv_src, seg = O.moe_dispatch(idx, E_loc=1)
+    assert recv_src[0].tolist() == list(range(T)) and seg[0].tolist() == [T]
+
+
+def test_expert_gemm_scaled_identity_closed_form():
+    # W_l = (l+1) * I: each received row comes back scaled by its expert's factor.
+    H = N = 8
+    seg = np.array([3, 0, 2])
+    rx = rand_int_bits((5, H), 123)
+    w = np.stack([bf(np.eye(H) * (l + 1)) for l in range(3)], 0)
+    y = O.moe_expert_gemm(rx, seg, w, out="f32")
+    scale = np.array([1, 1, 1, 3, 3])[:, None]
+    np.testing.assert_array_equal(y, (O.bf16_to_f64(rx) * scale).astype(np.float32))
+
+
+def test_moe_end_to_end_brute_force_tiny():
+    R, E_loc, T, H, N, topk = 2, 2, 3, 4, 3, 2
+    x = [rand_int_bits((T, H), 200 + r) for r in range(R)]
+    logits = [I.zipf_logits(T, R * E_loc, 300 + r).numpy() for r in range(R)]
+    w = [np.stack([rand_int_bits((H, N), 400 + 10 * d + l) for l in range(E_loc)], 0)
+         for d in range(R)]
+    res = O.moe_dispatch_gemm(x, logits, w, E_loc, topk, out="f32")
+    xall = np.concatenate([O.bf16_to_f64(v) for v in x], 0)
+    idx_all = np.concatenate(res["topk_idx"], 0)
+    for d in range(R):
+        for j, src in enumerate(res["recv_src"][d]):
+            g, slot = divmod(int(src), topk)
+            e = int(idx_all[g, slot])
+            assert e // E_loc == d
+            np.testing.assert_array_equal(res["recv_x"][d][j], np.concatenate(x, 0)[g])
+            want = brute_matmul(xall[g:g + 1], O.bf16_to_f64(w[d][e % E_loc]))[0]
+            np.testing.assert_array_equal(res["y"][d][j], want.astype(np.float32))
+
+
+def test_norm_scale():
+    assert O.norm_scale(16, 2.0, 0.5) == 4.0
+
+
+# ---------------------------------------------------------------- stored oracle outputs
+
+def test_golden_file_matches_oracle():
+    import hashlib
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "oracle_golden.json")
+    gold = json.load(open(path))
+    w = I.RS_R2_256_INT
+    a, b = I.gemm_inputs(w)
+    blocks = O.gemm_rs([I.bits(x) for x in a], [I.bits(x) for x in b], out="f32")
+    g = gold["rs_r2_256_int"]
+    for o, blk in enumerate(blocks):
+        assert hashlib.sha256(blk.tobytes()).hexdigest() == g["block_sha256_f32_le"][o]
+    for o, i, j, v in g["samples"]:
+        assert blocks[o][i, j] == v
+    gm = gold["moe_small_route"]
+    R, E_loc, T = 4, 4, 256
+    logits = [I.zipf_logits(T, R * E_loc, 7000 + r).numpy() for r in range(R)]
+    idx = [O.moe_route(lg, 2) for lg in logits]
+    assert O.moe_counts(idx, R * E_loc).tolist() == gm["counts"]
