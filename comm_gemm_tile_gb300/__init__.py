@@ -1,1 +1,238 @@
-"""Placeholder; replaced by the binding module."""
+"""Python binding of libmk.so: tile-pipelined fused collective + GEMM on one GB300.
+
+Argument marshalling only.  Every step of every op runs in the CUDA library
+(include/mk.h); PyTorch provides device memory and streams.  If the library is
+missing the calls raise -- there is no fallback path.
+
+The R virtual ranks of an op are R separate device buffers on one GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmk.so")
+
+MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_CUDA, MK_ERR_TIMEOUT, MK_ERR_CAPACITY = range(6)
+MK_BF16, MK_F32 = 0, 1
+OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR, OP_MOE = 0, 1, 2, 3
+MODE_FUSED, MODE_GEMM_ONLY, MODE_UNFUSED = 0, 1, 2
+MAX_RANKS = 16
+
+
+class MkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("n_copy_ctas", ctypes.c_int), ("n_reduce_ctas", ctypes.c_int),
+                ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("mode", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
+                ("inject", ctypes.c_int)]
+
+
+@dataclasses.dataclass
+class Config:
+    """Tuning / test knobs (mk_config); 0 means the library's own choice."""
+    n_copy_ctas: int = 0
+    n_reduce_ctas: int = 0
+    max_ctas: int = 0
+    group_m: int = 0
+    split_k: int = 0
+    mode: int = MODE_FUSED
+    wait_limit_ns: int = 0
+    inject: int = 0
+
+    def c(self) -> _Cfg:
+        return _Cfg(self.n_copy_ctas, self.n_reduce_ctas, self.max_ctas, self.group_m,
+                    self.split_k, self.mode, self.wait_limit_ns, self.inject)
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmk.so (built in-tree by build.py).  Raises if it is missing."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run comm_gemm_tile_gb300/build.py "
+                               "(or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, ll, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong, ctypes.c_int
+        P = ctypes.POINTER
+        L.mk_version.restype = i
+        L.mk_device_sm_count.restype = i
+        L.mk_status_string.restype = ctypes.c_char_p
+        L.mk_status_string.argtypes = [i]
+        L.mk_workspace_size.restype = sz
+        L.mk_workspace_size.argtypes = [i, i, ll, ll, ll, P(_Cfg)]
+        L.mk_moe_workspace_size.restype = sz
+        L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
+        L.mk_get_device_status.restype = i
+        L.mk_get_device_status.argtypes = [vp, vp, P(ll)]
+        L.mk_ag_gemm.restype = i
+        L.mk_ag_gemm.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
+        for name in ("mk_gemm_rs", "mk_gemm_ar"):
+            f = getattr(L, name)
+            f.restype = i
+            f.argtypes = [P(vp), P(vp), P(vp), i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
+        L.mk_moe_dispatch_gemm.restype = i
+        L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
+                                           P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
+        _lib = L
+        return L
+
+
+def status_string(s: int) -> str:
+    return lib().mk_status_string(int(s)).decode()
+
+
+def _ptrs(ts) -> ctypes.Array:
+    arr = (ctypes.c_void_p * len(ts))()
+    for j, t in enumerate(ts):
+        arr[j] = t.data_ptr() if isinstance(t, torch.Tensor) else t
+    return arr
+
+
+def _cfgp(cfg: Config | None):
+    return ctypes.byref(cfg.c()) if cfg is not None else None
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dt(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return MK_BF16
+    if dtype == torch.float32:
+        return MK_F32
+    raise ValueError(f"unsupported output dtype {dtype}")
+
+
+def _check(st: int, what: str):
+    if st != MK_OK:
+        raise MkError(st, what)
+
+
+# ------------------------------------------------------------------ workspaces
+
+class Workspace:
+    """A device workspace, zero-filled once at (re)allocation as the library requires."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def _ws(workspace, device) -> Workspace:
+    if workspace is not None:
+        return workspace
+    key = torch.device(device).index if torch.device(device).index is not None else \
+        torch.cuda.current_device()
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(torch.device("cuda", key))
+    return _default_ws[key]
+
+
+def workspace_size(op: int, R: int, m: int, n: int, k: int, cfg: Config | None = None) -> int:
+    return int(lib().mk_workspace_size(op, R, m, n, k, _cfgp(cfg)))
+
+
+def device_status(workspace: Workspace | None = None, stream=None, device=None):
+    """Synchronise the stream and read-and-clear the workspace's device status.
+    Returns (status, detail)."""
+    ws = _ws(workspace, device or "cuda")
+    detail = ctypes.c_longlong(0)
+    st = lib().mk_get_device_status(ctypes.c_void_p(ws.get(256).data_ptr()),
+                                    ctypes.c_void_p(_stream(stream, ws.device)), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+# ------------------------------------------------------------------ ops
+
+def ag_gemm(a_shards, b, *, local_rank: int = 0, out_dtype=torch.bfloat16, a_gathered=None,
+            c=None, cfg: Config | None = None, workspace: Workspace | None = None, stream=None):
+    """AllGather + GEMM: returns (a_gathered = [A_0; ...; A_{R-1}], c = a_gathered @ b)."""
+    R = len(a_shards)
+    m_r, k = a_shards[0].shape
+    n = b.shape[1]
+    dev = b.device
+    if a_gathered is None:
+        a_gathered = torch.empty((R * m_r, k), dtype=torch.bfloat16, device=dev)
+    if c is None:
+        c = torch.empty((R * m_r, n), dtype=out_dtype, device=dev)
+    ws = _ws(workspace, dev)
+    nb = workspace_size(OP_AG_GEMM, R, m_r, n, k, cfg)
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, "mk_workspace_size(AG)")
+    buf = ws.get(nb)
+    st = lib().mk_ag_gemm(_ptrs(a_shards), b.data_ptr(), a_gathered.data_ptr(), c.data_ptr(),
+                          _dt(c.dtype), R, local_rank, m_r, n, k, buf.data_ptr(), buf.numel(),
+                          _cfgp(cfg), _stream(stream, dev))
+    _check(st, "mk_ag_gemm")
+    return a_gathered, c
+
+
+def _rs_ar(fn, op, a, b, outs, R, m, n, k, cfg, workspace, stream, what):
+    dev = a[0].device
+    ws = _ws(workspace, dev)
+    nb = workspace_size(op, R, m, n, k, cfg)
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, f"mk_workspace_size({what})")
+    buf = ws.get(nb)
+    st = fn(_ptrs(a), _ptrs(b), _ptrs(outs), _dt(outs[0].dtype), R, m, n, k, buf.data_ptr(),
+            buf.numel(), _cfgp(cfg), _stream(stream, dev))
+    _check(st, what)
+    return outs
+
+
+def gemm_rs(a, b, *, out_dtype=torch.bfloat16, c_blocks=None, cfg: Config | None = None,
+            workspace: Workspace | None = None, stream=None):
+    """GEMM + ReduceScatter: S = sum_r a[r] @ b[r]; returns R row blocks of S."""
+    R = len(a)
+    m, k = a[0].shape
+    n = b[0].shape[1]
+    if c_blocks is None:
+        c_blocks = [torch.empty((m // R, n), dtype=out_dtype, device=a[0].device) for _ in range(R)]
+    return _rs_ar(lib().mk_gemm_rs, OP_GEMM_RS, a, b, c_blocks, R, m, n, k, cfg, workspace, stream,
+                  "mk_gemm_rs")
+
+
+def gemm_ar(a, b, *, out_dtype=torch.bfloat16, c_replicas=None, cfg: Config | None = None,
+            workspace: Workspace | None = None, stream=None):
+    """GEMM + AllReduce: S = sum_r a[r] @ b[r]; returns R identical replicas of S."""
+    R = len(a)
+    m, k = a[0].shape
+    n = b[0].shape[1]
+    if c_replicas is None:
+        c_replicas = [torch.empty((m, n), dtype=out_dtype, device=a[0].device) for _ in range(R)]
+    return _rs_ar(lib().mk_gemm_ar, OP_GEMM_AR, a, b, c_replicas, R, m, n, k, cfg, workspace,
+                  stream, "mk_gemm_ar")
+
+
+__all__ = ["Config", "MkError", "Workspace", "ag_gemm", "gemm_rs", "gemm_ar", "device_status",
+           "workspace_size", "lib", "status_string", "MODE_FUSED", "MODE_GEMM_ONLY",
+           "MODE_UNFUSED"]

@@ -1,0 +1,379 @@
+// mk_api.cu -- the C ABI for AllGather+GEMM, GEMM+ReduceScatter and
+// GEMM+AllReduce: argument checks, workspace layout, tensor-map encoding,
+// role split and the launch of the persistent fused kernel.
+#include <atomic>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+// ------------------------------------------------------------------ small utilities
+static std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch() {
+  uint32_t e = ++g_epoch;
+  while (e == 0) e = ++g_epoch;  // 0 is the value of a zero-filled flag
+  return e;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+long long default_wait_ns(const mk_config* cfg) {
+  if (cfg && cfg->wait_limit_ns > 0) return cfg->wait_limit_ns;
+  return 2000000000LL;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 2-D map over a row-major [outer x inner] matrix, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// SM count used for the device-independent parts of the plan (split-K), so
+// that mk_workspace_size gives the same answer with or without a GPU.
+constexpr int PLAN_SMS = 148;
+
+// ------------------------------------------------------------------ planning
+struct Plan {
+  int op, mode, R;
+  long long M, N, K, m_r;
+  int n_mblk, n_nblk, n_kblk, n_tiles;
+  int split_k, kps, P;
+  int group_m;
+  size_t flags_off, n_flags, staging_off, staging_bytes, total;
+};
+
+static bool plan_gemm(int op, int R, long long m, long long n, long long k, const mk_config* cfg,
+                      Plan& pl) {
+  if (R < 1 || R > MK_MAX_RANKS) return false;
+  if (m < 0 || n < 0 || k < 0) return false;
+  if ((n % 8) || (k % 8)) return false;
+  const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
+  if (mode < MK_MODE_FUSED || mode > MK_MODE_UNFUSED) return false;
+  pl.op = op;
+  pl.mode = mode;
+  pl.R = R;
+  pl.m_r = m;
+  pl.M = (op == OP_AG) ? m * R : m;
+  pl.N = n;
+  pl.K = k;
+  if (pl.M >= (1LL << 31) || n >= (1LL << 31) || k >= (1LL << 31)) return false;
+  if (op == OP_RS && R > 0 && (m % R)) return false;
+  pl.n_mblk = static_cast<int>(ceil_div_ll(pl.M, BM));
+  pl.n_nblk = static_cast<int>(ceil_div_ll(n, BN));
+  pl.n_kblk = static_cast<int>(ceil_div_ll(k, BK));
+  pl.n_tiles = pl.n_mblk * pl.n_nblk;
+  pl.split_k = 1;
+  pl.kps = pl.n_kblk;
+  pl.P = 1;
+  pl.group_m = (cfg && cfg->group_m > 0) ? cfg->group_m : 8;
+  pl.flags_off = WS_HDR_BYTES;
+  pl.n_flags = 0;
+  pl.staging_bytes = 0;
+  if (op == OP_AG) {
+    pl.n_flags = static_cast<size_t>(pl.n_mblk);
+  } else {
+    int sk = (cfg && cfg->split_k > 0) ? cfg->split_k : 0;
+    if (sk == 0) {
+      sk = 1;
+      const long long items = static_cast<long long>(pl.n_tiles) * R;
+      if (op == OP_AR && items > 0 && items < 2LL * PLAN_SMS)
+        sk = static_cast<int>(ceil_div_ll(2LL * PLAN_SMS, items));
+    }
+    sk = std::max(1, std::min(sk, MAX_PARTIALS / R));
+    sk = std::min(sk, std::max(1, pl.n_kblk));
+    pl.kps = static_cast<int>(ceil_div_ll(std::max(1, pl.n_kblk), sk));
+    sk = static_cast<int>(ceil_div_ll(std::max(1, pl.n_kblk), pl.kps));  // drop empty slices
+    pl.split_k = sk;
+    pl.P = R * sk;
+    if (pl.P > MAX_PARTIALS) return false;
+    if (mode != MK_MODE_GEMM_ONLY) {
+      pl.n_flags = static_cast<size_t>(pl.n_tiles) * pl.P;
+      pl.staging_bytes = static_cast<size_t>(pl.n_tiles) * pl.P * TILE_F32 * sizeof(float);
+    }
+  }
+  size_t off = pl.flags_off + pl.n_flags * sizeof(uint32_t);
+  off = (off + 1023) & ~static_cast<size_t>(1023);
+  pl.staging_off = off;
+  pl.total = off + pl.staging_bytes;
+  return true;
+}
+
+static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_config* cfg,
+                        mk_dtype c_dtype) {
+  std::memset(&p, 0, sizeof(p));
+  p.op = pl.op;
+  p.mode = pl.mode;
+  p.R = pl.R;
+  p.M = static_cast<int>(pl.M);
+  p.N = static_cast<int>(pl.N);
+  p.K = static_cast<int>(pl.K);
+  p.m_r = static_cast<int>(pl.m_r);
+  p.n_mblk = pl.n_mblk;
+  p.n_nblk = pl.n_nblk;
+  p.n_kblk = pl.n_kblk;
+  p.n_tiles = pl.n_tiles;
+  p.group_m = pl.group_m;
+  p.split_k = pl.split_k;
+  p.kps = pl.kps;
+  p.P = pl.P;
+  p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
+  p.hdr = reinterpret_cast<uint32_t*>(ws);
+  p.flags = reinterpret_cast<uint32_t*>(ws + pl.flags_off);
+  p.staging = reinterpret_cast<float*>(ws + pl.staging_off);
+  p.wait_ns = default_wait_ns(cfg);
+  p.inject = cfg ? cfg->inject : 0;
+  p.epoch = next_epoch();
+}
+
+static mk_status launch(FusedParams& p, int n_copy, int n_compute, int n_reduce, cudaStream_t s) {
+  p.n_copy = n_copy;
+  p.n_compute = n_compute;
+  p.n_reduce = n_reduce;
+  const int grid = n_copy + n_compute + n_reduce;
+  if (grid <= 0) return MK_OK;
+  return launch_fused(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+static int grid_cap(const mk_config* cfg) {
+  int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  if (cfg && cfg->max_ctas > 0) sms = std::min(sms, cfg->max_ctas);
+  return sms;
+}
+
+static mk_status zero_outputs(void* const* outs, int nout, size_t bytes, cudaStream_t s) {
+  for (int i = 0; i < nout; ++i)
+    if (bytes && cudaMemsetAsync(outs[i], 0, bytes, s) != cudaSuccess) return MK_ERR_CUDA;
+  return MK_OK;
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+int mk_version(void) { return MK_VERSION; }
+
+int mk_device_sm_count(void) { return device_sm_count(); }
+
+const char* mk_status_string(mk_status s) {
+  switch (s) {
+    case MK_OK: return "ok";
+    case MK_ERR_INVALID: return "invalid argument";
+    case MK_ERR_UNSUPPORTED: return "unsupported on this device or build";
+    case MK_ERR_CUDA: return "CUDA error";
+    case MK_ERR_TIMEOUT: return "device wait timed out (a ready flag or pipeline stage never arrived)";
+    case MK_ERR_CAPACITY: return "MoE receive capacity exceeded";
+  }
+  return "unknown status";
+}
+
+size_t mk_workspace_size(int op, int R, long long m, long long n, long long k, const mk_config* cfg) {
+  if (op == MK_OP_MOE) return 0;
+  if (op < MK_OP_AG_GEMM || op > MK_OP_GEMM_AR) return 0;
+  Plan pl;
+  if (!plan_gemm(op, R, m, n, k, cfg, pl)) return 0;
+  return pl.total;
+}
+
+mk_status mk_get_device_status(const void* workspace, mk_stream_t stream, long long* detail) {
+  if (!workspace) return MK_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MK_ERR_CUDA;
+  uint32_t h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MK_ERR_CUDA;
+  if (detail) *detail = static_cast<long long>(static_cast<int32_t>(h[HDR_DETAIL]));
+  if (h[HDR_STATUS] != 0) {
+    uint32_t z[2] = {0, 0};
+    if (cudaMemcpy(reinterpret_cast<uint8_t*>(const_cast<void*>(workspace)) + 4 * HDR_STATUS, z,
+                   sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MK_ERR_CUDA;
+  }
+  return static_cast<mk_status>(h[HDR_STATUS]);
+}
+
+mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathered, void* c,
+                     mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n, long long k,
+                     void* workspace, size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
+  if (!a_shards || !b || !a_gathered || !c || !workspace) return MK_ERR_INVALID;
+  if (c_dtype != MK_BF16 && c_dtype != MK_F32) return MK_ERR_INVALID;
+  if (R < 1 || R > MK_MAX_RANKS || local_rank < 0 || local_rank >= R) return MK_ERR_INVALID;
+  for (int r = 0; r < R; ++r)
+    if (!a_shards[r] || !aligned16(a_shards[r])) return MK_ERR_INVALID;
+  if (!aligned16(b) || !aligned16(a_gathered) || !aligned16(c) || !aligned16(workspace))
+    return MK_ERR_INVALID;
+  Plan pl;
+  if (!plan_gemm(OP_AG, R, m_r, n, k, cfg, pl)) return MK_ERR_INVALID;
+  if (ws_bytes < pl.total) return MK_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m_r == 0) return MK_OK;
+  const int sms = grid_cap(cfg);
+  if (sms <= 0) return MK_ERR_UNSUPPORTED;
+
+  FusedParams p;
+  fill_common(p, pl, static_cast<uint8_t*>(workspace), cfg, c_dtype);
+  p.local = local_rank;
+  p.gathered = static_cast<uint8_t*>(a_gathered);
+  for (int r = 0; r < R; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
+  p.out[0] = c;
+  const size_t row_bytes = static_cast<size_t>(k) * 2;
+  p.copy_local = (static_cast<const uint8_t*>(a_shards[local_rank]) !=
+                  static_cast<uint8_t*>(a_gathered) + static_cast<size_t>(local_rank) * m_r * row_bytes)
+                     ? 1 : 0;
+  p.ordered = (m_r % BM == 0) ? 1 : 0;
+  const int bps = static_cast<int>(m_r / BM);
+  p.n_copy_chunks = p.ordered ? (p.copy_local ? R : R - 1) * bps : pl.n_mblk;
+  const int n_items = (k > 0 && n > 0) ? pl.n_mblk * pl.n_nblk : 0;
+  p.n_items = n_items;
+
+  if (k == 0 || n == 0) {
+    // Nothing to multiply: C is all zeros (k == 0) or empty (n == 0); the
+    // gathered A is still produced.
+    if (n > 0) {
+      mk_status st = zero_outputs(&c, 1, static_cast<size_t>(pl.M) * n * (c_dtype == MK_F32 ? 4 : 2), s);
+      if (st != MK_OK) return st;
+    }
+    if (k == 0) return MK_OK;
+    return launch(p, std::min(sms, std::max(1, p.n_copy_chunks)), 0, 0, s);
+  }
+  if (!make_map_2d(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes, BK, BM) ||
+      !make_map_2d(&p.tmA[1], a_gathered, k, pl.M, row_bytes, BK, BM) ||
+      !make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK))
+    return MK_ERR_CUDA;
+
+  if (pl.mode == MK_MODE_GEMM_ONLY) {
+    return launch(p, 0, std::min(sms, n_items), 0, s);
+  }
+  if (pl.mode == MK_MODE_UNFUSED) {
+    const uint32_t e = p.epoch;
+    mk_status st = MK_OK;
+    if (p.n_copy_chunks > 0) st = launch(p, std::min(sms, p.n_copy_chunks), 0, 0, s);
+    if (st != MK_OK) return st;
+    p.epoch = e;
+    p.mode = MK_MODE_GEMM_ONLY;
+    return launch(p, 0, std::min(sms, n_items), 0, s);
+  }
+  int n_copy = (cfg && cfg->n_copy_ctas > 0) ? cfg->n_copy_ctas : 8;
+  n_copy = std::min(n_copy, p.n_copy_chunks);
+  n_copy = std::min(n_copy, sms - 1);
+  n_copy = std::max(n_copy, 0);
+  const int n_compute = std::min(sms - n_copy, n_items);
+  return launch(p, n_copy, n_compute, 0, s);
+}
+
+static mk_status rs_ar_common(int op, const void* const* a, const void* const* b, void* const* outs,
+                              mk_dtype c_dtype, int R, long long m, long long n, long long k,
+                              void* workspace, size_t ws_bytes, const mk_config* cfg,
+                              mk_stream_t stream) {
+  if (!a || !b || !outs || !workspace) return MK_ERR_INVALID;
+  if (c_dtype != MK_BF16 && c_dtype != MK_F32) return MK_ERR_INVALID;
+  if (R < 1 || R > MK_MAX_RANKS) return MK_ERR_INVALID;
+  for (int r = 0; r < R; ++r) {
+    if (!a[r] || !b[r] || !outs[r]) return MK_ERR_INVALID;
+    if (!aligned16(a[r]) || !aligned16(b[r]) || !aligned16(outs[r])) return MK_ERR_INVALID;
+  }
+  if (!aligned16(workspace)) return MK_ERR_INVALID;
+  Plan pl;
+  if (!plan_gemm(op, R, m, n, k, cfg, pl)) return MK_ERR_INVALID;
+  if (ws_bytes < pl.total) return MK_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m == 0 || n == 0) return MK_OK;
+  const size_t esz = (c_dtype == MK_F32) ? 4 : 2;
+  if (k == 0) {
+    const size_t rows = (op == OP_RS) ? static_cast<size_t>(m / R) : static_cast<size_t>(m);
+    return zero_outputs(outs, R, rows * n * esz, s);
+  }
+  const int sms = grid_cap(cfg);
+  if (sms <= 0) return MK_ERR_UNSUPPORTED;
+
+  FusedParams p;
+  fill_common(p, pl, static_cast<uint8_t*>(workspace), cfg, c_dtype);
+  p.rows_per_owner = static_cast<int>(m / R);
+  if (op == OP_AR) p.rows_per_owner = static_cast<int>(m);
+  for (int r = 0; r < R; ++r) {
+    p.out[r] = outs[r];
+    if (!make_map_2d(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2, BK, BM) ||
+        !make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK))
+      return MK_ERR_CUDA;
+  }
+  if (pl.mode == MK_MODE_GEMM_ONLY) {
+    p.n_items = pl.n_tiles;
+    return launch(p, 0, std::min(sms, pl.n_tiles), 0, s);
+  }
+  p.n_items = pl.n_tiles * pl.P;
+  if (pl.mode == MK_MODE_UNFUSED) {
+    const uint32_t e = p.epoch;
+    mk_status st = launch(p, 0, std::min(sms, p.n_items), 0, s);
+    if (st != MK_OK) return st;
+    p.epoch = e;
+    return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
+  }
+  int n_red = (cfg && cfg->n_reduce_ctas > 0) ? cfg->n_reduce_ctas : 8;
+  n_red = std::min(n_red, pl.n_tiles);
+  n_red = std::min(n_red, sms - 1);
+  n_red = std::max(n_red, 1);
+  const int n_compute = std::min(sms - n_red, p.n_items);
+  return launch(p, 0, n_compute, n_red, s);
+}
+
+mk_status mk_gemm_rs(const void* const* a, const void* const* b, void* const* c_blocks, mk_dtype c_dtype,
+                     int R, long long m, long long n, long long k, void* workspace, size_t ws_bytes,
+                     const mk_config* cfg, mk_stream_t stream) {
+  return rs_ar_common(OP_RS, a, b, c_blocks, c_dtype, R, m, n, k, workspace, ws_bytes, cfg, stream);
+}
+
+mk_status mk_gemm_ar(const void* const* a, const void* const* b, void* const* c_replicas,
+                     mk_dtype c_dtype, int R, long long m, long long n, long long k, void* workspace,
+                     size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
+  return rs_ar_common(OP_AR, a, b, c_replicas, c_dtype, R, m, n, k, workspace, ws_bytes, cfg, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,825 @@
+// mk_fused.cu -- the persistent fused kernel behind mk_ag_gemm, mk_gemm_rs and
+// mk_gemm_ar (and the grouped GEMM of mk_moe_dispatch_gemm).
+//
+// One launch, one CTA per SM.  Each CTA takes a ticket and with it a role
+// (mKernel write-up, news.chathome.org, "mKernel的功能": CTAs assign
+// themselves compute / communication / reduce roles, with the SM count per
+// role tunable per shape):
+//   * copy-in  (AllGather): moves remote row shards into the gathered A with
+//     bulk async copies and releases one ready flag per 128-row chunk;
+//   * compute: persistent tile loop, TMA -> 4-stage smem ring -> tcgen05.mma
+//     into a double-buffered TMEM accumulator -> epilogue (bf16/fp32 store, or
+//     an fp32 partial tile + ready flag);
+//   * reduce (ReduceScatter / AllReduce): waits until all partial tiles of an
+//     output tile are flagged, sums them in rank order and writes the owner's
+//     block (or every replica).
+// Tiles are consumed / reduced as soon as their inputs land ("五种融合内核"
+// table: each A tile is consumed on arrival; each output tile is reduced and
+// forwarded to its owner as soon as it is produced).
+//
+// Every wait (mbarrier phase, ready flag) is bounded by p.wait_ns of
+// %globaltimer time; on expiry the CTA records MK_ERR_TIMEOUT in the
+// workspace header, raises the abort word so that every other CTA stops at
+// its next wait, drains its own copies in flight, frees its tensor memory and
+// returns.
+#include "mk_internal.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
+
+// ------------------------------------------------------------------ errors / waits
+__device__ __forceinline__ bool aborted(const FusedParams& p) {
+  return ld_volatile(&p.hdr[HDR_ABORT]) == p.epoch;
+}
+
+__device__ __noinline__ void raise_error(const FusedParams& p, int code, int where, int item) {
+  int* st = reinterpret_cast<int*>(&p.hdr[HDR_STATUS]);
+  if (atomicCAS(st, 0, code) == 0) {
+    atomicExch(reinterpret_cast<int*>(&p.hdr[HDR_DETAIL]), where * 1000000 + (item % 1000000));
+  }
+  __threadfence();
+  atomicExch(&p.hdr[HDR_ABORT], p.epoch);
+}
+
+// Bounded mbarrier wait.  honor_abort = false is used only to drain copies
+// that are known to be in flight (they complete on their own).
+__device__ __noinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
+                                      int item, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++it & 31u) == 0) {
+      if (honor_abort && aborted(p)) return false;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+        raise_error(p, MK_ERR_TIMEOUT, where, item);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until *f == epoch (acquire, gpu scope).  Single thread.
+__device__ __noinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, int where, int item) {
+  if (ld_acquire_gpu(f) == p.epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (ld_acquire_gpu(f) != p.epoch) {
+    if ((++it & 7u) == 0) {
+      if (aborted(p)) return false;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+        raise_error(p, MK_ERR_TIMEOUT, where, item);
+        return false;
+      }
+    }
+    __nanosleep(100);
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ work decoding
+struct Item {
+  int mb, nb;       // tile coordinates in the op's output space
+  int arow;         // A row coordinate inside map tmA[amap]
+  int amap, bmap;   // first maps; segment s uses amap+s / bmap+s
+  int nseg;         // K segments (RS/AR GEMM-only: one per rank)
+  int kb0, nkb;     // k-block range within each segment
+  int wait_chunk;   // AG: chunk flag to wait for (-1 = none)
+  int slot;         // RS/AR fused: partial slot index (-1 = write the output)
+  int bz;           // MoE: local expert (3-D B map); -1 = 2-D B map
+  int row_lo, row_hi;  // valid tile rows [row_lo, row_hi) (tile-relative)
+  int out_row0;     // output row of tile row 0
+};
+
+// Grouped raster: group_m m-blocks per group, n-blocks outer inside a group.
+__device__ __forceinline__ void raster(const FusedParams& p, int q, int& mb, int& nb) {
+  const int gm = p.group_m;
+  const int per_group = gm * p.n_nblk;
+  const int g = q / per_group;
+  const int first_m = g * gm;
+  const int gsz = min(p.n_mblk - first_m, gm);
+  const int r = q - g * per_group;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+// AG: m-block processed at position `pos` of the compute order (local shard
+// first, then remote shards in ring order local+1, local+2, ...).
+__device__ __forceinline__ int ag_compute_mb(const FusedParams& p, int pos) {
+  if (!p.ordered) return pos;
+  const int bps = p.m_r / BM;
+  const int q = pos / bps, i = pos - q * bps;
+  const int s = (p.local + q) % p.R;
+  return s * bps + i;
+}
+// AG: chunk copied at position `c` of the copy order (remote shards in ring
+// order local+1, ..., then the local shard if it has to be copied).
+__device__ __forceinline__ int ag_copy_mb(const FusedParams& p, int c) {
+  if (!p.ordered) return c;
+  const int bps = p.m_r / BM;
+  const int q = c / bps, i = c - q * bps;
+  const int s = (p.local + 1 + q) % p.R;
+  return s * bps + i;
+}
+__device__ __forceinline__ bool ag_chunk_fully_local(const FusedParams& p, int mb) {
+  const long long lo = static_cast<long long>(mb) * BM;
+  const long long hi = min(lo + BM, static_cast<long long>(p.M));
+  const long long l0 = static_cast<long long>(p.local) * p.m_r;
+  return lo >= l0 && hi <= l0 + p.m_r;
+}
+
+__device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
+  it.bz = -1;
+  it.slot = -1;
+  it.wait_chunk = -1;
+  it.nseg = 1;
+  it.amap = 0;
+  it.bmap = 0;
+  it.kb0 = 0;
+  it.nkb = p.n_kblk;
+  it.row_lo = 0;
+  it.row_hi = BM;
+  if (p.op == OP_AG) {
+    const int pos = i / p.n_nblk;
+    it.nb = i - pos * p.n_nblk;
+    it.mb = ag_compute_mb(p, pos);
+    it.out_row0 = it.mb * BM;
+    if (p.mode == MK_MODE_FUSED && ag_chunk_fully_local(p, it.mb)) {
+      it.amap = 0;
+      it.arow = it.mb * BM - p.local * p.m_r;
+    } else {
+      it.amap = 1;
+      it.arow = it.mb * BM;
+      if (p.mode == MK_MODE_FUSED) it.wait_chunk = it.mb;
+    }
+    it.row_hi = min(BM, p.M - it.out_row0);
+    return true;
+  }
+  if (p.op == OP_RS || p.op == OP_AR) {
+    if (p.mode == MK_MODE_GEMM_ONLY) {
+      raster(p, i, it.mb, it.nb);
+      it.nseg = p.R;
+    } else {
+      const int q = i / p.P;
+      const int part = i - q * p.P;
+      raster(p, q, it.mb, it.nb);
+      const int r = part / p.split_k, ks = part - r * p.split_k;
+      it.amap = r;
+      it.bmap = r;
+      it.kb0 = ks * p.kps;
+      it.nkb = min(p.kps, p.n_kblk - it.kb0);
+      it.slot = (it.mb * p.n_nblk + it.nb) * p.P + part;
+    }
+    it.arow = it.mb * BM;
+    it.out_row0 = it.mb * BM;
+    it.row_hi = min(BM, p.M - it.out_row0);
+    return true;
+  }
+  // OP_MOE: entry i of the tile table written by the routing kernel:
+  // {dest rank d, local expert l, first row of the tile in recv_x[d], rows valid, n-block}
+  const int* e = p.moe_tiles + 5 * i;
+  const int d = e[0];
+  it.amap = d;
+  it.bmap = d;
+  it.bz = e[1];
+  it.arow = e[2];
+  it.out_row0 = e[2];
+  it.row_hi = e[3];
+  it.nb = e[4];
+  it.mb = d;  // output buffer index
+  return true;
+}
+
+// ------------------------------------------------------------------ compute role
+struct ComputeSmem {
+  uint32_t ring;  // smem address of stage 0
+  uint32_t bars;  // smem address of the barrier block
+  __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const { return bars + 32u + 8u * s; }
+  __device__ __forceinline__ uint32_t tfull(int b) const { return bars + 64u + 8u * b; }
+  __device__ __forceinline__ uint32_t tempty(int b) const { return bars + 80u + 8u * b; }
+  __device__ __forceinline__ uint32_t drain() const { return bars + 96u; }
+  __device__ __forceinline__ uint32_t pdone(int b) const { return bars + 104u + 8u * b; }
+};
+
+__device__ __forceinline__ int n_items_for(const FusedParams& p) {
+  if (p.op == OP_MOE) return min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)) ,
+                                 static_cast<uint32_t>(p.n_items));
+  return p.n_items;
+}
+
+__device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued_mask = 0, issued_par = 0;
+  const int n_items = n_items_for(p);
+  for (int i = cid; i < n_items; i += p.n_compute) {
+    Item it;
+    decode(p, i, it);
+    if (it.wait_chunk >= 0) {
+      if (!wait_flag(p, p.flags + it.wait_chunk, WHERE_PRODUCER, i)) goto done;
+      fence_proxy_async_global();
+    }
+    for (int seg = 0; seg < it.nseg; ++seg) {
+      const CUtensorMap* ma = &p.tmA[it.amap + seg];
+      const CUtensorMap* mbm = &p.tmB[it.bmap + seg];
+      for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
+        if (!wait_bar(p, S.empty(stage), phase ^ 1u, WHERE_PRODUCER, i)) goto done;
+        const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * STAGE_BYTES;
+        const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+        mbar_arrive_expect_tx(S.full(stage), STAGE_BYTES);
+        tma_load_2d(a_dst, ma, S.full(stage), kb * BK, it.arow);
+        const int n0 = it.nb * BN;
+        if (it.bz < 0) {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(b_dst + j * B_BOX_BYTES, mbm, S.full(stage), n0 + 64 * j, kb * BK);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_3d(b_dst + j * B_BOX_BYTES, mbm, S.full(stage), n0 + 64 * j, kb * BK, it.bz);
+        }
+        issued_mask |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+done:
+  // Every load issued must have landed before the CTA may exit.
+  for (int s = 0; s < STAGES; ++s)
+    if (issued_mask & (1u << s))
+      wait_bar(p, S.full(s), (issued_par >> s) & 1u, WHERE_DRAIN, s, /*honor_abort=*/false);
+}
+
+__device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int buf = 0;
+  uint32_t acc_phase = 0;
+  const int n_items = n_items_for(p);
+  for (int i = cid; i < n_items; i += p.n_compute) {
+    Item it;
+    decode(p, i, it);
+    if (!wait_bar(p, S.tempty(buf), acc_phase ^ 1u, WHERE_MMA, i)) goto done;
+    tc_fence_after();
+    {
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      uint32_t acc = 0;
+      for (int seg = 0; seg < it.nseg; ++seg) {
+        for (int kb = 0; kb < it.nkb; ++kb) {
+          if (!wait_bar(p, S.full(stage), phase, WHERE_MMA, i)) goto done;
+          tc_fence_after();
+          const uint32_t a_addr = S.ring + static_cast<uint32_t>(stage) * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // A: K-major, 128-B swizzle, 8-row atoms 1024 B apart; +32 B per 16-wide K step.
+            const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
+            // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
+            // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
+            const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
+            acc = 1;
+          }
+          tc_commit(S.empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    tc_commit(S.tfull(buf));
+    if (++buf == 2) {
+      buf = 0;
+      acc_phase ^= 1u;
+    }
+  }
+done:
+  // Every MMA issued must have completed before tensor memory is freed.
+  tc_commit(S.drain());
+  wait_bar(p, S.drain(), 0, WHERE_DRAIN, 0, /*honor_abort=*/false);
+}
+
+__device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&r)[32], int ncols_valid,
+                                                bool f32) {
+  // dst: first of 32 consecutive output columns of one row; ncols_valid in [0, 32], multiple of 8.
+  if (f32) {
+    float* d = reinterpret_cast<float*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (4 * q < ncols_valid) st_global_v4(d + 4 * q, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+  } else {
+    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (8 * q < ncols_valid) {
+        const uint32_t w0 = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+        const uint32_t w1 = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+        const uint32_t w2 = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+        const uint32_t w3 = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+        st_global_v4(d + 8 * q, w0, w1, w2, w3);
+      }
+    }
+  }
+}
+
+__device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
+  const int trow = quarter * 32 + lane;
+  const size_t esz = p.out_f32 ? 4 : 2;
+  int buf = 0;
+  uint32_t acc_phase = 0;
+  const int n_items = n_items_for(p);
+  for (int i = cid; i < n_items; i += p.n_compute) {
+    Item it;
+    decode(p, i, it);
+    if (!wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i)) return;
+    tc_fence_after();
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(buf * BN);
+    const bool row_ok = trow >= it.row_lo && trow < it.row_hi;
+    const int grow = it.out_row0 + trow;
+    const int n0 = it.nb * BN;
+    if (it.slot >= 0) {
+      // Partial tile -> staging slot.  Layout: float4 (row, column group cg)
+      // at index cg*BM + row, so a warp's 32 rows form 512 contiguous bytes.
+      float* slot = p.staging + static_cast<size_t>(it.slot) * TILE_F32;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float* d = slot + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4;
+          st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+        const int col = n0 + 32 * c;
+        const int nvalid = max(0, min(32, p.N - col));
+        if (!row_ok || nvalid == 0) continue;
+        if (p.op == OP_AG || p.op == OP_MOE) {
+          uint8_t* base = reinterpret_cast<uint8_t*>(p.out[p.op == OP_MOE ? it.mb : 0]);
+          store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
+        } else if (p.op == OP_RS) {
+          const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
+          uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
+          store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
+        } else {  // OP_AR: the same bits to every replica
+          for (int o = 0; o < p.R; ++o) {
+            uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
+            store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
+          }
+        }
+      }
+    }
+    // Tensor memory of this buffer may be overwritten by the next tile's MMAs.
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(S.tempty(buf));
+      if (it.slot >= 0) mbar_arrive(S.pdone(buf));
+    }
+    if (it.slot >= 0 && warp == 2 && lane == 0) {
+      // All four epilogue warps have stored their rows of this partial tile
+      // (bounded wait on the per-buffer barrier), then one gpu-scope release.
+      if (!wait_bar(p, S.pdone(buf), acc_phase, WHERE_EPILOGUE, i)) return;
+      const bool skip = (p.inject == 2 && it.slot == 0);
+      if (!skip) {
+        __threadfence();
+        st_release_gpu(p.flags + it.slot, p.epoch);
+      }
+    }
+    if (++buf == 2) {
+      buf = 0;
+      acc_phase ^= 1u;
+    }
+  }
+}
+
+__device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ComputeSmem S;
+  S.ring = smem_u32(smem);
+  S.bars = smem_u32(smem + RING_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + 168);
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(S.full(s), 1);
+      mbar_init(S.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(S.tfull(b), 1);
+      mbar_init(S.tempty(b), 4);
+    }
+    mbar_init(S.drain(), 1);
+    for (int b = 0; b < 2; ++b) mbar_init(S.pdone(b), 4);
+    fence_mbar_init();
+    for (int r = 0; r < MK_MAX_RANKS; ++r) {
+      if (r < p.R || r < 2) {
+        tma_prefetch_map(&p.tmA[r]);
+        tma_prefetch_map(&p.tmB[r]);
+      }
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) producer(p, S, cid);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(p, S, tmem_base, cid);
+    __syncwarp();
+  } else if (warp >= 2 && warp <= 5) {
+    epilogue(p, S, tmem_base, cid);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ copy-in role (AG)
+constexpr int COPY_NBUF = 6;
+constexpr uint32_t COPY_BUF = 32768;
+
+struct CopyIter {
+  int c;          // position in this CTA's chunk list (global copy-order index)
+  int mb;         // current chunk
+  long long row;  // next gathered row to copy in this chunk
+  long long off;  // byte offset inside the current contiguous run
+};
+
+struct Piece {
+  const uint8_t* src;
+  uint8_t* dst;
+  uint32_t bytes;
+  int chunk;
+  bool last;  // last piece of its chunk
+};
+
+// The contiguous run of the current chunk that starts at gathered row `row`:
+// rows of one shard, skipping the local shard's rows when it is not copied.
+__device__ __forceinline__ bool copy_run(const FusedParams& p, int mb, long long& row, long long& hi,
+                                         int& s) {
+  const long long end = min(static_cast<long long>(mb + 1) * BM, static_cast<long long>(p.M));
+  while (row < end) {
+    s = static_cast<int>(row / p.m_r);
+    hi = min(end, static_cast<long long>(s + 1) * p.m_r);
+    if (s == p.local && !p.copy_local) {
+      row = hi;
+      continue;
+    }
+    return true;
+  }
+  return false;
+}
+
+__device__ bool copy_next(const FusedParams& p, int cid, CopyIter& st, Piece& pc) {
+  const size_t rb = static_cast<size_t>(p.K) * 2;
+  while (st.c < p.n_copy_chunks) {
+    long long hi;
+    int s;
+    long long row = st.row;
+    if (copy_run(p, st.mb, row, hi, s)) {
+      const long long run_bytes = (hi - row) * static_cast<long long>(rb);
+      const long long left = run_bytes - st.off;
+      const uint32_t n = static_cast<uint32_t>(min(left, static_cast<long long>(COPY_BUF)));
+      pc.src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb + st.off;
+      pc.dst = p.gathered + static_cast<size_t>(row) * rb + st.off;
+      pc.bytes = n;
+      pc.chunk = st.mb;
+      st.off += n;
+      st.row = row;
+      if (st.off == run_bytes) {
+        st.row = hi;
+        st.off = 0;
+      }
+      // last piece of the chunk?
+      long long r2 = st.row, h2;
+      int s2;
+      pc.last = (st.off == 0) && !copy_run(p, st.mb, r2, h2, s2);
+      if (pc.last) {
+        st.c += p.n_copy;
+        if (st.c < p.n_copy_chunks) {
+          st.mb = ag_copy_mb(p, st.c);
+          st.row = static_cast<long long>(st.mb) * BM;
+        }
+      }
+      return true;
+    }
+    // chunk with nothing to copy (only local rows): signal it right away
+    pc.src = nullptr;
+    pc.dst = nullptr;
+    pc.bytes = 0;
+    pc.chunk = st.mb;
+    pc.last = true;
+    st.c += p.n_copy;
+    if (st.c < p.n_copy_chunks) {
+      st.mb = ag_copy_mb(p, st.c);
+      st.row = static_cast<long long>(st.mb) * BM;
+      st.off = 0;
+    }
+    return true;
+  }
+  return false;
+}
+
+__device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
+  if (threadIdx.x != 0) return;
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bars = smem_u32(smem + RING_BYTES) + 104u;
+  for (int b = 0; b < COPY_NBUF; ++b) mbar_init(bars + 8u * b, 1);
+  fence_mbar_init();
+
+  CopyIter st;
+  st.c = cid;
+  st.off = 0;
+  if (st.c < p.n_copy_chunks) {
+    st.mb = ag_copy_mb(p, st.c);
+    st.row = static_cast<long long>(st.mb) * BM;
+  }
+  Piece q[COPY_NBUF];  // pieces whose loads are in flight, by buffer
+  int pend_chunk[16];
+  long long pend_seq[16];
+  int n_pend = 0;
+  long long n_load = 0, n_store = 0;
+  bool more = true, ok = true;
+  const bool inject = (p.inject == 1 && cid == 0);
+  bool injected = false;
+
+  auto issue_load = [&](long long seq) -> bool {
+    Piece pc;
+    if (!copy_next(p, cid, st, pc)) return false;
+    const int b = static_cast<int>(seq % COPY_NBUF);
+    q[b] = pc;
+    const uint32_t bar = bars + 8u * b;
+    if (pc.bytes) {
+      mbar_arrive_expect_tx(bar, pc.bytes);
+      bulk_g2s(ring + static_cast<uint32_t>(b) * COPY_BUF, pc.src, pc.bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+    return true;
+  };
+  auto release = [&](int chunk) {
+    if (inject && !injected) {
+      injected = true;
+      return;
+    }
+    st_release_gpu(p.flags + chunk, p.epoch);
+  };
+
+  for (; n_load < COPY_NBUF - 1 && more; ++n_load) more = issue_load(n_load);
+  if (!more) --n_load;
+  while (n_store < n_load) {
+    const int b = static_cast<int>(n_store % COPY_NBUF);
+    if (!wait_bar(p, bars + 8u * b, static_cast<uint32_t>((n_store / COPY_NBUF) & 1), WHERE_COPY,
+                  q[b].chunk)) {
+      ok = false;
+      break;
+    }
+    if (q[b].bytes) bulk_s2g(q[b].dst, ring + static_cast<uint32_t>(b) * COPY_BUF, q[b].bytes);
+    bulk_commit();
+    if (q[b].last) {
+      pend_chunk[n_pend] = q[b].chunk;
+      pend_seq[n_pend] = n_store;
+      ++n_pend;
+    }
+    ++n_store;
+    // Release chunks whose stores are at least 8 groups old (complete).
+    bulk_wait<8>();
+    int keep = 0;
+    for (int j = 0; j < n_pend; ++j) {
+      if (pend_seq[j] <= n_store - 9) {
+        fence_proxy_async_global();
+        release(pend_chunk[j]);
+      } else {
+        pend_chunk[keep] = pend_chunk[j];
+        pend_seq[keep] = pend_seq[j];
+        ++keep;
+      }
+    }
+    n_pend = keep;
+    if (n_pend >= 15) {  // bound the queue: wait for everything, release all
+      bulk_wait<0>();
+      fence_proxy_async_global();
+      for (int j = 0; j < n_pend; ++j) release(pend_chunk[j]);
+      n_pend = 0;
+    }
+    // Refill the buffer whose store was issued one step ago.
+    if (more) {
+      bulk_wait_read<1>();
+      if (issue_load(n_load)) ++n_load;
+      else more = false;
+    }
+  }
+  bulk_wait<0>();
+  if (ok) {
+    fence_proxy_async_global();
+    for (int j = 0; j < n_pend; ++j) release(pend_chunk[j]);
+  }
+  // Loads that were issued but not stored (abort path) must land before exit.
+  for (long long s2 = n_store; s2 < n_load; ++s2) {
+    const int b = static_cast<int>(s2 % COPY_NBUF);
+    wait_bar(p, bars + 8u * b, static_cast<uint32_t>((s2 / COPY_NBUF) & 1), WHERE_DRAIN, 0, false);
+  }
+}
+
+// ------------------------------------------------------------------ reduce role (RS / AR)
+constexpr int RED_NSETS = 3;
+
+__device__ void reduce_role(const FusedParams& p, uint8_t* smem, int rid) {
+  const int tid = threadIdx.x;
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bars = smem_u32(smem + RING_BYTES) + 104u;
+  __shared__ int s_abort;
+  const int P = p.P;
+  const int pc = (P <= 8) ? 4 : 2;  // column groups (4 floats) per piece
+  const uint32_t piece_bytes = static_cast<uint32_t>(pc * BM * 16);
+  const uint32_t set_bytes = static_cast<uint32_t>(P) * piece_bytes;
+  const int ppt = (BN / 4) / pc;  // pieces per tile
+  const int my_tiles = (rid < p.n_tiles) ? (p.n_tiles - rid + p.n_reduce - 1) / p.n_reduce : 0;
+  const long long total = static_cast<long long>(my_tiles) * ppt;
+  if (tid == 0) {
+    for (int b = 0; b < RED_NSETS; ++b) mbar_init(bars + 8u * b, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+
+  __shared__ long long s_issued;
+  auto issue = [&](long long seq) -> bool {  // thread 0 only
+    const int t = static_cast<int>(seq / ppt), j = static_cast<int>(seq - static_cast<long long>(t) * ppt);
+    const int q = rid + t * p.n_reduce;
+    int mb, nb;
+    raster(p, q, mb, nb);
+    const int tile = mb * p.n_nblk + nb;
+    if (j == 0) {
+      for (int part = 0; part < P; ++part)
+        if (!wait_flag(p, p.flags + static_cast<size_t>(tile) * P + part, WHERE_REDUCE, q)) return false;
+      fence_proxy_async_global();
+    }
+    const int b = static_cast<int>(seq % RED_NSETS);
+    const uint32_t bar = bars + 8u * b;
+    mbar_arrive_expect_tx(bar, set_bytes);
+    for (int part = 0; part < P; ++part) {
+      const float* src = p.staging + (static_cast<size_t>(tile) * P + part) * TILE_F32 +
+                         static_cast<size_t>(j) * pc * BM * 4;
+      bulk_g2s(ring + b * (64u * 1024u) + part * piece_bytes, src, piece_bytes, bar);
+    }
+    return true;
+  };
+
+  if (tid == 0) {
+    long long n = 0;
+    for (; n < RED_NSETS - 1 && n < total; ++n)
+      if (!issue(n)) {
+        s_abort = 1;
+        break;
+      }
+    s_issued = n;
+  }
+  __syncthreads();
+  const size_t esz = p.out_f32 ? 4 : 2;
+  long long seq = 0;
+  for (; seq < total; ++seq) {
+    // 1. keep RED_NSETS-1 sets in flight (the set refilled here was consumed
+    //    in the previous iteration, which ended with a barrier)
+    if (tid == 0 && !s_abort && s_issued == seq + RED_NSETS - 1 && s_issued < total) {
+      if (issue(s_issued)) ++s_issued;
+      else s_abort = 1;
+    }
+    __syncthreads();
+    if (s_abort || seq >= s_issued) break;
+    // 2. wait for this set's partial pieces
+    const int b = static_cast<int>(seq % RED_NSETS);
+    if (!wait_bar(p, bars + 8u * b, static_cast<uint32_t>((seq / RED_NSETS) & 1), WHERE_REDUCE,
+                  static_cast<int>(seq)))
+      s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    // 3. sum the P partials in fixed order and store
+    const int t = static_cast<int>(seq / ppt), j = static_cast<int>(seq - static_cast<long long>(t) * ppt);
+    const int qq = rid + t * p.n_reduce;
+    int mb, nb;
+    raster(p, qq, mb, nb);
+    const uint8_t* buf = smem + b * (64 * 1024);
+    const int units = BM * pc / 2;  // (row, pair of column groups)
+    for (int u = tid; u < units; u += NTHREADS) {
+      const int row = u % BM, cp = u / BM;
+      float a[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) a[x] = 0.f;
+      for (int part = 0; part < P; ++part) {
+        const float4 v0 = *reinterpret_cast<const float4*>(buf + part * piece_bytes + ((2 * cp) * BM + row) * 16);
+        const float4 v1 = *reinterpret_cast<const float4*>(buf + part * piece_bytes + ((2 * cp + 1) * BM + row) * 16);
+        if (part == 0) {
+          a[0] = v0.x; a[1] = v0.y; a[2] = v0.z; a[3] = v0.w;
+          a[4] = v1.x; a[5] = v1.y; a[6] = v1.z; a[7] = v1.w;
+        } else {
+          a[0] += v0.x; a[1] += v0.y; a[2] += v0.z; a[3] += v0.w;
+          a[4] += v1.x; a[5] += v1.y; a[6] += v1.z; a[7] += v1.w;
+        }
+      }
+      const int grow = mb * BM + row;
+      const int col = nb * BN + (j * pc + 2 * cp) * 4;
+      if (grow >= p.M || col >= p.N) continue;
+      const int nrep = (p.op == OP_AR) ? p.R : 1;
+      for (int o = 0; o < nrep; ++o) {
+        uint8_t* base;
+        size_t off;
+        if (p.op == OP_RS) {
+          const int ow = grow / p.rows_per_owner;
+          base = reinterpret_cast<uint8_t*>(p.out[ow]);
+          off = (static_cast<size_t>(grow - ow * p.rows_per_owner) * p.N + col) * esz;
+        } else {
+          base = reinterpret_cast<uint8_t*>(p.out[o]);
+          off = (static_cast<size_t>(grow) * p.N + col) * esz;
+        }
+        if (p.out_f32) {
+          st_global_v4(base + off, __float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                       __float_as_uint(a[3]));
+          st_global_v4(base + off + 16, __float_as_uint(a[4]), __float_as_uint(a[5]),
+                       __float_as_uint(a[6]), __float_as_uint(a[7]));
+        } else {
+          st_global_v4(base + off, pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                       pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  // Sets issued but not consumed (abort path) must land before the CTA exits.
+  if (tid == 0) {
+    for (long long s2 = seq; s2 < s_issued; ++s2) {
+      const int b = static_cast<int>(s2 % RED_NSETS);
+      wait_bar(p, bars + 8u * b, static_cast<uint32_t>((s2 / RED_NSETS) & 1), WHERE_DRAIN, 0, false);
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_constant__ FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint32_t s_ticket;
+  if (threadIdx.x == 0) {
+    const uint32_t t = atomicAdd(&p.hdr[HDR_TICKET], 1u);
+    if (t == gridDim.x - 1) atomicExch(&p.hdr[HDR_TICKET], 0u);
+    s_ticket = t;
+  }
+  __syncthreads();
+  const int t = static_cast<int>(s_ticket);
+  if (t < p.n_copy) {
+    copy_role(p, smem, t);
+  } else if (t < p.n_copy + p.n_compute) {
+    compute_role(p, smem, t - p.n_copy);
+  } else {
+    reduce_role(p, smem, t - p.n_copy - p.n_compute);
+  }
+}
+
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(mk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  mk_fused_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

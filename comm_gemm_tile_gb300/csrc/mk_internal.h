@@ -1,0 +1,88 @@
+// mk_internal.h -- definitions shared by the host launchers and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mk.h"
+
+namespace mk {
+
+// Tile shape of the compute role: one 128 x 256 fp32 accumulator per tile in
+// tensor memory (two of them, double-buffered, fill all 512 TMEM columns),
+// K consumed in 64-element (128-byte) slabs through a 4-stage smem ring.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int NTHREADS = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, 6-7 spare
+constexpr int A_STAGE_BYTES = BM * BK * 2;    // 16 KiB, K-major, 128-B swizzle
+constexpr int B_BOX_BYTES = BK * 64 * 2;      // 8 KiB: 64 K-rows x 64 N-cols, MN-major
+constexpr int B_STAGE_BYTES = BN * BK * 2;    // 32 KiB = 4 boxes
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;   // 192 KiB, reused by copy/reduce roles
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int TILE_F32 = BM * BN;              // floats in one partial tile
+constexpr int MAX_PARTIALS = 16;               // partial tiles reduced per output tile
+
+// Workspace header words (uint32 each).
+enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_WORDS = 64 };
+constexpr size_t WS_HDR_BYTES = 256;
+
+enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3 };
+
+// Role codes used in the error detail word.
+enum { WHERE_PRODUCER = 1, WHERE_MMA = 2, WHERE_EPILOGUE = 3, WHERE_COPY = 4, WHERE_REDUCE = 5,
+       WHERE_DRAIN = 6, WHERE_MOE = 7 };
+
+struct FusedParams {
+  CUtensorMap tmA[MK_MAX_RANKS];   // AG: [0] local shard, [1] gathered A; RS/AR: A_r; MoE: recv_x[d]
+  CUtensorMap tmB[MK_MAX_RANKS];   // AG: [0] B; RS/AR: B_r; MoE: W[d] (3-D)
+  const uint8_t* shard[MK_MAX_RANKS];
+  void* out[MK_MAX_RANKS];
+  uint8_t* gathered;
+  uint32_t* flags;
+  float* staging;
+  uint32_t* hdr;
+  const int* moe_tiles;            // MoE: tile table (see mk_moe.cu)
+  const int* moe_ntiles;           // MoE: number of valid entries in the table
+  long long wait_ns;
+  uint32_t epoch;
+  int op, mode, R, local;
+  int M, N, K;
+  int m_r;
+  int n_mblk, n_nblk, n_kblk;
+  int group_m;
+  int split_k, kps;
+  int P;
+  int n_tiles, n_items;
+  int n_copy, n_compute, n_reduce;
+  int out_f32;
+  int copy_local, ordered;
+  int inject;
+  int rows_per_owner;
+  int n_copy_chunks;
+};
+
+// Workspace layout for the AG / RS / AR ops.
+struct WsLayout {
+  size_t flags_off, n_flags, staging_off, staging_bytes, total;
+};
+
+inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
+int device_sm_count();
+uint32_t next_epoch();
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+                 uint32_t b2);
+long long default_wait_ns(const mk_config* cfg);
+
+}  // namespace mk

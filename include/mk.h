@@ -1,0 +1,191 @@
+/*
+ * mk.h -- C ABI of the tile-pipelined fused collective + GEMM library for
+ * GB300 (sm_103a).
+ *
+ * The operations are the fused kernels of the mKernel write-up
+ * (news.chathome.org, "五种融合内核" table): AllGather + GEMM,
+ * GEMM + ReduceScatter, GEMM + AllReduce and MoE Dispatch + GEMM.  The R
+ * "ranks" are virtual: each rank's operands are separate device buffers (its
+ * partition) in the memory of ONE GPU, and one persistent kernel per call
+ * moves data between partitions with in-kernel copy / reduce roles while
+ * its compute role runs TMA-fed tcgen05 (TMEM-accumulated) bf16 tiles.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Matrices are row-major.  A operands are [rows x k], B operands [k x n]
+ *   (the x @ W convention); outputs are [rows x n].  bf16 inputs, fp32
+ *   accumulation, output rounded once to bf16 (round-to-nearest-even) or
+ *   written as fp32.
+ * - Alignment: every device pointer must be 16-byte aligned; k and n must be
+ *   multiples of 8 (16-byte row pitch for the tensor-memory-access engine).
+ *   Row counts may be anything (ragged tiles are masked).
+ * - Pointer arrays (`const void* const* a` etc.) are HOST arrays of R
+ *   DEVICE pointers; the library copies them at call time.
+ * - Ownership: the caller owns and allocates every buffer, including the
+ *   workspace.  The library allocates no device memory.  It keeps only a
+ *   per-device cache of SM count and kernel attributes, and a global call
+ *   counter (the epoch) used to tag ready flags.
+ * - Workspace: size it with mk_workspace_size() for the same op/shape/config
+ *   and zero-fill it ONCE before its first use (cudaMemset); the library
+ *   leaves it valid for later calls (flags are epoch-tagged, so no reset is
+ *   needed between calls).  One workspace must not be used by two calls that
+ *   may run at the same time.
+ * - Asynchrony: every compute entry point only enqueues work on `stream`
+ *   and returns.  Host-side argument errors return MK_ERR_INVALID /
+ *   MK_ERR_UNSUPPORTED before anything is launched; a failed launch returns
+ *   MK_ERR_CUDA.  Device-side errors (a ready-flag or pipeline wait that ran
+ *   past mk_config.wait_limit_ns, a MoE capacity overflow) are recorded in a
+ *   status word inside the workspace: read it with mk_get_device_status().
+ *   A wait that times out never hangs the GPU: the kernel stops, releases its
+ *   tensor memory and returns.
+ * - No C++ exception crosses this interface.
+ * - R is limited to MK_MAX_RANKS.
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_MAX_RANKS 16
+#define MK_VERSION 1
+
+/* Opaque CUDA stream (identical to cudaStream_t); NULL = legacy default stream. */
+typedef struct CUstream_st *mk_stream_t;
+
+typedef enum {
+  MK_OK = 0,
+  MK_ERR_INVALID = 1,      /* bad argument (NULL pointer, bad size, misaligned, R out of range) */
+  MK_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (e.g. no sm_103a device)   */
+  MK_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                                 */
+  MK_ERR_TIMEOUT = 4,      /* device: a bounded wait gave up (missing flag / stalled pipeline)  */
+  MK_ERR_CAPACITY = 5      /* device: MoE rows for a rank exceeded cap_rows                     */
+} mk_status;
+
+typedef enum { MK_BF16 = 0, MK_F32 = 1 } mk_dtype;
+
+typedef enum { MK_OP_AG_GEMM = 0, MK_OP_GEMM_RS = 1, MK_OP_GEMM_AR = 2, MK_OP_MOE = 3 } mk_op;
+
+/* Execution mode: the fused single-launch path, or one of the two baselines
+ * that the same library provides for measuring how much of the data movement
+ * the fused path hides. */
+typedef enum {
+  MK_MODE_FUSED = 0,     /* one persistent launch: copy/reduce roles overlap the GEMM tiles */
+  MK_MODE_GEMM_ONLY = 1, /* the same FLOPs with no data movement: AG reads a_gathered as
+                            already filled; RS/AR accumulate all ranks in tensor memory      */
+  MK_MODE_UNFUSED = 2    /* host-ordered: a copy launch then a GEMM launch (AG), or a
+                            partial-GEMM launch then a reduce launch (RS/AR)               */
+} mk_mode;
+
+/* Tuning and test knobs.  Pass NULL, or zero a field, for the built-in choice. */
+typedef struct {
+  int n_copy_ctas;          /* AG / MoE: CTAs taking the copy-in role                  */
+  int n_reduce_ctas;        /* RS / AR: CTAs taking the reduce role                    */
+  int max_ctas;             /* cap on the persistent grid (default: one CTA per SM)    */
+  int group_m;              /* tile raster: m-blocks per group (default per op)        */
+  int split_k;              /* RS / AR: K slices per rank, each its own partial tile   */
+  int mode;                 /* mk_mode                                                  */
+  long long wait_limit_ns;  /* bound on every device-side wait (default 2e9 ns)        */
+  int inject;               /* test only: 1 = one copy-in chunk never signals ready;
+                               2 = one partial tile never signals ready                */
+} mk_config;
+
+/* Bytes of workspace an op needs for this shape and config (0 on bad args).
+ *   AG:  m = rows per shard (m_r), n, k.        RS / AR: m = rows of each A_r, n, k.
+ *   MoE: m = tokens per rank T, n = N, k = H; R ranks; cfg->split_k is ignored.
+ * For MoE the E_loc/topk/cap_rows that matter are passed to mk_moe_workspace_size. */
+size_t mk_workspace_size(int op, int R, long long m, long long n, long long k,
+                         const mk_config *cfg);
+
+/* AllGather + GEMM (five-kernel table, row "AllGather + GEMM"): each rank
+ * holds one row shard of A; the shards are gathered and every A tile is
+ * consumed by the GEMM as soon as it has landed.  This call computes the
+ * result of rank `local_rank`:
+ *   a_gathered = [A_0; A_1; ...; A_{R-1}]   ([R*m_r x k] bf16, in rank order)
+ *   c          = a_gathered @ b             ([R*m_r x n], c_dtype)
+ * a_shards: R device pointers, each [m_r x k] bf16.  b: [k x n] bf16.
+ * a_gathered: [R*m_r x k] bf16, written (it may alias a_shards[local_rank]
+ * at row offset local_rank*m_r, in which case that shard is not copied).
+ * The copy-in role moves the remote shards in ring order local+1, local+2, ...
+ * and releases a ready flag per 128-row chunk; compute tiles of the local
+ * shard start at once, the others after their chunk's flag. */
+mk_status mk_ag_gemm(const void *const *a_shards, const void *b, void *a_gathered, void *c,
+                     mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n,
+                     long long k, void *workspace, size_t ws_bytes, const mk_config *cfg,
+                     mk_stream_t stream);
+
+/* GEMM + ReduceScatter (five-kernel table, row "GEMM + ReduceScatter"):
+ *   S = sum_r A_r @ B_r  (A_r [m x k], B_r [k x n], bf16; fp32 accumulation)
+ *   c_blocks[o] = rows [o*m/R, (o+1)*m/R) of S   ([m/R x n], c_dtype)
+ * m must be a multiple of R.  Every output tile's per-rank partial (fp32) is
+ * staged in the owner's slot as soon as it is produced; the reduce role sums
+ * the R partials of a tile in rank order 0..R-1 once all have been flagged
+ * ready, and writes the owner's block. */
+mk_status mk_gemm_rs(const void *const *a, const void *const *b, void *const *c_blocks,
+                     mk_dtype c_dtype, int R, long long m, long long n, long long k,
+                     void *workspace, size_t ws_bytes, const mk_config *cfg, mk_stream_t stream);
+
+/* GEMM + AllReduce (five-kernel table, row "GEMM + AllReduce"):
+ *   S = sum_r A_r @ B_r, and c_replicas[r] = S for every r  ([m x n], c_dtype).
+ * Reduced exactly like mk_gemm_rs (rank order 0..R-1); the one reduced tile is
+ * written to all R replica buffers, so the replicas are bit-identical. */
+mk_status mk_gemm_ar(const void *const *a, const void *const *b, void *const *c_replicas,
+                     mk_dtype c_dtype, int R, long long m, long long n, long long k,
+                     void *workspace, size_t ws_bytes, const mk_config *cfg, mk_stream_t stream);
+
+/* Workspace bytes for mk_moe_dispatch_gemm (0 on bad args). */
+size_t mk_moe_workspace_size(int R, int E_loc, int topk, long long T, long long H, long long N,
+                             long long cap_rows, const mk_config *cfg);
+
+/* MoE Dispatch + grouped GEMM (five-kernel table, row "MoE Dispatch + GEMM"):
+ * route every token of every rank to its top-k experts, move each
+ * (token, expert) row to the rank that holds the expert, and multiply the rows
+ * of each expert by that expert's weight, in one pipeline where a GEMM tile
+ * starts as soon as its rows have landed.
+ *   x[r]:      [T x H] bf16 tokens of rank r (device)
+ *   logits[r]: [T x E] fp32 router logits, E = R*E_loc, finite (device)
+ *   w[d]:      [E_loc x H x N] bf16 weights of the experts d*E_loc .. d*E_loc+E_loc-1
+ * Routing: top-k logits per token, largest first, ties to the lower expert id.
+ * Expert e is held by rank e / E_loc.  Rank d receives the rows routed to its
+ * experts ordered by (local expert, global token id g = r*T + t).
+ * Outputs (all device, int32 unless stated):
+ *   topk_idx   [R*T x topk]   expert ids (row g = r*T + t)
+ *   counts     [R x E]        counts[r*E + e] = rows of source rank r routed to e
+ *   recv_src[d][cap_rows]     g*topk + slot of each received row
+ *   recv_counts[R]            rows received by each rank
+ *   recv_x[d]  [cap_rows x H] bf16 received rows (bit copies of x rows)
+ *   y[d]       [cap_rows x N] bf16, y[d][j] = recv_x[d][j] @ w[d][local expert of j]
+ * Rows past recv_counts[d] are left untouched.  If a rank would receive more
+ * than cap_rows rows, nothing is dispatched for the call and the device status
+ * becomes MK_ERR_CAPACITY. */
+mk_status mk_moe_dispatch_gemm(const void *const *x, const float *const *logits,
+                               const void *const *w, int R, int E_loc, int topk, long long T,
+                               long long H, long long N, long long cap_rows, int *topk_idx,
+                               int *counts, int *const *recv_src, int *recv_counts,
+                               void *const *recv_x, void *const *y, void *workspace,
+                               size_t ws_bytes, const mk_config *cfg, mk_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of a
+ * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the
+ * stream itself reports an error).  `detail` (may be NULL) receives a code
+ * saying which wait failed (role * 1e6 + item index), for diagnostics. */
+mk_status mk_get_device_status(const void *workspace, mk_stream_t stream, long long *detail);
+
+/* Static text for a status code. */
+const char *mk_status_string(mk_status s);
+
+/* MK_VERSION of the loaded library. */
+int mk_version(void);
+
+/* Number of SMs the library will use on the current device (0 if none). */
+int mk_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H_ */

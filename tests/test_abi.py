@@ -1,0 +1,105 @@
+"""The C-ABI library: it loads, exports every entry point declared in
+include/mk.h, and rejects bad arguments before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import comm_gemm_tile_gb300 as mk
+from comm_gemm_tile_gb300 import build as mkbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    mkbuild.build()
+    return mk.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mk.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert L.mk_version() == 1
+    assert "timed out" in mk.status_string(mk.MK_ERR_TIMEOUT)
+    assert "capacity" in mk.status_string(mk.MK_ERR_CAPACITY)
+    assert mk.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(L):
+    # RS, 8 ranks, 8192x8192 output: 2048 tiles x 8 fp32 partials of 128x256.
+    sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584)
+    assert sz >= 2048 * 8 * 128 * 256 * 4
+    assert sz < 2048 * 8 * 128 * 256 * 4 + (1 << 20)
+    # GEMM-only mode needs no staging.
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584,
+                             mk.Config(mode=mk.MODE_GEMM_ONLY)) < (1 << 20)
+    # AG: one flag per 128-row chunk of the gathered A.
+    assert 256 < mk.workspace_size(mk.OP_AG_GEMM, 8, 1024, 3584, 8192) < 4096
+    # bad shapes -> 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8190, 64, 64) == 0     # m % R
+    assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 260, 64) == 0     # n % 8
+    assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 256, 60) == 0     # k % 8
+    assert mk.workspace_size(mk.OP_GEMM_RS, 0, 256, 256, 64) == 0     # R
+    assert mk.workspace_size(mk.OP_GEMM_RS, 17, 17 * 16, 256, 64) == 0
+    # AR split-K keeps at most 16 partials per tile
+    assert mk.workspace_size(mk.OP_GEMM_AR, 8, 128, 8192, 3584) <= 32 * 16 * 128 * 256 * 4 + (1 << 20)
+
+
+def _null_ptrs(n):
+    return (ctypes.c_void_p * n)()
+
+
+def test_argument_validation_without_launch(L):
+    V = ctypes.c_void_p
+    good = 0x10000
+    ws = V(good)
+    arr = (ctypes.c_void_p * 2)(good, good)
+    # NULL shard array
+    assert L.mk_ag_gemm(None, V(good), V(good), V(good), 0, 2, 0, 128, 256, 64, ws, 1 << 20,
+                        None, None) == mk.MK_ERR_INVALID
+    # NULL entry inside the array
+    assert L.mk_ag_gemm(_null_ptrs(2), V(good), V(good), V(good), 0, 2, 0, 128, 256, 64, ws,
+                        1 << 20, None, None) == mk.MK_ERR_INVALID
+    # local rank out of range
+    assert L.mk_ag_gemm(arr, V(good), V(good), V(good), 0, 2, 2, 128, 256, 64, ws, 1 << 20, None,
+                        None) == mk.MK_ERR_INVALID
+    # misaligned pointer
+    bad = (ctypes.c_void_p * 2)(good, good + 8)
+    assert L.mk_ag_gemm(bad, V(good), V(good), V(good), 0, 2, 0, 128, 256, 64, ws, 1 << 20, None,
+                        None) == mk.MK_ERR_INVALID
+    # workspace too small
+    assert L.mk_ag_gemm(arr, V(good), V(good), V(good), 0, 2, 0, 128, 256, 64, ws, 16, None,
+                        None) == mk.MK_ERR_INVALID
+    # bad dtype
+    assert L.mk_ag_gemm(arr, V(good), V(good), V(good), 7, 2, 0, 128, 256, 64, ws, 1 << 20, None,
+                        None) == mk.MK_ERR_INVALID
+    # RS: m not a multiple of R
+    assert L.mk_gemm_rs(arr, arr, arr, 0, 2, 255, 256, 64, ws, 1 << 30, None, None) == \
+        mk.MK_ERR_INVALID
+    # RS/AR: k not a multiple of 8, R too large
+    assert L.mk_gemm_ar(arr, arr, arr, 0, 2, 128, 256, 60, ws, 1 << 30, None, None) == \
+        mk.MK_ERR_INVALID
+    assert L.mk_gemm_ar(arr, arr, arr, 0, 17, 128, 256, 64, ws, 1 << 30, None, None) == \
+        mk.MK_ERR_INVALID
+    # NULL workspace / status read
+    assert L.mk_gemm_rs(arr, arr, arr, 0, 2, 256, 256, 64, None, 0, None, None) == \
+        mk.MK_ERR_INVALID
+    assert L.mk_get_device_status(None, None, None) == mk.MK_ERR_INVALID
+
+
+def test_config_struct_layout():
+    assert ctypes.sizeof(mk._Cfg) == 40
+    assert mk._Cfg.wait_limit_ns.offset == 24 and mk._Cfg.inject.offset == 32
