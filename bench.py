@@ -1,0 +1,428 @@
+"""Benchmark of the fused collective + GEMM library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference]
+
+Default workload: AllGather+GEMM with 8 virtual ranks, A shards 1024x8192
+bf16 gathered to 8192x8192, B 8192x3584 (TP=8 MLP up-projection), bf16 out.
+One step = one fused call (one persistent kernel launch) over one input set;
+three input sets (each larger than L2 together with its outputs) are used in
+rotation, so no step reads what the previous one left in L2.
+
+Prints one JSON line (rank 0).  Besides the fused throughput it reports the
+two baselines the same library provides -- the GEMM alone on pre-gathered A
+(no data movement) and the unfused copy-then-GEMM sequence -- and the exposed
+time (fused - GEMM only).  GEMM+ReduceScatter (8 ranks, 8192x3584 @
+3584x8192 per rank) and GEMM+AllReduce (8 ranks, 128x3584 @ 3584x8192) are
+measured the same way and reported under "other_configs".
+
+--impl reference times the CPU oracle (the only other implementation of these
+ops that exists here) on host cores, on a bounded row sample per step.
+With N > 1 each rank runs an independent replica of the workload on its own
+GPU (no collective between GPUs); throughput is the sum over ranks of the
+units processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from comm_gemm_tile_gb300 import inputs as I  # noqa: E402
+
+METRIC = "fused AG+GEMM TFLOP/s on 1 GB300 (AllGather+GEMM, 8 virtual ranks, 8192x8192x3584 bf16)"
+UNIT = "TFLOP/s"
+N_SETS = 3
+
+
+# ------------------------------------------------------------------ environment helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    """(bf16 burst TFLOP/s, bf16 sustained TFLOP/s, HBM GB/s, source)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 25):
+        self.idx = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dev_normal(shape, std, seed, device):
+    """Seeded N(0, std^2) samples drawn on the device, packed to bf16."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(torch.bfloat16)
+
+
+def time_loop(fn, steps, warmup, stream, dist=None):
+    """Device time (ms) of `steps` calls of fn, after `warmup` untimed calls."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_sample_rate(shards_bits, b_bits, target_s: float):
+    """Time the oracle's AG+GEMM on a row sample sized to ~target_s seconds.
+    Returns (TFLOP/s, rows, seconds)."""
+    import oracle as O
+    K = b_bits.shape[0]
+    N = b_bits.shape[1]
+    M = sum(s.shape[0] for s in shards_bits)
+    rows = 16
+    while True:
+        sel = np.linspace(0, M - 1, rows).astype(np.int64)
+        t0 = time.perf_counter()
+        O.ag_gemm(shards_bits, b_bits, rows=sel)
+        t = time.perf_counter() - t0
+        if t >= target_s * 0.5 or rows >= M:
+            break
+        rows = int(min(M, max(rows * 2, rows * target_s / max(t, 1e-3) * 0.9)))
+    return 2.0 * rows * N * K / t / 1e12, rows, t
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return int(max(d.get("num_threads", 1) for d in info))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ the reference (oracle) arm
+
+def run_reference(args):
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as O
+    w = I.AG_R8_TP8_UP
+    shards = [I.bits(I.normal_bf16((w.m, w.k), 1.0, w.a_seed + r)) for r in range(w.R)]
+    bmat = I.bits(I.normal_bf16((w.k, w.n), w.b_std, w.b_seed))
+    per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    _, rows, _ = oracle_sample_rate(shards, bmat, per_step)
+    M = w.R * w.m
+    sel = np.linspace(0, M - 1, rows).astype(np.int64)
+    for _ in range(args.warmup):
+        O.ag_gemm(shards, bmat, rows=sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.ag_gemm(shards, bmat, rows=sel)
+    dt = time.perf_counter() - t0
+    val = 2.0 * rows * w.n * w.k * args.steps / dt / 1e12
+    cores = blas_threads()
+    sample = f"{rows} of {M} output rows per step (all {w.n} columns, K={w.k}), fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "R": w.R, "m_r": w.m, "k": w.k,
+                                        "n": w.n, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ the library arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--other-steps", type=int, default=30)
+    ap.add_argument("--no-other", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--n-copy", type=int, default=0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(device)
+
+    import comm_gemm_tile_gb300 as mk
+    from comm_gemm_tile_gb300 import build as mkbuild
+    mkbuild.build()
+    mk.lib()
+    bf16_peak, _, hbm_peak, peak_src = peaks()
+
+    w = I.AG_R8_TP8_UP
+    seed_off = 100000 * rank          # replicas: an independent problem per rank
+    M = w.R * w.m
+    flops = 2.0 * M * w.n * w.k
+    sets = []
+    for s in range(N_SETS):
+        shards = [dev_normal((w.m, w.k), 1.0, w.a_seed + r + 1000 * s + seed_off, device)
+                  for r in range(w.R)]
+        b = dev_normal((w.k, w.n), w.b_std, w.b_seed + 1000 * s + seed_off, device)
+        g = torch.empty((M, w.k), dtype=torch.bfloat16, device=device)
+        c = torch.empty((M, w.n), dtype=torch.bfloat16, device=device)
+        sets.append((shards, b, g, c))
+    wsp = mk.Workspace(device)
+    cfg_f = mk.Config(n_copy_ctas=args.n_copy)
+
+    def step_fused(i):
+        shards, b, g, c = sets[i % N_SETS]
+        mk.ag_gemm(shards, b, a_gathered=g, c=c, cfg=cfg_f, workspace=wsp, stream=stream)
+
+    # guard for the timed configuration: device status and the gathered bits
+    step_fused(0)
+    st, detail = mk.device_status(wsp, stream)
+    if st != mk.MK_OK:
+        raise SystemExit(f"fused AG+GEMM reported {mk.status_string(st)} ({detail})")
+    if not torch.equal(sets[0][2], torch.cat(sets[0][0], 0)):
+        raise SystemExit("gathered A differs from the shards")
+
+    with ClockSampler(local) as clk:
+        t_fused = time_loop(step_fused, args.steps, args.warmup, stream, dist)
+    st, detail = mk.device_status(wsp, stream)
+    if st != mk.MK_OK:
+        raise SystemExit(f"fused AG+GEMM reported {mk.status_string(st)} ({detail})")
+
+    cfg_g = mk.Config(mode=mk.MODE_GEMM_ONLY)
+    cfg_u = mk.Config(mode=mk.MODE_UNFUSED)
+
+    def step_gemm(i):
+        shards, b, g, c = sets[i % N_SETS]
+        mk.ag_gemm(shards, b, a_gathered=g, c=c, cfg=cfg_g, workspace=wsp, stream=stream)
+
+    def step_unfused(i):
+        shards, b, g, c = sets[i % N_SETS]
+        mk.ag_gemm(shards, b, a_gathered=g, c=c, cfg=cfg_u, workspace=wsp, stream=stream)
+
+    base_steps = max(10, min(args.steps, 200))
+
+    def tmax(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    t_gemm = tmax(time_loop(step_gemm, base_steps, 5, stream, dist) / base_steps)
+    t_unf = tmax(time_loop(step_unfused, base_steps, 5, stream, dist) / base_steps)
+    t_fused_max = tmax(t_fused)
+    ms = t_fused_max / args.steps
+    value = world * flops * args.steps / (t_fused_max * 1e-3) / 1e12
+    achieved = flops / (t_fused / args.steps * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> fused call -> host result
+    hshards = [x.cpu().pin_memory() for x in sets[0][0]]
+    hb = sets[0][1].cpu().pin_memory()
+    hc = torch.empty((M, w.n), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(x.numel() * 2 for x in hshards) + hb.numel() * 2
+    d2h = hc.numel() * 2
+
+    def step_e2e(i):
+        shards, b, g, c = sets[i % N_SETS]
+        for d, h in zip(shards, hshards):
+            d.copy_(h, non_blocking=True)
+        b.copy_(hb, non_blocking=True)
+        mk.ag_gemm(shards, b, a_gathered=g, c=c, cfg=cfg_f, workspace=wsp, stream=stream)
+        hc.copy_(c, non_blocking=True)
+
+    t_e2e = tmax(time_loop(step_e2e, args.e2e_steps, 3, stream, dist))
+    e2e_val = world * flops * args.e2e_steps / (t_e2e * 1e-3) / 1e12
+    st, detail = mk.device_status(wsp, stream)
+    if st != mk.MK_OK:
+        raise SystemExit(f"e2e AG+GEMM reported {mk.status_string(st)} ({detail})")
+
+    other = {}
+    if not args.no_other:
+        other = bench_other(mk, device, stream, dist, args.other_steps, seed_off, tmax,
+                            bf16_peak, hbm_peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, rows, secs = oracle_sample_rate([I.bits(x) for x in hshards], I.bits(hb), 10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{rows} of {M} output rows (all {w.n} columns, K={w.k}), fp64 numpy, "
+                         f"{secs:.1f} s"}
+
+    clocks = clk.summary()
+    set_mb = ((w.R * w.m * w.k + w.k * w.n) * 2 + (M * w.k + M * w.n) * 2) / 1e6
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "R": w.R, "m_r": w.m, "k": w.k, "n": w.n,
+                       "local_rank": 0, "out": "bf16", "parallelism": f"replicas{world}",
+                       "l2": f"{N_SETS} input sets in rotation, each {set_mb:.0f} MB with "
+                             f"outputs (> L2)"},
+            "pct_of_peak": 100.0 * (flops / (ms * 1e-3) / 1e12) / bf16_peak,
+            "exposed_ms": ms - t_gemm,
+            "gemm_only_ms": t_gemm,
+            "unfused_ms": t_unf,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 burst"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "other_configs": other,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+    """Fused / GEMM-only / unfused timings of the RS and AR workloads."""
+    out = {}
+    for w in (I.RS_R8_TP8_DOWN, I.AR_R8_DECODE):
+        nsets = 2 if w.op == "rs" else 3
+        sets = []
+        for s in range(nsets):
+            a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r + 1000 * s + seed_off, device)
+                 for r in range(w.R)]
+            b = [dev_normal((w.k, w.n), w.b_std, w.b_seed + r + 1000 * s + seed_off, device)
+                 for r in range(w.R)]
+            rows = w.m // w.R if w.op == "rs" else w.m
+            o = [torch.empty((rows, w.n), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+            sets.append((a, b, o))
+        ws = mk.Workspace(device)
+        fn = mk.gemm_rs if w.op == "rs" else mk.gemm_ar
+        key = "c_blocks" if w.op == "rs" else "c_replicas"
+        res = {}
+        for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                          ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+            def step(i, cfg=cfg):
+                a, b, o = sets[i % nsets]
+                fn(a, b, cfg=cfg, workspace=ws, stream=stream, **{key: o})
+            n = steps if w.op == "rs" else steps * 10
+            res[name] = tmax(time_loop(step, n, 3, stream, dist)) / n
+        st, _ = mk.device_status(ws, stream)
+        flops = w.flops()
+        fused_tf = flops / (res["fused"] * 1e-3) / 1e12
+        entry = {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"],
+                 "unfused_ms": res["unfused"], "exposed_ms": res["fused"] - res["gemm_only"],
+                 "fused_tflops": fused_tf, "pct_of_peak": 100 * fused_tf / bf16_peak,
+                 "status": mk.status_string(st)}
+        if w.op == "ar":
+            hbm_bytes = w.R * (w.k * w.n * 2 + w.m * w.k * 2) + w.R * w.m * w.n * 2
+            entry["bound"] = "hbm"
+            entry["hbm_gbs"] = hbm_bytes / (res["fused"] * 1e-3) / 1e9
+            entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
+        out[w.name] = entry
+        del sets, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

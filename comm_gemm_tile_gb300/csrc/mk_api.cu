@@ -75,6 +75,14 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uin
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A buffer argument is valid when it is 16-byte aligned and, unless the
+// buffer it describes is empty, not NULL (empty framework tensors may carry
+// a NULL data pointer).
+static inline bool buf_ok(const void* p, long long elems) {
+  if (elems > 0 && !p) return false;
+  return aligned16(p);
+}
+
 // SM count used for the device-independent parts of the plan (split-K), so
 // that mk_workspace_size gives the same answer with or without a GPU.
 constexpr int PLAN_SMS = 148;
@@ -86,6 +94,7 @@ struct Plan {
   int n_mblk, n_nblk, n_kblk, n_tiles;
   int split_k, kps, P;
   int group_m;
+  int chain;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
 };
 
@@ -116,14 +125,17 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   pl.flags_off = WS_HDR_BYTES;
   pl.n_flags = 0;
   pl.staging_bytes = 0;
+  pl.chain = 0;
   if (op == OP_AG) {
-    pl.n_flags = static_cast<size_t>(pl.n_mblk);
+    pl.n_flags = static_cast<size_t>(pl.n_mblk) * COPY_SUB_MAX;
   } else {
     int sk = (cfg && cfg->split_k > 0) ? cfg->split_k : 0;
     if (sk == 0) {
       sk = 1;
       const long long items = static_cast<long long>(pl.n_tiles) * R;
-      if (op == OP_AR && items > 0 && items < 2LL * PLAN_SMS)
+      // Split K only for the staged reduce-role path of a small-M AllReduce;
+      // the running-sum reduction is fastest without it.
+      if (op == OP_AR && cfg && cfg->n_reduce_ctas > 0 && items > 0 && items < 2LL * PLAN_SMS)
         sk = static_cast<int>(ceil_div_ll(2LL * PLAN_SMS, items));
     }
     sk = std::max(1, std::min(sk, MAX_PARTIALS / R));
@@ -133,9 +145,16 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
     pl.split_k = sk;
     pl.P = R * sk;
     if (pl.P > MAX_PARTIALS) return false;
+    // Fused default: the partials of a tile are summed in rank order by the
+    // compute epilogues (one running-sum tile per output tile).  With
+    // n_reduce_ctas > 0, or in the unfused baseline, every partial is staged
+    // in its own slot and reduce-role CTAs sum them.
+    pl.chain = (mode == MK_MODE_FUSED && !(cfg && cfg->n_reduce_ctas > 0)) ? 1 : 0;
     if (mode != MK_MODE_GEMM_ONLY) {
       pl.n_flags = static_cast<size_t>(pl.n_tiles) * pl.P;
-      pl.staging_bytes = static_cast<size_t>(pl.n_tiles) * pl.P * TILE_F32 * sizeof(float);
+      const size_t slots = pl.chain ? static_cast<size_t>(pl.n_tiles)
+                                    : static_cast<size_t>(pl.n_tiles) * pl.P;
+      pl.staging_bytes = slots * TILE_F32 * sizeof(float);
     }
   }
   size_t off = pl.flags_off + pl.n_flags * sizeof(uint32_t);
@@ -163,6 +182,8 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.split_k = pl.split_k;
   p.kps = pl.kps;
   p.P = pl.P;
+  p.chain = pl.chain;
+  p.copy_sub = 1;
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
   p.flags = reinterpret_cast<uint32_t*>(ws + pl.flags_off);
@@ -243,12 +264,14 @@ mk_status mk_get_device_status(const void* workspace, mk_stream_t stream, long l
 mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathered, void* c,
                      mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n, long long k,
                      void* workspace, size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
-  if (!a_shards || !b || !a_gathered || !c || !workspace) return MK_ERR_INVALID;
+  if (!a_shards || !workspace) return MK_ERR_INVALID;
   if (c_dtype != MK_BF16 && c_dtype != MK_F32) return MK_ERR_INVALID;
   if (R < 1 || R > MK_MAX_RANKS || local_rank < 0 || local_rank >= R) return MK_ERR_INVALID;
+  if (m_r < 0 || n < 0 || k < 0) return MK_ERR_INVALID;
   for (int r = 0; r < R; ++r)
-    if (!a_shards[r] || !aligned16(a_shards[r])) return MK_ERR_INVALID;
-  if (!aligned16(b) || !aligned16(a_gathered) || !aligned16(c) || !aligned16(workspace))
+    if (!buf_ok(a_shards[r], m_r * k)) return MK_ERR_INVALID;
+  if (!buf_ok(b, k * n) || !buf_ok(a_gathered, R * m_r * k) || !buf_ok(c, R * m_r * n) ||
+      !aligned16(workspace))
     return MK_ERR_INVALID;
   Plan pl;
   if (!plan_gemm(OP_AG, R, m_r, n, k, cfg, pl)) return MK_ERR_INVALID;
@@ -274,6 +297,13 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
   const int n_items = (k > 0 && n > 0) ? pl.n_mblk * pl.n_nblk : 0;
   p.n_items = n_items;
 
+  // Sub-chunks per 128-row chunk: as many as copy CTAs (a power of two,
+  // <= 16), so that all copy CTAs move the same chunk at the same time.
+  auto sub_for = [](int ncopy) {
+    int S = 1;
+    while (S * 2 <= std::min(ncopy, COPY_SUB_MAX)) S *= 2;
+    return S;
+  };
   if (k == 0 || n == 0) {
     // Nothing to multiply: C is all zeros (k == 0) or empty (n == 0); the
     // gathered A is still produced.
@@ -282,7 +312,8 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
       if (st != MK_OK) return st;
     }
     if (k == 0) return MK_OK;
-    return launch(p, std::min(sms, std::max(1, p.n_copy_chunks)), 0, 0, s);
+    p.copy_sub = COPY_SUB_MAX;
+    return launch(p, std::min(sms, std::max(1, p.n_copy_chunks * COPY_SUB_MAX)), 0, 0, s);
   }
   if (!make_map_2d(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes, BK, BM) ||
       !make_map_2d(&p.tmA[1], a_gathered, k, pl.M, row_bytes, BK, BM) ||
@@ -295,16 +326,18 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
   if (pl.mode == MK_MODE_UNFUSED) {
     const uint32_t e = p.epoch;
     mk_status st = MK_OK;
-    if (p.n_copy_chunks > 0) st = launch(p, std::min(sms, p.n_copy_chunks), 0, 0, s);
+    p.copy_sub = COPY_SUB_MAX;
+    if (p.n_copy_chunks > 0) st = launch(p, std::min(sms, p.n_copy_chunks * COPY_SUB_MAX), 0, 0, s);
     if (st != MK_OK) return st;
     p.epoch = e;
     p.mode = MK_MODE_GEMM_ONLY;
     return launch(p, 0, std::min(sms, n_items), 0, s);
   }
-  int n_copy = (cfg && cfg->n_copy_ctas > 0) ? cfg->n_copy_ctas : 8;
-  n_copy = std::min(n_copy, p.n_copy_chunks);
+  int n_copy = (cfg && cfg->n_copy_ctas > 0) ? cfg->n_copy_ctas : 12;
+  n_copy = std::min(n_copy, p.n_copy_chunks * COPY_SUB_MAX);
   n_copy = std::min(n_copy, sms - 1);
   n_copy = std::max(n_copy, 0);
+  p.copy_sub = sub_for(std::max(1, n_copy));
   const int n_compute = std::min(sms - n_copy, n_items);
   return launch(p, n_copy, n_compute, 0, s);
 }
@@ -316,9 +349,11 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   if (!a || !b || !outs || !workspace) return MK_ERR_INVALID;
   if (c_dtype != MK_BF16 && c_dtype != MK_F32) return MK_ERR_INVALID;
   if (R < 1 || R > MK_MAX_RANKS) return MK_ERR_INVALID;
+  if (m < 0 || n < 0 || k < 0) return MK_ERR_INVALID;
+  const long long out_rows = (op == OP_RS) ? m / R : m;
   for (int r = 0; r < R; ++r) {
-    if (!a[r] || !b[r] || !outs[r]) return MK_ERR_INVALID;
-    if (!aligned16(a[r]) || !aligned16(b[r]) || !aligned16(outs[r])) return MK_ERR_INVALID;
+    if (!buf_ok(a[r], m * k) || !buf_ok(b[r], k * n) || !buf_ok(outs[r], out_rows * n))
+      return MK_ERR_INVALID;
   }
   if (!aligned16(workspace)) return MK_ERR_INVALID;
   Plan pl;
@@ -356,7 +391,12 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
     p.epoch = e;
     return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
   }
-  int n_red = (cfg && cfg->n_reduce_ctas > 0) ? cfg->n_reduce_ctas : 8;
+  if (pl.chain) {
+    const int n_compute = std::min(sms, p.n_items);
+    p.group_tiles = std::max(1, std::min(n_compute, pl.n_tiles));
+    return launch(p, 0, n_compute, 0, s);
+  }
+  int n_red = cfg->n_reduce_ctas;
   n_red = std::min(n_red, pl.n_tiles);
   n_red = std::min(n_red, sms - 1);
   n_red = std::max(n_red, 1);

@@ -163,8 +163,20 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
       raster(p, i, it.mb, it.nb);
       it.nseg = p.R;
     } else {
-      const int q = i / p.P;
-      const int part = i - q * p.P;
+      int q, part;
+      if (p.chain) {
+        // Groups of group_tiles tiles; inside a group all tiles take part 0,
+        // then part 1, ... so a tile's running sum moves on one part per round.
+        const int G = p.group_tiles;
+        const int g = i / (G * p.P);
+        const int Gg = min(G, p.n_tiles - g * G);
+        const int iin = i - g * G * p.P;
+        part = iin / Gg;
+        q = g * G + (iin - part * Gg);
+      } else {
+        q = i / p.P;
+        part = i - q * p.P;
+      }
       raster(p, q, it.mb, it.nb);
       const int r = part / p.split_k, ks = part - r * p.split_k;
       it.amap = r;
@@ -220,7 +232,8 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
     Item it;
     decode(p, i, it);
     if (it.wait_chunk >= 0) {
-      if (!wait_flag(p, p.flags + it.wait_chunk, WHERE_PRODUCER, i)) goto done;
+      for (int j = 0; j < p.copy_sub; ++j)
+        if (!wait_flag(p, p.flags + it.wait_chunk * COPY_SUB_MAX + j, WHERE_PRODUCER, i)) goto done;
       fence_proxy_async_global();
     }
     for (int seg = 0; seg < it.nseg; ++seg) {
@@ -349,7 +362,65 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     const bool row_ok = trow >= it.row_lo && trow < it.row_hi;
     const int grow = it.out_row0 + trow;
     const int n0 = it.nb * BN;
-    if (it.slot >= 0) {
+    if (it.slot >= 0 && p.chain) {
+      // Running sum of this output tile, forwarded in rank order:
+      //   sum_0 = P_0,  sum_j = sum_{j-1} + P_j,  output = round(sum_{P-1}).
+      const int tile = it.slot / p.P, part = it.slot - tile * p.P;
+      float* acc = p.staging + static_cast<size_t>(tile) * TILE_F32;
+      if (part > 0) {
+        // The running sum through part-1 must have been stored (acquire by
+        // lane 0; __syncwarp orders the other lanes' loads after it).
+        int ok = 1;
+        if (lane == 0) ok = wait_flag(p, p.flags + it.slot - 1, WHERE_EPILOGUE, i) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return;
+      }
+      const bool last = (part == p.P - 1);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        if (part > 0) {
+          float4 v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            v[q] = ld_global_cg_f4(acc + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            r[4 * q + 0] = __float_as_uint(v[q].x + __uint_as_float(r[4 * q + 0]));
+            r[4 * q + 1] = __float_as_uint(v[q].y + __uint_as_float(r[4 * q + 1]));
+            r[4 * q + 2] = __float_as_uint(v[q].z + __uint_as_float(r[4 * q + 2]));
+            r[4 * q + 3] = __float_as_uint(v[q].w + __uint_as_float(r[4 * q + 3]));
+          }
+        } else {
+          tc_wait_ld();
+        }
+        if (!last) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float* d = acc + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4;
+            st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+          }
+        } else {
+          const int col = n0 + 32 * c;
+          const int nvalid = max(0, min(32, p.N - col));
+          if (row_ok && nvalid > 0) {
+            if (p.op == OP_RS) {
+              const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
+              uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
+              store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
+            } else {
+              for (int o = 0; o < p.R; ++o) {
+                uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
+                store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid,
+                                p.out_f32);
+              }
+            }
+          }
+        }
+      }
+    } else if (it.slot >= 0) {
       // Partial tile -> staging slot.  Layout: float4 (row, column group cg)
       // at index cg*BM + row, so a warp's 32 rows form 512 contiguous bytes.
       float* slot = p.staging + static_cast<size_t>(it.slot) * TILE_F32;
@@ -465,34 +536,70 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
 }
 
 // ------------------------------------------------------------------ copy-in role (AG)
-constexpr int COPY_NBUF = 6;
-constexpr uint32_t COPY_BUF = 32768;
+#ifndef MK_COPY_NBUF
+#define MK_COPY_NBUF 3
+#endif
+#ifndef MK_COPY_BUF
+#define MK_COPY_BUF 65536
+#endif
+#ifndef MK_COPY_WAITN
+#define MK_COPY_WAITN 4
+#endif
+#ifndef MK_COPY_PFD
+#define MK_COPY_PFD 0
+#endif
+// Copy-in pipeline: NBUF smem buffers of BUF bytes (bulk loads run NBUF-1
+// pieces ahead, bulk stores drain them); a sub-chunk's flag is released once
+// its stores are WAITN bulk groups old; pieces PFD ahead are prefetched to L2.
+constexpr int COPY_NBUF = MK_COPY_NBUF;
+constexpr uint32_t COPY_BUF = MK_COPY_BUF;
+constexpr int COPY_WAITN = MK_COPY_WAITN;
+constexpr int COPY_PFD = MK_COPY_PFD;
+constexpr int COPY_PEND = 64;
+static_assert(COPY_NBUF * COPY_BUF <= RING_BYTES, "copy buffers exceed the smem ring");
+static_assert(104 + 8 * COPY_NBUF <= BAR_BYTES, "copy barriers exceed the barrier block");
+static_assert(COPY_WAITN + 2 < COPY_PEND, "pending-release queue too small");
 
 struct CopyIter {
-  int c;          // position in this CTA's chunk list (global copy-order index)
-  int mb;         // current chunk
-  long long row;  // next gathered row to copy in this chunk
-  long long off;  // byte offset inside the current contiguous run
+  long long piece;   // index into the work list: (chunk position, sub-chunk)
+  long long lo, hi;  // gathered rows of the current sub-chunk
+  long long row;     // next row to copy
+  long long off;     // byte offset inside the current contiguous run
+  int flag;          // ready flag of the current sub-chunk
 };
 
 struct Piece {
   const uint8_t* src;
   uint8_t* dst;
   uint32_t bytes;
-  int chunk;
-  bool last;  // last piece of its chunk
+  int flag;
+  bool last;  // last piece of its sub-chunk
 };
 
-// The contiguous run of the current chunk that starts at gathered row `row`:
-// rows of one shard, skipping the local shard's rows when it is not copied.
-__device__ __forceinline__ bool copy_run(const FusedParams& p, int mb, long long& row, long long& hi,
-                                         int& s) {
-  const long long end = min(static_cast<long long>(mb + 1) * BM, static_cast<long long>(p.M));
-  while (row < end) {
+// Rows [lo, hi) of the gathered A covered by work-list entry `piece`
+// (sub-chunk `sub` of the chunk at copy-order position c).
+__device__ __forceinline__ void sub_rows(const FusedParams& p, long long piece, CopyIter& st) {
+  const int S = p.copy_sub;
+  const int c = static_cast<int>(piece / S), sub = static_cast<int>(piece - static_cast<long long>(c) * S);
+  const int mb = ag_copy_mb(p, c);
+  const int rs = BM / S;
+  st.lo = static_cast<long long>(mb) * BM + static_cast<long long>(sub) * rs;
+  st.hi = min(st.lo + rs, min(static_cast<long long>(mb + 1) * BM, static_cast<long long>(p.M)));
+  if (st.hi < st.lo) st.hi = st.lo;
+  st.flag = mb * COPY_SUB_MAX + sub;
+  st.row = st.lo;
+  st.off = 0;
+}
+
+// The contiguous run at or after `row` below `hi`: rows of one shard,
+// skipping the local shard's rows when it is not copied.
+__device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, long long hi,
+                                         long long& run_hi, int& s) {
+  while (row < hi) {
     s = static_cast<int>(row / p.m_r);
-    hi = min(end, static_cast<long long>(s + 1) * p.m_r);
+    run_hi = min(hi, static_cast<long long>(s + 1) * p.m_r);
     if (s == p.local && !p.copy_local) {
-      row = hi;
+      row = run_hi;
       continue;
     }
     return true;
@@ -500,73 +607,68 @@ __device__ __forceinline__ bool copy_run(const FusedParams& p, int mb, long long
   return false;
 }
 
-__device__ bool copy_next(const FusedParams& p, int cid, CopyIter& st, Piece& pc) {
+__device__ bool copy_next(const FusedParams& p, CopyIter& st, Piece& pc) {
   const size_t rb = static_cast<size_t>(p.K) * 2;
-  while (st.c < p.n_copy_chunks) {
-    long long hi;
-    int s;
-    long long row = st.row;
-    if (copy_run(p, st.mb, row, hi, s)) {
-      const long long run_bytes = (hi - row) * static_cast<long long>(rb);
-      const long long left = run_bytes - st.off;
-      const uint32_t n = static_cast<uint32_t>(min(left, static_cast<long long>(COPY_BUF)));
-      pc.src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb + st.off;
-      pc.dst = p.gathered + static_cast<size_t>(row) * rb + st.off;
-      pc.bytes = n;
-      pc.chunk = st.mb;
-      st.off += n;
-      st.row = row;
-      if (st.off == run_bytes) {
-        st.row = hi;
-        st.off = 0;
-      }
-      // last piece of the chunk?
-      long long r2 = st.row, h2;
-      int s2;
-      pc.last = (st.off == 0) && !copy_run(p, st.mb, r2, h2, s2);
-      if (pc.last) {
-        st.c += p.n_copy;
-        if (st.c < p.n_copy_chunks) {
-          st.mb = ag_copy_mb(p, st.c);
-          st.row = static_cast<long long>(st.mb) * BM;
-        }
-      }
-      return true;
+  const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * p.copy_sub;
+  if (st.piece >= n_pieces) return false;
+  long long run_hi;
+  int s;
+  long long row = st.row;
+  if (copy_run(p, row, st.hi, run_hi, s)) {
+    const long long run_bytes = (run_hi - row) * static_cast<long long>(rb);
+    const uint32_t n = static_cast<uint32_t>(min(run_bytes - st.off, static_cast<long long>(COPY_BUF)));
+    pc.src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb + st.off;
+    pc.dst = p.gathered + static_cast<size_t>(row) * rb + st.off;
+    pc.bytes = n;
+    pc.flag = st.flag;
+    st.row = row;
+    st.off += n;
+    if (st.off == run_bytes) {
+      st.row = run_hi;
+      st.off = 0;
     }
-    // chunk with nothing to copy (only local rows): signal it right away
+    long long r2 = st.row, h2;
+    int s2;
+    pc.last = (st.off == 0) && !copy_run(p, r2, st.hi, h2, s2);
+  } else {
+    // a sub-chunk with nothing to copy (local rows only): signal it at once
     pc.src = nullptr;
     pc.dst = nullptr;
     pc.bytes = 0;
-    pc.chunk = st.mb;
+    pc.flag = st.flag;
     pc.last = true;
-    st.c += p.n_copy;
-    if (st.c < p.n_copy_chunks) {
-      st.mb = ag_copy_mb(p, st.c);
-      st.row = static_cast<long long>(st.mb) * BM;
-      st.off = 0;
-    }
-    return true;
   }
-  return false;
+  if (pc.last) {
+    st.piece += p.n_copy;
+    if (st.piece < n_pieces) sub_rows(p, st.piece, st);
+  }
+  return true;
 }
 
 __device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
+  // One thread drives the pipeline: bulk loads (global -> smem) run
+  // COPY_NBUF-1 pieces ahead; each landed piece is bulk-stored (smem ->
+  // global); a sub-chunk's flag is released once its last store is complete.
   if (threadIdx.x != 0) return;
   const uint32_t ring = smem_u32(smem);
   const uint32_t bars = smem_u32(smem + RING_BYTES) + 104u;
   for (int b = 0; b < COPY_NBUF; ++b) mbar_init(bars + 8u * b, 1);
   fence_mbar_init();
 
+  const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * p.copy_sub;
   CopyIter st;
-  st.c = cid;
-  st.off = 0;
-  if (st.c < p.n_copy_chunks) {
-    st.mb = ag_copy_mb(p, st.c);
-    st.row = static_cast<long long>(st.mb) * BM;
-  }
+  st.piece = cid;
+  if (st.piece < n_pieces) sub_rows(p, st.piece, st);
+  CopyIter pf = st;  // runs COPY_PFD pieces ahead, warming L2
+  auto prefetch_one = [&]() {
+    Piece x;
+    if (COPY_PFD > 0 && copy_next(p, pf, x) && x.bytes) bulk_prefetch_l2(x.src, x.bytes);
+  };
+  for (int j = 0; j < COPY_PFD; ++j) prefetch_one();
+
   Piece q[COPY_NBUF];  // pieces whose loads are in flight, by buffer
-  int pend_chunk[16];
-  long long pend_seq[16];
+  int pend_flag[COPY_PEND];
+  long long pend_seq[COPY_PEND];
   int n_pend = 0;
   long long n_load = 0, n_store = 0;
   bool more = true, ok = true;
@@ -575,7 +677,8 @@ __device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
 
   auto issue_load = [&](long long seq) -> bool {
     Piece pc;
-    if (!copy_next(p, cid, st, pc)) return false;
+    if (!copy_next(p, st, pc)) return false;
+    prefetch_one();
     const int b = static_cast<int>(seq % COPY_NBUF);
     q[b] = pc;
     const uint32_t bar = bars + 8u * b;
@@ -587,12 +690,12 @@ __device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
     }
     return true;
   };
-  auto release = [&](int chunk) {
+  auto release = [&](int flag) {
     if (inject && !injected) {
       injected = true;
       return;
     }
-    st_release_gpu(p.flags + chunk, p.epoch);
+    st_release_gpu(p.flags + flag, p.epoch);
   };
 
   for (; n_load < COPY_NBUF - 1 && more; ++n_load) more = issue_load(n_load);
@@ -600,36 +703,36 @@ __device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
   while (n_store < n_load) {
     const int b = static_cast<int>(n_store % COPY_NBUF);
     if (!wait_bar(p, bars + 8u * b, static_cast<uint32_t>((n_store / COPY_NBUF) & 1), WHERE_COPY,
-                  q[b].chunk)) {
+                  q[b].flag)) {
       ok = false;
       break;
     }
     if (q[b].bytes) bulk_s2g(q[b].dst, ring + static_cast<uint32_t>(b) * COPY_BUF, q[b].bytes);
     bulk_commit();
     if (q[b].last) {
-      pend_chunk[n_pend] = q[b].chunk;
+      pend_flag[n_pend] = q[b].flag;
       pend_seq[n_pend] = n_store;
       ++n_pend;
     }
     ++n_store;
-    // Release chunks whose stores are at least 8 groups old (complete).
-    bulk_wait<8>();
+    // Release sub-chunks whose stores are at least COPY_WAITN groups old (complete).
+    bulk_wait<COPY_WAITN>();
     int keep = 0;
     for (int j = 0; j < n_pend; ++j) {
-      if (pend_seq[j] <= n_store - 9) {
+      if (pend_seq[j] <= n_store - 1 - COPY_WAITN) {
         fence_proxy_async_global();
-        release(pend_chunk[j]);
+        release(pend_flag[j]);
       } else {
-        pend_chunk[keep] = pend_chunk[j];
+        pend_flag[keep] = pend_flag[j];
         pend_seq[keep] = pend_seq[j];
         ++keep;
       }
     }
     n_pend = keep;
-    if (n_pend >= 15) {  // bound the queue: wait for everything, release all
+    if (n_pend >= COPY_PEND - 1) {  // bound the queue: wait for everything, release all
       bulk_wait<0>();
       fence_proxy_async_global();
-      for (int j = 0; j < n_pend; ++j) release(pend_chunk[j]);
+      for (int j = 0; j < n_pend; ++j) release(pend_flag[j]);
       n_pend = 0;
     }
     // Refill the buffer whose store was issued one step ago.
@@ -642,7 +745,7 @@ __device__ void copy_role(const FusedParams& p, uint8_t* smem, int cid) {
   bulk_wait<0>();
   if (ok) {
     fence_proxy_async_global();
-    for (int j = 0; j < n_pend; ++j) release(pend_chunk[j]);
+    for (int j = 0; j < n_pend; ++j) release(pend_flag[j]);
   }
   // Loads that were issued but not stored (abort path) must land before exit.
   for (long long s2 = n_store; s2 < n_load; ++s2) {

@@ -6,7 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/mk.h"
+#include "mk.h"
 
 namespace mk {
 
@@ -28,6 +28,7 @@ constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int TILE_F32 = BM * BN;              // floats in one partial tile
 constexpr int MAX_PARTIALS = 16;               // partial tiles reduced per output tile
+constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chunk
 
 // Workspace header words (uint32 each).
 enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_WORDS = 64 };
@@ -65,7 +66,11 @@ struct FusedParams {
   int copy_local, ordered;
   int inject;
   int rows_per_owner;
-  int n_copy_chunks;
+  int n_copy_chunks;   // AG: 128-row chunks the copy-in role moves
+  int copy_sub;        // AG: sub-chunks per chunk (each its own ready flag), power of 2 <= 16
+  int chain;           // RS/AR: 1 = partials summed in rank order by the epilogues (running sum
+                       //        forwarded tile by tile); 0 = staged partials + reduce-role CTAs
+  int group_tiles;     // RS/AR chain: tiles per scheduling group
 };
 
 // Workspace layout for the AG / RS / AR ops.

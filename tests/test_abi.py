@@ -39,15 +39,19 @@ def test_version_and_status_strings(L):
 
 
 def test_workspace_sizes(L):
-    # RS, 8 ranks, 8192x8192 output: 2048 tiles x 8 fp32 partials of 128x256.
+    # RS, 8 ranks, 8192x8192 output, default (running sum per tile): 2048 fp32 tiles of 128x256.
     sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584)
-    assert sz >= 2048 * 8 * 128 * 256 * 4
-    assert sz < 2048 * 8 * 128 * 256 * 4 + (1 << 20)
+    assert 2048 * 128 * 256 * 4 <= sz < 2048 * 128 * 256 * 4 + (1 << 20)
+    # staged partials for reduce-role CTAs: 8 fp32 partial tiles per output tile.
+    sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(n_reduce_ctas=8))
+    assert 2048 * 8 * 128 * 256 * 4 <= sz < 2048 * 8 * 128 * 256 * 4 + (1 << 20)
+    sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(mode=mk.MODE_UNFUSED))
+    assert 2048 * 8 * 128 * 256 * 4 <= sz
     # GEMM-only mode needs no staging.
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584,
                              mk.Config(mode=mk.MODE_GEMM_ONLY)) < (1 << 20)
-    # AG: one flag per 128-row chunk of the gathered A.
-    assert 256 < mk.workspace_size(mk.OP_AG_GEMM, 8, 1024, 3584, 8192) < 4096
+    # AG: up to 16 sub-chunk flags per 128-row chunk of the gathered A (64 chunks).
+    assert 256 + 64 * 16 * 4 <= mk.workspace_size(mk.OP_AG_GEMM, 8, 1024, 3584, 8192) < 8192
     # bad shapes -> 0
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8190, 64, 64) == 0     # m % R
     assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 260, 64) == 0     # n % 8
