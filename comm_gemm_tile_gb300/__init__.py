@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = i
             f.argtypes = [P(vp), P(vp), P(vp), i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
+        L.mk_ag_gemm_noalloc.restype = i
+        L.mk_ag_gemm_noalloc.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, P(_Cfg), vp]
         L.mk_moe_dispatch_gemm.restype = i
         L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
                                            P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]

@@ -169,6 +169,39 @@ mk_status mk_moe_dispatch_gemm(const void *const *x, const float *const *logits,
                                void *const *recv_x, void *const *y, void *workspace,
                                size_t ws_bytes, const mk_config *cfg, mk_stream_t stream);
 
+/* Size of the library's own scratch array used by mk_ag_gemm_noalloc (bytes). */
+#define MK_NOALLOC_SCRATCH_BYTES 65536
+
+/* AllGather + GEMM for callers that cannot allocate device memory.
+ * The paper has no counterpart for this entry point.
+ * Same operation, arguments and results as mk_ag_gemm, but without a
+ * workspace: the small scratch the kernel needs (ticket counter, status, one
+ * ready flag per copied sub-chunk) lives in a fixed array of
+ * MK_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits.  It is meant for code that must not
+ * call cudaMalloc: a plug-in running inside a host application that owns all
+ * GPU memory through its own pool and does not let extensions allocate, or a
+ * latency-critical path that may not allocate after start-up (an allocation
+ * can synchronise the device and its size is not known in advance).
+ *   - Limit: shapes whose scratch would exceed the array (about 1020 chunks of
+ *     128 gathered rows, i.e. R*m_r up to 130560 rows) are rejected with
+ *     MK_ERR_INVALID before anything is enqueued.
+ *   - The first call on a device looks up the array's device address and
+ *     zero-fills it on `stream`; make that first call before any stream
+ *     capture on that device.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents; each call clears the part that must start at zero.  Two calls
+ *     whose GPU work can overlap (different streams without ordering, or
+ *     different host threads) race on the array: order them on one stream.
+ *   - device_status: optional (may be NULL) caller-owned device int, 4-byte
+ *     aligned, that receives this call's device status (MK_OK or
+ *     MK_ERR_TIMEOUT) once the call's work on `stream` has finished.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a_gathered, void *c,
+                             mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n,
+                             long long k, int *device_status, const mk_config *cfg,
+                             mk_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of a
  * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the
  * stream itself reports an error).  `detail` (may be NULL) receives a code
