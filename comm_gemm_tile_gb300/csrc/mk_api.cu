@@ -333,7 +333,17 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     p.mode = MK_MODE_GEMM_ONLY;
     return launch(p, 0, std::min(sms, n_items), 0, s);
   }
-  int n_copy = (cfg && cfg->n_copy_ctas > 0) ? cfg->n_copy_ctas : 12;
+  if (!(cfg && cfg->n_copy_ctas > 0)) {
+    // Default: the copy-in is done by two spare warps of every compute CTA,
+    // in pieces of about 16 KiB (rows of the gathered A), so every SM computes.
+    int pr = 1;
+    while (pr < BM && static_cast<long long>(pr) * row_bytes < 16384) pr *= 2;
+    p.copy_warps = 1;
+    p.copy_rows = pr;
+    const int n_compute = std::min(sms, n_items);
+    return launch(p, 0, n_compute, 0, s);
+  }
+  int n_copy = cfg->n_copy_ctas;
   n_copy = std::min(n_copy, p.n_copy_chunks * COPY_SUB_MAX);
   n_copy = std::min(n_copy, sms - 1);
   n_copy = std::max(n_copy, 0);

@@ -80,6 +80,37 @@ __device__ __noinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, 
   return true;
 }
 
+// AG copy warps: chunk mb is ready when its piece counter (the first word of
+// the chunk's flag slot) reaches pieces(mb).  The CTA with ticket 0 zeroes
+// the counters at kernel start and then releases hdr[HDR_READY] = epoch;
+// nobody touches a counter before seeing that word.
+__device__ __forceinline__ uint32_t* chunk_counter(const FusedParams& p, int mb) {
+  return p.flags + static_cast<size_t>(mb) * COPY_SUB_MAX;
+}
+__device__ __forceinline__ int chunk_pieces(const FusedParams& p, int mb) {
+  const int rows = min(BM, p.M - mb * BM);
+  return (rows + p.copy_rows - 1) / p.copy_rows;
+}
+// Bounded wait for a chunk counter (single thread).
+__device__ __noinline__ bool wait_chunk_count(const FusedParams& p, int mb, int item) {
+  const uint32_t* c = chunk_counter(p, mb);
+  const uint32_t want = static_cast<uint32_t>(chunk_pieces(p, mb));
+  if (ld_acquire_gpu(c) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (ld_acquire_gpu(c) != want) {
+    if ((++it & 7u) == 0) {
+      if (aborted(p)) return false;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+        raise_error(p, MK_ERR_TIMEOUT, WHERE_PRODUCER, item);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ work decoding
 struct Item {
   int mb, nb;       // tile coordinates in the op's output space
@@ -228,12 +259,21 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;
   const int n_items = n_items_for(p);
+  bool counters_ready = false;
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it);
+    if (it.wait_chunk >= 0 && p.copy_warps && !counters_ready) {
+      if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_PRODUCER, i)) goto done;
+      counters_ready = true;
+    }
     if (it.wait_chunk >= 0) {
-      for (int j = 0; j < p.copy_sub; ++j)
-        if (!wait_flag(p, p.flags + it.wait_chunk * COPY_SUB_MAX + j, WHERE_PRODUCER, i)) goto done;
+      if (p.copy_warps) {
+        if (!wait_chunk_count(p, it.wait_chunk, i)) goto done;
+      } else {
+        for (int j = 0; j < p.copy_sub; ++j)
+          if (!wait_flag(p, p.flags + it.wait_chunk * COPY_SUB_MAX + j, WHERE_PRODUCER, i)) goto done;
+      }
       fence_proxy_async_global();
     }
     for (int seg = 0; seg < it.nseg; ++seg) {
@@ -483,6 +523,84 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   }
 }
 
+// The contiguous run at or after `row` below `hi`: rows of one shard,
+// skipping the local shard's rows when it is not copied.
+__device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, long long hi,
+                                         long long& run_hi, int& s) {
+  while (row < hi) {
+    s = static_cast<int>(row / p.m_r);
+    run_hi = min(hi, static_cast<long long>(s + 1) * p.m_r);
+    if (s == p.local && !p.copy_local) {
+      row = run_hi;
+      continue;
+    }
+    return true;
+  }
+  return false;
+}
+
+// AG copy-in by warps 6-7 of every compute CTA.  The work list is (chunk in
+// copy order, piece of copy_rows rows); worker w = 2*cid + (warp - 6) takes
+// pieces w, w + 2*n_compute, ... so all workers move neighbouring pieces of
+// the same few chunks at a time.  Each lane streams 16-byte vectors, 8 loads
+// in flight; after a piece every lane fences and lane 0 bumps the chunk's
+// counter.  Copy warps never wait on anything, so they always progress.
+constexpr int CW_UNROLL = 8;
+
+__device__ void copy_warps_role(const FusedParams& p, int cid) {
+  const int lane = threadIdx.x & 31;
+  const int worker = cid * 2 + ((threadIdx.x >> 5) - 6);
+  const int n_workers = p.n_compute * 2;
+  const int pr = p.copy_rows;
+  const int J = BM / pr;
+  const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * J;
+  const size_t rb = static_cast<size_t>(p.K) * 2;
+  bool skip_first = (p.inject == 1 && worker == 0);
+  {
+    int ok = 1;
+    if (lane == 0) ok = wait_flag(p, &p.hdr[HDR_READY], WHERE_COPY, worker) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  }
+  for (long long pc = worker; pc < n_pieces; pc += n_workers) {
+    const int c = static_cast<int>(pc / J), j = static_cast<int>(pc - static_cast<long long>(c) * J);
+    const int mb = ag_copy_mb(p, c);
+    if (j >= chunk_pieces(p, mb)) continue;  // past the end of a short last chunk
+    int stop = 0;
+    if (lane == 0) stop = aborted(p) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) return;
+    long long row = static_cast<long long>(mb) * BM + static_cast<long long>(j) * pr;
+    const long long hi = min(row + pr, min(static_cast<long long>(mb + 1) * BM, static_cast<long long>(p.M)));
+    long long run_hi;
+    int s;
+    while (copy_run(p, row, hi, run_hi, s)) {
+      const uint8_t* src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb;
+      uint8_t* dst = p.gathered + static_cast<size_t>(row) * rb;
+      const size_t n16 = static_cast<size_t>(run_hi - row) * rb / 16;
+      for (size_t i0 = lane; i0 < n16; i0 += 32 * CW_UNROLL) {
+        uint4 v[CW_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CW_UNROLL; ++u) {
+          const size_t idx = i0 + static_cast<size_t>(u) * 32;
+          if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < CW_UNROLL; ++u) {
+          const size_t idx = i0 + static_cast<size_t>(u) * 32;
+          if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+        }
+      }
+      row = run_hi;
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      if (skip_first) skip_first = false;
+      else atomicAdd(chunk_counter(p, mb), 1u);   // after this warp's fences: a release
+    }
+    __syncwarp();
+  }
+}
+
 __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   ComputeSmem S;
@@ -525,6 +643,9 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     epilogue(p, S, tmem_base, cid);
+    __syncwarp();
+  } else if (p.copy_warps) {
+    copy_warps_role(p, cid);
     __syncwarp();
   }
   tc_fence_before();
@@ -589,22 +710,6 @@ __device__ __forceinline__ void sub_rows(const FusedParams& p, long long piece, 
   st.flag = mb * COPY_SUB_MAX + sub;
   st.row = st.lo;
   st.off = 0;
-}
-
-// The contiguous run at or after `row` below `hi`: rows of one shard,
-// skipping the local shard's rows when it is not copied.
-__device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, long long hi,
-                                         long long& run_hi, int& s) {
-  while (row < hi) {
-    s = static_cast<int>(row / p.m_r);
-    run_hi = min(hi, static_cast<long long>(s + 1) * p.m_r);
-    if (s == p.local && !p.copy_local) {
-      row = run_hi;
-      continue;
-    }
-    return true;
-  }
-  return false;
 }
 
 __device__ bool copy_next(const FusedParams& p, CopyIter& st, Piece& pc) {
@@ -902,6 +1007,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
   }
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
+  if (t == 0 && p.op == OP_AG && p.copy_warps) {
+    // Zero this call's chunk counters (the workspace may hold anything from
+    // earlier calls of any op), then publish them.
+    for (int mb = threadIdx.x; mb < p.n_mblk; mb += NTHREADS) *chunk_counter(p, mb) = 0u;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release_gpu(&p.hdr[HDR_READY], p.epoch);
+  }
   if (t < p.n_copy) {
     copy_role(p, smem, t);
   } else if (t < p.n_copy + p.n_compute) {

@@ -31,7 +31,7 @@ constexpr int MAX_PARTIALS = 16;               // partial tiles reduced per outp
 constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chunk
 
 // Workspace header words (uint32 each).
-enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_WORDS = 64 };
+enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_READY = 4, HDR_WORDS = 64 };
 constexpr size_t WS_HDR_BYTES = 256;
 
 enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3 };
@@ -71,6 +71,10 @@ struct FusedParams {
   int chain;           // RS/AR: 1 = partials summed in rank order by the epilogues (running sum
                        //        forwarded tile by tile); 0 = staged partials + reduce-role CTAs
   int group_tiles;     // RS/AR chain: tiles per scheduling group
+  int copy_warps;      // AG: 1 = copy-in done by warps 6-7 of every compute CTA, one
+                       //     piece counter per chunk (zeroed at kernel start by the CTA
+                       //     with ticket 0); 0 = copy-role CTAs with per-sub-chunk flags
+  int copy_rows;       // AG copy warps: gathered rows per piece (power of 2 dividing 128)
 };
 
 // Workspace layout for the AG / RS / AR ops.

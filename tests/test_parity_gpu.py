@@ -316,3 +316,28 @@ def test_missing_partial_flag_times_out(n_red):
     assert st == mk.MK_OK
     exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
     np.testing.assert_array_equal(gpu_bits(torch.cat(blocks, 0)), oracle_bits(exact, "bf16"))
+
+
+def test_ops_share_one_workspace():
+    # RS leaves epoch-tagged flags where AG keeps its chunk counters; AG must not care.
+    ws = mk.Workspace()
+    w = I.GemmWorkload("t", "rs", R=2, m=256, n=256, k=256, out="bf16", a_seed=21, b_seed=22,
+                       integer=True)
+    a, b = I.gemm_inputs(w)
+    mk.gemm_rs(dev(a), dev(b), workspace=ws)
+    wa = I.GemmWorkload("t", "ag", R=4, m=128, n=256, k=256, out="bf16", a_seed=23, b_seed=24,
+                        integer=True)
+    aa, bb = I.gemm_inputs(wa)
+    for cfg in (None, mk.Config(n_copy_ctas=4), None):
+        g, c = mk.ag_gemm(dev(aa), bb[0].cuda(), local_rank=1, cfg=cfg, workspace=ws)
+        st, detail = mk.device_status(ws)
+        assert st == mk.MK_OK, (mk.status_string(st), detail)
+        gathered, _ = O.ag_gemm([I.bits(x) for x in aa], I.bits(bb[0]))
+        np.testing.assert_array_equal(I.bits(g), gathered)
+        exact = O.bf16_to_f64(gathered) @ O.bf16_to_f64(I.bits(bb[0]))
+        np.testing.assert_array_equal(gpu_bits(c), oracle_bits(exact, "bf16"))
+    blocks = mk.gemm_rs(dev(a), dev(b), workspace=ws)
+    st, _ = mk.device_status(ws)
+    assert st == mk.MK_OK
+    exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
+    np.testing.assert_array_equal(gpu_bits(torch.cat(blocks, 0)), oracle_bits(exact, "bf16"))
