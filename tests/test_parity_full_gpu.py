@@ -1,0 +1,81 @@
+"""Full-size parity (GPU): the AllGather+GEMM, GEMM+ReduceScatter and
+GEMM+AllReduce workloads at their real sizes, run in the default launch
+configuration that bench.py times, against the CPU oracle on a seeded row
+sample (two rows per 128-row tile plus the first and last row, all columns).
+The gathered A is compared in full.  Each workload's integer-valued twin
+(values in {-2..2}, exact fp32 sums) must match bit for bit on the sample.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import comm_gemm_tile_gb300 as mk
+from comm_gemm_tile_gb300 import inputs as I
+from parity_util import TOL, absmax, gpu_bits, gpu_values, norm_err, oracle_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from comm_gemm_tile_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def _ok(ws):
+    st, detail = mk.device_status(ws)
+    assert st == mk.MK_OK, (mk.status_string(st), detail)
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_ag_full_size(integer):
+    w = I.AG_R8_TP8_UP.integer_twin() if integer else I.AG_R8_TP8_UP
+    a, b = I.gemm_inputs(w)
+    ws = mk.Workspace()
+    g, c = mk.ag_gemm([x.cuda() for x in a], b[0].cuda(), local_rank=w.local_rank, workspace=ws)
+    _ok(ws)
+    a_bits = [I.bits(x) for x in a]
+    assert np.array_equal(I.bits(g), O.allgather_rows(a_bits))
+    rows = I.sample_rows(w.R * w.m, seed=7)
+    exact = O.bf16_to_f64(O.allgather_rows(a_bits)[rows]) @ O.bf16_to_f64(I.bits(b[0]))
+    got = c[torch.from_numpy(rows).cuda()]
+    if integer:
+        np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
+    else:
+        assert norm_err(gpu_values(got), exact, w.k, absmax(a), absmax(b)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_rs_full_size(integer):
+    w = I.RS_R8_TP8_DOWN.integer_twin() if integer else I.RS_R8_TP8_DOWN
+    a, b = I.gemm_inputs(w)
+    ws = mk.Workspace()
+    blocks = mk.gemm_rs([x.cuda() for x in a], [x.cuda() for x in b], workspace=ws)
+    _ok(ws)
+    rows = I.sample_rows(w.m, seed=8)
+    exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b], rows=rows)
+    h = w.m // w.R
+    got = torch.stack([blocks[r // h][r % h] for r in rows.tolist()], 0)
+    if integer:
+        np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
+    else:
+        assert norm_err(gpu_values(got), exact, w.R * w.k, absmax(a), absmax(b)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_ar_full_size(integer):
+    w = I.AR_R8_DECODE.integer_twin() if integer else I.AR_R8_DECODE
+    a, b = I.gemm_inputs(w)
+    ws = mk.Workspace()
+    reps = mk.gemm_ar([x.cuda() for x in a], [x.cuda() for x in b], workspace=ws)
+    _ok(ws)
+    exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])   # all 128 rows
+    r0 = gpu_bits(reps[0])
+    for r in reps[1:]:
+        np.testing.assert_array_equal(gpu_bits(r), r0)
+    if integer:
+        np.testing.assert_array_equal(r0, oracle_bits(exact, "bf16"))
+    else:
+        assert norm_err(gpu_values(reps[0]), exact, w.R * w.k, absmax(a), absmax(b)) <= TOL["bf16"]
