@@ -235,6 +235,48 @@ def gemm_ar(a, b, *, out_dtype=torch.bfloat16, c_replicas=None, cfg: Config | No
                   stream, "mk_gemm_ar")
 
 
+def moe_workspace_size(R, E_loc, topk, T, H, N, cap_rows, cfg: Config | None = None) -> int:
+    return int(lib().mk_moe_workspace_size(R, E_loc, topk, T, H, N, cap_rows, _cfgp(cfg)))
+
+
+def moe_dispatch_gemm(x, logits, w, *, E_loc: int, topk: int = 2, cap_rows: int | None = None,
+                      out=None, cfg: Config | None = None, workspace: Workspace | None = None,
+                      stream=None):
+    """MoE dispatch + grouped GEMM over R virtual ranks.
+
+    x[r]: [T x H] bf16 tokens; logits[r]: [T x E] fp32 (E = R*E_loc); w[d]: [E_loc x H x N] bf16.
+    Returns a dict with topk_idx [R*T x topk], counts [R x E], recv_src[d] [cap],
+    recv_counts [R] (int32) and recv_x[d] [cap x H], y[d] [cap x N] (bf16); rows of rank d
+    past recv_counts[d] are left as they were.  `out` may pass preallocated buffers.
+    """
+    R = len(x)
+    T, H = x[0].shape
+    N = w[0].shape[2]
+    E = R * E_loc
+    cap = cap_rows if cap_rows is not None else R * T * topk
+    dev = x[0].device
+    o = dict(out or {})
+    i32 = torch.int32
+    o.setdefault("topk_idx", torch.empty((R * T, topk), dtype=i32, device=dev))
+    o.setdefault("counts", torch.empty((R, E), dtype=i32, device=dev))
+    o.setdefault("recv_counts", torch.empty((R,), dtype=i32, device=dev))
+    o.setdefault("recv_src", [torch.empty((cap,), dtype=i32, device=dev) for _ in range(R)])
+    o.setdefault("recv_x", [torch.empty((cap, H), dtype=torch.bfloat16, device=dev) for _ in range(R)])
+    o.setdefault("y", [torch.empty((cap, N), dtype=torch.bfloat16, device=dev) for _ in range(R)])
+    ws = _ws(workspace, dev)
+    nb = moe_workspace_size(R, E_loc, topk, T, H, N, cap, cfg)
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, "mk_moe_workspace_size")
+    buf = ws.get(nb)
+    st = lib().mk_moe_dispatch_gemm(_ptrs(x), _ptrs(logits), _ptrs(w), R, E_loc, topk, T, H, N, cap,
+                                    o["topk_idx"].data_ptr(), o["counts"].data_ptr(),
+                                    _ptrs(o["recv_src"]), o["recv_counts"].data_ptr(),
+                                    _ptrs(o["recv_x"]), _ptrs(o["y"]), buf.data_ptr(), buf.numel(),
+                                    _cfgp(cfg), _stream(stream, dev))
+    _check(st, "mk_moe_dispatch_gemm")
+    return o
+
+
 __all__ = ["Config", "MkError", "Workspace", "ag_gemm", "gemm_rs", "gemm_ar", "device_status",
            "workspace_size", "lib", "status_string", "MODE_FUSED", "MODE_GEMM_ONLY",
-           "MODE_UNFUSED"]
+           "MODE_UNFUSED", "moe_dispatch_gemm", "moe_workspace_size"]

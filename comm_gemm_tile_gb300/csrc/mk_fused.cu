@@ -91,10 +91,8 @@ __device__ __forceinline__ int chunk_pieces(const FusedParams& p, int mb) {
   const int rows = min(BM, p.M - mb * BM);
   return (rows + p.copy_rows - 1) / p.copy_rows;
 }
-// Bounded wait for a chunk counter (single thread).
-__device__ __noinline__ bool wait_chunk_count(const FusedParams& p, int mb, int item) {
-  const uint32_t* c = chunk_counter(p, mb);
-  const uint32_t want = static_cast<uint32_t>(chunk_pieces(p, mb));
+// Bounded wait until the counter *c reaches `want` (single thread).
+__device__ __noinline__ bool wait_count(const FusedParams& p, const uint32_t* c, uint32_t want, int item) {
   if (ld_acquire_gpu(c) == want) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
@@ -109,6 +107,9 @@ __device__ __noinline__ bool wait_chunk_count(const FusedParams& p, int mb, int 
     __nanosleep(64);
   }
   return true;
+}
+__device__ __forceinline__ bool wait_chunk_count(const FusedParams& p, int mb, int item) {
+  return wait_count(p, chunk_counter(p, mb), static_cast<uint32_t>(chunk_pieces(p, mb)), item);
 }
 
 // ------------------------------------------------------------------ work decoding
@@ -263,6 +264,17 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it);
+    if (p.op == OP_MOE) {
+      // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
+      const int d = it.amap;
+      const int rc = p.moe_recv_counts[d];
+      const int b0 = it.arow / BM, b1 = (it.arow + it.row_hi - 1) / BM;
+      for (int b = b0; b <= b1; ++b) {
+        const uint32_t want = static_cast<uint32_t>(min(BM, rc - b * BM));
+        if (!wait_count(p, p.flags + static_cast<size_t>(d) * p.moe_nblk + b, want, i)) goto done;
+      }
+      fence_proxy_async_global();
+    }
     if (it.wait_chunk >= 0 && p.copy_warps && !counters_ready) {
       if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_PRODUCER, i)) goto done;
       counters_ready = true;
@@ -545,7 +557,7 @@ __device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, l
 // the same few chunks at a time.  Each lane streams 16-byte vectors, 8 loads
 // in flight; after a piece every lane fences and lane 0 bumps the chunk's
 // counter.  Copy warps never wait on anything, so they always progress.
-constexpr int CW_UNROLL = 8;
+constexpr int CW_UNROLL = 16;
 
 __device__ void copy_warps_role(const FusedParams& p, int cid) {
   const int lane = threadIdx.x & 31;
@@ -601,6 +613,66 @@ __device__ void copy_warps_role(const FusedParams& p, int cid) {
   }
 }
 
+// MoE dispatch by warps 6-7 of every compute CTA: destination rows of all
+// ranks, rank-major, in pieces of moe_rows_per_piece rows inside one 128-row
+// block; row `row` of rank d is a bit copy of token g = recv_src[d][row] / topk
+// (rank g / T, token g % T).  After a piece every lane fences and lane 0 adds
+// the piece's rows to the block's counter (zeroed by the offsets kernel).
+__device__ void moe_copy_warps_role(const FusedParams& p, int cid) {
+  const int lane = threadIdx.x & 31;
+  const int worker = cid * 2 + ((threadIdx.x >> 5) - 6);
+  const int n_workers = p.n_compute * 2;
+  if (*reinterpret_cast<const volatile int*>(p.moe_ok) == 0) return;
+  const int pr = p.moe_rows_per_piece;
+  long long total = 0;
+  for (int d = 0; d < p.R; ++d) total += (p.moe_recv_counts[d] + pr - 1) / pr;
+  const size_t rb = static_cast<size_t>(p.K) * 2;
+  const size_t n16 = rb / 16;
+  bool skip_first = (p.inject == 1 && worker == 0);
+  for (long long q = worker; q < total; q += n_workers) {
+    int d = 0;
+    long long j = q;
+    int rc = p.moe_recv_counts[0];
+    while (j >= (rc + pr - 1) / pr) {
+      j -= (rc + pr - 1) / pr;
+      ++d;
+      rc = p.moe_recv_counts[d];
+    }
+    const int row0 = static_cast<int>(j) * pr;
+    const int rows = min(pr, rc - row0);
+    for (int rr = 0; rr < rows; ++rr) {
+      const int src = p.moe_src[d][row0 + rr];
+      const int g = src / p.moe_topk;
+      const int r = g / p.moe_T, t = g - r * p.moe_T;
+      const uint8_t* sp = p.shard[r] + static_cast<size_t>(t) * rb;
+      uint8_t* dp = p.moe_recv_x[d] + static_cast<size_t>(row0 + rr) * rb;
+      for (size_t i0 = lane; i0 < n16; i0 += 32 * CW_UNROLL) {
+        uint4 v[CW_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CW_UNROLL; ++u) {
+          const size_t idx = i0 + static_cast<size_t>(u) * 32;
+          if (idx < n16) v[u] = ld_nc_v4(sp + idx * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < CW_UNROLL; ++u) {
+          const size_t idx = i0 + static_cast<size_t>(u) * 32;
+          if (idx < n16) st_global_v4(dp + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+        }
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      if (skip_first) skip_first = false;
+      else atomicAdd(p.flags + static_cast<size_t>(d) * p.moe_nblk + row0 / BM, static_cast<uint32_t>(rows));
+    }
+    __syncwarp();
+    int stop = 0;
+    if (lane == 0) stop = aborted(p) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) return;
+  }
+}
+
 __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   ComputeSmem S;
@@ -643,6 +715,9 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     epilogue(p, S, tmem_base, cid);
+    __syncwarp();
+  } else if (p.op == OP_MOE) {
+    moe_copy_warps_role(p, cid);
     __syncwarp();
   } else if (p.copy_warps) {
     copy_warps_role(p, cid);

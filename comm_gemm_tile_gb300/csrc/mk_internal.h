@@ -75,6 +75,13 @@ struct FusedParams {
                        //     piece counter per chunk (zeroed at kernel start by the CTA
                        //     with ticket 0); 0 = copy-role CTAs with per-sub-chunk flags
   int copy_rows;       // AG copy warps: gathered rows per piece (power of 2 dividing 128)
+  // MoE dispatch (copy warps) and grouped GEMM
+  uint8_t* moe_recv_x[MK_MAX_RANKS];     // destination rows, [cap x H] per rank
+  const int* moe_src[MK_MAX_RANKS];      // recv_src per rank: g*topk + slot of each row
+  const int* moe_recv_counts;            // [R] rows received per rank
+  const int* moe_ok;                     // 1 when no rank exceeds its capacity
+  int moe_T, moe_topk, moe_nblk;         // tokens per rank, slots, 128-row blocks per rank
+  int moe_rows_per_piece;                // destination rows per copy piece (divides 128)
 };
 
 // Workspace layout for the AG / RS / AR ops.
@@ -85,6 +92,8 @@ struct WsLayout {
 inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
+constexpr int MOE_MAX_E = 256;        // experts in total (R * E_loc)
+constexpr int MOE_MAX_TOPK = 8;
 int device_sm_count();
 uint32_t next_epoch();
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,

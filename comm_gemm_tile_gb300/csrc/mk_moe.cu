@@ -1,12 +1,263 @@
-// mk_moe.cu -- MoE Dispatch + grouped GEMM (not built yet).
+// mk_moe.cu -- MoE Dispatch + grouped GEMM (mKernel write-up,
+// news.chathome.org, "五种融合内核" table, row "MoE Dispatch + GEMM": route
+// tokens to their expert ranks, all-to-all dispatch, per-expert grouped GEMM,
+// tokens processed on arrival).
+//
+// Four launches on the caller's stream:
+//   1. route + rank (one CTA per source rank): top-k experts of every token,
+//      and for every (token, slot) its position among the rank's rows routed to
+//      the same expert (a stable block-level multisplit), plus counts[r][e];
+//   2. offsets (one CTA): expert totals, per-destination segment offsets,
+//      per-(rank, expert) bases, received-row counts, the capacity check, the
+//      tile-table prefix, and zeroed per-block arrival counters;
+//   3. scatter: recv_src (the destination-ordered inverse map) and the
+//      grouped-GEMM tile table;
+//   4. the persistent fused kernel: copy warps move token rows into recv_x in
+//      destination order and count them per 128-row block; compute CTAs run
+//      the tiles of each expert as soon as their blocks are complete.
+// Row order inside a destination rank d: local expert, then global token
+// g = r*T + t; every (token, slot) pair is one row.
+#include <algorithm>
+#include <cstring>
+
 #include "mk_internal.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+namespace {
+
+constexpr int RR_THREADS = 512;
+constexpr int RR_WARPS = RR_THREADS / 32;
+enum { MISC_NTILES = 0, MISC_OK = 1, MISC_WORDS = 64 };
+
+struct MoeArgs {
+  const float* logits[MK_MAX_RANKS];
+  int* recv_src[MK_MAX_RANKS];
+  int* topk_idx;      // [R*T x topk]
+  int* counts;        // [R x E]
+  int* recv_counts;   // [R]
+  int* pos;           // [R*T*topk] position among the rank's rows of the same expert
+  int* base;          // [R x E]  rows of expert e from ranks before r
+  int* totals;        // [E]
+  int* segoff;        // [R x (E_loc+1)]
+  int* tprefix;       // [R*E_loc + 1] tile-table prefix per (rank, local expert)
+  int* tiles;         // [max_tiles x 5]
+  uint32_t* misc;     // MISC_* words
+  uint32_t* blocks;   // [R x nblk] arrival counters
+  uint32_t* hdr;      // workspace header (status)
+  int R, E_loc, E, topk, T, n_nblk, nblk;
+  long long cap;
+};
+
+__device__ __forceinline__ bool better(float v, int e, float ov, int oe) {
+  // (ov, oe) beats (v, e): larger logit, ties to the lower expert id; e < 0 = none
+  if (oe < 0) return false;
+  if (e < 0) return true;
+  return ov > v || (ov == v && oe < e);
+}
+
+__global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid_constant__ MoeArgs a) {
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, T = a.T, K = a.topk;
+  const float* lg = a.logits[r];
+  int* idx = a.topk_idx + static_cast<size_t>(r) * T * K;
+  // ---- top-k per token, one warp per token
+  for (int t = warp; t < T; t += RR_WARPS) {
+    float v[MOE_MAX_E / 32];
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_E / 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? lg[static_cast<size_t>(t) * E + e] : 0.f;
+    }
+    uint32_t taken = 0;
+    for (int j = 0; j < K; ++j) {
+      float bv = 0.f;
+      int be = -1;
+#pragma unroll
+      for (int i = 0; i < MOE_MAX_E / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && better(bv, be, v[i], e)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (better(bv, be, ov, oe)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == 0) idx[static_cast<size_t>(t) * K + j] = be;
+    }
+  }
+  __syncthreads();
+  // ---- stable multisplit of the rank's (token, slot) list by expert
+  __shared__ int wcnt[RR_WARPS * MOE_MAX_E];
+  __shared__ int run[MOE_MAX_E];
+  for (int e = tid; e < E; e += RR_THREADS) run[e] = 0;
+  const int n = T * K;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int b0 = 0; b0 < n; b0 += RR_THREADS) {
+    for (int x = tid; x < RR_WARPS * E; x += RR_THREADS) wcnt[x] = 0;
+    __syncthreads();
+    const int ai = b0 + tid;
+    const int e = (ai < n) ? idx[ai] : -1 - lane;   // distinct sentinels never group
+    const uint32_t mask = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(mask & lt);
+    if (ai < n && (__ffs(mask) - 1) == lane) wcnt[warp * E + e] = __popc(mask);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += RR_THREADS) {
+      int acc = run[ee];
+      for (int w = 0; w < RR_WARPS; ++w) {
+        const int c = wcnt[w * E + ee];
+        wcnt[w * E + ee] = acc;
+        acc += c;
+      }
+      run[ee] = acc;
+    }
+    __syncthreads();
+    if (ai < n) a.pos[static_cast<size_t>(r) * n + ai] = wcnt[warp * E + e] + rank_w;
+    __syncthreads();
+  }
+  for (int e = tid; e < E; e += RR_THREADS) a.counts[r * E + e] = run[e];
+}
+
+__global__ void __launch_bounds__(256) moe_offsets_kernel(const __grid_constant__ MoeArgs a) {
+  const int tid = threadIdx.x;
+  const int R = a.R, E = a.E, El = a.E_loc;
+  for (int e = tid; e < E; e += 256) {
+    int acc = 0;
+    for (int r = 0; r < R; ++r) {
+      a.base[r * E + e] = acc;
+      acc += a.counts[r * E + e];
+    }
+    a.totals[e] = acc;
+  }
+  __syncthreads();
+  if (tid < R) {
+    const int d = tid;
+    int acc = 0;
+    for (int l = 0; l < El; ++l) {
+      a.segoff[d * (El + 1) + l] = acc;
+      acc += a.totals[d * El + l];
+    }
+    a.segoff[d * (El + 1) + El] = acc;
+    a.recv_counts[d] = acc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ok = 1;
+    for (int d = 0; d < R; ++d)
+      if (a.recv_counts[d] > a.cap) ok = 0;
+    int acc = 0;
+    for (int k = 0; k < R * El; ++k) {
+      a.tprefix[k] = acc;
+      if (ok) acc += ((a.totals[k] + BM - 1) / BM) * a.n_nblk;
+    }
+    a.tprefix[R * El] = acc;
+    a.misc[MISC_NTILES] = static_cast<uint32_t>(acc);
+    a.misc[MISC_OK] = static_cast<uint32_t>(ok);
+    if (!ok) atomicCAS(reinterpret_cast<int*>(&a.hdr[HDR_STATUS]), 0, MK_ERR_CAPACITY);
+  }
+  for (int x = tid; x < R * a.nblk; x += 256) a.blocks[x] = 0u;
+}
+
+__global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant__ MoeArgs a) {
+  const int El = a.E_loc, E = a.E, K = a.topk, T = a.T;
+  if (a.misc[MISC_OK] == 0u) return;
+  const long long n = static_cast<long long>(a.R) * T * K;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long ai = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; ai < n; ai += stride) {
+    const int r = static_cast<int>(ai / (static_cast<long long>(T) * K));
+    const int aa = static_cast<int>(ai - static_cast<long long>(r) * T * K);
+    const int t = aa / K, j = aa - t * K;
+    const int e = a.topk_idx[ai];
+    const int d = e / El, l = e - d * El;
+    const int row = a.segoff[d * (El + 1) + l] + a.base[r * E + e] + a.pos[ai];
+    a.recv_src[d][row] = (r * T + t) * K + j;
+  }
+  const int ntiles = static_cast<int>(a.misc[MISC_NTILES]);
+  const int npairs = a.R * El;
+  for (long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; q < ntiles; q += stride) {
+    int lo = 0, hi = npairs - 1;  // last k with tprefix[k] <= q
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (a.tprefix[mid] <= q) lo = mid;
+      else hi = mid - 1;
+    }
+    const int k = lo;
+    const int d = k / El, l = k - d * El;
+    const int qq = static_cast<int>(q) - a.tprefix[k];
+    const int mi = qq / a.n_nblk, nb = qq - mi * a.n_nblk;
+    int* ent = a.tiles + 5 * q;
+    ent[0] = d;
+    ent[1] = l;
+    ent[2] = a.segoff[d * (El + 1) + l] + mi * BM;
+    ent[3] = min(BM, a.totals[k] - mi * BM);
+    ent[4] = nb;
+  }
+}
+
+struct MoeLayout {
+  size_t blocks_off, misc_off, pos_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
+  size_t total;
+  int nblk, n_nblk, max_tiles;
+};
+
+bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long N, long long cap,
+                MoeLayout& L) {
+  if (R < 1 || R > MK_MAX_RANKS || E_loc < 1) return false;
+  const long long E = static_cast<long long>(R) * E_loc;
+  if (E > MOE_MAX_E || topk < 1 || topk > MOE_MAX_TOPK || topk > E) return false;
+  if (T < 0 || H < 0 || N < 0 || cap < 0) return false;
+  if ((H % 8) || (N % 8)) return false;
+  const long long rows = static_cast<long long>(R) * T * topk;
+  if (rows >= (1LL << 31) || cap >= (1LL << 31) || H >= (1LL << 31) || N >= (1LL << 31)) return false;
+  if (cap * H >= (1LL << 40)) return false;
+  L.nblk = static_cast<int>(ceil_div_ll(cap, BM));
+  L.n_nblk = static_cast<int>(ceil_div_ll(N, BN));
+  const long long max_tiles = (rows / BM + E) * L.n_nblk;
+  if (max_tiles >= (1LL << 30)) return false;
+  L.max_tiles = static_cast<int>(max_tiles);
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  size_t off = WS_HDR_BYTES;
+  L.blocks_off = off;  off = al(off + static_cast<size_t>(R) * L.nblk * 4);
+  L.misc_off = off;    off = al(off + MISC_WORDS * 4);
+  L.pos_off = off;     off = al(off + static_cast<size_t>(rows) * 4);
+  L.base_off = off;    off = al(off + static_cast<size_t>(E) * R * 4);
+  L.totals_off = off;  off = al(off + static_cast<size_t>(E) * 4);
+  L.segoff_off = off;  off = al(off + static_cast<size_t>(R) * (E_loc + 1) * 4);
+  L.tprefix_off = off; off = al(off + (static_cast<size_t>(E) + 1) * 4);
+  L.tiles_off = off;   off = al(off + static_cast<size_t>(L.max_tiles) * 5 * 4);
+  L.total = off;
+  return true;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool okp(const void* p, long long elems, unsigned align) {
+  if (elems > 0 && !p) return false;
+  return (reinterpret_cast<uintptr_t>(p) & (align - 1)) == 0;
+}
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
 
 extern "C" {
 
 size_t mk_moe_workspace_size(int R, int E_loc, int topk, long long T, long long H, long long N,
                              long long cap_rows, const mk_config* cfg) {
-  (void)R; (void)E_loc; (void)topk; (void)T; (void)H; (void)N; (void)cap_rows; (void)cfg;
-  return 0;
+  (void)cfg;
+  MoeLayout L;
+  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, L)) return 0;
+  return L.total;
 }
 
 mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits, const void* const* w,
@@ -14,10 +265,111 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
                                long long cap_rows, int* topk_idx, int* counts, int* const* recv_src,
                                int* recv_counts, void* const* recv_x, void* const* y, void* workspace,
                                size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
-  (void)x; (void)logits; (void)w; (void)R; (void)E_loc; (void)topk; (void)T; (void)H; (void)N;
-  (void)cap_rows; (void)topk_idx; (void)counts; (void)recv_src; (void)recv_counts; (void)recv_x;
-  (void)y; (void)workspace; (void)ws_bytes; (void)cfg; (void)stream;
-  return MK_ERR_UNSUPPORTED;
+  if (!x || !logits || !w || !recv_src || !recv_x || !y || !workspace) return MK_ERR_INVALID;
+  MoeLayout L;
+  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, L)) return MK_ERR_INVALID;
+  if (ws_bytes < L.total || !al16(workspace)) return MK_ERR_INVALID;
+  const long long E = static_cast<long long>(R) * E_loc;
+  const long long rows = static_cast<long long>(R) * T * topk;
+  if (!okp(topk_idx, rows, 4) || !okp(counts, R * E, 4) || !okp(recv_counts, R, 4)) return MK_ERR_INVALID;
+  for (int r = 0; r < R; ++r) {
+    if (!okp(x[r], T * H, 16) || !okp(logits[r], T * E, 4) || !okp(w[r], E_loc * H * N, 16) ||
+        !okp(recv_src[r], cap_rows, 4) || !okp(recv_x[r], cap_rows * H, 16) || !okp(y[r], cap_rows * N, 16))
+      return MK_ERR_INVALID;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int) * R * E, s) != cudaSuccess) return MK_ERR_CUDA;
+    if (cudaMemsetAsync(recv_counts, 0, sizeof(int) * R, s) != cudaSuccess) return MK_ERR_CUDA;
+    return MK_OK;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return MK_ERR_UNSUPPORTED;
+  int grid_cap = sms;
+  if (cfg && cfg->max_ctas > 0) grid_cap = std::min(grid_cap, cfg->max_ctas);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  MoeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < R; ++r) {
+    a.logits[r] = logits[r];
+    a.recv_src[r] = recv_src[r];
+  }
+  a.topk_idx = topk_idx;
+  a.counts = counts;
+  a.recv_counts = recv_counts;
+  a.pos = reinterpret_cast<int*>(ws + L.pos_off);
+  a.base = reinterpret_cast<int*>(ws + L.base_off);
+  a.totals = reinterpret_cast<int*>(ws + L.totals_off);
+  a.segoff = reinterpret_cast<int*>(ws + L.segoff_off);
+  a.tprefix = reinterpret_cast<int*>(ws + L.tprefix_off);
+  a.tiles = reinterpret_cast<int*>(ws + L.tiles_off);
+  a.misc = reinterpret_cast<uint32_t*>(ws + L.misc_off);
+  a.blocks = reinterpret_cast<uint32_t*>(ws + L.blocks_off);
+  a.hdr = reinterpret_cast<uint32_t*>(ws);
+  a.R = R;
+  a.E_loc = E_loc;
+  a.E = static_cast<int>(E);
+  a.topk = topk;
+  a.T = static_cast<int>(T);
+  a.n_nblk = L.n_nblk;
+  a.nblk = L.nblk;
+  a.cap = cap_rows;
+
+  moe_route_rank_kernel<<<R, RR_THREADS, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  moe_offsets_kernel<<<1, 256, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  const long long work = std::max(rows, static_cast<long long>(L.max_tiles));
+  const int sgrid = static_cast<int>(std::min<long long>(ceil_div_ll(work, 256), 4LL * sms));
+  moe_scatter_kernel<<<std::max(1, sgrid), 256, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  if (H == 0 || N == 0 || cap_rows == 0) return MK_OK;
+
+  // ---- the persistent dispatch + grouped GEMM kernel
+  FusedParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.op = OP_MOE;
+  p.mode = MK_MODE_FUSED;
+  p.R = R;
+  p.M = static_cast<int>(cap_rows);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(H);
+  p.n_nblk = L.n_nblk;
+  p.n_kblk = static_cast<int>(ceil_div_ll(H, BK));
+  p.n_mblk = 1;
+  p.group_m = 1;
+  p.split_k = 1;
+  p.P = 1;
+  p.n_items = L.max_tiles;
+  p.moe_tiles = a.tiles;
+  p.moe_ntiles = reinterpret_cast<const int*>(a.misc + MISC_NTILES);
+  p.moe_ok = reinterpret_cast<const int*>(a.misc + MISC_OK);
+  p.moe_recv_counts = recv_counts;
+  p.moe_T = static_cast<int>(T);
+  p.moe_topk = topk;
+  p.moe_nblk = L.nblk;
+  int pr = 1;
+  while (pr < BM && static_cast<long long>(pr) * 2 * H * 2 <= 32768) pr *= 2;
+  p.moe_rows_per_piece = pr;
+  p.flags = a.blocks;
+  p.hdr = a.hdr;
+  p.wait_ns = default_wait_ns(cfg);
+  p.inject = cfg ? cfg->inject : 0;
+  p.epoch = next_epoch();
+  for (int r = 0; r < R; ++r) {
+    p.shard[r] = static_cast<const uint8_t*>(x[r]);
+    p.out[r] = y[r];
+    p.moe_recv_x[r] = static_cast<uint8_t*>(recv_x[r]);
+    p.moe_src[r] = recv_src[r];
+    if (!make_map_2d(&p.tmA[r], recv_x[r], H, cap_rows, static_cast<size_t>(H) * 2, BK, BM) ||
+        !make_map_3d(&p.tmB[r], w[r], N, H, E_loc, static_cast<size_t>(N) * 2,
+                     static_cast<size_t>(H) * N * 2, 64, BK, 1))
+      return MK_ERR_CUDA;
+  }
+  const int grid = std::max(1, std::min(grid_cap, L.max_tiles));
+  p.n_compute = grid;
+  return launch_fused(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 
 }  // extern "C"
