@@ -237,9 +237,13 @@ def main():
     ap.add_argument("--no-other", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--n-copy", type=int, default=0)
+    ap.add_argument("--only", choices=["rs", "ar", "moe"], default=None,
+                    help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
 
     world, rank, local = dist_env()
     dist = None
@@ -381,10 +385,30 @@ def main():
     return 0
 
 
-def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+def run_only(args):
+    """Time one secondary workload alone (fused / GEMM-only / unfused) and print it."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(device)
+    import comm_gemm_tile_gb300 as mk
+    from comm_gemm_tile_gb300 import build as mkbuild
+    mkbuild.build()
+    bf16_peak, _, hbm_peak, _ = peaks()
+    if args.only == "moe":
+        res = bench_moe(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    else:
+        w = I.RS_R8_TP8_DOWN if args.only == "rs" else I.AR_R8_DECODE
+        res = bench_other(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
+                          hbm_peak, only=[w], with_moe=False)[w.name]
+    print(json.dumps({"only": args.only, **res}), flush=True)
+    return 0
+
+
+def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak,
+                only=None, with_moe=True):
     """Fused / GEMM-only / unfused timings of the RS and AR workloads."""
     out = {}
-    for w in (I.RS_R8_TP8_DOWN, I.AR_R8_DECODE):
+    for w in (only or (I.RS_R8_TP8_DOWN, I.AR_R8_DECODE)):
         nsets = 2 if w.op == "rs" else 3
         sets = []
         for s in range(nsets):
@@ -421,7 +445,50 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         out[w.name] = entry
         del sets, ws
         torch.cuda.empty_cache()
+    if with_moe:
+        out[I.MOE_R8_E64.name] = bench_moe(mk, device, stream, dist, steps, seed_off, tmax,
+                                           bf16_peak, hbm_peak)
     return out
+
+
+def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+    """MoE dispatch + grouped GEMM: fused, GEMM-only and unfused timings."""
+    w = I.MOE_R8_E64
+    sets = []
+    for s in range(2):
+        x = [dev_normal((w.T, w.H), 1.0, w.x_seed + r + 1000 * s + seed_off, device) for r in range(w.R)]
+        lg = [I.zipf_logits(w.T, w.E, w.logit_seed + r + 1000 * s + seed_off).to(device)
+              for r in range(w.R)]
+        we = [dev_normal((w.E_loc, w.H, w.N), 0.02, w.w_seed + d + 1000 * s + seed_off, device)
+              for d in range(w.R)]
+        sets.append((x, lg, we))
+    ws = mk.Workspace(device)
+    outs = mk.moe_dispatch_gemm(*sets[0], E_loc=w.E_loc, topk=w.topk, workspace=ws, stream=stream)
+    res = {}
+    for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                      ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        def step(i, cfg=cfg):
+            x, lg, we = sets[i % 2]
+            mk.moe_dispatch_gemm(x, lg, we, E_loc=w.E_loc, topk=w.topk, out=outs, cfg=cfg,
+                                 workspace=ws, stream=stream)
+        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+    st, _ = mk.device_status(ws, stream)
+    flops = w.flops()
+    rows = w.R * w.T * w.topk
+    hbm_bytes = (rows * w.H * 2 * 2            # dispatch: read token rows, write recv_x
+                 + rows * w.H * 2              # grouped GEMM reads recv_x
+                 + w.R * w.E_loc * w.H * w.N * 2   # expert weights
+                 + rows * w.N * 2              # y
+                 + w.R * w.T * w.E * 4)        # logits
+    fused_tf = flops / (res["fused"] * 1e-3) / 1e12
+    t_tensor = flops / (bf16_peak * 1e12)
+    t_hbm = hbm_bytes / (hbm_peak * 1e9)
+    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "algorithmic_bytes": hbm_bytes,
+            "roofline_ms": 1e3 * max(t_tensor, t_hbm),
+            "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
+            "status": mk.status_string(st)}
 
 
 if __name__ == "__main__":

@@ -250,6 +250,7 @@ struct ComputeSmem {
 };
 
 __device__ __forceinline__ int n_items_for(const FusedParams& p) {
+  if (p.op == OP_MOE && p.mode == MK_MODE_UNFUSED) return 0;   // baseline: dispatch copy only
   if (p.op == OP_MOE) return min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)) ,
                                  static_cast<uint32_t>(p.n_items));
   return p.n_items;
@@ -264,7 +265,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it);
-    if (p.op == OP_MOE) {
+    if (p.op == OP_MOE && p.mode == MK_MODE_FUSED) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       const int d = it.amap;
       const int rc = p.moe_recv_counts[d];
@@ -622,6 +623,7 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cid) {
   const int lane = threadIdx.x & 31;
   const int worker = cid * 2 + ((threadIdx.x >> 5) - 6);
   const int n_workers = p.n_compute * 2;
+  if (p.mode == MK_MODE_GEMM_ONLY) return;   // baseline: recv_x is already filled
   if (*reinterpret_cast<const volatile int*>(p.moe_ok) == 0) return;
   const int pr = p.moe_rows_per_piece;
   long long total = 0;

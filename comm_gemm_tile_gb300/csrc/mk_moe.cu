@@ -369,6 +369,15 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   }
   const int grid = std::max(1, std::min(grid_cap, L.max_tiles));
   p.n_compute = grid;
+  const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
+  if (mode == MK_MODE_UNFUSED) {
+    // host-ordered baseline: the dispatch copy as one launch, then the grouped GEMM
+    p.mode = MK_MODE_UNFUSED;
+    if (launch_fused(p, grid, s) != cudaSuccess) return MK_ERR_CUDA;
+    p.mode = MK_MODE_GEMM_ONLY;
+  } else if (mode == MK_MODE_GEMM_ONLY) {
+    p.mode = MK_MODE_GEMM_ONLY;   // baseline: recv_x as left by an earlier call
+  }
   return launch_fused(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 

@@ -158,3 +158,25 @@ def test_moe_missing_rows_time_out():
     x, logits, wexp, res, st, _ = run_both(w)
     assert st == mk.MK_OK
     check_dispatch(w, x, logits, res)
+
+
+def test_moe_baseline_modes_match_fused():
+    w = I.MoeWorkload("t", R=4, E_loc=2, T=200, H=256, N=512, integer=True, x_seed=91,
+                      logit_seed=92, w_seed=93)
+    x, logits, wexp = I.moe_inputs(w)
+    args = ([t.cuda() for t in x], [t.cuda() for t in logits], [t.cuda() for t in wexp])
+    ws = mk.Workspace()
+    fused = mk.moe_dispatch_gemm(*args, E_loc=w.E_loc, topk=2, workspace=ws)
+    unf = mk.moe_dispatch_gemm(*args, E_loc=w.E_loc, topk=2, workspace=ws,
+                               cfg=mk.Config(mode=mk.MODE_UNFUSED))
+    # GEMM only: recv_x is taken as already filled (here: by the fused call)
+    out = {"recv_x": fused["recv_x"]}
+    gonly = mk.moe_dispatch_gemm(*args, E_loc=w.E_loc, topk=2, workspace=ws, out=out,
+                                 cfg=mk.Config(mode=mk.MODE_GEMM_ONLY))
+    st, _ = mk.device_status(ws)
+    assert st == mk.MK_OK
+    rc = fused["recv_counts"].cpu().numpy()
+    for d in range(w.R):
+        for other in (unf, gonly):
+            assert torch.equal(fused["y"][d][:rc[d]], other["y"][d][:rc[d]])
+        assert torch.equal(fused["recv_x"][d][:rc[d]], unf["recv_x"][d][:rc[d]])

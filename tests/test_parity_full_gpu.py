@@ -79,3 +79,44 @@ def test_ar_full_size(integer):
         np.testing.assert_array_equal(r0, oracle_bits(exact, "bf16"))
     else:
         assert norm_err(gpu_values(reps[0]), exact, w.R * w.k, absmax(a), absmax(b)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_moe_full_size(integer):
+    # 8 ranks x 8 experts, 4096 tokens per rank, hidden 4096, up-proj 1536, top-2, Zipf(1.1)
+    w = I.MOE_R8_E64.integer_twin() if integer else I.MOE_R8_E64
+    x, logits, wexp = I.moe_inputs(w)
+    ws = mk.Workspace()
+    res = mk.moe_dispatch_gemm([t.cuda() for t in x], [t.cuda() for t in logits],
+                               [t.cuda() for t in wexp], E_loc=w.E_loc, topk=w.topk,
+                               cap_rows=w.cap, workspace=ws)
+    _ok(ws)
+    idx = [O.moe_route(l.numpy(), w.topk) for l in logits]
+    np.testing.assert_array_equal(res["topk_idx"].cpu().numpy(), np.concatenate(idx, 0))
+    np.testing.assert_array_equal(res["counts"].cpu().numpy(), O.moe_counts(idx, w.E))
+    recv_src, seg = O.moe_dispatch(idx, w.E_loc)
+    rc = res["recv_counts"].cpu().numpy()
+    xb = [I.bits(t) for t in x]
+    amax, bmax = absmax(x), absmax(wexp)
+    for d in range(w.R):
+        assert rc[d] == len(recv_src[d])
+        np.testing.assert_array_equal(res["recv_src"][d][:rc[d]].cpu().numpy(), recv_src[d])
+        if rc[d] == 0:
+            continue
+        rows = I.sample_rows(int(rc[d]), seed=100 + d)
+        sel = torch.from_numpy(rows).cuda()
+        rx = O.moe_gather_rows(xb, recv_src[d][rows], w.topk)
+        np.testing.assert_array_equal(I.bits(res["recv_x"][d][sel]), rx)
+        full_rx = O.moe_gather_rows(xb, recv_src[d], w.topk)
+        starts = np.concatenate([[0], np.cumsum(seg[d])])
+        expert_of = np.searchsorted(starts, rows, side="right") - 1
+        exact = np.zeros((len(rows), w.N))
+        wb = I.bits(wexp[d])
+        for l in np.unique(expert_of):
+            pick = np.nonzero(expert_of == l)[0]
+            exact[pick] = O.bf16_to_f64(full_rx[rows[pick]]) @ O.bf16_to_f64(wb[l])
+        got = res["y"][d][sel]
+        if integer:
+            np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
+        else:
+            assert norm_err(gpu_values(got), exact, w.H, amax, bmax) <= TOL["bf16"]
