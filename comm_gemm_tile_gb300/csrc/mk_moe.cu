@@ -4,10 +4,12 @@
 // tokens processed on arrival).
 //
 // Four launches on the caller's stream:
-//   1. route + rank (one CTA per source rank): top-k experts of every token,
-//      and for every (token, slot) its position among the rank's rows routed to
-//      the same expert (a stable block-level multisplit), plus counts[r][e];
-//   2. offsets (one CTA): expert totals, per-destination segment offsets,
+//   1. route + rank (one CTA per chunk of 64 tokens of a source rank): top-k
+//      experts of every token, and for every (token, slot) its position among
+//      the chunk's rows routed to the same expert (a stable block-level
+//      multisplit), plus the chunk's per-expert counts;
+//   2. offsets (one CTA): chunk prefixes and counts[r][e], expert totals,
+//      per-destination segment offsets,
 //      per-(rank, expert) bases, received-row counts, the capacity check, the
 //      tile-table prefix, and zeroed per-block arrival counters;
 //   3. scatter: recv_src (the destination-ordered inverse map) and the
@@ -27,7 +29,8 @@ namespace mk {
 
 namespace {
 
-constexpr int RR_THREADS = 512;
+constexpr int RR_THREADS = 256;
+constexpr int RR_TOKENS = 64;   // tokens per route/rank CTA
 constexpr int RR_WARPS = RR_THREADS / 32;
 enum { MISC_NTILES = 0, MISC_OK = 1, MISC_WORDS = 64 };
 
@@ -37,7 +40,8 @@ struct MoeArgs {
   int* topk_idx;      // [R*T x topk]
   int* counts;        // [R x E]
   int* recv_counts;   // [R]
-  int* pos;           // [R*T*topk] position among the rank's rows of the same expert
+  int* pos;           // [R*T*topk] position among the chunk's rows of the same expert
+  int* hist;          // [R x C x E] per-chunk expert counts, turned into chunk prefixes
   int* base;          // [R x E]  rows of expert e from ranks before r
   int* totals;        // [E]
   int* segoff;        // [R x (E_loc+1)]
@@ -46,7 +50,7 @@ struct MoeArgs {
   uint32_t* misc;     // MISC_* words
   uint32_t* blocks;   // [R x nblk] arrival counters
   uint32_t* hdr;      // workspace header (status)
-  int R, E_loc, E, topk, T, n_nblk, nblk;
+  int R, E_loc, E, topk, T, n_nblk, nblk, C;
   long long cap;
 };
 
@@ -57,14 +61,17 @@ __device__ __forceinline__ bool better(float v, int e, float ov, int oe) {
   return ov > v || (ov == v && oe < e);
 }
 
+// Grid (C chunks, R ranks): CTA (c, r) routes tokens [c*RR_TOKENS, ...) of
+// rank r and ranks their (token, slot) pairs per expert inside the chunk.
 __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid_constant__ MoeArgs a) {
-  const int r = blockIdx.x;
+  const int c = blockIdx.x, r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, T = a.T, K = a.topk;
+  const int t0 = c * RR_TOKENS, t1 = min(T, t0 + RR_TOKENS);
   const float* lg = a.logits[r];
   int* idx = a.topk_idx + static_cast<size_t>(r) * T * K;
   // ---- top-k per token, one warp per token
-  for (int t = warp; t < T; t += RR_WARPS) {
+  for (int t = t0 + warp; t < t1; t += RR_WARPS) {
     float v[MOE_MAX_E / 32];
 #pragma unroll
     for (int i = 0; i < MOE_MAX_E / 32; ++i) {
@@ -97,17 +104,17 @@ __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid
     }
   }
   __syncthreads();
-  // ---- stable multisplit of the rank's (token, slot) list by expert
+  // ---- stable multisplit of the chunk's (token, slot) list by expert
   __shared__ int wcnt[RR_WARPS * MOE_MAX_E];
   __shared__ int run[MOE_MAX_E];
   for (int e = tid; e < E; e += RR_THREADS) run[e] = 0;
-  const int n = T * K;
+  const int a0 = t0 * K, n = (t1 - t0) * K;
   const uint32_t lt = (1u << lane) - 1u;
   for (int b0 = 0; b0 < n; b0 += RR_THREADS) {
     for (int x = tid; x < RR_WARPS * E; x += RR_THREADS) wcnt[x] = 0;
     __syncthreads();
     const int ai = b0 + tid;
-    const int e = (ai < n) ? idx[ai] : -1 - lane;   // distinct sentinels never group
+    const int e = (ai < n) ? idx[a0 + ai] : -1 - lane;   // distinct sentinels never group
     const uint32_t mask = __match_any_sync(0xffffffffu, e);
     const int rank_w = __popc(mask & lt);
     if (ai < n && (__ffs(mask) - 1) == lane) wcnt[warp * E + e] = __popc(mask);
@@ -115,22 +122,42 @@ __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid
     for (int ee = tid; ee < E; ee += RR_THREADS) {
       int acc = run[ee];
       for (int w = 0; w < RR_WARPS; ++w) {
-        const int c = wcnt[w * E + ee];
+        const int cnt = wcnt[w * E + ee];
         wcnt[w * E + ee] = acc;
-        acc += c;
+        acc += cnt;
       }
       run[ee] = acc;
     }
     __syncthreads();
-    if (ai < n) a.pos[static_cast<size_t>(r) * n + ai] = wcnt[warp * E + e] + rank_w;
+    if (ai < n) a.pos[static_cast<size_t>(r) * T * K + a0 + ai] = wcnt[warp * E + e] + rank_w;
     __syncthreads();
   }
-  for (int e = tid; e < E; e += RR_THREADS) a.counts[r * E + e] = run[e];
+  for (int e = tid; e < E; e += RR_THREADS)
+    a.hist[(static_cast<size_t>(r) * a.C + c) * E + e] = run[e];
 }
 
 __global__ void __launch_bounds__(256) moe_offsets_kernel(const __grid_constant__ MoeArgs a) {
   const int tid = threadIdx.x;
   const int R = a.R, E = a.E, El = a.E_loc;
+  // per (rank, expert): exclusive prefix over chunks (in place), and the count
+  for (int x = tid; x < R * E; x += 256) {
+    const int r = x / E, e = x - r * E;
+    int* h = a.hist + static_cast<size_t>(r) * a.C * E + e;
+    int acc = 0;
+    for (int c0 = 0; c0 < a.C; c0 += 8) {   // 8 loads in flight per thread
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (c0 + u < a.C) ? h[static_cast<size_t>(c0 + u) * E] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + u < a.C) {
+          h[static_cast<size_t>(c0 + u) * E] = acc;
+          acc += v[u];
+        }
+    }
+    a.counts[r * E + e] = acc;
+  }
+  __syncthreads();
   for (int e = tid; e < E; e += 256) {
     int acc = 0;
     for (int r = 0; r < R; ++r) {
@@ -179,7 +206,9 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
     const int t = aa / K, j = aa - t * K;
     const int e = a.topk_idx[ai];
     const int d = e / El, l = e - d * El;
-    const int row = a.segoff[d * (El + 1) + l] + a.base[r * E + e] + a.pos[ai];
+    const int c = t / RR_TOKENS;
+    const int row = a.segoff[d * (El + 1) + l] + a.base[r * E + e] +
+                    a.hist[(static_cast<size_t>(r) * a.C + c) * E + e] + a.pos[ai];
     a.recv_src[d][row] = (r * T + t) * K + j;
   }
   const int ntiles = static_cast<int>(a.misc[MISC_NTILES]);
@@ -205,9 +234,9 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
 }
 
 struct MoeLayout {
-  size_t blocks_off, misc_off, pos_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
+  size_t blocks_off, misc_off, pos_off, hist_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
   size_t total;
-  int nblk, n_nblk, max_tiles;
+  int nblk, n_nblk, max_tiles, C;
 };
 
 bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long N, long long cap,
@@ -230,6 +259,8 @@ bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long 
   L.blocks_off = off;  off = al(off + static_cast<size_t>(R) * L.nblk * 4);
   L.misc_off = off;    off = al(off + MISC_WORDS * 4);
   L.pos_off = off;     off = al(off + static_cast<size_t>(rows) * 4);
+  L.C = static_cast<int>(ceil_div_ll(std::max(T, 1LL), RR_TOKENS));
+  L.hist_off = off;    off = al(off + static_cast<size_t>(R) * L.C * E * 4);
   L.base_off = off;    off = al(off + static_cast<size_t>(E) * R * 4);
   L.totals_off = off;  off = al(off + static_cast<size_t>(E) * 4);
   L.segoff_off = off;  off = al(off + static_cast<size_t>(R) * (E_loc + 1) * 4);
@@ -299,6 +330,8 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   a.counts = counts;
   a.recv_counts = recv_counts;
   a.pos = reinterpret_cast<int*>(ws + L.pos_off);
+  a.hist = reinterpret_cast<int*>(ws + L.hist_off);
+  a.C = L.C;
   a.base = reinterpret_cast<int*>(ws + L.base_off);
   a.totals = reinterpret_cast<int*>(ws + L.totals_off);
   a.segoff = reinterpret_cast<int*>(ws + L.segoff_off);
@@ -316,7 +349,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   a.nblk = L.nblk;
   a.cap = cap_rows;
 
-  moe_route_rank_kernel<<<R, RR_THREADS, 0, s>>>(a);
+  moe_route_rank_kernel<<<dim3(L.C, R), RR_THREADS, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
   moe_offsets_kernel<<<1, 256, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
