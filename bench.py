@@ -55,6 +55,25 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_seed_offset(rank: int) -> int:
+    """Seed offset of a replica: every rank draws an independent problem."""
+    return 100000 * rank
+
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time (all ranks get the same value)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, t_max_ms: float) -> float:
+    """Units processed by all ranks per second, over the slowest rank's time."""
+    return world * units_per_rank / (t_max_ms * 1e-3)
+
+
 def peaks():
     """(bf16 burst TFLOP/s, bf16 sustained TFLOP/s, HBM GB/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -261,7 +280,7 @@ def main():
     bf16_peak, _, hbm_peak, peak_src = peaks()
 
     w = I.AG_R8_TP8_UP
-    seed_off = 100000 * rank          # replicas: an independent problem per rank
+    seed_off = replica_seed_offset(rank)   # replicas: an independent problem per rank
     M = w.R * w.m
     flops = 2.0 * M * w.n * w.k
     sets = []
@@ -307,17 +326,13 @@ def main():
     base_steps = max(10, min(args.steps, 200))
 
     def tmax(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, dist, device)
 
     t_gemm = tmax(time_loop(step_gemm, base_steps, 5, stream, dist) / base_steps)
     t_unf = tmax(time_loop(step_unfused, base_steps, 5, stream, dist) / base_steps)
     t_fused_max = tmax(t_fused)
     ms = t_fused_max / args.steps
-    value = world * flops * args.steps / (t_fused_max * 1e-3) / 1e12
+    value = whole_job_rate(flops * args.steps, world, t_fused_max) / 1e12
     achieved = flops / (t_fused / args.steps * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs -> device -> fused call -> host result
@@ -336,7 +351,7 @@ def main():
         hc.copy_(c, non_blocking=True)
 
     t_e2e = tmax(time_loop(step_e2e, args.e2e_steps, 3, stream, dist))
-    e2e_val = world * flops * args.e2e_steps / (t_e2e * 1e-3) / 1e12
+    e2e_val = whole_job_rate(flops * args.e2e_steps, world, t_e2e) / 1e12
     st, detail = mk.device_status(wsp, stream)
     if st != mk.MK_OK:
         raise SystemExit(f"e2e AG+GEMM reported {mk.status_string(st)} ({detail})")
