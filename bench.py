@@ -74,6 +74,29 @@ def whole_job_rate(units_per_rank: float, world: int, t_max_ms: float) -> float:
     return world * units_per_rank / (t_max_ms * 1e-3)
 
 
+def kernel_source_sha256() -> str:
+    """Hash of the CUDA sources, to tell whether recorded ncu counters still apply."""
+    import hashlib
+    root = os.path.join(ROOT, "comm_gemm_tile_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(root)):
+        h.update(f.encode())
+        h.update(open(os.path.join(root, f), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str, key: str = "fused_dram_bytes"):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    kernel sources changed since it was taken."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "mk_fused_kernel_traffic.json")))
+        if rec.get("source_sha256") != kernel_source_sha256():
+            return None
+        return rec[workload][key]
+    except Exception:
+        return None
+
+
 def peaks():
     """(bf16 burst TFLOP/s, bf16 sustained TFLOP/s, HBM GB/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -384,7 +407,8 @@ def main():
             "gemm_only_ms": t_gemm,
             "unfused_ms": t_unf,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                         "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                         "traffic": recorded_traffic(w.name),
                          "peak_source": f"{peak_src} bf16 burst"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
