@@ -94,7 +94,7 @@ struct Plan {
   int n_mblk, n_nblk, n_kblk, n_tiles;
   int split_k, kps, P;
   int group_m;
-  int chain;
+  int chain, last;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
 };
 
@@ -126,9 +126,22 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   pl.n_flags = 0;
   pl.staging_bytes = 0;
   pl.chain = 0;
+  pl.last = 0;
   if (op == OP_AG) {
     pl.n_flags = static_cast<size_t>(pl.n_mblk) * COPY_SUB_MAX;
   } else {
+    // Fused default: the partials of a tile are summed in rank order by the
+    // compute epilogues (one running-sum tile per output tile).  With
+    // n_reduce_ctas > 0, or in the unfused baseline, every partial is staged
+    // in its own slot and reduce-role CTAs sum them (at most MAX_PARTIALS).
+    // Without reduce-role CTAs the fused path reduces in the epilogues, either
+    // as a running sum (the default: measured fastest for both RS and AR) or by
+    // last arrival (the warp that completes a tile quarter sums all partials).
+    const bool in_epilogue = (mode == MK_MODE_FUSED && !(cfg && cfg->n_reduce_ctas > 0));
+    const int want = cfg ? cfg->reduce : 0;
+    pl.chain = (in_epilogue && want != 2) ? 1 : 0;
+    pl.last = (in_epilogue && !pl.chain) ? 1 : 0;
+    const int max_parts = in_epilogue ? MAX_CHAIN_PARTIALS : MAX_PARTIALS;
     int sk = (cfg && cfg->split_k > 0) ? cfg->split_k : 0;
     if (sk == 0) {
       sk = 1;
@@ -138,20 +151,16 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
       if (op == OP_AR && cfg && cfg->n_reduce_ctas > 0 && items > 0 && items < 2LL * PLAN_SMS)
         sk = static_cast<int>(ceil_div_ll(2LL * PLAN_SMS, items));
     }
-    sk = std::max(1, std::min(sk, MAX_PARTIALS / R));
+    sk = std::max(1, std::min(sk, max_parts / R));
     sk = std::min(sk, std::max(1, pl.n_kblk));
     pl.kps = static_cast<int>(ceil_div_ll(std::max(1, pl.n_kblk), sk));
     sk = static_cast<int>(ceil_div_ll(std::max(1, pl.n_kblk), pl.kps));  // drop empty slices
     pl.split_k = sk;
     pl.P = R * sk;
-    if (pl.P > MAX_PARTIALS) return false;
-    // Fused default: the partials of a tile are summed in rank order by the
-    // compute epilogues (one running-sum tile per output tile).  With
-    // n_reduce_ctas > 0, or in the unfused baseline, every partial is staged
-    // in its own slot and reduce-role CTAs sum them.
-    pl.chain = (mode == MK_MODE_FUSED && !(cfg && cfg->n_reduce_ctas > 0)) ? 1 : 0;
+    if (pl.P > max_parts) return false;
     if (mode != MK_MODE_GEMM_ONLY) {
-      pl.n_flags = static_cast<size_t>(pl.n_tiles) * pl.P;
+      // flags: one per (tile, partial); last arrival: four 64-bit counters per tile
+      pl.n_flags = pl.last ? static_cast<size_t>(pl.n_tiles) * 8 : static_cast<size_t>(pl.n_tiles) * pl.P;
       const size_t slots = pl.chain ? static_cast<size_t>(pl.n_tiles)
                                     : static_cast<size_t>(pl.n_tiles) * pl.P;
       pl.staging_bytes = slots * TILE_F32 * sizeof(float);
@@ -183,6 +192,7 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.kps = pl.kps;
   p.P = pl.P;
   p.chain = pl.chain;
+  p.last_arrival = pl.last;
   p.copy_sub = 1;
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
@@ -401,7 +411,7 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
     p.epoch = e;
     return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
   }
-  if (pl.chain) {
+  if (pl.chain || pl.last) {
     const int n_compute = std::min(sms, p.n_items);
     p.group_tiles = std::max(1, std::min(n_compute, pl.n_tiles));
     return launch(p, 0, n_compute, 0, s);

@@ -397,6 +397,73 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&r)[3
   }
 }
 
+// Last-arrival reduction: one counter per (tile, 32-row quarter), zeroed at
+// kernel start by the CTA with ticket 0 (published by hdr[HDR_READY]).
+// Returns the number of partials of this quarter stored before this one.
+__device__ __forceinline__ uint32_t bump_quarter(const FusedParams& p, int tile, int quarter) {
+  return atomicAdd(p.flags + static_cast<size_t>(tile) * 4 + quarter, 1u);
+}
+
+// Rows of one warp quarter of `tile`: sum of its P staged partials in order
+// 0..P-1, rounded and written to the owner block (RS) or every replica (AR).
+__device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, int trow, bool row_ok,
+                               int grow) {
+  const size_t esz = p.out_f32 ? 4 : 2;
+  const float* base = p.staging + static_cast<size_t>(tile) * p.P * TILE_F32;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float4 acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      acc[q] = ld_global_cg_f4(base + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
+    int part = 1;
+    for (; part + 1 < p.P; part += 2) {
+      float4 v0[8], v1[8];
+      const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
+      const float* s1 = s0 + TILE_F32;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v0[q] = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
+        v1[q] = ld_global_cg_f4(s1 + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        acc[q].x += v0[q].x; acc[q].y += v0[q].y; acc[q].z += v0[q].z; acc[q].w += v0[q].w;
+        acc[q].x += v1[q].x; acc[q].y += v1[q].y; acc[q].z += v1[q].z; acc[q].w += v1[q].w;
+      }
+    }
+    if (part < p.P) {
+      const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
+        acc[q].x += v.x; acc[q].y += v.y; acc[q].z += v.z; acc[q].w += v.w;
+      }
+    }
+    const int col = it.nb * BN + 32 * c;
+    const int nvalid = max(0, min(32, p.N - col));
+    if (!row_ok || nvalid == 0) continue;
+    uint32_t r[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      r[4 * q + 0] = __float_as_uint(acc[q].x);
+      r[4 * q + 1] = __float_as_uint(acc[q].y);
+      r[4 * q + 2] = __float_as_uint(acc[q].z);
+      r[4 * q + 3] = __float_as_uint(acc[q].w);
+    }
+    if (p.op == OP_RS) {
+      const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
+      uint8_t* ob = reinterpret_cast<uint8_t*>(p.out[o]);
+      store_row_chunk(ob + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
+    } else {
+      for (int o = 0; o < p.R; ++o) {
+        uint8_t* ob = reinterpret_cast<uint8_t*>(p.out[o]);
+        store_row_chunk(ob + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
+      }
+    }
+  }
+}
+
 __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
@@ -404,6 +471,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   const size_t esz = p.out_f32 ? 4 : 2;
   int buf = 0;
   uint32_t acc_phase = 0;
+  bool counters_ready = false;   // last-arrival counters published for this call
   const int n_items = n_items_for(p);
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
@@ -473,6 +541,48 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
           }
         }
       }
+    } else if (it.slot >= 0 && p.last_arrival) {
+      // Stage this partial, then the warp whose store completes its 32-row
+      // quarter of the tile (the P-th arrival) sums all P partials in order.
+      float* slot = p.staging + static_cast<size_t>(it.slot) * TILE_F32;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float* d = slot + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4;
+          st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(S.tempty(buf));   // tensor memory is free again
+      __threadfence();
+      __syncwarp();
+      const int tile = it.slot / p.P;
+      int last = 0;
+      if (lane == 0) {
+        if (!counters_ready) {
+          if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_EPILOGUE, i)) last = -1;
+          counters_ready = true;
+        }
+        const bool skip = (p.inject == 2 && it.slot == 0);
+        if (last == 0 && !skip)
+          last = (bump_quarter(p, tile, quarter) == static_cast<uint32_t>(p.P - 1)) ? 1 : 0;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last < 0) return;
+      if (last) {
+        __threadfence();   // the other partials' stores happened before their counts
+        reduce_quarter(p, it, tile, trow, row_ok, grow);
+      }
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1u;
+      }
+      continue;
     } else if (it.slot >= 0) {
       // Partial tile -> staging slot.  Layout: float4 (row, column group cg)
       // at index cg*BM + row, so a warp's 32 rows form 512 contiguous bytes.
@@ -555,7 +665,7 @@ __device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, l
 // AG copy-in by warps 6-7 of every compute CTA.  The work list is (chunk in
 // copy order, piece of copy_rows rows); worker w = 2*cid + (warp - 6) takes
 // pieces w, w + 2*n_compute, ... so all workers move neighbouring pieces of
-// the same few chunks at a time.  Each lane streams 16-byte vectors, 8 loads
+// the same few chunks at a time.  Each lane streams 16-byte vectors, 16 loads
 // in flight; after a piece every lane fences and lane 0 bumps the chunk's
 // counter.  Copy warps never wait on anything, so they always progress.
 constexpr int CW_UNROLL = 16;
@@ -1084,10 +1194,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
   }
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
-  if (t == 0 && p.op == OP_AG && p.copy_warps) {
-    // Zero this call's chunk counters (the workspace may hold anything from
-    // earlier calls of any op), then publish them.
-    for (int mb = threadIdx.x; mb < p.n_mblk; mb += NTHREADS) *chunk_counter(p, mb) = 0u;
+  if (t == 0 && ((p.op == OP_AG && p.copy_warps) || p.last_arrival)) {
+    // Zero this call's counters (the workspace may hold anything from earlier
+    // calls of any op), then publish them.
+    if (p.op == OP_AG) {
+      for (int mb = threadIdx.x; mb < p.n_mblk; mb += NTHREADS) *chunk_counter(p, mb) = 0u;
+    } else {
+      for (int x = threadIdx.x; x < p.n_tiles * 4; x += NTHREADS) p.flags[x] = 0u;
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) st_release_gpu(&p.hdr[HDR_READY], p.epoch);

@@ -27,7 +27,8 @@ constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int TILE_F32 = BM * BN;              // floats in one partial tile
-constexpr int MAX_PARTIALS = 16;               // partial tiles reduced per output tile
+constexpr int MAX_PARTIALS = 16;               // staged partial tiles reduced per output tile
+constexpr int MAX_CHAIN_PARTIALS = 128;        // partials per tile of the running-sum reduction
 constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chunk
 
 // Workspace header words (uint32 each).
@@ -70,6 +71,8 @@ struct FusedParams {
   int copy_sub;        // AG: sub-chunks per chunk (each its own ready flag), power of 2 <= 16
   int chain;           // RS/AR: 1 = partials summed in rank order by the epilogues (running sum
                        //        forwarded tile by tile); 0 = staged partials + reduce-role CTAs
+  int last_arrival;    // RS/AR: 1 = staged partials, the epilogue warp that completes a tile
+                       //        quarter (32 rows) sums its partials (with chain = 0)
   int group_tiles;     // RS/AR chain: tiles per scheduling group
   int copy_warps;      // AG: 1 = copy-in done by warps 6-7 of every compute CTA, one
                        //     piece counter per chunk (zeroed at kernel start by the CTA

@@ -92,6 +92,10 @@ typedef struct {
   long long wait_limit_ns;  /* bound on every device-side wait (default 2e9 ns)        */
   int inject;               /* test only: 1 = one copy-in chunk never signals ready;
                                2 = one partial tile never signals ready                */
+  int reduce;               /* RS / AR with n_reduce_ctas == 0: 0 = default (running sum),
+                               1 = running sum forwarded in rank order by the epilogues,
+                               2 = last arrival: every partial staged, the epilogue that
+                                   completes a tile sums all of them in rank order      */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).

@@ -106,9 +106,13 @@ def test_rs_reduce_role_matches_running_sum_bits():
     x = mk.gemm_rs(da, db, out_dtype=torch.float32)
     y = mk.gemm_rs(da, db, out_dtype=torch.float32, cfg=mk.Config(n_reduce_ctas=4))
     z = mk.gemm_rs(da, db, out_dtype=torch.float32, cfg=mk.Config(max_ctas=7))   # cross-CTA chains
+    u = mk.gemm_rs(da, db, out_dtype=torch.float32, cfg=mk.Config(reduce=mk.REDUCE_LAST_ARRIVAL))
+    v = mk.gemm_rs(da, db, out_dtype=torch.float32,
+                   cfg=mk.Config(reduce=mk.REDUCE_LAST_ARRIVAL, max_ctas=5))
     _ok()
     for o in range(R):
-        assert torch.equal(x[o], y[o]) and torch.equal(x[o], z[o])
+        for other in (y, z, u, v):
+            assert torch.equal(x[o], other[o])
 
 
 # ------------------------------------------------------------------ GEMM + AllReduce
@@ -139,6 +143,19 @@ def test_ar_float(R, m, n, k):
     for r in reps[1:]:
         np.testing.assert_array_equal(gpu_bits(r), r0)
     assert norm_err(gpu_values(reps[0]), exact, R * k, absmax(a), absmax(b)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("reduce", [mk.REDUCE_RUNNING_SUM, mk.REDUCE_LAST_ARRIVAL])
+@pytest.mark.parametrize("split_k", [1, 3])
+def test_ar_reductions_integer_bit_exact(reduce, split_k):
+    R, m, n, k = 8, 128, 1032, 512
+    w = I.GemmWorkload("t", "ar", R=R, m=m, n=n, k=k, out="bf16", a_seed=75, b_seed=85, integer=True)
+    a, b = I.gemm_inputs(w)
+    reps = mk.gemm_ar(dev(a), dev(b), cfg=mk.Config(reduce=reduce, split_k=split_k))
+    _ok()
+    exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
+    for r in reps:
+        np.testing.assert_array_equal(gpu_bits(r), oracle_bits(exact, "bf16"))
 
 
 def test_ar_equals_rs_blocks():
