@@ -59,6 +59,46 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_a(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uint64_t row_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {k, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BM)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n) {
+  auto fn = encode_fn();
+  if (!fn || (n % 64)) return false;
+  cuuint64_t dims[3] = {64, k, n / 64};
+  cuuint64_t strides[2] = {n * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BN / 64)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts) {
+  auto fn = encode_fn();
+  if (!fn || (n % 64)) return false;
+  cuuint64_t dims[4] = {64, h, n / 64, experts};
+  cuuint64_t strides[3] = {n * 2, 128, h * n * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BN / 64), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
   auto fn = encode_fn();
@@ -294,6 +334,7 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
   FusedParams p;
   fill_common(p, pl, static_cast<uint8_t*>(workspace), cfg, c_dtype);
   p.local = local_rank;
+  p.b_one_box = (n % 64 == 0) ? 1 : 0;
   p.gathered = static_cast<uint8_t*>(a_gathered);
   for (int r = 0; r < R; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
   p.out[0] = c;
@@ -325,9 +366,10 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     p.copy_sub = COPY_SUB_MAX;
     return launch(p, std::min(sms, std::max(1, p.n_copy_chunks * COPY_SUB_MAX)), 0, 0, s);
   }
-  if (!make_map_2d(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes, BK, BM) ||
-      !make_map_2d(&p.tmA[1], a_gathered, k, pl.M, row_bytes, BK, BM) ||
-      !make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK))
+  if (!make_map_a(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes) ||
+      !make_map_a(&p.tmA[1], a_gathered, k, pl.M, row_bytes) ||
+      !(p.b_one_box ? make_map_b_chunks(&p.tmB[0], b, k, n)
+                    : make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK)))
     return MK_ERR_CUDA;
 
   if (pl.mode == MK_MODE_GEMM_ONLY) {
@@ -393,10 +435,12 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   fill_common(p, pl, static_cast<uint8_t*>(workspace), cfg, c_dtype);
   p.rows_per_owner = static_cast<int>(m / R);
   if (op == OP_AR) p.rows_per_owner = static_cast<int>(m);
+  p.b_one_box = (n % 64 == 0) ? 1 : 0;
   for (int r = 0; r < R; ++r) {
     p.out[r] = outs[r];
-    if (!make_map_2d(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2, BK, BM) ||
-        !make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK))
+    if (!make_map_a(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2) ||
+        !(p.b_one_box ? make_map_b_chunks(&p.tmB[r], b[r], k, n)
+                      : make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK)))
       return MK_ERR_CUDA;
   }
   if (pl.mode == MK_MODE_GEMM_ONLY) {

@@ -238,15 +238,25 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
 }
 
 // ------------------------------------------------------------------ compute role
+// Barrier block of a compute CTA (8-byte mbarriers), then the TMEM base slot.
+constexpr uint32_t BAR_FULL = 0;
+constexpr uint32_t BAR_EMPTY = BAR_FULL + 8u * STAGES;
+constexpr uint32_t BAR_TFULL = BAR_EMPTY + 8u * STAGES;
+constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 16u;
+constexpr uint32_t BAR_DRAIN = BAR_TEMPTY + 16u;
+constexpr uint32_t BAR_PDONE = BAR_DRAIN + 8u;
+constexpr uint32_t TMEM_SLOT = BAR_PDONE + 16u;
+static_assert(TMEM_SLOT + 4 <= BAR_BYTES, "compute barriers exceed the barrier block");
+
 struct ComputeSmem {
   uint32_t ring;  // smem address of stage 0
   uint32_t bars;  // smem address of the barrier block
-  __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
-  __device__ __forceinline__ uint32_t empty(int s) const { return bars + 32u + 8u * s; }
-  __device__ __forceinline__ uint32_t tfull(int b) const { return bars + 64u + 8u * b; }
-  __device__ __forceinline__ uint32_t tempty(int b) const { return bars + 80u + 8u * b; }
-  __device__ __forceinline__ uint32_t drain() const { return bars + 96u; }
-  __device__ __forceinline__ uint32_t pdone(int b) const { return bars + 104u + 8u * b; }
+  __device__ __forceinline__ uint32_t full(int s) const { return bars + BAR_FULL + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const { return bars + BAR_EMPTY + 8u * s; }
+  __device__ __forceinline__ uint32_t tfull(int b) const { return bars + BAR_TFULL + 8u * b; }
+  __device__ __forceinline__ uint32_t tempty(int b) const { return bars + BAR_TEMPTY + 8u * b; }
+  __device__ __forceinline__ uint32_t drain() const { return bars + BAR_DRAIN; }
+  __device__ __forceinline__ uint32_t pdone(int b) const { return bars + BAR_PDONE + 8u * b; }
 };
 
 __device__ __forceinline__ int n_items_for(const FusedParams& p) {
@@ -299,7 +309,11 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
         mbar_arrive_expect_tx(S.full(stage), STAGE_BYTES);
         tma_load_2d(a_dst, ma, S.full(stage), kb * BK, it.arow);
         const int n0 = it.nb * BN;
-        if (it.bz < 0) {
+        if (p.b_one_box) {
+          // the whole BK x 256 B tile in one request (4 column chunks of 64)
+          if (it.bz < 0) tma_load_3d(b_dst, mbm, S.full(stage), 0, kb * BK, n0 / 64);
+          else tma_load_4d(b_dst, mbm, S.full(stage), 0, kb * BK, n0 / 64, it.bz);
+        } else if (it.bz < 0) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_2d(b_dst + j * B_BOX_BYTES, mbm, S.full(stage), n0 + 64 * j, kb * BK);
@@ -346,8 +360,9 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
           const uint32_t b_addr = a_addr + A_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            // A: K-major, 128-B swizzle, 8-row atoms 1024 B apart; +32 B per 16-wide K step.
-            const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
+            // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
+            const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 8u * A_SWIZZLE_BYTES,
+                                          A_SWIZZLE_BYTES == 128 ? 2u : 4u);
             // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
             // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
             const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
@@ -790,7 +805,7 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   ComputeSmem S;
   S.ring = smem_u32(smem);
   S.bars = smem_u32(smem + RING_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + 168);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + TMEM_SLOT);
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(S.full(s), 1);

@@ -15,12 +15,17 @@ namespace mk {
 // K consumed in 64-element (128-byte) slabs through a 4-stage smem ring.
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+#ifndef MK_BK
+#define MK_BK 64
+#endif
+constexpr int BK = MK_BK;                      // 64 (128-B rows of A) or 32 (64-B rows)
+static_assert(BK == 64 || BK == 32, "BK must be 64 or 32");
+constexpr int STAGES = (BK == 64) ? 4 : 8;
+constexpr int A_SWIZZLE_BYTES = BK * 2;        // A rows are one swizzle span wide
 constexpr int NTHREADS = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, 6-7 spare
-constexpr int A_STAGE_BYTES = BM * BK * 2;    // 16 KiB, K-major, 128-B swizzle
-constexpr int B_BOX_BYTES = BK * 64 * 2;      // 8 KiB: 64 K-rows x 64 N-cols, MN-major
-constexpr int B_STAGE_BYTES = BN * BK * 2;    // 32 KiB = 4 boxes
+constexpr int A_STAGE_BYTES = BM * BK * 2;    // K-major, BK*2-byte swizzle
+constexpr int B_BOX_BYTES = BK * 64 * 2;      // BK K-rows x 64 N-cols, MN-major, 128-B swizzle
+constexpr int B_STAGE_BYTES = BN * BK * 2;    // 4 boxes
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;   // 192 KiB, reused by copy/reduce roles
 constexpr int BAR_BYTES = 256;
@@ -85,6 +90,8 @@ struct FusedParams {
   const int* moe_ok;                     // 1 when no rank exceeds its capacity
   int moe_T, moe_topk, moe_nblk;         // tokens per rank, slots, 128-row blocks per rank
   int moe_rows_per_piece;                // destination rows per copy piece (divides 128)
+  int b_one_box;       // 1 = tmB maps are [64 cols, K, N/64 chunks (, experts)] views and a
+                       //     stage's B tile (4 column chunks) is one TMA request
 };
 
 // Workspace layout for the AG / RS / AR ops.
@@ -101,6 +108,13 @@ int device_sm_count();
 uint32_t next_epoch();
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// B-operand map over a row-major [k x n] matrix viewed as [64 cols, k, n/64 chunks]
+// (n % 64 == 0): one box {64, BK, 4} is a whole BK x 256 stage tile.
+bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n);
+// The same for the experts of a rank: [64 cols, H, N/64 chunks, E_loc].
+bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts);
+// A-operand map: box BK x BM with the swizzle that matches BK.
+bool make_map_a(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uint64_t row_bytes);
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
                  uint32_t b2);

@@ -385,6 +385,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   int pr = 1;
   while (pr < BM && static_cast<long long>(pr) * 2 * H * 2 <= 32768) pr *= 2;
   p.moe_rows_per_piece = pr;
+  p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
   p.hdr = a.hdr;
   p.wait_ns = default_wait_ns(cfg);
@@ -395,9 +396,10 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
     p.out[r] = y[r];
     p.moe_recv_x[r] = static_cast<uint8_t*>(recv_x[r]);
     p.moe_src[r] = recv_src[r];
-    if (!make_map_2d(&p.tmA[r], recv_x[r], H, cap_rows, static_cast<size_t>(H) * 2, BK, BM) ||
-        !make_map_3d(&p.tmB[r], w[r], N, H, E_loc, static_cast<size_t>(N) * 2,
-                     static_cast<size_t>(H) * N * 2, 64, BK, 1))
+    if (!make_map_a(&p.tmA[r], recv_x[r], H, cap_rows, static_cast<size_t>(H) * 2) ||
+        !(p.b_one_box ? make_map_w_chunks(&p.tmB[r], w[r], H, N, E_loc)
+                      : make_map_3d(&p.tmB[r], w[r], N, H, E_loc, static_cast<size_t>(N) * 2,
+                                    static_cast<size_t>(H) * N * 2, 64, BK, 1)))
       return MK_ERR_CUDA;
   }
   const int grid = std::max(1, std::min(grid_cap, L.max_tiles));
