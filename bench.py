@@ -279,6 +279,8 @@ def main():
     ap.add_argument("--no-other", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--n-copy", type=int, default=0)
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
     ap.add_argument("--only", choices=["rs", "ar", "moe"], default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
@@ -315,7 +317,7 @@ def main():
         c = torch.empty((M, w.n), dtype=torch.bfloat16, device=device)
         sets.append((shards, b, g, c))
     wsp = mk.Workspace(device)
-    cfg_f = mk.Config(n_copy_ctas=args.n_copy)
+    cfg_f = mk.Config(n_copy_ctas=args.n_copy, cta_pair=args.cta_pair)
 
     def step_fused(i):
         shards, b, g, c = sets[i % N_SETS]
@@ -335,8 +337,8 @@ def main():
     if st != mk.MK_OK:
         raise SystemExit(f"fused AG+GEMM reported {mk.status_string(st)} ({detail})")
 
-    cfg_g = mk.Config(mode=mk.MODE_GEMM_ONLY)
-    cfg_u = mk.Config(mode=mk.MODE_UNFUSED)
+    cfg_g = mk.Config(mode=mk.MODE_GEMM_ONLY, cta_pair=args.cta_pair)
+    cfg_u = mk.Config(mode=mk.MODE_UNFUSED, cta_pair=args.cta_pair)
 
     def step_gemm(i):
         shards, b, g, c = sets[i % N_SETS]
@@ -382,7 +384,7 @@ def main():
     other = {}
     if not args.no_other:
         other = bench_other(mk, device, stream, dist, args.other_steps, seed_off, tmax,
-                            bf16_peak, hbm_peak)
+                            bf16_peak, hbm_peak, pair=args.cta_pair)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -438,13 +440,13 @@ def run_only(args):
     else:
         w = I.RS_R8_TP8_DOWN if args.only == "rs" else I.AR_R8_DECODE
         res = bench_other(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
-                          hbm_peak, only=[w], with_moe=False)[w.name]
+                          hbm_peak, only=[w], with_moe=False, pair=args.cta_pair)[w.name]
     print(json.dumps({"only": args.only, **res}), flush=True)
     return 0
 
 
 def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak,
-                only=None, with_moe=True):
+                only=None, with_moe=True, pair=0):
     """Fused / GEMM-only / unfused timings of the RS and AR workloads."""
     out = {}
     for w in (only or (I.RS_R8_TP8_DOWN, I.AR_R8_DECODE)):
@@ -462,8 +464,9 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         fn = mk.gemm_rs if w.op == "rs" else mk.gemm_ar
         key = "c_blocks" if w.op == "rs" else "c_replicas"
         res = {}
-        for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
-                          ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        for name, cfg in (("fused", mk.Config(cta_pair=pair)),
+                          ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY, cta_pair=pair)),
+                          ("unfused", mk.Config(mode=mk.MODE_UNFUSED, cta_pair=pair))):
             def step(i, cfg=cfg):
                 a, b, o = sets[i % nsets]
                 fn(a, b, cfg=cfg, workspace=ws, stream=stream, **{key: o})

@@ -23,6 +23,7 @@ MK_BF16, MK_F32 = 0, 1
 OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR, OP_MOE = 0, 1, 2, 3
 MODE_FUSED, MODE_GEMM_ONLY, MODE_UNFUSED = 0, 1, 2
 REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL = 0, 1, 2
+PAIR_AUTO, PAIR_OFF, PAIR_ON = 0, 1, 2
 MAX_RANKS = 16
 
 
@@ -36,7 +37,7 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("n_copy_ctas", ctypes.c_int), ("n_reduce_ctas", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("mode", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
-                ("inject", ctypes.c_int), ("reduce", ctypes.c_int)]
+                ("inject", ctypes.c_int), ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
 
 @dataclasses.dataclass
@@ -51,10 +52,12 @@ class Config:
     wait_limit_ns: int = 0
     inject: int = 0
     reduce: int = 0
+    cta_pair: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.n_copy_ctas, self.n_reduce_ctas, self.max_ctas, self.group_m,
-                    self.split_k, self.mode, self.wait_limit_ns, self.inject, self.reduce)
+                    self.split_k, self.mode, self.wait_limit_ns, self.inject, self.reduce,
+                    self.cta_pair)
 
 
 _lib = None

@@ -73,12 +73,12 @@ bool make_map_a(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uin
   return r == CUDA_SUCCESS;
 }
 
-bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n) {
+bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n, uint32_t chunks) {
   auto fn = encode_fn();
   if (!fn || (n % 64)) return false;
   cuuint64_t dims[3] = {64, k, n / 64};
   cuuint64_t strides[2] = {n * 2, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BN / 64)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), chunks};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -227,6 +227,8 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.n_nblk = pl.n_nblk;
   p.n_kblk = pl.n_kblk;
   p.n_tiles = pl.n_tiles;
+  p.n_mrow = pl.n_mblk;
+  p.n_sched = pl.n_tiles;
   p.group_m = pl.group_m;
   p.split_k = pl.split_k;
   p.kps = pl.kps;
@@ -244,12 +246,55 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
 }
 
 static mk_status launch(FusedParams& p, int n_copy, int n_compute, int n_reduce, cudaStream_t s) {
+  p.pair = 0;
+  p.n_mrow = p.n_mblk;
+  p.n_sched = p.n_tiles;
   p.n_copy = n_copy;
   p.n_compute = n_compute;
   p.n_reduce = n_reduce;
   const int grid = n_copy + n_compute + n_reduce;
   if (grid <= 0) return MK_OK;
   return launch_fused(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+static int grid_cap(const mk_config* cfg);
+
+// CTA pairs where the config allows them (mk_config.cta_pair) and the device
+// co-schedules at least one pair within the grid cap.
+static bool use_pair(const mk_config* cfg, int sms) {
+  const int v = cfg ? cfg->cta_pair : 0;
+  if (v == 1) return false;
+  return std::min(max_pair_clusters(), sms / 2) > 0;
+}
+
+// Launch of compute CTAs only (no copy-role or reduce-role CTAs): CTA pairs
+// on 256 x 256 tiles when wanted and the device co-schedules them, else one
+// CTA per 128 x 256 tile.  Sets the item count for the chosen shape.
+static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t s) {
+  const int per = (p.op == OP_AG || p.mode == MK_MODE_GEMM_ONLY) ? 1 : p.P;
+  if (pair && p.op != OP_MOE) {
+    const int clusters = std::min(max_pair_clusters(), sms / 2);
+    {
+      p.pair = 1;
+      p.n_mrow = (p.n_mblk + 1) / 2;
+      p.n_sched = p.n_mrow * p.n_nblk;
+      p.n_items = p.n_sched * per;
+      const int n_pairs = std::min(clusters, p.n_items);
+      if (n_pairs <= 0) return MK_OK;
+      p.group_tiles = std::max(1, std::min(n_pairs, p.n_sched));
+      p.n_copy = 0;
+      p.n_compute = n_pairs;
+      p.n_reduce = 0;
+      return launch_fused(p, 2 * n_pairs, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
+  }
+  p.pair = 0;
+  p.n_mrow = p.n_mblk;
+  p.n_sched = p.n_mblk * p.n_nblk;
+  p.n_items = p.n_sched * per;
+  const int n = std::min(sms, p.n_items);
+  p.group_tiles = std::max(1, std::min(n, p.n_sched));
+  return launch(p, 0, n, 0, s);
 }
 
 static int grid_cap(const mk_config* cfg) {
@@ -366,15 +411,14 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     p.copy_sub = COPY_SUB_MAX;
     return launch(p, std::min(sms, std::max(1, p.n_copy_chunks * COPY_SUB_MAX)), 0, 0, s);
   }
+  // CTA pairs for every compute-only launch (not with copy-role CTAs).
+  const bool pair = use_pair(cfg, sms) && !(pl.mode == MK_MODE_FUSED && cfg && cfg->n_copy_ctas > 0);
   if (!make_map_a(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes) ||
       !make_map_a(&p.tmA[1], a_gathered, k, pl.M, row_bytes) ||
-      !(p.b_one_box ? make_map_b_chunks(&p.tmB[0], b, k, n)
+      !(p.b_one_box ? make_map_b_chunks(&p.tmB[0], b, k, n, pair ? 2 : 4)
                     : make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK)))
     return MK_ERR_CUDA;
-
-  if (pl.mode == MK_MODE_GEMM_ONLY) {
-    return launch(p, 0, std::min(sms, n_items), 0, s);
-  }
+  if (pl.mode == MK_MODE_GEMM_ONLY) return launch_compute(p, pair, sms, s);
   if (pl.mode == MK_MODE_UNFUSED) {
     const uint32_t e = p.epoch;
     mk_status st = MK_OK;
@@ -383,7 +427,7 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     if (st != MK_OK) return st;
     p.epoch = e;
     p.mode = MK_MODE_GEMM_ONLY;
-    return launch(p, 0, std::min(sms, n_items), 0, s);
+    return launch_compute(p, pair, sms, s);
   }
   if (!(cfg && cfg->n_copy_ctas > 0)) {
     // Default: the copy-in is done by two spare warps of every compute CTA,
@@ -392,8 +436,7 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     while (pr < BM && static_cast<long long>(pr) * row_bytes < 16384) pr *= 2;
     p.copy_warps = 1;
     p.copy_rows = pr;
-    const int n_compute = std::min(sms, n_items);
-    return launch(p, 0, n_compute, 0, s);
+    return launch_compute(p, pair, sms, s);
   }
   int n_copy = cfg->n_copy_ctas;
   n_copy = std::min(n_copy, p.n_copy_chunks * COPY_SUB_MAX);
@@ -436,30 +479,26 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   p.rows_per_owner = static_cast<int>(m / R);
   if (op == OP_AR) p.rows_per_owner = static_cast<int>(m);
   p.b_one_box = (n % 64 == 0) ? 1 : 0;
+  // CTA pairs for every compute-only launch (not with reduce-role CTAs).
+  const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last);
   for (int r = 0; r < R; ++r) {
     p.out[r] = outs[r];
     if (!make_map_a(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2) ||
-        !(p.b_one_box ? make_map_b_chunks(&p.tmB[r], b[r], k, n)
+        !(p.b_one_box ? make_map_b_chunks(&p.tmB[r], b[r], k, n, pair ? 2 : 4)
                       : make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK)))
       return MK_ERR_CUDA;
   }
-  if (pl.mode == MK_MODE_GEMM_ONLY) {
-    p.n_items = pl.n_tiles;
-    return launch(p, 0, std::min(sms, pl.n_tiles), 0, s);
-  }
-  p.n_items = pl.n_tiles * pl.P;
+  if (pl.mode == MK_MODE_GEMM_ONLY) return launch_compute(p, pair, sms, s);
   if (pl.mode == MK_MODE_UNFUSED) {
     const uint32_t e = p.epoch;
-    mk_status st = launch(p, 0, std::min(sms, p.n_items), 0, s);
+    mk_status st = launch_compute(p, pair, sms, s);
     if (st != MK_OK) return st;
     p.epoch = e;
+    p.n_items = pl.n_tiles * pl.P;
     return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
   }
-  if (pl.chain || pl.last) {
-    const int n_compute = std::min(sms, p.n_items);
-    p.group_tiles = std::max(1, std::min(n_compute, pl.n_tiles));
-    return launch(p, 0, n_compute, 0, s);
-  }
+  if (pl.chain || pl.last) return launch_compute(p, pair, sms, s);
+  p.n_items = pl.n_tiles * pl.P;
   int n_red = cfg->n_reduce_ctas;
   n_red = std::min(n_red, pl.n_tiles);
   n_red = std::min(n_red, sms - 1);

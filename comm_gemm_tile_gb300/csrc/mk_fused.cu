@@ -28,6 +28,7 @@
 namespace mk {
 
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
+constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(2 * BM, BN, false, true);   // M = 256 across the pair
 
 // ------------------------------------------------------------------ errors / waits
 __device__ __forceinline__ bool aborted(const FusedParams& p) {
@@ -126,13 +127,15 @@ struct Item {
   int out_row0;     // output row of tile row 0
 };
 
-// Grouped raster: group_m m-blocks per group, n-blocks outer inside a group.
+// Grouped raster over (m-position, n-block): group_m m-positions per group,
+// n-blocks outer inside a group.  An m-position is an m-block, or with CTA
+// pairs the m-block pair {2q, 2q+1}.
 __device__ __forceinline__ void raster(const FusedParams& p, int q, int& mb, int& nb) {
   const int gm = p.group_m;
   const int per_group = gm * p.n_nblk;
   const int g = q / per_group;
   const int first_m = g * gm;
-  const int gsz = min(p.n_mblk - first_m, gm);
+  const int gsz = min(p.n_mrow - first_m, gm);
   const int r = q - g * per_group;
   mb = first_m + r % gsz;
   nb = r / gsz;
@@ -163,7 +166,20 @@ __device__ __forceinline__ bool ag_chunk_fully_local(const FusedParams& p, int m
   return lo >= l0 && hi <= l0 + p.m_r;
 }
 
-__device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
+// Item i of the work list, as seen by CTA `rank` of a pair (0 without pairs).
+// With pairs an item covers two m-blocks; CTA r takes m-position 2q + r.  A
+// half past the last m-block is empty: its loads read the zero fill beyond
+// the matrix and it stores nothing and touches no flag.
+__device__ __forceinline__ void empty_half(Item& it, int mb) {
+  it.mb = mb;
+  it.slot = -1;
+  it.wait_chunk = -1;
+  it.arow = mb * BM;
+  it.out_row0 = mb * BM;
+  it.row_hi = 0;
+}
+
+__device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, int rank = 0) {
   it.bz = -1;
   it.slot = -1;
   it.wait_chunk = -1;
@@ -175,8 +191,16 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
   it.row_lo = 0;
   it.row_hi = BM;
   if (p.op == OP_AG) {
-    const int pos = i / p.n_nblk;
+    int pos = i / p.n_nblk;
     it.nb = i - pos * p.n_nblk;
+    if (p.pair) {
+      pos = 2 * pos + rank;
+      if (pos >= p.n_mblk) {
+        it.amap = 1;
+        empty_half(it, pos);
+        return true;
+      }
+    }
     it.mb = ag_compute_mb(p, pos);
     it.out_row0 = it.mb * BM;
     if (p.mode == MK_MODE_FUSED && ag_chunk_fully_local(p, it.mb)) {
@@ -194,6 +218,7 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
     if (p.mode == MK_MODE_GEMM_ONLY) {
       raster(p, i, it.mb, it.nb);
       it.nseg = p.R;
+      if (p.pair) it.mb = 2 * it.mb + rank;
     } else {
       int q, part;
       if (p.chain) {
@@ -201,7 +226,7 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
         // then part 1, ... so a tile's running sum moves on one part per round.
         const int G = p.group_tiles;
         const int g = i / (G * p.P);
-        const int Gg = min(G, p.n_tiles - g * G);
+        const int Gg = min(G, p.n_sched - g * G);
         const int iin = i - g * G * p.P;
         part = iin / Gg;
         q = g * G + (iin - part * Gg);
@@ -210,12 +235,17 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
         part = i - q * p.P;
       }
       raster(p, q, it.mb, it.nb);
+      if (p.pair) it.mb = 2 * it.mb + rank;
       const int r = part / p.split_k, ks = part - r * p.split_k;
       it.amap = r;
       it.bmap = r;
       it.kb0 = ks * p.kps;
       it.nkb = min(p.kps, p.n_kblk - it.kb0);
       it.slot = (it.mb * p.n_nblk + it.nb) * p.P + part;
+    }
+    if (it.mb >= p.n_mblk) {
+      empty_half(it, it.mb);
+      return true;
     }
     it.arow = it.mb * BM;
     it.out_row0 = it.mb * BM;
@@ -239,9 +269,12 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it) {
 
 // ------------------------------------------------------------------ compute role
 // Barrier block of a compute CTA (8-byte mbarriers), then the TMEM base slot.
+// With pairs, both CTAs lay it out alike: the leader's full and TMEM-empty
+// barriers gate the pair, each CTA's empty and TMEM-full barriers are
+// signalled by the leader's multicast commits.
 constexpr uint32_t BAR_FULL = 0;
-constexpr uint32_t BAR_EMPTY = BAR_FULL + 8u * STAGES;
-constexpr uint32_t BAR_TFULL = BAR_EMPTY + 8u * STAGES;
+constexpr uint32_t BAR_EMPTY = BAR_FULL + 8u * MAX_STAGES;
+constexpr uint32_t BAR_TFULL = BAR_EMPTY + 8u * MAX_STAGES;
 constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 16u;
 constexpr uint32_t BAR_DRAIN = BAR_TEMPTY + 16u;
 constexpr uint32_t BAR_PDONE = BAR_DRAIN + 8u;
@@ -259,6 +292,13 @@ struct ComputeSmem {
   __device__ __forceinline__ uint32_t pdone(int b) const { return bars + BAR_PDONE + 8u * b; }
 };
 
+// Ring geometry of the two compute variants.
+template <bool PAIR>
+struct Ring {
+  static constexpr int stages = PAIR ? PSTAGES : STAGES;
+  static constexpr uint32_t stage_bytes = PAIR ? PSTAGE_BYTES : STAGE_BYTES;
+};
+
 __device__ __forceinline__ int n_items_for(const FusedParams& p) {
   if (p.op == OP_MOE && p.mode == MK_MODE_UNFUSED) return 0;   // baseline: dispatch copy only
   if (p.op == OP_MOE) return min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)) ,
@@ -266,7 +306,13 @@ __device__ __forceinline__ int n_items_for(const FusedParams& p) {
   return p.n_items;
 }
 
-__device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
+// TMA producer (one thread).  With pairs each CTA loads its own 128 rows of A
+// and its 128 of the tile's 256 B columns into its own ring, completing on
+// the leader's full barrier, which the leader arms with both CTAs' bytes.
+template <bool PAIR>
+__device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, uint32_t rank) {
+  constexpr int NST = Ring<PAIR>::stages;
+  constexpr uint32_t SB = Ring<PAIR>::stage_bytes;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;
@@ -274,7 +320,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
   bool counters_ready = false;
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
-    decode(p, i, it);
+    decode(p, i, it, static_cast<int>(rank));
     if (p.op == OP_MOE && p.mode == MK_MODE_FUSED) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       const int d = it.amap;
@@ -304,11 +350,31 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
       const CUtensorMap* mbm = &p.tmB[it.bmap + seg];
       for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
         if (!wait_bar(p, S.empty(stage), phase ^ 1u, WHERE_PRODUCER, i)) goto done;
-        const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * STAGE_BYTES;
+        const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB;
         const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+        const int n0 = it.nb * BN;
+        if constexpr (PAIR) {
+          const uint32_t fb = mapa_shared(S.full(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(S.full(stage), 2u * PSTAGE_BYTES);
+          tma_load_2d_pair(a_dst, ma, fb, kb * BK, it.arow);
+          if (p.b_one_box) {
+            tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, n0 / 64 + 2 * static_cast<int>(rank));
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, n0 + 128 * static_cast<int>(rank) + 64 * j,
+                               kb * BK);
+          }
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         mbar_arrive_expect_tx(S.full(stage), STAGE_BYTES);
         tma_load_2d(a_dst, ma, S.full(stage), kb * BK, it.arow);
-        const int n0 = it.nb * BN;
         if (p.b_one_box) {
           // the whole BK x 256 B tile in one request (4 column chunks of 64)
           if (it.bz < 0) tma_load_3d(b_dst, mbm, S.full(stage), 0, kb * BK, n0 / 64);
@@ -324,7 +390,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
         }
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1u;
         }
@@ -332,13 +398,23 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid) {
     }
   }
 done:
-  // Every load issued must have landed before the CTA may exit.
-  for (int s = 0; s < STAGES; ++s)
+  // Every load issued must have landed before the CTA may exit.  With pairs
+  // the leader's full barriers also count the peer's loads; the peer's own
+  // loads of a stage the leader never armed (abort only) are waited out by
+  // the pause before the pair's final cluster barrier.
+  if (PAIR && rank != 0) return;
+  for (int s = 0; s < NST; ++s)
     if (issued_mask & (1u << s))
       wait_bar(p, S.full(s), (issued_par >> s) & 1u, WHERE_DRAIN, s, /*honor_abort=*/false);
 }
 
+// MMA issuer (one thread; with pairs only the leader's).  A pair's MMA has
+// M = 256: rows 0-127 from the leader's A stage, 128-255 from the peer's, and
+// the B columns from both CTAs' halves; each CTA's TMEM receives its own rows.
+template <bool PAIR>
 __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
+  constexpr int NST = Ring<PAIR>::stages;
+  constexpr uint32_t SB = Ring<PAIR>::stage_bytes;
   int stage = 0;
   uint32_t phase = 0;
   int buf = 0;
@@ -356,7 +432,7 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
         for (int kb = 0; kb < it.nkb; ++kb) {
           if (!wait_bar(p, S.full(stage), phase, WHERE_MMA, i)) goto done;
           tc_fence_after();
-          const uint32_t a_addr = S.ring + static_cast<uint32_t>(stage) * STAGE_BYTES;
+          const uint32_t a_addr = S.ring + static_cast<uint32_t>(stage) * SB;
           const uint32_t b_addr = a_addr + A_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
@@ -366,18 +442,21 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
             // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
             // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
             const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
+            if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, acc);
+            else tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
             acc = 1;
           }
-          tc_commit(S.empty(stage));
-          if (++stage == STAGES) {
+          if constexpr (PAIR) tc_commit_pair(S.empty(stage), 3);
+          else tc_commit(S.empty(stage));
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
     }
-    tc_commit(S.tfull(buf));
+    if constexpr (PAIR) tc_commit_pair(S.tfull(buf), 3);
+    else tc_commit(S.tfull(buf));
     if (++buf == 2) {
       buf = 0;
       acc_phase ^= 1u;
@@ -385,7 +464,8 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
   }
 done:
   // Every MMA issued must have completed before tensor memory is freed.
-  tc_commit(S.drain());
+  if constexpr (PAIR) tc_commit_pair(S.drain(), 1);
+  else tc_commit(S.drain());
   wait_bar(p, S.drain(), 0, WHERE_DRAIN, 0, /*honor_abort=*/false);
 }
 
@@ -479,7 +559,18 @@ __device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, i
   }
 }
 
-__device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
+// An epilogue warp is done reading TMEM buffer `buf`: arrive on the barrier
+// that lets the MMA issuer overwrite it (the leader's, with pairs: it counts
+// the four epilogue warps of both CTAs).
+template <bool PAIR>
+__device__ __forceinline__ void release_tmem(const ComputeSmem& S, int buf, uint32_t rank) {
+  if (PAIR && rank != 0) mbar_arrive_cluster(mapa_shared(S.tempty(buf), 0));
+  else mbar_arrive(S.tempty(buf));
+}
+
+template <bool PAIR>
+__device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid,
+                         uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
   const int trow = quarter * 32 + lane;
@@ -490,7 +581,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   const int n_items = n_items_for(p);
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
-    decode(p, i, it);
+    decode(p, i, it, static_cast<int>(rank));
     if (!wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i)) return;
     tc_fence_after();
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -573,7 +664,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(S.tempty(buf));   // tensor memory is free again
+      if (lane == 0) release_tmem<PAIR>(S, buf, rank);   // tensor memory is free again
       __threadfence();
       __syncwarp();
       const int tile = it.slot / p.P;
@@ -641,7 +732,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(S.tempty(buf));
+      release_tmem<PAIR>(S, buf, rank);
       if (it.slot >= 0) mbar_arrive(S.pdone(buf));
     }
     if (it.slot >= 0 && warp == 2 && lane == 0) {
@@ -678,17 +769,17 @@ __device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, l
 }
 
 // AG copy-in by warps 6-7 of every compute CTA.  The work list is (chunk in
-// copy order, piece of copy_rows rows); worker w = 2*cid + (warp - 6) takes
-// pieces w, w + 2*n_compute, ... so all workers move neighbouring pieces of
+// copy order, piece of copy_rows rows); worker w = 2*cta + (warp - 6) takes
+// pieces w, w + 2*n_ctas, ... so all workers move neighbouring pieces of
 // the same few chunks at a time.  Each lane streams 16-byte vectors, 16 loads
 // in flight; after a piece every lane fences and lane 0 bumps the chunk's
 // counter.  Copy warps never wait on anything, so they always progress.
 constexpr int CW_UNROLL = 16;
 
-__device__ void copy_warps_role(const FusedParams& p, int cid) {
+__device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const int lane = threadIdx.x & 31;
-  const int worker = cid * 2 + ((threadIdx.x >> 5) - 6);
-  const int n_workers = p.n_compute * 2;
+  const int worker = cta * 2 + ((threadIdx.x >> 5) - 6);
+  const int n_workers = n_ctas * 2;
   const int pr = p.copy_rows;
   const int J = BM / pr;
   const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * J;
@@ -800,20 +891,23 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cid) {
   }
 }
 
+// Compute CTA (cid = compute index; with pairs, the pair index).
+template <bool PAIR>
 __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
   ComputeSmem S;
   S.ring = smem_u32(smem);
   S.bars = smem_u32(smem + RING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + TMEM_SLOT);
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < Ring<PAIR>::stages; ++s) {
       mbar_init(S.full(s), 1);
       mbar_init(S.empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(S.tfull(b), 1);
-      mbar_init(S.tempty(b), 4);
+      mbar_init(S.tempty(b), PAIR ? 8 : 4);
     }
     mbar_init(S.drain(), 1);
     for (int b = 0; b < 2; ++b) mbar_init(S.pdone(b), 4);
@@ -826,35 +920,56 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();   // barriers of both CTAs initialised, TMEM allocated
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer(p, S, cid);
+    if (lane == 0) producer<PAIR>(p, S, cid, rank);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(p, S, tmem_base, cid);
+    if (lane == 0 && rank == 0) mma_issuer<PAIR>(p, S, tmem_base, cid);
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
-    epilogue(p, S, tmem_base, cid);
+    epilogue<PAIR>(p, S, tmem_base, cid, rank);
     __syncwarp();
   } else if (p.op == OP_MOE) {
     moe_copy_warps_role(p, cid);
     __syncwarp();
   } else if (p.copy_warps) {
-    copy_warps_role(p, cid);
+    if constexpr (PAIR) copy_warps_role(p, 2 * cid + static_cast<int>(rank), 2 * p.n_compute);
+    else copy_warps_role(p, cid, p.n_compute);
     __syncwarp();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    // After an abort a CTA of the pair may still have loads in flight into
+    // its ring that the leader never armed; they land within microseconds.
+    if (threadIdx.x == 0 && aborted(p)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
+    }
+    __syncwarp();
+    // Neither CTA leaves (or frees TMEM) while the leader's MMAs may still
+    // read the peer's ring or write its tensor memory.
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -1197,15 +1312,23 @@ __device__ void reduce_role(const FusedParams& p, uint8_t* smem, int rid) {
 }
 
 // ------------------------------------------------------------------ the kernel
+// PAIR = false: one CTA per SM, roles by ticket.  PAIR = true: launched as
+// clusters of two; every CTA computes (no copy-role or reduce-role CTAs) and
+// all tcgen05 work of the launch uses cta_group::2.
+template <bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_ticket;
-  if (threadIdx.x == 0) {
-    const uint32_t t = atomicAdd(&p.hdr[HDR_TICKET], 1u);
-    if (t == gridDim.x - 1) atomicExch(&p.hdr[HDR_TICKET], 0u);
-    s_ticket = t;
+  if constexpr (PAIR) {
+    if (threadIdx.x == 0) s_ticket = blockIdx.x;
+  } else {
+    if (threadIdx.x == 0) {
+      const uint32_t t = atomicAdd(&p.hdr[HDR_TICKET], 1u);
+      if (t == gridDim.x - 1) atomicExch(&p.hdr[HDR_TICKET], 0u);
+      s_ticket = t;
+    }
   }
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
@@ -1221,12 +1344,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
     __syncthreads();
     if (threadIdx.x == 0) st_release_gpu(&p.hdr[HDR_READY], p.epoch);
   }
-  if (t < p.n_copy) {
-    copy_role(p, smem, t);
-  } else if (t < p.n_copy + p.n_compute) {
-    compute_role(p, smem, t - p.n_copy);
+  if constexpr (PAIR) {
+    compute_role<true>(p, smem, t >> 1);
   } else {
-    reduce_role(p, smem, t - p.n_copy - p.n_compute);
+    if (t < p.n_copy) {
+      copy_role(p, smem, t);
+    } else if (t < p.n_copy + p.n_compute) {
+      compute_role<false>(p, smem, t - p.n_copy);
+    } else {
+      reduce_role(p, smem, t - p.n_copy - p.n_compute);
+    }
   }
 }
 
@@ -1236,12 +1363,55 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(mk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(mk_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mk_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  mk_fused_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  if (!p.pair) {
+    mk_fused_kernel<false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mk_fused_kernel<true>, p);
+}
+
+int max_pair_clusters() {
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cached_dev == dev) return cached;
+  if (cudaFuncSetAttribute(mk_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mk_fused_kernel<true>, &cfg) != cudaSuccess) n = 0;
+  cached_dev = dev;
+  cached = n;
+  return n;
 }
 
 }  // namespace mk

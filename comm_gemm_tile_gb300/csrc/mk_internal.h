@@ -28,6 +28,12 @@ constexpr int B_BOX_BYTES = BK * 64 * 2;      // BK K-rows x 64 N-cols, MN-major
 constexpr int B_STAGE_BYTES = BN * BK * 2;    // 4 boxes
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;   // 192 KiB, reused by copy/reduce roles
+// CTA pairs (tcgen05 cta_group::2): a pair computes one 256 x 256 tile, each
+// CTA holding its 128 rows of A and 128 of the 256 B columns per stage, so a
+// stage is 32 KiB (BK = 64) and the same ring holds 6 of them.
+constexpr int PSTAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES / 2;
+constexpr int PSTAGES = RING_BYTES / PSTAGE_BYTES;
+constexpr int MAX_STAGES = STAGES > PSTAGES ? STAGES : PSTAGES;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
@@ -91,7 +97,11 @@ struct FusedParams {
   int moe_T, moe_topk, moe_nblk;         // tokens per rank, slots, 128-row blocks per rank
   int moe_rows_per_piece;                // destination rows per copy piece (divides 128)
   int b_one_box;       // 1 = tmB maps are [64 cols, K, N/64 chunks (, experts)] views and a
-                       //     stage's B tile (4 column chunks) is one TMA request
+                       //     stage's B tile (4 column chunks, 2 per CTA of a pair) is one TMA request
+  int pair;            // 1 = launched as clusters of 2 CTAs sharing 256 x 256 tiles; items then
+                       //     run over m-block pairs and n_compute counts pairs
+  int n_mrow;          // m-positions of the raster: n_mblk, or ceil(n_mblk / 2) with pairs
+  int n_sched;         // RS/AR: scheduled tiles (n_mrow * n_nblk)
 };
 
 // Workspace layout for the AG / RS / AR ops.
@@ -101,7 +111,10 @@ struct WsLayout {
 
 inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
+// grid = CTAs (with pairs: 2 x pairs, launched as clusters of two).
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
+// Clusters of two CTAs of the fused kernel that fit on the device at once (0 on error).
+int max_pair_clusters();
 constexpr int MOE_MAX_E = 256;        // experts in total (R * E_loc)
 constexpr int MOE_MAX_TOPK = 8;
 int device_sm_count();
@@ -109,8 +122,9 @@ uint32_t next_epoch();
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 // B-operand map over a row-major [k x n] matrix viewed as [64 cols, k, n/64 chunks]
-// (n % 64 == 0): one box {64, BK, 4} is a whole BK x 256 stage tile.
-bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n);
+// (n % 64 == 0): one box {64, BK, chunks} is a BK x (64 * chunks) stage tile
+// (4 chunks: a single CTA's 256 columns; 2: one CTA's half of a pair's).
+bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n, uint32_t chunks = BN / 64);
 // The same for the experts of a rank: [64 cols, H, N/64 chunks, E_loc].
 bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts);
 // A-operand map: box BK x BM with the swizzle that matches BK.

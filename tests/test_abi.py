@@ -105,6 +105,6 @@ def test_argument_validation_without_launch(L):
 
 
 def test_config_struct_layout():
-    assert ctypes.sizeof(mk._Cfg) == 40
+    assert ctypes.sizeof(mk._Cfg) == 48
     assert mk._Cfg.wait_limit_ns.offset == 24 and mk._Cfg.inject.offset == 32
-    assert mk._Cfg.reduce.offset == 36
+    assert mk._Cfg.reduce.offset == 36 and mk._Cfg.cta_pair.offset == 40
