@@ -86,12 +86,13 @@ bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n,
   return r == CUDA_SUCCESS;
 }
 
-bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts) {
+bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts,
+                       uint32_t chunks) {
   auto fn = encode_fn();
   if (!fn || (n % 64)) return false;
   cuuint64_t dims[4] = {64, h, n / 64, experts};
   cuuint64_t strides[3] = {n * 2, 128, h * n * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BN / 64), 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK), chunks, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -122,6 +123,11 @@ static inline bool buf_ok(const void* p, long long elems) {
   if (elems > 0 && !p) return false;
   return aligned16(p);
 }
+
+// Target size of one copy-warp piece of the gathered A (whole rows, power-of-two count).
+#ifndef MK_CW_PIECE_BYTES
+#define MK_CW_PIECE_BYTES 16384
+#endif
 
 // SM count used for the device-independent parts of the plan (split-K), so
 // that mk_workspace_size gives the same answer with or without a GPU.
@@ -257,11 +263,9 @@ static mk_status launch(FusedParams& p, int n_copy, int n_compute, int n_reduce,
   return launch_fused(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 
-static int grid_cap(const mk_config* cfg);
-
 // CTA pairs where the config allows them (mk_config.cta_pair) and the device
 // co-schedules at least one pair within the grid cap.
-static bool use_pair(const mk_config* cfg, int sms) {
+bool use_pair(const mk_config* cfg, int sms) {
   const int v = cfg ? cfg->cta_pair : 0;
   if (v == 1) return false;
   return std::min(max_pair_clusters(), sms / 2) > 0;
@@ -297,7 +301,7 @@ static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t
   return launch(p, 0, n, 0, s);
 }
 
-static int grid_cap(const mk_config* cfg) {
+int grid_cap(const mk_config* cfg) {
   int sms = device_sm_count();
   if (sms <= 0) return 0;
   if (cfg && cfg->max_ctas > 0) sms = std::min(sms, cfg->max_ctas);
@@ -433,9 +437,12 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     // Default: the copy-in is done by two spare warps of every compute CTA,
     // in pieces of about 16 KiB (rows of the gathered A), so every SM computes.
     int pr = 1;
-    while (pr < BM && static_cast<long long>(pr) * row_bytes < 16384) pr *= 2;
+    while (pr < BM && static_cast<long long>(pr) * row_bytes < MK_CW_PIECE_BYTES) pr *= 2;
     p.copy_warps = 1;
     p.copy_rows = pr;
+    // two copy warps per CTA move the 7/8 of A in well under the GEMM's time;
+    // more of them measured no faster and compete with the operand loads
+    p.n_cw = std::min(2, N_COPY_WARPS);
     return launch_compute(p, pair, sms, s);
   }
   int n_copy = cfg->n_copy_ctas;

@@ -253,15 +253,16 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
     return true;
   }
   // OP_MOE: entry i of the tile table written by the routing kernel:
-  // {dest rank d, local expert l, first row of the tile in recv_x[d], rows valid, n-block}
+  // {dest rank d, local expert l, first row of the tile in recv_x[d], rows valid, n-block}.
+  // With pairs an entry spans up to 256 rows; CTA r takes rows 128r .. 128r+127 of it.
   const int* e = p.moe_tiles + 5 * i;
   const int d = e[0];
   it.amap = d;
   it.bmap = d;
   it.bz = e[1];
-  it.arow = e[2];
-  it.out_row0 = e[2];
-  it.row_hi = e[3];
+  it.arow = e[2] + (p.pair ? BM * rank : 0);
+  it.out_row0 = it.arow;
+  it.row_hi = p.pair ? max(0, min(BM, e[3] - BM * rank)) : e[3];
   it.nb = e[4];
   it.mb = d;  // output buffer index
   return true;
@@ -321,8 +322,9 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it, static_cast<int>(rank));
-    if (p.op == OP_MOE && p.mode == MK_MODE_FUSED) {
+    if (p.op == OP_MOE && p.mode == MK_MODE_FUSED && it.row_hi > 0) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
+      // (an empty pair half covers no rows and waits for nothing)
       const int d = it.amap;
       const int rc = p.moe_recv_counts[d];
       const int b0 = it.arow / BM, b1 = (it.arow + it.row_hi - 1) / BM;
@@ -357,13 +359,18 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
           const uint32_t fb = mapa_shared(S.full(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(S.full(stage), 2u * PSTAGE_BYTES);
           tma_load_2d_pair(a_dst, ma, fb, kb * BK, it.arow);
+          const int c0 = n0 / 64 + 2 * static_cast<int>(rank);   // this CTA's first column chunk
           if (p.b_one_box) {
-            tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, n0 / 64 + 2 * static_cast<int>(rank));
+            if (it.bz < 0) tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, c0);
+            else tma_load_4d_pair(b_dst, mbm, fb, 0, kb * BK, c0, it.bz);
+          } else if (it.bz < 0) {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, n0 + 128 * static_cast<int>(rank) + 64 * j,
-                               kb * BK);
+              tma_load_3d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK, it.bz);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -768,23 +775,38 @@ __device__ __forceinline__ bool copy_run(const FusedParams& p, long long& row, l
   return false;
 }
 
-// AG copy-in by warps 6-7 of every compute CTA.  The work list is (chunk in
-// copy order, piece of copy_rows rows); worker w = 2*cta + (warp - 6) takes
-// pieces w, w + 2*n_ctas, ... so all workers move neighbouring pieces of
+// AG copy-in by the copy warps (6 and up) of every compute CTA.  The work list is (chunk in
+// copy order, piece of copy_rows rows); worker w = n_cw*cta + (warp - 6) takes
+// pieces w, w + n_cw*n_ctas, ... so all workers move neighbouring pieces of
 // the same few chunks at a time.  Each lane streams 16-byte vectors, 16 loads
 // in flight; after a piece every lane fences and lane 0 bumps the chunk's
 // counter.  Copy warps never wait on anything, so they always progress.
-constexpr int CW_UNROLL = 16;
+#ifndef MK_CW_UNROLL
+#define MK_CW_UNROLL 16
+#endif
+constexpr int CW_UNROLL = MK_CW_UNROLL;
+#ifndef MK_MOE_CW_UNROLL
+#define MK_MOE_CW_UNROLL MK_CW_UNROLL
+#endif
+constexpr int MOE_CW_UNROLL = MK_MOE_CW_UNROLL;   // 16-byte loads in flight per lane (MoE rows)
+// MK_CW_HINT = 1: shard reads marked L2 evict_first, gathered-A writes evict_last.
+#ifndef MK_CW_HINT
+#define MK_CW_HINT 0
+#endif
 
 __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const int lane = threadIdx.x & 31;
-  const int worker = cta * 2 + ((threadIdx.x >> 5) - 6);
-  const int n_workers = n_ctas * 2;
+  if ((threadIdx.x >> 5) - 6 >= p.n_cw) return;
+  const int worker = cta * p.n_cw + ((threadIdx.x >> 5) - 6);
+  const int n_workers = n_ctas * p.n_cw;
   const int pr = p.copy_rows;
   const int J = BM / pr;
   const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * J;
   const size_t rb = static_cast<size_t>(p.K) * 2;
   bool skip_first = (p.inject == 1 && worker == 0);
+#if MK_CW_HINT
+  const uint64_t pol_src = l2_policy_evict_first(), pol_dst = l2_policy_evict_last();
+#endif
   {
     int ok = 1;
     if (lane == 0) ok = wait_flag(p, &p.hdr[HDR_READY], WHERE_COPY, worker) ? 1 : 0;
@@ -810,12 +832,20 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
 #pragma unroll
         for (int u = 0; u < CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
+#if MK_CW_HINT
+          if (idx < n16) v[u] = ld_nc_v4_pol(src + idx * 16, pol_src);
+#else
           if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
+#endif
         }
 #pragma unroll
         for (int u = 0; u < CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
+#if MK_CW_HINT
+          if (idx < n16) st_global_v4_pol(dst + idx * 16, v[u], pol_dst);
+#else
           if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+#endif
         }
       }
       row = run_hi;
@@ -830,15 +860,16 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   }
 }
 
-// MoE dispatch by warps 6-7 of every compute CTA: destination rows of all
+// MoE dispatch by the copy warps of every compute CTA: destination rows of all
 // ranks, rank-major, in pieces of moe_rows_per_piece rows inside one 128-row
 // block; row `row` of rank d is a bit copy of token g = recv_src[d][row] / topk
 // (rank g / T, token g % T).  After a piece every lane fences and lane 0 adds
 // the piece's rows to the block's counter (zeroed by the offsets kernel).
-__device__ void moe_copy_warps_role(const FusedParams& p, int cid) {
+__device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const int lane = threadIdx.x & 31;
-  const int worker = cid * 2 + ((threadIdx.x >> 5) - 6);
-  const int n_workers = p.n_compute * 2;
+  if ((threadIdx.x >> 5) - 6 >= p.n_cw) return;
+  const int worker = cta * p.n_cw + ((threadIdx.x >> 5) - 6);
+  const int n_workers = n_ctas * p.n_cw;
   if (p.mode == MK_MODE_GEMM_ONLY) return;   // baseline: recv_x is already filled
   if (*reinterpret_cast<const volatile int*>(p.moe_ok) == 0) return;
   const int pr = p.moe_rows_per_piece;
@@ -864,15 +895,15 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cid) {
       const int r = g / p.moe_T, t = g - r * p.moe_T;
       const uint8_t* sp = p.shard[r] + static_cast<size_t>(t) * rb;
       uint8_t* dp = p.moe_recv_x[d] + static_cast<size_t>(row0 + rr) * rb;
-      for (size_t i0 = lane; i0 < n16; i0 += 32 * CW_UNROLL) {
-        uint4 v[CW_UNROLL];
+      for (size_t i0 = lane; i0 < n16; i0 += 32 * MOE_CW_UNROLL) {
+        uint4 v[MOE_CW_UNROLL];
 #pragma unroll
-        for (int u = 0; u < CW_UNROLL; ++u) {
+        for (int u = 0; u < MOE_CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
           if (idx < n16) v[u] = ld_nc_v4(sp + idx * 16);
         }
 #pragma unroll
-        for (int u = 0; u < CW_UNROLL; ++u) {
+        for (int u = 0; u < MOE_CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
           if (idx < n16) st_global_v4(dp + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
         }
@@ -944,7 +975,8 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     epilogue<PAIR>(p, S, tmem_base, cid, rank);
     __syncwarp();
   } else if (p.op == OP_MOE) {
-    moe_copy_warps_role(p, cid);
+    if constexpr (PAIR) moe_copy_warps_role(p, 2 * cid + static_cast<int>(rank), 2 * p.n_compute);
+    else moe_copy_warps_role(p, cid, p.n_compute);
     __syncwarp();
   } else if (p.copy_warps) {
     if constexpr (PAIR) copy_warps_role(p, 2 * cid + static_cast<int>(rank), 2 * p.n_compute);

@@ -22,7 +22,13 @@ constexpr int BK = MK_BK;                      // 64 (128-B rows of A) or 32 (64
 static_assert(BK == 64 || BK == 32, "BK must be 64 or 32");
 constexpr int STAGES = (BK == 64) ? 4 : 8;
 constexpr int A_SWIZZLE_BYTES = BK * 2;        // A rows are one swizzle span wide
-constexpr int NTHREADS = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, 6-7 spare
+#ifndef MK_NTHREADS
+#define MK_NTHREADS 384
+#endif
+// warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6.. copy (AG / MoE copy-in)
+constexpr int NTHREADS = MK_NTHREADS;
+constexpr int N_COPY_WARPS = NTHREADS / 32 - 6;
+static_assert(N_COPY_WARPS >= 1 && NTHREADS % 32 == 0, "need at least one copy warp");
 constexpr int A_STAGE_BYTES = BM * BK * 2;    // K-major, BK*2-byte swizzle
 constexpr int B_BOX_BYTES = BK * 64 * 2;      // BK K-rows x 64 N-cols, MN-major, 128-B swizzle
 constexpr int B_STAGE_BYTES = BN * BK * 2;    // 4 boxes
@@ -85,10 +91,11 @@ struct FusedParams {
   int last_arrival;    // RS/AR: 1 = staged partials, the epilogue warp that completes a tile
                        //        quarter (32 rows) sums its partials (with chain = 0)
   int group_tiles;     // RS/AR chain: tiles per scheduling group
-  int copy_warps;      // AG: 1 = copy-in done by warps 6-7 of every compute CTA, one
+  int copy_warps;      // AG: 1 = copy-in done by the copy warps of every compute CTA, one
                        //     piece counter per chunk (zeroed at kernel start by the CTA
                        //     with ticket 0); 0 = copy-role CTAs with per-sub-chunk flags
   int copy_rows;       // AG copy warps: gathered rows per piece (power of 2 dividing 128)
+  int n_cw;            // copy warps per CTA that take part (1 .. N_COPY_WARPS)
   // MoE dispatch (copy warps) and grouped GEMM
   uint8_t* moe_recv_x[MK_MAX_RANKS];     // destination rows, [cap x H] per rank
   const int* moe_src[MK_MAX_RANKS];      // recv_src per rank: g*topk + slot of each row
@@ -126,7 +133,12 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 // (4 chunks: a single CTA's 256 columns; 2: one CTA's half of a pair's).
 bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n, uint32_t chunks = BN / 64);
 // The same for the experts of a rank: [64 cols, H, N/64 chunks, E_loc].
-bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts);
+bool make_map_w_chunks(CUtensorMap* m, const void* base, uint64_t h, uint64_t n, uint64_t experts,
+                       uint32_t chunks = BN / 64);
+// Grid cap for a call (SM count, or mk_config.max_ctas when smaller); 0 without a device.
+int grid_cap(const mk_config* cfg);
+// CTA pairs where mk_config.cta_pair allows them and at least one pair fits the grid cap.
+bool use_pair(const mk_config* cfg, int sms);
 // A-operand map: box BK x BM with the swizzle that matches BK.
 bool make_map_a(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uint64_t row_bytes);
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -51,6 +51,7 @@ struct MoeArgs {
   uint32_t* blocks;   // [R x nblk] arrival counters
   uint32_t* hdr;      // workspace header (status)
   int R, E_loc, E, topk, T, n_nblk, nblk, C;
+  int tile_rows;      // rows per tile-table entry: 128, or 256 for CTA pairs
   long long cap;
 };
 
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(256) moe_offsets_kernel(const __grid_constant_
     int acc = 0;
     for (int k = 0; k < R * El; ++k) {
       a.tprefix[k] = acc;
-      if (ok) acc += ((a.totals[k] + BM - 1) / BM) * a.n_nblk;
+      if (ok) acc += ((a.totals[k] + a.tile_rows - 1) / a.tile_rows) * a.n_nblk;
     }
     a.tprefix[R * El] = acc;
     a.misc[MISC_NTILES] = static_cast<uint32_t>(acc);
@@ -227,8 +228,8 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
     int* ent = a.tiles + 5 * q;
     ent[0] = d;
     ent[1] = l;
-    ent[2] = a.segoff[d * (El + 1) + l] + mi * BM;
-    ent[3] = min(BM, a.totals[k] - mi * BM);
+    ent[2] = a.segoff[d * (El + 1) + l] + mi * a.tile_rows;
+    ent[3] = min(a.tile_rows, a.totals[k] - mi * a.tile_rows);
     ent[4] = nb;
   }
 }
@@ -314,10 +315,10 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
     if (cudaMemsetAsync(recv_counts, 0, sizeof(int) * R, s) != cudaSuccess) return MK_ERR_CUDA;
     return MK_OK;
   }
-  const int sms = device_sm_count();
+  const int sms = grid_cap(cfg);
   if (sms <= 0) return MK_ERR_UNSUPPORTED;
-  int grid_cap = sms;
-  if (cfg && cfg->max_ctas > 0) grid_cap = std::min(grid_cap, cfg->max_ctas);
+  // CTA pairs take 256-row tiles of an expert's rows (one 128-row half each).
+  const bool pair = use_pair(cfg, sms);
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   MoeArgs a;
@@ -348,6 +349,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   a.n_nblk = L.n_nblk;
   a.nblk = L.nblk;
   a.cap = cap_rows;
+  a.tile_rows = pair ? 2 * BM : BM;
 
   moe_route_rank_kernel<<<dim3(L.C, R), RR_THREADS, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
@@ -385,6 +387,8 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   int pr = 1;
   while (pr < BM && static_cast<long long>(pr) * 2 * H * 2 <= 32768) pr *= 2;
   p.moe_rows_per_piece = pr;
+  // the dispatch moves 4x the bytes of the AG copy-in: every copy warp takes part
+  p.n_cw = N_COPY_WARPS;
   p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
   p.hdr = a.hdr;
@@ -397,13 +401,21 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
     p.moe_recv_x[r] = static_cast<uint8_t*>(recv_x[r]);
     p.moe_src[r] = recv_src[r];
     if (!make_map_a(&p.tmA[r], recv_x[r], H, cap_rows, static_cast<size_t>(H) * 2) ||
-        !(p.b_one_box ? make_map_w_chunks(&p.tmB[r], w[r], H, N, E_loc)
+        !(p.b_one_box ? make_map_w_chunks(&p.tmB[r], w[r], H, N, E_loc, pair ? 2 : 4)
                       : make_map_3d(&p.tmB[r], w[r], N, H, E_loc, static_cast<size_t>(N) * 2,
                                     static_cast<size_t>(H) * N * 2, 64, BK, 1)))
       return MK_ERR_CUDA;
   }
-  const int grid = std::max(1, std::min(grid_cap, L.max_tiles));
-  p.n_compute = grid;
+  int grid;
+  if (pair) {
+    const int n_pairs = std::max(1, std::min(std::min(max_pair_clusters(), sms / 2), L.max_tiles));
+    p.pair = 1;
+    p.n_compute = n_pairs;
+    grid = 2 * n_pairs;
+  } else {
+    grid = std::max(1, std::min(sms, L.max_tiles));
+    p.n_compute = grid;
+  }
   const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
   if (mode == MK_MODE_UNFUSED) {
     // host-ordered baseline: the dispatch copy as one launch, then the grouped GEMM

@@ -63,11 +63,13 @@ SMALL = [  # R, E_loc, T, H, N
 ]
 
 
+@pytest.mark.parametrize("pair", [mk.PAIR_OFF, mk.PAIR_ON])
 @pytest.mark.parametrize("R,E_loc,T,H,N", SMALL)
-def test_moe_integer_bit_exact(R, E_loc, T, H, N):
+def test_moe_integer_bit_exact(R, E_loc, T, H, N, pair):
+    # pairs: 256-row tiles of each expert's rows, one 128-row half per CTA
     w = I.MoeWorkload("t", R=R, E_loc=E_loc, T=T, H=H, N=N, integer=True, x_seed=31,
                       logit_seed=41, w_seed=51)
-    x, logits, wexp, res, st, detail = run_both(w)
+    x, logits, wexp, res, st, detail = run_both(w, cfg=mk.Config(cta_pair=pair))
     assert st == mk.MK_OK, (mk.status_string(st), detail)
     recv_src, seg = check_dispatch(w, x, logits, res)
     xb = [I.bits(t) for t in x]
@@ -151,9 +153,11 @@ def test_moe_single_expert_identity():
     np.testing.assert_array_equal(gpu_bits(res["y"][0][:T]), oracle_bits(want, "bf16"))
 
 
-def test_moe_missing_rows_time_out():
+@pytest.mark.parametrize("pair", [mk.PAIR_OFF, mk.PAIR_ON])
+def test_moe_missing_rows_time_out(pair):
     w = I.MoeWorkload("t", R=2, E_loc=2, T=128, H=64, N=256, integer=True)
-    x, logits, wexp, res, st, _ = run_both(w, cfg=mk.Config(inject=1, wait_limit_ns=20_000_000))
+    x, logits, wexp, res, st, _ = run_both(w, cfg=mk.Config(inject=1, wait_limit_ns=20_000_000,
+                                                             cta_pair=pair))
     assert st == mk.MK_ERR_TIMEOUT
     x, logits, wexp, res, st, _ = run_both(w)
     assert st == mk.MK_OK
