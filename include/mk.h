@@ -99,9 +99,10 @@ typedef struct {
   int cta_pair;             /* GEMM tiles: 0 = default, 1 = one CTA per 128 x 256 tile,
                                2 = CTA pairs (clusters of two SMs sharing a 256 x 256 tile
                                    through tcgen05 cta_group::2).  Pairs serve every launch
-                                   without copy-role or reduce-role CTAs and outside MoE;
-                                   elsewhere, or where the device cannot co-schedule
-                                   pairs, single CTAs run.  Results are identical.      */
+                                   without copy-role or reduce-role CTAs (MoE: 256-row
+                                   tiles of each expert's rows); elsewhere, or where the
+                                   device cannot co-schedule pairs, single CTAs run.
+                                   Results are identical.                               */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).
