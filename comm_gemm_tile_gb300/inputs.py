@@ -131,6 +131,43 @@ class MoeWorkload:
                                    x_seed=self.x_seed + 50000, w_seed=self.w_seed + 50000)
 
 
+@dataclasses.dataclass(frozen=True)
+class MoeCombineWorkload:
+    """MoE combine: the expert hidden rows h[d] ([cap x N], in dispatch order,
+    routed by the same Zipf logits as the dispatch), the down-projection
+    W2[d] ([E_loc x N x H]) and the gate weights gates[r] ([T x topk] fp32)."""
+    name: str
+    R: int
+    E_loc: int
+    T: int               # tokens per rank
+    H: int               # model width (output)
+    N: int               # expert width (contraction)
+    topk: int = 2
+    zipf_s: float = 1.1
+    logit_seed: int = 1800
+    h_seed: int = 2100
+    w2_seed: int = 2200
+    gate_seed: int = 2300
+    integer: bool = False
+    cap_rows: int = 0
+
+    @property
+    def E(self) -> int:
+        return self.R * self.E_loc
+
+    @property
+    def cap(self) -> int:
+        return self.cap_rows or self.R * self.T * self.topk
+
+    def flops(self) -> float:
+        return 2.0 * self.R * self.T * self.topk * self.N * self.H
+
+    def integer_twin(self) -> "MoeCombineWorkload":
+        return dataclasses.replace(self, name=self.name + "_int", integer=True,
+                                   h_seed=self.h_seed + 50000, w2_seed=self.w2_seed + 50000,
+                                   gate_seed=self.gate_seed + 50000)
+
+
 # The five workloads: a tiny bit-exact GEMM+RS, then TP=8 MLP up-proj (AG),
 # down-proj (RS), a decode-shaped AR and a 64-expert top-2 MoE layer.
 RS_R2_256_INT = GemmWorkload("rs_r2_256_int", "rs", R=2, m=256, n=256, k=256, out="f32",
@@ -142,9 +179,12 @@ RS_R8_TP8_DOWN = GemmWorkload("rs_r8_m8192_k3584_n8192", "rs", R=8, m=8192, n=81
 AR_R8_DECODE = GemmWorkload("ar_r8_m128_k3584_n8192", "ar", R=8, m=128, n=8192, k=3584,
                             out="bf16", a_seed=1500, b_seed=1600)
 MOE_R8_E64 = MoeWorkload("moe_r8x8e_t4096_h4096_n1536", R=8, E_loc=8, T=4096, H=4096, N=1536)
+# The combine that follows it: down-projection 1536 -> 4096 and the top-2 weighted sum.
+MOE_COMBINE_R8_E64 = MoeCombineWorkload("moe_combine_r8x8e_t4096_n1536_h4096", R=8, E_loc=8,
+                                        T=4096, H=4096, N=1536)
 
 WORKLOADS = {w.name: w for w in (RS_R2_256_INT, AG_R8_TP8_UP, RS_R8_TP8_DOWN, AR_R8_DECODE,
-                                 MOE_R8_E64)}
+                                 MOE_R8_E64, MOE_COMBINE_R8_E64)}
 
 
 def gemm_inputs(w: GemmWorkload):
@@ -176,6 +216,32 @@ def moe_inputs(w: MoeWorkload):
         per = [draw((w.H, w.N), 0.02, w.w_seed + d * w.E_loc + l) for l in range(w.E_loc)]
         wexp.append(torch.stack(per, 0))
     return x, logits, wexp
+
+
+def combine_inputs(w: MoeCombineWorkload):
+    """logits[r] (T x E) fp32 (the routing), h[d] (cap x N) bf16, w2[d]
+    (E_loc x N x H) bf16, gates[r] (T x topk) fp32.  Float gates are uniform
+    in [0.05, 1) scaled to sum to 1 per token; integer-twin gates are drawn from
+    {0.25, 0.5, 0.75, 1} so that every weighted sum is exact in fp32."""
+    def draw(shape, std, seed):
+        return int_bf16(shape, seed) if w.integer else normal_bf16(shape, std, seed)
+
+    logits = [zipf_logits(w.T, w.E, w.logit_seed + r, w.zipf_s) for r in range(w.R)]
+    h = [draw((w.cap, w.N), 1.0, w.h_seed + d) for d in range(w.R)]
+    w2 = []
+    for d in range(w.R):
+        per = [draw((w.N, w.H), 0.02, w.w2_seed + d * w.E_loc + l) for l in range(w.E_loc)]
+        w2.append(torch.stack(per, 0))
+    gates = []
+    for r in range(w.R):
+        g = rng(w.gate_seed + r)
+        if w.integer:
+            v = g.choice(np.array([0.25, 0.5, 0.75, 1.0], dtype=np.float32), size=(w.T, w.topk))
+        else:
+            u = g.uniform(0.05, 1.0, size=(w.T, w.topk)).astype(np.float32)
+            v = u / u.sum(axis=1, keepdims=True, dtype=np.float32)
+        gates.append(torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)))
+    return logits, h, w2, gates
 
 
 def sample_rows(M: int, seed: int, per_tile: int = 2, tile: int = 128) -> np.ndarray:

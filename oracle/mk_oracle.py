@@ -31,6 +31,12 @@ The ops (mKernel write-up, news.chathome.org, "五种融合内核" table):
   used here are: top-k on the raw logits (largest first, ties to the lower
   expert id), expert e lives on rank e // E_loc, and the rows that rank d
   receives are ordered by (local expert, global token id g = r*T + t).
+* MoE combine, the step after the same row: the expert rows are multiplied
+  by each expert's down-projection, the products (rounded to bf16, the
+  expert output) return to the token's source rank, and each token's output
+  is the gate-weighted sum of its top-k returned rows.  The pages do not
+  describe combine; its readings: the gate weights are an input (fp32,
+  [T x topk] per source rank), and the weighted sum is exact, rounded once.
 
 Pins: every function here is checked in ``tests/test_oracle.py`` against
 brute force on tiny inputs, closed forms, invariants, and special cases that
@@ -256,6 +262,74 @@ def moe_dispatch_gemm(x_list, logits_list, w_list, E_loc: int, topk: int, out: s
     recv_x = [moe_gather_rows(x_list, recv_src[d], topk) for d in range(len(x_list))]
     y = [moe_expert_gemm(recv_x[d], seg[d], w_list[d], out) for d in range(len(x_list))]
     return dict(topk_idx=topk_idx, counts=counts, recv_src=recv_src, seg=seg, recv_x=recv_x, y=y)
+
+
+def moe_seg_from_counts(counts, E_loc: int):
+    """seg[d][l]: rows that rank d holds for its local expert l, i.e. the
+    total over source ranks of counts[:, d*E_loc + l]."""
+    counts = np.asarray(counts, dtype=np.int64)
+    R = counts.shape[0]
+    tot = counts.sum(axis=0)
+    return [tot[d * E_loc:(d + 1) * E_loc].copy() for d in range(R)]
+
+
+def moe_return_rows(y2_list, recv_src_list, topk: int, T: int, R: int):
+    """The return all-to-all of MoE combine: row j of destination rank d came
+    from (token g, slot k) with recv_src[d][j] = g*topk + k; it goes back to
+    source rank r = g // T at ret[r][t, k] (t = g % T).  Returns R arrays
+    [T x topk x H] of bf16 bits; every (r, t, k) must be covered exactly once."""
+    H = None
+    for y in y2_list:
+        if np.asarray(y).ndim == 2 and np.asarray(y).shape[0] > 0:
+            H = np.asarray(y).shape[1]
+    H = 0 if H is None else H
+    ret = [np.zeros((T, topk, H), dtype=np.uint16) for _ in range(R)]
+    seen = [np.zeros((T, topk), dtype=np.int64) for _ in range(R)]
+    for d in range(R):
+        src = np.asarray(recv_src_list[d], dtype=np.int64)
+        y = np.asarray(y2_list[d], dtype=np.uint16)
+        for j, s_ in enumerate(src.tolist()):
+            g, k = divmod(s_, topk)
+            r, t = divmod(g, T)
+            ret[r][t, k] = y[j]
+            seen[r][t, k] += 1
+    for r in range(R):
+        if not np.all(seen[r] == 1):
+            raise ValueError("the received rows do not cover every (token, slot) exactly once")
+    return ret
+
+
+def moe_weighted_sum(ret_r, gates_r, out: str = "bf16"):
+    """Combine of one source rank: out[t] = sum_k gates[t, k] * ret[t, k], the
+    slot rows widened exactly, the sum exact in float64, rounded once."""
+    ret64 = bf16_to_f64(np.asarray(ret_r, dtype=np.uint16))            # [T x topk x H]
+    g = np.asarray(gates_r, dtype=np.float64)                           # [T x topk]
+    return round_out(np.einsum("tk,tkh->th", g, ret64), out)
+
+
+def moe_combine(h_list, recv_src_list, counts, w2_list, gates_list, E_loc: int, topk: int,
+                T: int, out: str = "bf16"):
+    """MoE combine, the step after dispatch + up-projection: each destination
+    rank multiplies the rows of local expert l by that expert's down-projection
+    W2_l (rounded to bf16: the expert output), the rows return to their source
+    ranks (slot k of token t), and every token's output is the gate-weighted
+    sum of its top-k returned rows.
+
+    h_list[d]: [>= rows_d x N] bf16 bits (the expert hidden rows, in the order
+    the dispatch delivered them); recv_src_list[d]: g*topk + k per row;
+    counts: [R x E] (source rank x expert) from the dispatch; w2_list[d]:
+    [E_loc x N x H] bf16 bits; gates_list[r]: [T x topk] fp32.
+    Returns dict(y2=[per d: rows_d x H bits], ret=[per r: T x topk x H bits],
+    out=[per r: T x H])."""
+    R = len(h_list)
+    seg = moe_seg_from_counts(counts, E_loc)
+    y2 = []
+    for d in range(R):
+        n = int(np.sum(seg[d]))
+        y2.append(moe_expert_gemm(np.asarray(h_list[d])[:n], seg[d], w2_list[d], "bf16"))
+    ret = moe_return_rows(y2, recv_src_list, topk, T, R)
+    res = [moe_weighted_sum(ret[r], gates_list[r], out) for r in range(R)]
+    return dict(y2=y2, ret=ret, out=res)
 
 
 # ----------------------------------------------------------------------------

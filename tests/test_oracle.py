@@ -344,6 +344,101 @@ def test_moe_end_to_end_brute_force_tiny():
             np.testing.assert_array_equal(res["y"][d][j], want.astype(np.float32))
 
 
+# ---------------------------------------------------------------- MoE combine
+
+def _combine_case(R, E_loc, T, N, H, topk, seed, gates=None):
+    """Routing from seeded Zipf logits, integer hidden rows and weights."""
+    logits = [I.zipf_logits(T, R * E_loc, seed + r).numpy() for r in range(R)]
+    idx = [O.moe_route(lg, topk) for lg in logits]
+    counts = O.moe_counts(idx, R * E_loc)
+    recv_src, seg = O.moe_dispatch(idx, E_loc)
+    h = [rand_int_bits((len(recv_src[d]) + 3, N), seed + 100 + d) for d in range(R)]  # + junk rows
+    w2 = [np.stack([rand_int_bits((N, H), seed + 200 + 10 * d + l) for l in range(E_loc)], 0)
+          for d in range(R)]
+    if gates is None:
+        g = np.random.default_rng(seed + 300)
+        gates = [g.choice([0.25, 0.5, 0.75, 1.0], size=(T, topk)).astype(np.float32)
+                 for _ in range(R)]
+    return idx, counts, recv_src, seg, h, w2, gates
+
+
+def test_combine_brute_force_tiny():
+    # Every (token, slot): find its received row by a linear search of recv_src
+    # (not the inverse map), multiply by the slot's expert with a triple loop,
+    # round to bf16, weight and sum over slots in Python floats.
+    R, E_loc, T, N, H, topk = 2, 2, 5, 3, 4, 2
+    idx, counts, recv_src, seg, h, w2, gates = _combine_case(R, E_loc, T, N, H, topk, 510)
+    res = O.moe_combine(h, recv_src, counts, w2, gates, E_loc, topk, T, out="f32")
+    idx_all = np.concatenate(idx, 0)
+    for r in range(R):
+        for t in range(T):
+            g = r * T + t
+            acc = np.zeros(H)
+            for k in range(topk):
+                e = int(idx_all[g, k])
+                d, l = divmod(e, E_loc)
+                j = [i for i, v in enumerate(recv_src[d].tolist()) if v == g * topk + k]
+                assert len(j) == 1
+                z = brute_matmul(O.bf16_to_f64(h[d][j[0]:j[0] + 1]), O.bf16_to_f64(w2[d][l]))[0]
+                y = O.bf16_to_f64(O.f64_to_bf16_bits(z))
+                np.testing.assert_array_equal(res["ret"][r][t, k], O.f64_to_bf16_bits(z))
+                acc += float(gates[r][t, k]) * y
+            np.testing.assert_array_equal(res["out"][r][t], acc.astype(np.float32))
+
+
+def test_combine_one_hot_gates_return_the_slot_rows():
+    # gates (1, 0) give back slot 0's expert row exactly, (0, 1) slot 1's:
+    # catches a swapped slot or a transposed gate matrix.
+    R, E_loc, T, N, H, topk = 3, 2, 9, 4, 5, 2
+    for hot in range(topk):
+        gates = [np.eye(topk, dtype=np.float32)[np.full(T, hot)] for _ in range(R)]
+        idx, counts, recv_src, seg, h, w2, _ = _combine_case(R, E_loc, T, N, H, topk, 520)
+        res = O.moe_combine(h, recv_src, counts, w2, gates, E_loc, topk, T)
+        for r in range(R):
+            np.testing.assert_array_equal(res["out"][r], res["ret"][r][:, hot, :])
+
+
+def test_dispatch_then_combine_with_identity_experts_returns_the_tokens():
+    # x -> dispatch -> (expert = identity) -> combine with gates summing to 1
+    # in powers of two gives back x exactly.
+    R, E_loc, T, H, topk = 2, 3, 11, 6, 2
+    x = [rand_int_bits((T, H), 530 + r) for r in range(R)]
+    logits = [I.zipf_logits(T, R * E_loc, 540 + r).numpy() for r in range(R)]
+    idx = [O.moe_route(lg, topk) for lg in logits]
+    counts = O.moe_counts(idx, R * E_loc)
+    recv_src, seg = O.moe_dispatch(idx, E_loc)
+    recv_x = [O.moe_gather_rows(x, recv_src[d], topk) for d in range(R)]
+    eye = [np.stack([bf(np.eye(H))] * E_loc, 0) for _ in range(R)]
+    gates = [np.tile(np.array([[0.75, 0.25]], np.float32), (T, 1)) for _ in range(R)]
+    res = O.moe_combine(recv_x, recv_src, counts, eye, gates, E_loc, topk, T)
+    for r in range(R):
+        np.testing.assert_array_equal(res["out"][r], x[r])
+
+
+def test_combine_is_linear_in_gates_and_single_rounding():
+    # out(a*g) == RNE(a * exact(g)) for a power of two a; and a non-dyadic
+    # gate is rounded once (not once per slot).
+    R, E_loc, T, N, H, topk = 2, 2, 7, 3, 4, 2
+    idx, counts, recv_src, seg, h, w2, gates = _combine_case(R, E_loc, T, N, H, topk, 550)
+    base = O.moe_combine(h, recv_src, counts, w2, gates, E_loc, topk, T, out="f32")
+    dbl = O.moe_combine(h, recv_src, counts, w2, [2 * g for g in gates], E_loc, topk, T, out="f32")
+    for r in range(R):
+        np.testing.assert_array_equal(dbl["out"][r], 2 * base["out"][r])
+    third = [np.full((T, topk), 1.0 / 3.0) for _ in range(R)]
+    res = O.moe_combine(h, recv_src, counts, w2, third, E_loc, topk, T, out="f32")
+    for r in range(R):
+        exact = O.bf16_to_f64(base["ret"][r]).sum(axis=1) / 3.0
+        np.testing.assert_array_equal(res["out"][r], exact.astype(np.float32))
+
+
+def test_combine_seg_from_counts_and_coverage_check():
+    counts = np.array([[1, 2, 0, 3], [4, 0, 5, 6]])
+    seg = O.moe_seg_from_counts(counts, 2)
+    assert [s.tolist() for s in seg] == [[5, 2], [5, 9]]
+    with pytest.raises(ValueError):
+        O.moe_return_rows([np.zeros((1, 2), np.uint16)], [np.array([0])], topk=2, T=1, R=1)
+
+
 def test_norm_scale():
     assert O.norm_scale(16, 2.0, 0.5) == 4.0
 
