@@ -94,6 +94,11 @@ def lib() -> ctypes.CDLL:
             f.argtypes = [P(vp), P(vp), P(vp), i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
         L.mk_ag_gemm_noalloc.restype = i
         L.mk_ag_gemm_noalloc.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, P(_Cfg), vp]
+        L.mk_moe_combine_workspace_size.restype = sz
+        L.mk_moe_combine_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
+        L.mk_moe_combine.restype = i
+        L.mk_moe_combine.argtypes = [P(vp), P(vp), P(vp), P(vp), vp, i, i, i, ll, ll, ll, ll,
+                                     P(vp), P(vp), vp, sz, P(_Cfg), vp]
         L.mk_moe_dispatch_gemm.restype = i
         L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
                                            P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
@@ -282,6 +287,43 @@ def moe_dispatch_gemm(x, logits, w, *, E_loc: int, topk: int = 2, cap_rows: int 
     return o
 
 
+def moe_combine_workspace_size(R, E_loc, topk, T, N, H, cap_rows, cfg: Config | None = None) -> int:
+    return int(lib().mk_moe_combine_workspace_size(R, E_loc, topk, T, N, H, cap_rows, _cfgp(cfg)))
+
+
+def moe_combine(h, w2, gates, recv_src, counts, *, E_loc: int, topk: int = 2,
+                cap_rows: int | None = None, out=None, cfg: Config | None = None,
+                workspace: Workspace | None = None, stream=None):
+    """MoE combine over R virtual ranks: down-projection of every expert's rows,
+    return of the rows to their source ranks, gate-weighted sum over the top-k.
+
+    h[d]: [cap x N] bf16 expert hidden rows in dispatch order; w2[d]: [E_loc x N x H] bf16;
+    gates[r]: [T x topk] fp32; recv_src[d]: [cap] int32 and counts: [R x E] int32 from the
+    dispatch.  Returns a dict with ret[r] [T x topk x H] (the returned expert rows) and
+    out[r] [T x H] (bf16).  `out` may pass preallocated buffers.
+    """
+    R = len(h)
+    cap = cap_rows if cap_rows is not None else h[0].shape[0]
+    N = h[0].shape[1]
+    H = w2[0].shape[2]
+    T = gates[0].shape[0]
+    dev = h[0].device
+    o = dict(out or {})
+    o.setdefault("ret", [torch.empty((T, topk, H), dtype=torch.bfloat16, device=dev) for _ in range(R)])
+    o.setdefault("out", [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(R)])
+    ws = _ws(workspace, dev)
+    nb = moe_combine_workspace_size(R, E_loc, topk, T, N, H, cap, cfg)
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, "mk_moe_combine_workspace_size")
+    buf = ws.get(nb)
+    st = lib().mk_moe_combine(_ptrs(h), _ptrs(w2), _ptrs(gates), _ptrs(recv_src), counts.data_ptr(),
+                              R, E_loc, topk, T, N, H, cap, _ptrs(o["ret"]), _ptrs(o["out"]),
+                              buf.data_ptr(), buf.numel(), _cfgp(cfg), _stream(stream, dev))
+    _check(st, "mk_moe_combine")
+    return o
+
+
 __all__ = ["Config", "MkError", "Workspace", "ag_gemm", "gemm_rs", "gemm_ar", "device_status",
            "workspace_size", "lib", "status_string", "MODE_FUSED", "MODE_GEMM_ONLY",
-           "MODE_UNFUSED", "moe_dispatch_gemm", "moe_workspace_size"]
+           "MODE_UNFUSED", "moe_dispatch_gemm", "moe_workspace_size", "moe_combine",
+           "moe_combine_workspace_size"]

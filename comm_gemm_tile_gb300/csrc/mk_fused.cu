@@ -252,7 +252,7 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
     it.row_hi = min(BM, p.M - it.out_row0);
     return true;
   }
-  // OP_MOE: entry i of the tile table written by the routing kernel:
+  // OP_MOE / OP_MOE_COMBINE: entry i of the tile table written by the routing kernel:
   // {dest rank d, local expert l, first row of the tile in recv_x[d], rows valid, n-block}.
   // With pairs an entry spans up to 256 rows; CTA r takes rows 128r .. 128r+127 of it.
   const int* e = p.moe_tiles + 5 * i;
@@ -302,8 +302,9 @@ struct Ring {
 
 __device__ __forceinline__ int n_items_for(const FusedParams& p) {
   if (p.op == OP_MOE && p.mode == MK_MODE_UNFUSED) return 0;   // baseline: dispatch copy only
-  if (p.op == OP_MOE) return min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)) ,
-                                 static_cast<uint32_t>(p.n_items));
+  if (p.op == OP_MOE || p.op == OP_MOE_COMBINE)
+    return min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)),
+               static_cast<uint32_t>(p.n_items));
   return p.n_items;
 }
 
@@ -575,6 +576,73 @@ __device__ __forceinline__ void release_tmem(const ComputeSmem& S, int buf, uint
   else mbar_arrive(S.tempty(buf));
 }
 
+// MoE combine epilogue of one warp (32 rows of a tile, 256 columns):
+//  1. return: row j of destination rank d holds (token g, slot k) =
+//     divmod(recv_src[d][j], topk); its bf16 product row goes to
+//     ret[g / T][g % T][k] (columns n0 .. n0+255);
+//  2. TMEM is released at once, so the next tile's MMAs may start;
+//  3. last arrival: after a gpu-scope fence each lane counts its slot in the
+//     (token, column block) counter; the lane that brings it to topk sums the
+//     token's topk rows for these columns, gate-weighted in fp32 in slot order,
+//     and writes the bf16 output row piece.
+template <bool PAIR>
+__device__ __forceinline__ void combine_epilogue(const FusedParams& p, const ComputeSmem& S, const Item& it,
+                                                 uint32_t taddr, int buf, uint32_t rank, int lane, int trow,
+                                                 bool row_ok, int grow) {
+  const int topk = p.moe_topk, T = p.moe_T;
+  const int n0 = it.nb * BN;
+  int r = 0, t = 0, k = 0;
+  if (row_ok) {
+    const int src = p.moe_src[it.mb][grow];
+    const int g = src / topk;
+    k = src - g * topk;
+    r = g / T;
+    t = g - r * T;
+  }
+  uint8_t* slot_row = p.moe_ret[r] + (static_cast<size_t>(t) * topk + k) * p.N * 2;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tc_ld_32x32b_x32(taddr + 32u * c, v);
+    tc_wait_ld();
+    const int col = n0 + 32 * c;
+    const int nvalid = max(0, min(32, p.N - col));
+    if (row_ok && nvalid > 0) store_row_chunk(slot_row + static_cast<size_t>(col) * 2, v, nvalid, false);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) release_tmem<PAIR>(S, buf, rank);
+  if (p.mode != MK_MODE_FUSED || !row_ok) return;
+  __threadfence();
+  const uint32_t before = atomicAdd(p.moe_cnt + (static_cast<size_t>(r) * T + t) * p.n_nblk + it.nb, 1u);
+  if (before != static_cast<uint32_t>(topk - 1)) return;
+  __threadfence();   // every other slot's stores happened before its count
+  const float* gate = p.moe_gates[r] + static_cast<size_t>(t) * topk;
+  const uint8_t* tok = p.moe_ret[r] + static_cast<size_t>(t) * topk * p.N * 2;
+  uint8_t* orow = reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<size_t>(t) * p.N * 2;
+  const int cols = min(BN, p.N - n0);   // a multiple of 8
+#pragma unroll 1
+  for (int c8 = 0; c8 < cols; c8 += 8) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int q = 0; q < topk; ++q) {
+      const float gq = __ldg(gate + q);
+      const float4 raw = ld_global_cg_f4(reinterpret_cast<const float*>(
+          tok + (static_cast<size_t>(q) * p.N + n0 + c8) * 2));
+      const uint32_t w4[4] = {__float_as_uint(raw.x), __float_as_uint(raw.y), __float_as_uint(raw.z),
+                              __float_as_uint(raw.w)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(gq, __uint_as_float(w4[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(gq, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
+    }
+    st_global_v4(orow + static_cast<size_t>(n0 + c8) * 2, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
 template <bool PAIR>
 __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid,
                          uint32_t rank) {
@@ -691,6 +759,13 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         __threadfence();   // the other partials' stores happened before their counts
         reduce_quarter(p, it, tile, trow, row_ok, grow);
       }
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1u;
+      }
+      continue;
+    } else if (p.op == OP_MOE_COMBINE) {
+      combine_epilogue<PAIR>(p, S, it, taddr, buf, rank, lane, trow, row_ok, grow);
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;

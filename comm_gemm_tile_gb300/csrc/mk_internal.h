@@ -52,7 +52,7 @@ constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chu
 enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_READY = 4, HDR_WORDS = 64 };
 constexpr size_t WS_HDR_BYTES = 256;
 
-enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3 };
+enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3, OP_MOE_COMBINE = 4 };
 
 // Role codes used in the error detail word.
 enum { WHERE_PRODUCER = 1, WHERE_MMA = 2, WHERE_EPILOGUE = 3, WHERE_COPY = 4, WHERE_REDUCE = 5,
@@ -103,6 +103,10 @@ struct FusedParams {
   const int* moe_ok;                     // 1 when no rank exceeds its capacity
   int moe_T, moe_topk, moe_nblk;         // tokens per rank, slots, 128-row blocks per rank
   int moe_rows_per_piece;                // destination rows per copy piece (divides 128)
+  // MoE combine (out[r] = combined rows of source rank r)
+  uint8_t* moe_ret[MK_MAX_RANKS];        // [T x topk x N] bf16 returned expert rows per source rank
+  const float* moe_gates[MK_MAX_RANKS];  // [T x topk] gate weights per source rank
+  uint32_t* moe_cnt;                     // [R*T x n_nblk] slots landed per (token, 256-col block)
   int b_one_box;       // 1 = tmB maps are [64 cols, K, N/64 chunks (, experts)] views and a
                        //     stage's B tile (4 column chunks, 2 per CTA of a pair) is one TMA request
   int pair;            // 1 = launched as clusters of 2 CTAs sharing 256 x 256 tiles; items then

@@ -180,6 +180,44 @@ mk_status mk_moe_dispatch_gemm(const void *const *x, const float *const *logits,
                                void *const *recv_x, void *const *y, void *workspace,
                                size_t ws_bytes, const mk_config *cfg, mk_stream_t stream);
 
+/* Workspace bytes for mk_moe_combine (0 on bad args). */
+size_t mk_moe_combine_workspace_size(int R, int E_loc, int topk, long long T, long long N,
+                                     long long H, long long cap_rows, const mk_config *cfg);
+
+/* MoE combine: the step after "MoE Dispatch + GEMM" (five-kernel table, row
+ * "MoE Dispatch + GEMM", run in the return direction; the pages describe the
+ * dispatch side only).  In one pipeline, every destination rank multiplies the
+ * rows of each local expert by that expert's down-projection.  Each product
+ * row returns to its token's source rank as soon as its tile is done.  The
+ * last of a token's top-k rows to land (per 256-column block) forms the
+ * gate-weighted sum.
+ *   h[d]:       [cap_rows x N] bf16 expert hidden rows of rank d, in the order
+ *               the dispatch delivered them (rows past recv_counts[d] unused)
+ *   w2[d]:      [E_loc x N x H] bf16 down-projection of experts d*E_loc ..
+ *   gates[r]:   [T x topk] fp32 gate weight of each (token, slot) of rank r
+ *   recv_src[d]: [cap_rows] g*topk + slot of each received row (from the dispatch)
+ *   counts:     [R x E] int32 rows of source rank r routed to expert e (from
+ *               the dispatch; fixes each expert's row segment on its rank)
+ *   All pointers are device pointers.
+ * Outputs:
+ *   ret[r]:  [T x topk x H] bf16; ret[r][t][k] = round_bf16(h[d][j] @ w2[d][l]),
+ *            for the row j of rank d that holds (token g = r*T + t, slot k) and
+ *            its local expert l (the returned expert rows)
+ *   out[r]:  [T x H] bf16; out[r][t] = round_bf16(sum_k gates[r][t][k] * ret[r][t][k]),
+ *            summed in fp32 in slot order k = 0..topk-1
+ * Every (token, slot) must appear exactly once in the recv_src of the rank
+ * that holds its expert.  If a rank's rows (from counts) exceed cap_rows,
+ * nothing is computed and the device status becomes MK_ERR_CAPACITY.
+ * mode: FUSED (one launch), GEMM_ONLY (the grouped GEMM and the return of the
+ * rows; out is not written), UNFUSED (that launch, then a separate
+ * weighted-sum launch).  N and H must be multiples of 8, 1 <= topk <= 8,
+ * R*E_loc <= 256. */
+mk_status mk_moe_combine(const void *const *h, const void *const *w2, const float *const *gates,
+                         const int *const *recv_src, const int *counts, int R, int E_loc, int topk,
+                         long long T, long long N, long long H, long long cap_rows,
+                         void *const *ret, void *const *out, void *workspace, size_t ws_bytes,
+                         const mk_config *cfg, mk_stream_t stream);
+
 /* Size of the library's own scratch array used by mk_ag_gemm_noalloc (bytes). */
 #define MK_NOALLOC_SCRATCH_BYTES 65536
 

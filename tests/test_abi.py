@@ -62,6 +62,39 @@ def test_workspace_sizes(L):
     assert mk.workspace_size(mk.OP_GEMM_AR, 8, 128, 8192, 3584) <= 32 * 16 * 128 * 256 * 4 + (1 << 20)
 
 
+def test_combine_workspace_sizes(L):
+    # 8 ranks x 8 experts, T=4096, top-2, N=1536 -> H=4096 (16 column blocks)
+    sz = mk.moe_combine_workspace_size(8, 8, 2, 4096, 1536, 4096, 65536)
+    cnt = 8 * 4096 * 16 * 4
+    tiles = (8 * 4096 * 2 // 128 + 64) * 16 * 5 * 4
+    assert cnt + tiles <= sz < cnt + tiles + (1 << 16)
+    assert mk.moe_combine_workspace_size(8, 8, 2, 4096, 1532, 4096, 65536) == 0   # N % 8
+    assert mk.moe_combine_workspace_size(8, 8, 2, 4096, 1536, 4100, 65536) == 0   # H % 8
+    assert mk.moe_combine_workspace_size(8, 8, 9, 4096, 1536, 4096, 65536) == 0   # topk > 8
+    assert mk.moe_combine_workspace_size(16, 17, 2, 64, 64, 64, 64) == 0          # E > 256
+
+
+def test_combine_argument_validation_without_launch(L):
+    V = ctypes.c_void_p
+    good = 0x10000
+    ws = V(good)
+    arr = (ctypes.c_void_p * 2)(good, good)
+    args = (arr, arr, arr, arr, V(good), 2, 2, 2, 64, 64, 256, 256, arr, arr, ws, 1 << 20, None, None)
+    # NULL pointer arrays, misaligned rows, small workspace, bad topk
+    assert L.mk_moe_combine(None, *args[1:]) == mk.MK_ERR_INVALID
+    a = list(args); a[0] = _null_ptrs(2)
+    assert L.mk_moe_combine(*a) == mk.MK_ERR_INVALID
+    a = list(args); a[12] = (ctypes.c_void_p * 2)(good, good + 2)
+    assert L.mk_moe_combine(*a) == mk.MK_ERR_INVALID
+    a = list(args); a[15] = 16
+    assert L.mk_moe_combine(*a) == mk.MK_ERR_INVALID
+    a = list(args); a[7] = 0
+    assert L.mk_moe_combine(*a) == mk.MK_ERR_INVALID
+    cfg = mk.Config(mode=7).c()
+    a = list(args); a[16] = ctypes.pointer(cfg)
+    assert L.mk_moe_combine(*a) == mk.MK_ERR_INVALID
+
+
 def _null_ptrs(n):
     return (ctypes.c_void_p * n)()
 

@@ -120,3 +120,53 @@ def test_moe_full_size(integer):
             np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
         else:
             assert norm_err(gpu_values(got), exact, w.H, amax, bmax) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_moe_combine_full_size(integer):
+    # 8 ranks x 8 experts, 4096 tokens per rank, top-2 (Zipf 1.1), down-proj 1536 -> 4096
+    w = I.MOE_COMBINE_R8_E64.integer_twin() if integer else I.MOE_COMBINE_R8_E64
+    logits, h, w2, gates = I.combine_inputs(w)
+    idx = [O.moe_route(l.numpy(), w.topk) for l in logits]
+    counts = O.moe_counts(idx, w.E)
+    recv_src, seg = O.moe_dispatch(idx, w.E_loc)
+    rs_d = []
+    for d in range(w.R):
+        t = torch.zeros(w.cap, dtype=torch.int32)
+        t[:len(recv_src[d])] = torch.from_numpy(recv_src[d].astype(np.int32))
+        rs_d.append(t.cuda())
+    ws = mk.Workspace()
+    res = mk.moe_combine([t.cuda() for t in h], [t.cuda() for t in w2], [g.cuda() for g in gates],
+                         rs_d, torch.from_numpy(counts.astype(np.int32)).cuda(), E_loc=w.E_loc,
+                         topk=w.topk, cap_rows=w.cap, workspace=ws)
+    _ok(ws)
+    # where each (token, slot) landed: rank d and row j
+    where = np.empty(w.R * w.T * w.topk, dtype=np.int64)
+    for d in range(w.R):
+        where[recv_src[d]] = d * w.cap + np.arange(len(recv_src[d]))
+    idx_all = np.concatenate(idx, 0)
+    amax, bmax = absmax(h), absmax(w2)
+    for r in range(w.R):
+        toks = I.sample_rows(w.T, seed=300 + r)
+        g = r * w.T + toks
+        y2 = np.zeros((len(toks), w.topk, w.H))
+        for k in range(w.topk):
+            e = idx_all[g, k]
+            loc = where[g * w.topk + k]
+            for ex in np.unique(e):                     # one product per expert used
+                pick = np.nonzero(e == ex)[0]
+                d, l = divmod(int(ex), w.E_loc)
+                rows = loc[pick] - d * w.cap
+                hb = O.bf16_to_f64(I.bits(h[d][torch.from_numpy(rows)]))
+                y2[pick, k] = O.bf16_to_f64(O.f64_to_bf16_bits(hb @ O.bf16_to_f64(I.bits(w2[d][l]))))
+        gt = gates[r].numpy().astype(np.float64)[toks]
+        exact_out = np.einsum("tk,tkh->th", gt, y2)
+        sel = torch.from_numpy(toks).cuda()
+        got_ret, got_out = res["ret"][r][sel], res["out"][r][sel]
+        if integer:
+            np.testing.assert_array_equal(gpu_bits(got_ret), O.f64_to_bf16_bits(y2))
+            np.testing.assert_array_equal(gpu_bits(got_out), oracle_bits(exact_out, "bf16"))
+        else:
+            assert norm_err(gpu_values(got_ret).reshape(len(toks), -1), y2.reshape(len(toks), -1),
+                            w.N, amax, bmax) <= TOL["bf16"]
+            assert norm_err(gpu_values(got_out), exact_out, w.N, amax, bmax) <= TOL["bf16"]
