@@ -281,7 +281,7 @@ def main():
     ap.add_argument("--n-copy", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
-    ap.add_argument("--only", choices=["rs", "ar", "moe"], default=None,
+    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine"], default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -437,6 +437,9 @@ def run_only(args):
     bf16_peak, _, hbm_peak, _ = peaks()
     if args.only == "moe":
         res = bench_moe(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    elif args.only == "combine":
+        res = bench_moe_combine(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
+                                hbm_peak)
     else:
         w = I.RS_R8_TP8_DOWN if args.only == "rs" else I.AR_R8_DECODE
         res = bench_other(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
@@ -490,6 +493,10 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
     if with_moe:
         out[I.MOE_R8_E64.name] = bench_moe(mk, device, stream, dist, steps, seed_off, tmax,
                                            bf16_peak, hbm_peak)
+        torch.cuda.empty_cache()
+        out[I.MOE_COMBINE_R8_E64.name] = bench_moe_combine(mk, device, stream, dist, steps, seed_off,
+                                                           tmax, bf16_peak, hbm_peak)
+        torch.cuda.empty_cache()
     return out
 
 
@@ -522,6 +529,59 @@ def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
                  + w.R * w.E_loc * w.H * w.N * 2   # expert weights
                  + rows * w.N * 2              # y
                  + w.R * w.T * w.E * 4)        # logits
+    fused_tf = flops / (res["fused"] * 1e-3) / 1e12
+    t_tensor = flops / (bf16_peak * 1e12)
+    t_hbm = hbm_bytes / (hbm_peak * 1e9)
+    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "algorithmic_bytes": hbm_bytes,
+            "roofline_ms": 1e3 * max(t_tensor, t_hbm),
+            "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
+            "status": mk.status_string(st)}
+
+
+def bench_moe_combine(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+    """MoE combine (down-projection, return, top-k weighted sum): fused, GEMM-only
+    (grouped GEMM + return of the rows, no sum) and unfused (that, then a sum launch)."""
+    w = I.MOE_COMBINE_R8_E64
+    wd = I.MOE_R8_E64
+    # the routing of the MoE layer: one dispatch on the layer's token/logit inputs
+    x = [dev_normal((wd.T, wd.H), 1.0, wd.x_seed + r + seed_off, device) for r in range(wd.R)]
+    lg = [I.zipf_logits(w.T, w.E, w.logit_seed + r + seed_off).to(device) for r in range(w.R)]
+    we = [dev_normal((wd.E_loc, wd.H, wd.N), 0.02, wd.w_seed + d + seed_off, device) for d in range(wd.R)]
+    ws = mk.Workspace(device)
+    disp = mk.moe_dispatch_gemm(x, lg, we, E_loc=w.E_loc, topk=w.topk, workspace=ws, stream=stream)
+    del x, we
+    sets = []
+    for s in range(2):
+        h = [dev_normal((w.cap, w.N), 1.0, w.h_seed + d + 1000 * s + seed_off, device) for d in range(w.R)]
+        w2 = [dev_normal((w.E_loc, w.N, w.H), 0.02, w.w2_seed + d + 1000 * s + seed_off, device)
+              for d in range(w.R)]
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.gate_seed + 1000 * s + seed_off)
+        gates = []
+        for r in range(w.R):
+            u = torch.rand((w.T, w.topk), generator=gen, device=device) * 0.95 + 0.05
+            gates.append((u / u.sum(dim=1, keepdim=True)).contiguous())
+        sets.append((h, w2, gates))
+    outs = mk.moe_combine(*sets[0], disp["recv_src"], disp["counts"], E_loc=w.E_loc, topk=w.topk,
+                          workspace=ws, stream=stream)
+    res = {}
+    for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                      ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        def step(i, cfg=cfg):
+            h, w2, gates = sets[i % 2]
+            mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"], E_loc=w.E_loc, topk=w.topk,
+                           out=outs, cfg=cfg, workspace=ws, stream=stream)
+        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+    st, _ = mk.device_status(ws, stream)
+    flops = w.flops()
+    rows = w.R * w.T * w.topk
+    hbm_bytes = (rows * w.N * 2                     # expert hidden rows
+                 + w.R * w.E_loc * w.N * w.H * 2    # down-projection weights
+                 + rows * w.H * 2 * 2               # returned rows: written, read by the sum
+                 + w.R * w.T * w.H * 2              # combined outputs
+                 + rows * (4 + 4))                  # gates, recv_src
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12
     t_tensor = flops / (bf16_peak * 1e12)
     t_hbm = hbm_bytes / (hbm_peak * 1e9)

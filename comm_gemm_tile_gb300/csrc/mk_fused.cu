@@ -282,9 +282,15 @@ constexpr uint32_t BAR_PDONE = BAR_DRAIN + 8u;
 constexpr uint32_t TMEM_SLOT = BAR_PDONE + 16u;
 static_assert(TMEM_SLOT + 4 <= BAR_BYTES, "compute barriers exceed the barrier block");
 
+// MoE combine queue: control words (u32 index) and entries (byte offset) in the queue block.
+enum { CQ_TAIL = 0, CQ_CLAIM = 1, CQ_DONE = 2 };
+constexpr uint32_t CQ_ENT = 64;
+
 struct ComputeSmem {
   uint32_t ring;  // smem address of stage 0
   uint32_t bars;  // smem address of the barrier block
+  uint32_t cq;    // smem address of the MoE combine queue block
+  uint32_t* cq_ctl;   // the same block, generic pointer (control words)
   __device__ __forceinline__ uint32_t full(int s) const { return bars + BAR_FULL + 8u * s; }
   __device__ __forceinline__ uint32_t empty(int s) const { return bars + BAR_EMPTY + 8u * s; }
   __device__ __forceinline__ uint32_t tfull(int b) const { return bars + BAR_TFULL + 8u * b; }
@@ -582,9 +588,9 @@ __device__ __forceinline__ void release_tmem(const ComputeSmem& S, int buf, uint
 //     ret[g / T][g % T][k] (columns n0 .. n0+255);
 //  2. TMEM is released at once, so the next tile's MMAs may start;
 //  3. last arrival: after a gpu-scope fence each lane counts its slot in the
-//     (token, column block) counter; the lane that brings it to topk sums the
-//     token's topk rows for these columns, gate-weighted in fp32 in slot order,
-//     and writes the bf16 output row piece.
+//     (token, column block) counter; the lane that brings it to topk hands the
+//     (token, column block) to the CTA's copy warps (combine_sum_role), which
+//     form the gate-weighted sum while the epilogue moves on.
 template <bool PAIR>
 __device__ __forceinline__ void combine_epilogue(const FusedParams& p, const ComputeSmem& S, const Item& it,
                                                  uint32_t taddr, int buf, uint32_t rank, int lane, int trow,
@@ -594,10 +600,15 @@ __device__ __forceinline__ void combine_epilogue(const FusedParams& p, const Com
   int r = 0, t = 0, k = 0;
   if (row_ok) {
     const int src = p.moe_src[it.mb][grow];
-    const int g = src / topk;
-    k = src - g * topk;
-    r = g / T;
-    t = g - r * T;
+    if (src < 0 || src >= p.R * T * topk) {   // not a (token, slot) of this call: skip the row
+      raise_error(p, MK_ERR_INVALID, WHERE_EPILOGUE, grow);
+      row_ok = false;
+    } else {
+      const int g = src / topk;
+      k = src - g * topk;
+      r = g / T;
+      t = g - r * T;
+    }
   }
   uint8_t* slot_row = p.moe_ret[r] + (static_cast<size_t>(t) * topk + k) * p.N * 2;
 #pragma unroll 1
@@ -617,29 +628,193 @@ __device__ __forceinline__ void combine_epilogue(const FusedParams& p, const Com
   const uint32_t before = atomicAdd(p.moe_cnt + (static_cast<size_t>(r) * T + t) * p.n_nblk + it.nb, 1u);
   if (before != static_cast<uint32_t>(topk - 1)) return;
   __threadfence();   // every other slot's stores happened before its count
-  const float* gate = p.moe_gates[r] + static_cast<size_t>(t) * topk;
-  const uint8_t* tok = p.moe_ret[r] + static_cast<size_t>(t) * topk * p.N * 2;
-  uint8_t* orow = reinterpret_cast<uint8_t*>(p.out[r]) + static_cast<size_t>(t) * p.N * 2;
-  const int cols = min(BN, p.N - n0);   // a multiple of 8
-#pragma unroll 1
-  for (int c8 = 0; c8 < cols; c8 += 8) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int q = 0; q < topk; ++q) {
-      const float gq = __ldg(gate + q);
-      const float4 raw = ld_global_cg_f4(reinterpret_cast<const float*>(
-          tok + (static_cast<size_t>(q) * p.N + n0 + c8) * 2));
-      const uint32_t w4[4] = {__float_as_uint(raw.x), __float_as_uint(raw.y), __float_as_uint(raw.z),
-                              __float_as_uint(raw.w)};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(gq, __uint_as_float(w4[i] << 16), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(gq, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+  // Hand (token row, column block) to the copy warps.  Entry s of the ring
+  // (16 bytes: sequence word, unused, r*T + t, column block) is free for slot
+  // s when its sequence word is 2s, full when it is 2s+1.
+  const uint32_t slot = atomicAdd(S.cq_ctl + CQ_TAIL, 1u);
+  const uint32_t e = S.cq + CQ_ENT + 16u * (slot % CQ_CAP);
+  if (ld_acquire_cta_shared(e) != 2u * slot) {
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t it2 = 0;
+    while (ld_acquire_cta_shared(e) != 2u * slot) {
+      if ((++it2 & 15u) == 0) {
+        if (aborted(p)) return;
+        if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+          raise_error(p, MK_ERR_TIMEOUT, WHERE_EPILOGUE, static_cast<int>(slot));
+          return;
+        }
+      }
+      __nanosleep(64);
+    }
+  }
+  asm volatile("st.shared::cta.v2.u32 [%0], {%1, %2};" ::"r"(e + 8u),
+               "r"(static_cast<uint32_t>(r * T + t)), "r"(static_cast<uint32_t>(it.nb)) : "memory");
+  st_release_cta_shared(e, 2u * slot + 1u);
+}
+
+// MoE combine sums by the copy warps: each warp claims up to 8 handed-over rows
+// at a time and sums them coalesced (lane l: columns n0 + 8l .. n0 + 8l + 7 of
+// each row, 512 contiguous bytes per row and slot, 8 loads per slot in flight):
+// out[r][t] = bf16(sum_k gates[r][t][k] * ret[r][t][k]) in fp32, slot order.
+// A warp leaves when the four epilogue warps have finished and every
+// handed-over row has been claimed (or on abort).
+__device__ void combine_sum_role(const FusedParams& p, const ComputeSmem& S) {
+  const int lane = threadIdx.x & 31;
+  const int topk = p.moe_topk, T = p.moe_T;
+  constexpr int CW = 8;
+  const uint64_t t_start = globaltimer_ns();
+  uint64_t t_idle = t_start;
+  uint32_t spins = 0;
+  while (true) {
+    uint32_t c = 0, n = 0;
+    int state = 0;   // 0 = nothing yet, 1 = claimed [c, c+n), 2 = leave
+    if (lane == 0) {
+      const uint32_t done = ld_acquire_cta_shared(S.cq + 4u * CQ_DONE);
+      const uint32_t tail = ld_acquire_cta_shared(S.cq + 4u * CQ_TAIL);
+      const uint32_t claim = ld_acquire_cta_shared(S.cq + 4u * CQ_CLAIM);
+      if (claim < tail) {
+        n = min(static_cast<uint32_t>(CW), tail - claim);
+        if (atomicCAS(S.cq_ctl + CQ_CLAIM, claim, claim + n) == claim) {
+          c = claim;
+          state = 1;
+        }
+      } else if (done == 4u) {
+        state = 2;
+      }
+      if (state == 0 && (++spins & 15u) == 0) {
+        if (aborted(p)) state = 2;
+        else if (globaltimer_ns() - t_idle > static_cast<uint64_t>(p.wait_ns)) {
+          raise_error(p, MK_ERR_TIMEOUT, WHERE_COPY, static_cast<int>(claim));
+          state = 2;
+        }
       }
     }
-    st_global_v4(orow + static_cast<size_t>(n0 + c8) * 2, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state == 2) return;
+    if (state == 0) {
+      __nanosleep(128);
+      continue;
+    }
+    c = __shfl_sync(0xffffffffu, c, 0);
+    n = __shfl_sync(0xffffffffu, n, 0);
+    if (lane == 0) t_idle = globaltimer_ns();
+    // lane i < n takes entry c + i once it is full, then frees it for slot c + i + CQ_CAP
+    int rt = -1, nb = 0, ok = 1;
+    if (lane < static_cast<int>(n)) {
+      const uint32_t slot = c + lane;
+      const uint32_t e = S.cq + CQ_ENT + 16u * (slot % CQ_CAP);
+      const uint64_t t0 = globaltimer_ns();
+      uint32_t it2 = 0;
+      while (ld_acquire_cta_shared(e) != 2u * slot + 1u) {
+        if ((++it2 & 15u) == 0) {
+          if (aborted(p)) { ok = 0; break; }
+          if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+            raise_error(p, MK_ERR_TIMEOUT, WHERE_COPY, static_cast<int>(slot));
+            ok = 0;
+            break;
+          }
+        }
+        __nanosleep(32);
+      }
+      if (ok) {
+        uint32_t a, b;
+        asm volatile("ld.shared::cta.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(e + 8u) : "memory");
+        rt = static_cast<int>(a);
+        nb = static_cast<int>(b);
+        st_release_cta_shared(e, 2u * (slot + CQ_CAP));
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return;
+    int rr[CW], tt[CW], n0s[CW];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) {
+      const int x = __shfl_sync(0xffffffffu, rt, i);
+      const int y = __shfl_sync(0xffffffffu, nb, i);
+      const bool valid = i < static_cast<int>(n) && x >= 0 && x < p.R * T && y >= 0 && y < p.n_nblk;
+      rr[i] = valid ? x / T : -1;
+      tt[i] = valid ? x - (x / T) * T : 0;
+      n0s[i] = valid ? y * BN : 0;
+    }
+    if (topk == 2) {
+      // both slots of all rows in flight at once (16 loads per lane)
+      uint4 v0[CW], v1[CW];
+      float g0[CW], g1[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        v0[i] = v1[i] = make_uint4(0u, 0u, 0u, 0u);
+        g0[i] = g1[i] = 0.f;
+        const int col = n0s[i] + 8 * lane;
+        if (rr[i] >= 0 && col < p.N) {
+          const uint8_t* base = p.moe_ret[rr[i]] + (static_cast<size_t>(tt[i]) * 2 * p.N + col) * 2;
+          const float4 f0 = ld_global_cg_f4(base);
+          const float4 f1 = ld_global_cg_f4(base + static_cast<size_t>(p.N) * 2);
+          v0[i] = make_uint4(__float_as_uint(f0.x), __float_as_uint(f0.y), __float_as_uint(f0.z),
+                             __float_as_uint(f0.w));
+          v1[i] = make_uint4(__float_as_uint(f1.x), __float_as_uint(f1.y), __float_as_uint(f1.z),
+                             __float_as_uint(f1.w));
+          const float* gp = p.moe_gates[rr[i]] + static_cast<size_t>(tt[i]) * 2;
+          g0[i] = __ldg(gp);
+          g1[i] = __ldg(gp + 1);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const int col = n0s[i] + 8 * lane;
+        if (rr[i] < 0 || col >= p.N) continue;
+        const uint32_t a4[4] = {v0[i].x, v0[i].y, v0[i].z, v0[i].w};
+        const uint32_t b4[4] = {v1[i].x, v1[i].y, v1[i].z, v1[i].w};
+        float o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // the same fused multiply-adds, in slot order, as the general path
+          o[2 * j] = fmaf(g1[i], __uint_as_float(b4[j] << 16), fmaf(g0[i], __uint_as_float(a4[j] << 16), 0.f));
+          o[2 * j + 1] = fmaf(g1[i], __uint_as_float(b4[j] & 0xFFFF0000u),
+                              fmaf(g0[i], __uint_as_float(a4[j] & 0xFFFF0000u), 0.f));
+        }
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.out[rr[i]]) + (static_cast<size_t>(tt[i]) * p.N + col) * 2;
+        st_global_v4(dst, pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                     pack_bf16x2(o[6], o[7]));
+      }
+      continue;
+    }
+    float acc[CW][8];
+#pragma unroll
+    for (int i = 0; i < CW; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int q = 0; q < topk; ++q) {
+      uint4 v[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int col = n0s[i] + 8 * lane;
+        if (rr[i] >= 0 && col < p.N) {
+          const float4 f = ld_global_cg_f4(
+              p.moe_ret[rr[i]] + ((static_cast<size_t>(tt[i]) * topk + q) * p.N + col) * 2);
+          v[i] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
+                            __float_as_uint(f.w));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        if (rr[i] < 0) continue;
+        const float gq = __ldg(p.moe_gates[rr[i]] + static_cast<size_t>(tt[i]) * topk + q);
+        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][2 * j] = fmaf(gq, __uint_as_float(w4[j] << 16), acc[i][2 * j]);
+          acc[i][2 * j + 1] = fmaf(gq, __uint_as_float(w4[j] & 0xFFFF0000u), acc[i][2 * j + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CW; ++i) {
+      const int col = n0s[i] + 8 * lane;
+      if (rr[i] < 0 || col >= p.N) continue;
+      uint8_t* o = reinterpret_cast<uint8_t*>(p.out[rr[i]]) + (static_cast<size_t>(tt[i]) * p.N + col) * 2;
+      st_global_v4(o, pack_bf16x2(acc[i][0], acc[i][1]), pack_bf16x2(acc[i][2], acc[i][3]),
+                   pack_bf16x2(acc[i][4], acc[i][5]), pack_bf16x2(acc[i][6], acc[i][7]));
+    }
   }
 }
 
@@ -657,7 +832,9 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it, static_cast<int>(rank));
-    if (!wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i)) return;
+    // warp-uniform outcome: the tcgen05.ld below needs every lane of the warp
+    const int landed = wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i) ? 1 : 0;
+    if (!__all_sync(0xffffffffu, landed)) return;
     tc_fence_after();
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(buf * BN);
@@ -766,6 +943,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       continue;
     } else if (p.op == OP_MOE_COMBINE) {
       combine_epilogue<PAIR>(p, S, it, taddr, buf, rank, lane, trow, row_ok, grow);
+      __syncwarp();   // lanes that handed a row over rejoin before the next tcgen05.ld
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;
@@ -1005,7 +1183,15 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   ComputeSmem S;
   S.ring = smem_u32(smem);
   S.bars = smem_u32(smem + RING_BYTES);
+  S.cq = smem_u32(smem + RING_BYTES + BAR_BYTES);
+  S.cq_ctl = reinterpret_cast<uint32_t*>(smem + RING_BYTES + BAR_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + TMEM_SLOT);
+  if (p.op == OP_MOE_COMBINE) {
+    // queue: control words zero, entry i free for slot i (sequence word 2i)
+    if (threadIdx.x < 16) S.cq_ctl[threadIdx.x] = 0u;
+    uint32_t* ent = S.cq_ctl + CQ_ENT / 4;
+    for (int i = threadIdx.x; i < CQ_CAP; i += NTHREADS) ent[4 * i] = 2u * i;
+  }
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < Ring<PAIR>::stages; ++s) {
       mbar_init(S.full(s), 1);
@@ -1048,6 +1234,14 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     epilogue<PAIR>(p, S, tmem_base, cid, rank);
+    __syncwarp();
+    if (p.op == OP_MOE_COMBINE && lane == 0) {
+      __threadfence_block();
+      atomicAdd(S.cq_ctl + CQ_DONE, 1u);   // this warp hands over no more rows
+    }
+    __syncwarp();
+  } else if (p.op == OP_MOE_COMBINE) {
+    if (p.mode == MK_MODE_FUSED) combine_sum_role(p, S);
     __syncwarp();
   } else if (p.op == OP_MOE) {
     if constexpr (PAIR) moe_copy_warps_role(p, 2 * cid + static_cast<int>(rank), 2 * p.n_compute);

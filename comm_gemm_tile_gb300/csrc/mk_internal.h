@@ -41,7 +41,11 @@ constexpr int PSTAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES / 2;
 constexpr int PSTAGES = RING_BYTES / PSTAGE_BYTES;
 constexpr int MAX_STAGES = STAGES > PSTAGES ? STAGES : PSTAGES;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES;
+// MoE combine: ring of rows handed from the epilogue warps to the copy warps
+// (16-byte entries after a 64-byte control block), placed after the barriers.
+constexpr int CQ_CAP = 512;
+constexpr int CQ_BYTES = 64 + 16 * CQ_CAP;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + CQ_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int TILE_F32 = BM * BN;              // floats in one partial tile
 constexpr int MAX_PARTIALS = 16;               // staged partial tiles reduced per output tile

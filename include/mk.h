@@ -206,8 +206,10 @@ size_t mk_moe_combine_workspace_size(int R, int E_loc, int topk, long long T, lo
  *   out[r]:  [T x H] bf16; out[r][t] = round_bf16(sum_k gates[r][t][k] * ret[r][t][k]),
  *            summed in fp32 in slot order k = 0..topk-1
  * Every (token, slot) must appear exactly once in the recv_src of the rank
- * that holds its expert.  If a rank's rows (from counts) exceed cap_rows,
- * nothing is computed and the device status becomes MK_ERR_CAPACITY.
+ * that holds its expert; a recv_src entry outside [0, R*T*topk) is skipped and
+ * sets the device status to MK_ERR_INVALID.  If a rank's rows (from counts)
+ * exceed cap_rows, nothing is computed and the device status becomes
+ * MK_ERR_CAPACITY.
  * mode: FUSED (one launch), GEMM_ONLY (the grouped GEMM and the return of the
  * rows; out is not written), UNFUSED (that launch, then a separate
  * weighted-sum launch).  N and H must be multiples of 8, 1 <= topk <= 8,

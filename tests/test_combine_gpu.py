@@ -77,6 +77,19 @@ def test_combine_integer_bit_exact(R, E_loc, T, N, H, pair):
         np.testing.assert_array_equal(I.bits(res["out"][r]), want["out"][r])
 
 
+@pytest.mark.parametrize("topk", [1, 3])
+def test_combine_other_topk_bit_exact(topk):
+    w = I.MoeCombineWorkload("t", R=4, E_loc=3, T=150, N=128, H=264, topk=topk, integer=True,
+                             logit_seed=64, h_seed=74, w2_seed=84, gate_seed=94)
+    (logits, h, w2, gates), (counts, recv_src), res, st, detail = run(w)
+    assert st == mk.MK_OK, (mk.status_string(st), detail)
+    want = O.moe_combine([I.bits(t) for t in h], recv_src, counts, [I.bits(t) for t in w2],
+                         [g.numpy() for g in gates], w.E_loc, w.topk, w.T)
+    for r in range(w.R):
+        np.testing.assert_array_equal(I.bits(res["ret"][r]), want["ret"][r])
+        np.testing.assert_array_equal(I.bits(res["out"][r]), want["out"][r])
+
+
 @pytest.mark.parametrize("R,E_loc,T,N,H", SMALL[:3])
 def test_combine_float_within_tolerance(R, E_loc, T, N, H):
     w = I.MoeCombineWorkload("t", R=R, E_loc=E_loc, T=T, N=N, H=H, logit_seed=62, h_seed=72,
