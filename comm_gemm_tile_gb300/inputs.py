@@ -168,6 +168,43 @@ class MoeCombineWorkload:
                                    gate_seed=self.gate_seed + 50000)
 
 
+@dataclasses.dataclass(frozen=True)
+class MlpWorkload:
+    """Tensor-parallel MLP layer: x shards [m x h] per rank, W1_r [h x f_r]
+    (column shard of the up-projection), W2_r [f_r x h] (row shard of the
+    down-projection)."""
+    name: str
+    R: int
+    m: int               # rows per shard
+    h: int               # model width
+    f_r: int             # hidden width per rank
+    x_seed: int = 2500
+    w1_seed: int = 2600
+    w2_seed: int = 2700
+    w_std: float = 0.02
+    integer: bool = False
+
+    def flops(self) -> float:
+        M = self.R * self.m
+        return 2.0 * M * self.h * self.f_r * self.R * 2
+
+    def integer_twin(self) -> "MlpWorkload":
+        return dataclasses.replace(self, name=self.name + "_int", integer=True,
+                                   x_seed=self.x_seed + 50000, w1_seed=self.w1_seed + 50000,
+                                   w2_seed=self.w2_seed + 50000)
+
+
+def mlp_inputs(w: MlpWorkload):
+    """x[r] (m x h), w1[r] (h x f_r), w2[r] (f_r x h), all bf16."""
+    def draw(shape, std, seed):
+        return int_bf16(shape, seed) if w.integer else normal_bf16(shape, std, seed)
+
+    x = [draw((w.m, w.h), 1.0, w.x_seed + r) for r in range(w.R)]
+    w1 = [draw((w.h, w.f_r), w.w_std, w.w1_seed + r) for r in range(w.R)]
+    w2 = [draw((w.f_r, w.h), w.w_std, w.w2_seed + r) for r in range(w.R)]
+    return x, w1, w2
+
+
 # The five workloads: a tiny bit-exact GEMM+RS, then TP=8 MLP up-proj (AG),
 # down-proj (RS), a decode-shaped AR and a 64-expert top-2 MoE layer.
 RS_R2_256_INT = GemmWorkload("rs_r2_256_int", "rs", R=2, m=256, n=256, k=256, out="f32",
@@ -183,8 +220,11 @@ MOE_R8_E64 = MoeWorkload("moe_r8x8e_t4096_h4096_n1536", R=8, E_loc=8, T=4096, H=
 MOE_COMBINE_R8_E64 = MoeCombineWorkload("moe_combine_r8x8e_t4096_n1536_h4096", R=8, E_loc=8,
                                         T=4096, H=4096, N=1536)
 
+# The whole TP=8 MLP layer those two GEMMs belong to, as one chained kernel.
+MLP_R8_TP8 = MlpWorkload("mlp_r8_m1024x8_h8192_f3584x8", R=8, m=1024, h=8192, f_r=3584)
+
 WORKLOADS = {w.name: w for w in (RS_R2_256_INT, AG_R8_TP8_UP, RS_R8_TP8_DOWN, AR_R8_DECODE,
-                                 MOE_R8_E64, MOE_COMBINE_R8_E64)}
+                                 MOE_R8_E64, MOE_COMBINE_R8_E64, MLP_R8_TP8)}
 
 
 def gemm_inputs(w: GemmWorkload):

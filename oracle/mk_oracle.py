@@ -31,6 +31,13 @@ The ops (mKernel write-up, news.chathome.org, "五种融合内核" table):
   used here are: top-k on the raw logits (largest first, ties to the lower
   expert id), expert e lives on rank e // E_loc, and the rows that rank d
   receives are ordered by (local expert, global token id g = r*T + t).
+* Chained MLP (the roadmap's multi-step kernel, built from the rows
+  "AllGather + GEMM" and "GEMM + ReduceScatter"): X = gather(X_r); every rank
+  r computes H_r = bf16(ReLU(X @ W1_r)) with its column shard W1_r, then
+  S = sum_r H_r @ W2_r with its row shard W2_r, and rank o keeps row block o
+  of S.  The pages name no activation; ReLU is the reading used (exact, so
+  the integer twins stay bit-exact), and H_r is rounded to bf16 as the
+  layer's stored activation.
 * MoE combine, the step after the same row: the expert rows are multiplied
   by each expert's down-projection, the products (rounded to bf16, the
   expert output) return to the token's source rank, and each token's output
@@ -330,6 +337,34 @@ def moe_combine(h_list, recv_src_list, counts, w2_list, gates_list, E_loc: int, 
     ret = moe_return_rows(y2, recv_src_list, topk, T, R)
     res = [moe_weighted_sum(ret[r], gates_list[r], out) for r in range(R)]
     return dict(y2=y2, ret=ret, out=res)
+
+
+def mlp_hidden(x_shards, w1_r) -> np.ndarray:
+    """Up-projection of one rank in the tensor-parallel MLP: the gathered input
+    times the rank's column shard W1_r, ReLU, rounded once to bf16 (bits)."""
+    x = bf16_to_f64(allgather_rows(x_shards))
+    h = x @ bf16_to_f64(np.asarray(w1_r, dtype=np.uint16))
+    return f64_to_bf16_bits(np.maximum(h, 0.0))
+
+
+def mlp_ag_rs(x_shards, w1_list, w2_list, out: str = "bf16", rows=None):
+    """Tensor-parallel MLP over R ranks, the chained AllGather+GEMM -> ReLU ->
+    GEMM+ReduceScatter layer: X = gather_r(X_r) (rank order); H_r =
+    bf16(ReLU(X @ W1_r)); S = sum_r H_r @ W2_r; rank o receives rows
+    [o*m, (o+1)*m) of S (m = rows per shard), rounded once.
+    rows: optional sample of S's rows (then returns (H list, S rows rounded)).
+    Returns dict(gathered=bits, hidden=[H_r bits], blocks=[per rank o])."""
+    R = len(x_shards)
+    m = np.asarray(x_shards[0]).shape[0]
+    gathered = allgather_rows(x_shards)
+    hidden = [mlp_hidden(x_shards, w1_list[r]) for r in range(R)]
+    sel = slice(None) if rows is None else np.asarray(rows, dtype=np.int64)
+    s = sum(bf16_to_f64(hidden[r][sel]) @ bf16_to_f64(np.asarray(w2_list[r], dtype=np.uint16))
+            for r in range(R))
+    if rows is not None:
+        return dict(gathered=gathered, hidden=hidden, rows=round_out(s, out))
+    blocks = [round_out(s[o * m:(o + 1) * m], out) for o in range(R)]
+    return dict(gathered=gathered, hidden=hidden, blocks=blocks)
 
 
 # ----------------------------------------------------------------------------

@@ -439,6 +439,61 @@ def test_combine_seg_from_counts_and_coverage_check():
         O.moe_return_rows([np.zeros((1, 2), np.uint16)], [np.array([0])], topk=2, T=1, R=1)
 
 
+# ---------------------------------------------------------------- chained MLP (AG+GEMM -> ReLU -> GEMM+RS)
+
+def test_mlp_brute_force_tiny():
+    # triple loops: gather in rank order, ReLU, bf16 rounding of H, sum over ranks, owner blocks
+    R, m, h, f = 2, 2, 3, 2
+    x = [rand_int_bits((m, h), 600 + r) for r in range(R)]
+    w1 = [rand_int_bits((h, f), 610 + r) for r in range(R)]
+    w2 = [rand_int_bits((f, h), 620 + r) for r in range(R)]
+    res = O.mlp_ag_rs(x, w1, w2, out="f32")
+    X = np.concatenate([O.bf16_to_f64(v) for v in x], 0)
+    S = np.zeros((R * m, h))
+    for r in range(R):
+        H = brute_matmul(X, O.bf16_to_f64(w1[r]))
+        H = np.where(H > 0, H, 0.0)
+        Hb = O.bf16_to_f64(O.f64_to_bf16_bits(H))
+        np.testing.assert_array_equal(res["hidden"][r], O.f64_to_bf16_bits(H))
+        S += brute_matmul(Hb, O.bf16_to_f64(w2[r]))
+    for o in range(R):
+        np.testing.assert_array_equal(res["blocks"][o], S[o * m:(o + 1) * m].astype(np.float32))
+
+
+def test_mlp_relu_kills_negative_preactivations():
+    # W1 = -I: every pre-activation is -x, so H = ReLU(-x) keeps only the negative inputs
+    R, m, h = 2, 3, 4
+    x = [rand_int_bits((m, h), 630 + r) for r in range(R)]
+    w1 = [bf(-np.eye(h)) for _ in range(R)]
+    hid = O.mlp_hidden(x, w1[0])
+    X = np.concatenate([O.bf16_to_f64(v) for v in x], 0)
+    np.testing.assert_array_equal(O.bf16_to_f64(hid), np.maximum(-X, 0))
+
+
+def test_mlp_identity_weights_closed_form():
+    # W1_r = I on rank 0 only (others zero), W2_0 = I: the layer returns ReLU(x) row blocks
+    R, m, h = 3, 2, 5
+    x = [rand_int_bits((m, h), 640 + r) for r in range(R)]
+    eye, zero = bf(np.eye(h)), bf(np.zeros((h, h)))
+    w1 = [eye] + [zero] * (R - 1)
+    w2 = [eye] + [zero] * (R - 1)
+    res = O.mlp_ag_rs(x, w1, w2, out="f32")
+    for o in range(R):
+        np.testing.assert_array_equal(res["blocks"][o],
+                                      np.maximum(O.bf16_to_f64(x[o]), 0).astype(np.float32))
+
+
+def test_mlp_row_sample_matches_full_and_rank_blocks_tile():
+    R, m, h, f = 4, 3, 6, 5
+    x = [rand_int_bits((m, h), 650 + r) for r in range(R)]
+    w1 = [rand_int_bits((h, f), 660 + r) for r in range(R)]
+    w2 = [rand_int_bits((f, h), 670 + r) for r in range(R)]
+    full = O.mlp_ag_rs(x, w1, w2)
+    rows = np.array([0, 5, 11])
+    part = O.mlp_ag_rs(x, w1, w2, rows=rows)
+    np.testing.assert_array_equal(part["rows"], np.concatenate(full["blocks"], 0)[rows])
+
+
 def test_norm_scale():
     assert O.norm_scale(16, 2.0, 0.5) == 4.0
 
