@@ -281,7 +281,7 @@ def main():
     ap.add_argument("--n-copy", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
-    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine"], default=None,
+    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp"], default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -437,6 +437,8 @@ def run_only(args):
     bf16_peak, _, hbm_peak, _ = peaks()
     if args.only == "moe":
         res = bench_moe(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    elif args.only == "mlp":
+        res = bench_mlp(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
     elif args.only == "combine":
         res = bench_moe_combine(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
                                 hbm_peak)
@@ -496,6 +498,9 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         torch.cuda.empty_cache()
         out[I.MOE_COMBINE_R8_E64.name] = bench_moe_combine(mk, device, stream, dist, steps, seed_off,
                                                            tmax, bf16_peak, hbm_peak)
+        torch.cuda.empty_cache()
+        out[I.MLP_R8_TP8.name] = bench_mlp(mk, device, stream, dist, max(3, steps // 3), seed_off, tmax,
+                                           bf16_peak, hbm_peak)
         torch.cuda.empty_cache()
     return out
 
@@ -591,6 +596,33 @@ def bench_moe_combine(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak
             "roofline_ms": 1e3 * max(t_tensor, t_hbm),
             "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
             "status": mk.status_string(st)}
+
+
+def bench_mlp(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+    """Chained TP MLP (AllGather+GEMM -> ReLU -> GEMM+ReduceScatter): fused, GEMM-only
+    (pre-gathered input, ranks summed in tensor memory) and unfused (four launches)."""
+    w = I.MLP_R8_TP8
+    M = w.R * w.m
+    x = [dev_normal((w.m, w.h), 1.0, w.x_seed + r + seed_off, device) for r in range(w.R)]
+    w1 = [dev_normal((w.h, w.f_r), w.w_std, w.w1_seed + r + seed_off, device) for r in range(w.R)]
+    w2 = [dev_normal((w.f_r, w.h), w.w_std, w.w2_seed + r + seed_off, device) for r in range(w.R)]
+    xg = torch.empty((M, w.h), dtype=torch.bfloat16, device=device)
+    hid = [torch.empty((M, w.f_r), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+    y = [torch.empty((w.m, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+    ws = mk.Workspace(device)
+    res = {}
+    for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                      ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        def step(i, cfg=cfg):
+            mk.mlp_ag_rs(x, w1, w2, x_gathered=xg, hid=hid, y_blocks=y, cfg=cfg, workspace=ws,
+                         stream=stream)
+        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+    st, _ = mk.device_status(ws, stream)
+    flops = w.flops()
+    fused_tf = flops / (res["fused"] * 1e-3) / 1e12
+    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "status": mk.status_string(st)}
 
 
 if __name__ == "__main__":

@@ -99,6 +99,11 @@ def lib() -> ctypes.CDLL:
         L.mk_moe_combine.restype = i
         L.mk_moe_combine.argtypes = [P(vp), P(vp), P(vp), P(vp), vp, i, i, i, ll, ll, ll, ll,
                                      P(vp), P(vp), vp, sz, P(_Cfg), vp]
+        L.mk_mlp_workspace_size.restype = sz
+        L.mk_mlp_workspace_size.argtypes = [i, ll, ll, ll, P(_Cfg)]
+        L.mk_mlp_ag_rs.restype = i
+        L.mk_mlp_ag_rs.argtypes = [P(vp), P(vp), P(vp), i, ll, ll, ll, vp, P(vp), P(vp), vp, sz,
+                                   P(_Cfg), vp]
         L.mk_moe_dispatch_gemm.restype = i
         L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
                                            P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
@@ -323,7 +328,40 @@ def moe_combine(h, w2, gates, recv_src, counts, *, E_loc: int, topk: int = 2,
     return o
 
 
+def mlp_workspace_size(R, m, h, f_r, cfg: Config | None = None) -> int:
+    return int(lib().mk_mlp_workspace_size(R, m, h, f_r, _cfgp(cfg)))
+
+
+def mlp_ag_rs(x_shards, w1, w2, *, x_gathered=None, hid=None, y_blocks=None,
+              cfg: Config | None = None, workspace: Workspace | None = None, stream=None):
+    """Chained tensor-parallel MLP over R virtual ranks: AllGather + GEMM (w1[r]) ->
+    ReLU -> GEMM (w2[r]) + ReduceScatter.  x_shards[r]: [m x h]; w1[r]: [h x f_r];
+    w2[r]: [f_r x h] (bf16).  Returns (x_gathered [R*m x h], hid [R x [R*m x f_r]],
+    y_blocks [R x [m x h]])."""
+    R = len(x_shards)
+    m, h = x_shards[0].shape
+    f_r = w1[0].shape[1]
+    dev = x_shards[0].device
+    bf = torch.bfloat16
+    if x_gathered is None:
+        x_gathered = torch.empty((R * m, h), dtype=bf, device=dev)
+    if hid is None:
+        hid = [torch.empty((R * m, f_r), dtype=bf, device=dev) for _ in range(R)]
+    if y_blocks is None:
+        y_blocks = [torch.empty((m, h), dtype=bf, device=dev) for _ in range(R)]
+    ws = _ws(workspace, dev)
+    nb = mlp_workspace_size(R, m, h, f_r, cfg)
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, "mk_mlp_workspace_size")
+    buf = ws.get(nb)
+    st = lib().mk_mlp_ag_rs(_ptrs(x_shards), _ptrs(w1), _ptrs(w2), R, m, h, f_r, x_gathered.data_ptr(),
+                            _ptrs(hid), _ptrs(y_blocks), buf.data_ptr(), buf.numel(), _cfgp(cfg),
+                            _stream(stream, dev))
+    _check(st, "mk_mlp_ag_rs")
+    return x_gathered, hid, y_blocks
+
+
 __all__ = ["Config", "MkError", "Workspace", "ag_gemm", "gemm_rs", "gemm_ar", "device_status",
            "workspace_size", "lib", "status_string", "MODE_FUSED", "MODE_GEMM_ONLY",
            "MODE_UNFUSED", "moe_dispatch_gemm", "moe_workspace_size", "moe_combine",
-           "moe_combine_workspace_size"]
+           "moe_combine_workspace_size", "mlp_ag_rs", "mlp_workspace_size"]

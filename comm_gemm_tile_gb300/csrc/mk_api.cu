@@ -245,6 +245,7 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
   p.flags = reinterpret_cast<uint32_t*>(ws + pl.flags_off);
+  p.chunk_cnt = p.flags;
   p.staging = reinterpret_cast<float*>(ws + pl.staging_off);
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
@@ -274,7 +275,15 @@ bool use_pair(const mk_config* cfg, int sms) {
 // Launch of compute CTAs only (no copy-role or reduce-role CTAs): CTA pairs
 // on 256 x 256 tiles when wanted and the device co-schedules them, else one
 // CTA per 128 x 256 tile.  Sets the item count for the chosen shape.
-static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t s) {
+// Chained MLP: phases = 1 (up-projection items only), 2 (down-projection only), 3 (both).
+static void set_items(FusedParams& p, int per, int mlp_phases) {
+  p.n_items = p.n_sched * per;
+  if (p.op != OP_MLP) return;
+  p.mlp_n1 = (mlp_phases & 1) ? p.n_mrow * p.R * p.mlp_nb1 : 0;
+  p.n_items = p.mlp_n1 + ((mlp_phases & 2) ? p.n_items : 0);
+}
+
+static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t s, int mlp_phases = 3) {
   const int per = (p.op == OP_AG || p.mode == MK_MODE_GEMM_ONLY) ? 1 : p.P;
   if (pair && p.op != OP_MOE) {
     const int clusters = std::min(max_pair_clusters(), sms / 2);
@@ -282,7 +291,7 @@ static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t
       p.pair = 1;
       p.n_mrow = (p.n_mblk + 1) / 2;
       p.n_sched = p.n_mrow * p.n_nblk;
-      p.n_items = p.n_sched * per;
+      set_items(p, per, mlp_phases);
       const int n_pairs = std::min(clusters, p.n_items);
       if (n_pairs <= 0) return MK_OK;
       p.group_tiles = std::max(1, std::min(n_pairs, p.n_sched));
@@ -295,10 +304,14 @@ static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t
   p.pair = 0;
   p.n_mrow = p.n_mblk;
   p.n_sched = p.n_mblk * p.n_nblk;
-  p.n_items = p.n_sched * per;
+  set_items(p, per, mlp_phases);
   const int n = std::min(sms, p.n_items);
+  if (n <= 0) return MK_OK;
   p.group_tiles = std::max(1, std::min(n, p.n_sched));
-  return launch(p, 0, n, 0, s);
+  p.n_copy = 0;
+  p.n_compute = n;
+  p.n_reduce = 0;
+  return launch_fused(p, n, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 
 int grid_cap(const mk_config* cfg) {
@@ -524,6 +537,148 @@ mk_status mk_gemm_ar(const void* const* a, const void* const* b, void* const* c_
                      mk_dtype c_dtype, int R, long long m, long long n, long long k, void* workspace,
                      size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
   return rs_ar_common(OP_AR, a, b, c_replicas, c_dtype, R, m, n, k, workspace, ws_bytes, cfg, stream);
+}
+
+}  // extern "C"
+
+namespace mk {
+namespace {
+
+// Workspace of the chained MLP: header | AG chunk counters | H_r row-block
+// counters | the down-projection's GEMM+ReduceScatter flags and staging.
+struct MlpLayout {
+  Plan pl;
+  size_t chunk_off, cnt_off, flags_off, staging_off, total;
+};
+
+bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* cfg, MlpLayout& L) {
+  if (R < 1 || R > MK_MLP_MAX_RANKS || m < 0 || h < 0 || f_r < 0) return false;
+  if ((h % 8) || (f_r % 8)) return false;
+  if (cfg && (cfg->reduce == 2 || cfg->n_reduce_ctas > 0 || cfg->split_k > 1)) return false;
+  if (!plan_gemm(OP_RS, R, static_cast<long long>(R) * m, h, f_r, cfg, L.pl)) return false;
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  size_t off = WS_HDR_BYTES;
+  L.chunk_off = off;  off = al(off + static_cast<size_t>(L.pl.n_mblk) * COPY_SUB_MAX * 4);
+  L.cnt_off = off;    off = al(off + static_cast<size_t>(R) * L.pl.n_mblk * 4);
+  L.flags_off = off;  off = off + L.pl.n_flags * 4;
+  off = (off + 1023) & ~static_cast<size_t>(1023);
+  L.staging_off = off;
+  L.total = off + L.pl.staging_bytes;
+  return true;
+}
+
+}  // namespace
+}  // namespace mk
+
+extern "C" {
+
+size_t mk_mlp_workspace_size(int R, long long m, long long h, long long f_r, const mk_config* cfg) {
+  MlpLayout L;
+  if (!mlp_plan(R, m, h, f_r, cfg, L)) return 0;
+  return L.total;
+}
+
+mk_status mk_mlp_ag_rs(const void* const* x_shards, const void* const* w1, const void* const* w2, int R,
+                       long long m, long long h, long long f_r, void* x_gathered, void* const* hid,
+                       void* const* y_blocks, void* workspace, size_t ws_bytes, const mk_config* cfg,
+                       mk_stream_t stream) {
+  if (!x_shards || !w1 || !w2 || !hid || !y_blocks || !workspace) return MK_ERR_INVALID;
+  MlpLayout L;
+  if (!mlp_plan(R, m, h, f_r, cfg, L)) return MK_ERR_INVALID;
+  if (ws_bytes < L.total || !aligned16(workspace)) return MK_ERR_INVALID;
+  const long long M = static_cast<long long>(R) * m;
+  for (int r = 0; r < R; ++r) {
+    if (!buf_ok(x_shards[r], m * h) || !buf_ok(w1[r], h * f_r) || !buf_ok(w2[r], f_r * h) ||
+        !buf_ok(hid[r], M * f_r) || !buf_ok(y_blocks[r], m * h))
+      return MK_ERR_INVALID;
+  }
+  if (!buf_ok(x_gathered, M * h)) return MK_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m == 0 || h == 0) return MK_OK;
+  if (f_r == 0) {   // no hidden units: every output is zero, the gathered input is still produced
+    mk_status st = zero_outputs(y_blocks, R, static_cast<size_t>(m) * h * 2, s);
+    if (st != MK_OK) return st;
+    for (int r = 0; r < R; ++r)
+      if (cudaMemcpyAsync(static_cast<uint8_t*>(x_gathered) + static_cast<size_t>(r) * m * h * 2, x_shards[r],
+                          static_cast<size_t>(m) * h * 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MK_ERR_CUDA;
+    return MK_OK;
+  }
+  const int sms = grid_cap(cfg);
+  if (sms <= 0) return MK_ERR_UNSUPPORTED;
+  const Plan& pl = L.pl;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  FusedParams p;
+  fill_common(p, pl, ws, cfg, MK_BF16);
+  p.op = OP_MLP;
+  p.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
+  p.staging = reinterpret_cast<float*>(ws + L.staging_off);
+  p.chunk_cnt = reinterpret_cast<uint32_t*>(ws + L.chunk_off);
+  p.mlp_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt_off);
+  p.K = static_cast<int>(h);      // gathered row width (copy-in)
+  p.N = static_cast<int>(h);      // down-projection output width
+  p.m_r = static_cast<int>(m);
+  p.rows_per_owner = static_cast<int>(m);
+  p.mlp_f = static_cast<int>(f_r);
+  p.mlp_nb1 = static_cast<int>(ceil_div_ll(f_r, BN));
+  p.mlp_kb1 = static_cast<int>(ceil_div_ll(h, BK));
+  p.mlp_wait = 1;
+  p.gathered = static_cast<uint8_t*>(x_gathered);
+  p.copy_local = 1;
+  p.ordered = 0;
+  p.n_copy_chunks = pl.n_mblk;
+  for (int r = 0; r < R; ++r) {
+    p.shard[r] = static_cast<const uint8_t*>(x_shards[r]);
+    p.out[r] = y_blocks[r];
+    p.mlp_hid[r] = static_cast<uint8_t*>(hid[r]);
+  }
+  const bool pair = use_pair(cfg, sms);
+  p.b_one_box = (h % 64 == 0 && f_r % 64 == 0) ? 1 : 0;
+  const uint32_t chunks = pair ? 2 : 4;
+  if (!make_map_a(&p.tmA[0], x_gathered, h, M, static_cast<size_t>(h) * 2)) return MK_ERR_CUDA;
+  for (int r = 0; r < R; ++r) {
+    if (!make_map_a(&p.tmA[1 + r], hid[r], f_r, M, static_cast<size_t>(f_r) * 2)) return MK_ERR_CUDA;
+    const bool ok1 = p.b_one_box ? make_map_b_chunks(&p.tmB[r], w1[r], h, f_r, chunks)
+                                 : make_map_2d(&p.tmB[r], w1[r], f_r, h, static_cast<size_t>(f_r) * 2, 64, BK);
+    const bool ok2 = p.b_one_box ? make_map_b_chunks(&p.tmB[R + r], w2[r], f_r, h, chunks)
+                                 : make_map_2d(&p.tmB[R + r], w2[r], h, f_r, static_cast<size_t>(h) * 2, 64, BK);
+    if (!ok1 || !ok2) return MK_ERR_CUDA;
+  }
+  int pr = 1;
+  while (pr < BM && static_cast<long long>(pr) * h * 2 < MK_CW_PIECE_BYTES) pr *= 2;
+  p.copy_rows = pr;
+  p.n_cw = std::min(2, N_COPY_WARPS);
+
+  if (pl.mode == MK_MODE_FUSED) {
+    p.copy_warps = 1;
+    return launch_compute(p, pair, sms, s, 3);
+  }
+  if (pl.mode == MK_MODE_GEMM_ONLY) {   // x_gathered as already filled; ranks summed in TMEM
+    return launch_compute(p, pair, sms, s, 3);
+  }
+  // Unfused, host-ordered: copy-in launch, up-projection launch, then the
+  // down-projection as partial tiles and a reduce launch.
+  const uint32_t e = p.epoch;
+  p.copy_sub = COPY_SUB_MAX;
+  uint32_t* chain_flags = p.flags;
+  p.flags = p.chunk_cnt;          // copy-role sub-chunk flags
+  mk_status st = launch(p, std::min(sms, std::max(1, p.n_copy_chunks * COPY_SUB_MAX)), 0, 0, s);
+  if (st != MK_OK) return st;
+  p.flags = chain_flags;
+  p.epoch = e;
+  p.mode = MK_MODE_GEMM_ONLY;
+  st = launch_compute(p, pair, sms, s, 1);
+  if (st != MK_OK) return st;
+  p.epoch = e;
+  p.mode = MK_MODE_UNFUSED;
+  p.mlp_wait = 0;                  // the hidden activations are complete
+  st = launch_compute(p, pair, sms, s, 2);
+  if (st != MK_OK) return st;
+  p.epoch = e;
+  p.mlp_n1 = 0;
+  p.n_items = pl.n_tiles * pl.P;
+  return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
 }
 
 }  // extern "C"

@@ -86,7 +86,7 @@ __device__ __noinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, 
 // the counters at kernel start and then releases hdr[HDR_READY] = epoch;
 // nobody touches a counter before seeing that word.
 __device__ __forceinline__ uint32_t* chunk_counter(const FusedParams& p, int mb) {
-  return p.flags + static_cast<size_t>(mb) * COPY_SUB_MAX;
+  return p.chunk_cnt + static_cast<size_t>(mb) * COPY_SUB_MAX;
 }
 __device__ __forceinline__ int chunk_pieces(const FusedParams& p, int mb) {
   const int rows = min(BM, p.M - mb * BM);
@@ -125,6 +125,8 @@ struct Item {
   int bz;           // MoE: local expert (3-D B map); -1 = 2-D B map
   int row_lo, row_hi;  // valid tile rows [row_lo, row_hi) (tile-relative)
   int out_row0;     // output row of tile row 0
+  int phase;        // chained MLP: 1 = up-projection tile (of rank hid_r), 2 = down-projection; else 0
+  int hid_r;
 };
 
 // Grouped raster over (m-position, n-block): group_m m-positions per group,
@@ -190,6 +192,36 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
   it.nkb = p.n_kblk;
   it.row_lo = 0;
   it.row_hi = BM;
+  it.phase = 0;
+  it.hid_r = 0;
+  if (p.op == OP_MLP && i < p.mlp_n1) {
+    // up-projection of every rank, row-block major so that a block of H_r
+    // completes early: item = (m-position, rank, n-block), n-block innermost
+    const int per_m = p.R * p.mlp_nb1;
+    int pos = i / per_m;
+    const int rem = i - pos * per_m;
+    it.hid_r = rem / p.mlp_nb1;
+    it.nb = rem - it.hid_r * p.mlp_nb1;
+    it.phase = 1;
+    it.amap = 0;
+    it.bmap = it.hid_r;
+    it.nkb = p.mlp_kb1;
+    if (p.pair) pos = 2 * pos + rank;
+    if (pos >= p.n_mblk) {
+      empty_half(it, pos);
+      return true;
+    }
+    it.mb = pos;
+    it.arow = pos * BM;
+    it.out_row0 = pos * BM;
+    it.row_hi = min(BM, p.M - it.out_row0);
+    if (p.mode == MK_MODE_FUSED) it.wait_chunk = pos;
+    return true;
+  }
+  if (p.op == OP_MLP) {
+    i -= p.mlp_n1;
+    it.phase = 2;
+  }
   if (p.op == OP_AG) {
     int pos = i / p.n_nblk;
     it.nb = i - pos * p.n_nblk;
@@ -214,7 +246,7 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
     it.row_hi = min(BM, p.M - it.out_row0);
     return true;
   }
-  if (p.op == OP_RS || p.op == OP_AR) {
+  if (p.op == OP_RS || p.op == OP_AR || p.op == OP_MLP) {
     if (p.mode == MK_MODE_GEMM_ONLY) {
       raster(p, i, it.mb, it.nb);
       it.nseg = p.R;
@@ -242,6 +274,10 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
       it.kb0 = ks * p.kps;
       it.nkb = min(p.kps, p.n_kblk - it.kb0);
       it.slot = (it.mb * p.n_nblk + it.nb) * p.P + part;
+    }
+    if (p.op == OP_MLP) {   // A = H_r (maps 1..R), B = W2_r (maps R..2R-1)
+      it.amap += 1;
+      it.bmap += p.R;
     }
     if (it.mb >= p.n_mblk) {
       empty_half(it, it.mb);
@@ -357,6 +393,18 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
     for (int seg = 0; seg < it.nseg; ++seg) {
       const CUtensorMap* ma = &p.tmA[it.amap + seg];
       const CUtensorMap* mbm = &p.tmB[it.bmap + seg];
+      if (it.phase == 2 && it.row_hi > 0 && p.mlp_wait) {
+        // chained MLP: every up-projection tile of this row block of H_r has been stored
+        if (!counters_ready) {
+          if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_PRODUCER, i)) goto done;
+          counters_ready = true;
+        }
+        const int r = it.amap + seg - 1;
+        if (!wait_count(p, p.mlp_cnt + static_cast<size_t>(r) * p.n_mblk + it.mb,
+                        static_cast<uint32_t>(p.mlp_nb1), i))
+          goto done;
+        fence_proxy_async_global();
+      }
       for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
         if (!wait_bar(p, S.empty(stage), phase ^ 1u, WHERE_PRODUCER, i)) goto done;
         const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB;
@@ -560,7 +608,7 @@ __device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, i
       r[4 * q + 2] = __float_as_uint(acc[q].z);
       r[4 * q + 3] = __float_as_uint(acc[q].w);
     }
-    if (p.op == OP_RS) {
+    if (p.op != OP_AR) {
       const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
       uint8_t* ob = reinterpret_cast<uint8_t*>(p.out[o]);
       store_row_chunk(ob + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
@@ -827,6 +875,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   const size_t esz = p.out_f32 ? 4 : 2;
   int buf = 0;
   uint32_t acc_phase = 0;
+  uint32_t pd_par = 0;           // phase bit of pdone(b) in bit b
   bool counters_ready = false;   // last-arrival counters published for this call
   const int n_items = n_items_for(p);
   for (int i = cid; i < n_items; i += p.n_compute) {
@@ -885,7 +934,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
           const int col = n0 + 32 * c;
           const int nvalid = max(0, min(32, p.N - col));
           if (row_ok && nvalid > 0) {
-            if (p.op == OP_RS) {
+            if (p.op != OP_AR) {   // RS and the chained MLP: the owner's row block
               const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
               uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
               store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
@@ -949,6 +998,21 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         acc_phase ^= 1u;
       }
       continue;
+    } else if (it.phase == 1) {
+      // chained MLP up-projection: H_r = bf16(ReLU(acc)) into rank hid_r's hidden buffer
+      uint8_t* hrow = p.mlp_hid[it.hid_r] + static_cast<size_t>(grow) * p.mlp_f * 2;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+        const int col = n0 + 32 * c;
+        const int nvalid = max(0, min(32, p.mlp_f - col));
+        if (!row_ok || nvalid == 0) continue;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(fmaxf(__uint_as_float(r[q]), 0.f));
+        store_row_chunk(hrow + static_cast<size_t>(col) * 2, r, nvalid, false);
+      }
     } else if (it.slot >= 0) {
       // Partial tile -> staging slot.  Layout: float4 (row, column group cg)
       // at index cg*BM + row, so a warp's 32 rows form 512 contiguous bytes.
@@ -976,7 +1040,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         if (p.op == OP_AG || p.op == OP_MOE) {
           uint8_t* base = reinterpret_cast<uint8_t*>(p.out[p.op == OP_MOE ? it.mb : 0]);
           store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
-        } else if (p.op == OP_RS) {
+        } else if (p.op == OP_RS || p.op == OP_MLP) {
           const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
           uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
           store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
@@ -991,20 +1055,29 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     // Tensor memory of this buffer may be overwritten by the next tile's MMAs.
     tc_fence_before();
     __syncwarp();
+    // A tile that others wait for (a partial tile, an up-projection tile of
+    // the chained MLP) is published once all four warps have stored it.  The
+    // per-buffer barrier completes once per such tile, so it keeps its own
+    // phase bit (items that publish nothing do not use it).
+    const bool publish = it.slot >= 0 || (it.phase == 1 && it.row_hi > 0);
     if (lane == 0) {
       release_tmem<PAIR>(S, buf, rank);
-      if (it.slot >= 0) mbar_arrive(S.pdone(buf));
+      if (publish) mbar_arrive(S.pdone(buf));
     }
-    if (it.slot >= 0 && warp == 2 && lane == 0) {
-      // All four epilogue warps have stored their rows of this partial tile
-      // (bounded wait on the per-buffer barrier), then one gpu-scope release.
-      if (!wait_bar(p, S.pdone(buf), acc_phase, WHERE_EPILOGUE, i)) return;
-      const bool skip = (p.inject == 2 && it.slot == 0);
-      if (!skip) {
+    if (publish && warp == 2 && lane == 0) {
+      if (!wait_bar(p, S.pdone(buf), (pd_par >> buf) & 1u, WHERE_EPILOGUE, i)) return;
+      if (it.phase == 1) {
         __threadfence();
-        st_release_gpu(p.flags + it.slot, p.epoch);
+        atomicAdd(p.mlp_cnt + static_cast<size_t>(it.hid_r) * p.n_mblk + it.mb, 1u);
+      } else {
+        const bool skip = (p.inject == 2 && it.slot == 0);
+        if (!skip) {
+          __threadfence();
+          st_release_gpu(p.flags + it.slot, p.epoch);
+        }
       }
     }
+    if (publish) pd_par ^= 1u << buf;
     if (++buf == 2) {
       buf = 0;
       acc_phase ^= 1u;
@@ -1580,7 +1653,7 @@ __device__ void reduce_role(const FusedParams& p, uint8_t* smem, int rid) {
       for (int o = 0; o < nrep; ++o) {
         uint8_t* base;
         size_t off;
-        if (p.op == OP_RS) {
+        if (p.op != OP_AR) {   // RS and the chained MLP: the owner's row block
           const int ow = grow / p.rows_per_owner;
           base = reinterpret_cast<uint8_t*>(p.out[ow]);
           off = (static_cast<size_t>(grow - ow * p.rows_per_owner) * p.N + col) * esz;
@@ -1633,11 +1706,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
   }
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
-  if (t == 0 && ((p.op == OP_AG && p.copy_warps) || p.last_arrival)) {
+  if (t == 0 && ((p.op == OP_AG && p.copy_warps) || p.last_arrival || p.op == OP_MLP)) {
     // Zero this call's counters (the workspace may hold anything from earlier
     // calls of any op), then publish them.
     if (p.op == OP_AG) {
       for (int mb = threadIdx.x; mb < p.n_mblk; mb += NTHREADS) *chunk_counter(p, mb) = 0u;
+    } else if (p.op == OP_MLP) {
+      if (p.copy_warps)
+        for (int mb = threadIdx.x; mb < p.n_mblk; mb += NTHREADS) *chunk_counter(p, mb) = 0u;
+      for (int x = threadIdx.x; x < p.R * p.n_mblk; x += NTHREADS) p.mlp_cnt[x] = 0u;
     } else {
       for (int x = threadIdx.x; x < p.n_tiles * 4; x += NTHREADS) p.flags[x] = 0u;
     }

@@ -56,7 +56,7 @@ constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chu
 enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_READY = 4, HDR_WORDS = 64 };
 constexpr size_t WS_HDR_BYTES = 256;
 
-enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3, OP_MOE_COMBINE = 4 };
+enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3, OP_MOE_COMBINE = 4, OP_MLP = 5 };
 
 // Role codes used in the error detail word.
 enum { WHERE_PRODUCER = 1, WHERE_MMA = 2, WHERE_EPILOGUE = 3, WHERE_COPY = 4, WHERE_REDUCE = 5,
@@ -111,6 +111,14 @@ struct FusedParams {
   uint8_t* moe_ret[MK_MAX_RANKS];        // [T x topk x N] bf16 returned expert rows per source rank
   const float* moe_gates[MK_MAX_RANKS];  // [T x topk] gate weights per source rank
   uint32_t* moe_cnt;                     // [R*T x n_nblk] slots landed per (token, 256-col block)
+  // AG copy-in chunk counters (one per 128-row chunk, COPY_SUB_MAX words apart)
+  uint32_t* chunk_cnt;
+  // Chained MLP: phase 1 = up-projection tiles of every rank (items 0 .. mlp_n1-1),
+  // phase 2 = the down-projection GEMM+ReduceScatter items after them
+  uint8_t* mlp_hid[MK_MAX_RANKS];        // [M x mlp_f] bf16 hidden activations per rank
+  uint32_t* mlp_cnt;                     // [R x n_mblk] phase-1 tiles done per (rank, row block)
+  int mlp_n1, mlp_nb1, mlp_kb1, mlp_f;   // phase-1 items, n-blocks, k-blocks; hidden width
+  int mlp_wait;                          // 1 = phase-2 tiles wait for their H_r row block
   int b_one_box;       // 1 = tmB maps are [64 cols, K, N/64 chunks (, experts)] views and a
                        //     stage's B tile (4 column chunks, 2 per CTA of a pair) is one TMA request
   int pair;            // 1 = launched as clusters of 2 CTAs sharing 256 x 256 tiles; items then
@@ -131,6 +139,7 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
 // Clusters of two CTAs of the fused kernel that fit on the device at once (0 on error).
 int max_pair_clusters();
 constexpr int MOE_MAX_E = 256;        // experts in total (R * E_loc)
+static_assert(2 * MK_MLP_MAX_RANKS <= MK_MAX_RANKS, "the MLP holds W1_r and W2_r maps");
 constexpr int MOE_MAX_TOPK = 8;
 int device_sm_count();
 uint32_t next_epoch();

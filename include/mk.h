@@ -220,6 +220,37 @@ mk_status mk_moe_combine(const void *const *h, const void *const *w2, const floa
                          void *const *ret, void *const *out, void *workspace, size_t ws_bytes,
                          const mk_config *cfg, mk_stream_t stream);
 
+/* Ranks the chained MLP supports (it holds W1_r and W2_r tensor maps for every rank). */
+#define MK_MLP_MAX_RANKS 8
+
+/* Workspace bytes for mk_mlp_ag_rs (0 on bad args or an unsupported config). */
+size_t mk_mlp_workspace_size(int R, long long m, long long h, long long f_r, const mk_config *cfg);
+
+/* Chained tensor-parallel MLP layer: "AllGather + GEMM" -> ReLU -> "GEMM +
+ * ReduceScatter" (five-kernel table, those two rows; chained in one
+ * persistent kernel as the roadmap's multi-step kernel folds fused steps into
+ * one launch), over R virtual ranks:
+ *   x_gathered = [x_0; ...; x_{R-1}]                  ([R*m x h] bf16, written)
+ *   hid[r]     = bf16(ReLU(x_gathered @ w1[r]))       ([R*m x f_r] bf16, written)
+ *   S          = sum_r hid[r] @ w2[r]                 (fp32, ranks summed in order 0..R-1)
+ *   y_blocks[o] = bf16(rows [o*m, (o+1)*m) of S)      ([m x h] bf16)
+ * x_shards[r]: [m x h]; w1[r]: [h x f_r] (column shard of the up-projection);
+ * w2[r]: [f_r x h] (row shard of the down-projection); all bf16, device.
+ * In one launch, copy warps gather x, the up-projection tiles of every rank
+ * start as their row chunk lands, and each down-projection tile starts once
+ * the row block of hid[r] it reads is complete; its partial sums run through
+ * the running-sum reduction of mk_gemm_rs.  The virtual ranks share one
+ * gathered x (every rank's copy would hold the same rows).
+ * R <= MK_MLP_MAX_RANKS; h and f_r multiples of 8.  mode: FUSED; GEMM_ONLY
+ * (x_gathered as already filled, ranks summed in tensor memory); UNFUSED
+ * (copy launch, up-projection launch, partial-tile launch, reduce launch).
+ * Configs with split_k > 1, reduce = 2 or n_reduce_ctas > 0 are rejected
+ * (MK_ERR_INVALID). */
+mk_status mk_mlp_ag_rs(const void *const *x_shards, const void *const *w1, const void *const *w2,
+                       int R, long long m, long long h, long long f_r, void *x_gathered,
+                       void *const *hid, void *const *y_blocks, void *workspace, size_t ws_bytes,
+                       const mk_config *cfg, mk_stream_t stream);
+
 /* Size of the library's own scratch array used by mk_ag_gemm_noalloc (bytes). */
 #define MK_NOALLOC_SCRATCH_BYTES 65536
 

@@ -339,11 +339,15 @@ def moe_combine(h_list, recv_src_list, counts, w2_list, gates_list, E_loc: int, 
     return dict(y2=y2, ret=ret, out=res)
 
 
-def mlp_hidden(x_shards, w1_r) -> np.ndarray:
+def mlp_hidden(x_shards, w1_r, rows=None) -> np.ndarray:
     """Up-projection of one rank in the tensor-parallel MLP: the gathered input
-    times the rank's column shard W1_r, ReLU, rounded once to bf16 (bits)."""
-    x = bf16_to_f64(allgather_rows(x_shards))
-    h = x @ bf16_to_f64(np.asarray(w1_r, dtype=np.uint16))
+    times the rank's column shard W1_r, ReLU, rounded once to bf16 (bits).
+    rows: optional sample of the gathered rows (each hidden row depends only
+    on the input row of the same index)."""
+    xg = allgather_rows(x_shards)
+    if rows is not None:
+        xg = xg[np.asarray(rows, dtype=np.int64)]
+    h = bf16_to_f64(xg) @ bf16_to_f64(np.asarray(w1_r, dtype=np.uint16))
     return f64_to_bf16_bits(np.maximum(h, 0.0))
 
 
@@ -352,16 +356,16 @@ def mlp_ag_rs(x_shards, w1_list, w2_list, out: str = "bf16", rows=None):
     GEMM+ReduceScatter layer: X = gather_r(X_r) (rank order); H_r =
     bf16(ReLU(X @ W1_r)); S = sum_r H_r @ W2_r; rank o receives rows
     [o*m, (o+1)*m) of S (m = rows per shard), rounded once.
-    rows: optional sample of S's rows (then returns (H list, S rows rounded)).
+    rows: optional sample of S's rows (then hidden holds those rows only and
+    the result is dict(gathered, hidden, rows=S rows rounded)).
     Returns dict(gathered=bits, hidden=[H_r bits], blocks=[per rank o])."""
     R = len(x_shards)
     m = np.asarray(x_shards[0]).shape[0]
     gathered = allgather_rows(x_shards)
-    hidden = [mlp_hidden(x_shards, w1_list[r]) for r in range(R)]
-    sel = slice(None) if rows is None else np.asarray(rows, dtype=np.int64)
-    s = sum(bf16_to_f64(hidden[r][sel]) @ bf16_to_f64(np.asarray(w2_list[r], dtype=np.uint16))
+    hidden = [mlp_hidden(x_shards, w1_list[r], rows) for r in range(R)]
+    s = sum(bf16_to_f64(hidden[r]) @ bf16_to_f64(np.asarray(w2_list[r], dtype=np.uint16))
             for r in range(R))
-    if rows is not None:
+    if rows is not None:   # hidden holds the sampled rows only
         return dict(gathered=gathered, hidden=hidden, rows=round_out(s, out))
     blocks = [round_out(s[o * m:(o + 1) * m], out) for o in range(R)]
     return dict(gathered=gathered, hidden=hidden, blocks=blocks)

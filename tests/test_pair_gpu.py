@@ -162,3 +162,14 @@ def test_pair_abort_on_missing_partial(reduce):
     _ok(ws)
     exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
     np.testing.assert_array_equal(gpu_bits(torch.cat(blocks, 0)), oracle_bits(exact, "bf16"))
+
+
+@pytest.mark.parametrize("max_ctas", [2, 4])
+@pytest.mark.parametrize("reduce", [mk.REDUCE_RUNNING_SUM, mk.REDUCE_LAST_ARRIVAL])
+def test_few_pairs_odd_row_blocks(max_ctas, reduce):
+    # 5 row blocks: every pass over the last pair row has an empty half, and a
+    # pair goes on to later items after it (the per-buffer publish barrier
+    # must keep its own phase across items that publish nothing)
+    cfg = mk.Config(cta_pair=mk.PAIR_ON, max_ctas=max_ctas, reduce=reduce)
+    _rs_check(4, 640, 520, 256, cfg)
+    _ar_check(2, 640, 264, 136, cfg)
