@@ -205,6 +205,43 @@ def mlp_inputs(w: MlpWorkload):
     return x, w1, w2
 
 
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Ring attention: every rank holds a contiguous block of s_r positions of
+    the sequence, q/k/v per rank [heads x s_r x d]."""
+    name: str
+    R: int
+    heads: int
+    s_r: int
+    d: int = 128
+    causal: bool = False
+    q_seed: int = 2800
+    k_seed: int = 2900
+    v_seed: int = 3000
+    integer: bool = False
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops(self) -> float:
+        S = self.R * self.s_r
+        full = 4.0 * self.heads * S * S * self.d
+        return full / 2 if self.causal else full
+
+
+def attn_inputs(w: AttnWorkload):
+    """q[r], k[r], v[r]: [heads x s_r x d] bf16 (N(0,1), or integers in {-2..2})."""
+    def draw(shape, seed):
+        return int_bf16(shape, seed) if w.integer else normal_bf16(shape, 1.0, seed)
+
+    shape = (w.heads, w.s_r, w.d)
+    q = [draw(shape, w.q_seed + r) for r in range(w.R)]
+    k = [draw(shape, w.k_seed + r) for r in range(w.R)]
+    v = [draw(shape, w.v_seed + r) for r in range(w.R)]
+    return q, k, v
+
+
 # The five workloads: a tiny bit-exact GEMM+RS, then TP=8 MLP up-proj (AG),
 # down-proj (RS), a decode-shaped AR and a 64-expert top-2 MoE layer.
 RS_R2_256_INT = GemmWorkload("rs_r2_256_int", "rs", R=2, m=256, n=256, k=256, out="f32",
@@ -223,8 +260,14 @@ MOE_COMBINE_R8_E64 = MoeCombineWorkload("moe_combine_r8x8e_t4096_n1536_h4096", R
 # The whole TP=8 MLP layer those two GEMMs belong to, as one chained kernel.
 MLP_R8_TP8 = MlpWorkload("mlp_r8_m1024x8_h8192_f3584x8", R=8, m=1024, h=8192, f_r=3584)
 
+# Ring attention over 8 ranks x 4096 positions (32768 in all), 8 heads of 128.
+RING_R8_H8_S4096 = AttnWorkload("ring_r8_h8_s4096x8_d128", R=8, heads=8, s_r=4096, d=128)
+RING_R8_H8_S4096_CAUSAL = AttnWorkload("ring_r8_h8_s4096x8_d128_causal", R=8, heads=8, s_r=4096,
+                                       d=128, causal=True)
+
 WORKLOADS = {w.name: w for w in (RS_R2_256_INT, AG_R8_TP8_UP, RS_R8_TP8_DOWN, AR_R8_DECODE,
-                                 MOE_R8_E64, MOE_COMBINE_R8_E64, MLP_R8_TP8)}
+                                 MOE_R8_E64, MOE_COMBINE_R8_E64, MLP_R8_TP8, RING_R8_H8_S4096,
+                                 RING_R8_H8_S4096_CAUSAL)}
 
 
 def gemm_inputs(w: GemmWorkload):

@@ -38,6 +38,11 @@ The ops (mKernel write-up, news.chathome.org, "五种融合内核" table):
   of S.  The pages name no activation; ReLU is the reading used (exact, so
   the integer twins stay bit-exact), and H_r is rounded to bf16 as the
   layer's stored activation.
+* Ring Attention (row "Ring Attention"): every rank holds one contiguous
+  block of the sequence's Q, K and V; the K/V blocks travel around the ring
+  and each rank attends its queries to all of them, merging the partial
+  softmax results as the blocks arrive.  The result is plain (optionally
+  causal) softmax attention over the whole sequence, computed here directly.
 * MoE combine, the step after the same row: the expert rows are multiplied
   by each expert's down-projection, the products (rounded to bf16, the
   expert output) return to the token's source rank, and each token's output
@@ -369,6 +374,40 @@ def mlp_ag_rs(x_shards, w1_list, w2_list, out: str = "bf16", rows=None):
         return dict(gathered=gathered, hidden=hidden, rows=round_out(s, out))
     blocks = [round_out(s[o * m:(o + 1) * m], out) for o in range(R)]
     return dict(gathered=gathered, hidden=hidden, blocks=blocks)
+
+
+def ring_order(r: int, R: int):
+    """The KV blocks rank r sees in a ring: its own first, then the block of
+    rank r-1, r-2, ... (each step passes every block one rank forward)."""
+    return [(r - j) % R for j in range(R)]
+
+
+def ring_attention(q_list, k_list, v_list, causal: bool, scale: float, out: str = "bf16"):
+    """Ring attention over R ranks that each hold a contiguous block of the
+    sequence (rank s: positions [s*S_r, (s+1)*S_r)) for every head.
+    q_list[r], k_list[r], v_list[r]: [heads x S_r x d] bf16 bits.
+    O_r = softmax(scale * Q_r @ K^T + mask) @ V for the whole sequence's K, V
+    (mask: -inf where the key position is after the query position when
+    causal).  The ring only fixes the order in which the blocks arrive; the
+    result is the plain attention, computed here in float64 with the
+    row-wise maximum subtracted, rounded once.  Returns R arrays."""
+    R = len(q_list)
+    k = np.concatenate([bf16_to_f64(np.asarray(x, dtype=np.uint16)) for x in k_list], axis=1)
+    v = np.concatenate([bf16_to_f64(np.asarray(x, dtype=np.uint16)) for x in v_list], axis=1)
+    outs = []
+    for r in range(R):
+        q = bf16_to_f64(np.asarray(q_list[r], dtype=np.uint16))          # [heads x S_r x d]
+        s_r = q.shape[1]
+        logits = scale * np.einsum("hqd,hkd->hqk", q, k)
+        if causal:
+            qpos = r * s_r + np.arange(s_r)[:, None]
+            kpos = np.arange(k.shape[1])[None, :]
+            logits = np.where(kpos <= qpos, logits, -np.inf)
+        mx = logits.max(axis=2, keepdims=True)
+        w = np.exp(logits - mx)
+        w = w / w.sum(axis=2, keepdims=True)
+        outs.append(round_out(np.einsum("hqk,hkd->hqd", w, v), out))
+    return outs
 
 
 # ----------------------------------------------------------------------------

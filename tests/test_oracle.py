@@ -494,6 +494,82 @@ def test_mlp_row_sample_matches_full_and_rank_blocks_tile():
     np.testing.assert_array_equal(part["rows"], np.concatenate(full["blocks"], 0)[rows])
 
 
+# ---------------------------------------------------------------- ring attention
+
+def _attn_case(R, heads, s_r, d, seed):
+    q = [rand_int_bits((heads, s_r, d), seed + r, -2, 2) for r in range(R)]
+    k = [rand_int_bits((heads, s_r, d), seed + 10 + r, -2, 2) for r in range(R)]
+    v = [rand_int_bits((heads, s_r, d), seed + 20 + r, -2, 2) for r in range(R)]
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_attention_brute_force_tiny(causal):
+    # per query: Python loops over every key of every rank, softmax by its definition
+    import math
+    R, heads, s_r, d, scale = 3, 2, 2, 3, 0.25
+    q, k, v = _attn_case(R, heads, s_r, d, 700)
+    got = O.ring_attention(q, k, v, causal, scale, out="f32")
+    for r in range(R):
+        for hh in range(heads):
+            for i in range(s_r):
+                qi = O.bf16_to_f64(q[r][hh, i])
+                scores, vals = [], []
+                for s_ in range(R):
+                    for j in range(s_r):
+                        if causal and s_ * s_r + j > r * s_r + i:
+                            continue
+                        scores.append(scale * float(np.dot(qi, O.bf16_to_f64(k[s_][hh, j]))))
+                        vals.append(O.bf16_to_f64(v[s_][hh, j]))
+                e = [math.exp(x) for x in scores]
+                want = sum(w * vv for w, vv in zip(e, vals)) / sum(e)
+                np.testing.assert_allclose(got[r][hh, i], want.astype(np.float32), rtol=1e-6, atol=1e-6)
+
+
+def test_ring_attention_zero_queries_average_the_values():
+    # Q = 0: every score is 0, so each output row is the mean of the visible values
+    R, heads, s_r, d = 2, 3, 4, 5
+    _, k, v = _attn_case(R, heads, s_r, d, 710)
+    q = [bf(np.zeros((heads, s_r, d))) for _ in range(R)]
+    vall = np.concatenate([O.bf16_to_f64(x) for x in v], axis=1)
+    got = O.ring_attention(q, k, v, False, 1.0, out="f32")
+    for r in range(R):
+        np.testing.assert_allclose(got[r], np.broadcast_to(vall.mean(axis=1, keepdims=True),
+                                                           got[r].shape), rtol=1e-6, atol=1e-6)
+    got = O.ring_attention(q, k, v, True, 1.0, out="f32")
+    for r in range(R):
+        for i in range(s_r):
+            n = r * s_r + i + 1
+            np.testing.assert_allclose(got[r][:, i], vall[:, :n].mean(axis=1), rtol=1e-6, atol=1e-6)
+
+
+def test_ring_attention_single_key_and_rank_one_match_softmax_library():
+    # one position in all: the output is that value row; R = 1 reduces to
+    # scipy's softmax times V
+    from scipy.special import softmax
+    q, k, v = _attn_case(1, 2, 1, 4, 720)
+    np.testing.assert_array_equal(O.ring_attention(q, k, v, True, 0.5)[0], v[0])
+    q, k, v = _attn_case(1, 2, 6, 4, 730)
+    Q, K, V = (O.bf16_to_f64(x[0]) for x in (q, k, v))
+    want = np.einsum("hqk,hkd->hqd", softmax(0.5 * np.einsum("hqd,hkd->hqk", Q, K), axis=2), V)
+    np.testing.assert_allclose(O.ring_attention(q, k, v, False, 0.5, out="f32")[0], want.astype(np.float32),
+                               rtol=1e-6)
+
+
+def test_ring_attention_rank_blocks_and_causal_mask_positions():
+    # moving rank 1's keys/values away (zero logits cannot do it; use a huge
+    # negative score instead) changes only rows that see them: with causal
+    # masking, rank 0's queries never see rank 1's keys
+    R, heads, s_r, d = 2, 1, 3, 4
+    q, k, v = _attn_case(R, heads, s_r, d, 740)
+    a = O.ring_attention(q, k, v, True, 0.3, out="f32")
+    v2 = [v[0], bf(np.full((heads, s_r, d), 64.0))]
+    b = O.ring_attention(q, k, v2, True, 0.3, out="f32")
+    np.testing.assert_array_equal(a[0], b[0])          # rank 0 only sees its own block
+    assert not np.array_equal(a[1], b[1])
+    assert O.ring_order(0, 4) == [0, 3, 2, 1] and O.ring_order(3, 4) == [3, 2, 1, 0]
+
+
 def test_norm_scale():
     assert O.norm_scale(16, 2.0, 0.5) == 4.0
 
