@@ -281,7 +281,7 @@ def main():
     ap.add_argument("--n-copy", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
-    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp"], default=None,
+    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring"], default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -437,6 +437,11 @@ def run_only(args):
     bf16_peak, _, hbm_peak, _ = peaks()
     if args.only == "moe":
         res = bench_moe(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    elif args.only == "ring":
+        res = {"full": bench_ring(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
+                                  hbm_peak),
+               "causal": bench_ring(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
+                                    hbm_peak, causal=True)}
     elif args.only == "mlp":
         res = bench_mlp(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
     elif args.only == "combine":
@@ -502,6 +507,11 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         out[I.MLP_R8_TP8.name] = bench_mlp(mk, device, stream, dist, max(3, steps // 3), seed_off, tmax,
                                            bf16_peak, hbm_peak)
         torch.cuda.empty_cache()
+        for causal in (False, True):
+            wr = I.RING_R8_H8_S4096_CAUSAL if causal else I.RING_R8_H8_S4096
+            out[wr.name] = bench_ring(mk, device, stream, dist, max(3, steps // 3), seed_off, tmax,
+                                      bf16_peak, hbm_peak, causal=causal)
+            torch.cuda.empty_cache()
     return out
 
 
@@ -616,6 +626,34 @@ def bench_mlp(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
         def step(i, cfg=cfg):
             mk.mlp_ag_rs(x, w1, w2, x_gathered=xg, hid=hid, y_blocks=y, cfg=cfg, workspace=ws,
                          stream=stream)
+        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+    st, _ = mk.device_status(ws, stream)
+    flops = w.flops()
+    fused_tf = flops / (res["fused"] * 1e-3) / 1e12
+    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "status": mk.status_string(st)}
+
+
+def bench_ring(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak, causal=False):
+    """Ring attention: fused (ring transfers overlapped), GEMM-only (no ring: K/V read from
+    their source ranks) and unfused (a transfer launch, then the attention)."""
+    w = I.RING_R8_H8_S4096_CAUSAL if causal else I.RING_R8_H8_S4096
+    shape = (w.heads, w.s_r, w.d)
+    q = [dev_normal(shape, 1.0, w.q_seed + r + seed_off, device) for r in range(w.R)]
+    k = [dev_normal(shape, 1.0, w.k_seed + r + seed_off, device) for r in range(w.R)]
+    v = [dev_normal(shape, 1.0, w.v_seed + r + seed_off, device) for r in range(w.R)]
+    out = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+    kr = [torch.empty(((w.R - 1) * w.heads, w.s_r, w.d), dtype=torch.bfloat16, device=device)
+          for _ in range(w.R)]
+    vr = [torch.empty_like(t) for t in kr]
+    ws = mk.Workspace(device)
+    res = {}
+    for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                      ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        def step(i, cfg=cfg):
+            mk.ring_attention(q, k, v, causal=causal, out=out, k_recv=kr, v_recv=vr, cfg=cfg,
+                              workspace=ws, stream=stream)
         res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
     st, _ = mk.device_status(ws, stream)
     flops = w.flops()

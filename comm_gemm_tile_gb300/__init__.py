@@ -9,6 +9,7 @@ The R virtual ranks of an op are R separate device buffers on one GPU.
 from __future__ import annotations
 
 import ctypes
+import math
 import dataclasses
 import os
 import threading
@@ -104,6 +105,11 @@ def lib() -> ctypes.CDLL:
         L.mk_mlp_ag_rs.restype = i
         L.mk_mlp_ag_rs.argtypes = [P(vp), P(vp), P(vp), i, ll, ll, ll, vp, P(vp), P(vp), vp, sz,
                                    P(_Cfg), vp]
+        L.mk_ring_attention_workspace_size.restype = sz
+        L.mk_ring_attention_workspace_size.argtypes = [i, i, ll, i, i, P(_Cfg)]
+        L.mk_ring_attention.restype = i
+        L.mk_ring_attention.argtypes = [P(vp), P(vp), P(vp), i, i, ll, i, i, ctypes.c_float, P(vp),
+                                        P(vp), P(vp), vp, sz, P(_Cfg), vp]
         L.mk_moe_dispatch_gemm.restype = i
         L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
                                            P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
@@ -361,7 +367,41 @@ def mlp_ag_rs(x_shards, w1, w2, *, x_gathered=None, hid=None, y_blocks=None,
     return x_gathered, hid, y_blocks
 
 
+def ring_attention(q, k, v, *, causal: bool = False, scale: float | None = None, out=None,
+                   k_recv=None, v_recv=None, cfg: Config | None = None,
+                   workspace: Workspace | None = None, stream=None):
+    """Ring attention over R virtual ranks.  q[r], k[r], v[r]: [heads x s_r x d] bf16
+    (d = 128), rank r holding positions [r*s_r, (r+1)*s_r).  Returns out[r] (same shape)
+    = softmax(scale * Q_r K^T (+ causal mask)) V over the whole sequence."""
+    R = len(q)
+    heads, s_r, d = q[0].shape
+    dev = q[0].device
+    bf = torch.bfloat16
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = [torch.empty((heads, s_r, d), dtype=bf, device=dev) for _ in range(R)]
+    mode = cfg.mode if cfg is not None else MODE_FUSED
+    if R > 1 and mode != MODE_GEMM_ONLY:
+        if k_recv is None:
+            k_recv = [torch.empty(((R - 1) * heads, s_r, d), dtype=bf, device=dev) for _ in range(R)]
+        if v_recv is None:
+            v_recv = [torch.empty(((R - 1) * heads, s_r, d), dtype=bf, device=dev) for _ in range(R)]
+    kr = _ptrs(k_recv) if k_recv is not None else None
+    vr = _ptrs(v_recv) if v_recv is not None else None
+    ws = _ws(workspace, dev)
+    nb = int(lib().mk_ring_attention_workspace_size(R, heads, s_r, d, int(causal), _cfgp(cfg)))
+    if nb == 0:
+        raise MkError(MK_ERR_INVALID, "mk_ring_attention_workspace_size")
+    buf = ws.get(nb)
+    st = lib().mk_ring_attention(_ptrs(q), _ptrs(k), _ptrs(v), R, heads, s_r, d, int(causal),
+                                 float(scale), kr, vr, _ptrs(out), buf.data_ptr(), buf.numel(),
+                                 _cfgp(cfg), _stream(stream, dev))
+    _check(st, "mk_ring_attention")
+    return out
+
+
 __all__ = ["Config", "MkError", "Workspace", "ag_gemm", "gemm_rs", "gemm_ar", "device_status",
            "workspace_size", "lib", "status_string", "MODE_FUSED", "MODE_GEMM_ONLY",
            "MODE_UNFUSED", "moe_dispatch_gemm", "moe_workspace_size", "moe_combine",
-           "moe_combine_workspace_size", "mlp_ag_rs", "mlp_workspace_size"]
+           "moe_combine_workspace_size", "mlp_ag_rs", "mlp_workspace_size", "ring_attention"]

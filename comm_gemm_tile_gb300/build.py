@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["mk_api.cu", "mk_fused.cu", "mk_moe.cu", "mk_combine.cu", "mk_noalloc.cu"]
+SOURCES = ["mk_api.cu", "mk_fused.cu", "mk_moe.cu", "mk_combine.cu", "mk_attn.cu", "mk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,671 @@
+// mk_attn.cu -- ring attention (mKernel write-up, news.chathome.org,
+// "五种融合内核" table, row "Ring Attention"): every rank holds a contiguous
+// block of the sequence's Q, K and V; the K/V blocks travel around the ring
+// while each rank attends its queries to every block that has arrived,
+// merging the partial softmax results.
+//
+// One persistent launch of 384 threads per CTA, one CTA per SM:
+//   * warp 0 (TMA): a 128-query tile of one (rank, head), then the K/V tiles
+//     (128 keys each) in ring order -- the rank's own block, then the blocks
+//     of ranks r-1, r-2, ... as they land in its receive buffer;
+//   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
+//     into a TMEM accumulator (tcgen05, bf16 -> fp32);
+//   * warps 2-5 (softmax): online softmax on their 32 rows of S: running
+//     maximum and sum in fp32, P = exp2(scale * log2(e) * s - m) written as
+//     bf16 into shared memory for the PV product; O is rescaled only when the
+//     maximum grows by more than 2^8 (the final division uses the same stale
+//     maximum for O and the sum, so the result is unchanged);
+//   * warps 6-11 (copy): the ring's transfers -- rank r receives the block of
+//     rank (r - j) mod R at step j -- as bulk row copies into its receive
+//     buffer, one counter per (rank, step, head, 128-key tile).
+// Causal attention skips the tiles after each query tile (and, in ring order,
+// every block of a later rank: those blocks are not moved either).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "mk_internal.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+namespace {
+
+constexpr int AT_D = 128;                    // head dimension
+constexpr int AT_T = 128;                    // query rows / keys per tile
+constexpr int AT_THREADS = 384;
+constexpr int AT_MAX_R = 8;
+// shared memory (from the 1024-aligned base)
+constexpr uint32_t AT_Q = 0;                 // Q tile: 2 K-major atoms of [128 rows x 128 B]
+constexpr uint32_t AT_KV = 32768;            // 2 stages of K (32 KB) + V (32 KB)
+constexpr uint32_t AT_KV_STAGE = 65536;
+constexpr uint32_t AT_P = AT_KV + 2 * AT_KV_STAGE;   // P tile, same layout as Q
+constexpr uint32_t AT_BARS = AT_P + 32768;
+constexpr int AT_SMEM = 1024 + AT_BARS + 256;
+// barriers (byte offsets in the barrier block)
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KVFULL = 16, B_KVEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
+                   B_PFULL = 80, B_PVDONE = 88, B_OFREE = 96, B_TMEM = 104;
+constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t AT_O_COL = 256;
+// S = Q K^T: both operands K-major; O += P V: V MN-major
+constexpr uint32_t IDESC_S = idesc_bf16_f32(AT_T, AT_T, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(AT_T, AT_D, false, true);
+constexpr float RESCALE_LOG2 = 8.f;          // rescale O when the maximum grows by more than 2^8
+
+struct AttnParams {
+  CUtensorMap tmQ[AT_MAX_R], tmK[AT_MAX_R], tmV[AT_MAX_R], tmKr[AT_MAX_R], tmVr[AT_MAX_R];
+  uint8_t* out[AT_MAX_R];            // O_r [heads x s_r x d] bf16
+  const uint8_t* ksrc[AT_MAX_R];     // K_r, V_r: the ring's sources
+  const uint8_t* vsrc[AT_MAX_R];
+  uint8_t* krecv[AT_MAX_R];          // [(R-1) x heads x s_r x d]: step j at block j-1
+  uint8_t* vrecv[AT_MAX_R];
+  uint32_t* cnt;                     // [R x (R-1) x heads x nkt] K/V pieces landed
+  uint32_t* hdr;
+  long long wait_ns;
+  uint32_t epoch;
+  float scale_log2;                  // softmax scale * log2(e)
+  int R, heads, s_r, nkt, nqt, causal, n_items;
+  int copy, use_recv, wait;          // ring copies by the copy warps; read them; wait for them
+  int n_cw;
+  int inject;                        // test only: 1 = one ring piece is never counted
+};
+
+// ------------------------------------------------------------------ waits (bounded)
+__device__ __forceinline__ bool at_aborted(const AttnParams& p) {
+  return ld_volatile(&p.hdr[HDR_ABORT]) == p.epoch;
+}
+__device__ __noinline__ void at_error(const AttnParams& p, int where, int item) {
+  int* st = reinterpret_cast<int*>(&p.hdr[HDR_STATUS]);
+  if (atomicCAS(st, 0, MK_ERR_TIMEOUT) == 0)
+    atomicExch(reinterpret_cast<int*>(&p.hdr[HDR_DETAIL]), where * 1000000 + (item % 1000000));
+  __threadfence();
+  atomicExch(&p.hdr[HDR_ABORT], p.epoch);
+}
+__device__ __noinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
+                                         bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++it & 31u) == 0) {
+      if (honor_abort && at_aborted(p)) return false;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+        at_error(p, where, item);
+        return false;
+      }
+    }
+  }
+}
+__device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* f, uint32_t want, int where,
+                                           int item) {
+  if (ld_acquire_gpu(f) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (ld_acquire_gpu(f) != want) {
+    if ((++it & 7u) == 0) {
+      if (at_aborted(p)) return false;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+        at_error(p, where, item);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ work lists
+struct AtItem {
+  int r, h, qt, n;   // rank, head, query tile, K/V tiles to visit
+};
+// Items run longest first (causal: the last rank's queries see the most keys).
+__device__ __forceinline__ AtItem at_item(const AttnParams& p, int i) {
+  AtItem it;
+  const int per_r = p.heads * p.nqt;
+  it.r = p.R - 1 - i / per_r;
+  const int rem = i - (p.R - 1 - it.r) * per_r;
+  it.h = rem / p.nqt;
+  it.qt = rem - it.h * p.nqt;
+  it.n = p.causal ? (it.qt + 1) + it.r * p.nkt : p.R * p.nkt;
+  return it;
+}
+// Tile t of an item: ring step j (source rank s = r - j mod R) and key tile kt.
+__device__ __forceinline__ void at_tile(const AttnParams& p, const AtItem& it, int t, int& j, int& s, int& kt) {
+  if (p.causal) {
+    if (t <= it.qt) {
+      j = 0;
+      s = it.r;
+      kt = t;
+      return;
+    }
+    const int u = t - (it.qt + 1);
+    j = 1 + u / p.nkt;
+    s = it.r - j;
+    kt = u - (j - 1) * p.nkt;
+    return;
+  }
+  j = t / p.nkt;
+  kt = t - j * p.nkt;
+  s = (it.r - j + p.R) % p.R;
+}
+__device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int j, int h, int kt) {
+  return p.cnt + ((static_cast<size_t>(r) * (p.R - 1) + (j - 1)) * p.heads + h) * p.nkt + kt;
+}
+
+// ------------------------------------------------------------------ roles
+__device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
+  int stage = 0;
+  uint32_t kv_ph = 0, q_ph = 0;
+  uint32_t issued_mask = 0, issued_par = 0;
+  bool ready = false;
+  bool q_issued = false;
+  uint32_t q_par = 0;
+  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+    const AtItem it = at_item(p, i);
+    if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+    q_ph ^= 1u;
+    {
+      const int qrow = it.h * p.s_r + it.qt * AT_T;
+      mbar_arrive_expect_tx(bars + B_QFULL, 2u * 16384u);
+      tma_load_2d(base + AT_Q, &p.tmQ[it.r], bars + B_QFULL, 0, qrow);
+      tma_load_2d(base + AT_Q + 16384u, &p.tmQ[it.r], bars + B_QFULL, 64, qrow);
+      q_issued = true;
+      q_par ^= 1u;
+    }
+    for (int t = 0; t < it.n; ++t) {
+      int j, s, kt;
+      at_tile(p, it, t, j, s, kt);
+      if (!at_wait_bar(p, bars + B_KVEMPTY + 8u * stage, kv_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+      const CUtensorMap* mk = &p.tmK[s];
+      const CUtensorMap* mv = &p.tmV[s];
+      int row = it.h * p.s_r + kt * AT_T;
+      if (j > 0 && p.use_recv) {
+        if (p.wait) {
+          if (!ready) {
+            if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, i)) goto done;
+            ready = true;
+          }
+          if (!at_wait_value(p, at_counter(p, it.r, j, it.h, kt), 2u, WHERE_PRODUCER, i)) goto done;
+          fence_proxy_async_global();
+        }
+        mk = &p.tmKr[it.r];
+        mv = &p.tmVr[it.r];
+        row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
+      }
+      const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
+      const uint32_t vb = kb + 32768u;
+      const uint32_t full = bars + B_KVFULL + 8u * stage;
+      mbar_arrive_expect_tx(full, 65536u);
+      tma_load_2d(kb, mk, full, 0, row);
+      tma_load_2d(kb + 16384u, mk, full, 64, row);
+      tma_load_3d(vb, mv, full, 0, row, 0);
+      tma_load_3d(vb + 16384u, mv, full, 0, row + 64, 0);
+      issued_mask |= 1u << stage;
+      issued_par = (issued_par & ~(1u << stage)) | (kv_ph << stage);
+      if (++stage == 2) {
+        stage = 0;
+        kv_ph ^= 1u;
+      }
+    }
+  }
+done:
+  for (int s2 = 0; s2 < 2; ++s2)
+    if (issued_mask & (1u << s2))
+      at_wait_bar(p, bars + B_KVFULL + 8u * s2, (issued_par >> s2) & 1u, WHERE_DRAIN, s2, false);
+  if (q_issued) at_wait_bar(p, bars + B_QFULL, q_par ^ 1u, WHERE_DRAIN, 0, false);
+}
+
+__device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
+  uint32_t q_ph = 0, kv_ph = 0, pf_ph = 0, of_ph = 0;
+  uint32_t se_ph[2] = {0u, 0u};
+  int stage = 0, prev_stage = 0;
+  int g = 0;   // tiles issued (S buffer = g % 2)
+  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+    const AtItem it = at_item(p, i);
+    if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
+    q_ph ^= 1u;
+    for (int t = 0; t <= it.n; ++t) {
+      if (t < it.n) {
+        const int sb = g & 1;
+        if (!at_wait_bar(p, bars + B_KVFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, se_ph[sb] ^ 1u, WHERE_MMA, i)) goto done;
+        se_ph[sb] ^= 1u;
+        tc_fence_after();
+        const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_swz(base + AT_Q + 16384u * a + 32u * k, 16u, 1024u, 2u);
+            const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
+            tc_mma_bf16(tmem + static_cast<uint32_t>(sb) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
+          }
+        tc_commit(bars + B_SFULL + 8u * sb);
+        if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
+        ++g;
+      }
+      if (t > 0) {
+        // O += P_{t-1} V_{t-1}
+        if (!at_wait_bar(p, bars + B_PFULL, pf_ph, WHERE_MMA, i)) goto done;
+        pf_ph ^= 1u;
+        if (t == 1) {   // the previous item's O has been read out
+          if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
+          of_ph ^= 1u;
+        }
+        tc_fence_after();
+        const uint32_t vb = base + AT_KV + static_cast<uint32_t>(prev_stage) * AT_KV_STAGE + 32768u;
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_swz(base + AT_P + 16384u * a + 32u * k, 16u, 1024u, 2u);
+            const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
+            tc_mma_bf16(tmem + AT_O_COL, ad, bd, IDESC_PV, (t > 1 || a || k) ? 1u : 0u);
+          }
+        tc_commit(bars + B_KVEMPTY + 8u * prev_stage);
+        tc_commit(bars + B_PVDONE);
+      }
+      if (t < it.n) {
+        prev_stage = stage;
+        if (++stage == 2) {
+          stage = 0;
+          kv_ph ^= 1u;
+        }
+      }
+    }
+  }
+done:
+  tc_commit(bars + B_TMEM + 8u);   // drain barrier (below the TMEM slot word)
+  at_wait_bar(p, bars + B_TMEM + 8u, 0, WHERE_DRAIN, 0, false);
+}
+
+// P tile element (row, key): K-major, 128-byte swizzle, two 64-key atoms.
+__device__ __forceinline__ uint32_t p_chunk_addr(uint32_t pbase, int row, int kchunk) {
+  // kchunk: 8-key group 0..15
+  const int atom = kchunk >> 3, c = kchunk & 7;
+  return pbase + static_cast<uint32_t>(atom) * 16384u + static_cast<uint32_t>(row >> 3) * 1024u +
+         static_cast<uint32_t>(row & 7) * 128u + static_cast<uint32_t>((c ^ (row & 7)) << 4);
+}
+
+__device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;                       // query row within the tile
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  uint32_t sf_ph[2] = {0u, 0u};
+  uint32_t pv_ph = 0;
+  int g = 0;
+  int pv_pending = 0;   // PV products issued but not yet waited for (0 or 1)
+  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+    const AtItem it = at_item(p, i);
+    const int qpos = it.qt * AT_T + row;                     // position within rank r's block
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int t = 0; t < it.n; ++t) {
+      int j, s, kt;
+      at_tile(p, it, t, j, s, kt);
+      const int sb = g & 1;
+      const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
+      const bool diag = p.causal && j == 0 && kt == it.qt;   // keys after the query are masked
+      const int lim = diag ? min(valid, row + 1) : valid;
+      {
+        int ok = at_wait_bar(p, bars + B_SFULL + 8u * sb, sf_ph[sb], WHERE_EPILOGUE, i) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
+      sf_ph[sb] ^= 1u;
+      tc_fence_after();
+      const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(sb) * AT_T;
+      // pass 1: row maximum (log2 domain)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(sbase + 32u * c, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (32 * c + q < lim) mx = fmaxf(mx, __uint_as_float(v[q]) * p.scale_log2);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      // P of the previous tile has been consumed (and O updated) before P is rewritten
+      if (pv_pending) {
+        int ok = at_wait_bar(p, bars + B_PVDONE, pv_ph, WHERE_EPILOGUE, i) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        pv_ph ^= 1u;
+        pv_pending = 0;
+      }
+      float factor = 1.f;
+      if (t == 0) {
+        m_run = m_new;
+      } else if (m_new > m_run + RESCALE_LOG2) {
+        factor = exp2f(m_run - m_new);
+        m_run = m_new;
+        l_run *= factor;
+      }
+      if (__any_sync(0xffffffffu, factor != 1.f)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < AT_D / 32; ++c) {
+          uint32_t v[32];
+          const uint32_t oaddr = tmem + lane_off + AT_O_COL + 32u * c;
+          tc_ld_32x32b_x32(oaddr, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
+          tc_st_32x32b_x32(oaddr, v);
+        }
+        tc_wait_st();
+      }
+      // pass 2: P = exp2(x - m), the running sum, P as bf16 into shared memory
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(sbase + 32u * c, v);
+        tc_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int k0 = 32 * c + 2 * q;
+          const float p0 = (k0 < lim) ? exp2f(__uint_as_float(v[2 * q]) * p.scale_log2 - mref) : 0.f;
+          const float p1 = (k0 + 1 < lim) ? exp2f(__uint_as_float(v[2 * q + 1]) * p.scale_log2 - mref) : 0.f;
+          l_run += p0 + p1;
+          pk[q] = pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t a = p_chunk_addr(base + AT_P, row, 4 * c + q);
+          asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * q]),
+                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();   // P (generic stores) is read by the tensor cores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars + B_SEMPTY + 8u * sb);
+        mbar_arrive(bars + B_PFULL);
+      }
+      pv_pending = 1;
+      ++g;
+    }
+    // O of this item: the last PV has completed
+    {
+      int ok = at_wait_bar(p, bars + B_PVDONE, pv_ph, WHERE_EPILOGUE, i) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, ok)) return;
+      pv_ph ^= 1u;
+      pv_pending = 0;
+    }
+    tc_fence_after();
+    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    const bool row_ok = qpos < p.s_r;
+    uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2;
+#pragma unroll 1
+    for (int c = 0; c < AT_D / 32; ++c) {
+      uint32_t v[32];
+      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + 32u * c, v);
+      tc_wait_ld();
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        st_global_v4(orow + (32 * c + 8 * q) * 2,
+                     pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + B_OFREE);
+  }
+}
+
+// The ring's transfers: piece = (rank r, step j >= 1, head h, key tile kt, K or V),
+// in the order the work list needs them (ranks as the items run, then head, step, tile).
+__device__ void at_copy(const AttnParams& p) {
+  const int lane = threadIdx.x & 31;
+  const int cw = (threadIdx.x >> 5) - 6;
+  if (cw >= p.n_cw) return;
+  const int worker = blockIdx.x * p.n_cw + cw;
+  const int n_workers = gridDim.x * p.n_cw;
+  {
+    int ok = 1;
+    if (lane == 0) ok = at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, worker) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  }
+  const long long per_r = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2;
+  const long long total = per_r * p.R;
+  bool skip_first = (p.inject == 1 && worker == 0);
+  for (long long q = worker; q < total; q += n_workers) {
+    const int rr = static_cast<int>(q / per_r);
+    long long rem = q - rr * per_r;
+    const int r = p.R - 1 - rr;
+    const int h = static_cast<int>(rem / ((p.R - 1) * p.nkt * 2));
+    rem -= static_cast<long long>(h) * (p.R - 1) * p.nkt * 2;
+    const int j = 1 + static_cast<int>(rem / (p.nkt * 2));
+    rem -= static_cast<long long>(j - 1) * p.nkt * 2;
+    const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
+    const int s = (r - j + p.R) % p.R;
+    if (p.causal && s > r) continue;            // a later rank's keys: never read
+    int stop = 0;
+    if (lane == 0) stop = at_aborted(p) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) return;
+    const int rows = min(AT_T, p.s_r - kt * AT_T);
+    const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
+    const size_t dst_off = ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) *
+                           AT_D * 2;
+    const uint8_t* src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
+    uint8_t* dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
+    const size_t n16 = static_cast<size_t>(rows) * AT_D * 2 / 16;
+    constexpr int U = 16;
+    for (size_t i0 = lane; i0 < n16; i0 += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = i0 + static_cast<size_t>(u) * 32;
+        if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = i0 + static_cast<size_t>(u) * 32;
+        if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      if (skip_first) skip_first = false;
+      else atomicAdd(at_counter(p, r, j, h, kt), 1u);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bars = base + AT_BARS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_BARS + B_TMEM);
+  if (blockIdx.x == 0 && p.copy) {
+    // zero this call's ring counters, then publish them
+    const long long n = static_cast<long long>(p.R) * (p.R - 1) * p.heads * p.nkt;
+    for (long long x = threadIdx.x; x < n; x += AT_THREADS) p.cnt[x] = 0u;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release_gpu(&p.hdr[HDR_READY], p.epoch);
+  }
+  if (warp == 0 && lane == 0) {
+    mbar_init(bars + B_QFULL, 1);
+    mbar_init(bars + B_QEMPTY, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bars + B_KVFULL + 8u * s, 1);
+      mbar_init(bars + B_KVEMPTY + 8u * s, 1);
+      mbar_init(bars + B_SFULL + 8u * s, 1);
+      mbar_init(bars + B_SEMPTY + 8u * s, 4);
+    }
+    mbar_init(bars + B_PFULL, 4);
+    mbar_init(bars + B_PVDONE, 1);
+    mbar_init(bars + B_OFREE, 4);
+    mbar_init(bars + B_TMEM + 8u, 1);   // MMA drain
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), AT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp == 0) {
+    if (lane == 0) at_producer(p, bars, base);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) at_mma(p, bars, base, tmem);
+    __syncwarp();
+  } else if (warp <= 5) {
+    at_softmax(p, bars, base, tmem);
+    __syncwarp();
+  } else if (p.copy) {
+    at_copy(p);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, AT_TMEM_COLS);
+  }
+}
+
+struct AttnLayout {
+  size_t cnt_off, total;
+  int nkt, nqt;
+};
+
+bool attn_layout(int R, int heads, long long s_r, int d, AttnLayout& L) {
+  if (R < 1 || R > AT_MAX_R || heads < 1 || s_r < 0 || d != AT_D) return false;
+  if (static_cast<long long>(heads) * s_r >= (1LL << 31) / AT_D) return false;
+  L.nkt = static_cast<int>(ceil_div_ll(s_r, AT_T));
+  L.nqt = L.nkt;
+  L.cnt_off = WS_HDR_BYTES;
+  L.total = L.cnt_off + ((static_cast<size_t>(R) * std::max(R - 1, 0) * heads * L.nkt * 4 + 255) & ~size_t(255));
+  return true;
+}
+
+cudaError_t attn_launch(const AttnParams& p, int grid, cudaStream_t s) {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(mk_ring_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  mk_ring_attn_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+size_t mk_ring_attention_workspace_size(int R, int heads, long long s_r, int d, int causal,
+                                        const mk_config* cfg) {
+  (void)cfg;
+  (void)causal;
+  AttnLayout L;
+  if (!attn_layout(R, heads, s_r, d, L)) return 0;
+  return L.total;
+}
+
+mk_status mk_ring_attention(const void* const* q, const void* const* k, const void* const* v, int R, int heads,
+                            long long s_r, int d, int causal, float scale, void* const* k_recv,
+                            void* const* v_recv, void* const* out, void* workspace, size_t ws_bytes,
+                            const mk_config* cfg, mk_stream_t stream) {
+  if (!q || !k || !v || !out || !workspace) return MK_ERR_INVALID;
+  AttnLayout L;
+  if (!attn_layout(R, heads, s_r, d, L)) return MK_ERR_INVALID;
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u)) return MK_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MK_ERR_INVALID;
+  const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
+  if (mode < MK_MODE_FUSED || mode > MK_MODE_UNFUSED) return MK_ERR_INVALID;
+  const long long blk = static_cast<long long>(heads) * s_r * d;
+  const bool need_recv = (R > 1 && mode != MK_MODE_GEMM_ONLY);
+  if (need_recv && (!k_recv || !v_recv)) return MK_ERR_INVALID;
+  for (int r = 0; r < R; ++r) {
+    auto bad = [&](const void* ptr, long long elems) {
+      return (elems > 0 && !ptr) || (reinterpret_cast<uintptr_t>(ptr) & 15u);
+    };
+    if (bad(q[r], blk) || bad(k[r], blk) || bad(v[r], blk) || bad(out[r], blk)) return MK_ERR_INVALID;
+    if (need_recv && (bad(k_recv[r], blk * (R - 1)) || bad(v_recv[r], blk * (R - 1)))) return MK_ERR_INVALID;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (s_r == 0) return MK_OK;
+  int sms = device_sm_count();
+  if (sms <= 0) return MK_ERR_UNSUPPORTED;
+  if (cfg && cfg->max_ctas > 0) sms = std::min(sms, cfg->max_ctas);
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.R = R;
+  p.heads = heads;
+  p.s_r = static_cast<int>(s_r);
+  p.nkt = L.nkt;
+  p.nqt = L.nqt;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.cnt_off);
+  p.hdr = static_cast<uint32_t*>(workspace);
+  p.wait_ns = default_wait_ns(cfg);
+  p.inject = cfg ? cfg->inject : 0;
+  p.epoch = next_epoch();
+  p.n_cw = AT_THREADS / 32 - 6;
+  const uint64_t rows = static_cast<uint64_t>(heads) * s_r;
+  for (int r = 0; r < R; ++r) {
+    p.out[r] = static_cast<uint8_t*>(out[r]);
+    p.ksrc[r] = static_cast<const uint8_t*>(k[r]);
+    p.vsrc[r] = static_cast<const uint8_t*>(v[r]);
+    if (!make_map_a(&p.tmQ[r], q[r], AT_D, rows, AT_D * 2) || !make_map_a(&p.tmK[r], k[r], AT_D, rows, AT_D * 2) ||
+        !make_map_b_chunks(&p.tmV[r], v[r], rows, AT_D, 2))
+      return MK_ERR_CUDA;
+    if (need_recv) {
+      p.krecv[r] = static_cast<uint8_t*>(k_recv[r]);
+      p.vrecv[r] = static_cast<uint8_t*>(v_recv[r]);
+      const uint64_t rrows = rows * (R - 1);
+      if (!make_map_a(&p.tmKr[r], k_recv[r], AT_D, rrows, AT_D * 2) ||
+          !make_map_b_chunks(&p.tmVr[r], v_recv[r], rrows, AT_D, 2))
+        return MK_ERR_CUDA;
+    }
+  }
+  const int n_items = R * heads * L.nqt;
+  const int grid = std::max(1, std::min(sms, n_items));
+  if (mode == MK_MODE_GEMM_ONLY || R == 1) {   // K/V read from the source ranks: no ring
+    p.n_items = n_items;
+    return attn_launch(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+  }
+  if (mode == MK_MODE_FUSED) {
+    p.copy = p.use_recv = p.wait = 1;
+    p.n_items = n_items;
+    return attn_launch(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+  }
+  // unfused: the ring's transfers as one launch, then the attention reading them
+  p.copy = 1;
+  p.n_items = 0;
+  if (attn_launch(p, sms, s) != cudaSuccess) return MK_ERR_CUDA;
+  p.copy = 0;
+  p.use_recv = 1;
+  p.n_items = n_items;
+  return attn_launch(p, grid, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+}  // extern "C"

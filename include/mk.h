@@ -251,6 +251,32 @@ mk_status mk_mlp_ag_rs(const void *const *x_shards, const void *const *w1, const
                        void *const *hid, void *const *y_blocks, void *workspace, size_t ws_bytes,
                        const mk_config *cfg, mk_stream_t stream);
 
+/* Workspace bytes for mk_ring_attention (0 on bad args). */
+size_t mk_ring_attention_workspace_size(int R, int heads, long long s_r, int d, int causal,
+                                        const mk_config *cfg);
+
+/* Ring Attention (five-kernel table, row "Ring Attention") over R virtual
+ * ranks, each holding a contiguous block of s_r positions of the sequence
+ * (rank s: positions [s*s_r, (s+1)*s_r)) for every head:
+ *   q[r], k[r], v[r]: [heads x s_r x d] bf16 (device), d = 128
+ *   out[r] = softmax(scale * Q_r K^T (+ causal mask)) V over the whole
+ *            sequence's K and V, [heads x s_r x d] bf16
+ * The K/V blocks travel around the ring: at step j rank r receives the block
+ * of rank (r - j) mod R into k_recv[r] / v_recv[r] ([(R-1) x heads x s_r x d]
+ * bf16 each, step j at block j-1, written), and its query tiles consume each
+ * 128-key tile as soon as it has landed, merging the partial softmax results
+ * online in fp32 (P rounded to bf16 for the tensor cores).  causal != 0 masks
+ * keys after the query position; then the blocks of later ranks are neither
+ * moved nor read.  scale > 0 (usually 1/sqrt(d)).  R <= 8.
+ * mode: FUSED (one launch); GEMM_ONLY (no ring: K/V read from the source
+ * ranks, k_recv/v_recv unused and may be NULL); UNFUSED (a transfer launch,
+ * then the attention launch reading the receive buffers). */
+mk_status mk_ring_attention(const void *const *q, const void *const *k, const void *const *v, int R,
+                            int heads, long long s_r, int d, int causal, float scale,
+                            void *const *k_recv, void *const *v_recv, void *const *out,
+                            void *workspace, size_t ws_bytes, const mk_config *cfg,
+                            mk_stream_t stream);
+
 /* Size of the library's own scratch array used by mk_ag_gemm_noalloc (bytes). */
 #define MK_NOALLOC_SCRATCH_BYTES 65536
 

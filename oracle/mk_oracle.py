@@ -382,7 +382,8 @@ def ring_order(r: int, R: int):
     return [(r - j) % R for j in range(R)]
 
 
-def ring_attention(q_list, k_list, v_list, causal: bool, scale: float, out: str = "bf16"):
+def ring_attention(q_list, k_list, v_list, causal: bool, scale: float, out: str = "bf16",
+                   q_rows=None):
     """Ring attention over R ranks that each hold a contiguous block of the
     sequence (rank s: positions [s*S_r, (s+1)*S_r)) for every head.
     q_list[r], k_list[r], v_list[r]: [heads x S_r x d] bf16 bits.
@@ -390,7 +391,9 @@ def ring_attention(q_list, k_list, v_list, causal: bool, scale: float, out: str 
     (mask: -inf where the key position is after the query position when
     causal).  The ring only fixes the order in which the blocks arrive; the
     result is the plain attention, computed here in float64 with the
-    row-wise maximum subtracted, rounded once.  Returns R arrays."""
+    row-wise maximum subtracted, rounded once.  Returns R arrays.
+    q_rows: optional per-rank arrays of query positions within the rank's
+    block (a row sample); then only those rows are returned."""
     R = len(q_list)
     k = np.concatenate([bf16_to_f64(np.asarray(x, dtype=np.uint16)) for x in k_list], axis=1)
     v = np.concatenate([bf16_to_f64(np.asarray(x, dtype=np.uint16)) for x in v_list], axis=1)
@@ -398,9 +401,11 @@ def ring_attention(q_list, k_list, v_list, causal: bool, scale: float, out: str 
     for r in range(R):
         q = bf16_to_f64(np.asarray(q_list[r], dtype=np.uint16))          # [heads x S_r x d]
         s_r = q.shape[1]
+        rows = np.arange(s_r) if q_rows is None else np.asarray(q_rows[r], dtype=np.int64)
+        q = q[:, rows]
         logits = scale * np.einsum("hqd,hkd->hqk", q, k)
         if causal:
-            qpos = r * s_r + np.arange(s_r)[:, None]
+            qpos = r * s_r + rows[:, None]
             kpos = np.arange(k.shape[1])[None, :]
             logits = np.where(kpos <= qpos, logits, -np.inf)
         mx = logits.max(axis=2, keepdims=True)
