@@ -10,14 +10,16 @@
 //     of ranks r-1, r-2, ... as they land in its receive buffer;
 //   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
 //     into a TMEM accumulator (tcgen05, bf16 -> fp32);
-//   * warps 2-5 (softmax): online softmax on their 32 rows of S: running
-//     maximum and sum in fp32, P = exp2(scale * log2(e) * s - m) written as
-//     bf16 into shared memory for the PV product; O is rescaled only when the
-//     maximum grows by more than 2^8 (the final division uses the same stale
-//     maximum for O and the sum, so the result is unchanged);
-//   * warps 6-11 (copy): the ring's transfers -- rank r receives the block of
-//     rank (r - j) mod R at step j -- as bulk row copies into its receive
-//     buffer, one counter per (rank, step, head, 128-key tile).
+//   * warps 2-9 (softmax): online softmax, two warps per 32 query rows, each
+//     on half of the columns: running maximum and sum in fp32, P =
+//     exp2(scale * log2(e) * s - m) written as bf16 into shared memory for the
+//     PV product; O is rescaled only when the maximum grows by more than 2^8
+//     (the final division uses the same stale maximum for O and the sum, so
+//     the result is unchanged);
+//   * warp 10 (copy): the ring's transfers -- rank r receives the block of
+//     rank (r - j) mod R at step j -- as bulk async copies through shared
+//     memory into its receive buffer, one counter per (rank, step, head);
+//     warp 11 is idle.
 // Causal attention skips the tiles after each query tile (and, in ring order,
 // every block of a later rank: those blocks are not moved either).
 #include <algorithm>
@@ -41,10 +43,13 @@ constexpr uint32_t AT_KV = 32768;            // 2 stages of K (32 KB) + V (32 KB
 constexpr uint32_t AT_KV_STAGE = 65536;
 constexpr uint32_t AT_P = AT_KV + 2 * AT_KV_STAGE;   // P tile, same layout as Q
 constexpr uint32_t AT_BARS = AT_P + 32768;
-constexpr int AT_SMEM = 1024 + AT_BARS + 256;
+constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima / sums exchanged by the softmax warp pairs
+constexpr uint32_t AT_CPY = AT_XCH + 4 * AT_T * 4;   // bulk-copy staging of the ring's transfers
+constexpr int AT_SMEM = 1024 + AT_CPY + 3 * 8192;
 // barriers (byte offsets in the barrier block)
 constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KVFULL = 16, B_KVEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
-                   B_PFULL = 80, B_PVDONE = 88, B_OFREE = 96, B_TMEM = 104;
+                   B_PFULL = 80, B_PVDONE = 88, B_OFREE = 96, B_TMEM = 104, B_DRAIN = 112, B_PAIR = 128,
+                   B_COPY = 160;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t AT_O_COL = 256;
 // S = Q K^T: both operands K-major; O += P V: V MN-major
@@ -59,7 +64,7 @@ struct AttnParams {
   const uint8_t* vsrc[AT_MAX_R];
   uint8_t* krecv[AT_MAX_R];          // [(R-1) x heads x s_r x d]: step j at block j-1
   uint8_t* vrecv[AT_MAX_R];
-  uint32_t* cnt;                     // [R x (R-1) x heads x nkt] K/V pieces landed
+  uint32_t* cnt;                     // [R x (R-1) x heads] K/V pieces landed per step block
   uint32_t* hdr;
   long long wait_ns;
   uint32_t epoch;
@@ -149,8 +154,11 @@ __device__ __forceinline__ void at_tile(const AttnParams& p, const AtItem& it, i
   kt = t - j * p.nkt;
   s = (it.r - j + p.R) % p.R;
 }
-__device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int j, int h, int kt) {
-  return p.cnt + ((static_cast<size_t>(r) * (p.R - 1) + (j - 1)) * p.heads + h) * p.nkt + kt;
+// Pieces of rank r's step-j block of head h that have landed (K and V of
+// every key tile: 2 * nkt when complete).  One acquire per step keeps the
+// counter reads off the per-tile load path.
+__device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int j, int h) {
+  return p.cnt + (static_cast<size_t>(r) * (p.R - 1) + (j - 1)) * p.heads + h;
 }
 
 // ------------------------------------------------------------------ roles
@@ -173,6 +181,7 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
       q_issued = true;
       q_par ^= 1u;
     }
+    int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
@@ -181,13 +190,14 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
       const CUtensorMap* mv = &p.tmV[s];
       int row = it.h * p.s_r + kt * AT_T;
       if (j > 0 && p.use_recv) {
-        if (p.wait) {
+        if (p.wait && j != waited_j) {
           if (!ready) {
             if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, i)) goto done;
             ready = true;
           }
-          if (!at_wait_value(p, at_counter(p, it.r, j, it.h, kt), 2u, WHERE_PRODUCER, i)) goto done;
+          if (!at_wait_value(p, at_counter(p, it.r, j, it.h), 2u * p.nkt, WHERE_PRODUCER, i)) goto done;
           fence_proxy_async_global();
+          waited_j = j;
         }
         mk = &p.tmKr[it.r];
         mv = &p.tmVr[it.r];
@@ -276,8 +286,8 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     }
   }
 done:
-  tc_commit(bars + B_TMEM + 8u);   // drain barrier (below the TMEM slot word)
-  at_wait_bar(p, bars + B_TMEM + 8u, 0, WHERE_DRAIN, 0, false);
+  tc_commit(bars + B_DRAIN);
+  at_wait_bar(p, bars + B_DRAIN, 0, WHERE_DRAIN, 0, false);
 }
 
 // P tile element (row, key): K-major, 128-byte swizzle, two 64-key atoms.
@@ -288,11 +298,28 @@ __device__ __forceinline__ uint32_t p_chunk_addr(uint32_t pbase, int row, int kc
          static_cast<uint32_t>(row & 7) * 128u + static_cast<uint32_t>((c ^ (row & 7)) << 4);
 }
 
-__device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
+// Softmax warps 2-9: warp w handles TMEM lanes 32*(w%4) .. +31 (query rows)
+// and half (w-2)/4 of the 128 columns (keys of S, head dims of O).  The two
+// warps of a row quarter exchange their row maxima and, at the end, their row
+// sums through shared memory, meeting at a two-arrival mbarrier (a bounded
+// wait, so that one warp leaving on an abort cannot strand the other).
+__device__ __forceinline__ bool pair_sync(const AttnParams& p, uint32_t bar, uint32_t& ph, int item) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const int ok = at_wait_bar(p, bar, ph, WHERE_EPILOGUE, item) ? 1 : 0;
+  ph ^= 1u;
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+__device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
+  const int half = (warp - 2) >> 2;
   const int row = quarter * 32 + lane;                       // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const int c0 = 64 * half;                                  // first column of this warp's half
+  const uint32_t pbar = bars + B_PAIR + 8u * quarter;
+  uint32_t pair_ph = 0;
   uint32_t sf_ph[2] = {0u, 0u};
   uint32_t pv_ph = 0;
   int g = 0;
@@ -307,25 +334,42 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       const int sb = g & 1;
       const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
       const bool diag = p.causal && j == 0 && kt == it.qt;   // keys after the query are masked
-      const int lim = diag ? min(valid, row + 1) : valid;
+      const int lim = (diag ? min(valid, row + 1) : valid) - c0;   // valid keys in this half
       {
         int ok = at_wait_bar(p, bars + B_SFULL + 8u * sb, sf_ph[sb], WHERE_EPILOGUE, i) ? 1 : 0;
         if (!__all_sync(0xffffffffu, ok)) return;
       }
       sf_ph[sb] ^= 1u;
       tc_fence_after();
-      const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(sb) * AT_T;
-      // pass 1: row maximum (log2 domain)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(sbase + 32u * c, v);
+      const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(sb) * AT_T + static_cast<uint32_t>(c0);
+      uint32_t x[64];
+      {
+        uint32_t v0[32], v1[32];
+        tc_ld_32x32b_x32(sbase, v0);
+        tc_ld_32x32b_x32(sbase + 32u, v1);
         tc_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (32 * c + q < lim) mx = fmaxf(mx, __uint_as_float(v[q]) * p.scale_log2);
+        for (int q = 0; q < 32; ++q) {
+          x[q] = v0[q];
+          x[32 + q] = v1[q];
+        }
       }
+      // S has been read: the MMA may overwrite this buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + B_SEMPTY + 8u * sb);
+      // scaled scores (log2 domain) and this half's row maximum
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 64; ++q) {
+        const float xv = (q < lim) ? __uint_as_float(x[q]) * p.scale_log2 : -INFINITY;
+        x[q] = __float_as_uint(xv);
+        mx = fmaxf(mx, xv);
+      }
+      xch[half * AT_T + row] = mx;
+      if (!pair_sync(p, pbar, pair_ph, i)) return;
+      mx = fmaxf(xch[row], xch[AT_T + row]);
+      if (!pair_sync(p, pbar, pair_ph, i)) return;   // both halves have read the maxima
       const float m_new = fmaxf(m_run, mx);
       // P of the previous tile has been consumed (and O updated) before P is rewritten
       if (pv_pending) {
@@ -345,9 +389,9 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       if (__any_sync(0xffffffffu, factor != 1.f)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < AT_D / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          const uint32_t oaddr = tmem + lane_off + AT_O_COL + 32u * c;
+          const uint32_t oaddr = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * c);
           tc_ld_32x32b_x32(oaddr, v);
           tc_wait_ld();
 #pragma unroll
@@ -356,55 +400,49 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         }
         tc_wait_st();
       }
-      // pass 2: P = exp2(x - m), the running sum, P as bf16 into shared memory
+      // P = exp2(x - m), the running sum, P as bf16 into shared memory
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(sbase + 32u * c, v);
-        tc_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int k0 = 32 * c + 2 * q;
-          const float p0 = (k0 < lim) ? exp2f(__uint_as_float(v[2 * q]) * p.scale_log2 - mref) : 0.f;
-          const float p1 = (k0 + 1 < lim) ? exp2f(__uint_as_float(v[2 * q + 1]) * p.scale_log2 - mref) : 0.f;
+      for (int c = 0; c < 8; ++c) {   // 8 keys per 16-byte chunk
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float p0 = exp2f(__uint_as_float(x[8 * c + 2 * q]) - mref);
+          const float p1 = exp2f(__uint_as_float(x[8 * c + 2 * q + 1]) - mref);
           l_run += p0 + p1;
           pk[q] = pack_bf16x2(p0, p1);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t a = p_chunk_addr(base + AT_P, row, 4 * c + q);
-          asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * q]),
-                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                       : "memory");
-        }
+        const uint32_t a = p_chunk_addr(base + AT_P, row, 8 * half + c);
+        asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
+                     "r"(pk[2]), "r"(pk[3])
+                     : "memory");
       }
       fence_proxy_async_smem();   // P (generic stores) is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bars + B_SEMPTY + 8u * sb);
-        mbar_arrive(bars + B_PFULL);
-      }
+      if (lane == 0) mbar_arrive(bars + B_PFULL);
       pv_pending = 1;
       ++g;
     }
-    // O of this item: the last PV has completed
+    // O of this item: the last PV has completed; the row sum is the two halves' sum
     {
       int ok = at_wait_bar(p, bars + B_PVDONE, pv_ph, WHERE_EPILOGUE, i) ? 1 : 0;
       if (!__all_sync(0xffffffffu, ok)) return;
       pv_ph ^= 1u;
       pv_pending = 0;
     }
+    xch[2 * AT_T + half * AT_T + row] = l_run;
+    if (!pair_sync(p, pbar, pair_ph, i)) return;
+    const float l_all = xch[2 * AT_T + row] + xch[3 * AT_T + row];
+    if (!pair_sync(p, pbar, pair_ph, i)) return;
     tc_fence_after();
-    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const bool row_ok = qpos < p.s_r;
-    uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2;
+    uint8_t* orow = p.out[it.r] + ((static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D + c0) * 2;
 #pragma unroll 1
-    for (int c = 0; c < AT_D / 32; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t v[32];
-      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + 32u * c, v);
+      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * c), v);
       tc_wait_ld();
       if (!row_ok) continue;
 #pragma unroll
@@ -423,63 +461,164 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
 }
 
 // The ring's transfers: piece = (rank r, step j >= 1, head h, key tile kt, K or V),
-// in the order the work list needs them (ranks as the items run, then head, step, tile).
-__device__ void at_copy(const AttnParams& p) {
-  const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 6;
-  if (cw >= p.n_cw) return;
-  const int worker = blockIdx.x * p.n_cw + cw;
-  const int n_workers = gridDim.x * p.n_cw;
-  {
-    int ok = 1;
-    if (lane == 0) ok = at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, worker) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-  }
+// in the order the work list needs them (ranks as the items run, then step,
+// head, tile).  One thread per CTA moves its pieces (every gridDim.x-th) with
+// bulk copies through CP_NB shared-memory buffers of CP_SUB bytes: loads run
+// CP_NB-1 sub-pieces ahead of the stores, and a piece is counted once its
+// stores are complete.  The copy engine does the work, so the softmax warps
+// keep the issue slots.
+constexpr int CP_NB = 3;
+constexpr uint32_t CP_SUB = 8192;
+constexpr int CP_PEND = 16;
+
+struct RingPiece {
+  const uint8_t* src;
+  uint8_t* dst;
+  uint32_t bytes;
+  uint32_t* cnt;
+  bool skip;
+};
+
+__device__ __forceinline__ RingPiece ring_piece(const AttnParams& p, long long q) {
   const long long per_r = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2;
-  const long long total = per_r * p.R;
-  bool skip_first = (p.inject == 1 && worker == 0);
-  for (long long q = worker; q < total; q += n_workers) {
-    const int rr = static_cast<int>(q / per_r);
-    long long rem = q - rr * per_r;
-    const int r = p.R - 1 - rr;
-    const int h = static_cast<int>(rem / ((p.R - 1) * p.nkt * 2));
-    rem -= static_cast<long long>(h) * (p.R - 1) * p.nkt * 2;
-    const int j = 1 + static_cast<int>(rem / (p.nkt * 2));
-    rem -= static_cast<long long>(j - 1) * p.nkt * 2;
-    const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
-    const int s = (r - j + p.R) % p.R;
-    if (p.causal && s > r) continue;            // a later rank's keys: never read
-    int stop = 0;
-    if (lane == 0) stop = at_aborted(p) ? 1 : 0;
-    if (__shfl_sync(0xffffffffu, stop, 0)) return;
-    const int rows = min(AT_T, p.s_r - kt * AT_T);
-    const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
-    const size_t dst_off = ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) *
-                           AT_D * 2;
-    const uint8_t* src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
-    uint8_t* dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
-    const size_t n16 = static_cast<size_t>(rows) * AT_D * 2 / 16;
-    constexpr int U = 16;
-    for (size_t i0 = lane; i0 < n16; i0 += 32 * U) {
-      uint4 v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t idx = i0 + static_cast<size_t>(u) * 32;
-        if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
+  const int rr = static_cast<int>(q / per_r);
+  long long rem = q - rr * per_r;
+  const int r = p.R - 1 - rr;
+  // step-major: the query tiles of a rank run in parallel and all need step j before step j+1
+  const int j = 1 + static_cast<int>(rem / (static_cast<long long>(p.heads) * p.nkt * 2));
+  rem -= static_cast<long long>(j - 1) * p.heads * p.nkt * 2;
+  const int h = static_cast<int>(rem / (p.nkt * 2));
+  rem -= static_cast<long long>(h) * p.nkt * 2;
+  const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
+  const int s = (r - j + p.R) % p.R;
+  RingPiece pc;
+  pc.skip = p.causal && s > r;            // a later rank's keys: never read
+  const int rows = min(AT_T, p.s_r - kt * AT_T);
+  const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
+  const size_t dst_off =
+      ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
+  pc.src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
+  pc.dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
+  pc.bytes = static_cast<uint32_t>(rows) * AT_D * 2;
+  pc.cnt = at_counter(p, r, j, h);
+  return pc;
+}
+
+__device__ void at_copy(const AttnParams& p, uint32_t bufs, uint32_t cbars) {
+  if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, blockIdx.x)) return;
+  for (int b = 0; b < CP_NB; ++b) mbar_init(cbars + 8u * b, 1);
+  fence_mbar_init();
+  const long long total = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2 * p.R;
+  bool skip_first = (p.inject == 1 && blockIdx.x == 0);
+  // the sub-piece stream of this CTA: piece q (every gridDim.x-th), offset off
+  long long lq = blockIdx.x;   // next piece to load
+  uint32_t loff = 0;
+  RingPiece lp;
+  bool have = false;
+  auto next_sub = [&](RingPiece& pc, uint32_t& off, uint32_t& sz, bool& last) -> bool {
+    while (true) {
+      if (!have) {
+        while (lq < total) {
+          lp = ring_piece(p, lq);
+          if (!lp.skip) break;
+          lq += gridDim.x;
+        }
+        if (lq >= total) return false;
+        have = true;
+        loff = 0;
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t idx = i0 + static_cast<size_t>(u) * 32;
-        if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+      pc = lp;
+      off = loff;
+      sz = min(CP_SUB, lp.bytes - loff);
+      loff += sz;
+      last = (loff >= lp.bytes);
+      if (last) {
+        have = false;
+        lq += gridDim.x;
+      }
+      return true;
+    }
+  };
+  RingPiece q[CP_NB];
+  uint32_t qoff[CP_NB], qsz[CP_NB];
+  bool qlast[CP_NB];
+  uint32_t* pend_cnt[CP_PEND];
+  long long pend_seq[CP_PEND];
+  int n_pend = 0;
+  long long n_load = 0, n_store = 0;
+  bool more = true, ok = true;
+  auto issue = [&](long long seq) -> bool {
+    const int b = static_cast<int>(seq % CP_NB);
+    if (!next_sub(q[b], qoff[b], qsz[b], qlast[b])) return false;
+    mbar_arrive_expect_tx(cbars + 8u * b, qsz[b]);
+    bulk_g2s(bufs + static_cast<uint32_t>(b) * CP_SUB, q[b].src + qoff[b], qsz[b], cbars + 8u * b);
+    return true;
+  };
+  auto count = [&](uint32_t* c) {
+    if (skip_first) {
+      skip_first = false;
+      return;
+    }
+    atomicAdd(c, 1u);
+  };
+  for (; n_load < CP_NB - 1 && more; ++n_load) more = issue(n_load);
+  if (!more) --n_load;
+  while (n_store < n_load) {
+    const int b = static_cast<int>(n_store % CP_NB);
+    if (!at_wait_bar(p, cbars + 8u * b, static_cast<uint32_t>((n_store / CP_NB) & 1), WHERE_COPY,
+                     static_cast<int>(n_store))) {
+      ok = false;
+      break;
+    }
+    bulk_s2g(q[b].dst + qoff[b], bufs + static_cast<uint32_t>(b) * CP_SUB, qsz[b]);
+    bulk_commit();
+    if (qlast[b]) {
+      pend_cnt[n_pend] = q[b].cnt;
+      pend_seq[n_pend] = n_store;
+      ++n_pend;
+    }
+    ++n_store;
+    // count the pieces whose stores are at least two groups old (complete)
+    bulk_wait<2>();
+    int keep = 0;
+    for (int k = 0; k < n_pend; ++k) {
+      if (pend_seq[k] <= n_store - 3) {
+        fence_proxy_async_global();
+        __threadfence();
+        count(pend_cnt[k]);
+      } else {
+        pend_cnt[keep] = pend_cnt[k];
+        pend_seq[keep] = pend_seq[k];
+        ++keep;
       }
     }
+    n_pend = keep;
+    if (n_pend >= CP_PEND - 1) {
+      bulk_wait<0>();
+      fence_proxy_async_global();
+      __threadfence();
+      for (int k = 0; k < n_pend; ++k) count(pend_cnt[k]);
+      n_pend = 0;
+    }
+    if (more) {
+      bulk_wait_read<1>();   // the buffer refilled next was last stored two groups ago
+      if (issue(n_load)) ++n_load;
+      else more = false;
+    }
+    if (at_aborted(p)) {
+      ok = false;
+      break;
+    }
+  }
+  bulk_wait<0>();
+  // loads issued but never stored (abort) must land before the CTA leaves
+  for (long long k = n_store; k < n_load; ++k)
+    at_wait_bar(p, cbars + 8u * static_cast<uint32_t>(k % CP_NB), static_cast<uint32_t>((k / CP_NB) & 1),
+                WHERE_DRAIN, 0, false);
+  if (ok) {
+    fence_proxy_async_global();
     __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-      if (skip_first) skip_first = false;
-      else atomicAdd(at_counter(p, r, j, h, kt), 1u);
-    }
-    __syncwarp();
+    for (int k = 0; k < n_pend; ++k) count(pend_cnt[k]);
   }
 }
 
@@ -493,7 +632,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_BARS + B_TMEM);
   if (blockIdx.x == 0 && p.copy) {
     // zero this call's ring counters, then publish them
-    const long long n = static_cast<long long>(p.R) * (p.R - 1) * p.heads * p.nkt;
+    const long long n = static_cast<long long>(p.R) * (p.R - 1) * p.heads;
     for (long long x = threadIdx.x; x < n; x += AT_THREADS) p.cnt[x] = 0u;
     __threadfence();
     __syncthreads();
@@ -506,12 +645,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_KVFULL + 8u * s, 1);
       mbar_init(bars + B_KVEMPTY + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
-      mbar_init(bars + B_SEMPTY + 8u * s, 4);
+      mbar_init(bars + B_SEMPTY + 8u * s, 8);
     }
-    mbar_init(bars + B_PFULL, 4);
+    mbar_init(bars + B_PFULL, 8);
     mbar_init(bars + B_PVDONE, 1);
-    mbar_init(bars + B_OFREE, 4);
-    mbar_init(bars + B_TMEM + 8u, 1);   // MMA drain
+    mbar_init(bars + B_OFREE, 8);
+    mbar_init(bars + B_DRAIN, 1);       // MMA drain
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bars + B_PAIR + 8u * qq, 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -528,11 +668,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   } else if (warp == 1) {
     if (lane == 0) at_mma(p, bars, base, tmem);
     __syncwarp();
-  } else if (warp <= 5) {
-    at_softmax(p, bars, base, tmem);
+  } else if (warp <= 9) {
+    at_softmax(p, bars, base, tmem, reinterpret_cast<float*>(smem + AT_XCH));
     __syncwarp();
-  } else if (p.copy) {
-    at_copy(p);
+  } else if (warp == 10 && p.copy) {
+    if (lane == 0) at_copy(p, base + AT_CPY, bars + B_COPY);
     __syncwarp();
   }
   tc_fence_before();
@@ -554,7 +694,7 @@ bool attn_layout(int R, int heads, long long s_r, int d, AttnLayout& L) {
   L.nkt = static_cast<int>(ceil_div_ll(s_r, AT_T));
   L.nqt = L.nkt;
   L.cnt_off = WS_HDR_BYTES;
-  L.total = L.cnt_off + ((static_cast<size_t>(R) * std::max(R - 1, 0) * heads * L.nkt * 4 + 255) & ~size_t(255));
+  L.total = L.cnt_off + ((static_cast<size_t>(R) * std::max(R - 1, 0) * heads * 4 + 255) & ~size_t(255));
   return true;
 }
 
@@ -629,7 +769,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();
-  p.n_cw = AT_THREADS / 32 - 6;
+  p.n_cw = AT_THREADS / 32 - 10;
   const uint64_t rows = static_cast<uint64_t>(heads) * s_r;
   for (int r = 0; r < R; ++r) {
     p.out[r] = static_cast<uint8_t*>(out[r]);
