@@ -12,14 +12,15 @@
 //     into a TMEM accumulator (tcgen05, bf16 -> fp32);
 //   * warps 2-9 (softmax): online softmax, two warps per 32 query rows, each
 //     on half of the columns: running maximum and sum in fp32, P =
-//     exp2(scale * log2(e) * s - m) written as bf16 into shared memory for the
-//     PV product; O is rescaled only when the maximum grows by more than 2^8
+//     exp2(scale * log2(e) * s - m) written as bf16 into one of two shared
+//     memory buffers (by tile parity, so the next tile's P can be written
+//     while the PV product reads this one); O is rescaled only when the
+//     maximum grows by more than 2^8
 //     (the final division uses the same stale maximum for O and the sum, so
 //     the result is unchanged);
-//   * warp 10 (copy): the ring's transfers -- rank r receives the block of
-//     rank (r - j) mod R at step j -- as bulk async copies through shared
-//     memory into its receive buffer, one counter per (rank, step, head);
-//     warp 11 is idle.
+//   * warps 10-11 (copy): the ring's transfers -- rank r receives the block
+//     of rank (r - j) mod R at step j -- as row copies into its receive
+//     buffer, one counter per (rank, step, head).
 // Causal attention skips the tiles after each query tile (and, in ring order,
 // every block of a later rank: those blocks are not moved either).
 #include <algorithm>
@@ -41,15 +42,13 @@ constexpr int AT_MAX_R = 8;
 constexpr uint32_t AT_Q = 0;                 // Q tile: 2 K-major atoms of [128 rows x 128 B]
 constexpr uint32_t AT_KV = 32768;            // 2 stages of K (32 KB) + V (32 KB)
 constexpr uint32_t AT_KV_STAGE = 65536;
-constexpr uint32_t AT_P = AT_KV + 2 * AT_KV_STAGE;   // P tile, same layout as Q
-constexpr uint32_t AT_BARS = AT_P + 32768;
-constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima / sums exchanged by the softmax warp pairs
-constexpr uint32_t AT_CPY = AT_XCH + 4 * AT_T * 4;   // bulk-copy staging of the ring's transfers
-constexpr int AT_SMEM = 1024 + AT_CPY + 3 * 8192;
+constexpr uint32_t AT_P = AT_KV + 2 * AT_KV_STAGE;   // two P tiles (same layout as Q), by tile parity
+constexpr uint32_t AT_BARS = AT_P + 2 * 32768;
+constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of the softmax warp pairs
+constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
 constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KVFULL = 16, B_KVEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
-                   B_PFULL = 80, B_PVDONE = 88, B_OFREE = 96, B_TMEM = 104, B_DRAIN = 112, B_PAIR = 128,
-                   B_COPY = 160;
+                   B_PFULL = 80, B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t AT_O_COL = 256;
 // S = Q K^T: both operands K-major; O += P V: V MN-major
@@ -227,10 +226,10 @@ done:
 }
 
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, kv_ph = 0, pf_ph = 0, of_ph = 0;
-  uint32_t se_ph[2] = {0u, 0u};
+  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
+  uint32_t se_ph[2] = {0u, 0u}, pf_ph[2] = {0u, 0u};
   int stage = 0, prev_stage = 0;
-  int g = 0;   // tiles issued (S buffer = g % 2)
+  int g = 0;   // tiles issued (S buffer and P buffer = tile parity)
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
@@ -253,30 +252,32 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
           }
         tc_commit(bars + B_SFULL + 8u * sb);
         if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
-        ++g;
       }
       if (t > 0) {
-        // O += P_{t-1} V_{t-1}
-        if (!at_wait_bar(p, bars + B_PFULL, pf_ph, WHERE_MMA, i)) goto done;
-        pf_ph ^= 1u;
+        // O += P_{t-1} V_{t-1}; P_{t-1} sits in P buffer (g-1) & 1
+        const int pb = (g - 1) & 1;
+        if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, pf_ph[pb], WHERE_MMA, i)) goto done;
+        pf_ph[pb] ^= 1u;
         if (t == 1) {   // the previous item's O has been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
           of_ph ^= 1u;
         }
         tc_fence_after();
         const uint32_t vb = base + AT_KV + static_cast<uint32_t>(prev_stage) * AT_KV_STAGE + 32768u;
+        const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(pb);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_swz(base + AT_P + 16384u * a + 32u * k, 16u, 1024u, 2u);
+            const uint64_t ad = sdesc_swz(pbase + 16384u * a + 32u * k, 16u, 1024u, 2u);
             const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
             tc_mma_bf16(tmem + AT_O_COL, ad, bd, IDESC_PV, (t > 1 || a || k) ? 1u : 0u);
           }
         tc_commit(bars + B_KVEMPTY + 8u * prev_stage);
-        tc_commit(bars + B_PVDONE);
+        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer free, and O holds this product
       }
       if (t < it.n) {
+        ++g;
         prev_stage = stage;
         if (++stage == 2) {
           stage = 0;
@@ -311,6 +312,13 @@ __device__ __forceinline__ bool pair_sync(const AttnParams& p, uint32_t bar, uin
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// 2^x for x <= 0 or -inf (the hardware approximation, flushing subnormals).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -319,11 +327,17 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const int c0 = 64 * half;                                  // first column of this warp's half
   const uint32_t pbar = bars + B_PAIR + 8u * quarter;
+  const float c = p.scale_log2;
   uint32_t pair_ph = 0;
   uint32_t sf_ph[2] = {0u, 0u};
-  uint32_t pv_ph = 0;
+  uint32_t uses[2] = {0u, 0u};   // P tiles written into each buffer so far
   int g = 0;
-  int pv_pending = 0;   // PV products issued but not yet waited for (0 or 1)
+  // the product that last read P buffer b (its uses[b]-th) has completed
+  auto wait_pfree = [&](int b, int item) -> bool {
+    if (uses[b] == 0u) return true;
+    const int ok = at_wait_bar(p, bars + B_PFREE + 8u * b, (uses[b] - 1u) & 1u, WHERE_EPILOGUE, item) ? 1 : 0;
+    return __all_sync(0xffffffffu, ok) != 0;
+  };
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     const int qpos = it.qt * AT_T + row;                     // position within rank r's block
@@ -342,7 +356,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       sf_ph[sb] ^= 1u;
       tc_fence_after();
       const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(sb) * AT_T + static_cast<uint32_t>(c0);
-      uint32_t x[64];
+      float x[64];
       {
         uint32_t v0[32], v1[32];
         tc_ld_32x32b_x32(sbase, v0);
@@ -350,48 +364,47 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         tc_wait_ld();
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
-          x[q] = v0[q];
-          x[32 + q] = v1[q];
+          x[q] = __uint_as_float(v0[q]);
+          x[32 + q] = __uint_as_float(v1[q]);
         }
       }
       // S has been read: the MMA may overwrite this buffer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + B_SEMPTY + 8u * sb);
-      // scaled scores (log2 domain) and this half's row maximum
+      // masked keys become -inf (scale > 0 keeps the order, so the maximum is taken unscaled)
       float mx = -INFINITY;
+      if (__any_sync(0xffffffffu, lim < 64)) {
 #pragma unroll
-      for (int q = 0; q < 64; ++q) {
-        const float xv = (q < lim) ? __uint_as_float(x[q]) * p.scale_log2 : -INFINITY;
-        x[q] = __float_as_uint(xv);
-        mx = fmaxf(mx, xv);
+        for (int q = 0; q < 64; ++q) {
+          x[q] = (q < lim) ? x[q] : -INFINITY;
+          mx = fmaxf(mx, x[q]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) mx = fmaxf(mx, x[q]);
       }
-      xch[half * AT_T + row] = mx;
+      xch[half * AT_T + row] = mx * c;
       if (!pair_sync(p, pbar, pair_ph, i)) return;
-      mx = fmaxf(xch[row], xch[AT_T + row]);
-      if (!pair_sync(p, pbar, pair_ph, i)) return;   // both halves have read the maxima
+      mx = fmaxf(xch[row], xch[AT_T + row]);                 // the row's maximum, log2 domain
+      if (!pair_sync(p, pbar, pair_ph, i)) return;           // both halves have read the maxima
       const float m_new = fmaxf(m_run, mx);
-      // P of the previous tile has been consumed (and O updated) before P is rewritten
-      if (pv_pending) {
-        int ok = at_wait_bar(p, bars + B_PVDONE, pv_ph, WHERE_EPILOGUE, i) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, ok)) return;
-        pv_ph ^= 1u;
-        pv_pending = 0;
-      }
       float factor = 1.f;
       if (t == 0) {
         m_run = m_new;
       } else if (m_new > m_run + RESCALE_LOG2) {
-        factor = exp2f(m_run - m_new);
+        factor = ex2(m_run - m_new);
         m_run = m_new;
         l_run *= factor;
       }
       if (__any_sync(0xffffffffu, factor != 1.f)) {
+        // O must hold every earlier product: the one that read the other P buffer
+        if (!wait_pfree(sb ^ 1, i)) return;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
-          const uint32_t oaddr = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * c);
+          const uint32_t oaddr = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * cc);
           tc_ld_32x32b_x32(oaddr, v);
           tc_wait_ld();
 #pragma unroll
@@ -400,19 +413,22 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         }
         tc_wait_st();
       }
-      // P = exp2(x - m), the running sum, P as bf16 into shared memory
-      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      // P buffer sb was last read by the product two tiles ago
+      if (!wait_pfree(sb, i)) return;
+      // P = 2^(c*s - m), the running sum, P as bf16 into shared memory
+      const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
+      const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(sb);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {   // 8 keys per 16-byte chunk
+      for (int k8 = 0; k8 < 8; ++k8) {   // 8 keys per 16-byte chunk
         uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float p0 = exp2f(__uint_as_float(x[8 * c + 2 * q]) - mref);
-          const float p1 = exp2f(__uint_as_float(x[8 * c + 2 * q + 1]) - mref);
+          const float p0 = ex2(fmaf(x[8 * k8 + 2 * q], c, nm));
+          const float p1 = ex2(fmaf(x[8 * k8 + 2 * q + 1], c, nm));
           l_run += p0 + p1;
           pk[q] = pack_bf16x2(p0, p1);
         }
-        const uint32_t a = p_chunk_addr(base + AT_P, row, 8 * half + c);
+        const uint32_t a = p_chunk_addr(pbase, row, 8 * half + k8);
         asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
                      "r"(pk[2]), "r"(pk[3])
                      : "memory");
@@ -420,34 +436,29 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       fence_proxy_async_smem();   // P (generic stores) is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_PFULL);
-      pv_pending = 1;
+      if (lane == 0) mbar_arrive(bars + B_PFULL + 8u * sb);
+      ++uses[sb];
       ++g;
     }
-    // O of this item: the last PV has completed; the row sum is the two halves' sum
-    {
-      int ok = at_wait_bar(p, bars + B_PVDONE, pv_ph, WHERE_EPILOGUE, i) ? 1 : 0;
-      if (!__all_sync(0xffffffffu, ok)) return;
-      pv_ph ^= 1u;
-      pv_pending = 0;
-    }
-    xch[2 * AT_T + half * AT_T + row] = l_run;
+    // O of this item: the last product has completed; the row sum is the two halves' sum
+    if (!wait_pfree((g - 1) & 1, i)) return;
+    xch[half * AT_T + row] = l_run;
     if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const float l_all = xch[2 * AT_T + row] + xch[3 * AT_T + row];
+    const float l_all = xch[row] + xch[AT_T + row];
     if (!pair_sync(p, pbar, pair_ph, i)) return;
     tc_fence_after();
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const bool row_ok = qpos < p.s_r;
     uint8_t* orow = p.out[it.r] + ((static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D + c0) * 2;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
+    for (int cc = 0; cc < 2; ++cc) {
       uint32_t v[32];
-      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * c), v);
+      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * cc), v);
       tc_wait_ld();
       if (!row_ok) continue;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        st_global_v4(orow + (32 * c + 8 * q) * 2,
+        st_global_v4(orow + (32 * cc + 8 * q) * 2,
                      pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
                      pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
                      pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
@@ -462,163 +473,66 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
 
 // The ring's transfers: piece = (rank r, step j >= 1, head h, key tile kt, K or V),
 // in the order the work list needs them (ranks as the items run, then step,
-// head, tile).  One thread per CTA moves its pieces (every gridDim.x-th) with
-// bulk copies through CP_NB shared-memory buffers of CP_SUB bytes: loads run
-// CP_NB-1 sub-pieces ahead of the stores, and a piece is counted once its
-// stores are complete.  The copy engine does the work, so the softmax warps
-// keep the issue slots.
-constexpr int CP_NB = 3;
-constexpr uint32_t CP_SUB = 8192;
-constexpr int CP_PEND = 16;
-
-struct RingPiece {
-  const uint8_t* src;
-  uint8_t* dst;
-  uint32_t bytes;
-  uint32_t* cnt;
-  bool skip;
-};
-
-__device__ __forceinline__ RingPiece ring_piece(const AttnParams& p, long long q) {
-  const long long per_r = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2;
-  const int rr = static_cast<int>(q / per_r);
-  long long rem = q - rr * per_r;
-  const int r = p.R - 1 - rr;
-  // step-major: the query tiles of a rank run in parallel and all need step j before step j+1
-  const int j = 1 + static_cast<int>(rem / (static_cast<long long>(p.heads) * p.nkt * 2));
-  rem -= static_cast<long long>(j - 1) * p.heads * p.nkt * 2;
-  const int h = static_cast<int>(rem / (p.nkt * 2));
-  rem -= static_cast<long long>(h) * p.nkt * 2;
-  const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
-  const int s = (r - j + p.R) % p.R;
-  RingPiece pc;
-  pc.skip = p.causal && s > r;            // a later rank's keys: never read
-  const int rows = min(AT_T, p.s_r - kt * AT_T);
-  const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
-  const size_t dst_off =
-      ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
-  pc.src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
-  pc.dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
-  pc.bytes = static_cast<uint32_t>(rows) * AT_D * 2;
-  pc.cnt = at_counter(p, r, j, h);
-  return pc;
-}
-
-__device__ void at_copy(const AttnParams& p, uint32_t bufs, uint32_t cbars) {
-  if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, blockIdx.x)) return;
-  for (int b = 0; b < CP_NB; ++b) mbar_init(cbars + 8u * b, 1);
-  fence_mbar_init();
-  const long long total = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2 * p.R;
-  bool skip_first = (p.inject == 1 && blockIdx.x == 0);
-  // the sub-piece stream of this CTA: piece q (every gridDim.x-th), offset off
-  long long lq = blockIdx.x;   // next piece to load
-  uint32_t loff = 0;
-  RingPiece lp;
-  bool have = false;
-  auto next_sub = [&](RingPiece& pc, uint32_t& off, uint32_t& sz, bool& last) -> bool {
-    while (true) {
-      if (!have) {
-        while (lq < total) {
-          lp = ring_piece(p, lq);
-          if (!lp.skip) break;
-          lq += gridDim.x;
-        }
-        if (lq >= total) return false;
-        have = true;
-        loff = 0;
-      }
-      pc = lp;
-      off = loff;
-      sz = min(CP_SUB, lp.bytes - loff);
-      loff += sz;
-      last = (loff >= lp.bytes);
-      if (last) {
-        have = false;
-        lq += gridDim.x;
-      }
-      return true;
-    }
-  };
-  RingPiece q[CP_NB];
-  uint32_t qoff[CP_NB], qsz[CP_NB];
-  bool qlast[CP_NB];
-  uint32_t* pend_cnt[CP_PEND];
-  long long pend_seq[CP_PEND];
-  int n_pend = 0;
-  long long n_load = 0, n_store = 0;
-  bool more = true, ok = true;
-  auto issue = [&](long long seq) -> bool {
-    const int b = static_cast<int>(seq % CP_NB);
-    if (!next_sub(q[b], qoff[b], qsz[b], qlast[b])) return false;
-    mbar_arrive_expect_tx(cbars + 8u * b, qsz[b]);
-    bulk_g2s(bufs + static_cast<uint32_t>(b) * CP_SUB, q[b].src + qoff[b], qsz[b], cbars + 8u * b);
-    return true;
-  };
-  auto count = [&](uint32_t* c) {
-    if (skip_first) {
-      skip_first = false;
-      return;
-    }
-    atomicAdd(c, 1u);
-  };
-  for (; n_load < CP_NB - 1 && more; ++n_load) more = issue(n_load);
-  if (!more) --n_load;
-  while (n_store < n_load) {
-    const int b = static_cast<int>(n_store % CP_NB);
-    if (!at_wait_bar(p, cbars + 8u * b, static_cast<uint32_t>((n_store / CP_NB) & 1), WHERE_COPY,
-                     static_cast<int>(n_store))) {
-      ok = false;
-      break;
-    }
-    bulk_s2g(q[b].dst + qoff[b], bufs + static_cast<uint32_t>(b) * CP_SUB, qsz[b]);
-    bulk_commit();
-    if (qlast[b]) {
-      pend_cnt[n_pend] = q[b].cnt;
-      pend_seq[n_pend] = n_store;
-      ++n_pend;
-    }
-    ++n_store;
-    // count the pieces whose stores are at least two groups old (complete)
-    bulk_wait<2>();
-    int keep = 0;
-    for (int k = 0; k < n_pend; ++k) {
-      if (pend_seq[k] <= n_store - 3) {
-        fence_proxy_async_global();
-        __threadfence();
-        count(pend_cnt[k]);
-      } else {
-        pend_cnt[keep] = pend_cnt[k];
-        pend_seq[keep] = pend_seq[k];
-        ++keep;
-      }
-    }
-    n_pend = keep;
-    if (n_pend >= CP_PEND - 1) {
-      bulk_wait<0>();
-      fence_proxy_async_global();
-      __threadfence();
-      for (int k = 0; k < n_pend; ++k) count(pend_cnt[k]);
-      n_pend = 0;
-    }
-    if (more) {
-      bulk_wait_read<1>();   // the buffer refilled next was last stored two groups ago
-      if (issue(n_load)) ++n_load;
-      else more = false;
-    }
-    if (at_aborted(p)) {
-      ok = false;
-      break;
-    }
+// head, tile).  Copy warp w takes pieces w, w + n_workers, ...; each lane
+// streams 16-byte vectors, 16 loads in flight; after a piece every lane fences
+// and lane 0 counts it in its (rank, step, head) counter.
+__device__ void at_copy(const AttnParams& p) {
+  const int lane = threadIdx.x & 31;
+  const int cw = (threadIdx.x >> 5) - 10;
+  if (cw >= p.n_cw) return;
+  const int worker = blockIdx.x * p.n_cw + cw;
+  const int n_workers = gridDim.x * p.n_cw;
+  {
+    int ok = 1;
+    if (lane == 0) ok = at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, worker) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
   }
-  bulk_wait<0>();
-  // loads issued but never stored (abort) must land before the CTA leaves
-  for (long long k = n_store; k < n_load; ++k)
-    at_wait_bar(p, cbars + 8u * static_cast<uint32_t>(k % CP_NB), static_cast<uint32_t>((k / CP_NB) & 1),
-                WHERE_DRAIN, 0, false);
-  if (ok) {
-    fence_proxy_async_global();
+  const long long per_r = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2;
+  const long long total = per_r * p.R;
+  bool skip_first = (p.inject == 1 && worker == 0);
+  for (long long q = worker; q < total; q += n_workers) {
+    const int rr = static_cast<int>(q / per_r);
+    long long rem = q - rr * per_r;
+    const int r = p.R - 1 - rr;
+    // step-major: the query tiles of a rank run in parallel and all need step j before j+1
+    const int j = 1 + static_cast<int>(rem / (static_cast<long long>(p.heads) * p.nkt * 2));
+    rem -= static_cast<long long>(j - 1) * p.heads * p.nkt * 2;
+    const int h = static_cast<int>(rem / (p.nkt * 2));
+    rem -= static_cast<long long>(h) * p.nkt * 2;
+    const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
+    const int s = (r - j + p.R) % p.R;
+    if (p.causal && s > r) continue;            // a later rank's keys: never read
+    int stop = 0;
+    if (lane == 0) stop = at_aborted(p) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) return;
+    const int rows = min(AT_T, p.s_r - kt * AT_T);
+    const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
+    const size_t dst_off =
+        ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
+    const uint8_t* src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
+    uint8_t* dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
+    const size_t n16 = static_cast<size_t>(rows) * AT_D * 2 / 16;
+    constexpr int U = 16;
+    for (size_t i0 = lane; i0 < n16; i0 += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = i0 + static_cast<size_t>(u) * 32;
+        if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = i0 + static_cast<size_t>(u) * 32;
+        if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+      }
+    }
     __threadfence();
-    for (int k = 0; k < n_pend; ++k) count(pend_cnt[k]);
+    __syncwarp();
+    if (lane == 0) {
+      if (skip_first) skip_first = false;
+      else atomicAdd(at_counter(p, r, j, h), 1u);
+    }
+    __syncwarp();
   }
 }
 
@@ -647,8 +561,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_SFULL + 8u * s, 1);
       mbar_init(bars + B_SEMPTY + 8u * s, 8);
     }
-    mbar_init(bars + B_PFULL, 8);
-    mbar_init(bars + B_PVDONE, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars + B_PFULL + 8u * b, 8);
+      mbar_init(bars + B_PFREE + 8u * b, 1);
+    }
     mbar_init(bars + B_OFREE, 8);
     mbar_init(bars + B_DRAIN, 1);       // MMA drain
     for (int qq = 0; qq < 4; ++qq) mbar_init(bars + B_PAIR + 8u * qq, 2);
@@ -671,8 +587,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   } else if (warp <= 9) {
     at_softmax(p, bars, base, tmem, reinterpret_cast<float*>(smem + AT_XCH));
     __syncwarp();
-  } else if (warp == 10 && p.copy) {
-    if (lane == 0) at_copy(p, base + AT_CPY, bars + B_COPY);
+  } else if (p.copy) {
+    at_copy(p);
     __syncwarp();
   }
   tc_fence_before();
