@@ -9,15 +9,15 @@
 //     (128 keys each) in ring order -- the rank's own block, then the blocks
 //     of ranks r-1, r-2, ... as they land in its receive buffer;
 //   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
-//     into a TMEM accumulator (tcgen05, bf16 -> fp32);
-//   * warps 2-9 (softmax): online softmax, two warps per 32 query rows, each
-//     on half of the columns: running maximum and sum in fp32, P =
-//     exp2(scale * log2(e) * s - m) written as bf16 into one of two shared
-//     memory buffers (by tile parity, so the next tile's P can be written
-//     while the PV product reads this one); O is rescaled only when the
-//     maximum grows by more than 2^8
-//     (the final division uses the same stale maximum for O and the sum, so
-//     the result is unchanged);
+//     into one of two TMEM accumulators (tcgen05, bf16 -> fp32);
+//   * warps 2-9 (softmax): online softmax in two groups of four warps, one
+//     for the even key tiles of a query tile and one for the odd ones, each
+//     with its own running maximum, sum, P buffer (shared memory) and O
+//     accumulator (TMEM), so that two tiles' softmax runs at once; P =
+//     exp2(scale * log2(e) * s - m) as bf16; O is rescaled only when the
+//     maximum grows by more than 2^8 (the final division uses the same stale
+//     maximum for O and the sum, so the result is unchanged); at the end of a
+//     query tile the two groups merge their maxima, sums and O;
 //   * warps 10-11 (copy): the ring's transfers -- rank r receives the block
 //     of rank (r - j) mod R at step j -- as row copies into its receive
 //     buffer, one counter per (rank, step, head).
@@ -49,8 +49,8 @@ constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
 constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KVFULL = 16, B_KVEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
                    B_PFULL = 80, B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136;
-constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O [256,384)
-constexpr uint32_t AT_O_COL = 256;
+constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
+constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
 // S = Q K^T: both operands K-major; O += P V: V MN-major
 constexpr uint32_t IDESC_S = idesc_bf16_f32(AT_T, AT_T, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(AT_T, AT_D, false, true);
@@ -225,18 +225,20 @@ done:
   if (q_issued) at_wait_bar(p, bars + B_QFULL, q_par ^ 1u, WHERE_DRAIN, 0, false);
 }
 
+// MMA issuer.  Tile t of an item uses S, P and O buffers t & 1: the even
+// tiles' softmax (warps 2-5) and the odd tiles' (warps 6-9) each keep their
+// own running maximum, sum and O; they are merged when the item ends.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
   uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
   uint32_t se_ph[2] = {0u, 0u}, pf_ph[2] = {0u, 0u};
   int stage = 0, prev_stage = 0;
-  int g = 0;   // tiles issued (S buffer and P buffer = tile parity)
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
     q_ph ^= 1u;
     for (int t = 0; t <= it.n; ++t) {
       if (t < it.n) {
-        const int sb = g & 1;
+        const int sb = t & 1;
         if (!at_wait_bar(p, bars + B_KVFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
         if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, se_ph[sb] ^ 1u, WHERE_MMA, i)) goto done;
         se_ph[sb] ^= 1u;
@@ -254,30 +256,30 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
         if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
       }
       if (t > 0) {
-        // O += P_{t-1} V_{t-1}; P_{t-1} sits in P buffer (g-1) & 1
-        const int pb = (g - 1) & 1;
+        // O[pb] += P_{t-1} V_{t-1}
+        const int pb = (t - 1) & 1;
         if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, pf_ph[pb], WHERE_MMA, i)) goto done;
         pf_ph[pb] ^= 1u;
-        if (t == 1) {   // the previous item's O has been read out
+        if (t == 1) {   // the previous item's O buffers have been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
           of_ph ^= 1u;
         }
         tc_fence_after();
         const uint32_t vb = base + AT_KV + static_cast<uint32_t>(prev_stage) * AT_KV_STAGE + 32768u;
         const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(pb);
+        const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(pb) * AT_T;
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = sdesc_swz(pbase + 16384u * a + 32u * k, 16u, 1024u, 2u);
             const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
-            tc_mma_bf16(tmem + AT_O_COL, ad, bd, IDESC_PV, (t > 1 || a || k) ? 1u : 0u);
+            tc_mma_bf16(obuf, ad, bd, IDESC_PV, (t > 2 || a || k) ? 1u : 0u);
           }
         tc_commit(bars + B_KVEMPTY + 8u * prev_stage);
-        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer free, and O holds this product
+        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer free, and O[pb] holds this product
       }
       if (t < it.n) {
-        ++g;
         prev_stage = stage;
         if (++stage == 2) {
           stage = 0;
@@ -322,75 +324,56 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int half = (warp - 2) >> 2;
+  const int grp = (warp - 2) >> 2;                           // 0: even tiles, 1: odd tiles
   const int row = quarter * 32 + lane;                       // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const int c0 = 64 * half;                                  // first column of this warp's half
   const uint32_t pbar = bars + B_PAIR + 8u * quarter;
+  const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(grp) * AT_T;
+  const uint32_t obase = tmem + lane_off + AT_O_COL;
+  const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(grp);
   const float c = p.scale_log2;
-  uint32_t pair_ph = 0;
-  uint32_t sf_ph[2] = {0u, 0u};
-  uint32_t uses[2] = {0u, 0u};   // P tiles written into each buffer so far
-  int g = 0;
-  // the product that last read P buffer b (its uses[b]-th) has completed
-  auto wait_pfree = [&](int b, int item) -> bool {
-    if (uses[b] == 0u) return true;
-    const int ok = at_wait_bar(p, bars + B_PFREE + 8u * b, (uses[b] - 1u) & 1u, WHERE_EPILOGUE, item) ? 1 : 0;
-    return __all_sync(0xffffffffu, ok) != 0;
-  };
+  uint32_t pair_ph = 0, sf_ph = 0, uses = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     const int qpos = it.qt * AT_T + row;                     // position within rank r's block
     float m_run = -INFINITY, l_run = 0.f;
-    for (int t = 0; t < it.n; ++t) {
+    for (int t = grp; t < it.n; t += 2) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
-      const int sb = g & 1;
       const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
       const bool diag = p.causal && j == 0 && kt == it.qt;   // keys after the query are masked
-      const int lim = (diag ? min(valid, row + 1) : valid) - c0;   // valid keys in this half
+      const int lim = diag ? min(valid, row + 1) : valid;
+      const bool masked = __any_sync(0xffffffffu, lim < AT_T);
       {
-        int ok = at_wait_bar(p, bars + B_SFULL + 8u * sb, sf_ph[sb], WHERE_EPILOGUE, i) ? 1 : 0;
+        int ok = at_wait_bar(p, bars + B_SFULL + 8u * grp, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
         if (!__all_sync(0xffffffffu, ok)) return;
       }
-      sf_ph[sb] ^= 1u;
+      sf_ph ^= 1u;
       tc_fence_after();
-      const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(sb) * AT_T + static_cast<uint32_t>(c0);
-      float x[64];
-      {
-        uint32_t v0[32], v1[32];
-        tc_ld_32x32b_x32(sbase, v0);
-        tc_ld_32x32b_x32(sbase + 32u, v1);
-        tc_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          x[q] = __uint_as_float(v0[q]);
-          x[32 + q] = __uint_as_float(v1[q]);
-        }
-      }
-      // S has been read: the MMA may overwrite this buffer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_SEMPTY + 8u * sb);
-      // masked keys become -inf (scale > 0 keeps the order, so the maximum is taken unscaled)
+      // pass 1: the row maximum (scale > 0 keeps the order: taken unscaled)
       float mx = -INFINITY;
-      if (__any_sync(0xffffffffu, lim < 64)) {
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(sbase + 32u * cc, v);
+        tc_wait_ld();
+        if (masked) {
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          x[q] = (q < lim) ? x[q] : -INFINITY;
-          mx = fmaxf(mx, x[q]);
+          for (int q = 0; q < 32; ++q)
+            if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(v[q]));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) mx = fmaxf(mx, __uint_as_float(v[q]));
         }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 64; ++q) mx = fmaxf(mx, x[q]);
       }
-      xch[half * AT_T + row] = mx * c;
-      if (!pair_sync(p, pbar, pair_ph, i)) return;
-      mx = fmaxf(xch[row], xch[AT_T + row]);                 // the row's maximum, log2 domain
-      if (!pair_sync(p, pbar, pair_ph, i)) return;           // both halves have read the maxima
-      const float m_new = fmaxf(m_run, mx);
+      const float m_new = fmaxf(m_run, mx * c);
+      // the product that last read this P buffer (and wrote this O) has completed
+      if (uses > 0u) {
+        int ok = at_wait_bar(p, bars + B_PFREE + 8u * grp, (uses - 1u) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
       float factor = 1.f;
-      if (t == 0) {
+      if (t == grp) {
         m_run = m_new;
       } else if (m_new > m_run + RESCALE_LOG2) {
         factor = ex2(m_run - m_new);
@@ -398,72 +381,96 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         l_run *= factor;
       }
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        // O must hold every earlier product: the one that read the other P buffer
-        if (!wait_pfree(sb ^ 1, i)) return;
         tc_fence_after();
+        const uint32_t ob = obase + static_cast<uint32_t>(grp) * AT_T;
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t v[32];
-          const uint32_t oaddr = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * cc);
-          tc_ld_32x32b_x32(oaddr, v);
+          tc_ld_32x32b_x32(ob + 32u * cc, v);
           tc_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
-          tc_st_32x32b_x32(oaddr, v);
+          tc_st_32x32b_x32(ob + 32u * cc, v);
         }
         tc_wait_st();
       }
-      // P buffer sb was last read by the product two tiles ago
-      if (!wait_pfree(sb, i)) return;
-      // P = 2^(c*s - m), the running sum, P as bf16 into shared memory
-      const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
-      const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(sb);
+      // pass 2: P = 2^(c*s - m), the running sum, P as bf16 into shared memory
+      const float nm = -m_run;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(sbase + 32u * cc, v);
+        tc_wait_ld();
 #pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8) {   // 8 keys per 16-byte chunk
-        uint32_t pk[4];
+        for (int k8 = 0; k8 < 4; ++k8) {   // 8 keys per 16-byte chunk
+          uint32_t pk[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float p0 = ex2(fmaf(x[8 * k8 + 2 * q], c, nm));
-          const float p1 = ex2(fmaf(x[8 * k8 + 2 * q + 1], c, nm));
-          l_run += p0 + p1;
-          pk[q] = pack_bf16x2(p0, p1);
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 32 * cc + 8 * k8 + 2 * q;
+            float p0 = ex2(fmaf(__uint_as_float(v[8 * k8 + 2 * q]), c, nm));
+            float p1 = ex2(fmaf(__uint_as_float(v[8 * k8 + 2 * q + 1]), c, nm));
+            if (masked) {
+              p0 = (kk < lim) ? p0 : 0.f;
+              p1 = (kk + 1 < lim) ? p1 : 0.f;
+            }
+            l_run += p0 + p1;
+            pk[q] = pack_bf16x2(p0, p1);
+          }
+          const uint32_t a = p_chunk_addr(pbase, row, 4 * cc + k8);
+          asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
+                       "r"(pk[2]), "r"(pk[3])
+                       : "memory");
         }
-        const uint32_t a = p_chunk_addr(pbase, row, 8 * half + k8);
-        asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
-                     "r"(pk[2]), "r"(pk[3])
-                     : "memory");
       }
-      fence_proxy_async_smem();   // P (generic stores) is read by the tensor cores
+      // S read out: the MMA may overwrite it; P written: the product may read it
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_PFULL + 8u * sb);
-      ++uses[sb];
-      ++g;
+      if (lane == 0) {
+        mbar_arrive(bars + B_SEMPTY + 8u * grp);
+        mbar_arrive(bars + B_PFULL + 8u * grp);
+      }
+      ++uses;
     }
-    // O of this item: the last product has completed; the row sum is the two halves' sum
-    if (!wait_pfree((g - 1) & 1, i)) return;
-    xch[half * AT_T + row] = l_run;
+    // item done: this group's last product has completed
+    if (grp < it.n) {
+      int ok = at_wait_bar(p, bars + B_PFREE + 8u * grp, (uses - 1u) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, ok)) return;
+    }
+    // merge the two groups' (maximum, sum, O): exchange maxima, then scaled sums
+    xch[grp * AT_T + row] = m_run;
     if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const float l_all = xch[row] + xch[AT_T + row];
+    const float m0 = xch[row], m1 = xch[AT_T + row];
+    if (!pair_sync(p, pbar, pair_ph, i)) return;
+    const bool two = it.n > 1;                               // the odd group had tiles
+    const float m = two ? fmaxf(m0, m1) : m0;
+    const float f0 = ex2(m0 - m), f1 = two ? ex2(m1 - m) : 0.f;
+    xch[grp * AT_T + row] = l_run * (grp ? f1 : f0);
+    if (!pair_sync(p, pbar, pair_ph, i)) return;
+    const float l_all = xch[row] + (two ? xch[AT_T + row] : 0.f);
     if (!pair_sync(p, pbar, pair_ph, i)) return;
     tc_fence_after();
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const bool row_ok = qpos < p.s_r;
+    const int c0 = 64 * grp;                                 // this group writes output columns c0 .. c0+63
     uint8_t* orow = p.out[it.r] + ((static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D + c0) * 2;
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
-      uint32_t v[32];
-      tc_ld_32x32b_x32(tmem + lane_off + AT_O_COL + static_cast<uint32_t>(c0 + 32 * cc), v);
+      uint32_t v0[32], v1[32];
+      tc_ld_32x32b_x32(obase + static_cast<uint32_t>(c0 + 32 * cc), v0);
+      tc_ld_32x32b_x32(obase + AT_T + static_cast<uint32_t>(c0 + 32 * cc), v1);
       tc_wait_ld();
       if (!row_ok) continue;
+      float o[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        st_global_v4(orow + (32 * cc + 8 * q) * 2,
-                     pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
-      }
+      for (int q = 0; q < 32; ++q)
+        o[q] = (two ? fmaf(__uint_as_float(v0[q]), f0, __uint_as_float(v1[q]) * f1)
+                    : __uint_as_float(v0[q]) * f0) * inv;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_global_v4(orow + (32 * cc + 8 * q) * 2, pack_bf16x2(o[8 * q], o[8 * q + 1]),
+                     pack_bf16x2(o[8 * q + 2], o[8 * q + 3]), pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
+                     pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
     }
     tc_fence_before();
     __syncwarp();
@@ -559,10 +566,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_KVFULL + 8u * s, 1);
       mbar_init(bars + B_KVEMPTY + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
-      mbar_init(bars + B_SEMPTY + 8u * s, 8);
+      mbar_init(bars + B_SEMPTY + 8u * s, 4);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + B_PFULL + 8u * b, 8);
+      mbar_init(bars + B_PFULL + 8u * b, 4);
       mbar_init(bars + B_PFREE + 8u * b, 1);
     }
     mbar_init(bars + B_OFREE, 8);
