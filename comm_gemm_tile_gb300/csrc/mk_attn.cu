@@ -320,6 +320,30 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Two fp32 lanes in one 64-bit register: a*b + c and a + b on both lanes at once.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -363,7 +387,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
             if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(v[q]));
         } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) mx = fmaxf(mx, __uint_as_float(v[q]));
+          for (int q = 0; q < 32; q += 2) mx = fmax3(mx, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
         }
       }
       const float m_new = fmaxf(m_run, mx * c);
@@ -395,7 +419,9 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         tc_wait_st();
       }
       // pass 2: P = 2^(c*s - m), the running sum, P as bf16 into shared memory
-      const float nm = -m_run;
+      // (two lanes per packed fp32 fused multiply-add / add)
+      const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_run, -m_run);
+      uint64_t l2 = f2pack(0.f, 0.f);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
@@ -407,13 +433,16 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int kk = 32 * cc + 8 * k8 + 2 * q;
-            float p0 = ex2(fmaf(__uint_as_float(v[8 * k8 + 2 * q]), c, nm));
-            float p1 = ex2(fmaf(__uint_as_float(v[8 * k8 + 2 * q + 1]), c, nm));
+            float e0, e1;
+            f2unpack(f2fma(f2pack(__uint_as_float(v[8 * k8 + 2 * q]), __uint_as_float(v[8 * k8 + 2 * q + 1])), c2,
+                           nm2),
+                     e0, e1);
+            float p0 = ex2(e0), p1 = ex2(e1);
             if (masked) {
               p0 = (kk < lim) ? p0 : 0.f;
               p1 = (kk + 1 < lim) ? p1 : 0.f;
             }
-            l_run += p0 + p1;
+            l2 = f2add(l2, f2pack(p0, p1));
             pk[q] = pack_bf16x2(p0, p1);
           }
           const uint32_t a = p_chunk_addr(pbase, row, 4 * cc + k8);
@@ -421,6 +450,11 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
                        "r"(pk[2]), "r"(pk[3])
                        : "memory");
         }
+      }
+      {
+        float la, lb;
+        f2unpack(l2, la, lb);
+        l_run += la + lb;
       }
       // S read out: the MMA may overwrite it; P written: the product may read it
       fence_proxy_async_smem();
