@@ -4,10 +4,11 @@
 // while each rank attends its queries to every block that has arrived,
 // merging the partial softmax results.
 //
-// One persistent launch of 384 threads per CTA, one CTA per SM:
-//   * warp 0 (TMA): a 128-query tile of one (rank, head), then the K/V tiles
-//     (128 keys each) in ring order -- the rank's own block, then the blocks
-//     of ranks r-1, r-2, ... as they land in its receive buffer;
+// One persistent launch of 416 threads per CTA, one CTA per SM:
+//   * warps 0 and 12 (TMA): a 128-query tile of one (rank, head), then the K
+//     (warp 0) and V (warp 12) tiles, 128 keys each, in ring order -- the
+//     rank's own block, then the blocks of ranks r-1, r-2, ... as they land
+//     in its receive buffer;
 //   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
 //     into one of two TMEM accumulators (tcgen05, bf16 -> fp32);
 //   * warps 2-9 (softmax): online softmax in two groups of four warps, one
@@ -36,7 +37,7 @@ namespace {
 
 constexpr int AT_D = 128;                    // head dimension
 constexpr int AT_T = 128;                    // query rows / keys per tile
-constexpr int AT_THREADS = 384;
+constexpr int AT_THREADS = 416;              // 13 warps: see the role list above
 constexpr int AT_MAX_R = 8;
 // shared memory (from the 1024-aligned base)
 constexpr uint32_t AT_Q = 0;                 // Q tile: 2 K-major atoms of [128 rows x 128 B]
@@ -47,8 +48,9 @@ constexpr uint32_t AT_BARS = AT_P + 2 * 32768;
 constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of the softmax warp pairs
 constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KVFULL = 16, B_KVEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
-                   B_PFULL = 80, B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136;
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_KEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
+                   B_PFULL = 80, B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136,
+                   B_VFULL = 168, B_VEMPTY = 184;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
 // S = Q K^T: both operands K-major; O += P V: V MN-major
@@ -161,18 +163,24 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 }
 
 // ------------------------------------------------------------------ roles
+// TMA producers: warp 0 loads the Q tile of each item and the K tiles, warp 12
+// the V tiles, each into its half of the two K/V stages with its own
+// full/empty barriers -- a K stage is free again once S has read it, long
+// before the PV product frees the V stage.
+template <bool IS_V>
 __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
+  const uint32_t FULL = IS_V ? B_VFULL : B_KFULL, EMPTY = IS_V ? B_VEMPTY : B_KEMPTY;
   int stage = 0;
-  uint32_t kv_ph = 0, q_ph = 0;
+  uint32_t ph = 0, q_ph = 0;
   uint32_t issued_mask = 0, issued_par = 0;
   bool ready = false;
   bool q_issued = false;
   uint32_t q_par = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
-    if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
-    q_ph ^= 1u;
-    {
+    if (!IS_V) {
+      if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+      q_ph ^= 1u;
       const int qrow = it.h * p.s_r + it.qt * AT_T;
       mbar_arrive_expect_tx(bars + B_QFULL, 2u * 16384u);
       tma_load_2d(base + AT_Q, &p.tmQ[it.r], bars + B_QFULL, 0, qrow);
@@ -184,9 +192,8 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
     for (int t = 0; t < it.n; ++t) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
-      if (!at_wait_bar(p, bars + B_KVEMPTY + 8u * stage, kv_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
-      const CUtensorMap* mk = &p.tmK[s];
-      const CUtensorMap* mv = &p.tmV[s];
+      if (!at_wait_bar(p, bars + EMPTY + 8u * stage, ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+      const CUtensorMap* m = IS_V ? &p.tmV[s] : &p.tmK[s];
       int row = it.h * p.s_r + kt * AT_T;
       if (j > 0 && p.use_recv) {
         if (p.wait && j != waited_j) {
@@ -198,30 +205,31 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
           fence_proxy_async_global();
           waited_j = j;
         }
-        mk = &p.tmKr[it.r];
-        mv = &p.tmVr[it.r];
+        m = IS_V ? &p.tmVr[it.r] : &p.tmKr[it.r];
         row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
       }
-      const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
-      const uint32_t vb = kb + 32768u;
-      const uint32_t full = bars + B_KVFULL + 8u * stage;
-      mbar_arrive_expect_tx(full, 65536u);
-      tma_load_2d(kb, mk, full, 0, row);
-      tma_load_2d(kb + 16384u, mk, full, 64, row);
-      tma_load_3d(vb, mv, full, 0, row, 0);
-      tma_load_3d(vb + 16384u, mv, full, 0, row + 64, 0);
+      const uint32_t dst = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE + (IS_V ? 32768u : 0u);
+      const uint32_t full = bars + FULL + 8u * stage;
+      mbar_arrive_expect_tx(full, 32768u);
+      if (IS_V) {
+        tma_load_3d(dst, m, full, 0, row, 0);
+        tma_load_3d(dst + 16384u, m, full, 0, row + 64, 0);
+      } else {
+        tma_load_2d(dst, m, full, 0, row);
+        tma_load_2d(dst + 16384u, m, full, 64, row);
+      }
       issued_mask |= 1u << stage;
-      issued_par = (issued_par & ~(1u << stage)) | (kv_ph << stage);
+      issued_par = (issued_par & ~(1u << stage)) | (ph << stage);
       if (++stage == 2) {
         stage = 0;
-        kv_ph ^= 1u;
+        ph ^= 1u;
       }
     }
   }
 done:
   for (int s2 = 0; s2 < 2; ++s2)
     if (issued_mask & (1u << s2))
-      at_wait_bar(p, bars + B_KVFULL + 8u * s2, (issued_par >> s2) & 1u, WHERE_DRAIN, s2, false);
+      at_wait_bar(p, bars + FULL + 8u * s2, (issued_par >> s2) & 1u, WHERE_DRAIN, s2, false);
   if (q_issued) at_wait_bar(p, bars + B_QFULL, q_par ^ 1u, WHERE_DRAIN, 0, false);
 }
 
@@ -229,7 +237,7 @@ done:
 // tiles' softmax (warps 2-5) and the odd tiles' (warps 6-9) each keep their
 // own running maximum, sum and O; they are merged when the item ends.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
+  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0, prev_ph = 0;
   uint32_t se_ph[2] = {0u, 0u}, pf_ph[2] = {0u, 0u};
   int stage = 0, prev_stage = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
@@ -239,7 +247,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     for (int t = 0; t <= it.n; ++t) {
       if (t < it.n) {
         const int sb = t & 1;
-        if (!at_wait_bar(p, bars + B_KVFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_bar(p, bars + B_KFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
         if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, se_ph[sb] ^ 1u, WHERE_MMA, i)) goto done;
         se_ph[sb] ^= 1u;
         tc_fence_after();
@@ -253,6 +261,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
             tc_mma_bf16(tmem + static_cast<uint32_t>(sb) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
           }
         tc_commit(bars + B_SFULL + 8u * sb);
+        tc_commit(bars + B_KEMPTY + 8u * stage);          // this K stage may be refilled
         if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
       }
       if (t > 0) {
@@ -260,6 +269,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
         const int pb = (t - 1) & 1;
         if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, pf_ph[pb], WHERE_MMA, i)) goto done;
         pf_ph[pb] ^= 1u;
+        if (!at_wait_bar(p, bars + B_VFULL + 8u * prev_stage, prev_ph, WHERE_MMA, i)) goto done;
         if (t == 1) {   // the previous item's O buffers have been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
           of_ph ^= 1u;
@@ -276,11 +286,12 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
             const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
             tc_mma_bf16(obuf, ad, bd, IDESC_PV, (t > 2 || a || k) ? 1u : 0u);
           }
-        tc_commit(bars + B_KVEMPTY + 8u * prev_stage);
+        tc_commit(bars + B_VEMPTY + 8u * prev_stage);
         tc_commit(bars + B_PFREE + 8u * pb);   // P buffer free, and O[pb] holds this product
       }
       if (t < it.n) {
         prev_stage = stage;
+        prev_ph = kv_ph;
         if (++stage == 2) {
           stage = 0;
           kv_ph ^= 1u;
@@ -597,8 +608,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     mbar_init(bars + B_QFULL, 1);
     mbar_init(bars + B_QEMPTY, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bars + B_KVFULL + 8u * s, 1);
-      mbar_init(bars + B_KVEMPTY + 8u * s, 1);
+      mbar_init(bars + B_KFULL + 8u * s, 1);
+      mbar_init(bars + B_KEMPTY + 8u * s, 1);
+      mbar_init(bars + B_VFULL + 8u * s, 1);
+      mbar_init(bars + B_VEMPTY + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
       mbar_init(bars + B_SEMPTY + 8u * s, 4);
     }
@@ -619,8 +632,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp == 0) {
-    if (lane == 0) at_producer(p, bars, base);
+  if (warp == 0 || warp == 12) {
+    if (lane == 0) {
+      if (warp == 0) at_producer<false>(p, bars, base);
+      else at_producer<true>(p, bars, base);
+    }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) at_mma(p, bars, base, tmem);
@@ -628,7 +644,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   } else if (warp <= 9) {
     at_softmax(p, bars, base, tmem, reinterpret_cast<float*>(smem + AT_XCH));
     __syncwarp();
-  } else if (p.copy) {
+  } else if (warp <= 11 && p.copy) {
     at_copy(p);
     __syncwarp();
   }
@@ -726,7 +742,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();
-  p.n_cw = AT_THREADS / 32 - 10;
+  p.n_cw = 2;   // warps 10-11
   const uint64_t rows = static_cast<uint64_t>(heads) * s_r;
   for (int r = 0; r < R; ++r) {
     p.out[r] = static_cast<uint8_t*>(out[r]);
