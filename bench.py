@@ -74,12 +74,16 @@ def whole_job_rate(units_per_rank: float, world: int, t_max_ms: float) -> float:
     return world * units_per_rank / (t_max_ms * 1e-3)
 
 
+# The sources of mk_fused_kernel and of the host code that plans its launches.
+FUSED_KERNEL_SOURCES = ("mk_api.cu", "mk_fused.cu", "mk_internal.h", "mk_ptx.cuh")
+
+
 def kernel_source_sha256() -> str:
-    """Hash of the CUDA sources, to tell whether recorded ncu counters still apply."""
+    """Hash of mk_fused_kernel's sources, to tell whether recorded ncu counters still apply."""
     import hashlib
     root = os.path.join(ROOT, "comm_gemm_tile_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(root)):
+    for f in FUSED_KERNEL_SOURCES:
         h.update(f.encode())
         h.update(open(os.path.join(root, f), "rb").read())
     return h.hexdigest()
