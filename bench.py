@@ -285,7 +285,8 @@ def main():
     ap.add_argument("--n-copy", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
-    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring"], default=None,
+    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring", "ring_small"],
+                    default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -441,6 +442,14 @@ def run_only(args):
     bf16_peak, _, hbm_peak, _ = peaks()
     if args.only == "moe":
         res = bench_moe(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    elif args.only == "ring_small":
+        # profiling aid: three calls of a mid-size ring attention (4 ranks x 2048, 4 heads), K/V in place
+        shape = (4, 2048, 128)
+        q, k, v = ([dev_normal(shape, 1.0, seed + r, device) for r in range(4)] for seed in (1, 11, 21))
+        for _ in range(3):
+            mk.ring_attention(q, k, v, cfg=mk.Config(mode=mk.MODE_GEMM_ONLY))
+        torch.cuda.synchronize()
+        res = {"status": mk.status_string(mk.device_status()[0])}
     elif args.only == "ring":
         res = {"full": bench_ring(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
                                   hbm_peak),
