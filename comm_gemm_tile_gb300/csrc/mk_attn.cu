@@ -48,9 +48,8 @@ constexpr uint32_t AT_BARS = AT_P + 2 * 32768;
 constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of the softmax warp pairs
 constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_KEMPTY = 32, B_SFULL = 48, B_SEMPTY = 64,
-                   B_PFULL = 80, B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136,
-                   B_VFULL = 168, B_VEMPTY = 184;
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_SFULL = 48, B_SEMPTY = 64, B_PFULL = 80,
+                   B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136, B_VFULL = 168;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
 // S = Q K^T: both operands K-major; O += P V: V MN-major
@@ -164,12 +163,16 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 
 // ------------------------------------------------------------------ roles
 // TMA producers: warp 0 loads the Q tile of each item and the K tiles, warp 12
-// the V tiles, each into its half of the two K/V stages with its own
-// full/empty barriers -- a K stage is free again once S has read it, long
-// before the PV product frees the V stage.
+// the V tiles, each into its half of the two K/V stages with its own full
+// barrier.  Stage, S buffer, P buffer and O buffer of a tile are all the
+// parity of the CTA's running tile count, so the MMA's two completion
+// signals per tile also free the stages: a K stage once S of its previous
+// tile is done (S full), a V stage once that tile's product is done (P free)
+// -- a K stage is free again long before the V stage.  Each tcgen05.commit
+// stalls the MMA issue briefly, so the MMA commits only these two per tile.
 template <bool IS_V>
 __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
-  const uint32_t FULL = IS_V ? B_VFULL : B_KFULL, EMPTY = IS_V ? B_VEMPTY : B_KEMPTY;
+  const uint32_t FULL = IS_V ? B_VFULL : B_KFULL, EMPTY = IS_V ? B_PFREE : B_SFULL;
   int stage = 0;
   uint32_t ph = 0, q_ph = 0;
   uint32_t issued_mask = 0, issued_par = 0;
@@ -233,12 +236,13 @@ done:
   if (q_issued) at_wait_bar(p, bars + B_QFULL, q_par ^ 1u, WHERE_DRAIN, 0, false);
 }
 
-// MMA issuer.  Tile t of an item uses S, P and O buffers t & 1: the even
-// tiles' softmax (warps 2-5) and the odd tiles' (warps 6-9) each keep their
-// own running maximum, sum and O; they are merged when the item ends.
+// MMA issuer.  The CTA's n-th tile (counted over all its items) uses K/V
+// stage, S, P and O buffers n & 1: the softmax of the even ones (warps 2-5)
+// and of the odd ones (warps 6-9) each keep their own running maximum, sum
+// and O for the item; they are merged when the item ends.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
   uint32_t q_ph = 0, kv_ph = 0, of_ph = 0, prev_ph = 0;
-  uint32_t se_ph[2] = {0u, 0u}, pf_ph[2] = {0u, 0u};
+  uint32_t se_ph = 0, pf_ph = 0;   // phase bits of the S-empty / P-full barriers, bit b for buffer b
   int stage = 0, prev_stage = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
@@ -246,10 +250,10 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     q_ph ^= 1u;
     for (int t = 0; t <= it.n; ++t) {
       if (t < it.n) {
-        const int sb = t & 1;
+        const int sb = stage;
         if (!at_wait_bar(p, bars + B_KFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
-        if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, se_ph[sb] ^ 1u, WHERE_MMA, i)) goto done;
-        se_ph[sb] ^= 1u;
+        if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, ((se_ph >> sb) & 1u) ^ 1u, WHERE_MMA, i)) goto done;
+        se_ph ^= 1u << sb;
         tc_fence_after();
         const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
 #pragma unroll
@@ -260,15 +264,14 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
             const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
             tc_mma_bf16(tmem + static_cast<uint32_t>(sb) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
           }
-        tc_commit(bars + B_SFULL + 8u * sb);
-        tc_commit(bars + B_KEMPTY + 8u * stage);          // this K stage may be refilled
+        tc_commit(bars + B_SFULL + 8u * sb);              // S ready; this K stage may be refilled
         if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
       }
       if (t > 0) {
         // O[pb] += P_{t-1} V_{t-1}
-        const int pb = (t - 1) & 1;
-        if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, pf_ph[pb], WHERE_MMA, i)) goto done;
-        pf_ph[pb] ^= 1u;
+        const int pb = prev_stage;
+        if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, (pf_ph >> pb) & 1u, WHERE_MMA, i)) goto done;
+        pf_ph ^= 1u << pb;
         if (!at_wait_bar(p, bars + B_VFULL + 8u * prev_stage, prev_ph, WHERE_MMA, i)) goto done;
         if (t == 1) {   // the previous item's O buffers have been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
@@ -286,8 +289,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
             const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
             tc_mma_bf16(obuf, ad, bd, IDESC_PV, (t > 2 || a || k) ? 1u : 0u);
           }
-        tc_commit(bars + B_VEMPTY + 8u * prev_stage);
-        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer free, and O[pb] holds this product
+        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer and V stage free; O[pb] holds this product
       }
       if (t < it.n) {
         prev_stage = stage;
@@ -359,7 +361,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int grp = (warp - 2) >> 2;                           // 0: even tiles, 1: odd tiles
+  const int grp = (warp - 2) >> 2;                           // 0: even tiles, 1: odd tiles (running count)
   const int row = quarter * 32 + lane;                       // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t pbar = bars + B_PAIR + 8u * quarter;
@@ -368,11 +370,15 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
   const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(grp);
   const float c = p.scale_log2;
   uint32_t pair_ph = 0, sf_ph = 0, uses = 0;
+  uint32_t count = 0;                                        // tiles of the CTA's earlier items
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     const int qpos = it.qt * AT_T + row;                     // position within rank r's block
+    const int par = static_cast<int>(count & 1u);
+    const int t0 = grp ^ par;                                // this group's first tile of the item
+    count += static_cast<uint32_t>(it.n);
     float m_run = -INFINITY, l_run = 0.f;
-    for (int t = grp; t < it.n; t += 2) {
+    for (int t = t0; t < it.n; t += 2) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
       const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
@@ -408,7 +414,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         if (!__all_sync(0xffffffffu, ok)) return;
       }
       float factor = 1.f;
-      if (t == grp) {
+      if (t == t0) {
         m_run = m_new;
       } else if (m_new > m_run + RESCALE_LOG2) {
         factor = ex2(m_run - m_new);
@@ -478,7 +484,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       ++uses;
     }
     // item done: this group's last product has completed
-    if (grp < it.n) {
+    if (t0 < it.n) {
       int ok = at_wait_bar(p, bars + B_PFREE + 8u * grp, (uses - 1u) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
       if (!__all_sync(0xffffffffu, ok)) return;
     }
@@ -487,12 +493,12 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
     if (!pair_sync(p, pbar, pair_ph, i)) return;
     const float m0 = xch[row], m1 = xch[AT_T + row];
     if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const bool two = it.n > 1;                               // the odd group had tiles
-    const float m = two ? fmaxf(m0, m1) : m0;
-    const float f0 = ex2(m0 - m), f1 = two ? ex2(m1 - m) : 0.f;
+    const bool h0 = par < it.n, h1 = (par ^ 1) < it.n;       // the group had tiles of this item
+    const float m = h0 ? (h1 ? fmaxf(m0, m1) : m0) : m1;
+    const float f0 = h0 ? ex2(m0 - m) : 0.f, f1 = h1 ? ex2(m1 - m) : 0.f;
     xch[grp * AT_T + row] = l_run * (grp ? f1 : f0);
     if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const float l_all = xch[row] + (two ? xch[AT_T + row] : 0.f);
+    const float l_all = (h0 ? xch[row] : 0.f) + (h1 ? xch[AT_T + row] : 0.f);
     if (!pair_sync(p, pbar, pair_ph, i)) return;
     tc_fence_after();
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
@@ -509,8 +515,9 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       float o[32];
 #pragma unroll
       for (int q = 0; q < 32; ++q)
-        o[q] = (two ? fmaf(__uint_as_float(v0[q]), f0, __uint_as_float(v1[q]) * f1)
-                    : __uint_as_float(v0[q]) * f0) * inv;
+        o[q] = (h0 ? (h1 ? fmaf(__uint_as_float(v0[q]), f0, __uint_as_float(v1[q]) * f1)
+                         : __uint_as_float(v0[q]) * f0)
+                   : __uint_as_float(v1[q]) * f1) * inv;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         st_global_v4(orow + (32 * cc + 8 * q) * 2, pack_bf16x2(o[8 * q], o[8 * q + 1]),
@@ -609,9 +616,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     mbar_init(bars + B_QEMPTY, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + B_KFULL + 8u * s, 1);
-      mbar_init(bars + B_KEMPTY + 8u * s, 1);
       mbar_init(bars + B_VFULL + 8u * s, 1);
-      mbar_init(bars + B_VEMPTY + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
       mbar_init(bars + B_SEMPTY + 8u * s, 4);
     }
