@@ -48,7 +48,7 @@ constexpr uint32_t AT_BARS = AT_P + 2 * 32768;
 constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of the softmax warp pairs
 constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_SFULL = 48, B_SEMPTY = 64, B_PFULL = 80,
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_SFULL = 48, B_PFULL = 80,
                    B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136, B_VFULL = 168;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
@@ -242,7 +242,7 @@ done:
 // and O for the item; they are merged when the item ends.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
   uint32_t q_ph = 0, kv_ph = 0, of_ph = 0, prev_ph = 0;
-  uint32_t se_ph = 0, pf_ph = 0;   // phase bits of the S-empty / P-full barriers, bit b for buffer b
+  uint32_t pf_ph = 0;   // phase bits of the P-full barriers, bit b for buffer b
   int stage = 0, prev_stage = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
@@ -252,8 +252,9 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       if (t < it.n) {
         const int sb = stage;
         if (!at_wait_bar(p, bars + B_KFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
-        if (!at_wait_bar(p, bars + B_SEMPTY + 8u * sb, ((se_ph >> sb) & 1u) ^ 1u, WHERE_MMA, i)) goto done;
-        se_ph ^= 1u << sb;
+        // S buffer sb was last read by the softmax of the running tile two back,
+        // whose P-full phase this thread already waited for (before that
+        // tile's product, issued earlier): no wait for the buffer here.
         tc_fence_after();
         const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
 #pragma unroll
@@ -478,7 +479,6 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bars + B_SEMPTY + 8u * grp);
         mbar_arrive(bars + B_PFULL + 8u * grp);
       }
       ++uses;
@@ -618,7 +618,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_KFULL + 8u * s, 1);
       mbar_init(bars + B_VFULL + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
-      mbar_init(bars + B_SEMPTY + 8u * s, 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars + B_PFULL + 8u * b, 4);
