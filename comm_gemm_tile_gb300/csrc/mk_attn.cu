@@ -49,7 +49,7 @@ constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of t
 constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
 // barriers (byte offsets in the barrier block)
 constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_SFULL = 48, B_PFULL = 80,
-                   B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136, B_VFULL = 168;
+                   B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136;
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
 // S = Q K^T: both operands K-major; O += P V: V MN-major
@@ -172,7 +172,10 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 // stalls the MMA issue briefly, so the MMA commits only these two per tile.
 template <bool IS_V>
 __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
-  const uint32_t FULL = IS_V ? B_VFULL : B_KFULL, EMPTY = IS_V ? B_PFREE : B_SFULL;
+  // V tiles land on the P-full barrier of their buffer (one arrival and the
+  // bytes, besides the four softmax warps' arrivals): the MMA's one wait
+  // there covers both operands of the product
+  const uint32_t FULL = IS_V ? B_PFULL : B_KFULL, EMPTY = IS_V ? B_PFREE : B_SFULL;
   int stage = 0;
   uint32_t ph = 0, q_ph = 0;
   uint32_t issued_mask = 0, issued_par = 0;
@@ -230,6 +233,13 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
     }
   }
 done:
+  if (IS_V && issued_mask && at_aborted(p)) {
+    // the P-full phases also wait for softmax arrivals that an abort may have
+    // cancelled: give the loads in flight time to land instead
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
+    issued_mask = 0;
+  }
   for (int s2 = 0; s2 < 2; ++s2)
     if (issued_mask & (1u << s2))
       at_wait_bar(p, bars + FULL + 8u * s2, (issued_par >> s2) & 1u, WHERE_DRAIN, s2, false);
@@ -241,7 +251,7 @@ done:
 // and of the odd ones (warps 6-9) each keep their own running maximum, sum
 // and O for the item; they are merged when the item ends.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0, prev_ph = 0;
+  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
   uint32_t pf_ph = 0;   // phase bits of the P-full barriers, bit b for buffer b
   int stage = 0, prev_stage = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
@@ -271,9 +281,9 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       if (t > 0) {
         // O[pb] += P_{t-1} V_{t-1}
         const int pb = prev_stage;
+        // P of tile t-1 written and its V tile landed (one barrier)
         if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, (pf_ph >> pb) & 1u, WHERE_MMA, i)) goto done;
         pf_ph ^= 1u << pb;
-        if (!at_wait_bar(p, bars + B_VFULL + 8u * prev_stage, prev_ph, WHERE_MMA, i)) goto done;
         if (t == 1) {   // the previous item's O buffers have been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
           of_ph ^= 1u;
@@ -294,7 +304,6 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       }
       if (t < it.n) {
         prev_stage = stage;
-        prev_ph = kv_ph;
         if (++stage == 2) {
           stage = 0;
           kv_ph ^= 1u;
@@ -616,11 +625,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     mbar_init(bars + B_QEMPTY, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + B_KFULL + 8u * s, 1);
-      mbar_init(bars + B_VFULL + 8u * s, 1);
       mbar_init(bars + B_SFULL + 8u * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + B_PFULL + 8u * b, 4);
+      mbar_init(bars + B_PFULL + 8u * b, 5);   // four softmax warps + the V load
       mbar_init(bars + B_PFREE + 8u * b, 1);
     }
     mbar_init(bars + B_OFREE, 8);
