@@ -335,11 +335,17 @@ struct ComputeSmem {
   __device__ __forceinline__ uint32_t pdone(int b) const { return bars + BAR_PDONE + 8u * b; }
 };
 
-// Ring geometry of the two compute variants.
+// Ring geometry of the two compute variants.  With pairs a stage holds two
+// consecutive k-blocks of a segment (each A + this CTA's half of B): the MMA
+// issuer then waits once and commits once per 8 MMAs -- a satisfied mbarrier
+// wait in the issuing thread costs on the order of a hundred cycles that the
+// tensor pipe's short queue cannot hide.
 template <bool PAIR>
 struct Ring {
-  static constexpr int stages = PAIR ? PSTAGES : STAGES;
-  static constexpr uint32_t stage_bytes = PAIR ? PSTAGE_BYTES : STAGE_BYTES;
+  static constexpr int kps = PAIR ? 2 : 1;                                   // k-blocks per stage
+  static constexpr uint32_t kb_bytes = PAIR ? PSTAGE_BYTES : STAGE_BYTES;    // one k-block's part
+  static constexpr int stages = (PAIR ? PSTAGES : STAGES) / kps;
+  static constexpr uint32_t stage_bytes = kb_bytes * kps;
 };
 
 __device__ __forceinline__ int n_items_for(const FusedParams& p) {
@@ -405,27 +411,32 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
           goto done;
         fence_proxy_async_global();
       }
-      for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
+      const int kend = it.kb0 + it.nkb;
+      for (int kb0 = it.kb0; kb0 < kend; kb0 += Ring<PAIR>::kps) {
         if (!wait_bar(p, S.empty(stage), phase ^ 1u, WHERE_PRODUCER, i)) goto done;
-        const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB;
-        const uint32_t b_dst = a_dst + A_STAGE_BYTES;
         const int n0 = it.nb * BN;
         if constexpr (PAIR) {
+          const int nk = min(Ring<PAIR>::kps, kend - kb0);   // k-blocks in this stage
           const uint32_t fb = mapa_shared(S.full(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(S.full(stage), 2u * PSTAGE_BYTES);
-          tma_load_2d_pair(a_dst, ma, fb, kb * BK, it.arow);
+          if (rank == 0) mbar_arrive_expect_tx(S.full(stage), 2u * PSTAGE_BYTES * static_cast<uint32_t>(nk));
           const int c0 = n0 / 64 + 2 * static_cast<int>(rank);   // this CTA's first column chunk
-          if (p.b_one_box) {
-            if (it.bz < 0) tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, c0);
-            else tma_load_4d_pair(b_dst, mbm, fb, 0, kb * BK, c0, it.bz);
-          } else if (it.bz < 0) {
+          for (int h = 0; h < nk; ++h) {
+            const int kb = kb0 + h;
+            const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * PSTAGE_BYTES;
+            const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+            tma_load_2d_pair(a_dst, ma, fb, kb * BK, it.arow);
+            if (p.b_one_box) {
+              if (it.bz < 0) tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, c0);
+              else tma_load_4d_pair(b_dst, mbm, fb, 0, kb * BK, c0, it.bz);
+            } else if (it.bz < 0) {
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK);
-          } else {
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tma_load_3d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK, it.bz);
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK, it.bz);
+            }
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -435,6 +446,9 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
           }
           continue;
         }
+        const int kb = kb0;
+        const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB;
+        const uint32_t b_dst = a_dst + A_STAGE_BYTES;
         mbar_arrive_expect_tx(S.full(stage), STAGE_BYTES);
         tma_load_2d(a_dst, ma, S.full(stage), kb * BK, it.arow);
         if (p.b_one_box) {
@@ -491,22 +505,26 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
       uint32_t acc = 0;
       for (int seg = 0; seg < it.nseg; ++seg) {
-        for (int kb = 0; kb < it.nkb; ++kb) {
+        for (int kb0 = 0; kb0 < it.nkb; kb0 += Ring<PAIR>::kps) {
+          const int nk = min(Ring<PAIR>::kps, it.nkb - kb0);   // k-blocks in this stage
           if (!wait_bar(p, S.full(stage), phase, WHERE_MMA, i)) goto done;
           tc_fence_after();
-          const uint32_t a_addr = S.ring + static_cast<uint32_t>(stage) * SB;
-          const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+          for (int h = 0; h < nk; ++h) {
+            const uint32_t a_addr =
+                S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * Ring<PAIR>::kb_bytes;
+            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
-            const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 8u * A_SWIZZLE_BYTES,
-                                          A_SWIZZLE_BYTES == 128 ? 2u : 4u);
-            // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
-            // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
-            const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
-            if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, acc);
-            else tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
-            acc = 1;
+            for (int k = 0; k < BK / 16; ++k) {
+              // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
+              const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 8u * A_SWIZZLE_BYTES,
+                                            A_SWIZZLE_BYTES == 128 ? 2u : 4u);
+              // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
+              // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
+              const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
+              if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, acc);
+              else tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
+              acc = 1;
+            }
           }
           if constexpr (PAIR) tc_commit_pair(S.empty(stage), 3);
           else tc_commit(S.empty(stage));
