@@ -250,66 +250,96 @@ done:
 // stage, S, P and O buffers n & 1: the softmax of the even ones (warps 2-5)
 // and of the odd ones (warps 6-9) each keep their own running maximum, sum
 // and O for the item; they are merged when the item ends.
+//
+// Issue order: when the softmax of running tile n-2 has published P (one
+// wait, which also covers V of that tile and frees S buffer n & 1), the
+// issuer starts S of tile n first and then the product of tile n-2, so the
+// softmax group's next S is not queued behind a product.  Per tile one
+// mbarrier wait besides the K tile and two commits: S full (which also frees
+// the K stage) and P free (which also frees the V stage and marks O
+// updated).  Every wait and commit in this thread stalls the tensor pipe's
+// short queue, so there are no others.
+__device__ __forceinline__ void at_pv(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, int pb,
+                                      int tile) {
+  const uint32_t vb = base + AT_KV + static_cast<uint32_t>(pb) * AT_KV_STAGE + 32768u;
+  const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(pb);
+  const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(pb) * AT_T;
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t ad = sdesc_swz(pbase + 16384u * a + 32u * k, 16u, 1024u, 2u);
+      const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
+      // the first product of each O buffer in an item (tiles 0 and 1) overwrites it
+      tc_mma_bf16(obuf, ad, bd, IDESC_PV, (tile >= 2 || a || k) ? 1u : 0u);
+    }
+  tc_commit(bars + B_PFREE + 8u * pb);   // P buffer and V stage free; O[pb] holds this product
+}
+
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
   uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
-  uint32_t pf_ph = 0;   // phase bits of the P-full barriers, bit b for buffer b
-  int stage = 0, prev_stage = 0;
+  uint32_t pf_ph = 0;        // phase bits of the P-full barriers, bit b for buffer b
+  int stage = 0;
+  // products not yet issued: the tile two back (pend2) and one back (pend1),
+  // as their tile index within their item (-1: none)
+  int pend2 = -1, pend1 = -1;
+  int item = -1;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
+    item = i;
     if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
     q_ph ^= 1u;
-    for (int t = 0; t <= it.n; ++t) {
-      if (t < it.n) {
-        const int sb = stage;
-        if (!at_wait_bar(p, bars + B_KFULL + 8u * stage, kv_ph, WHERE_MMA, i)) goto done;
-        // S buffer sb was last read by the softmax of the running tile two back,
-        // whose P-full phase this thread already waited for (before that
-        // tile's product, issued earlier): no wait for the buffer here.
-        tc_fence_after();
-        const uint32_t kb = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE;
+    for (int t = 0; t < it.n; ++t) {
+      const int b = stage;
+      if (pend2 >= 0) {
+        // P and V of the tile two back (same buffer): S buffer b is free too
+        if (!at_wait_bar(p, bars + B_PFULL + 8u * b, (pf_ph >> b) & 1u, WHERE_MMA, i)) goto done;
+        pf_ph ^= 1u << b;
+        if (pend2 == 0) {   // first product of an item: the previous item's O has been read out
+          if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
+          of_ph ^= 1u;
+        }
+      }
+      if (!at_wait_bar(p, bars + B_KFULL + 8u * b, kv_ph, WHERE_MMA, i)) goto done;
+      tc_fence_after();
+      {
+        const uint32_t kb = base + AT_KV + static_cast<uint32_t>(b) * AT_KV_STAGE;
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = sdesc_swz(base + AT_Q + 16384u * a + 32u * k, 16u, 1024u, 2u);
             const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
-            tc_mma_bf16(tmem + static_cast<uint32_t>(sb) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
+            tc_mma_bf16(tmem + static_cast<uint32_t>(b) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
           }
-        tc_commit(bars + B_SFULL + 8u * sb);              // S ready; this K stage may be refilled
+        tc_commit(bars + B_SFULL + 8u * b);              // S ready; this K stage may be refilled
         if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
       }
-      if (t > 0) {
-        // O[pb] += P_{t-1} V_{t-1}
-        const int pb = prev_stage;
-        // P of tile t-1 written and its V tile landed (one barrier)
-        if (!at_wait_bar(p, bars + B_PFULL + 8u * pb, (pf_ph >> pb) & 1u, WHERE_MMA, i)) goto done;
-        pf_ph ^= 1u << pb;
-        if (t == 1) {   // the previous item's O buffers have been read out
-          if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
-          of_ph ^= 1u;
-        }
-        tc_fence_after();
-        const uint32_t vb = base + AT_KV + static_cast<uint32_t>(prev_stage) * AT_KV_STAGE + 32768u;
-        const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(pb);
-        const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(pb) * AT_T;
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_swz(pbase + 16384u * a + 32u * k, 16u, 1024u, 2u);
-            const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
-            tc_mma_bf16(obuf, ad, bd, IDESC_PV, (t > 2 || a || k) ? 1u : 0u);
-          }
-        tc_commit(bars + B_PFREE + 8u * pb);   // P buffer and V stage free; O[pb] holds this product
-      }
-      if (t < it.n) {
-        prev_stage = stage;
-        if (++stage == 2) {
-          stage = 0;
-          kv_ph ^= 1u;
-        }
+      if (pend2 >= 0) at_pv(p, bars, base, tmem, b, pend2);
+      pend2 = pend1;
+      pend1 = t;
+      if (++stage == 2) {
+        stage = 0;
+        kv_ph ^= 1u;
       }
     }
+  }
+  // the last two products (tiles two back and one back of the running count)
+  for (int r = 0; r < 2; ++r) {
+    if (pend2 >= 0) {
+      const int b = stage;
+      if (!at_wait_bar(p, bars + B_PFULL + 8u * b, (pf_ph >> b) & 1u, WHERE_MMA, item)) goto done;
+      pf_ph ^= 1u << b;
+      if (pend2 == 0) {
+        if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, item)) goto done;
+        of_ph ^= 1u;
+      }
+      tc_fence_after();
+      at_pv(p, bars, base, tmem, b, pend2);
+    }
+    pend2 = pend1;
+    pend1 = -1;
+    if (++stage == 2) stage = 0;
   }
 done:
   tc_commit(bars + B_DRAIN);
