@@ -431,20 +431,27 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
       }
       sf_ph ^= 1u;
       tc_fence_after();
-      // pass 1: the row maximum (scale > 0 keeps the order: taken unscaled)
+      // pass 1: the row maximum (scale > 0 keeps the order: taken unscaled); the
+      // next 32 columns load while these are reduced
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(sbase + 32u * cc, v);
-        tc_wait_ld();
-        if (masked) {
+      {
+        uint32_t va[32], vb[32];
+        tc_ld_32x32b_x32(sbase, va);
+        tc_wait_ld_regs(va);
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(v[q]));
-        } else {
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+          uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+          if (cc < 3) tc_ld_32x32b_x32(sbase + 32u * (cc + 1), nxt);
+          if (masked) {
 #pragma unroll
-          for (int q = 0; q < 32; q += 2) mx = fmax3(mx, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
+            for (int q = 0; q < 32; ++q)
+              if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(cur[q]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) mx = fmax3(mx, __uint_as_float(cur[q]), __uint_as_float(cur[q + 1]));
+          }
+          if (cc < 3) tc_wait_ld_regs(nxt);
         }
       }
       const float m_new = fmaxf(m_run, mx * c);
