@@ -163,51 +163,48 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 
 // ------------------------------------------------------------------ roles
 // TMA producers: warp 0 loads the Q tile of each item and the K tiles, warp 12
-// the V tiles, each into its half of the two K/V stages with its own full
-// barrier.  Stage, S buffer, P buffer and O buffer of a tile are all the
-// parity of the CTA's running tile count, so the MMA's two completion
-// signals per tile also free the stages: a K stage once S of its previous
-// tile is done (S full), a V stage once that tile's product is done (P free)
-// -- a K stage is free again long before the V stage.  Each tcgen05.commit
-// stalls the MMA issue briefly, so the MMA commits only these two per tile.
+// the V tiles, each into its half of the two K/V stages.  Stage, S, P and O
+// buffer of a tile are all the parity of the CTA's running tile count n.
+// A K stage is free once S of tile n-2 is done (S full), a V stage once the
+// product of tile n-2 is done (P free).  Both land on the P-full barrier of
+// their buffer, V of tile n on the phase of tile n and K of tile n on the
+// phase of tile n-2 (six arrivals: the four softmax warps', the V load's and
+// the K load's, the loads with their bytes).  The MMA issuer's one wait per
+// tile there, before S of tile n and the product of tile n-2, then covers
+// K, P and V.  K of tiles 0 and 1, which have no tile two back, land on
+// their own barriers; after the last tile the K producer still arrives,
+// without bytes, on the two phases that no K tile follows.
 template <bool IS_V>
 __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
-  // V tiles land on the P-full barrier of their buffer (one arrival and the
-  // bytes, besides the four softmax warps' arrivals): the MMA's one wait
-  // there covers both operands of the product
-  const uint32_t FULL = IS_V ? B_PFULL : B_KFULL, EMPTY = IS_V ? B_PFREE : B_SFULL;
+  const uint32_t EMPTY = IS_V ? B_PFREE : B_SFULL;
   int stage = 0;
   uint32_t ph = 0, q_ph = 0;
-  uint32_t issued_mask = 0, issued_par = 0;
+  uint32_t count = 0;        // running tile count n of the next tile
   bool ready = false;
-  bool q_issued = false;
-  uint32_t q_par = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     if (!IS_V) {
-      if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+      if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) return;
       q_ph ^= 1u;
       const int qrow = it.h * p.s_r + it.qt * AT_T;
       mbar_arrive_expect_tx(bars + B_QFULL, 2u * 16384u);
       tma_load_2d(base + AT_Q, &p.tmQ[it.r], bars + B_QFULL, 0, qrow);
       tma_load_2d(base + AT_Q + 16384u, &p.tmQ[it.r], bars + B_QFULL, 64, qrow);
-      q_issued = true;
-      q_par ^= 1u;
     }
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
-      if (!at_wait_bar(p, bars + EMPTY + 8u * stage, ph ^ 1u, WHERE_PRODUCER, i)) goto done;
+      if (!at_wait_bar(p, bars + EMPTY + 8u * stage, ph ^ 1u, WHERE_PRODUCER, i)) return;
       const CUtensorMap* m = IS_V ? &p.tmV[s] : &p.tmK[s];
       int row = it.h * p.s_r + kt * AT_T;
       if (j > 0 && p.use_recv) {
         if (p.wait && j != waited_j) {
           if (!ready) {
-            if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, i)) goto done;
+            if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, i)) return;
             ready = true;
           }
-          if (!at_wait_value(p, at_counter(p, it.r, j, it.h), 2u * p.nkt, WHERE_PRODUCER, i)) goto done;
+          if (!at_wait_value(p, at_counter(p, it.r, j, it.h), 2u * p.nkt, WHERE_PRODUCER, i)) return;
           fence_proxy_async_global();
           waited_j = j;
         }
@@ -215,7 +212,7 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
         row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
       }
       const uint32_t dst = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE + (IS_V ? 32768u : 0u);
-      const uint32_t full = bars + FULL + 8u * stage;
+      const uint32_t full = bars + ((IS_V || count >= 2u) ? B_PFULL : B_KFULL) + 8u * stage;
       mbar_arrive_expect_tx(full, 32768u);
       if (IS_V) {
         tma_load_3d(dst, m, full, 0, row, 0);
@@ -224,26 +221,27 @@ __device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
         tma_load_2d(dst, m, full, 0, row);
         tma_load_2d(dst + 16384u, m, full, 64, row);
       }
-      issued_mask |= 1u << stage;
-      issued_par = (issued_par & ~(1u << stage)) | (ph << stage);
+      ++count;
       if (++stage == 2) {
         stage = 0;
         ph ^= 1u;
       }
     }
   }
-done:
-  if (IS_V && issued_mask && at_aborted(p)) {
-    // the P-full phases also wait for softmax arrivals that an abort may have
-    // cancelled: give the loads in flight time to land instead
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
-    issued_mask = 0;
+  if (!IS_V) {
+    // the phases of the last two tiles count a K arrival too: made once S of
+    // those tiles is done, as a K load for the tiles after them would be
+    for (uint32_t n = count; n < count + 2u; ++n) {
+      if (n >= 2u) {
+        if (!at_wait_bar(p, bars + B_SFULL + 8u * stage, ph ^ 1u, WHERE_PRODUCER, 0)) return;
+        mbar_arrive(bars + B_PFULL + 8u * stage);
+      }
+      if (++stage == 2) {
+        stage = 0;
+        ph ^= 1u;
+      }
+    }
   }
-  for (int s2 = 0; s2 < 2; ++s2)
-    if (issued_mask & (1u << s2))
-      at_wait_bar(p, bars + FULL + 8u * s2, (issued_par >> s2) & 1u, WHERE_DRAIN, s2, false);
-  if (q_issued) at_wait_bar(p, bars + B_QFULL, q_par ^ 1u, WHERE_DRAIN, 0, false);
 }
 
 // MMA issuer.  The CTA's n-th tile (counted over all its items) uses K/V
@@ -277,7 +275,7 @@ __device__ __forceinline__ void at_pv(const AttnParams& p, uint32_t bars, uint32
 }
 
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, kv_ph = 0, of_ph = 0;
+  uint32_t q_ph = 0, of_ph = 0;
   uint32_t pf_ph = 0;        // phase bits of the P-full barriers, bit b for buffer b
   int stage = 0;
   // products not yet issued: the tile two back (pend2) and one back (pend1),
@@ -292,15 +290,18 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     for (int t = 0; t < it.n; ++t) {
       const int b = stage;
       if (pend2 >= 0) {
-        // P and V of the tile two back (same buffer): S buffer b is free too
+        // P and V of the tile two back (same buffer; S buffer b is free too)
+        // and K of this tile
         if (!at_wait_bar(p, bars + B_PFULL + 8u * b, (pf_ph >> b) & 1u, WHERE_MMA, i)) goto done;
         pf_ph ^= 1u << b;
         if (pend2 == 0) {   // first product of an item: the previous item's O has been read out
           if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
           of_ph ^= 1u;
         }
+      } else {
+        // the CTA's first two tiles: K on its own barrier
+        if (!at_wait_bar(p, bars + B_KFULL + 8u * b, 0u, WHERE_MMA, i)) goto done;
       }
-      if (!at_wait_bar(p, bars + B_KFULL + 8u * b, kv_ph, WHERE_MMA, i)) goto done;
       tc_fence_after();
       {
         const uint32_t kb = base + AT_KV + static_cast<uint32_t>(b) * AT_KV_STAGE;
@@ -318,10 +319,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       if (pend2 >= 0) at_pv(p, bars, base, tmem, b, pend2);
       pend2 = pend1;
       pend1 = t;
-      if (++stage == 2) {
-        stage = 0;
-        kv_ph ^= 1u;
-      }
+      if (++stage == 2) stage = 0;
     }
   }
   // the last two products (tiles two back and one back of the running count)
@@ -665,7 +663,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_SFULL + 8u * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + B_PFULL + 8u * b, 5);   // four softmax warps + the V load
+      mbar_init(bars + B_PFULL + 8u * b, 6);   // four softmax warps, the V load, the K load
       mbar_init(bars + B_PFREE + 8u * b, 1);
     }
     mbar_init(bars + B_OFREE, 8);
@@ -698,6 +696,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     __syncwarp();
   }
   tc_fence_before();
+  // after an abort, TMA loads whose barrier phases will never complete may
+  // still be in flight: give them time to land before the CTA exits
+  if (threadIdx.x == 0 && at_aborted(p)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
