@@ -489,7 +489,10 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         res = {}
         for name, cfg in (("fused", mk.Config(cta_pair=pair)),
                           ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY, cta_pair=pair)),
-                          ("unfused", mk.Config(mode=mk.MODE_UNFUSED, cta_pair=pair))):
+                          ("unfused", mk.Config(mode=mk.MODE_UNFUSED, cta_pair=pair)),
+                          # the reduction variants: bf16 running sum, atomic fp32 tiles
+                          ("wire_bf16", mk.Config(wire=mk.WIRE_BF16, cta_pair=pair)),
+                          ("atomic", mk.Config(reduce=mk.REDUCE_ATOMIC, cta_pair=pair))):
             def step(i, cfg=cfg):
                 a, b, o = sets[i % nsets]
                 fn(a, b, cfg=cfg, workspace=ws, stream=stream, **{key: o})
@@ -501,6 +504,7 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         entry = {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"],
                  "unfused_ms": res["unfused"], "exposed_ms": res["fused"] - res["gemm_only"],
                  "fused_tflops": fused_tf, "pct_of_peak": 100 * fused_tf / bf16_peak,
+                 "wire_bf16_ms": res["wire_bf16"], "atomic_ms": res["atomic"],
                  "status": mk.status_string(st)}
         if w.op == "ar":
             hbm_bytes = w.R * (w.k * w.n * 2 + w.m * w.k * 2) + w.R * w.m * w.n * 2

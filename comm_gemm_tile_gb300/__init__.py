@@ -23,7 +23,8 @@ MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_CUDA, MK_ERR_TIMEOUT, MK_ERR_C
 MK_BF16, MK_F32 = 0, 1
 OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR, OP_MOE = 0, 1, 2, 3
 MODE_FUSED, MODE_GEMM_ONLY, MODE_UNFUSED = 0, 1, 2
-REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL = 0, 1, 2
+REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL, REDUCE_ATOMIC = 0, 1, 2, 3
+WIRE_F32, WIRE_BF16 = 0, 1
 PAIR_AUTO, PAIR_OFF, PAIR_ON = 0, 1, 2
 MAX_RANKS = 16
 
@@ -38,7 +39,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("n_copy_ctas", ctypes.c_int), ("n_reduce_ctas", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("mode", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
-                ("inject", ctypes.c_int), ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int)]
+                ("inject", ctypes.c_int), ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("wire", ctypes.c_int)]
 
 
 @dataclasses.dataclass
@@ -54,11 +56,12 @@ class Config:
     inject: int = 0
     reduce: int = 0
     cta_pair: int = 0
+    wire: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.n_copy_ctas, self.n_reduce_ctas, self.max_ctas, self.group_m,
                     self.split_k, self.mode, self.wait_limit_ns, self.inject, self.reduce,
-                    self.cta_pair)
+                    self.cta_pair, self.wire)
 
 
 _lib = None

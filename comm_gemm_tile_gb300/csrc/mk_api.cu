@@ -140,9 +140,10 @@ struct Plan {
   int n_mblk, n_nblk, n_kblk, n_tiles;
   int split_k, kps, P;
   int group_m;
-  int chain, last;
+  int chain, last, atomic, wire;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
 };
+constexpr int ZFLAG_WORDS = 1024;   // atomic reduction: one zero-done word per CTA
 
 static bool plan_gemm(int op, int R, long long m, long long n, long long k, const mk_config* cfg,
                       Plan& pl) {
@@ -173,6 +174,11 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   pl.staging_bytes = 0;
   pl.chain = 0;
   pl.last = 0;
+  pl.atomic = 0;
+  pl.wire = 0;
+  const int want_reduce = cfg ? cfg->reduce : 0;
+  const int want_wire = cfg ? cfg->wire : 0;
+  if (want_reduce < 0 || want_reduce > 3 || want_wire < 0 || want_wire > 1) return false;
   if (op == OP_AG) {
     pl.n_flags = static_cast<size_t>(pl.n_mblk) * COPY_SUB_MAX;
   } else {
@@ -183,10 +189,16 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
     // Without reduce-role CTAs the fused path reduces in the epilogues, either
     // as a running sum (the default: measured fastest for both RS and AR) or by
     // last arrival (the warp that completes a tile quarter sums all partials).
+    // Two variants of the in-epilogue reduction trade the fixed rank order for
+    // less partial traffic: the running sum forwarded in bf16 (wire = 1), and
+    // red.global.add of every partial into one fp32 tile per output tile
+    // (reduce = 3), converted by the warp that completes it.
     const bool in_epilogue = (mode == MK_MODE_FUSED && !(cfg && cfg->n_reduce_ctas > 0));
-    const int want = cfg ? cfg->reduce : 0;
-    pl.chain = (in_epilogue && want != 2) ? 1 : 0;
-    pl.last = (in_epilogue && !pl.chain) ? 1 : 0;
+    const int want = want_reduce;
+    pl.chain = (in_epilogue && want != 2 && want != 3) ? 1 : 0;
+    pl.last = (in_epilogue && want == 2) ? 1 : 0;
+    pl.atomic = (in_epilogue && want == 3) ? 1 : 0;
+    pl.wire = (pl.chain && want_wire == 1) ? 1 : 0;
     const int max_parts = in_epilogue ? MAX_CHAIN_PARTIALS : MAX_PARTIALS;
     int sk = (cfg && cfg->split_k > 0) ? cfg->split_k : 0;
     if (sk == 0) {
@@ -205,10 +217,13 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
     pl.P = R * sk;
     if (pl.P > max_parts) return false;
     if (mode != MK_MODE_GEMM_ONLY) {
-      // flags: one per (tile, partial); last arrival: four 64-bit counters per tile
-      pl.n_flags = pl.last ? static_cast<size_t>(pl.n_tiles) * 8 : static_cast<size_t>(pl.n_tiles) * pl.P;
-      const size_t slots = pl.chain ? static_cast<size_t>(pl.n_tiles)
-                                    : static_cast<size_t>(pl.n_tiles) * pl.P;
+      // flags: one per (tile, partial); last arrival: four 64-bit counters per tile;
+      // atomic: four counters per tile, then one zero-done word per CTA
+      pl.n_flags = pl.last     ? static_cast<size_t>(pl.n_tiles) * 8
+                   : pl.atomic ? static_cast<size_t>(pl.n_tiles) * 4 + ZFLAG_WORDS
+                               : static_cast<size_t>(pl.n_tiles) * pl.P;
+      const size_t slots = (pl.chain || pl.atomic) ? static_cast<size_t>(pl.n_tiles)
+                                                   : static_cast<size_t>(pl.n_tiles) * pl.P;
       pl.staging_bytes = slots * TILE_F32 * sizeof(float);
     }
   }
@@ -241,12 +256,15 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.P = pl.P;
   p.chain = pl.chain;
   p.last_arrival = pl.last;
+  p.atomic = pl.atomic;
+  p.wire_bf16 = pl.wire;
   p.copy_sub = 1;
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
   p.flags = reinterpret_cast<uint32_t*>(ws + pl.flags_off);
   p.chunk_cnt = p.flags;
   p.staging = reinterpret_cast<float*>(ws + pl.staging_off);
+  p.zflags = pl.atomic ? p.flags + static_cast<size_t>(pl.n_tiles) * 4 : nullptr;
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();
@@ -298,6 +316,7 @@ static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t
       p.n_copy = 0;
       p.n_compute = n_pairs;
       p.n_reduce = 0;
+      if (p.atomic && 2 * n_pairs > ZFLAG_WORDS) return MK_ERR_UNSUPPORTED;
       return launch_fused(p, 2 * n_pairs, s) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
     }
   }
@@ -307,6 +326,7 @@ static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t
   set_items(p, per, mlp_phases);
   const int n = std::min(sms, p.n_items);
   if (n <= 0) return MK_OK;
+  if (p.atomic && n > ZFLAG_WORDS) return MK_ERR_UNSUPPORTED;
   p.group_tiles = std::max(1, std::min(n, p.n_sched));
   p.n_copy = 0;
   p.n_compute = n;
@@ -500,7 +520,7 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   if (op == OP_AR) p.rows_per_owner = static_cast<int>(m);
   p.b_one_box = (n % 64 == 0) ? 1 : 0;
   // CTA pairs for every compute-only launch (not with reduce-role CTAs).
-  const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last);
+  const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last || pl.atomic);
   for (int r = 0; r < R; ++r) {
     p.out[r] = outs[r];
     if (!make_map_a(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2) ||
@@ -517,7 +537,7 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
     p.n_items = pl.n_tiles * pl.P;
     return launch(p, 0, 0, std::min(sms, pl.n_tiles), s);
   }
-  if (pl.chain || pl.last) return launch_compute(p, pair, sms, s);
+  if (pl.chain || pl.last || pl.atomic) return launch_compute(p, pair, sms, s);
   p.n_items = pl.n_tiles * pl.P;
   int n_red = cfg->n_reduce_ctas;
   n_red = std::min(n_red, pl.n_tiles);
@@ -554,7 +574,7 @@ struct MlpLayout {
 bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* cfg, MlpLayout& L) {
   if (R < 1 || R > MK_MLP_MAX_RANKS || m < 0 || h < 0 || f_r < 0) return false;
   if ((h % 8) || (f_r % 8)) return false;
-  if (cfg && (cfg->reduce == 2 || cfg->n_reduce_ctas > 0 || cfg->split_k > 1)) return false;
+  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->n_reduce_ctas > 0 || cfg->split_k > 1)) return false;
   if (!plan_gemm(OP_RS, R, static_cast<long long>(R) * m, h, f_r, cfg, L.pl)) return false;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   size_t off = WS_HDR_BYTES;

@@ -579,12 +579,12 @@ __device__ __forceinline__ uint32_t bump_quarter(const FusedParams& p, int tile,
   return atomicAdd(p.flags + static_cast<size_t>(tile) * 4 + quarter, 1u);
 }
 
-// Rows of one warp quarter of `tile`: sum of its P staged partials in order
-// 0..P-1, rounded and written to the owner block (RS) or every replica (AR).
-__device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, int trow, bool row_ok,
-                               int grow) {
+// Rows of one warp quarter of a tile: sum of `nparts` staged fp32 tiles
+// starting at `base`, in order, rounded and written to the owner block (RS)
+// or every replica (AR).  nparts = 1 converts an accumulated tile.
+__device__ void reduce_quarter(const FusedParams& p, const Item& it, const float* base, int nparts, int trow,
+                               bool row_ok, int grow) {
   const size_t esz = p.out_f32 ? 4 : 2;
-  const float* base = p.staging + static_cast<size_t>(tile) * p.P * TILE_F32;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float4 acc[8];
@@ -592,7 +592,7 @@ __device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, i
     for (int q = 0; q < 8; ++q)
       acc[q] = ld_global_cg_f4(base + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4);
     int part = 1;
-    for (; part + 1 < p.P; part += 2) {
+    for (; part + 1 < nparts; part += 2) {
       float4 v0[8], v1[8];
       const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
       const float* s1 = s0 + TILE_F32;
@@ -607,7 +607,7 @@ __device__ void reduce_quarter(const FusedParams& p, const Item& it, int tile, i
         acc[q].x += v1[q].x; acc[q].y += v1[q].y; acc[q].z += v1[q].z; acc[q].w += v1[q].w;
       }
     }
-    if (part < p.P) {
+    if (part < nparts) {
       const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -895,6 +895,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   uint32_t acc_phase = 0;
   uint32_t pd_par = 0;           // phase bit of pdone(b) in bit b
   bool counters_ready = false;   // last-arrival counters published for this call
+  bool zero_ready = false;       // atomic: every CTA's share of the fp32 tiles is zero
   const int n_items = n_items_for(p);
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
@@ -922,11 +923,45 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         if (!ok) return;
       }
       const bool last = (part == p.P - 1);
+      // bf16 wire: the forwarded sum is a bf16 tile, uint4 (8 columns) at index
+      // (32-column chunk * 4 + group) * BM + row
+      uint8_t* accb = reinterpret_cast<uint8_t*>(p.staging) + static_cast<size_t>(tile) * TILE_F32 * 2;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tc_ld_32x32b_x32(taddr + 32u * c, r);
-        if (part > 0) {
+        if (p.wire_bf16) {
+          if (part > 0) {
+            uint4 v[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              v[g] = ld_global_cg_u4(accb + (static_cast<size_t>((c * 4 + g) * BM + trow)) * 16);
+            tc_wait_ld();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                r[8 * g + 2 * e] = __float_as_uint(__uint_as_float(w[e] << 16) + __uint_as_float(r[8 * g + 2 * e]));
+                r[8 * g + 2 * e + 1] =
+                    __float_as_uint(__uint_as_float(w[e] & 0xffff0000u) + __uint_as_float(r[8 * g + 2 * e + 1]));
+              }
+            }
+          } else {
+            tc_wait_ld();
+          }
+          if (!last) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint8_t* d = accb + (static_cast<size_t>((c * 4 + g) * BM + trow)) * 16;
+              st_global_v4(d, pack_bf16x2(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
+            }
+            continue;
+          }
+        } else if (part > 0) {
           float4 v[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -942,7 +977,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         } else {
           tc_wait_ld();
         }
-        if (!last) {
+        if (!last && !p.wire_bf16) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             float* d = acc + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4;
@@ -966,6 +1001,55 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
           }
         }
       }
+    } else if (it.slot >= 0 && p.atomic) {
+      // Add this partial into the tile's fp32 accumulator (zeroed by every CTA at
+      // kernel start: wait once for all of them), then the warp whose count
+      // completes its 32-row quarter (the P-th) converts and stores it.
+      const int tile = it.slot / p.P;
+      float* acc = p.staging + static_cast<size_t>(tile) * TILE_F32;
+      if (!zero_ready) {
+        int ok = 1;
+        if (lane == 0)
+          for (unsigned c = 0; c < gridDim.x && ok; ++c) ok = wait_flag(p, p.zflags + c, WHERE_EPILOGUE, i) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        zero_ready = true;
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          red_add_v4_f32(acc + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4, r[4 * q], r[4 * q + 1],
+                         r[4 * q + 2], r[4 * q + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release_tmem<PAIR>(S, buf, rank);   // tensor memory is free again
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        if (!counters_ready) {
+          if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_EPILOGUE, i)) last = -1;
+          counters_ready = true;
+        }
+        const bool skip = (p.inject == 2 && it.slot == 0);
+        if (last == 0 && !skip)
+          last = (bump_quarter(p, tile, quarter) == static_cast<uint32_t>(p.P - 1)) ? 1 : 0;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last < 0) return;
+      if (last) {
+        __threadfence();   // the other partials' additions happened before their counts
+        reduce_quarter(p, it, acc, 1, trow, row_ok, grow);
+      }
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1u;
+      }
+      continue;
     } else if (it.slot >= 0 && p.last_arrival) {
       // Stage this partial, then the warp whose store completes its 32-row
       // quarter of the tile (the P-th arrival) sums all P partials in order.
@@ -1001,7 +1085,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       if (last < 0) return;
       if (last) {
         __threadfence();   // the other partials' stores happened before their counts
-        reduce_quarter(p, it, tile, trow, row_ok, grow);
+        reduce_quarter(p, it, p.staging + static_cast<size_t>(tile) * p.P * TILE_F32, p.P, trow, row_ok, grow);
       }
       if (++buf == 2) {
         buf = 0;
@@ -1267,6 +1351,23 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
 }
 
 // Compute CTA (cid = compute index; with pairs, the pair index).
+// Atomic reduction: the spare warps of every CTA zero its share of the fp32
+// accumulator tiles, then publish zflags[CTA] = epoch (all shares are waited
+// for before the first addition into any tile).
+__device__ void zero_role(const FusedParams& p) {
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - 6;
+  const size_t total4 = static_cast<size_t>(p.n_tiles) * TILE_F32 / 4;
+  const size_t per = (total4 + gridDim.x - 1) / gridDim.x;
+  const size_t lo = static_cast<size_t>(blockIdx.x) * per;
+  const size_t hi = min(total4, lo + per);
+  float* base = p.staging;
+  for (size_t x = lo + static_cast<size_t>(w) * 32 + lane; x < hi; x += static_cast<size_t>(N_COPY_WARPS) * 32)
+    st_global_v4(base + x * 4, 0u, 0u, 0u, 0u);
+  __threadfence();
+  asm volatile("barrier.sync 2, %0;" ::"n"(N_COPY_WARPS * 32) : "memory");   // the spare warps only
+  if (w == 0 && lane == 0) st_release_gpu(p.zflags + blockIdx.x, p.epoch);
+}
+
 template <bool PAIR>
 __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1342,6 +1443,8 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     if constexpr (PAIR) copy_warps_role(p, 2 * cid + static_cast<int>(rank), 2 * p.n_compute);
     else copy_warps_role(p, cid, p.n_compute);
     __syncwarp();
+  } else if (p.atomic) {
+    zero_role(p);
   }
   tc_fence_before();
   if constexpr (PAIR) {
@@ -1724,7 +1827,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
   }
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
-  if (t == 0 && ((p.op == OP_AG && p.copy_warps) || p.last_arrival || p.op == OP_MLP)) {
+  if (t == 0 && ((p.op == OP_AG && p.copy_warps) || p.last_arrival || p.atomic || p.op == OP_MLP)) {
     // Zero this call's counters (the workspace may hold anything from earlier
     // calls of any op), then publish them.
     if (p.op == OP_AG) {

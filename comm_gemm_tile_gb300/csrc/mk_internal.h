@@ -94,6 +94,10 @@ struct FusedParams {
                        //        forwarded tile by tile); 0 = staged partials + reduce-role CTAs
   int last_arrival;    // RS/AR: 1 = staged partials, the epilogue warp that completes a tile
                        //        quarter (32 rows) sums its partials (with chain = 0)
+  int atomic;          // RS/AR: 1 = every partial added into one fp32 tile per output tile with
+                       //        red.global.add; the warp that completes a quarter converts it
+  int wire_bf16;       // RS/AR running sum: 1 = the sum forwarded between parts is bf16
+  uint32_t* zflags;    // atomic: one word per CTA, = epoch once its slice of the fp32 tiles is zero
   int group_tiles;     // RS/AR chain: tiles per scheduling group
   int copy_warps;      // AG: 1 = copy-in done by the copy warps of every compute CTA, one
                        //     piece counter per chunk (zeroed at kernel start by the CTA

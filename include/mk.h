@@ -95,7 +95,13 @@ typedef struct {
   int reduce;               /* RS / AR with n_reduce_ctas == 0: 0 = default (running sum),
                                1 = running sum forwarded in rank order by the epilogues,
                                2 = last arrival: every partial staged, the epilogue that
-                                   completes a tile sums all of them in rank order      */
+                                   completes a tile sums all of them in rank order,
+                               3 = atomic: every partial added into one fp32 tile per
+                                   output tile (red.global.add), the epilogue that
+                                   completes a tile converts it.  The fp32 summation
+                                   order is not fixed: results agree with the other
+                                   modes within rounding (exactly when every partial
+                                   sum is exact in fp32).                              */
   int cta_pair;             /* GEMM tiles: 0 = default, 1 = one CTA per 128 x 256 tile,
                                2 = CTA pairs (clusters of two SMs sharing a 256 x 256 tile
                                    through tcgen05 cta_group::2).  Pairs serve every launch
@@ -103,6 +109,11 @@ typedef struct {
                                    tiles of each expert's rows); elsewhere, or where the
                                    device cannot co-schedule pairs, single CTAs run.
                                    Results are identical.                               */
+  int wire;                 /* RS / AR running sum (reduce 0 or 1): 0 = the sum forwarded
+                               from part to part is fp32; 1 = it is rounded to bf16
+                               (round-to-nearest-even) at every forward, halving the
+                               partial traffic.  Ignored by the other reductions.
+                               The chained MLP takes neither reduce = 2, 3 nor wire.    */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).

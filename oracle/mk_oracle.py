@@ -23,7 +23,9 @@ The ops (mKernel write-up, news.chathome.org, "五种融合内核" table):
 * GEMM + ReduceScatter (row "GEMM + ReduceScatter"): S = sum_r A_r @ B_r;
   row block o of S (rows [o*m/R, (o+1)*m/R)) belongs to rank o.
 * GEMM + AllReduce (row "GEMM + AllReduce"): S as above, and every rank ends
-  with all of S.
+  with all of S.  One reduction variant has a result of its own:
+  ``running_sum_bf16_wire`` (the running sum forwarded in bf16); the atomic
+  variant's result is S itself, up to fp32 rounding in an unfixed order.
 * MoE Dispatch + GEMM (row "MoE Dispatch + GEMM"): route each token to its
   top-k experts, move each (token, expert) row to the rank that holds the
   expert, then multiply the rows of each expert by that expert's weight.
@@ -171,6 +173,40 @@ def gemm_ar(a_list, b_list, out: str = "bf16"):
     """GEMM + AllReduce: returns R replicas, each equal to all of S."""
     c = round_out(sum_over_ranks(a_list, b_list), out)
     return [c.copy() for _ in range(len(a_list))]
+
+
+def rank_partials(a_list, b_list) -> list:
+    """The terms of S: P_r = A_r @ B_r in float64, one per rank, in rank order
+    (table row "GEMM + ReduceScatter": each rank's partial product)."""
+    assert len(a_list) == len(b_list) and len(a_list) >= 1
+    return [bf16_to_f64(np.asarray(a)) @ bf16_to_f64(np.asarray(b)) for a, b in zip(a_list, b_list)]
+
+
+def f64_to_f32(x) -> np.ndarray:
+    """Round float64 to the nearest fp32 (ties to even) and widen back, exactly."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def running_sum_bf16_wire(partials, out: str = "bf16") -> np.ndarray:
+    """S = sum of the partials, reduced as a running sum forwarded from part to
+    part with bf16 on the wire (the reduction variant that halves the partial
+    traffic of "GEMM + ReduceScatter" / "GEMM + AllReduce").
+
+    The pages fix no dtype for the partials in flight; the reading used for this
+    variant: every part holds its own partial in fp32, adds the bf16 sum it
+    received in one fp32 addition, and forwards that sum rounded to bf16
+    (nearest, ties to even); the last part rounds once to the output dtype:
+
+        s_0 = bf16(f32(P_0)),  s_j = bf16(f32(s_{j-1} + f32(P_j))) for 0 < j < P-1,
+        result = round_out(f32(s_{P-2} + f32(P_{P-1})))      (P = 1: round_out(P_0)).
+    """
+    parts = [np.asarray(x, dtype=np.float64) for x in partials]
+    if len(parts) == 1:
+        return round_out(parts[0], out)
+    s = bf16_to_f64(f64_to_bf16_bits(f64_to_f32(parts[0])))
+    for x in parts[1:-1]:
+        s = bf16_to_f64(f64_to_bf16_bits(f64_to_f32(s + f64_to_f32(x))))
+    return round_out(f64_to_f32(s + f64_to_f32(parts[-1])), out)
 
 
 # ----------------------------------------------------------------------------

@@ -47,6 +47,14 @@ def test_workspace_sizes(L):
     assert 2048 * 8 * 128 * 256 * 4 <= sz < 2048 * 8 * 128 * 256 * 4 + (1 << 20)
     sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(mode=mk.MODE_UNFUSED))
     assert 2048 * 8 * 128 * 256 * 4 <= sz
+    # atomic reduction: one fp32 tile per output tile, like the running sum
+    sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=mk.REDUCE_ATOMIC))
+    assert 2048 * 128 * 256 * 4 <= sz < 2048 * 128 * 256 * 4 + (1 << 20)
+    # bf16 wire: the same staging (half of each tile used)
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(wire=mk.WIRE_BF16)) > 0
+    # out-of-range reduce / wire -> 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=4)) == 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(wire=2)) == 0
     # GEMM-only mode needs no staging.
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584,
                              mk.Config(mode=mk.MODE_GEMM_ONLY)) < (1 << 20)
@@ -137,7 +145,16 @@ def test_argument_validation_without_launch(L):
     assert L.mk_get_device_status(None, None, None) == mk.MK_ERR_INVALID
 
 
+def test_mlp_rejects_the_reduction_variants(L):
+    # the chained MLP reduces by the fp32 running sum only
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584) > 0
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(reduce=mk.REDUCE_ATOMIC)) == 0
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(wire=mk.WIRE_BF16)) == 0
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(reduce=mk.REDUCE_LAST_ARRIVAL)) == 0
+
+
 def test_config_struct_layout():
     assert ctypes.sizeof(mk._Cfg) == 48
     assert mk._Cfg.wait_limit_ns.offset == 24 and mk._Cfg.inject.offset == 32
     assert mk._Cfg.reduce.offset == 36 and mk._Cfg.cta_pair.offset == 40
+    assert mk._Cfg.wire.offset == 44

@@ -244,6 +244,63 @@ def test_integer_config_sums_are_exact_in_fp32():
 
 # ---------------------------------------------------------------- MoE
 
+# ---- the bf16-wire running sum (a reduction variant of GEMM + ReduceScatter / AllReduce)
+
+
+def test_wire_single_partial_is_plain_rounding():
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(4, 9)) * 100
+    for out in ("bf16", "f32"):
+        np.testing.assert_array_equal(O.running_sum_bf16_wire([x], out), O.round_out(x, out))
+
+
+def test_wire_hand_worked_example():
+    # partials 256, 1, 1 (exact sum 258): s0 = bf16(256) = 256; 256 + 1 = 257 lies halfway
+    # between the bf16 neighbours 256 and 258 and rounds to the even mantissa, 256; the last
+    # part adds 1 in fp32: 257 (fp32 out), which rounds to 256 in bf16 (halfway again).
+    parts = [np.array([[256.0]]), np.array([[1.0]]), np.array([[1.0]])]
+    assert float(O.running_sum_bf16_wire(parts, "f32")[0, 0]) == 257.0
+    assert O.bf16_to_f64(O.running_sum_bf16_wire(parts, "bf16"))[0, 0] == 256.0
+    # with two parts nothing is rounded before the last addition: 256 + 1 + 1 ... = plain sum
+    assert float(O.running_sum_bf16_wire([np.array([[256.0]]), np.array([[2.0]])], "f32")[0, 0]) == 258.0
+    # the order matters once rounding happens: 1, 1, 256 keeps every bit
+    assert float(O.running_sum_bf16_wire(parts[::-1], "f32")[0, 0]) == 258.0
+
+
+def test_wire_equals_plain_sum_when_every_forward_is_exact():
+    # integers whose running sums stay within bf16's exact range (|s| <= 256)
+    rng = np.random.default_rng(6)
+    parts = [rng.integers(-30, 31, size=(8, 16)).astype(np.float64) for _ in range(8)]
+    exact = sum(parts)
+    for out in ("bf16", "f32"):
+        np.testing.assert_array_equal(O.running_sum_bf16_wire(parts, out), O.round_out(exact, out))
+
+
+def test_wire_error_within_its_roundings():
+    # each forward rounds to bf16 (at most half a bf16 unit, 2^-9 relative) and the last
+    # addition to fp32; the result stays within the sum of those half-units of the exact sum
+    rng = np.random.default_rng(7)
+    parts = [rng.normal(size=(32, 32)) * 50 for _ in range(6)]
+    got = O.running_sum_bf16_wire(parts, "f32").astype(np.float64)
+    bound = np.zeros_like(got)
+    s = np.zeros_like(got)
+    for x in parts[:-1]:
+        s = s + x
+        bound += np.abs(s) * 2.0 ** -8 + 1e-12
+    exact = sum(parts)
+    bound += np.abs(exact) * 2.0 ** -23 + 1e-12
+    assert np.all(np.abs(got - exact) <= bound)
+    # and it is not the plain rounding in general (the wire does round)
+    assert not np.array_equal(got, O.round_out(exact, "f32"))
+
+
+def test_rank_partials_sum_to_s():
+    rng = np.random.default_rng(8)
+    a = [I.bits(torch.from_numpy(rng.normal(size=(6, 10)).astype(np.float32)).bfloat16()) for _ in range(3)]
+    b = [I.bits(torch.from_numpy(rng.normal(size=(10, 5)).astype(np.float32)).bfloat16()) for _ in range(3)]
+    np.testing.assert_allclose(sum(O.rank_partials(a, b)), O.sum_over_ranks(a, b), rtol=0, atol=1e-12)
+
+
 def test_route_matches_stable_argsort():
     g = np.random.default_rng(11)
     lg = np.round(g.standard_normal((500, 16)) * 2) / 2      # many ties
