@@ -25,6 +25,17 @@ OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR, OP_MOE = 0, 1, 2, 3
 MODE_FUSED, MODE_GEMM_ONLY, MODE_UNFUSED = 0, 1, 2
 REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL, REDUCE_ATOMIC = 0, 1, 2, 3
 WIRE_F32, WIRE_BF16 = 0, 1
+OPERAND_BF16, OPERAND_FP8 = 0, 1
+FP8 = torch.float8_e4m3fn
+
+
+def _with_operand(cfg, t):
+    """The config for operands of t's dtype: fp8 e4m3 tensors set operand = 1."""
+    if t.dtype != FP8:
+        return cfg
+    c = dataclasses.replace(cfg) if cfg is not None else Config()
+    c.operand = OPERAND_FP8
+    return c
 PAIR_AUTO, PAIR_OFF, PAIR_ON = 0, 1, 2
 MAX_RANKS = 16
 
@@ -40,7 +51,7 @@ class _Cfg(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("mode", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
                 ("inject", ctypes.c_int), ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("wire", ctypes.c_int)]
+                ("wire", ctypes.c_int), ("operand", ctypes.c_int)]
 
 
 @dataclasses.dataclass
@@ -57,11 +68,12 @@ class Config:
     reduce: int = 0
     cta_pair: int = 0
     wire: int = 0
+    operand: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.n_copy_ctas, self.n_reduce_ctas, self.max_ctas, self.group_m,
                     self.split_k, self.mode, self.wait_limit_ns, self.inject, self.reduce,
-                    self.cta_pair, self.wire)
+                    self.cta_pair, self.wire, self.operand)
 
 
 _lib = None
@@ -201,13 +213,15 @@ def device_status(workspace: Workspace | None = None, stream=None, device=None):
 
 def ag_gemm(a_shards, b, *, local_rank: int = 0, out_dtype=torch.bfloat16, a_gathered=None,
             c=None, cfg: Config | None = None, workspace: Workspace | None = None, stream=None):
-    """AllGather + GEMM: returns (a_gathered = [A_0; ...; A_{R-1}], c = a_gathered @ b)."""
+    """AllGather + GEMM: returns (a_gathered = [A_0; ...; A_{R-1}], c = a_gathered @ b).
+    With fp8 e4m3 operands b is B^T ([n x k]) and c = a_gathered @ b.T."""
     R = len(a_shards)
     m_r, k = a_shards[0].shape
-    n = b.shape[1]
+    cfg = _with_operand(cfg, a_shards[0])
+    n = b.shape[0] if a_shards[0].dtype == FP8 else b.shape[1]
     dev = b.device
     if a_gathered is None:
-        a_gathered = torch.empty((R * m_r, k), dtype=torch.bfloat16, device=dev)
+        a_gathered = torch.empty((R * m_r, k), dtype=a_shards[0].dtype, device=dev)
     if c is None:
         c = torch.empty((R * m_r, n), dtype=out_dtype, device=dev)
     ws = _ws(workspace, dev)
@@ -237,10 +251,12 @@ def _rs_ar(fn, op, a, b, outs, R, m, n, k, cfg, workspace, stream, what):
 
 def gemm_rs(a, b, *, out_dtype=torch.bfloat16, c_blocks=None, cfg: Config | None = None,
             workspace: Workspace | None = None, stream=None):
-    """GEMM + ReduceScatter: S = sum_r a[r] @ b[r]; returns R row blocks of S."""
+    """GEMM + ReduceScatter: S = sum_r a[r] @ b[r]; returns R row blocks of S.
+    With fp8 e4m3 operands b[r] is B_r^T ([n x k]) and S = sum_r a[r] @ b[r].T."""
     R = len(a)
     m, k = a[0].shape
-    n = b[0].shape[1]
+    cfg = _with_operand(cfg, a[0])
+    n = b[0].shape[0] if a[0].dtype == FP8 else b[0].shape[1]
     if c_blocks is None:
         c_blocks = [torch.empty((m // R, n), dtype=out_dtype, device=a[0].device) for _ in range(R)]
     return _rs_ar(lib().mk_gemm_rs, OP_GEMM_RS, a, b, c_blocks, R, m, n, k, cfg, workspace, stream,
@@ -249,10 +265,12 @@ def gemm_rs(a, b, *, out_dtype=torch.bfloat16, c_blocks=None, cfg: Config | None
 
 def gemm_ar(a, b, *, out_dtype=torch.bfloat16, c_replicas=None, cfg: Config | None = None,
             workspace: Workspace | None = None, stream=None):
-    """GEMM + AllReduce: S = sum_r a[r] @ b[r]; returns R identical replicas of S."""
+    """GEMM + AllReduce: S = sum_r a[r] @ b[r]; returns R identical replicas of S.
+    With fp8 e4m3 operands b[r] is B_r^T ([n x k]) and S = sum_r a[r] @ b[r].T."""
     R = len(a)
     m, k = a[0].shape
-    n = b[0].shape[1]
+    cfg = _with_operand(cfg, a[0])
+    n = b[0].shape[0] if a[0].dtype == FP8 else b[0].shape[1]
     if c_replicas is None:
         c_replicas = [torch.empty((m, n), dtype=out_dtype, device=a[0].device) for _ in range(R)]
     return _rs_ar(lib().mk_gemm_ar, OP_GEMM_AR, a, b, c_replicas, R, m, n, k, cfg, workspace,

@@ -73,6 +73,21 @@ bool make_map_a(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uin
   return r == CUDA_SUCCESS;
 }
 
+// fp8 (byte) 2-D map over a row-major [rows x k] matrix, K-major boxes of
+// 128 bytes x box_rows with 128-byte swizzle (A, and B given as B^T).
+bool make_map_k8(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {k, rows};
+  cuuint64_t strides[1] = {k};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_map_b_chunks(CUtensorMap* m, const void* base, uint64_t k, uint64_t n, uint32_t chunks) {
   auto fn = encode_fn();
   if (!fn || (n % 64)) return false;
@@ -140,7 +155,7 @@ struct Plan {
   int n_mblk, n_nblk, n_kblk, n_tiles;
   int split_k, kps, P;
   int group_m;
-  int chain, last, atomic, wire;
+  int chain, last, atomic, wire, fp8;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
 };
 constexpr int ZFLAG_WORDS = 1024;   // atomic reduction: one zero-done word per CTA
@@ -179,6 +194,11 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   const int want_reduce = cfg ? cfg->reduce : 0;
   const int want_wire = cfg ? cfg->wire : 0;
   if (want_reduce < 0 || want_reduce > 3 || want_wire < 0 || want_wire > 1) return false;
+  // fp8 operands: 128-element k-blocks, and every row a whole number of 16-byte units
+  pl.fp8 = cfg ? cfg->operand : 0;
+  if (pl.fp8 < 0 || pl.fp8 > 1) return false;
+  if (pl.fp8 && (k % 16)) return false;
+  if (pl.fp8) pl.n_kblk = static_cast<int>(ceil_div_ll(k, 2 * BK));
   if (op == OP_AG) {
     pl.n_flags = static_cast<size_t>(pl.n_mblk) * COPY_SUB_MAX;
   } else {
@@ -258,6 +278,8 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.last_arrival = pl.last;
   p.atomic = pl.atomic;
   p.wire_bf16 = pl.wire;
+  p.fp8 = pl.fp8;
+  p.a_esz = pl.fp8 ? 1 : 2;
   p.copy_sub = 1;
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
@@ -420,7 +442,7 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
   p.gathered = static_cast<uint8_t*>(a_gathered);
   for (int r = 0; r < R; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
   p.out[0] = c;
-  const size_t row_bytes = static_cast<size_t>(k) * 2;
+  const size_t row_bytes = static_cast<size_t>(k) * p.a_esz;
   p.copy_local = (static_cast<const uint8_t*>(a_shards[local_rank]) !=
                   static_cast<uint8_t*>(a_gathered) + static_cast<size_t>(local_rank) * m_r * row_bytes)
                      ? 1 : 0;
@@ -450,11 +472,16 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
   }
   // CTA pairs for every compute-only launch (not with copy-role CTAs).
   const bool pair = use_pair(cfg, sms) && !(pl.mode == MK_MODE_FUSED && cfg && cfg->n_copy_ctas > 0);
-  if (!make_map_a(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes) ||
-      !make_map_a(&p.tmA[1], a_gathered, k, pl.M, row_bytes) ||
-      !(p.b_one_box ? make_map_b_chunks(&p.tmB[0], b, k, n, pair ? 2 : 4)
-                    : make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK)))
+  if (pl.fp8) {   // A shards / gathered A [rows x k] and B^T [n x k], all bytes
+    if (!make_map_k8(&p.tmA[0], a_shards[local_rank], k, m_r, BM) ||
+        !make_map_k8(&p.tmA[1], a_gathered, k, pl.M, BM) || !make_map_k8(&p.tmB[0], b, k, n, pair ? 128u : 256u))
+      return MK_ERR_CUDA;
+  } else if (!make_map_a(&p.tmA[0], a_shards[local_rank], k, m_r, row_bytes) ||
+             !make_map_a(&p.tmA[1], a_gathered, k, pl.M, row_bytes) ||
+             !(p.b_one_box ? make_map_b_chunks(&p.tmB[0], b, k, n, pair ? 2 : 4)
+                           : make_map_2d(&p.tmB[0], b, n, k, static_cast<size_t>(n) * 2, 64, BK))) {
     return MK_ERR_CUDA;
+  }
   if (pl.mode == MK_MODE_GEMM_ONLY) return launch_compute(p, pair, sms, s);
   if (pl.mode == MK_MODE_UNFUSED) {
     const uint32_t e = p.epoch;
@@ -523,10 +550,14 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last || pl.atomic);
   for (int r = 0; r < R; ++r) {
     p.out[r] = outs[r];
-    if (!make_map_a(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2) ||
-        !(p.b_one_box ? make_map_b_chunks(&p.tmB[r], b[r], k, n, pair ? 2 : 4)
-                      : make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK)))
+    if (pl.fp8) {   // A_r [m x k] and B_r^T [n x k], bytes
+      if (!make_map_k8(&p.tmA[r], a[r], k, m, BM) || !make_map_k8(&p.tmB[r], b[r], k, n, pair ? 128u : 256u))
+        return MK_ERR_CUDA;
+    } else if (!make_map_a(&p.tmA[r], a[r], k, m, static_cast<size_t>(k) * 2) ||
+               !(p.b_one_box ? make_map_b_chunks(&p.tmB[r], b[r], k, n, pair ? 2 : 4)
+                             : make_map_2d(&p.tmB[r], b[r], n, k, static_cast<size_t>(n) * 2, 64, BK))) {
       return MK_ERR_CUDA;
+    }
   }
   if (pl.mode == MK_MODE_GEMM_ONLY) return launch_compute(p, pair, sms, s);
   if (pl.mode == MK_MODE_UNFUSED) {
@@ -574,7 +605,9 @@ struct MlpLayout {
 bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* cfg, MlpLayout& L) {
   if (R < 1 || R > MK_MLP_MAX_RANKS || m < 0 || h < 0 || f_r < 0) return false;
   if ((h % 8) || (f_r % 8)) return false;
-  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->n_reduce_ctas > 0 || cfg->split_k > 1)) return false;
+  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->operand != 0 || cfg->n_reduce_ctas > 0 ||
+              cfg->split_k > 1))
+    return false;
   if (!plan_gemm(OP_RS, R, static_cast<long long>(R) * m, h, f_r, cfg, L.pl)) return false;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   size_t off = WS_HDR_BYTES;

@@ -765,6 +765,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
   if (!(scale > 0.f) || !std::isfinite(scale)) return MK_ERR_INVALID;
   const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
   if (mode < MK_MODE_FUSED || mode > MK_MODE_UNFUSED) return MK_ERR_INVALID;
+  if (cfg && cfg->operand != 0) return MK_ERR_INVALID;   // bf16 operands only
   const long long blk = static_cast<long long>(heads) * s_r * d;
   const bool need_recv = (R > 1 && mode != MK_MODE_GEMM_ONLY);
   if (need_recv && (!k_recv || !v_recv)) return MK_ERR_INVALID;

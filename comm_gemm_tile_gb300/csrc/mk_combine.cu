@@ -202,6 +202,7 @@ mk_status mk_moe_combine(const void* const* h, const void* const* w2, const floa
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u)) return MK_ERR_INVALID;
   const int mode = cfg ? cfg->mode : MK_MODE_FUSED;
   if (mode < MK_MODE_FUSED || mode > MK_MODE_UNFUSED) return MK_ERR_INVALID;
+  if (cfg && cfg->operand != 0) return MK_ERR_INVALID;   // bf16 operands only
   const long long E = static_cast<long long>(R) * E_loc;
   if (!okp(counts, R * E, 4)) return MK_ERR_INVALID;
   for (int r = 0; r < R; ++r) {

@@ -29,6 +29,8 @@ namespace mk {
 
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
 constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(2 * BM, BN, false, true);   // M = 256 across the pair
+constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);                        // fp8: both operands K-major
+constexpr uint32_t IDESC_F8_PAIR = idesc_e4m3_f32(2 * BM, BN);
 
 // ------------------------------------------------------------------ errors / waits
 __device__ __forceinline__ bool aborted(const FusedParams& p) {
@@ -422,20 +424,23 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
           const int c0 = n0 / 64 + 2 * static_cast<int>(rank);   // this CTA's first column chunk
           for (int h = 0; h < nk; ++h) {
             const int kb = kb0 + h;
+            const int kx = kb * (p.fp8 ? 2 * BK : BK);   // K coordinate (elements) of the k-block
             const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * PSTAGE_BYTES;
             const uint32_t b_dst = a_dst + A_STAGE_BYTES;
-            tma_load_2d_pair(a_dst, ma, fb, kb * BK, it.arow);
-            if (p.b_one_box) {
-              if (it.bz < 0) tma_load_3d_pair(b_dst, mbm, fb, 0, kb * BK, c0);
-              else tma_load_4d_pair(b_dst, mbm, fb, 0, kb * BK, c0, it.bz);
+            tma_load_2d_pair(a_dst, ma, fb, kx, it.arow);
+            if (p.fp8) {   // B^T [n x k]: this CTA's 128 rows of the tile's 256
+              tma_load_2d_pair(b_dst, mbm, fb, kx, n0 + 128 * static_cast<int>(rank));
+            } else if (p.b_one_box) {
+              if (it.bz < 0) tma_load_3d_pair(b_dst, mbm, fb, 0, kx, c0);
+              else tma_load_4d_pair(b_dst, mbm, fb, 0, kx, c0, it.bz);
             } else if (it.bz < 0) {
 #pragma unroll
               for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK);
+                tma_load_2d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kx);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 128; ++j)
-                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kb * BK, it.bz);
+                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, mbm, fb, 64 * (c0 + j), kx, it.bz);
             }
           }
           issued_mask |= 1u << stage;
@@ -450,6 +455,10 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
         const uint32_t a_dst = S.ring + static_cast<uint32_t>(stage) * SB;
         const uint32_t b_dst = a_dst + A_STAGE_BYTES;
         mbar_arrive_expect_tx(S.full(stage), STAGE_BYTES);
+        if (p.fp8) {   // 128-element k-blocks; B^T [n x k]: the tile's 256 rows in one box
+          tma_load_2d(a_dst, ma, S.full(stage), kb * 2 * BK, it.arow);
+          tma_load_2d(b_dst, mbm, S.full(stage), kb * 2 * BK, n0);
+        } else {
         tma_load_2d(a_dst, ma, S.full(stage), kb * BK, it.arow);
         if (p.b_one_box) {
           // the whole BK x 256 B tile in one request (4 column chunks of 64)
@@ -463,6 +472,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
             tma_load_3d(b_dst + j * B_BOX_BYTES, mbm, S.full(stage), n0 + 64 * j, kb * BK, it.bz);
+        }
         }
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -513,6 +523,19 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
             const uint32_t a_addr =
                 S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * Ring<PAIR>::kb_bytes;
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+            if (p.fp8) {
+              // fp8: four K = 32 steps of 32 bytes; A and B^T both K-major, 128-byte
+              // swizzle, 8-row groups 1024 B apart
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 1024u, 2u);
+                const uint64_t bd = sdesc_swz(b_addr + 32u * k, 16u, 1024u, 2u);
+                if constexpr (PAIR) tc_mma_f8_pair(d_tmem, ad, bd, IDESC_F8_PAIR, acc);
+                else tc_mma_f8(d_tmem, ad, bd, IDESC_F8, acc);
+                acc = 1;
+              }
+              continue;
+            }
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
@@ -1230,7 +1253,7 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const int pr = p.copy_rows;
   const int J = BM / pr;
   const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * J;
-  const size_t rb = static_cast<size_t>(p.K) * 2;
+  const size_t rb = static_cast<size_t>(p.K) * p.a_esz;   // bytes per gathered row
   bool skip_first = (p.inject == 1 && worker == 0);
 #if MK_CW_HINT
   const uint64_t pol_src = l2_policy_evict_first(), pol_dst = l2_policy_evict_last();
@@ -1525,7 +1548,7 @@ __device__ __forceinline__ void sub_rows(const FusedParams& p, long long piece, 
 }
 
 __device__ bool copy_next(const FusedParams& p, CopyIter& st, Piece& pc) {
-  const size_t rb = static_cast<size_t>(p.K) * 2;
+  const size_t rb = static_cast<size_t>(p.K) * p.a_esz;   // bytes per gathered row
   const long long n_pieces = static_cast<long long>(p.n_copy_chunks) * p.copy_sub;
   if (st.piece >= n_pieces) return false;
   long long run_hi;

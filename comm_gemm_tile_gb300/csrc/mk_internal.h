@@ -97,6 +97,9 @@ struct FusedParams {
   int atomic;          // RS/AR: 1 = every partial added into one fp32 tile per output tile with
                        //        red.global.add; the warp that completes a quarter converts it
   int wire_bf16;       // RS/AR running sum: 1 = the sum forwarded between parts is bf16
+  int fp8;             // AG/RS/AR: 1 = A and B are fp8 e4m3, B given as its transpose [n x k]
+                       //           (both K-major); a k-block is 128 elements (128 bytes)
+  int a_esz;           // bytes per A element (2 bf16, 1 fp8)
   uint32_t* zflags;    // atomic: one word per CTA, = epoch once its slice of the fp32 tiles is zero
   int group_tiles;     // RS/AR chain: tiles per scheduling group
   int copy_warps;      // AG: 1 = copy-in done by the copy warps of every compute CTA, one

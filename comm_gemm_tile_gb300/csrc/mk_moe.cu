@@ -300,6 +300,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   if (!x || !logits || !w || !recv_src || !recv_x || !y || !workspace) return MK_ERR_INVALID;
   MoeLayout L;
   if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, L)) return MK_ERR_INVALID;
+  if (cfg && cfg->operand != 0) return MK_ERR_INVALID;   // bf16 operands only
   if (ws_bytes < L.total || !al16(workspace)) return MK_ERR_INVALID;
   const long long E = static_cast<long long>(R) * E_loc;
   const long long rows = static_cast<long long>(R) * T * topk;

@@ -48,6 +48,25 @@ def int_bf16(shape, seed: int, lo: int = -2, hi: int = 2) -> torch.Tensor:
     return to_bf16(x)
 
 
+def normal_fp8(shape, std: float, seed: int) -> torch.Tensor:
+    """N(0, std) samples converted by torch to fp8 e4m3 (CPU tensor)."""
+    x = rng(seed).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn)
+
+
+def int_fp8(shape, seed: int, lo: int = -2, hi: int = 2) -> torch.Tensor:
+    """Integers uniform in [lo, hi] as fp8 e4m3 (exact for |x| <= 16)."""
+    x = rng(seed).integers(lo, hi + 1, size=shape, dtype=np.int32).astype(np.float32)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn)
+
+
+def fp8_bytes(t: torch.Tensor) -> np.ndarray:
+    """Raw bytes of an fp8 tensor (any device) as a uint8 array."""
+    return t.detach().cpu().view(torch.uint8).numpy()
+
+
 def zipf_logits(tokens: int, experts: int, seed: int, s: float = 1.1) -> torch.Tensor:
     """Router logits whose top-k picks expert e with popularity ~ (e+1)^-s.
 
@@ -284,6 +303,20 @@ def gemm_inputs(w: GemmWorkload):
         b = [draw((w.k, w.n), w.b_std, w.b_seed)]
     else:
         b = [draw((w.k, w.n), w.b_std, w.b_seed + r) for r in range(w.R)]
+    return a, b
+
+
+def gemm_inputs_fp8(w: GemmWorkload):
+    """Per-rank fp8 e4m3 operands (CPU tensors) of an AG / RS / AR workload,
+    B given as its transpose: a = [A_r (m x k)], b = [B^T (n x k)] (AG: one)."""
+    def draw(shape, std, seed):
+        return int_fp8(shape, seed) if w.integer else normal_fp8(shape, std, seed)
+
+    a = [draw((w.m, w.k), w.a_std, w.a_seed + r) for r in range(w.R)]
+    if w.op == "ag":
+        b = [draw((w.n, w.k), w.b_std, w.b_seed)]
+    else:
+        b = [draw((w.n, w.k), w.b_std, w.b_seed + r) for r in range(w.R)]
     return a, b
 
 

@@ -114,6 +114,13 @@ typedef struct {
                                (round-to-nearest-even) at every forward, halving the
                                partial traffic.  Ignored by the other reductions.
                                The chained MLP takes neither reduce = 2, 3 nor wire.    */
+  int operand;              /* AG / RS / AR operand type: 0 = bf16 A and B, B given as
+                               [k x n] row-major; 1 = fp8 e4m3 A and B, B given as its
+                               transpose B^T [n x k] row-major (both operands K-major,
+                               the layout of the tensor cores' fp8 path); k % 16 == 0.
+                               fp32 accumulation, bf16 / fp32 output as for bf16.  The
+                               gathered A of AG is fp8 too.  MoE, combine, the MLP and
+                               ring attention take bf16 only (MK_ERR_INVALID).           */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).
@@ -134,7 +141,9 @@ size_t mk_workspace_size(int op, int R, long long m, long long n, long long k,
  * at row offset local_rank*m_r, in which case that shard is not copied).
  * The copy-in role moves the remote shards in ring order local+1, local+2, ...
  * and releases a ready flag per 128-row chunk; compute tiles of the local
- * shard start at once, the others after their chunk's flag. */
+ * shard start at once, the others after their chunk's flag.
+ * With cfg->operand = 1 the shards, a_gathered and b are fp8 e4m3 and b is
+ * B^T ([n x k]): c = a_gathered @ (b)^T.  The same holds for RS and AR. */
 mk_status mk_ag_gemm(const void *const *a_shards, const void *b, void *a_gathered, void *c,
                      mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n,
                      long long k, void *workspace, size_t ws_bytes, const mk_config *cfg,

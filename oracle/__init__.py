@@ -9,4 +9,5 @@ from .mk_oracle import (ag_gemm, allgather_rows, bf16_to_f64, f64_to_bf16_bits, 
                         moe_expert_gemm, moe_gather_rows, moe_return_rows, moe_route,
                         moe_seg_from_counts, moe_weighted_sum, norm_scale, owner_rows,
                         ring_attention, ring_order, round_out, sum_over_ranks, rank_partials,
-                        running_sum_bf16_wire, f64_to_f32)
+                        running_sum_bf16_wire, f64_to_f32, e4m3_to_f64, ag_gemm_fp8,
+                        sum_over_ranks_fp8)

@@ -210,6 +210,49 @@ def running_sum_bf16_wire(partials, out: str = "bf16") -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# fp8 operands (the e4m3 variant of AllGather + GEMM, GEMM + ReduceScatter /
+# AllReduce).  The write-up names fp8 only as a capability of the GB300 rack
+# (first section, "问题：主机驱动通信", point (1)); the format is the OCP 8-bit
+# e4m3 encoding: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+# exponent field 0 for subnormals (m/8 * 2^-6), no infinities, and S.1111.111
+# the only NaN (largest finite value 448).  Reading used for the operand
+# layout: B is given as its transpose B^T [n x k] (both operands K-major).
+# ----------------------------------------------------------------------------
+
+
+def e4m3_to_f64(b) -> np.ndarray:
+    """Exact value of raw e4m3 bytes (uint8) as float64."""
+    b = np.asarray(b, dtype=np.uint8)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = ((b >> 3) & 0x0F).astype(np.int64)
+    m = (b & 0x07).astype(np.float64)
+    val = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    val = sign * val
+    return np.where((b & 0x7F) == 0x7F, np.nan, val)
+
+
+def ag_gemm_fp8(a_shards, b_t, out: str = "bf16", rows=None):
+    """C = gather_r(A_r) @ B with fp8 operands: a_shards R arrays of e4m3
+    bytes [m_r x k], b_t the bytes of B^T [n x k].  Returns (gathered bytes,
+    C rounded to `out`)."""
+    gathered = np.concatenate([np.asarray(a, dtype=np.uint8) for a in a_shards], axis=0)
+    a_sel = gathered if rows is None else gathered[np.asarray(rows)]
+    c = e4m3_to_f64(a_sel) @ e4m3_to_f64(b_t).T
+    return gathered, round_out(c, out)
+
+
+def sum_over_ranks_fp8(a_list, bt_list, rows=None) -> np.ndarray:
+    """S = sum_r A_r @ B_r in float64, fp8 operands (bt_list: the bytes of B_r^T)."""
+    assert len(a_list) == len(bt_list) and len(a_list) >= 1
+    s = None
+    for a, bt in zip(a_list, bt_list):
+        a_sel = np.asarray(a) if rows is None else np.asarray(a)[np.asarray(rows)]
+        p = e4m3_to_f64(a_sel) @ e4m3_to_f64(bt).T
+        s = p if s is None else s + p
+    return s
+
+
+# ----------------------------------------------------------------------------
 # MoE dispatch + grouped GEMM
 # ----------------------------------------------------------------------------
 

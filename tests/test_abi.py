@@ -55,6 +55,11 @@ def test_workspace_sizes(L):
     # out-of-range reduce / wire -> 0
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=4)) == 0
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(wire=2)) == 0
+    # fp8 operands: k must be a multiple of 16 (rows of whole 16-byte units)
+    assert mk.workspace_size(mk.OP_AG_GEMM, 8, 1024, 3584, 8192, mk.Config(operand=mk.OPERAND_FP8)) > 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 256, 24, mk.Config(operand=mk.OPERAND_FP8)) == 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 256, 24) > 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 2, 256, 256, 64, mk.Config(operand=2)) == 0
     # GEMM-only mode needs no staging.
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584,
                              mk.Config(mode=mk.MODE_GEMM_ONLY)) < (1 << 20)
@@ -154,7 +159,7 @@ def test_mlp_rejects_the_reduction_variants(L):
 
 
 def test_config_struct_layout():
-    assert ctypes.sizeof(mk._Cfg) == 48
+    assert ctypes.sizeof(mk._Cfg) == 56
     assert mk._Cfg.wait_limit_ns.offset == 24 and mk._Cfg.inject.offset == 32
     assert mk._Cfg.reduce.offset == 36 and mk._Cfg.cta_pair.offset == 40
-    assert mk._Cfg.wire.offset == 44
+    assert mk._Cfg.wire.offset == 44 and mk._Cfg.operand.offset == 48

@@ -301,6 +301,47 @@ def test_rank_partials_sum_to_s():
     np.testing.assert_allclose(sum(O.rank_partials(a, b)), O.sum_over_ranks(a, b), rtol=0, atol=1e-12)
 
 
+# ---- fp8 e4m3 operands
+
+
+def test_e4m3_all_patterns_match_torch():
+    b = np.arange(256, dtype=np.uint8)
+    mine = O.e4m3_to_f64(b)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    np.testing.assert_array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+
+
+@pytest.mark.parametrize("byte,val", [(0x38, 1.0), (0xB8, -1.0), (0x7E, 448.0), (0x01, 2.0 ** -9),
+                                      (0x08, 2.0 ** -6), (0x07, 7 * 2.0 ** -9), (0x40, 2.0),
+                                      (0x3C, 1.5), (0x00, 0.0)])
+def test_e4m3_closed_forms(byte, val):
+    assert O.e4m3_to_f64(np.array([byte], dtype=np.uint8))[0] == val
+
+
+def test_e4m3_nan_patterns_only():
+    v = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert set(np.flatnonzero(np.isnan(v)).tolist()) == {0x7F, 0xFF}
+    assert np.nanmax(np.abs(v)) == 448.0
+
+
+def test_fp8_gemm_brute_force_tiny():
+    rng = np.random.default_rng(9)
+    ok = np.array([x for x in range(256) if (x & 0x7F) != 0x7F], dtype=np.uint8)
+    a = [rng.choice(ok, size=(3, 16)) for _ in range(2)]
+    bt = rng.choice(ok, size=(5, 16))
+    gathered, c = O.ag_gemm_fp8(a, bt, "f32")
+    np.testing.assert_array_equal(gathered, np.concatenate(a, 0))
+    dec = O.e4m3_to_f64
+    for i in range(6):
+        for j in range(5):
+            row = dec(gathered[i])
+            want = sum(row[kk] * dec(bt[j])[kk] for kk in range(16))
+            assert c[i, j] == np.float32(want)
+    s = O.sum_over_ranks_fp8(a, [bt, bt])
+    np.testing.assert_allclose(s, dec(a[0]) @ dec(bt).T + dec(a[1]) @ dec(bt).T, rtol=0, atol=0)
+
+
 def test_route_matches_stable_argsort():
     g = np.random.default_rng(11)
     lg = np.round(g.standard_normal((500, 16)) * 2) / 2      # many ties
