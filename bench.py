@@ -285,7 +285,7 @@ def main():
     ap.add_argument("--n-copy", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiles: 0 library default, 1 one CTA per tile, 2 CTA pairs")
-    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring", "ring_small"],
+    ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring", "ring_small", "ag_fp8"],
                     default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
     args = ap.parse_args()
@@ -457,6 +457,8 @@ def run_only(args):
                                     hbm_peak, causal=True)}
     elif args.only == "mlp":
         res = bench_mlp(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
+    elif args.only == "ag_fp8":
+        res = bench_ag_fp8(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak, hbm_peak)
     elif args.only == "combine":
         res = bench_moe_combine(mk, device, stream, None, args.other_steps, 0, lambda x: x, bf16_peak,
                                 hbm_peak)
@@ -523,6 +525,9 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         torch.cuda.empty_cache()
         out[I.MLP_R8_TP8.name] = bench_mlp(mk, device, stream, dist, max(3, steps // 3), seed_off, tmax,
                                            bf16_peak, hbm_peak)
+        torch.cuda.empty_cache()
+        out[I.AG_R8_TP8_UP.name + "_fp8"] = bench_ag_fp8(mk, device, stream, dist, steps, seed_off, tmax,
+                                                         bf16_peak, hbm_peak)
         torch.cuda.empty_cache()
         for causal in (False, True):
             wr = I.RING_R8_H8_S4096_CAUSAL if causal else I.RING_R8_H8_S4096
@@ -650,6 +655,37 @@ def bench_mlp(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
     return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
             "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
             "pct_of_peak": 100 * fused_tf / bf16_peak, "status": mk.status_string(st)}
+
+
+def bench_ag_fp8(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+    """AllGather+GEMM of the headline shape with fp8 e4m3 operands (B given as B^T):
+    fused, GEMM-only and unfused.  Peak: the measured bf16 peak times the nominal
+    fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)."""
+    w = I.AG_R8_TP8_UP
+    nsets = 3
+    sets = []
+    for s in range(nsets):
+        a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r + 1000 * s + seed_off, device).to(mk.FP8)
+             for r in range(w.R)]
+        bt = dev_normal((w.n, w.k), 1.0, w.b_seed + 1000 * s + seed_off, device).to(mk.FP8)
+        g = torch.empty((w.R * w.m, w.k), dtype=mk.FP8, device=device)
+        c = torch.empty((w.R * w.m, w.n), dtype=torch.bfloat16, device=device)
+        sets.append((a, bt, g, c))
+    ws = mk.Workspace(device)
+    res = {}
+    for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
+                      ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
+        def step(i, cfg=cfg):
+            a, bt, g, c = sets[i % nsets]
+            mk.ag_gemm(a, bt, a_gathered=g, c=c, cfg=cfg, workspace=ws, stream=stream)
+        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+    st, _ = mk.device_status(ws, stream)
+    fp8_peak = 2.0 * bf16_peak
+    fused_tf = w.flops() / (res["fused"] * 1e-3) / 1e12
+    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+            "fp8_peak_tflops": fp8_peak, "pct_of_fp8_peak": 100 * fused_tf / fp8_peak,
+            "status": mk.status_string(st)}
 
 
 def bench_ring(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak, causal=False):
