@@ -497,7 +497,7 @@ done:
 // MMA issuer (one thread; with pairs only the leader's).  A pair's MMA has
 // M = 256: rows 0-127 from the leader's A stage, 128-255 from the peer's, and
 // the B columns from both CTAs' halves; each CTA's TMEM receives its own rows.
-template <bool PAIR>
+template <bool PAIR, bool F8>
 __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t tmem_base, int cid) {
   constexpr int NST = Ring<PAIR>::stages;
   constexpr uint32_t SB = Ring<PAIR>::stage_bytes;
@@ -523,7 +523,7 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
             const uint32_t a_addr =
                 S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * Ring<PAIR>::kb_bytes;
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
-            if (p.fp8) {
+            if constexpr (F8) {
               // fp8: four K = 32 steps of 32 bytes; A and B^T both K-major, 128-byte
               // swizzle, 8-row groups 1024 B apart
 #pragma unroll
@@ -1445,7 +1445,11 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     if (lane == 0) producer<PAIR>(p, S, cid, rank);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_issuer<PAIR>(p, S, tmem_base, cid);
+    // the operand type picks the MMA loop once (the issuing thread's loop stays branch-free)
+    if (lane == 0 && rank == 0) {
+      if (p.fp8) mma_issuer<PAIR, true>(p, S, tmem_base, cid);
+      else mma_issuer<PAIR, false>(p, S, tmem_base, cid);
+    }
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     epilogue<PAIR>(p, S, tmem_base, cid, rank);
