@@ -10,9 +10,11 @@
 //     rank's own block, then the blocks of ranks r-1, r-2, ... as they land
 //     in its receive buffer;
 //   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
-//     into one of two TMEM accumulators (tcgen05, bf16 -> fp32);
+//     into one of two TMEM accumulators (tcgen05, bf16 -> fp32), with one
+//     mbarrier wait and two commits per tile (see at_mma);
 //   * warps 2-9 (softmax): online softmax in two groups of four warps, one
-//     for the even key tiles of a query tile and one for the odd ones, each
+//     for the even tiles of the CTA's running tile count and one for the odd
+//     ones (so a query tile's key tiles alternate between them), each
 //     with its own running maximum, sum, P buffer (shared memory) and O
 //     accumulator (TMEM), so that two tiles' softmax runs at once; P =
 //     exp2(scale * log2(e) * s - m) as bf16; O is rescaled only when the
