@@ -4,7 +4,12 @@ configuration that bench.py times, against the CPU oracle on a seeded row
 sample (two rows per 128-row tile plus the first and last row, all columns).
 The gathered A is compared in full.  Each workload's integer-valued twin
 (values in {-2..2}, exact fp32 sums) must match bit for bit on the sample.
+The same holds for the fp8 AllGather+GEMM of the headline shape and for the
+RS reduction variants (bf16 wire against the oracle's bf16-wire schedule,
+atomic against the plain sum).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -170,3 +175,45 @@ def test_moe_combine_full_size(integer):
             assert norm_err(gpu_values(got_ret).reshape(len(toks), -1), y2.reshape(len(toks), -1),
                             w.N, amax, bmax) <= TOL["bf16"]
             assert norm_err(gpu_values(got_out), exact_out, w.N, amax, bmax) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("integer", [False, True])
+def test_ag_fp8_full_size(integer):
+    # the headline shape with fp8 e4m3 operands (B as B^T), default launch configuration
+    w = I.AG_R8_TP8_UP.integer_twin() if integer else I.AG_R8_TP8_UP
+    w = dataclasses.replace(w, b_std=1.0)
+    a, bt = I.gemm_inputs_fp8(w)
+    ws = mk.Workspace()
+    g, c = mk.ag_gemm([x.cuda() for x in a], bt[0].cuda(), local_rank=w.local_rank, workspace=ws)
+    _ok(ws)
+    a_bytes = [I.fp8_bytes(x) for x in a]
+    assert np.array_equal(I.fp8_bytes(g), np.concatenate(a_bytes, 0))
+    rows = I.sample_rows(w.R * w.m, seed=17)
+    exact = O.e4m3_to_f64(np.concatenate(a_bytes, 0)[rows]) @ O.e4m3_to_f64(I.fp8_bytes(bt[0])).T
+    got = c[torch.from_numpy(rows).cuda()]
+    if integer:
+        np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
+    else:
+        amax = max(float(x.float().abs().max()) for x in a)
+        assert norm_err(gpu_values(got), exact, w.k, amax, float(bt[0].float().abs().max())) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("variant", ["wire", "atomic"])
+def test_rs_reduction_variants_full_size(variant):
+    # integer twin: the atomic sum is exact in any order; the bf16 wire follows the oracle's schedule
+    w = I.RS_R8_TP8_DOWN.integer_twin()
+    a, b = I.gemm_inputs(w)
+    ws = mk.Workspace()
+    cfg = mk.Config(wire=mk.WIRE_BF16) if variant == "wire" else mk.Config(reduce=mk.REDUCE_ATOMIC)
+    blocks = mk.gemm_rs([x.cuda() for x in a], [x.cuda() for x in b], workspace=ws, cfg=cfg)
+    _ok(ws)
+    rows = I.sample_rows(w.m, seed=18)
+    h = w.m // w.R
+    got = torch.stack([blocks[r // h][r % h] for r in rows.tolist()], 0)
+    a_bits, b_bits = [I.bits(x) for x in a], [I.bits(x) for x in b]
+    if variant == "atomic":
+        want = oracle_bits(O.sum_over_ranks(a_bits, b_bits, rows=rows), "bf16")
+    else:
+        parts = [O.bf16_to_f64(x[rows]) @ O.bf16_to_f64(y) for x, y in zip(a_bits, b_bits)]
+        want = O.running_sum_bf16_wire(parts, "bf16")
+    np.testing.assert_array_equal(gpu_bits(got), want)
