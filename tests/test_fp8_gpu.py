@@ -132,3 +132,21 @@ def test_fp8_rejected_by_ops_without_it():
                           [torch.zeros((1, 128, 128), dtype=torch.bfloat16, device="cuda")] * 2,
                           cfg=mk.Config(operand=mk.OPERAND_FP8))
     del x
+
+
+def test_ag_fp8_copy_role_ctas_and_missing_piece():
+    a, b = I.gemm_inputs_fp8(_w("ag", 4, 256, 512, 256, True, 251))
+    _, want = O.ag_gemm_fp8([I.fp8_bytes(x) for x in a], I.fp8_bytes(b[0]), "bf16")
+    # copy-role CTAs (bulk copies of fp8 rows) instead of the compute CTAs' copy warps
+    _, c = mk.ag_gemm(_cuda(a), b[0].cuda(), cfg=mk.Config(n_copy_ctas=8))
+    _ok()
+    np.testing.assert_array_equal(gpu_bits(c), want)
+    # a copy piece that never signals: the bounded waits report a timeout, and the next
+    # call on the same workspace is correct
+    ws = mk.Workspace()
+    mk.ag_gemm(_cuda(a), b[0].cuda(), workspace=ws, cfg=mk.Config(inject=1, wait_limit_ns=20_000_000))
+    st, _ = mk.device_status(ws)
+    assert st == mk.MK_ERR_TIMEOUT
+    _, c = mk.ag_gemm(_cuda(a), b[0].cuda(), workspace=ws)
+    _ok(ws)
+    np.testing.assert_array_equal(gpu_bits(c), want)
