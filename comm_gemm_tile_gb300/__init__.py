@@ -51,7 +51,7 @@ class _Cfg(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("group_m", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("mode", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
                 ("inject", ctypes.c_int), ("reduce", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("wire", ctypes.c_int), ("operand", ctypes.c_int)]
+                ("wire", ctypes.c_int), ("operand", ctypes.c_int), ("trace", ctypes.c_int)]
 
 
 @dataclasses.dataclass
@@ -69,11 +69,12 @@ class Config:
     cta_pair: int = 0
     wire: int = 0
     operand: int = 0
+    trace: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.n_copy_ctas, self.n_reduce_ctas, self.max_ctas, self.group_m,
                     self.split_k, self.mode, self.wait_limit_ns, self.inject, self.reduce,
-                    self.cta_pair, self.wire, self.operand)
+                    self.cta_pair, self.wire, self.operand, self.trace)
 
 
 _lib = None
@@ -98,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.mk_status_string.argtypes = [i]
         L.mk_workspace_size.restype = sz
         L.mk_workspace_size.argtypes = [i, i, ll, ll, ll, P(_Cfg)]
+        L.mk_trace_entries.restype = sz
+        L.mk_trace_entries.argtypes = [i, i, ll, ll, ll, P(_Cfg), P(sz)]
         L.mk_moe_workspace_size.restype = sz
         L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
         L.mk_get_device_status.restype = i
@@ -275,6 +278,22 @@ def gemm_ar(a, b, *, out_dtype=torch.bfloat16, c_replicas=None, cfg: Config | No
         c_replicas = [torch.empty((m, n), dtype=out_dtype, device=a[0].device) for _ in range(R)]
     return _rs_ar(lib().mk_gemm_ar, OP_GEMM_AR, a, b, c_replicas, R, m, n, k, cfg, workspace,
                   stream, "mk_gemm_ar")
+
+
+def trace_records(workspace: Workspace, op: int, R, m, n, k, cfg: Config):
+    """The in-kernel trace of the last AG / RS / AR call made on `workspace` with
+    cfg.trace = 1 and these arguments (m = rows per shard for AG, as for
+    workspace_size): an int64 tensor [records x 4] = (producer start ns, accumulator
+    ready ns, epilogue done ns, epoch << 32 | CTA << 1 | pair rank); record 2*i + c is
+    work item i on the CTA of pair rank c.  Records the call did not write keep older
+    contents (another epoch) or zeros."""
+    off = ctypes.c_size_t(0)
+    n_rec = int(lib().mk_trace_entries(op, R, m, n, k, _cfgp(cfg), ctypes.byref(off)))
+    if n_rec == 0:
+        return torch.zeros((0, 4), dtype=torch.int64)
+    buf = workspace.get(int(off.value) + n_rec * 32)
+    raw = buf[int(off.value):int(off.value) + n_rec * 32]
+    return raw.view(torch.int64).view(n_rec, 4).cpu()
 
 
 def moe_workspace_size(R, E_loc, topk, T, H, N, cap_rows, cfg: Config | None = None) -> int:

@@ -157,6 +157,7 @@ struct Plan {
   int group_m;
   int chain, last, atomic, wire, fp8;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
+  size_t trace_off, trace_n;   // in-kernel trace records (4 x u64 each) at the end, or none
 };
 constexpr int ZFLAG_WORDS = 1024;   // atomic reduction: one zero-done word per CTA
 
@@ -251,6 +252,15 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   off = (off + 1023) & ~static_cast<size_t>(1023);
   pl.staging_off = off;
   pl.total = off + pl.staging_bytes;
+  pl.trace_off = 0;
+  pl.trace_n = 0;
+  if (cfg && cfg->trace) {
+    if (cfg->trace != 1) return false;
+    // two records per work item (the CTAs of a pair); items <= tiles x partials
+    pl.trace_n = static_cast<size_t>(std::max(pl.n_tiles, 1)) * std::max(pl.P, 1) * 2;
+    pl.trace_off = (pl.total + 255) & ~static_cast<size_t>(255);
+    pl.total = pl.trace_off + pl.trace_n * 32;
+  }
   return true;
 }
 
@@ -280,6 +290,8 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.wire_bf16 = pl.wire;
   p.fp8 = pl.fp8;
   p.a_esz = pl.fp8 ? 1 : 2;
+  p.trace = pl.trace_n ? reinterpret_cast<unsigned long long*>(ws + pl.trace_off) : nullptr;
+  p.trace_cap = static_cast<int>(pl.trace_n);
   p.copy_sub = 1;
   p.out_f32 = (c_dtype == MK_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<uint32_t*>(ws);
@@ -397,6 +409,16 @@ size_t mk_workspace_size(int op, int R, long long m, long long n, long long k, c
   Plan pl;
   if (!plan_gemm(op, R, m, n, k, cfg, pl)) return 0;
   return pl.total;
+}
+
+size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, const mk_config* cfg,
+                        size_t* offset) {
+  if (offset) *offset = 0;
+  if (op < MK_OP_AG_GEMM || op > MK_OP_GEMM_AR) return 0;
+  Plan pl;
+  if (!plan_gemm(op, R, m, n, k, cfg, pl)) return 0;
+  if (offset) *offset = pl.trace_off;
+  return pl.trace_n;
 }
 
 mk_status mk_get_device_status(const void* workspace, mk_stream_t stream, long long* detail) {
@@ -605,8 +627,8 @@ struct MlpLayout {
 bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* cfg, MlpLayout& L) {
   if (R < 1 || R > MK_MLP_MAX_RANKS || m < 0 || h < 0 || f_r < 0) return false;
   if ((h % 8) || (f_r % 8)) return false;
-  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->operand != 0 || cfg->n_reduce_ctas > 0 ||
-              cfg->split_k > 1))
+  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->operand != 0 || cfg->trace != 0 ||
+              cfg->n_reduce_ctas > 0 || cfg->split_k > 1))
     return false;
   if (!plan_gemm(OP_RS, R, static_cast<long long>(R) * m, h, f_r, cfg, L.pl)) return false;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };

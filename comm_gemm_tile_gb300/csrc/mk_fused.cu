@@ -358,6 +358,19 @@ __device__ __forceinline__ int n_items_for(const FusedParams& p) {
   return p.n_items;
 }
 
+// In-kernel trace (mk_config.trace): word w of the record of (item i, pair rank).
+__device__ __forceinline__ void trace_put(const FusedParams& p, int i, uint32_t rank, int w,
+                                          unsigned long long v) {
+  const int idx = 2 * i + static_cast<int>(rank);
+  if (p.trace != nullptr && idx < p.trace_cap) p.trace[static_cast<size_t>(idx) * 4 + w] = v;
+}
+__device__ __forceinline__ void trace_end(const FusedParams& p, int i, uint32_t rank) {
+  if (p.trace == nullptr) return;
+  trace_put(p, i, rank, 2, globaltimer_ns());
+  trace_put(p, i, rank, 3, (static_cast<unsigned long long>(p.epoch) << 32) |
+                               (static_cast<unsigned long long>(blockIdx.x) << 1) | rank);
+}
+
 // TMA producer (one thread).  With pairs each CTA loads its own 128 rows of A
 // and its 128 of the tile's 256 B columns into its own ring, completing on
 // the leader's full barrier, which the leader arms with both CTAs' bytes.
@@ -373,6 +386,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it, static_cast<int>(rank));
+    if (p.trace != nullptr) trace_put(p, i, rank, 0, globaltimer_ns());
     if (p.op == OP_MOE && p.mode == MK_MODE_FUSED && it.row_hi > 0) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       // (an empty pair half covers no rows and waits for nothing)
@@ -926,6 +940,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     // warp-uniform outcome: the tcgen05.ld below needs every lane of the warp
     const int landed = wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i) ? 1 : 0;
     if (!__all_sync(0xffffffffu, landed)) return;
+    if (p.trace != nullptr && warp == 2 && lane == 0) trace_put(p, i, rank, 1, globaltimer_ns());
     tc_fence_after();
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(buf * BN);
@@ -1068,6 +1083,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         __threadfence();   // the other partials' additions happened before their counts
         reduce_quarter(p, it, acc, 1, trow, row_ok, grow);
       }
+      if (warp == 2 && lane == 0) trace_end(p, i, rank);
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;
@@ -1110,6 +1126,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         __threadfence();   // the other partials' stores happened before their counts
         reduce_quarter(p, it, p.staging + static_cast<size_t>(tile) * p.P * TILE_F32, p.P, trow, row_ok, grow);
       }
+      if (warp == 2 && lane == 0) trace_end(p, i, rank);
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;
@@ -1203,6 +1220,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       }
     }
     if (publish) pd_par ^= 1u << buf;
+    if (warp == 2 && lane == 0) trace_end(p, i, rank);
     if (++buf == 2) {
       buf = 0;
       acc_phase ^= 1u;

@@ -121,6 +121,8 @@ typedef struct {
                                fp32 accumulation, bf16 / fp32 output as for bf16.  The
                                gathered A of AG is fp8 too.  MoE, combine, the MLP and
                                ring attention take bf16 only (MK_ERR_INVALID).           */
+  int trace;                /* AG / RS / AR: 1 = record per-item timestamps into a region at
+                               the end of the workspace (see mk_trace_entries); 0 = off. */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).
@@ -334,6 +336,17 @@ mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a
  * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the
  * stream itself reports an error).  `detail` (may be NULL) receives a code
  * saying which wait failed (role * 1e6 + item index), for diagnostics. */
+/* In-kernel trace of an AG / RS / AR call made with cfg->trace = 1: the number
+ * of records and (in *offset) their byte offset in the workspace; 0 records
+ * when tracing is off or the arguments are bad.  Record 2*i + c (c = the CTA's
+ * rank in its pair, 0 without pairs) belongs to work item i and holds four
+ * uint64: [0] %globaltimer (ns) when the TMA producer started the item, [1] when
+ * the epilogue found the accumulator complete, [2] when the epilogue had stored
+ * (and published) the item, [3] (call epoch << 32) | (CTA index << 1) | c.
+ * Records of items a call did not run keep older contents (a lower epoch). */
+size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, const mk_config *cfg,
+                        size_t *offset);
+
 mk_status mk_get_device_status(const void *workspace, mk_stream_t stream, long long *detail);
 
 /* Static text for a status code. */

@@ -150,6 +150,24 @@ def test_argument_validation_without_launch(L):
     assert L.mk_get_device_status(None, None, None) == mk.MK_ERR_INVALID
 
 
+def test_trace_layout(L):
+    off = ctypes.c_size_t(7)
+    cfg_off = mk.Config()
+    cfg_on = mk.Config(trace=1)
+    assert L.mk_trace_entries(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, ctypes.byref(cfg_off.c()),
+                              ctypes.byref(off)) == 0 and off.value == 0
+    n = L.mk_trace_entries(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, ctypes.byref(cfg_on.c()), ctypes.byref(off))
+    # two records (4 x u64) per (tile, partial): 2048 tiles x 8 ranks
+    assert n == 2048 * 8 * 2 and off.value % 256 == 0
+    base = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584)
+    assert off.value >= base
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, cfg_on) == off.value + n * 32
+    n = L.mk_trace_entries(mk.OP_AG_GEMM, 8, 1024, 3584, 8192, ctypes.byref(cfg_on.c()), ctypes.byref(off))
+    assert n == 64 * 14 * 2
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(trace=2)) == 0
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1)) == 0
+
+
 def test_mlp_rejects_the_reduction_variants(L):
     # the chained MLP reduces by the fp32 running sum only
     assert mk.mlp_workspace_size(8, 1024, 8192, 3584) > 0
@@ -162,4 +180,4 @@ def test_config_struct_layout():
     assert ctypes.sizeof(mk._Cfg) == 56
     assert mk._Cfg.wait_limit_ns.offset == 24 and mk._Cfg.inject.offset == 32
     assert mk._Cfg.reduce.offset == 36 and mk._Cfg.cta_pair.offset == 40
-    assert mk._Cfg.wire.offset == 44 and mk._Cfg.operand.offset == 48
+    assert mk._Cfg.wire.offset == 44 and mk._Cfg.operand.offset == 48 and mk._Cfg.trace.offset == 52
