@@ -201,6 +201,27 @@ def time_loop(fn, steps, warmup, stream, dist=None):
     return e0.elapsed_time(e1)
 
 
+def time_interleaved(fns: dict, steps: int, warmup: int, stream, dist=None, rounds: int = 5):
+    """Device time (ms per call) of each named mode, the modes timed in turn in `rounds`
+    blocks of about steps / rounds calls each, so that every mode sees the same clock
+    and power state (a mode timed in one long loop after another runs hotter or cooler).
+    Each block starts after one untimed call of its own mode, so that it does not pay for
+    the caches the previous mode left dirty.  Call index i runs on over the blocks of a
+    mode, rotating its input sets."""
+    block = max(1, steps // rounds)
+    for fn in fns.values():
+        for i in range(warmup):
+            fn(i)
+    total = {name: 0.0 for name in fns}
+    done = {name: 0 for name in fns}
+    for _ in range(rounds):
+        for name, fn in fns.items():
+            i0 = done[name]
+            total[name] += time_loop(lambda i, fn=fn, i0=i0: fn(i0 + i), block, 1, stream, dist)
+            done[name] += block
+    return {name: total[name] / done[name] for name in fns}
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 
 def oracle_sample_rate(shards_bits, b_bits, target_s: float):
@@ -358,8 +379,12 @@ def main():
     def tmax(x):
         return max_over_ranks(x, dist, device)
 
-    t_gemm = tmax(time_loop(step_gemm, base_steps, 5, stream, dist) / base_steps)
-    t_unf = tmax(time_loop(step_unfused, base_steps, 5, stream, dist) / base_steps)
+    # fused against GEMM-only and unfused: interleaved blocks under the same clocks
+    cmp_ms = time_interleaved({"fused": step_fused, "gemm_only": step_gemm,
+                               "unfused": step_unfused}, base_steps, 5, stream, dist)
+    t_cmp = tmax(cmp_ms["fused"])
+    t_gemm = tmax(cmp_ms["gemm_only"])
+    t_unf = tmax(cmp_ms["unfused"])
     t_fused_max = tmax(t_fused)
     ms = t_fused_max / args.steps
     value = whole_job_rate(flops * args.steps, world, t_fused_max) / 1e12
@@ -456,7 +481,9 @@ def main():
                        "l2": f"{N_SETS} input sets in rotation, each {set_mb:.0f} MB with "
                              f"outputs (> L2)"},
             "pct_of_peak": 100.0 * (flops / (ms * 1e-3) / 1e12) / bf16_peak,
-            "exposed_ms": ms - t_gemm,
+            # exposed: fused minus GEMM-only, both from the interleaved comparison
+            "exposed_ms": t_cmp - t_gemm,
+            "fused_ms_interleaved": t_cmp,
             "gemm_only_ms": t_gemm,
             "unfused_ms": t_unf,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
@@ -534,7 +561,7 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
         ws = mk.Workspace(device)
         fn = mk.gemm_rs if w.op == "rs" else mk.gemm_ar
         key = "c_blocks" if w.op == "rs" else "c_replicas"
-        res = {}
+        steps_fns = {}
         for name, cfg in (("fused", mk.Config(cta_pair=pair)),
                           ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY, cta_pair=pair)),
                           ("unfused", mk.Config(mode=mk.MODE_UNFUSED, cta_pair=pair)),
@@ -544,8 +571,10 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
             def step(i, cfg=cfg):
                 a, b, o = sets[i % nsets]
                 fn(a, b, cfg=cfg, workspace=ws, stream=stream, **{key: o})
-            n = steps if w.op == "rs" else steps * 10
-            res[name] = tmax(time_loop(step, n, 3, stream, dist)) / n
+            steps_fns[name] = step
+        n = steps if w.op == "rs" else steps * 10
+        res = {name: tmax(t) for name, t in
+               time_interleaved(steps_fns, n, 3, stream, dist).items()}
         st, _ = mk.device_status(ws, stream)
         flops = w.flops()
         fused_tf = flops / (res["fused"] * 1e-3) / 1e12
@@ -596,14 +625,15 @@ def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
         sets.append((x, lg, we))
     ws = mk.Workspace(device)
     outs = mk.moe_dispatch_gemm(*sets[0], E_loc=w.E_loc, topk=w.topk, workspace=ws, stream=stream)
-    res = {}
+    fns = {}
     for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
                       ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
         def step(i, cfg=cfg):
             x, lg, we = sets[i % 2]
             mk.moe_dispatch_gemm(x, lg, we, E_loc=w.E_loc, topk=w.topk, out=outs, cfg=cfg,
                                  workspace=ws, stream=stream)
-        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+        fns[name] = step
+    res = {name: tmax(t) for name, t in time_interleaved(fns, steps, 3, stream, dist).items()}
     st, _ = mk.device_status(ws, stream)
     flops = w.flops()
     rows = w.R * w.T * w.topk
@@ -649,14 +679,15 @@ def bench_moe_combine(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak
         sets.append((h, w2, gates))
     outs = mk.moe_combine(*sets[0], disp["recv_src"], disp["counts"], E_loc=w.E_loc, topk=w.topk,
                           workspace=ws, stream=stream)
-    res = {}
+    fns = {}
     for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
                       ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
         def step(i, cfg=cfg):
             h, w2, gates = sets[i % 2]
             mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"], E_loc=w.E_loc, topk=w.topk,
                            out=outs, cfg=cfg, workspace=ws, stream=stream)
-        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+        fns[name] = step
+    res = {name: tmax(t) for name, t in time_interleaved(fns, steps, 3, stream, dist).items()}
     st, _ = mk.device_status(ws, stream)
     flops = w.flops()
     rows = w.R * w.T * w.topk
@@ -688,13 +719,14 @@ def bench_mlp(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
     hid = [torch.empty((M, w.f_r), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
     y = [torch.empty((w.m, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
     ws = mk.Workspace(device)
-    res = {}
+    fns = {}
     for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
                       ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
         def step(i, cfg=cfg):
             mk.mlp_ag_rs(x, w1, w2, x_gathered=xg, hid=hid, y_blocks=y, cfg=cfg, workspace=ws,
                          stream=stream)
-        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+        fns[name] = step
+    res = {name: tmax(t) for name, t in time_interleaved(fns, steps, 3, stream, dist).items()}
     st, _ = mk.device_status(ws, stream)
     flops = w.flops()
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12
@@ -718,13 +750,14 @@ def bench_ag_fp8(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm
         c = torch.empty((w.R * w.m, w.n), dtype=torch.bfloat16, device=device)
         sets.append((a, bt, g, c))
     ws = mk.Workspace(device)
-    res = {}
+    fns = {}
     for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
                       ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
         def step(i, cfg=cfg):
             a, bt, g, c = sets[i % nsets]
             mk.ag_gemm(a, bt, a_gathered=g, c=c, cfg=cfg, workspace=ws, stream=stream)
-        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+        fns[name] = step
+    res = {name: tmax(t) for name, t in time_interleaved(fns, steps, 3, stream, dist).items()}
     st, _ = mk.device_status(ws, stream)
     fp8_peak = 2.0 * bf16_peak
     fused_tf = w.flops() / (res["fused"] * 1e-3) / 1e12
@@ -747,13 +780,14 @@ def bench_ring(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_p
           for _ in range(w.R)]
     vr = [torch.empty_like(t) for t in kr]
     ws = mk.Workspace(device)
-    res = {}
+    fns = {}
     for name, cfg in (("fused", None), ("gemm_only", mk.Config(mode=mk.MODE_GEMM_ONLY)),
                       ("unfused", mk.Config(mode=mk.MODE_UNFUSED))):
         def step(i, cfg=cfg):
             mk.ring_attention(q, k, v, causal=causal, out=out, k_recv=kr, v_recv=vr, cfg=cfg,
                               workspace=ws, stream=stream)
-        res[name] = tmax(time_loop(step, steps, 3, stream, dist)) / steps
+        fns[name] = step
+    res = {name: tmax(t) for name, t in time_interleaved(fns, steps, 3, stream, dist).items()}
     st, _ = mk.device_status(ws, stream)
     flops = w.flops()
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12

@@ -27,6 +27,11 @@ REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL, REDUCE_ATOMIC = 0, 1, 2, 3
 WIRE_F32, WIRE_BF16 = 0, 1
 OPERAND_BF16, OPERAND_FP8 = 0, 1
 FP8 = torch.float8_e4m3fn
+# columns of trace_records()
+(TRACE_START, TRACE_INPUTS, TRACE_ISSUED, TRACE_READY, TRACE_END, TRACE_CLK_START,
+ TRACE_CLK_READY, TRACE_ID) = range(8)
+TRACE_WORDS = 8
+TRACE_COPY_RECORDS = 1024
 
 
 def _with_operand(cfg, t):
@@ -283,17 +288,34 @@ def gemm_ar(a, b, *, out_dtype=torch.bfloat16, c_replicas=None, cfg: Config | No
 def trace_records(workspace: Workspace, op: int, R, m, n, k, cfg: Config):
     """The in-kernel trace of the last AG / RS / AR call made on `workspace` with
     cfg.trace = 1 and these arguments (m = rows per shard for AG, as for
-    workspace_size): an int64 tensor [records x 4] = (producer start ns, accumulator
-    ready ns, epilogue done ns, epoch << 32 | CTA << 1 | pair rank); record 2*i + c is
-    work item i on the CTA of pair rank c.  Records the call did not write keep older
-    contents (another epoch) or zeros."""
+    workspace_size): an int64 tensor [records x 8], record 2*i + c for work item i
+    on the CTA of pair rank c.  Columns (TRACE_* below): ns stamps when the
+    producer takes the item, its inputs are ready, its last load is issued, the
+    accumulator is ready, the epilogue is done; the SM's clock64 at the first and
+    fourth stamps; epoch << 32 | CTA << 1 | pair rank.  Records the call did not
+    write keep older contents (another epoch) or zeros."""
     off = ctypes.c_size_t(0)
     n_rec = int(lib().mk_trace_entries(op, R, m, n, k, _cfgp(cfg), ctypes.byref(off)))
     if n_rec == 0:
-        return torch.zeros((0, 4), dtype=torch.int64)
-    buf = workspace.get(int(off.value) + n_rec * 32)
-    raw = buf[int(off.value):int(off.value) + n_rec * 32]
-    return raw.view(torch.int64).view(n_rec, 4).cpu()
+        return torch.zeros((0, TRACE_WORDS), dtype=torch.int64)
+    nb = n_rec * TRACE_WORDS * 8
+    buf = workspace.get(int(off.value) + nb)
+    raw = buf[int(off.value):int(off.value) + nb]
+    return raw.view(torch.int64).view(n_rec, TRACE_WORDS).cpu()
+
+
+def trace_copy_records(workspace: Workspace, op: int, R, m, n, k, cfg: Config):
+    """The copy-warp records that follow the item records: int64 [TRACE_COPY_RECORDS x 8],
+    record w for copy worker w: start ns, end ns, pieces, bytes, 0, 0, 0,
+    epoch << 32 | w.  Only an AllGather copy-in by copy warps writes them."""
+    off = ctypes.c_size_t(0)
+    n_rec = int(lib().mk_trace_entries(op, R, m, n, k, _cfgp(cfg), ctypes.byref(off)))
+    if n_rec == 0:
+        return torch.zeros((0, TRACE_WORDS), dtype=torch.int64)
+    o = int(off.value) + n_rec * TRACE_WORDS * 8
+    nb = TRACE_COPY_RECORDS * TRACE_WORDS * 8
+    buf = workspace.get(o + nb)
+    return buf[o:o + nb].view(torch.int64).view(TRACE_COPY_RECORDS, TRACE_WORDS).cpu()
 
 
 def moe_workspace_size(R, E_loc, topk, T, H, N, cap_rows, cfg: Config | None = None) -> int:

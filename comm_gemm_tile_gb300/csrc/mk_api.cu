@@ -140,6 +140,9 @@ static inline bool buf_ok(const void* p, long long elems) {
 }
 
 // Target size of one copy-warp piece of the gathered A (whole rows, power-of-two count).
+#ifndef MK_AG_COPY_WARPS
+#define MK_AG_COPY_WARPS 2   // copy warps per compute CTA for the AllGather copy-in
+#endif
 #ifndef MK_CW_PIECE_BYTES
 #define MK_CW_PIECE_BYTES 16384
 #endif
@@ -157,7 +160,7 @@ struct Plan {
   int group_m;
   int chain, last, atomic, wire, fp8;
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
-  size_t trace_off, trace_n;   // in-kernel trace records (4 x u64 each) at the end, or none
+  size_t trace_off, trace_n;   // in-kernel trace records (8 x u64 each) at the end, or none
 };
 constexpr int ZFLAG_WORDS = 1024;   // atomic reduction: one zero-done word per CTA
 
@@ -259,7 +262,7 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
     // two records per work item (the CTAs of a pair); items <= tiles x partials
     pl.trace_n = static_cast<size_t>(std::max(pl.n_tiles, 1)) * std::max(pl.P, 1) * 2;
     pl.trace_off = (pl.total + 255) & ~static_cast<size_t>(255);
-    pl.total = pl.trace_off + pl.trace_n * 32;
+    pl.total = pl.trace_off + (pl.trace_n + MK_TRACE_COPY_RECORDS) * 64;
   }
   return true;
 }
@@ -524,7 +527,7 @@ mk_status mk_ag_gemm(const void* const* a_shards, const void* b, void* a_gathere
     p.copy_rows = pr;
     // two copy warps per CTA move the 7/8 of A in well under the GEMM's time;
     // more of them measured no faster and compete with the operand loads
-    p.n_cw = std::min(2, N_COPY_WARPS);
+    p.n_cw = std::min(MK_AG_COPY_WARPS, N_COPY_WARPS);
     return launch_compute(p, pair, sms, s);
   }
   int n_copy = cfg->n_copy_ctas;

@@ -359,15 +359,33 @@ __device__ __forceinline__ int n_items_for(const FusedParams& p) {
 }
 
 // In-kernel trace (mk_config.trace): word w of the record of (item i, pair rank).
+// Words: 0 producer takes the item, 1 its inputs are ready, 2 its last load is
+// issued, 3 accumulator ready, 4 epilogue done (all %globaltimer ns); 5 / 6 the
+// SM's clock64 at 0 / 3; 7 epoch << 32 | CTA << 1 | pair rank.
+constexpr int TRACE_WORDS = 8;
 __device__ __forceinline__ void trace_put(const FusedParams& p, int i, uint32_t rank, int w,
                                           unsigned long long v) {
   const int idx = 2 * i + static_cast<int>(rank);
-  if (p.trace != nullptr && idx < p.trace_cap) p.trace[static_cast<size_t>(idx) * 4 + w] = v;
+  if (p.trace != nullptr && idx < p.trace_cap)
+    p.trace[static_cast<size_t>(idx) * TRACE_WORDS + w] = v;
+}
+// Copy-warp records follow the item records: record trace_cap + worker holds
+// [0] start ns (after the kernel-start handshake), [1] end ns (last piece
+// released), [2] pieces copied, [3] bytes copied, [7] epoch << 32 | worker.
+__device__ __forceinline__ void trace_copy(const FusedParams& p, int worker, unsigned long long t0,
+                                           unsigned long long pieces, unsigned long long bytes) {
+  if (p.trace == nullptr || worker >= MK_TRACE_COPY_RECORDS) return;
+  unsigned long long* r = p.trace + (static_cast<size_t>(p.trace_cap) + worker) * TRACE_WORDS;
+  r[0] = t0;
+  r[1] = globaltimer_ns();
+  r[2] = pieces;
+  r[3] = bytes;
+  r[7] = (static_cast<unsigned long long>(p.epoch) << 32) | static_cast<unsigned long long>(worker);
 }
 __device__ __forceinline__ void trace_end(const FusedParams& p, int i, uint32_t rank) {
   if (p.trace == nullptr) return;
-  trace_put(p, i, rank, 2, globaltimer_ns());
-  trace_put(p, i, rank, 3, (static_cast<unsigned long long>(p.epoch) << 32) |
+  trace_put(p, i, rank, 4, globaltimer_ns());
+  trace_put(p, i, rank, 7, (static_cast<unsigned long long>(p.epoch) << 32) |
                                (static_cast<unsigned long long>(blockIdx.x) << 1) | rank);
 }
 
@@ -386,7 +404,10 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it, static_cast<int>(rank));
-    if (p.trace != nullptr) trace_put(p, i, rank, 0, globaltimer_ns());
+    if (p.trace != nullptr) {
+      trace_put(p, i, rank, 0, globaltimer_ns());
+      trace_put(p, i, rank, 5, clock64());
+    }
     if (p.op == OP_MOE && p.mode == MK_MODE_FUSED && it.row_hi > 0) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       // (an empty pair half covers no rows and waits for nothing)
@@ -412,6 +433,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
       }
       fence_proxy_async_global();
     }
+    if (p.trace != nullptr) trace_put(p, i, rank, 1, globaltimer_ns());
     for (int seg = 0; seg < it.nseg; ++seg) {
       const CUtensorMap* ma = &p.tmA[it.amap + seg];
       const CUtensorMap* mbm = &p.tmB[it.bmap + seg];
@@ -496,6 +518,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
         }
       }
     }
+    if (p.trace != nullptr) trace_put(p, i, rank, 2, globaltimer_ns());
   }
 done:
   // Every load issued must have landed before the CTA may exit.  With pairs
@@ -940,7 +963,10 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     // warp-uniform outcome: the tcgen05.ld below needs every lane of the warp
     const int landed = wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i) ? 1 : 0;
     if (!__all_sync(0xffffffffu, landed)) return;
-    if (p.trace != nullptr && warp == 2 && lane == 0) trace_put(p, i, rank, 1, globaltimer_ns());
+    if (p.trace != nullptr && warp == 2 && lane == 0) {
+      trace_put(p, i, rank, 3, globaltimer_ns());
+      trace_put(p, i, rank, 6, clock64());
+    }
     tc_fence_after();
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(buf * BN);
@@ -1258,7 +1284,8 @@ constexpr int CW_UNROLL = MK_CW_UNROLL;
 #define MK_MOE_CW_UNROLL MK_CW_UNROLL
 #endif
 constexpr int MOE_CW_UNROLL = MK_MOE_CW_UNROLL;   // 16-byte loads in flight per lane (MoE rows)
-// MK_CW_HINT = 1: shard reads marked L2 evict_first, gathered-A writes evict_last.
+// MK_CW_HINT = 1: shard reads marked L2 evict_first, gathered-A writes evict_last;
+// 2: both evict_first.
 #ifndef MK_CW_HINT
 #define MK_CW_HINT 0
 #endif
@@ -1274,13 +1301,16 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const size_t rb = static_cast<size_t>(p.K) * p.a_esz;   // bytes per gathered row
   bool skip_first = (p.inject == 1 && worker == 0);
 #if MK_CW_HINT
-  const uint64_t pol_src = l2_policy_evict_first(), pol_dst = l2_policy_evict_last();
+  const uint64_t pol_src = l2_policy_evict_first();
+  const uint64_t pol_dst = MK_CW_HINT == 2 ? l2_policy_evict_first() : l2_policy_evict_last();
 #endif
   {
     int ok = 1;
     if (lane == 0) ok = wait_flag(p, &p.hdr[HDR_READY], WHERE_COPY, worker) ? 1 : 0;
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
   }
+  const unsigned long long t_start = p.trace != nullptr ? globaltimer_ns() : 0ull;
+  unsigned long long n_done = 0, b_done = 0;
   for (long long pc = worker; pc < n_pieces; pc += n_workers) {
     const int c = static_cast<int>(pc / J), j = static_cast<int>(pc - static_cast<long long>(c) * J);
     const int mb = ag_copy_mb(p, c);
@@ -1296,6 +1326,7 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
       const uint8_t* src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb;
       uint8_t* dst = p.gathered + static_cast<size_t>(row) * rb;
       const size_t n16 = static_cast<size_t>(run_hi - row) * rb / 16;
+      b_done += n16 * 16;
       for (size_t i0 = lane; i0 < n16; i0 += 32 * CW_UNROLL) {
         uint4 v[CW_UNROLL];
 #pragma unroll
@@ -1326,7 +1357,9 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
       else atomicAdd(chunk_counter(p, mb), 1u);   // after this warp's fences: a release
     }
     __syncwarp();
+    ++n_done;
   }
+  if (p.trace != nullptr && lane == 0) trace_copy(p, worker, t_start, n_done, b_done);
 }
 
 // MoE dispatch by the copy warps of every compute CTA: destination rows of all

@@ -100,8 +100,9 @@ struct FusedParams {
   int fp8;             // AG/RS/AR: 1 = A and B are fp8 e4m3, B given as its transpose [n x k]
                        //           (both K-major); a k-block is 128 elements (128 bytes)
   int a_esz;           // bytes per A element (2 bf16, 1 fp8)
-  unsigned long long* trace;   // per (item, pair rank) records of 4 x u64, or null
-  int trace_cap;               // records available (2 per item)
+  unsigned long long* trace;   // per (item, pair rank) records of 8 x u64, or null
+  int trace_cap;               // item records available (2 per item); then
+                               // MK_TRACE_COPY_RECORDS copy-warp records
   uint32_t* zflags;    // atomic: one word per CTA, = epoch once its slice of the fp32 tiles is zero
   int group_tiles;     // RS/AR chain: tiles per scheduling group
   int copy_warps;      // AG: 1 = copy-in done by the copy warps of every compute CTA, one

@@ -339,11 +339,23 @@ mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a
 /* In-kernel trace of an AG / RS / AR call made with cfg->trace = 1: the number
  * of records and (in *offset) their byte offset in the workspace; 0 records
  * when tracing is off or the arguments are bad.  Record 2*i + c (c = the CTA's
- * rank in its pair, 0 without pairs) belongs to work item i and holds four
- * uint64: [0] %globaltimer (ns) when the TMA producer started the item, [1] when
- * the epilogue found the accumulator complete, [2] when the epilogue had stored
- * (and published) the item, [3] (call epoch << 32) | (CTA index << 1) | c.
+ * rank in its pair, 0 without pairs) belongs to work item i and holds eight
+ * uint64, the first five %globaltimer (ns):
+ *   [0] the TMA producer takes the item,
+ *   [1] the item's inputs are ready (AG: its gathered rows have landed;
+ *       otherwise the same as [0]),
+ *   [2] the producer has issued the item's last load,
+ *   [3] the epilogue finds the accumulator complete,
+ *   [4] the epilogue has stored (and published) the item;
+ *   [5], [6] the SM's clock64 at [0] and at [3] (their ratio to [3] - [0] is
+ *       the SM clock over the item);
+ *   [7] (call epoch << 32) | (CTA index << 1) | c.
+ * MK_TRACE_COPY_RECORDS records of the same size follow, one per copy warp of
+ * the AllGather copy-in (record w for worker w = CTA * copy warps + warp):
+ *   [0] start and [1] end (ns; the end follows its last chunk release),
+ *   [2] pieces and [3] bytes it copied, [7] (call epoch << 32) | w.
  * Records of items a call did not run keep older contents (a lower epoch). */
+#define MK_TRACE_COPY_RECORDS 1024
 size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, const mk_config *cfg,
                         size_t *offset);
 

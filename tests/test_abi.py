@@ -157,15 +157,21 @@ def test_trace_layout(L):
     assert L.mk_trace_entries(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, ctypes.byref(cfg_off.c()),
                               ctypes.byref(off)) == 0 and off.value == 0
     n = L.mk_trace_entries(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, ctypes.byref(cfg_on.c()), ctypes.byref(off))
-    # two records (4 x u64) per (tile, partial): 2048 tiles x 8 ranks
+    # two records (8 x u64) per (tile, partial): 2048 tiles x 8 ranks
     assert n == 2048 * 8 * 2 and off.value % 256 == 0
     base = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584)
     assert off.value >= base
-    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, cfg_on) == off.value + n * 32
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, cfg_on) == \
+        off.value + (n + mk.TRACE_COPY_RECORDS) * 64
     n = L.mk_trace_entries(mk.OP_AG_GEMM, 8, 1024, 3584, 8192, ctypes.byref(cfg_on.c()), ctypes.byref(off))
     assert n == 64 * 14 * 2
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(trace=2)) == 0
     assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1)) == 0
+
+
+def test_trace_copy_record_count_matches_header():
+    hdr = open(os.path.join(ROOT, "include", "mk.h")).read()
+    assert int(re.search(r"#define MK_TRACE_COPY_RECORDS (\d+)", hdr).group(1)) == mk.TRACE_COPY_RECORDS
 
 
 def test_mlp_rejects_the_reduction_variants(L):

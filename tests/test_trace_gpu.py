@@ -1,12 +1,15 @@
 """In-kernel trace of the fused GEMM kernels (GPU).
 
 With mk_config.trace = 1 every work item of an AllGather+GEMM, GEMM+ReduceScatter
-or GEMM+AllReduce call writes, per CTA of the pair, three %globaltimer stamps
-(producer start, accumulator ready, epilogue done) and its epoch / CTA / pair
-rank.  Checked here: tracing leaves the results bit-identical; the call's
+or GEMM+AllReduce call writes, per CTA of the pair, five %globaltimer stamps
+(producer takes the item, inputs ready, last load issued, accumulator ready,
+epilogue done), the SM's clock64 at the first and fourth, and its epoch / CTA /
+pair rank; AllGather's copy warps add one record each (start, end, pieces,
+bytes).  Checked here: tracing leaves the results bit-identical; the call's
 records are the newest epoch, cover every item index from 0 up with the same
-pair ranks, and are ordered start <= ready <= end; a second call on the same
-workspace overwrites them with a later epoch.
+pair ranks, and their stamps are ordered; the clock stamps give an SM clock
+within the device's range; a second call on the same workspace overwrites them
+with a later epoch.
 """
 import pytest
 import torch
@@ -46,7 +49,7 @@ CASES = [  # op, R, m (rows per shard for AG), n, k, reduce
 
 
 def _latest(rec):
-    epochs = rec[:, 3] >> 32
+    epochs = rec[:, mk.TRACE_ID] >> 32
     e = int(epochs.max())
     sel = (epochs == e) & (rec[:, 0] != 0)
     return e, sel
@@ -81,13 +84,32 @@ def test_trace_records(op, R, m, n, k, reduce, pair):
     ranks = {int(j) % 2 for j in idx}
     assert len(idx) == len(items) * len(ranks)        # every item on the same pair ranks
     r = rec[idx]
-    assert bool((r[:, 0] <= r[:, 1]).all()) and bool((r[:, 1] <= r[:, 2]).all())
-    assert bool(((r[:, 3] & 1) == idx % 2).all())     # the pair rank of the record's slot
-    ctas = (r[:, 3] >> 1) & 0x7FFFFFFF
+    assert rec.shape[1] == mk.TRACE_WORDS
+    for a_, b_ in ((mk.TRACE_START, mk.TRACE_INPUTS), (mk.TRACE_INPUTS, mk.TRACE_ISSUED),
+                   (mk.TRACE_START, mk.TRACE_READY), (mk.TRACE_READY, mk.TRACE_END)):
+        assert bool((r[:, a_] <= r[:, b_]).all()), (a_, b_)
+    # the SM clock over an item (clock64 ticks / ns), where the item spans over 2 us
+    dt = (r[:, mk.TRACE_READY] - r[:, mk.TRACE_START]).double()
+    dc = (r[:, mk.TRACE_CLK_READY] - r[:, mk.TRACE_CLK_START]).double()
+    long_ = dt > 2000
+    if bool(long_.any()):
+        ghz = dc[long_] / dt[long_]
+        assert float(ghz.min()) > 0.3 and float(ghz.max()) < 3.5, (float(ghz.min()), float(ghz.max()))
+    assert bool(((r[:, mk.TRACE_ID] & 1) == idx % 2).all())     # the pair rank of the slot
+    ctas = (r[:, mk.TRACE_ID] >> 1) & 0x7FFFFFFF
     assert int(ctas.max()) < 4 * torch.cuda.get_device_properties(0).multi_processor_count
     # a tile is split over at most R*split_k items; at least one item per 2 tiles
     n_tiles = -(-(m * (R if op == "ag" else 1)) // 128) * -(-n // 256)
     assert len(items) >= n_tiles // 2
+
+    if op == "ag":
+        # the copy warps' records: together they moved every row of the gathered A
+        cr = mk.trace_copy_records(ws, OPS[op], R, m, n, k, cfg)
+        mine = cr[(cr[:, mk.TRACE_ID] >> 32) == e1]
+        assert mine.shape[0] > 0
+        assert int(mine[:, 3].sum()) == R * m * k * 2
+        assert bool((mine[:, 0] <= mine[:, 1]).all()) and bool((mine[:, 2] >= 0).all())
+        assert set((mine[:, mk.TRACE_ID] & 0xFFFFFFFF).tolist()) == set(range(mine.shape[0]))
 
     got2 = _call(op, a, b, cfg, ws)
     assert torch.equal(got2, plain)
