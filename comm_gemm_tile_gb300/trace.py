@@ -1,0 +1,184 @@
+"""Summaries of the in-kernel trace (mk_config.trace = 1) of one AG / RS / AR call.
+
+`summarize(records, copy_records)` reduces the records of the newest call to
+per-wave figures: wave w is the w-th work item of every CTA.  For each wave it
+gives the median time between consecutive accumulator-ready stamps of a CTA (the
+item's MMA time in steady state), in microseconds and in SM cycles, the median
+wait for the item's inputs, the epilogue time and the SM clock; the copy warps'
+records give when the AllGather copy-in started and ended and its rate.
+
+Run as a module on one GPU to trace a bench workload:
+
+    python -m comm_gemm_tile_gb300.trace ag|rs|ar [--mode fused|gemm] [--calls N]
+
+It makes the workload's inputs (seeded normal bf16, drawn on the device), runs N
+untraced calls back to back to reach a steady clock and power state, then one
+traced call, and prints the summary of that call.
+"""
+from __future__ import annotations
+
+import argparse
+import statistics
+
+import torch
+
+import comm_gemm_tile_gb300 as mk
+
+
+def _newest(rec: torch.Tensor):
+    """Indices of the records written by the newest call."""
+    ep = rec[:, mk.TRACE_ID] >> 32
+    sel = (ep == ep.max()) & (rec[:, mk.TRACE_START] != 0)
+    return torch.nonzero(sel).flatten()
+
+
+def _med(xs):
+    return statistics.median(xs) if xs else float("nan")
+
+
+def summarize(rec: torch.Tensor, copy_rec: torch.Tensor | None = None, max_rows: int = 12) -> dict:
+    idx = _newest(rec)
+    r = rec[idx]
+    t0i = int(r[:, mk.TRACE_START].min())
+    # differences in int64 first: the stamps are ~1e18 ns, beyond a double's integer range
+    us = lambda col: ((r[:, col] - t0i).double() / 1e3).tolist()   # noqa: E731
+    start, inputs, ready, end = us(mk.TRACE_START), us(mk.TRACE_INPUTS), us(mk.TRACE_READY), us(mk.TRACE_END)
+    c0 = int(r[:, mk.TRACE_CLK_START].min())
+    clk_s = (r[:, mk.TRACE_CLK_START] - c0).double().tolist()
+    clk_r = (r[:, mk.TRACE_CLK_READY] - c0).double().tolist()
+    ident = rec[idx, mk.TRACE_ID]
+    cta = ((ident >> 1) & 0x7FFFFFFF).tolist()
+    item = (idx // 2).tolist()
+    per_cta: dict = {}
+    for j in range(len(item)):
+        per_cta.setdefault(cta[j], []).append(j)
+    waves: dict = {}
+    for js in per_cta.values():
+        js.sort(key=lambda j: item[j])
+        prev_t, prev_c = 0.0, None
+        for w, j in enumerate(js):
+            dt_ns = (ready[j] - start[j]) * 1e3
+            mhz = (clk_r[j] - clk_s[j]) / dt_ns * 1e3 if dt_ns > 2000 else None
+            gap_cyc = clk_r[j] - prev_c if prev_c is not None else None
+            waves.setdefault(w, []).append({
+                "gap_us": ready[j] - prev_t, "gap_cycles": gap_cyc, "input_wait_us": inputs[j] - start[j],
+                "epilogue_us": end[j] - ready[j], "start_us": start[j], "mhz": mhz})
+            prev_t, prev_c = ready[j], clk_r[j]
+    out = {"records": len(item), "items": len(set(item)), "ctas": len(per_cta),
+           "span_us": max(end) if end else 0.0, "waves": []}
+    # at most max_rows rows: consecutive waves pooled into groups
+    ws_ = sorted(waves)
+    per = max(1, -(-len(ws_) // max_rows))
+    for g0 in range(0, len(ws_), per):
+        grp = ws_[g0:g0 + per]
+        v = [x for w in grp for x in waves[w]]
+        out["waves"].append({
+            "wave": f"{grp[0]}" if len(grp) == 1 else f"{grp[0]}-{grp[-1]}", "n": len(v),
+            "start_us": _med([x["start_us"] for x in v]),
+            "ready_gap_us": _med([x["gap_us"] for x in v]),
+            "ready_gap_cycles": _med([x["gap_cycles"] for x in v if x["gap_cycles"] is not None]),
+            "input_wait_us": _med([x["input_wait_us"] for x in v]),
+            "input_wait_max_us": max(x["input_wait_us"] for x in v),
+            "epilogue_us": _med([x["epilogue_us"] for x in v]),
+            "sm_mhz": _med([x["mhz"] for x in v if x["mhz"] is not None]),
+        })
+    if copy_rec is not None and copy_rec.shape[0]:
+        ep_new = int(rec[idx, mk.TRACE_ID].max()) >> 32
+        c = copy_rec[(copy_rec[:, mk.TRACE_ID] >> 32) == ep_new]
+        if c.shape[0]:
+            s_ = ((c[:, 0] - t0i).double() / 1e3).tolist()
+            e_ = ((c[:, 1] - t0i).double() / 1e3).tolist()
+            nbytes = float(c[:, 3].sum())
+            out["copy"] = {"warps": c.shape[0], "start_us": _med(s_), "end_med_us": _med(e_),
+                           "end_max_us": max(e_), "bytes": nbytes,
+                           "tb_per_s": nbytes / ((max(e_) - min(s_)) * 1e-6) / 1e12}
+    return out
+
+
+def format_summary(d: dict, title: str = "") -> str:
+    lines = []
+    if title:
+        lines.append(title)
+    lines.append(f"{d['items']} items on {d['ctas']} CTAs ({d['records']} records), "
+                 f"span {d['span_us']:.1f} us")
+    lines.append("| wave | CTA items | start us | ready gap us | ready gap cycles | input wait us "
+                 "(max) | epilogue us | SM MHz |")
+    lines.append("|---|---|---|---|---|---|---|---|")
+    for w in d["waves"]:
+        lines.append(f"| {w['wave']} | {w['n']} | {w['start_us']:.1f} | {w['ready_gap_us']:.2f} | "
+                     f"{w['ready_gap_cycles']:.0f} | {w['input_wait_us']:.2f} ({w['input_wait_max_us']:.2f}) | "
+                     f"{w['epilogue_us']:.2f} | {w['sm_mhz']:.0f} |")
+    if "copy" in d:
+        c = d["copy"]
+        lines.append(f"copy warps: {c['warps']}, start {c['start_us']:.1f} us, end median "
+                     f"{c['end_med_us']:.1f} / max {c['end_max_us']:.1f} us, {c['bytes'] / 1e6:.1f} MB "
+                     f"at {c['tb_per_s']:.2f} TB/s")
+    return "\n".join(lines)
+
+
+def _dev_normal(shape, std, seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    return (x * std).to(torch.bfloat16)
+
+
+def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0") -> str:
+    from comm_gemm_tile_gb300 import build
+    from comm_gemm_tile_gb300 import inputs as I
+    build.build()
+    dev = torch.device(device)
+    w = {"ag": I.AG_R8_TP8_UP, "rs": I.RS_R8_TP8_DOWN, "ar": I.AR_R8_DECODE}[op]
+    m_mode = {"fused": mk.MODE_FUSED, "gemm": mk.MODE_GEMM_ONLY}[mode]
+    nsets = 2
+    sets = []
+    for s in range(nsets):
+        a = [_dev_normal((w.m, w.k), 1.0, w.a_seed + r + 1000 * s, dev) for r in range(w.R)]
+        if op == "ag":
+            b = _dev_normal((w.k, w.n), w.b_std, w.b_seed + 1000 * s, dev)
+            g = torch.empty((w.R * w.m, w.k), dtype=torch.bfloat16, device=dev)
+            c = torch.empty((w.R * w.m, w.n), dtype=torch.bfloat16, device=dev)
+            sets.append((a, b, g, c))
+        else:
+            b = [_dev_normal((w.k, w.n), w.b_std, w.b_seed + r + 1000 * s, dev) for r in range(w.R)]
+            rows = w.m // w.R if op == "rs" else w.m
+            o = [torch.empty((rows, w.n), dtype=torch.bfloat16, device=dev) for _ in range(w.R)]
+            sets.append((a, b, o))
+    ws = mk.Workspace(dev)
+    op_code = {"ag": mk.OP_AG_GEMM, "rs": mk.OP_GEMM_RS, "ar": mk.OP_GEMM_AR}[op]
+
+    def call(i, cfg):
+        st = sets[i % nsets]
+        if op == "ag":
+            mk.ag_gemm(st[0], st[1], a_gathered=st[2], c=st[3], cfg=cfg, workspace=ws)
+        elif op == "rs":
+            mk.gemm_rs(st[0], st[1], c_blocks=st[2], cfg=cfg, workspace=ws)
+        else:
+            mk.gemm_ar(st[0], st[1], c_replicas=st[2], cfg=cfg, workspace=ws)
+
+    if op == "ag" and m_mode == mk.MODE_GEMM_ONLY:
+        for i in range(nsets):           # GEMM-only reads the gathered A as it stands
+            call(i, mk.Config())
+    cfg = mk.Config(mode=m_mode, trace=1)
+    for i in range(calls):
+        call(i, mk.Config(mode=m_mode))
+    call(calls, cfg)
+    st, detail = mk.device_status(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"traced call reported {mk.status_string(st)} ({detail})")
+    rec = mk.trace_records(ws, op_code, w.R, w.m, w.n, w.k, cfg)
+    crec = mk.trace_copy_records(ws, op_code, w.R, w.m, w.n, w.k, cfg) if op == "ag" else None
+    return format_summary(summarize(rec, crec), f"{w.name}, {mode}, after {calls} untraced calls")
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("op", choices=["ag", "rs", "ar"])
+    ap.add_argument("--mode", choices=["fused", "gemm"], default="fused")
+    ap.add_argument("--calls", type=int, default=30)
+    args = ap.parse_args()
+    print(trace_workload(args.op, args.mode, args.calls))
+
+
+if __name__ == "__main__":
+    main()
