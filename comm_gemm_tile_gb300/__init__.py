@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.mk_workspace_size.argtypes = [i, i, ll, ll, ll, P(_Cfg)]
         L.mk_trace_entries.restype = sz
         L.mk_trace_entries.argtypes = [i, i, ll, ll, ll, P(_Cfg), P(sz)]
+        L.mk_moe_trace_entries.restype = sz
+        L.mk_moe_trace_entries.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg), P(sz)]
         L.mk_moe_workspace_size.restype = sz
         L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
         L.mk_get_device_status.restype = i
@@ -316,6 +318,23 @@ def trace_copy_records(workspace: Workspace, op: int, R, m, n, k, cfg: Config):
     nb = TRACE_COPY_RECORDS * TRACE_WORDS * 8
     buf = workspace.get(o + nb)
     return buf[o:o + nb].view(torch.int64).view(TRACE_COPY_RECORDS, TRACE_WORDS).cpu()
+
+
+def moe_trace_records(workspace: Workspace, R, E_loc, topk, T, H, N, cap_rows, cfg: Config):
+    """The in-kernel trace of the last MoE dispatch + grouped GEMM call made on
+    `workspace` with cfg.trace = 1 and these arguments (cap_rows as the call used it):
+    (item records [2 x tile-table entries x 8], the reserved copy-warp records), int64,
+    with the words of trace_records.  The dispatch copy writes no copy-warp records."""
+    off = ctypes.c_size_t(0)
+    n_rec = int(lib().mk_moe_trace_entries(R, E_loc, topk, T, H, N, cap_rows, _cfgp(cfg),
+                                           ctypes.byref(off)))
+    if n_rec == 0:
+        z = torch.zeros((0, TRACE_WORDS), dtype=torch.int64)
+        return z, z
+    o = int(off.value)
+    nb = (n_rec + TRACE_COPY_RECORDS) * TRACE_WORDS * 8
+    raw = workspace.get(o + nb)[o:o + nb].view(torch.int64).view(-1, TRACE_WORDS).cpu()
+    return raw[:n_rec], raw[n_rec:]
 
 
 def moe_workspace_size(R, E_loc, topk, T, H, N, cap_rows, cfg: Config | None = None) -> int:

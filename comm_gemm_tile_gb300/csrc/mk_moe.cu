@@ -236,12 +236,15 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
 
 struct MoeLayout {
   size_t blocks_off, misc_off, pos_off, hist_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
+  size_t trace_off, trace_n;   // in-kernel trace: item records (8 x u64), then copy-warp records
   size_t total;
   int nblk, n_nblk, max_tiles, C;
 };
 
 bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long N, long long cap,
-                MoeLayout& L) {
+                const mk_config* cfg, MoeLayout& L) {
+  const int trace = cfg ? cfg->trace : 0;
+  if (trace < 0 || trace > 1) return false;
   if (R < 1 || R > MK_MAX_RANKS || E_loc < 1) return false;
   const long long E = static_cast<long long>(R) * E_loc;
   if (E > MOE_MAX_E || topk < 1 || topk > MOE_MAX_TOPK || topk > E) return false;
@@ -267,6 +270,13 @@ bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long 
   L.segoff_off = off;  off = al(off + static_cast<size_t>(R) * (E_loc + 1) * 4);
   L.tprefix_off = off; off = al(off + (static_cast<size_t>(E) + 1) * 4);
   L.tiles_off = off;   off = al(off + static_cast<size_t>(L.max_tiles) * 5 * 4);
+  L.trace_off = 0;
+  L.trace_n = 0;
+  if (trace) {   // two records per tile-table entry (the CTAs of a pair)
+    L.trace_n = static_cast<size_t>(std::max(L.max_tiles, 1)) * 2;
+    L.trace_off = off;
+    off = al(off + (L.trace_n + MK_TRACE_COPY_RECORDS) * 64);
+  }
   L.total = off;
   return true;
 }
@@ -286,10 +296,18 @@ extern "C" {
 
 size_t mk_moe_workspace_size(int R, int E_loc, int topk, long long T, long long H, long long N,
                              long long cap_rows, const mk_config* cfg) {
-  (void)cfg;
   MoeLayout L;
-  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, L)) return 0;
+  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, cfg, L)) return 0;
   return L.total;
+}
+
+size_t mk_moe_trace_entries(int R, int E_loc, int topk, long long T, long long H, long long N,
+                            long long cap_rows, const mk_config* cfg, size_t* offset) {
+  if (offset) *offset = 0;
+  MoeLayout L;
+  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, cfg, L)) return 0;
+  if (offset) *offset = L.trace_off;
+  return L.trace_n;
 }
 
 mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits, const void* const* w,
@@ -299,7 +317,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
                                size_t ws_bytes, const mk_config* cfg, mk_stream_t stream) {
   if (!x || !logits || !w || !recv_src || !recv_x || !y || !workspace) return MK_ERR_INVALID;
   MoeLayout L;
-  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, L)) return MK_ERR_INVALID;
+  if (!moe_layout(R, E_loc, topk, T, H, N, cap_rows, cfg, L)) return MK_ERR_INVALID;
   if (cfg && cfg->operand != 0) return MK_ERR_INVALID;   // bf16 operands only
   if (ws_bytes < L.total || !al16(workspace)) return MK_ERR_INVALID;
   const long long E = static_cast<long long>(R) * E_loc;
@@ -396,6 +414,9 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();
+  p.trace = L.trace_n ? reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.trace_off)
+                      : nullptr;
+  p.trace_cap = static_cast<int>(L.trace_n);
   for (int r = 0; r < R; ++r) {
     p.shard[r] = static_cast<const uint8_t*>(x[r]);
     p.out[r] = y[r];

@@ -1,4 +1,4 @@
-"""Summaries of the in-kernel trace (mk_config.trace = 1) of one AG / RS / AR call.
+"""Summaries of the in-kernel trace (mk_config.trace = 1) of one AG / RS / AR / MoE call.
 
 `summarize(records, copy_records)` reduces the records of the newest call to
 per-wave figures: wave w is the w-th work item of every CTA.  For each wave it
@@ -9,7 +9,7 @@ records give when the AllGather copy-in started and ended and its rate.
 
 Run as a module on one GPU to trace a bench workload:
 
-    python -m comm_gemm_tile_gb300.trace ag|rs|ar [--mode fused|gemm] [--calls N]
+    python -m comm_gemm_tile_gb300.trace ag|rs|ar|moe [--mode fused|gemm] [--calls N]
 
 It makes the workload's inputs (seeded normal bf16, drawn on the device), runs N
 untraced calls back to back to reach a steady clock and power state, then one
@@ -123,11 +123,41 @@ def _dev_normal(shape, std, seed, device):
     return (x * std).to(torch.bfloat16)
 
 
+def _trace_moe(mode: str, calls: int, dev) -> str:
+    from comm_gemm_tile_gb300 import inputs as I
+    w = I.MOE_R8_E64
+    m_mode = {"fused": mk.MODE_FUSED, "gemm": mk.MODE_GEMM_ONLY}[mode]
+    sets = []
+    for s in range(2):
+        x = [_dev_normal((w.T, w.H), 1.0, w.x_seed + r + 1000 * s, dev) for r in range(w.R)]
+        lg = [I.zipf_logits(w.T, w.E, w.logit_seed + r + 1000 * s).to(dev) for r in range(w.R)]
+        we = [_dev_normal((w.E_loc, w.H, w.N), 0.02, w.w_seed + d + 1000 * s, dev) for d in range(w.R)]
+        sets.append((x, lg, we))
+    ws = mk.Workspace(dev)
+    out = mk.moe_dispatch_gemm(*sets[0], E_loc=w.E_loc, topk=w.topk, cap_rows=w.cap, workspace=ws)
+
+    def call(i, cfg):
+        mk.moe_dispatch_gemm(*sets[i % 2], E_loc=w.E_loc, topk=w.topk, cap_rows=w.cap, out=out,
+                             cfg=cfg, workspace=ws)
+
+    cfg = mk.Config(mode=m_mode, trace=1)
+    for i in range(calls):
+        call(i, mk.Config(mode=m_mode))
+    call(calls, cfg)
+    st, detail = mk.device_status(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"traced call reported {mk.status_string(st)} ({detail})")
+    rec, crec = mk.moe_trace_records(ws, w.R, w.E_loc, w.topk, w.T, w.H, w.N, w.cap, cfg)
+    return format_summary(summarize(rec), f"{w.name}, {mode}, after {calls} untraced calls")
+
+
 def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0") -> str:
     from comm_gemm_tile_gb300 import build
     from comm_gemm_tile_gb300 import inputs as I
     build.build()
     dev = torch.device(device)
+    if op == "moe":
+        return _trace_moe(mode, calls, dev)
     w = {"ag": I.AG_R8_TP8_UP, "rs": I.RS_R8_TP8_DOWN, "ar": I.AR_R8_DECODE}[op]
     m_mode = {"fused": mk.MODE_FUSED, "gemm": mk.MODE_GEMM_ONLY}[mode]
     nsets = 2
@@ -173,7 +203,7 @@ def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("op", choices=["ag", "rs", "ar"])
+    ap.add_argument("op", choices=["ag", "rs", "ar", "moe"])
     ap.add_argument("--mode", choices=["fused", "gemm"], default="fused")
     ap.add_argument("--calls", type=int, default=30)
     args = ap.parse_args()

@@ -121,8 +121,9 @@ typedef struct {
                                fp32 accumulation, bf16 / fp32 output as for bf16.  The
                                gathered A of AG is fp8 too.  MoE, combine, the MLP and
                                ring attention take bf16 only (MK_ERR_INVALID).           */
-  int trace;                /* AG / RS / AR: 1 = record per-item timestamps into a region at
-                               the end of the workspace (see mk_trace_entries); 0 = off. */
+  int trace;                /* AG / RS / AR / MoE dispatch: 1 = record per-item timestamps
+                               into a region at the end of the workspace (see
+                               mk_trace_entries, mk_moe_trace_entries); 0 = off. */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).
@@ -342,7 +343,7 @@ mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a
  * rank in its pair, 0 without pairs) belongs to work item i and holds eight
  * uint64, the first five %globaltimer (ns):
  *   [0] the TMA producer takes the item,
- *   [1] the item's inputs are ready (AG: its gathered rows have landed;
+ *   [1] the item's inputs are ready (AG, MoE: its rows have landed;
  *       otherwise the same as [0]),
  *   [2] the producer has issued the item's last load,
  *   [3] the epilogue finds the accumulator complete,
@@ -358,6 +359,14 @@ mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a
 #define MK_TRACE_COPY_RECORDS 1024
 size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, const mk_config *cfg,
                         size_t *offset);
+
+/* The same for a MoE dispatch + grouped GEMM call (arguments as for
+ * mk_moe_workspace_size): record 2*i + c belongs to entry i of the call's tile
+ * table, with the words of mk_trace_entries ([1]: the tile's rows have been
+ * dispatched).  The copy-warp records that follow are reserved (the dispatch
+ * copy writes none). */
+size_t mk_moe_trace_entries(int R, int E_loc, int topk, long long T, long long H, long long N,
+                            long long cap_rows, const mk_config *cfg, size_t *offset);
 
 mk_status mk_get_device_status(const void *workspace, mk_stream_t stream, long long *detail);
 

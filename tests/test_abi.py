@@ -169,6 +169,20 @@ def test_trace_layout(L):
     assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1)) == 0
 
 
+def test_moe_trace_layout(L):
+    off = ctypes.c_size_t(7)
+    args = (8, 8, 2, 4096, 4096, 1536, 65536)
+    assert L.mk_moe_trace_entries(*args, ctypes.byref(mk.Config().c()), ctypes.byref(off)) == 0
+    assert off.value == 0
+    on = mk.Config(trace=1)
+    n = L.mk_moe_trace_entries(*args, ctypes.byref(on.c()), ctypes.byref(off))
+    # two records per tile-table entry: (65536 / 128 + 64) row tiles x 6 column tiles
+    assert n == 2 * (65536 // 128 + 64) * 6
+    assert off.value >= mk.moe_workspace_size(*args) and off.value % 256 == 0
+    assert mk.moe_workspace_size(*args, cfg=on) >= off.value + (n + mk.TRACE_COPY_RECORDS) * 64
+    assert mk.moe_workspace_size(*args, cfg=mk.Config(trace=2)) == 0
+
+
 def test_trace_copy_record_count_matches_header():
     hdr = open(os.path.join(ROOT, "include", "mk.h")).read()
     assert int(re.search(r"#define MK_TRACE_COPY_RECORDS (\d+)", hdr).group(1)) == mk.TRACE_COPY_RECORDS

@@ -116,3 +116,40 @@ def test_trace_records(op, R, m, n, k, reduce, pair):
     rec2 = mk.trace_records(ws, OPS[op], R, m, n, k, cfg)
     e2, sel2 = _latest(rec2)
     assert e2 > e1 and torch.equal(sel2, sel)
+
+
+@pytest.mark.parametrize("pair", [mk.PAIR_OFF, mk.PAIR_ON])
+def test_moe_trace_records(pair):
+    w = I.MoeWorkload("t", R=4, E_loc=3, T=257, H=520, N=264, integer=True, x_seed=31,
+                      logit_seed=41, w_seed=51)
+    x, logits, wexp = I.moe_inputs(w)
+    args = ([t.cuda() for t in x], [t.cuda() for t in logits], [t.cuda() for t in wexp])
+
+    def run(cfg, ws):
+        res = mk.moe_dispatch_gemm(*args, E_loc=w.E_loc, topk=w.topk, cap_rows=w.cap, cfg=cfg,
+                                   workspace=ws)
+        st, detail = mk.device_status(ws)
+        assert st == mk.MK_OK, (mk.status_string(st), detail)
+        return res
+
+    plain = run(mk.Config(cta_pair=pair), mk.Workspace())
+    cfg = mk.Config(cta_pair=pair, trace=1)
+    ws = mk.Workspace()
+    got = run(cfg, ws)
+    rc = got["recv_counts"].cpu()
+    assert torch.equal(rc, plain["recv_counts"].cpu())
+    for d in range(w.R):
+        n = int(rc[d])
+        assert torch.equal(got["y"][d][:n], plain["y"][d][:n])
+        assert torch.equal(got["recv_x"][d][:n], plain["recv_x"][d][:n])
+    rec, crec = mk.moe_trace_records(ws, w.R, w.E_loc, w.topk, w.T, w.H, w.N, w.cap, cfg)
+    e, sel = _latest(rec)
+    idx = torch.nonzero(sel).flatten()
+    items = sorted({int(j) // 2 for j in idx})
+    assert items and items == list(range(len(items)))
+    r = rec[idx]
+    for a_, b_ in ((mk.TRACE_START, mk.TRACE_INPUTS), (mk.TRACE_INPUTS, mk.TRACE_ISSUED),
+                   (mk.TRACE_START, mk.TRACE_READY), (mk.TRACE_READY, mk.TRACE_END)):
+        assert bool((r[:, a_] <= r[:, b_]).all()), (a_, b_)
+    assert crec.shape == (mk.TRACE_COPY_RECORDS, mk.TRACE_WORDS)
+    assert not bool(((crec[:, mk.TRACE_ID] >> 32) == e).any())   # the dispatch writes none
