@@ -25,6 +25,10 @@
 #include "mk_internal.h"
 #include "mk_ptx.cuh"
 
+#ifndef MK_MOE_COPY_WARPS
+#define MK_MOE_COPY_WARPS 6   // copy warps per compute CTA for the MoE dispatch
+#endif
+
 namespace mk {
 
 namespace {
@@ -407,7 +411,8 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   while (pr < BM && static_cast<long long>(pr) * 2 * H * 2 <= 32768) pr *= 2;
   p.moe_rows_per_piece = pr;
   // the dispatch moves 4x the bytes of the AG copy-in: every copy warp takes part
-  p.n_cw = N_COPY_WARPS;
+  // (MK_MOE_COPY_WARPS < 6 paces the copy; two warps starved the tiles)
+  p.n_cw = std::max(1, std::min(MK_MOE_COPY_WARPS, N_COPY_WARPS));
   p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
   p.hdr = a.hdr;
