@@ -195,7 +195,9 @@ size_t mk_moe_workspace_size(int R, int E_loc, int topk, long long T, long long 
  *   y[d]       [cap_rows x N] bf16, y[d][j] = recv_x[d][j] @ w[d][local expert of j]
  * Rows past recv_counts[d] are left untouched.  If a rank would receive more
  * than cap_rows rows, nothing is dispatched for the call and the device status
- * becomes MK_ERR_CAPACITY. */
+ * becomes MK_ERR_CAPACITY.  Limits (else MK_ERR_INVALID, workspace size 0):
+ * E = R*E_loc <= 256, 1 <= topk <= min(8, E), H and N multiples of 8,
+ * R*T*topk, cap_rows, H and N below 2^31, cap_rows*H below 2^40. */
 mk_status mk_moe_dispatch_gemm(const void *const *x, const float *const *logits,
                                const void *const *w, int R, int E_loc, int topk, long long T,
                                long long H, long long N, long long cap_rows, int *topk_idx,

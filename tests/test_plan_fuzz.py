@@ -1,6 +1,6 @@
-"""Host planning of the AG / RS / AR workspaces (CPU, no launch): for random shapes
-and configs, mk_workspace_size is non-zero exactly when the arguments are valid, and
-the trace region sits after the untraced layout."""
+"""Host planning of the AG / RS / AR and MoE workspaces (CPU, no launch): for random
+shapes and configs, mk_workspace_size / mk_moe_workspace_size are non-zero exactly when
+the arguments are valid, and the trace region sits after the untraced layout."""
 import ctypes
 
 import pytest
@@ -58,3 +58,38 @@ def test_workspace_size_matches_validity(L, op, R, m, n, k, mode, reduce, wire, 
         n_rec = L.mk_trace_entries(op, R, m, n, k, ctypes.byref(c.c()), ctypes.byref(off))
         assert n_rec > 0 and off.value >= base and off.value % 256 == 0
         assert size == off.value + (n_rec + mk.TRACE_COPY_RECORDS) * 64
+
+
+def moe_valid(R, E_loc, topk, T, H, N, cap, trace):
+    if not (1 <= R <= mk.MAX_RANKS) or E_loc < 1:
+        return False
+    E = R * E_loc
+    if E > 256 or not (1 <= topk <= 8) or topk > E:
+        return False
+    if min(T, H, N, cap) < 0 or H % 8 or N % 8 or trace not in (0, 1):
+        return False
+    rows = R * T * topk
+    if rows >= 1 << 31 or cap >= 1 << 31 or H >= 1 << 31 or N >= 1 << 31 or cap * H >= 1 << 40:
+        return False
+    n_nblk = -(-N // 256)
+    return (rows // 128 + E) * n_nblk < 1 << 30
+
+
+@hyp.settings(max_examples=400, deadline=None)
+@hyp.given(R=st.integers(-1, 18), E_loc=st.integers(-1, 40), topk=st.integers(-1, 10),
+           T=st.one_of(st.integers(0, 5000), st.sampled_from([-1, 1 << 28])),
+           H=st.one_of(st.integers(0, 9000), st.sampled_from([-8, 1 << 31])),
+           N=st.one_of(st.integers(0, 9000), st.sampled_from([-8, 1 << 31])),
+           cap=st.one_of(st.integers(0, 1 << 20), st.sampled_from([-1, 1 << 31, 1 << 33])),
+           trace=st.integers(-1, 2))
+def test_moe_workspace_size_matches_validity(L, R, E_loc, topk, T, H, N, cap, trace):
+    c = mk.Config(trace=trace)
+    size = L.mk_moe_workspace_size(R, E_loc, topk, T, H, N, cap, ctypes.byref(c.c()))
+    assert (size > 0) == moe_valid(R, E_loc, topk, T, H, N, cap, trace)
+    if size and trace == 1:
+        off = ctypes.c_size_t(0)
+        n_rec = L.mk_moe_trace_entries(R, E_loc, topk, T, H, N, cap, ctypes.byref(c.c()),
+                                       ctypes.byref(off))
+        base = L.mk_moe_workspace_size(R, E_loc, topk, T, H, N, cap, None)
+        assert n_rec > 0 and off.value >= base
+        assert size >= off.value + (n_rec + mk.TRACE_COPY_RECORDS) * 64
