@@ -1,5 +1,5 @@
-"""Host planning of the AG / RS / AR and MoE workspaces (CPU, no launch): for random
-shapes and configs, mk_workspace_size / mk_moe_workspace_size are non-zero exactly when
+"""Host planning of the AG / RS / AR, MoE and ring-attention workspaces (CPU, no
+launch): for random shapes and configs the workspace sizes are non-zero exactly when
 the arguments are valid, and the trace region sits after the untraced layout."""
 import ctypes
 
@@ -93,3 +93,13 @@ def test_moe_workspace_size_matches_validity(L, R, E_loc, topk, T, H, N, cap, tr
         base = L.mk_moe_workspace_size(R, E_loc, topk, T, H, N, cap, None)
         assert n_rec > 0 and off.value >= base
         assert size >= off.value + (n_rec + mk.TRACE_COPY_RECORDS) * 64
+
+
+@hyp.settings(max_examples=300, deadline=None)
+@hyp.given(R=st.integers(-1, 10), heads=st.integers(-1, 70), s_r=st.one_of(
+               st.integers(-1, 70000), st.sampled_from([1 << 20, 1 << 24])),
+           d=st.sampled_from([64, 128, 127, 256]), causal=st.integers(0, 1))
+def test_attention_workspace_size_matches_validity(L, R, heads, s_r, d, causal):
+    size = L.mk_ring_attention_workspace_size(R, heads, s_r, d, causal, None)
+    ok = 1 <= R <= 8 and heads >= 1 and s_r >= 0 and d == 128 and heads * s_r < (1 << 31) // 128
+    assert (size > 0) == ok
