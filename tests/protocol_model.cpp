@@ -1,0 +1,493 @@
+// A CPU model of the signalling protocol of the fused kernels (test
+// infrastructure; built and run by tests/test_protocol_cpu.py).
+//
+// CTAs are std::threads.  Every wait of the kernels is a bounded spin on a
+// std::atomic, every publication the release that pairs with it, and the data
+// they order (gathered rows, running sums, hidden activations) are plain ints,
+// so ThreadSanitizer reports any access the protocol leaves unordered.  The
+// work lists follow the kernels' own orders: the AllGather copy order (remote
+// shards in ring order from local+1, local shard last), the compute order
+// (local shard first), the grouped raster, the running-sum chain's
+// part-major groups of one wave, the chained MLP's up-projection items ahead
+// of its down-projection items, and CTA pairs sharing one MMA issuer whose
+// two accumulator buffers are freed by both CTAs' epilogues.
+//
+// Roles per CTA: a producer (waits for its item's inputs, then reads them), the
+// pair's MMA issuer (one per pair: waits for both producers and for the
+// accumulator buffer), an epilogue (waits for the accumulator and, in the
+// running-sum chain, for the previous part; then publishes), and copy workers
+// (never wait once started).  Each model launch runs twice with epochs 1 and
+// 2 on the same flags, as back-to-back calls on one workspace do.
+//
+//   protocol_model ag  R m_r n_nblk n_pairs pair n_cw rows_per_piece local copy_local [bug]
+//   protocol_model rs  R m n_nblk n_ctas pair group_m [bug]
+//   protocol_model mlp R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
+// with an optional last argument wait=S (the wait bound, default 20 s).
+// Prints "OK" and exits 0, or exits 2 on a wait that gives up (a deadlock in
+// the modelled protocol) and 3 on wrong data.  Planted mistakes, for the
+// tests that the model catches them: ag bug "relaxed" makes the copy workers
+// publish with relaxed increments (the race a missing fence would be); rs bug
+// "reversed" runs each group's parts in descending order (a chain that waits
+// on work queued behind it).
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <functional>
+#include <string>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int BM = 128;      // rows of a CTA's tile
+constexpr int KW = 4;        // model words per matrix row
+double g_wait_s = 20.0;        // bound of every wait (seconds; argument "wait=S")
+
+std::atomic<int> g_fail{0};
+
+// Bounded wait until pred() holds (the kernels bound every wait in time).
+bool wait_until(const std::function<bool()>& pred, const char* what, long long who) {
+  const auto t0 = std::chrono::steady_clock::now();
+  while (!pred()) {
+    if (g_fail.load(std::memory_order_relaxed)) return false;
+    if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > g_wait_s) {
+      std::fprintf(stderr, "wait gave up: %s (%lld)\n", what, who);
+      g_fail.store(2);
+      return false;
+    }
+    std::this_thread::yield();
+  }
+  return true;
+}
+
+void fail_data(const char* what, long long a, long long b) {
+  std::fprintf(stderr, "wrong data: %s (%lld vs %lld)\n", what, a, b);
+  int z = 0;
+  g_fail.compare_exchange_strong(z, 3);
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Grouped raster over (m-position, n-block).
+void raster(int q, int group_m, int n_mrow, int n_nblk, int& mb, int& nb) {
+  const int per_group = group_m * n_nblk;
+  const int g = q / per_group;
+  const int first_m = g * group_m;
+  const int gsz = std::min(n_mrow - first_m, group_m);
+  const int r = q - g * per_group;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+// One modelled launch: n_units CTA units (a pair or a single CTA), each with
+// `halves` producer/epilogue threads, one MMA issuer, and copy workers.
+struct Item {
+  bool empty = false;
+  std::function<bool()> inputs;     // producer: wait for and read the inputs
+  std::function<bool()> epilogue;   // epilogue: chain wait, store, publish
+};
+
+struct Launch {
+  int n_units = 1, halves = 1, n_items = 0, n_cw = 0;
+  std::function<Item(int item, int half)> decode;
+  std::function<void(int worker, int n_workers)> copy;      // copy worker body
+  std::function<void()> prologue;                           // the ticket-0 CTA's counter reset
+
+  void run(uint32_t epoch, std::atomic<uint32_t>& ready) {
+    std::vector<std::thread> th;
+    // per unit: items loaded per half, accumulators issued, epilogues done per half
+    struct Unit {
+      std::atomic<int> loaded[2];
+      std::atomic<int> issued{0};
+      std::atomic<int> done[2];
+      Unit() { loaded[0] = loaded[1] = done[0] = done[1] = 0; }
+    };
+    std::vector<Unit> units(n_units);
+    auto my_items = [&](int u) {
+      std::vector<int> v;
+      for (int i = u; i < n_items; i += n_units) v.push_back(i);
+      return v;
+    };
+    for (int u = 0; u < n_units; ++u) {
+      for (int h = 0; h < halves; ++h) {
+        // producer
+        th.emplace_back([&, u, h] {
+          if (u == 0 && h == 0 && prologue) {
+            prologue();
+            ready.store(epoch, std::memory_order_release);
+          }
+          if (!wait_until([&] { return ready.load(std::memory_order_acquire) == epoch; }, "ready", u)) return;
+          int k = 0;
+          for (int i : my_items(u)) {
+            // the operand ring holds less than an item: item k+1's loads start once
+            // the MMAs of item k have been issued
+            if (!wait_until([&] { return units[u].issued.load(std::memory_order_acquire) >= k; }, "ring", i))
+              return;
+            Item it = decode(i, h);
+            if (!it.empty && it.inputs && !it.inputs()) return;
+            units[u].loaded[h].store(++k, std::memory_order_release);
+          }
+        });
+        // epilogue
+        th.emplace_back([&, u, h] {
+          int k = 0;
+          for (int i : my_items(u)) {
+            ++k;
+            if (!wait_until([&] { return units[u].issued.load(std::memory_order_acquire) >= k; }, "accumulator", i))
+              return;
+            Item it = decode(i, h);
+            if (!it.empty && it.epilogue && !it.epilogue()) return;
+            units[u].done[h].store(k, std::memory_order_release);
+          }
+        });
+      }
+      // the unit's MMA issuer: both halves loaded, and the accumulator buffer of
+      // two items back drained by both epilogues
+      th.emplace_back([&, u] {
+        int k = 0;
+        for (int i : my_items(u)) {
+          ++k;
+          for (int h = 0; h < halves; ++h) {
+            if (!wait_until([&] { return units[u].loaded[h].load(std::memory_order_acquire) >= k; }, "loads", i)) return;
+            if (!wait_until([&] { return units[u].done[h].load(std::memory_order_acquire) >= k - 2; }, "tmem", i)) return;
+          }
+          units[u].issued.store(k, std::memory_order_release);
+        }
+      });
+      // copy workers of the unit's CTAs
+      for (int h = 0; h < halves && copy; ++h)
+        for (int w = 0; w < n_cw; ++w)
+          th.emplace_back([&, u, h, w] {
+            if (!wait_until([&] { return ready.load(std::memory_order_acquire) == epoch; }, "ready", u)) return;
+            copy((u * halves + h) * n_cw + w, n_units * halves * n_cw);
+          });
+    }
+    for (auto& t : th) t.join();
+  }
+};
+
+int arg(char** argv, int i) { return std::atoi(argv[i]); }
+
+// ------------------------------------------------------------------ AllGather + GEMM
+int run_ag(int argc, char** argv) {
+  if (argc < 11) return 64;
+  const int R = arg(argv, 2), m_r = arg(argv, 3), n_nblk = arg(argv, 4), n_units = arg(argv, 5);
+  const int pair = arg(argv, 6), n_cw = arg(argv, 7), pr = arg(argv, 8), local = arg(argv, 9);
+  const int copy_local = arg(argv, 10);
+  const bool relaxed = argc > 11 && std::string(argv[11]) == "relaxed";
+  const int M = R * m_r, n_mblk = ceil_div(M, BM);
+  const bool ordered = m_r % BM == 0;
+  const int bps = m_r / BM;
+  const int n_chunks = ordered ? (copy_local ? R : R - 1) * bps : n_mblk;
+  const int J = BM / pr;
+  auto shard_val = [](int s, int row, int w) { return s * 1000003 + row * 131 + w; };
+  std::vector<int> gathered(static_cast<size_t>(M) * KW, -1);
+  auto reset_gathered = [&] {
+    std::fill(gathered.begin(), gathered.end(), -1);
+    if (!copy_local)   // the local block of the gathered A is the local shard itself
+      for (int row = 0; row < m_r; ++row)
+        for (int w = 0; w < KW; ++w)
+          gathered[(static_cast<size_t>(local) * m_r + row) * KW + w] = shard_val(local, row, w);
+  };
+  std::vector<std::atomic<uint32_t>> cnt(n_mblk);
+  std::vector<int> c_tiles(static_cast<size_t>(n_mblk) * n_nblk, 0);
+  std::atomic<uint32_t> ready{0};
+  auto copy_mb = [&](int c) { return ordered ? ((local + 1 + c / bps) % R) * bps + c % bps : c; };
+  auto compute_mb = [&](int pos) { return ordered ? ((local + pos / bps) % R) * bps + pos % bps : pos; };
+  auto pieces = [&](int mb) { return ceil_div(std::min(BM, M - mb * BM), pr); };
+  auto fully_local = [&](int mb) {
+    const int lo = mb * BM, hi = std::min(lo + BM, M);
+    return lo >= local * m_r && hi <= (local + 1) * m_r;
+  };
+  Launch L;
+  L.n_units = n_units;
+  L.halves = pair ? 2 : 1;
+  L.n_cw = n_cw;
+  const int n_mrow = pair ? (n_mblk + 1) / 2 : n_mblk;
+  L.n_items = n_mrow * n_nblk;
+  L.prologue = [&] { for (auto& c : cnt) c.store(0, std::memory_order_relaxed); };
+  L.copy = [&](int worker, int n_workers) {
+    for (long long pc = worker; pc < static_cast<long long>(n_chunks) * J; pc += n_workers) {
+      const int c = static_cast<int>(pc / J), j = static_cast<int>(pc % J);
+      const int mb = copy_mb(c);
+      if (j >= pieces(mb)) continue;
+      const int lo = mb * BM + j * pr, hi = std::min({lo + pr, (mb + 1) * BM, M});
+      for (int row = lo; row < hi; ++row) {
+        const int s = row / m_r;
+        if (s == local && !copy_local) continue;
+        for (int w = 0; w < KW; ++w) gathered[static_cast<size_t>(row) * KW + w] = shard_val(s, row - s * m_r, w);
+      }
+      cnt[mb].fetch_add(1, relaxed ? std::memory_order_relaxed : std::memory_order_release);
+    }
+  };
+  L.decode = [&](int i, int half) {
+    Item it;
+    int pos = i / n_nblk;
+    const int nb = i % n_nblk;
+    if (pair) pos = 2 * pos + half;
+    if (pos >= n_mblk) {
+      it.empty = true;
+      return it;
+    }
+    const int mb = compute_mb(pos);
+    it.inputs = [&, mb, i] {
+      if (!fully_local(mb)) {
+        const uint32_t want = static_cast<uint32_t>(pieces(mb));
+        if (!wait_until([&] { return cnt[mb].load(std::memory_order_acquire) == want; }, "chunk", i)) return false;
+      }
+      for (int row = mb * BM; row < std::min((mb + 1) * BM, M); ++row) {
+        const int s = row / m_r;
+        for (int w = 0; w < KW; ++w) {
+          const int got = fully_local(mb) ? shard_val(s, row - s * m_r, w) : gathered[static_cast<size_t>(row) * KW + w];
+          if (got != shard_val(s, row - s * m_r, w)) {
+            fail_data("gathered row", got, shard_val(s, row - s * m_r, w));
+            return false;
+          }
+        }
+      }
+      return true;
+    };
+    it.epilogue = [&, mb, nb] {
+      c_tiles[static_cast<size_t>(mb) * n_nblk + nb] += 1;
+      return true;
+    };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    reset_gathered();
+    L.run(e, ready);
+  }
+  for (size_t t = 0; t < c_tiles.size() && !g_fail.load(); ++t)
+    if (c_tiles[t] != 2) fail_data("output tile stores", c_tiles[t], 2);
+  return g_fail.load();
+}
+
+// ------------------------------------------------------------------ the running-sum chain
+struct Chain {
+  int P, n_mblk, n_nblk, n_mrow, n_sched, G, group_m, pair;
+  std::vector<std::atomic<uint32_t>>* flags;
+  std::vector<long long>* sums;
+  std::vector<long long>* out;
+  bool reversed = false;   // planted mistake: the parts of a group in descending order
+  // item -> (mb, nb, part), or empty half
+  bool decode(int i, int half, int& mb, int& nb, int& part) const {
+    const int g = i / (G * P);
+    const int Gg = std::min(G, n_sched - g * G);
+    const int iin = i - g * G * P;
+    part = iin / Gg;
+    const int q_in = iin - part * Gg;
+    if (reversed) part = P - 1 - part;
+    const int q = g * G + q_in;
+    raster(q, group_m, n_mrow, n_nblk, mb, nb);
+    if (pair) mb = 2 * mb + half;
+    return mb < n_mblk;
+  }
+  static long long partial(int tile, int part) { return 1000LL * tile + 7 * part + 1; }
+  // epilogue of (tile, part): wait for part-1, add, store or forward, release
+  bool epilogue(int mb, int nb, int part, uint32_t epoch, int item) const {
+    const int tile = mb * n_nblk + nb;
+    const size_t slot = static_cast<size_t>(tile) * P + part;
+    if (part > 0 && !wait_until([&] { return (*flags)[slot - 1].load(std::memory_order_acquire) == epoch; },
+                                "chain", item))
+      return false;
+    const long long s = (part > 0 ? (*sums)[tile] : 0) + partial(tile, part);
+    if (part == P - 1) (*out)[tile] = s;
+    else (*sums)[tile] = s;
+    (*flags)[slot].store(epoch, std::memory_order_release);
+    return true;
+  }
+  bool check() const {
+    for (int t = 0; t < n_mblk * n_nblk; ++t) {
+      long long want = 0;
+      for (int p = 0; p < P; ++p) want += partial(t, p);
+      if ((*out)[t] != want) {
+        fail_data("reduced tile", (*out)[t], want);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+int run_rs(int argc, char** argv) {
+  if (argc < 8) return 64;
+  const int R = arg(argv, 2), m = arg(argv, 3), n_nblk = arg(argv, 4), n_ctas = arg(argv, 5);
+  const int pair = arg(argv, 6), group_m = arg(argv, 7);
+  const int n_mblk = ceil_div(m, BM);
+  std::vector<std::atomic<uint32_t>> flags(static_cast<size_t>(n_mblk) * n_nblk * R);
+  std::vector<long long> sums(static_cast<size_t>(n_mblk) * n_nblk), out(sums.size());
+  Chain ch;
+  ch.P = R;
+  ch.n_mblk = n_mblk;
+  ch.n_nblk = n_nblk;
+  ch.pair = pair;
+  ch.group_m = group_m;
+  ch.n_mrow = pair ? (n_mblk + 1) / 2 : n_mblk;
+  ch.n_sched = ch.n_mrow * n_nblk;
+  const int n_units = pair ? std::max(1, n_ctas / 2) : n_ctas;
+  ch.G = std::max(1, std::min(n_units, ch.n_sched));
+  ch.flags = &flags;
+  ch.sums = &sums;
+  ch.out = &out;
+  ch.reversed = argc > 8 && std::string(argv[8]) == "reversed";
+  std::atomic<uint32_t> ready{0};
+  Launch L;
+  L.n_units = n_units;
+  L.halves = pair ? 2 : 1;
+  L.n_items = ch.n_sched * ch.P;
+  L.prologue = [] {};
+  uint32_t epoch = 0;
+  L.decode = [&](int i, int half) {
+    Item it;
+    int mb, nb, part;
+    if (!ch.decode(i, half, mb, nb, part)) {
+      it.empty = true;
+      return it;
+    }
+    it.epilogue = [&, mb, nb, part, i] { return ch.epilogue(mb, nb, part, epoch, i); };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    epoch = e;
+    std::fill(out.begin(), out.end(), 0);
+    L.run(e, ready);
+    if (!g_fail.load()) ch.check();
+  }
+  return g_fail.load();
+}
+
+// ------------------------------------------------------------------ the chained MLP
+int run_mlp(int argc, char** argv) {
+  if (argc < 10) return 64;
+  const int R = arg(argv, 2), m = arg(argv, 3), f_nblk = arg(argv, 4), h_nblk = arg(argv, 5);
+  const int n_ctas = arg(argv, 6), pair = arg(argv, 7), n_cw = arg(argv, 8), pr = arg(argv, 9);
+  const int M = R * m, n_mblk = ceil_div(M, BM);
+  const int n_mrow = pair ? (n_mblk + 1) / 2 : n_mblk;
+  const int n_units = pair ? std::max(1, n_ctas / 2) : n_ctas;
+  const int J = BM / pr;
+  auto x_val = [](int row, int w) { return row * 17 + w + 5; };
+  auto h_val = [](int r, int row, int nb) { return r * 7919 + row * 3 + nb; };
+  std::vector<int> xg(static_cast<size_t>(M) * KW, -1);
+  std::vector<int> hid(static_cast<size_t>(R) * M * f_nblk, -1);
+  std::vector<std::atomic<uint32_t>> chunk(n_mblk), hcnt(static_cast<size_t>(R) * n_mblk);
+  std::vector<std::atomic<uint32_t>> flags(static_cast<size_t>(n_mblk) * h_nblk * R);
+  std::vector<long long> sums(static_cast<size_t>(n_mblk) * h_nblk), out(sums.size());
+  auto pieces = [&](int mb) { return ceil_div(std::min(BM, M - mb * BM), pr); };
+  Chain ch;
+  ch.P = R;
+  ch.n_mblk = n_mblk;
+  ch.n_nblk = h_nblk;
+  ch.pair = pair;
+  ch.group_m = 8;
+  ch.n_mrow = n_mrow;
+  ch.n_sched = n_mrow * h_nblk;
+  ch.G = std::max(1, std::min(n_units, ch.n_sched));
+  ch.flags = &flags;
+  ch.sums = &sums;
+  ch.out = &out;
+  const int n1 = n_mrow * R * f_nblk;
+  std::atomic<uint32_t> ready{0};
+  uint32_t epoch = 0;
+  Launch L;
+  L.n_units = n_units;
+  L.halves = pair ? 2 : 1;
+  L.n_cw = n_cw;
+  L.n_items = n1 + ch.n_sched * ch.P;
+  L.prologue = [&] {
+    for (auto& c : chunk) c.store(0, std::memory_order_relaxed);
+    for (auto& c : hcnt) c.store(0, std::memory_order_relaxed);
+  };
+  L.copy = [&](int worker, int n_workers) {
+    for (long long pc = worker; pc < static_cast<long long>(n_mblk) * J; pc += n_workers) {
+      const int mb = static_cast<int>(pc / J), j = static_cast<int>(pc % J);
+      if (j >= pieces(mb)) continue;
+      const int lo = mb * BM + j * pr, hi = std::min({lo + pr, (mb + 1) * BM, M});
+      for (int row = lo; row < hi; ++row)
+        for (int w = 0; w < KW; ++w) xg[static_cast<size_t>(row) * KW + w] = x_val(row, w);
+      chunk[mb].fetch_add(1, std::memory_order_release);
+    }
+  };
+  L.decode = [&](int i, int half) {
+    Item it;
+    if (i < n1) {   // up-projection: (m-position, rank, n-block), n-block innermost
+      const int per_m = R * f_nblk;
+      int pos = i / per_m;
+      const int r = (i % per_m) / f_nblk, nb = i % f_nblk;
+      if (pair) pos = 2 * pos + half;
+      if (pos >= n_mblk) {
+        it.empty = true;
+        return it;
+      }
+      const int mb = pos;
+      it.inputs = [&, mb, i] {
+        const uint32_t want = static_cast<uint32_t>(pieces(mb));
+        if (!wait_until([&] { return chunk[mb].load(std::memory_order_acquire) == want; }, "x chunk", i)) return false;
+        for (int row = mb * BM; row < std::min((mb + 1) * BM, M); ++row)
+          if (xg[static_cast<size_t>(row) * KW] != x_val(row, 0)) {
+            fail_data("gathered x", xg[static_cast<size_t>(row) * KW], x_val(row, 0));
+            return false;
+          }
+        return true;
+      };
+      it.epilogue = [&, mb, r, nb] {
+        for (int row = mb * BM; row < std::min((mb + 1) * BM, M); ++row)
+          hid[(static_cast<size_t>(r) * M + row) * f_nblk + nb] = h_val(r, row, nb);
+        hcnt[static_cast<size_t>(r) * n_mblk + mb].fetch_add(1, std::memory_order_release);
+        return true;
+      };
+      return it;
+    }
+    int mb, nb, part;
+    if (!ch.decode(i - n1, half, mb, nb, part)) {
+      it.empty = true;
+      return it;
+    }
+    const int r = part;   // one part per rank
+    it.inputs = [&, mb, r, i] {
+      if (!wait_until([&] {
+            return hcnt[static_cast<size_t>(r) * n_mblk + mb].load(std::memory_order_acquire) ==
+                   static_cast<uint32_t>(f_nblk);
+          }, "hidden block", i))
+        return false;
+      for (int row = mb * BM; row < std::min((mb + 1) * BM, M); ++row)
+        for (int fb = 0; fb < f_nblk; ++fb)
+          if (hid[(static_cast<size_t>(r) * M + row) * f_nblk + fb] != h_val(r, row, fb)) {
+            fail_data("hidden rows", hid[(static_cast<size_t>(r) * M + row) * f_nblk + fb], h_val(r, row, fb));
+            return false;
+          }
+      return true;
+    };
+    it.epilogue = [&, mb, nb, part, i] { return ch.epilogue(mb, nb, part, epoch, i); };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    epoch = e;
+    std::fill(out.begin(), out.end(), 0);
+    std::fill(hid.begin(), hid.end(), -1);
+    std::fill(xg.begin(), xg.end(), -1);
+    L.run(e, ready);
+    if (!g_fail.load()) ch.check();
+  }
+  return g_fail.load();
+}
+
+}  // namespace
+
+int main(int argc, char** argv) {
+  // a trailing "wait=S" sets the wait bound
+  if (argc > 2 && std::strncmp(argv[argc - 1], "wait=", 5) == 0) {
+    g_wait_s = std::atof(argv[argc - 1] + 5);
+    --argc;
+  }
+  if (argc < 2) return 64;
+  const std::string op = argv[1];
+  int rc = 64;
+  if (op == "ag") rc = run_ag(argc, argv);
+  else if (op == "rs") rc = run_rs(argc, argv);
+  else if (op == "mlp") rc = run_mlp(argc, argv);
+  if (rc == 0) std::printf("OK\n");
+  return rc;
+}
