@@ -9,7 +9,8 @@
 // shards in ring order from local+1, local shard last), the compute order
 // (local shard first), the grouped raster, the running-sum chain's
 // part-major groups of one wave, the chained MLP's up-projection items ahead
-// of its down-projection items, and CTA pairs sharing one MMA issuer whose
+// of its down-projection items, the MoE tile table in (rank, expert, row tile,
+// column block) order, and CTA pairs sharing one MMA issuer whose
 // two accumulator buffers are freed by both CTAs' epilogues.
 //
 // Roles per CTA: a producer (waits for its item's inputs, then reads them), the
@@ -22,6 +23,7 @@
 //   protocol_model ag  R m_r n_nblk n_pairs pair n_cw rows_per_piece local copy_local [bug]
 //   protocol_model rs  R m n_nblk n_ctas pair group_m [bug]
 //   protocol_model mlp R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
+//   protocol_model moe R E_loc n_nblk n_units pair n_cw rows_per_piece seed
 // with an optional last argument wait=S (the wait bound, default 20 s).
 // Prints "OK" and exits 0, or exits 2 on a wait that gives up (a deadlock in
 // the modelled protocol) and 3 on wrong data.  Planted mistakes, for the
@@ -474,6 +476,110 @@ int run_mlp(int argc, char** argv) {
   return g_fail.load();
 }
 
+// ------------------------------------------------------------------ MoE dispatch + grouped GEMM
+// Expert segments of random sizes; the tile table lists, for each (rank d,
+// local expert l) in order, its row tiles (128 rows, or 256 with CTA pairs)
+// times the column blocks; copy workers move the received rows of every rank
+// in pieces and count them per 128-row block; a tile waits until every block
+// it covers holds all its rows.  The counters are zeroed by an earlier launch.
+int run_moe(int argc, char** argv) {
+  if (argc < 10) return 64;
+  const int R = arg(argv, 2), E_loc = arg(argv, 3), n_nblk = arg(argv, 4), n_units = arg(argv, 5);
+  const int pair = arg(argv, 6), n_cw = arg(argv, 7), pr = arg(argv, 8);
+  unsigned seed = static_cast<unsigned>(arg(argv, 9));
+  auto rnd = [&] { seed = seed * 1103515245u + 12345u; return (seed >> 8) % 1000u; };
+  const int tile_rows = pair ? 2 * BM : BM;
+  std::vector<int> seg(static_cast<size_t>(R) * E_loc), segoff(static_cast<size_t>(R) * (E_loc + 1));
+  std::vector<int> rc(R, 0);
+  for (int d = 0; d < R; ++d) {
+    for (int l = 0; l < E_loc; ++l) {
+      const unsigned u = rnd();
+      seg[static_cast<size_t>(d) * E_loc + l] = u < 150 ? 0 : static_cast<int>(u % 700);   // some empty experts
+      segoff[static_cast<size_t>(d) * (E_loc + 1) + l] = rc[d];
+      rc[d] += seg[static_cast<size_t>(d) * E_loc + l];
+    }
+    segoff[static_cast<size_t>(d) * (E_loc + 1) + E_loc] = rc[d];
+  }
+  struct Ent { int d, first, rows, nb; };
+  std::vector<Ent> table;
+  for (int d = 0; d < R; ++d)
+    for (int l = 0; l < E_loc; ++l) {
+      const int tot = seg[static_cast<size_t>(d) * E_loc + l];
+      for (int mi = 0; mi < ceil_div(tot, tile_rows); ++mi)
+        for (int nb = 0; nb < n_nblk; ++nb)
+          table.push_back({d, segoff[static_cast<size_t>(d) * (E_loc + 1) + l] + mi * tile_rows,
+                           std::min(tile_rows, tot - mi * tile_rows), nb});
+    }
+  auto row_val = [](int d, int row) { return d * 100003 + row * 7 + 1; };
+  std::vector<std::vector<int>> recv(R);
+  std::vector<int> nblk(R);
+  std::vector<std::vector<std::atomic<uint32_t>>> cnt(R);
+  for (int d = 0; d < R; ++d) {
+    recv[d].assign(static_cast<size_t>(std::max(rc[d], 1)), -1);
+    nblk[d] = ceil_div(std::max(rc[d], 1), BM);
+    cnt[d] = std::vector<std::atomic<uint32_t>>(nblk[d]);
+  }
+  std::vector<int> y(table.size() * 2, 0);
+  long long total_pieces = 0;
+  for (int d = 0; d < R; ++d) total_pieces += ceil_div(rc[d], pr);
+  std::atomic<uint32_t> ready{0};
+  Launch L;
+  L.n_units = n_units;
+  L.halves = pair ? 2 : 1;
+  L.n_cw = n_cw;
+  L.n_items = static_cast<int>(table.size());
+  L.prologue = [] {};
+  L.copy = [&](int worker, int n_workers) {
+    for (long long q = worker; q < total_pieces; q += n_workers) {
+      int d = 0;
+      long long j = q;
+      while (j >= ceil_div(rc[d], pr)) j -= ceil_div(rc[d++], pr);
+      const int row0 = static_cast<int>(j) * pr, rows = std::min(pr, rc[d] - row0);
+      for (int r = 0; r < rows; ++r) recv[d][row0 + r] = row_val(d, row0 + r);
+      cnt[d][row0 / BM].fetch_add(static_cast<uint32_t>(rows), std::memory_order_release);
+    }
+  };
+  L.decode = [&](int i, int half) {
+    Item it;
+    const Ent& e = table[i];
+    const int first = e.first + half * BM, rows = std::min(BM, e.rows - half * BM);
+    if (rows <= 0) {
+      it.empty = true;
+      return it;
+    }
+    const int d = e.d;
+    it.inputs = [&, d, first, rows, i] {
+      for (int b = first / BM; b <= (first + rows - 1) / BM; ++b) {
+        const uint32_t want = static_cast<uint32_t>(std::min(BM, rc[d] - b * BM));
+        if (!wait_until([&] { return cnt[d][b].load(std::memory_order_acquire) == want; }, "rows", i)) return false;
+      }
+      for (int r = first; r < first + rows; ++r)
+        if (recv[d][r] != row_val(d, r)) {
+          fail_data("received row", recv[d][r], row_val(d, r));
+          return false;
+        }
+      return true;
+    };
+    it.epilogue = [&, i, half] {
+      y[static_cast<size_t>(i) * 2 + half] += 1;
+      return true;
+    };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    for (int d = 0; d < R; ++d) {   // the offsets launch zeroes the block counters
+      for (auto& c : cnt[d]) c.store(0, std::memory_order_relaxed);
+      std::fill(recv[d].begin(), recv[d].end(), -1);
+    }
+    ready.store(e, std::memory_order_release);
+    L.run(e, ready);
+  }
+  for (size_t i = 0; i < table.size() && !g_fail.load(); ++i)
+    for (int h = 0; h < L.halves; ++h)
+      if (std::min(BM, table[i].rows - h * BM) > 0 && y[i * 2 + h] != 2) fail_data("expert tile stores", y[i * 2 + h], 2);
+  return g_fail.load();
+}
+
 }  // namespace
 
 int main(int argc, char** argv) {
@@ -488,6 +594,7 @@ int main(int argc, char** argv) {
   if (op == "ag") rc = run_ag(argc, argv);
   else if (op == "rs") rc = run_rs(argc, argv);
   else if (op == "mlp") rc = run_mlp(argc, argv);
+  else if (op == "moe") rc = run_moe(argc, argv);
   if (rc == 0) std::printf("OK\n");
   return rc;
 }

@@ -2,8 +2,8 @@
 
 Threads stand for the CTAs' roles, atomics for the flags and counters, and the
 work lists follow the kernels' orders (see the model's header).  Checked here:
-every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain
-and the chained MLP completes (no wait gives up) and reads exactly the data its
+every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain,
+the chained MLP and the MoE dispatch completes (no wait gives up) and reads exactly the data its
 producers published, twice on the same flags (epochs 1 and 2); ThreadSanitizer
 finds no access the protocol leaves unordered.  Two planted mistakes show that
 the model catches what it is for: copy workers that publish with relaxed
@@ -31,6 +31,11 @@ RS = [  # R m n_nblk n_ctas pair group_m
     "2 256 2 2 0 8",
     "8 1024 4 6 1 2",
     "3 384 5 16 0 8",             # more CTAs than tiles
+]
+MOE = [  # R E_loc n_nblk n_units pair n_cw rows_per_piece seed
+    "4 3 2 3 1 6 32 7",           # pairs: 256-row tiles, empty experts
+    "2 4 3 5 0 2 64 11",
+    "8 2 1 8 1 6 16 3",
 ]
 MLP = [  # R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
     "4 256 2 3 6 1 2 32",
@@ -76,14 +81,15 @@ def _run(exe, op, args, timeout=240):
 
 
 @pytest.mark.parametrize("op,args", [("ag", a) for a in AG] + [("rs", a) for a in RS] +
-                         [("mlp", a) for a in MLP])
+                         [("mlp", a) for a in MLP] + [("moe", a) for a in MOE])
 def test_protocol_completes_with_the_published_data(model, op, args):
     r = _run(model, op, args)
     assert r.returncode == 0 and r.stdout.strip() == "OK", (r.returncode, r.stderr[-2000:])
 
 
 @pytest.mark.parametrize("op,args", [("ag", AG[0]), ("ag", AG[1]), ("ag", AG[2]), ("rs", RS[0]),
-                                     ("rs", RS[2]), ("mlp", MLP[0]), ("mlp", MLP[1])])
+                                     ("rs", RS[2]), ("mlp", MLP[0]), ("mlp", MLP[1]),
+                                     ("moe", MOE[0]), ("moe", MOE[1])])
 def test_protocol_has_no_unordered_access(model_tsan, op, args):
     r = _run(model_tsan, op, args)
     assert "ThreadSanitizer" not in r.stderr, r.stderr[-3000:]
