@@ -10,7 +10,7 @@
 // (local shard first), the grouped raster, the running-sum chain's
 // part-major groups of one wave, the chained MLP's up-projection items ahead
 // of its down-projection items, the MoE tile table in (rank, expert, row tile,
-// column block) order, and CTA pairs sharing one MMA issuer whose
+// column block) order, the combine's hand-over ring, and CTA pairs sharing one MMA issuer whose
 // two accumulator buffers are freed by both CTAs' epilogues.
 //
 // Roles per CTA: a producer (waits for its item's inputs, then reads them), the
@@ -24,13 +24,15 @@
 //   protocol_model rs  R m n_nblk n_ctas pair group_m [bug]
 //   protocol_model mlp R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
 //   protocol_model moe R E_loc n_nblk n_units pair n_cw rows_per_piece seed
+//   protocol_model combine R T topk n_nblk n_ctas n_cw ring_entries seed [bug]
 // with an optional last argument wait=S (the wait bound, default 20 s).
 // Prints "OK" and exits 0, or exits 2 on a wait that gives up (a deadlock in
 // the modelled protocol) and 3 on wrong data.  Planted mistakes, for the
 // tests that the model catches them: ag bug "relaxed" makes the copy workers
 // publish with relaxed increments (the race a missing fence would be); rs bug
 // "reversed" runs each group's parts in descending order (a chain that waits
-// on work queued behind it).
+// on work queued behind it); combine bug "earlyfree" frees a ring entry before
+// reading it (a race with the next lap's writer).
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -580,6 +582,137 @@ int run_moe(int argc, char** argv) {
   return g_fail.load();
 }
 
+// ------------------------------------------------------------------ MoE combine
+// Every (token, slot) row of every column block is produced by some tile's
+// epilogue, which stores it into ret[r][t][slot] and counts it in the (token,
+// column block) counter (a release after the stores); the row that completes
+// a count hands (token, column block) to its CTA's copy warps through a ring
+// of `cap` entries whose sequence word is 2s when entry s is free and 2s + 1
+// when full.  A copy warp claims up to 8 entries at a time (tail / claim
+// counters), frees each entry for the next lap, then sums the token's slots;
+// it leaves when its CTA's epilogue is done and every entry is claimed.
+int run_combine(int argc, char** argv) {
+  if (argc < 9) return 64;
+  const int R = arg(argv, 2), T = arg(argv, 3), topk = arg(argv, 4), n_nblk = arg(argv, 5);
+  const int n_units = arg(argv, 6), n_cw = arg(argv, 7), cap = arg(argv, 8);
+  unsigned seed = argc > 9 ? static_cast<unsigned>(arg(argv, 9)) : 1u;
+  const bool early_free = argc > 10 && std::string(argv[10]) == "earlyfree";
+  auto rnd = [&] { seed = seed * 1103515245u + 12345u; return seed >> 8; };
+  const int n_tok = R * T, n_rows = n_tok * topk;
+  std::vector<int> order(n_rows);   // the dispatch order of the (token, slot) rows
+  for (int i = 0; i < n_rows; ++i) order[i] = i;
+  for (int i = n_rows - 1; i > 0; --i) std::swap(order[i], order[rnd() % (i + 1)]);
+  const int n_tiles = ceil_div(n_rows, BM);
+  auto val = [](int g, int k, int nb) { return g * 31 + k * 7 + nb + 1; };
+  std::vector<int> ret(static_cast<size_t>(n_rows) * n_nblk, 0), out(static_cast<size_t>(n_tok) * n_nblk, 0);
+  std::vector<int> writes(out.size(), 0);
+  std::vector<std::atomic<uint32_t>> cnt(out.size());
+  struct Ring {
+    std::vector<std::atomic<uint32_t>> seq;
+    std::vector<int> payload;
+    std::atomic<uint32_t> tail{0}, claim{0}, done{0};
+  };
+  std::vector<Ring> rings(n_units);
+  for (auto& rg : rings) {
+    rg.seq = std::vector<std::atomic<uint32_t>>(cap);
+    rg.payload.assign(static_cast<size_t>(cap) * 2, 0);
+  }
+  Launch L;
+  L.n_units = n_units;
+  L.halves = 1;
+  L.n_items = n_tiles * n_nblk;
+  L.n_cw = n_cw;
+  std::atomic<uint32_t> ready{0};
+  std::vector<std::atomic<int>> epi_left(n_units);
+  L.prologue = [] {};
+  L.decode = [&](int i, int) {
+    Item it;
+    const int tile = i / n_nblk, nb = i % n_nblk;
+    const int u = i % n_units;
+    it.epilogue = [&, tile, nb, u, i] {
+      Ring& rg = rings[u];
+      for (int j = tile * BM; j < std::min((tile + 1) * BM, n_rows); ++j) {
+        const int g = order[j] / topk, k = order[j] % topk;
+        ret[static_cast<size_t>(order[j]) * n_nblk + nb] = val(g, k, nb);
+        const uint32_t before = cnt[static_cast<size_t>(g) * n_nblk + nb].fetch_add(1, std::memory_order_acq_rel);
+        if (before != static_cast<uint32_t>(topk - 1)) continue;
+        const uint32_t slot = rg.tail.fetch_add(1, std::memory_order_acq_rel);
+        if (!wait_until([&] { return rg.seq[slot % cap].load(std::memory_order_acquire) == 2u * slot; }, "ring free", i))
+          return false;
+        rg.payload[(slot % cap) * 2] = g;
+        rg.payload[(slot % cap) * 2 + 1] = nb;
+        rg.seq[slot % cap].store(2u * slot + 1u, std::memory_order_release);
+      }
+      if (epi_left[u].fetch_sub(1, std::memory_order_acq_rel) == 1) rg.done.store(1, std::memory_order_release);
+      return true;
+    };
+    return it;
+  };
+  L.copy = [&](int worker, int) {
+    Ring& rg = rings[worker / n_cw];
+    const auto t0 = std::chrono::steady_clock::now();
+    while (true) {
+      const uint32_t done = rg.done.load(std::memory_order_acquire);
+      const uint32_t tail = rg.tail.load(std::memory_order_acquire);
+      uint32_t claim = rg.claim.load(std::memory_order_acquire);
+      if (claim < tail) {
+        const uint32_t n = std::min(8u, tail - claim);
+        if (!rg.claim.compare_exchange_strong(claim, claim + n, std::memory_order_acq_rel)) continue;
+        std::vector<std::pair<int, int>> got;
+        for (uint32_t s = claim; s < claim + n; ++s) {
+          if (!wait_until([&] { return rg.seq[s % cap].load(std::memory_order_acquire) == 2u * s + 1u; },
+                          "ring full", static_cast<long long>(s)))
+            return;
+          if (early_free) rg.seq[s % cap].store(2u * (s + static_cast<uint32_t>(cap)), std::memory_order_release);
+          got.emplace_back(rg.payload[(s % cap) * 2], rg.payload[(s % cap) * 2 + 1]);
+          if (!early_free) rg.seq[s % cap].store(2u * (s + static_cast<uint32_t>(cap)), std::memory_order_release);
+        }
+        for (auto [g, nb] : got) {
+          int sum = 0;
+          for (int k = 0; k < topk; ++k) sum += ret[static_cast<size_t>(g * topk + k) * n_nblk + nb];
+          out[static_cast<size_t>(g) * n_nblk + nb] = sum;
+          writes[static_cast<size_t>(g) * n_nblk + nb] += 1;
+        }
+      } else if (done == 1) {
+        return;
+      } else if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > g_wait_s) {
+        std::fprintf(stderr, "wait gave up: copy warp idle\n");
+        g_fail.store(2);
+        return;
+      } else if (g_fail.load()) {
+        return;
+      } else {
+        std::this_thread::yield();
+      }
+    }
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    for (auto& c : cnt) c.store(0, std::memory_order_relaxed);   // zeroed by the plan launch
+    std::fill(writes.begin(), writes.end(), 0);
+    for (int u = 0; u < n_units; ++u) {
+      Ring& rg = rings[u];
+      for (int x = 0; x < cap; ++x) rg.seq[x].store(2u * x, std::memory_order_relaxed);
+      rg.tail = 0;
+      rg.claim = 0;
+      rg.done = 0;
+      int mine = 0;
+      for (int i = u; i < L.n_items; i += n_units) ++mine;
+      epi_left[u] = mine;
+      if (mine == 0) rg.done = 1;
+    }
+    L.run(e, ready);
+    for (int g = 0; g < n_tok && !g_fail.load(); ++g)
+      for (int nb = 0; nb < n_nblk; ++nb) {
+        int want = 0;
+        for (int k = 0; k < topk; ++k) want += val(g, k, nb);
+        const size_t x = static_cast<size_t>(g) * n_nblk + nb;
+        if (writes[x] != 1) fail_data("combined rows written", writes[x], 1);
+        else if (out[x] != want) fail_data("combined row", out[x], want);
+      }
+  }
+  return g_fail.load();
+}
+
 }  // namespace
 
 int main(int argc, char** argv) {
@@ -595,6 +728,7 @@ int main(int argc, char** argv) {
   else if (op == "rs") rc = run_rs(argc, argv);
   else if (op == "mlp") rc = run_mlp(argc, argv);
   else if (op == "moe") rc = run_moe(argc, argv);
+  else if (op == "combine") rc = run_combine(argc, argv);
   if (rc == 0) std::printf("OK\n");
   return rc;
 }

@@ -3,12 +3,13 @@
 Threads stand for the CTAs' roles, atomics for the flags and counters, and the
 work lists follow the kernels' orders (see the model's header).  Checked here:
 every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain,
-the chained MLP and the MoE dispatch completes (no wait gives up) and reads exactly the data its
-producers published, twice on the same flags (epochs 1 and 2); ThreadSanitizer
-finds no access the protocol leaves unordered.  Two planted mistakes show that
-the model catches what it is for: copy workers that publish with relaxed
-increments (a data race under ThreadSanitizer) and a chain whose parts run in
-descending order (a wait that gives up).
+the chained MLP, the MoE dispatch and the MoE combine's hand-over ring completes
+(no wait gives up) and reads exactly the data its producers published, twice on the
+same flags (epochs 1 and 2); ThreadSanitizer finds no access the protocol leaves
+unordered.  Three planted mistakes show that the model catches what it is for: copy
+workers that publish with relaxed increments and a ring entry freed before it is
+read (data races under ThreadSanitizer), and a chain whose parts run in descending
+order (a wait that gives up).
 """
 import os
 import shutil
@@ -36,6 +37,11 @@ MOE = [  # R E_loc n_nblk n_units pair n_cw rows_per_piece seed
     "4 3 2 3 1 6 32 7",           # pairs: 256-row tiles, empty experts
     "2 4 3 5 0 2 64 11",
     "8 2 1 8 1 6 16 3",
+]
+COMBINE = [  # R T topk n_nblk n_ctas n_cw ring_entries seed
+    "4 300 2 3 5 6 4 1",          # a 4-entry ring: many laps
+    "2 500 3 2 3 2 2 5",          # top-3, a 2-entry ring
+    "8 64 2 1 7 6 512 9",         # the kernel's ring size
 ]
 MLP = [  # R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
     "4 256 2 3 6 1 2 32",
@@ -81,7 +87,8 @@ def _run(exe, op, args, timeout=240):
 
 
 @pytest.mark.parametrize("op,args", [("ag", a) for a in AG] + [("rs", a) for a in RS] +
-                         [("mlp", a) for a in MLP] + [("moe", a) for a in MOE])
+                         [("mlp", a) for a in MLP] + [("moe", a) for a in MOE] +
+                         [("combine", a) for a in COMBINE])
 def test_protocol_completes_with_the_published_data(model, op, args):
     r = _run(model, op, args)
     assert r.returncode == 0 and r.stdout.strip() == "OK", (r.returncode, r.stderr[-2000:])
@@ -89,7 +96,8 @@ def test_protocol_completes_with_the_published_data(model, op, args):
 
 @pytest.mark.parametrize("op,args", [("ag", AG[0]), ("ag", AG[1]), ("ag", AG[2]), ("rs", RS[0]),
                                      ("rs", RS[2]), ("mlp", MLP[0]), ("mlp", MLP[1]),
-                                     ("moe", MOE[0]), ("moe", MOE[1])])
+                                     ("moe", MOE[0]), ("moe", MOE[1]), ("combine", COMBINE[0]),
+                                     ("combine", COMBINE[1])])
 def test_protocol_has_no_unordered_access(model_tsan, op, args):
     r = _run(model_tsan, op, args)
     assert "ThreadSanitizer" not in r.stderr, r.stderr[-3000:]
@@ -98,6 +106,11 @@ def test_protocol_has_no_unordered_access(model_tsan, op, args):
 
 def test_planted_relaxed_publication_is_a_data_race(model_tsan):
     r = _run(model_tsan, "ag", AG[0] + " relaxed")
+    assert "WARNING: ThreadSanitizer: data race" in r.stderr
+
+
+def test_planted_early_ring_free_is_a_data_race(model_tsan):
+    r = _run(model_tsan, "combine", COMBINE[0].rsplit(" ", 2)[0] + " 2 4 earlyfree")
     assert "WARNING: ThreadSanitizer: data race" in r.stderr
 
 
