@@ -10,7 +10,8 @@
 // (local shard first), the grouped raster, the running-sum chain's
 // part-major groups of one wave, the chained MLP's up-projection items ahead
 // of its down-projection items, the MoE tile table in (rank, expert, row tile,
-// column block) order, the combine's hand-over ring, and CTA pairs sharing one MMA issuer whose
+// column block) order, the combine's hand-over ring, ring attention's
+// step-major transfers, and CTA pairs sharing one MMA issuer whose
 // two accumulator buffers are freed by both CTAs' epilogues.
 //
 // Roles per CTA: a producer (waits for its item's inputs, then reads them), the
@@ -25,6 +26,7 @@
 //   protocol_model mlp R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
 //   protocol_model moe R E_loc n_nblk n_units pair n_cw rows_per_piece seed
 //   protocol_model combine R T topk n_nblk n_ctas n_cw ring_entries seed [bug]
+//   protocol_model attn R heads key_tiles n_ctas n_cw causal
 // with an optional last argument wait=S (the wait bound, default 20 s).
 // Prints "OK" and exits 0, or exits 2 on a wait that gives up (a deadlock in
 // the modelled protocol) and 3 on wrong data.  Planted mistakes, for the
@@ -582,6 +584,88 @@ int run_moe(int argc, char** argv) {
   return g_fail.load();
 }
 
+// ------------------------------------------------------------------ ring attention
+// Items (rank, head, query tile), the last rank's first; an item visits its own
+// block, then the blocks of ranks r-1, r-2, ... (step j), and before the first
+// key tile of a remote step waits until the (rank, step, head) counter holds
+// all 2 * nkt pieces (K and V of every key tile) that the copy workers move
+// into the rank's receive buffer, step-major.  Causal: only earlier ranks'
+// blocks and the diagonal block's first tiles.
+int run_attn(int argc, char** argv) {
+  if (argc < 8) return 64;
+  const int R = arg(argv, 2), heads = arg(argv, 3), nkt = arg(argv, 4), n_units = arg(argv, 5);
+  const int n_cw = arg(argv, 6), causal = arg(argv, 7);
+  const int nqt = nkt;
+  auto kv_val = [](int s, int h, int kt, int isv) { return ((s * 97 + h) * 89 + kt) * 2 + isv + 1; };
+  auto rix = [&](int r, int j, int h, int kt, int isv) {
+    return (((static_cast<size_t>(r) * R + j) * heads + h) * nkt + kt) * 2 + isv;
+  };
+  std::vector<int> recv(static_cast<size_t>(R) * R * heads * nkt * 2, -1);
+  std::vector<std::atomic<uint32_t>> cnt(static_cast<size_t>(R) * R * heads);
+  std::atomic<uint32_t> ready{0};
+  const int per_r = heads * nqt;
+  Launch L;
+  L.n_units = n_units;
+  L.halves = 1;
+  L.n_cw = n_cw;
+  L.n_items = R * per_r;
+  L.prologue = [&] { for (auto& c : cnt) c.store(0, std::memory_order_relaxed); };
+  L.copy = [&](int worker, int n_workers) {
+    const long long per = static_cast<long long>(heads) * (R - 1) * nkt * 2;
+    for (long long q = worker; q < per * R; q += n_workers) {
+      const int r = R - 1 - static_cast<int>(q / per);
+      long long rem = q % per;
+      const int j = 1 + static_cast<int>(rem / (static_cast<long long>(heads) * nkt * 2));
+      rem %= static_cast<long long>(heads) * nkt * 2;
+      const int h = static_cast<int>(rem / (nkt * 2)), kt = static_cast<int>(rem % (nkt * 2)) / 2;
+      const int isv = static_cast<int>(rem & 1);
+      const int s = (r - j + R) % R;
+      if (causal && s > r) continue;
+      recv[rix(r, j, h, kt, isv)] = kv_val(s, h, kt, isv);
+      cnt[(static_cast<size_t>(r) * R + j) * heads + h].fetch_add(1, std::memory_order_release);
+    }
+  };
+  L.decode = [&](int i, int) {
+    Item it;
+    const int r = R - 1 - i / per_r, rem = i % per_r, h = rem / nqt, qt = rem % nqt;
+    const int n = causal ? (qt + 1) + r * nkt : R * nkt;
+    it.inputs = [&, r, h, qt, n, i] {
+      int waited = 0;
+      for (int t = 0; t < n; ++t) {
+        int j, s, kt;
+        if (causal && t <= qt) {
+          j = 0; s = r; kt = t;
+        } else if (causal) {
+          const int u = t - (qt + 1);
+          j = 1 + u / nkt; s = r - j; kt = u % nkt;
+        } else {
+          j = t / nkt; kt = t % nkt; s = (r - j + R) % R;
+        }
+        if (j == 0) continue;   // the rank's own block, read in place
+        if (j != waited) {
+          const uint32_t want = static_cast<uint32_t>(2 * nkt);
+          if (!wait_until([&] { return cnt[(static_cast<size_t>(r) * R + j) * heads + h].load(std::memory_order_acquire) == want; },
+                          "ring step", i))
+            return false;
+          waited = j;
+        }
+        for (int isv = 0; isv < 2; ++isv)
+          if (recv[rix(r, j, h, kt, isv)] != kv_val(s, h, kt, isv)) {
+            fail_data("received K/V tile", recv[rix(r, j, h, kt, isv)], kv_val(s, h, kt, isv));
+            return false;
+          }
+      }
+      return true;
+    };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    std::fill(recv.begin(), recv.end(), -1);
+    L.run(e, ready);
+  }
+  return g_fail.load();
+}
+
 // ------------------------------------------------------------------ MoE combine
 // Every (token, slot) row of every column block is produced by some tile's
 // epilogue, which stores it into ret[r][t][slot] and counts it in the (token,
@@ -729,6 +813,7 @@ int main(int argc, char** argv) {
   else if (op == "mlp") rc = run_mlp(argc, argv);
   else if (op == "moe") rc = run_moe(argc, argv);
   else if (op == "combine") rc = run_combine(argc, argv);
+  else if (op == "attn") rc = run_attn(argc, argv);
   if (rc == 0) std::printf("OK\n");
   return rc;
 }

@@ -3,7 +3,8 @@
 Threads stand for the CTAs' roles, atomics for the flags and counters, and the
 work lists follow the kernels' orders (see the model's header).  Checked here:
 every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain,
-the chained MLP, the MoE dispatch and the MoE combine's hand-over ring completes
+the chained MLP, the MoE dispatch, the MoE combine's hand-over ring and ring
+attention's transfers completes
 (no wait gives up) and reads exactly the data its producers published, twice on the
 same flags (epochs 1 and 2); ThreadSanitizer finds no access the protocol leaves
 unordered.  Three planted mistakes show that the model catches what it is for: copy
@@ -42,6 +43,12 @@ COMBINE = [  # R T topk n_nblk n_ctas n_cw ring_entries seed
     "4 300 2 3 5 6 4 1",          # a 4-entry ring: many laps
     "2 500 3 2 3 2 2 5",          # top-3, a 2-entry ring
     "8 64 2 1 7 6 512 9",         # the kernel's ring size
+]
+ATTN = [  # R heads key_tiles n_ctas n_cw causal
+    "4 2 3 5 2 0",
+    "4 2 3 5 2 1",                # causal: only earlier ranks' blocks travel
+    "8 1 2 3 2 1",
+    "2 3 4 1 1 0",                # one CTA, one copy worker
 ]
 MLP = [  # R m f_nblk h_nblk n_ctas pair n_cw rows_per_piece
     "4 256 2 3 6 1 2 32",
@@ -88,7 +95,7 @@ def _run(exe, op, args, timeout=240):
 
 @pytest.mark.parametrize("op,args", [("ag", a) for a in AG] + [("rs", a) for a in RS] +
                          [("mlp", a) for a in MLP] + [("moe", a) for a in MOE] +
-                         [("combine", a) for a in COMBINE])
+                         [("combine", a) for a in COMBINE] + [("attn", a) for a in ATTN])
 def test_protocol_completes_with_the_published_data(model, op, args):
     r = _run(model, op, args)
     assert r.returncode == 0 and r.stdout.strip() == "OK", (r.returncode, r.stderr[-2000:])
@@ -97,7 +104,7 @@ def test_protocol_completes_with_the_published_data(model, op, args):
 @pytest.mark.parametrize("op,args", [("ag", AG[0]), ("ag", AG[1]), ("ag", AG[2]), ("rs", RS[0]),
                                      ("rs", RS[2]), ("mlp", MLP[0]), ("mlp", MLP[1]),
                                      ("moe", MOE[0]), ("moe", MOE[1]), ("combine", COMBINE[0]),
-                                     ("combine", COMBINE[1])])
+                                     ("combine", COMBINE[1]), ("attn", ATTN[0]), ("attn", ATTN[1])])
 def test_protocol_has_no_unordered_access(model_tsan, op, args):
     r = _run(model_tsan, op, args)
     assert "ThreadSanitizer" not in r.stderr, r.stderr[-3000:]
