@@ -27,6 +27,7 @@
 //   protocol_model moe R E_loc n_nblk n_units pair n_cw rows_per_piece seed
 //   protocol_model combine R T topk n_nblk n_ctas n_cw ring_entries seed [bug]
 //   protocol_model attn R heads key_tiles n_ctas n_cw causal
+//   protocol_model rsv R m n_nblk n_ctas pair group_m atomic|last [bug]
 // with an optional last argument wait=S (the wait bound, default 20 s).
 // Prints "OK" and exits 0, or exits 2 on a wait that gives up (a deadlock in
 // the modelled protocol) and 3 on wrong data.  Planted mistakes, for the
@@ -34,7 +35,8 @@
 // publish with relaxed increments (the race a missing fence would be); rs bug
 // "reversed" runs each group's parts in descending order (a chain that waits
 // on work queued behind it); combine bug "earlyfree" frees a ring entry before
-// reading it (a race with the next lap's writer).
+// reading it (a race with the next lap's writer); rsv bug "nozerowait" adds
+// into the accumulators without waiting for the zero flags.
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -361,6 +363,112 @@ int run_rs(int argc, char** argv) {
     std::fill(out.begin(), out.end(), 0);
     L.run(e, ready);
     if (!g_fail.load()) ch.check();
+  }
+  return g_fail.load();
+}
+
+// ------------------------------------------------------------------ RS / AR reduction variants
+// Items (tile, part) with a tile's parts consecutive.  "atomic": the spare
+// warps of every CTA zero their share of the fp32 accumulator tiles and then
+// publish the CTA's zero flag; an epilogue waits once for every CTA's flag,
+// adds its rows into the tile's accumulator (relaxed atomic adds), and counts
+// each 32-row quarter (a release); the warp whose count completes a quarter
+// reads the accumulator and stores the output rows.  "last": every partial is
+// staged in its own slot (plain stores) and counted the same way; the warp that
+// completes a quarter sums the slots in rank order.  The quarter counters are
+// zeroed by the ticket-0 CTA before the ready word.
+int run_rsv(int argc, char** argv) {
+  if (argc < 9) return 64;
+  const int R = arg(argv, 2), m = arg(argv, 3), n_nblk = arg(argv, 4), n_ctas = arg(argv, 5);
+  const int pair = arg(argv, 6), group_m = arg(argv, 7);
+  const bool atomic_mode = std::string(argv[8]) == "atomic";
+  const bool skip_zero_wait = argc > 9 && std::string(argv[9]) == "nozerowait";
+  const int n_mblk = ceil_div(m, BM), P = R, Q = 4, QR = 8;   // 4 quarters, 8 model rows each
+  const int n_tiles = n_mblk * n_nblk;
+  const int n_mrow = pair ? (n_mblk + 1) / 2 : n_mblk, n_sched = n_mrow * n_nblk;
+  const int n_units = pair ? std::max(1, n_ctas / 2) : n_ctas, halves = pair ? 2 : 1;
+  const int grid = n_units * halves;
+  auto partial = [](int tile, int part, int row) { return 1000LL * tile + 37LL * part + row + 1; };
+  std::vector<std::atomic<long long>> acc(static_cast<size_t>(n_tiles) * Q * QR);
+  std::vector<long long> slots(static_cast<size_t>(n_tiles) * P * Q * QR, 0);
+  std::vector<long long> out(static_cast<size_t>(n_tiles) * Q * QR, 0);
+  std::vector<std::atomic<uint32_t>> qcnt(static_cast<size_t>(n_tiles) * Q), zflag(grid), zdone(grid);
+  std::atomic<uint32_t> ready{0};
+  uint32_t epoch = 0;
+  Launch L;
+  L.n_units = n_units;
+  L.halves = halves;
+  L.n_cw = atomic_mode ? 3 : 0;   // the spare warps zero the accumulators
+  L.n_items = n_sched * P;
+  L.prologue = [&] { for (auto& c : qcnt) c.store(0, std::memory_order_relaxed); };
+  if (atomic_mode)
+    L.copy = [&](int worker, int) {
+      const int cta = worker / L.n_cw, w = worker % L.n_cw;
+      const size_t total = acc.size(), per = (total + grid - 1) / grid;
+      const size_t lo = std::min(total, static_cast<size_t>(cta) * per), hi = std::min(total, lo + per);
+      for (size_t x = lo + w; x < hi; x += L.n_cw) acc[x].store(0, std::memory_order_relaxed);
+      // the spare warps meet at a named barrier; one of them publishes the flag
+      if (zdone[cta].fetch_add(1, std::memory_order_acq_rel) == static_cast<uint32_t>(L.n_cw - 1))
+        zflag[cta].store(epoch, std::memory_order_release);
+    };
+  std::vector<int> zero_seen(grid, 0);
+  L.decode = [&](int i, int half) {
+    Item it;
+    const int q = i / P, part = i % P;
+    int mb, nb;
+    raster(q, group_m, n_mrow, n_nblk, mb, nb);
+    if (pair) mb = 2 * mb + half;
+    if (mb >= n_mblk) {
+      it.empty = true;
+      return it;
+    }
+    const int tile = mb * n_nblk + nb;
+    const int cta = (i % n_units) * halves + half;
+    it.epilogue = [&, tile, part, cta, i] {
+      if (atomic_mode && !zero_seen[cta] && !skip_zero_wait) {
+        for (int c = 0; c < grid; ++c)
+          if (!wait_until([&] { return zflag[c].load(std::memory_order_acquire) == epoch; }, "zero flags", i))
+            return false;
+        zero_seen[cta] = 1;
+      }
+      for (int qq = 0; qq < Q; ++qq) {
+        for (int row = 0; row < QR; ++row) {
+          const size_t x = (static_cast<size_t>(tile) * Q + qq) * QR + row;
+          const long long v = partial(tile, part, qq * QR + row);
+          if (atomic_mode) acc[x].fetch_add(v, std::memory_order_relaxed);
+          else slots[((static_cast<size_t>(tile) * P + part) * Q + qq) * QR + row] = v;
+        }
+        const uint32_t before = qcnt[static_cast<size_t>(tile) * Q + qq].fetch_add(1, std::memory_order_acq_rel);
+        if (before != static_cast<uint32_t>(P - 1)) continue;
+        for (int row = 0; row < QR; ++row) {   // this warp completes the quarter
+          const size_t x = (static_cast<size_t>(tile) * Q + qq) * QR + row;
+          long long sum = 0;
+          if (atomic_mode) sum = acc[x].load(std::memory_order_relaxed);
+          else
+            for (int p2 = 0; p2 < P; ++p2) sum += slots[((static_cast<size_t>(tile) * P + p2) * Q + qq) * QR + row];
+          out[x] = sum;
+        }
+      }
+      return true;
+    };
+    return it;
+  };
+  for (uint32_t e = 1; e <= 2 && !g_fail.load(); ++e) {
+    epoch = e;
+    std::fill(out.begin(), out.end(), 0);
+    std::fill(zero_seen.begin(), zero_seen.end(), 0);
+    for (auto& z : zdone) z.store(0, std::memory_order_relaxed);
+    for (auto& a : acc) a.store(e == 1 ? 0 : 123456789, std::memory_order_relaxed);   // stale sums
+    L.run(e, ready);
+    for (int t = 0; t < n_tiles && !g_fail.load(); ++t)
+      for (int r = 0; r < Q * QR; ++r) {
+        long long want = 0;
+        for (int p2 = 0; p2 < P; ++p2) want += partial(t, p2, r);
+        if (out[static_cast<size_t>(t) * Q * QR + r] != want) {
+          fail_data("reduced row", out[static_cast<size_t>(t) * Q * QR + r], want);
+          break;
+        }
+      }
   }
   return g_fail.load();
 }
@@ -814,6 +922,7 @@ int main(int argc, char** argv) {
   else if (op == "moe") rc = run_moe(argc, argv);
   else if (op == "combine") rc = run_combine(argc, argv);
   else if (op == "attn") rc = run_attn(argc, argv);
+  else if (op == "rsv") rc = run_rsv(argc, argv);
   if (rc == 0) std::printf("OK\n");
   return rc;
 }

@@ -2,15 +2,17 @@
 
 Threads stand for the CTAs' roles, atomics for the flags and counters, and the
 work lists follow the kernels' orders (see the model's header).  Checked here:
-every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain,
+every modelled launch of AllGather+GEMM, the GEMM+ReduceScatter running-sum chain
+and its atomic and last-arrival variants,
 the chained MLP, the MoE dispatch, the MoE combine's hand-over ring and ring
 attention's transfers completes
 (no wait gives up) and reads exactly the data its producers published, twice on the
 same flags (epochs 1 and 2); ThreadSanitizer finds no access the protocol leaves
-unordered.  Three planted mistakes show that the model catches what it is for: copy
+unordered.  Four planted mistakes show that the model catches what it is for: copy
 workers that publish with relaxed increments and a ring entry freed before it is
-read (data races under ThreadSanitizer), and a chain whose parts run in descending
-order (a wait that gives up).
+read (data races under ThreadSanitizer), additions that do not wait for the zeroed
+accumulators (wrong sums), and a chain whose parts run in descending order (a wait
+that gives up).
 """
 import os
 import shutil
@@ -33,6 +35,12 @@ RS = [  # R m n_nblk n_ctas pair group_m
     "2 256 2 2 0 8",
     "8 1024 4 6 1 2",
     "3 384 5 16 0 8",             # more CTAs than tiles
+]
+RSV = [  # R m n_nblk n_ctas pair group_m mode
+    "4 520 3 5 1 8 atomic",       # zero flags, relaxed adds, quarter counts
+    "2 256 2 3 0 8 atomic",
+    "4 520 3 5 1 8 last",         # staged slots summed by the last arrival
+    "8 512 2 6 1 2 last",
 ]
 MOE = [  # R E_loc n_nblk n_units pair n_cw rows_per_piece seed
     "4 3 2 3 1 6 32 7",           # pairs: 256-row tiles, empty experts
@@ -94,6 +102,7 @@ def _run(exe, op, args, timeout=240):
 
 
 @pytest.mark.parametrize("op,args", [("ag", a) for a in AG] + [("rs", a) for a in RS] +
+                         [("rsv", a) for a in RSV] +
                          [("mlp", a) for a in MLP] + [("moe", a) for a in MOE] +
                          [("combine", a) for a in COMBINE] + [("attn", a) for a in ATTN])
 def test_protocol_completes_with_the_published_data(model, op, args):
@@ -104,7 +113,8 @@ def test_protocol_completes_with_the_published_data(model, op, args):
 @pytest.mark.parametrize("op,args", [("ag", AG[0]), ("ag", AG[1]), ("ag", AG[2]), ("rs", RS[0]),
                                      ("rs", RS[2]), ("mlp", MLP[0]), ("mlp", MLP[1]),
                                      ("moe", MOE[0]), ("moe", MOE[1]), ("combine", COMBINE[0]),
-                                     ("combine", COMBINE[1]), ("attn", ATTN[0]), ("attn", ATTN[1])])
+                                     ("combine", COMBINE[1]), ("attn", ATTN[0]), ("attn", ATTN[1]),
+                                     ("rsv", RSV[0]), ("rsv", RSV[2])])
 def test_protocol_has_no_unordered_access(model_tsan, op, args):
     r = _run(model_tsan, op, args)
     assert "ThreadSanitizer" not in r.stderr, r.stderr[-3000:]
@@ -119,6 +129,11 @@ def test_planted_relaxed_publication_is_a_data_race(model_tsan):
 def test_planted_early_ring_free_is_a_data_race(model_tsan):
     r = _run(model_tsan, "combine", COMBINE[0].rsplit(" ", 2)[0] + " 2 4 earlyfree")
     assert "WARNING: ThreadSanitizer: data race" in r.stderr
+
+
+def test_planted_missing_zero_wait_gives_wrong_sums(model):
+    r = _run(model, "rsv", RSV[0] + " nozerowait")
+    assert r.returncode == 3 and "wrong data" in r.stderr
 
 
 def test_planted_reversed_chain_is_a_wait_that_gives_up(model):
