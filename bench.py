@@ -274,6 +274,81 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+def _timed_rows(run, n_total: int, target_s: float):
+    """Run the oracle on a growing evenly spaced row sample until one run takes
+    about target_s seconds (or covers every row).  Returns (rows, seconds)."""
+    rows = min(8, n_total)
+    while True:
+        sel = np.linspace(0, n_total - 1, rows).astype(np.int64)
+        t0 = time.perf_counter()
+        run(sel)
+        t = time.perf_counter() - t0
+        if t >= target_s * 0.5 or rows >= n_total:
+            return rows, t
+        rows = int(min(n_total, max(rows * 2, rows * target_s / max(t, 1e-3) * 0.9)))
+
+
+def cpu_gemm_baseline(a_dev, b_dev, w, target_s: float = 4.0):
+    """The oracle's S = sum_r A_r @ B_r (GEMM+ReduceScatter / GEMM+AllReduce) on a
+    row sample of the workload, on the host cores: TFLOP/s of the sampled rows."""
+    import oracle as O
+    a_bits = [I.bits(x) for x in a_dev]
+    b_bits = [I.bits(x) for x in b_dev]
+    rows, t = _timed_rows(lambda sel: O.sum_over_ranks(a_bits, b_bits, rows=sel), w.m, target_s)
+    rate = 2.0 * rows * w.n * w.k * w.R / t / 1e12
+    return {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{rows} of {w.m} rows of S (all {w.n} columns, {w.R} ranks x K={w.k}), "
+                      f"fp64 numpy, {t:.1f} s"}
+
+
+def cpu_moe_baseline(x_dev, lg_dev, we_dev, w, target_s: float = 4.0):
+    """The oracle's MoE path on the host cores: routing, counts and the dispatch
+    permutation for every token, then the gather and grouped GEMM of an evenly
+    spaced sample of each destination rank's received rows.  TFLOP/s of the
+    sampled rows' GEMM over the whole time."""
+    import oracle as O
+    x_bits = [I.bits(t) for t in x_dev]
+    w_bits = [I.bits(t) for t in we_dev]
+    logits = [t.cpu().numpy() for t in lg_dev]
+    t0 = time.perf_counter()
+    idx = [O.moe_route(lg, w.topk) for lg in logits]
+    O.moe_counts(idx, w.E)
+    recv_src, seg = O.moe_dispatch(idx, w.E_loc)
+    t_route = time.perf_counter() - t0
+    total = sum(len(s) for s in recv_src)
+
+    def run(sel_frac):
+        n = 0
+        for d in range(w.R):
+            nd = len(recv_src[d])
+            if nd == 0:
+                continue
+            sel = np.unique((sel_frac * (nd - 1)).astype(np.int64))
+            rx = O.moe_gather_rows(x_bits, recv_src[d][sel], w.topk)
+            # the gathered rows are the sample: expert of each from the segment bounds
+            starts = np.concatenate([[0], np.cumsum(seg[d])])
+            ex = np.searchsorted(starts, sel, side="right") - 1
+            for l in np.unique(ex):
+                pick = np.nonzero(ex == l)[0]
+                O.moe_expert_gemm(rx[pick], [len(pick)], w_bits[d][l:l + 1])
+            n += len(sel)
+        run.rows = n
+
+    per = 8
+    while True:
+        frac = np.linspace(0.0, 1.0, per)
+        t1 = time.perf_counter()
+        run(frac)
+        t = time.perf_counter() - t1
+        if t >= target_s * 0.5 or per >= total:
+            break
+        per = int(min(total, max(per * 2, per * target_s / max(t, 1e-3) * 0.9)))
+    rate = 2.0 * run.rows * w.H * w.N / (t + t_route) / 1e12
+    return {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"routing + dispatch of all {total} rows ({t_route:.1f} s), then gather + "
+                      f"expert GEMM of {run.rows} received rows ({t:.1f} s), fp64 numpy"}
+
+
 # ------------------------------------------------------------------ the reference (oracle) arm
 
 def run_reference(args):
@@ -483,7 +558,8 @@ def main():
     other = {}
     if not args.no_other:
         other = bench_other(mk, device, stream, dist, args.other_steps, seed_off, tmax,
-                            bf16_peak, hbm_peak, pair=args.cta_pair)
+                            bf16_peak, hbm_peak, pair=args.cta_pair,
+                            cpu=(rank == 0 and not args.no_cpu))
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -568,8 +644,9 @@ def run_only(args):
 
 
 def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak,
-                only=None, with_moe=True, pair=0):
-    """Fused / GEMM-only / unfused timings of the RS and AR workloads."""
+                only=None, with_moe=True, pair=0, cpu=False):
+    """Fused / GEMM-only / unfused timings of the RS and AR workloads (and, with
+    cpu=True, the CPU oracle on a row sample of each)."""
     out = {}
     for w in (only or (I.RS_R8_TP8_DOWN, I.AR_R8_DECODE)):
         nsets = 2 if w.op == "rs" else 3
@@ -608,16 +685,27 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
                  "wire_bf16_ms": res["wire_bf16"], "atomic_ms": res["atomic"],
                  "status": mk.status_string(st)}
         if w.op == "ar":
-            hbm_bytes = w.R * (w.k * w.n * 2 + w.m * w.k * 2) + w.R * w.m * w.n * 2
+            # algorithmic bytes: every B_r and A_r read once, the fp32 running sum forwarded
+            # R-1 times (written and read back), and the R bf16 replicas written
+            hbm_bytes = (w.R * (w.k * w.n * 2 + w.m * w.k * 2) + (w.R - 1) * 2 * w.m * w.n * 4
+                         + w.R * w.m * w.n * 2)
             entry["bound"] = "hbm"
+            entry["algorithmic_bytes"] = hbm_bytes
             entry["hbm_gbs"] = hbm_bytes / (res["fused"] * 1e-3) / 1e9
             entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
+            entry["roofline_frac"] = entry["hbm_frac"]
+        else:
+            entry["bound"] = "tensor"
+            entry["roofline_frac"] = fused_tf / bf16_peak
+        entry["traffic"] = recorded_traffic(w.name)
+        if cpu:
+            entry["cpu_baseline"] = cpu_gemm_baseline(sets[0][0], sets[0][1], w)
         out[w.name] = entry
         del sets, ws
         torch.cuda.empty_cache()
     if with_moe:
         out[I.MOE_R8_E64.name] = bench_moe(mk, device, stream, dist, steps, seed_off, tmax,
-                                           bf16_peak, hbm_peak)
+                                           bf16_peak, hbm_peak, cpu=cpu)
         torch.cuda.empty_cache()
         out[I.MOE_COMBINE_R8_E64.name] = bench_moe_combine(mk, device, stream, dist, steps, seed_off,
                                                            tmax, bf16_peak, hbm_peak)
@@ -636,7 +724,7 @@ def bench_other(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_
     return out
 
 
-def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
+def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak, cpu=False):
     """MoE dispatch + grouped GEMM: fused, GEMM-only and unfused timings."""
     w = I.MOE_R8_E64
     sets = []
@@ -669,12 +757,16 @@ def bench_moe(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12
     t_tensor = flops / (bf16_peak * 1e12)
     t_hbm = hbm_bytes / (hbm_peak * 1e9)
-    return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
-            "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
-            "pct_of_peak": 100 * fused_tf / bf16_peak, "algorithmic_bytes": hbm_bytes,
-            "roofline_ms": 1e3 * max(t_tensor, t_hbm),
-            "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
-            "status": mk.status_string(st)}
+    entry = {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
+             "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
+             "pct_of_peak": 100 * fused_tf / bf16_peak, "algorithmic_bytes": hbm_bytes,
+             "roofline_ms": 1e3 * max(t_tensor, t_hbm),
+             "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
+             "traffic": recorded_traffic(w.name),
+             "status": mk.status_string(st)}
+    if cpu:
+        entry["cpu_baseline"] = cpu_moe_baseline(*sets[0], w)
+    return entry
 
 
 def bench_moe_combine(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):

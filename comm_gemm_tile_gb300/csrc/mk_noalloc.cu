@@ -46,6 +46,9 @@ extern "C" mk_status mk_ag_gemm_noalloc(const void* const* a_shards, const void*
                                         void* c, mk_dtype c_dtype, int R, int local_rank, long long m_r,
                                         long long n, long long k, int* device_status,
                                         const mk_config* cfg, mk_stream_t stream) {
+  // The in-kernel trace would land in the library's own array, where the
+  // caller cannot read it: rejected.
+  if (cfg && cfg->trace != 0) return MK_ERR_INVALID;
   // Size check first: it needs no GPU and rejects shapes whose scratch would
   // not fit in the fixed array.
   const size_t need = mk_workspace_size(MK_OP_AG_GEMM, R, m_r, n, k, cfg);

@@ -30,6 +30,11 @@
  *   leaves it valid for later calls (flags are epoch-tagged, so no reset is
  *   needed between calls).  One workspace must not be used by two calls that
  *   may run at the same time.
+ * - Epoch: every call of an entry point that takes a workspace draws a new
+ *   epoch on the host and passes it to its kernels by value; the ready flags
+ *   of that call are valid only for that epoch.  A CUDA graph that captured
+ *   such a call would replay the epoch of the capture, which leaves stale
+ *   flags looking ready, so these calls must not be captured into a graph.
  * - Asynchrony: every compute entry point only enqueues work on `stream`
  *   and returns.  Host-side argument errors return MK_ERR_INVALID /
  *   MK_ERR_UNSUPPORTED before anything is launched; a failed launch returns
@@ -320,8 +325,9 @@ mk_status mk_ring_attention(const void *const *q, const void *const *k, const vo
  *     128 gathered rows, i.e. R*m_r up to 130560 rows) are rejected with
  *     MK_ERR_INVALID before anything is enqueued.
  *   - The first call on a device looks up the array's device address and
- *     zero-fills it on `stream`; make that first call before any stream
- *     capture on that device.
+ *     zero-fills it on `stream`.  That set-up may not run while a stream is
+ *     being captured, so make the first call on each device outside any
+ *     stream capture.
  *   - Every call shares the one array and it keeps the previous call's
  *     contents; each call clears the part that must start at zero.  Two calls
  *     whose GPU work can overlap (different streams without ordering, or
@@ -329,16 +335,14 @@ mk_status mk_ring_attention(const void *const *q, const void *const *k, const vo
  *   - device_status: optional (may be NULL) caller-owned device int, 4-byte
  *     aligned, that receives this call's device status (MK_OK or
  *     MK_ERR_TIMEOUT) once the call's work on `stream` has finished.
+ *   - cfg->trace must be 0 (MK_ERR_INVALID otherwise): the trace region would
+ *     sit in the library's array, where the caller cannot read it.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 mk_status mk_ag_gemm_noalloc(const void *const *a_shards, const void *b, void *a_gathered, void *c,
                              mk_dtype c_dtype, int R, int local_rank, long long m_r, long long n,
                              long long k, int *device_status, const mk_config *cfg,
                              mk_stream_t stream);
 
-/* Synchronises `stream`, then reads and clears the device status word of a
- * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the
- * stream itself reports an error).  `detail` (may be NULL) receives a code
- * saying which wait failed (role * 1e6 + item index), for diagnostics. */
 /* In-kernel trace of an AG / RS / AR call made with cfg->trace = 1: the number
  * of records and (in *offset) their byte offset in the workspace; 0 records
  * when tracing is off or the arguments are bad.  Record 2*i + c (c = the CTA's
@@ -370,6 +374,10 @@ size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, co
 size_t mk_moe_trace_entries(int R, int E_loc, int topk, long long T, long long H, long long N,
                             long long cap_rows, const mk_config *cfg, size_t *offset);
 
+/* Synchronises `stream`, then reads and clears the device status word of a
+ * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the
+ * stream itself reports an error).  `detail` (may be NULL) receives a code
+ * saying which wait failed (role * 1e6 + item index), for diagnostics. */
 mk_status mk_get_device_status(const void *workspace, mk_stream_t stream, long long *detail);
 
 /* Static text for a status code. */

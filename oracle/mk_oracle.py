@@ -101,11 +101,14 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 def round_out(x: np.ndarray, out: str) -> np.ndarray:
     """Round an exact float64 result to the output dtype: 'bf16' -> uint16
-    bit patterns, 'f32' -> float32 values."""
+    bit patterns, 'f32' -> float32 values.  'f64' leaves the float64 result
+    unrounded (the value the float parity bar measures errors against)."""
     if out == "bf16":
         return f64_to_bf16_bits(x)
     if out == "f32":
         return np.asarray(x, dtype=np.float64).astype(np.float32)
+    if out == "f64":
+        return np.asarray(x, dtype=np.float64)
     raise ValueError(f"unknown output dtype {out!r}")
 
 
@@ -175,11 +178,13 @@ def gemm_ar(a_list, b_list, out: str = "bf16"):
     return [c.copy() for _ in range(len(a_list))]
 
 
-def rank_partials(a_list, b_list) -> list:
+def rank_partials(a_list, b_list, rows=None) -> list:
     """The terms of S: P_r = A_r @ B_r in float64, one per rank, in rank order
-    (table row "GEMM + ReduceScatter": each rank's partial product)."""
+    (table row "GEMM + ReduceScatter": each rank's partial product).
+    rows: optional sample of S's rows (every partial restricted to them)."""
     assert len(a_list) == len(b_list) and len(a_list) >= 1
-    return [bf16_to_f64(np.asarray(a)) @ bf16_to_f64(np.asarray(b)) for a, b in zip(a_list, b_list)]
+    sel = (lambda a: np.asarray(a)) if rows is None else (lambda a: np.asarray(a)[np.asarray(rows)])
+    return [bf16_to_f64(sel(a)) @ bf16_to_f64(np.asarray(b)) for a, b in zip(a_list, b_list)]
 
 
 def f64_to_f32(x) -> np.ndarray:

@@ -301,6 +301,31 @@ def test_rank_partials_sum_to_s():
     np.testing.assert_allclose(sum(O.rank_partials(a, b)), O.sum_over_ranks(a, b), rtol=0, atol=1e-12)
 
 
+def test_rank_partials_brute_force_and_row_sample():
+    # each term is its own rank's product (brute force), and a row sample is those rows
+    R, m, k, n = 3, 5, 4, 3
+    a = [rand_int_bits((m, k), 60 + r) for r in range(R)]
+    b = [rand_int_bits((k, n), 70 + r) for r in range(R)]
+    parts = O.rank_partials(a, b)
+    for r in range(R):
+        np.testing.assert_array_equal(parts[r], brute_matmul(O.bf16_to_f64(a[r]), O.bf16_to_f64(b[r])))
+    rows = np.array([4, 0, 2])
+    for full, part in zip(parts, O.rank_partials(a, b, rows=rows)):
+        np.testing.assert_array_equal(part, full[rows])
+
+
+def test_unrounded_output_is_the_float64_result():
+    # out='f64' returns the exact sum itself: a value no fp32 or bf16 holds survives unrounded
+    x = np.array([1.0 + 2.0 ** -40, -3.0, 2.0 ** -140])
+    np.testing.assert_array_equal(O.round_out(x, "f64"), x)
+    shards = [rand_int_bits((2, 3), 80 + r) for r in range(2)]
+    b = rand_int_bits((3, 2), 90)
+    _, c64 = O.ag_gemm(shards, b, out="f64")
+    A = np.concatenate([O.bf16_to_f64(s) for s in shards], 0)
+    np.testing.assert_array_equal(c64, brute_matmul(A, O.bf16_to_f64(b)))
+    assert c64.dtype == np.float64
+
+
 # ---- fp8 e4m3 operands
 
 

@@ -4,8 +4,10 @@ Some callers cannot allocate device memory (a plug-in inside an application
 that owns every GPU byte through its own pool, or a path that must not
 allocate after start-up).  For them the library keeps the kernel's small
 scratch in a fixed array of its own.  These tests call that entry point
-through the C ABI and check it against the ordinary mk_ag_gemm, twice in a
-row, since every call reuses the same array.  This file is collected last.
+through the C ABI and check it against the ordinary mk_ag_gemm (bit for bit:
+the same kernel) and the oracle, twice in a row, since every call reuses the
+same array, and once more after a call that timed out and left its error
+words in that array.  This file is collected last.
 """
 import ctypes
 
@@ -15,6 +17,7 @@ import torch
 
 import comm_gemm_tile_gb300 as mk
 from comm_gemm_tile_gb300 import inputs as I
+import oracle as O
 from parity_util import TOL, absmax, dev, gpu_values, norm_err
 
 NOALLOC_SCRATCH_BYTES = 65536
@@ -43,6 +46,38 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
                                 None, None, None) == mk.MK_ERR_INVALID
 
 
+def test_noalloc_rejects_trace():
+    # a trace would be written into the library's own array, out of the caller's reach
+    from comm_gemm_tile_gb300 import build
+    build.build()
+    L = mk.lib()
+    ptrs = (ctypes.c_void_p * 2)(0x10000, 0x10000)
+    cfg = mk.Config(trace=1).c()
+    assert L.mk_ag_gemm_noalloc(ptrs, 0x10000, 0x10000, 0x10000, mk.MK_BF16, 2, 0, 128, 64, 64,
+                                None, ctypes.byref(cfg), None) == mk.MK_ERR_INVALID
+
+
+def _run(L, w, local, dtype, status):
+    """One mk_ag_gemm (caller workspace) and two back-to-back mk_ag_gemm_noalloc
+    calls on the same inputs; both no-alloc results must equal the workspace
+    call's bit for bit (the same kernel and launch configuration)."""
+    a, b = I.gemm_inputs(w)
+    shards, bd = dev(a), b[0].cuda()
+    g_ref, c_ref = mk.ag_gemm(shards, bd, local_rank=local, out_dtype=dtype)
+    st_ref, _ = mk.device_status()
+    assert st_ref == mk.MK_OK
+    for _ in range(2):   # the second call finds the first call's contents in the shared array
+        g = torch.zeros_like(g_ref)
+        c = torch.zeros_like(c_ref)
+        status.fill_(-1)
+        assert _noalloc(L, shards, bd, g, c, local, status_dev=status) == mk.MK_OK
+        torch.cuda.synchronize()
+        assert int(status.item()) == mk.MK_OK
+        assert torch.equal(g, g_ref)                       # the gathered A is a bit copy
+        assert torch.equal(c, c_ref)
+    return a, b, g, c
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice():
     from comm_gemm_tile_gb300 import build
@@ -54,21 +89,38 @@ def test_noalloc_matches_workspace_entry_point_twice():
         (8, 128, 512, 256, 6, torch.float32, 12),
     ]
     for R, mr, n, k, local, dtype, seed in cases:
-        w = I.GemmWorkload("noalloc", "ag", R=R, m=mr, n=n, k=k,
-                           out="bf16" if dtype == torch.bfloat16 else "f32",
-                           a_seed=seed, b_seed=seed + 100)
-        a, b = I.gemm_inputs(w)
-        shards, bd = dev(a), b[0].cuda()
-        g_ref, c_ref = mk.ag_gemm(shards, bd, local_rank=local, out_dtype=dtype)
-        st_ref, _ = mk.device_status()
-        assert st_ref == mk.MK_OK
-        g = torch.zeros_like(g_ref)
-        c = torch.zeros_like(c_ref)
-        status.fill_(-1)
-        assert _noalloc(L, shards, bd, g, c, local, status_dev=status) == mk.MK_OK
-        torch.cuda.synchronize()
-        assert int(status.item()) == mk.MK_OK
-        assert torch.equal(g, g_ref)                       # the gathered A is a bit copy
         out = "bf16" if dtype == torch.bfloat16 else "f32"
-        exact = gpu_values(c_ref)
+        w = I.GemmWorkload("noalloc", "ag", R=R, m=mr, n=n, k=k, out=out, a_seed=seed, b_seed=seed + 100)
+        a, b, g, c = _run(L, w, local, dtype, status)
+        _, exact = O.ag_gemm([I.bits(x) for x in a], I.bits(b[0]), out="f64")
         assert norm_err(gpu_values(c), exact, k, absmax(a), absmax(b)) <= TOL[out]
+
+
+@pytest.mark.gpu
+def test_noalloc_integer_twin_bit_exact_and_recovers_after_timeout():
+    from comm_gemm_tile_gb300 import build
+    build.build()
+    L = mk.lib()
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    w = I.GemmWorkload("noalloc_int", "ag", R=4, m=256, n=520, k=264, out="bf16", a_seed=13,
+                       b_seed=113, integer=True)
+    a, b, g, c = _run(L, w, 2, torch.bfloat16, status)
+    a_bits, b_bits = [I.bits(x) for x in a], I.bits(b[0])
+    gathered, want = O.ag_gemm(a_bits, b_bits, out="bf16")
+    np.testing.assert_array_equal(I.bits(g), gathered)
+    np.testing.assert_array_equal(I.bits(c), want)
+    # a call whose copy-in drops one ready signal times out (20 ms) and leaves its status,
+    # detail and abort words in the shared array; the next call clears them and is exact
+    shards, bd = dev(a), b[0].cuda()
+    status.fill_(-1)
+    assert _noalloc(L, shards, bd, torch.zeros_like(g), torch.zeros_like(c), 2, status_dev=status,
+                    cfg=mk.Config(inject=1, wait_limit_ns=20_000_000)) == mk.MK_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == mk.MK_ERR_TIMEOUT
+    g2, c2 = torch.zeros_like(g), torch.zeros_like(c)
+    status.fill_(-1)
+    assert _noalloc(L, shards, bd, g2, c2, 2, status_dev=status) == mk.MK_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == mk.MK_OK
+    np.testing.assert_array_equal(I.bits(g2), gathered)
+    np.testing.assert_array_equal(I.bits(c2), want)
