@@ -4,27 +4,28 @@
 // while each rank attends its queries to every block that has arrived,
 // merging the partial softmax results.
 //
-// One persistent launch of 416 threads per CTA, one CTA per SM:
-//   * warps 0 and 12 (TMA): a 128-query tile of one (rank, head), then the K
-//     (warp 0) and V (warp 12) tiles, 128 keys each, in ring order -- the
-//     rank's own block, then the blocks of ranks r-1, r-2, ... as they land
-//     in its receive buffer;
-//   * warp 1 (MMA): S = Q K^T into one of two TMEM buffers, then O += P V
-//     into one of two TMEM accumulators (tcgen05, bf16 -> fp32), with one
-//     mbarrier wait and two commits per tile (see at_mma);
-//   * warps 2-9 (softmax): online softmax in two groups of four warps, one
-//     for the even tiles of the CTA's running tile count and one for the odd
-//     ones (so a query tile's key tiles alternate between them), each
-//     with its own running maximum, sum, P buffer (shared memory) and O
-//     accumulator (TMEM), so that two tiles' softmax runs at once; P =
-//     exp2(scale * log2(e) * s - m) as bf16; O is rescaled only when the
-//     maximum grows by more than 2^8 (the final division uses the same stale
-//     maximum for O and the sum, so the result is unchanged); at the end of a
-//     query tile the two groups merge their maxima, sums and O;
+// One persistent launch of 416 threads per CTA, one CTA per SM.  A work item
+// is a pair of 128-query tiles (Q0, Q1) of one (rank, head), so that every
+// K/V tile brought into shared memory serves 256 query rows:
+//   * warp 0 (TMA): the item's two Q tiles, then the K tiles, 128 keys each,
+//     in ring order -- the rank's own block, then the blocks of ranks r-1,
+//     r-2, ... as they land in its receive buffer; warp 12 (TMA): the V tiles;
+//   * warp 1 (MMA): per K/V tile, S_i = Q_i K^T (i = 0, 1) into tensor memory,
+//     and O_i += P_i V with P_i read from tensor memory (tcgen05, bf16 ->
+//     fp32), in the order PV_0(u-1), S_0(u), PV_1(u-1), S_1(u), so that the
+//     product of one query tile runs while the other's softmax works;
+//   * warps 2-5 / 6-9 (softmax of Q0 / Q1): online softmax over the rows of
+//     their query tile, P = 2^(scale * log2(e) * s - m) written as bf16 over
+//     the first 64 columns of S_i in tensor memory (the columns of S already
+//     read); O_i is rescaled only when the maximum grows by more than 2^8
+//     (the final division uses the same stale maximum for O and the sum, so
+//     the result is unchanged); part of the exponentials run as a polynomial
+//     on the FMA pipe beside the hardware ex2; at the end of an item the
+//     group scales O_i by 1 / sum and stores it;
 //   * warps 10-11 (copy): the ring's transfers -- rank r receives the block
 //     of rank (r - j) mod R at step j -- as row copies into its receive
 //     buffer, one counter per (rank, step, head).
-// Causal attention skips the tiles after each query tile (and, in ring order,
+// Causal attention skips the tiles after each query pair (and, in ring order,
 // every block of a later rank: those blocks are not moved either).
 #include <algorithm>
 #include <cmath>
@@ -41,23 +42,33 @@ constexpr int AT_D = 128;                    // head dimension
 constexpr int AT_T = 128;                    // query rows / keys per tile
 constexpr int AT_THREADS = 416;              // 13 warps: see the role list above
 constexpr int AT_MAX_R = 8;
+constexpr int AT_KST = 2;                    // K stages
+constexpr int AT_VST = 2;                    // V stages
 // shared memory (from the 1024-aligned base)
-constexpr uint32_t AT_Q = 0;                 // Q tile: 2 K-major atoms of [128 rows x 128 B]
-constexpr uint32_t AT_KV = 32768;            // 2 stages of K (32 KB) + V (32 KB)
-constexpr uint32_t AT_KV_STAGE = 65536;
-constexpr uint32_t AT_P = AT_KV + 2 * AT_KV_STAGE;   // two P tiles (same layout as Q), by tile parity
-constexpr uint32_t AT_BARS = AT_P + 2 * 32768;
-constexpr uint32_t AT_XCH = AT_BARS + 256;    // row maxima, then row sums, of the softmax warp pairs
-constexpr int AT_SMEM = 1024 + AT_XCH + 2 * AT_T * 4;
+constexpr uint32_t AT_TILE = 32768;          // one 128 x 128 bf16 tile: 2 K-major atoms of [128 rows x 128 B]
+constexpr uint32_t AT_Q = 0;                 // Q0, Q1
+constexpr uint32_t AT_K = 2 * AT_TILE;       // K stages
+constexpr uint32_t AT_V = AT_K + AT_KST * AT_TILE;   // V stages
+constexpr uint32_t AT_BARS = AT_V + AT_VST * AT_TILE;
+constexpr int AT_SMEM = 1024 + AT_BARS + 256;
 // barriers (byte offsets in the barrier block)
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_SFULL = 48, B_PFULL = 80,
-                   B_PFREE = 96, B_OFREE = 112, B_TMEM = 120, B_DRAIN = 128, B_PAIR = 136;
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFIRST = 16, B_KEMPTY = 24, B_VEMPTY = B_KEMPTY + 8 * AT_KST,
+                   B_SFULL = B_VEMPTY + 8 * AT_VST, B_GO = B_SFULL + 16, B_OFULL = B_GO + 16,
+                   B_DRAIN = B_OFULL + 16, B_TMEM = B_DRAIN + 8;
+static_assert(B_TMEM + 4 <= 256, "barrier block");
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
-constexpr uint32_t AT_O_COL = 256;           // O of tile parity b at AT_O_COL + 128 b
-// S = Q K^T: both operands K-major; O += P V: V MN-major
+constexpr uint32_t AT_O_COL = 256;           // O_i at AT_O_COL + 128 i; S_i (and P_i) at 128 i
+// S = Q K^T: both operands K-major; O += P V: P from tensor memory (K-major), V MN-major
 constexpr uint32_t IDESC_S = idesc_bf16_f32(AT_T, AT_T, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(AT_T, AT_D, false, true);
 constexpr float RESCALE_LOG2 = 8.f;          // rescale O when the maximum grows by more than 2^8
+// Of every 16 pairs of exponentials in a 32-key chunk, this many are computed by
+// the polynomial on the FMA pipe, the rest by the hardware ex2 (MUFU).
+#ifndef MK_ATTN_POLY_PAIRS
+#define MK_ATTN_POLY_PAIRS 6
+#endif
+constexpr int POLY_PAIRS = MK_ATTN_POLY_PAIRS;
+static_assert(POLY_PAIRS >= 0 && POLY_PAIRS <= 16, "pairs per chunk");
 
 struct AttnParams {
   CUtensorMap tmQ[AT_MAX_R], tmK[AT_MAX_R], tmV[AT_MAX_R], tmKr[AT_MAX_R], tmVr[AT_MAX_R];
@@ -71,7 +82,7 @@ struct AttnParams {
   long long wait_ns;
   uint32_t epoch;
   float scale_log2;                  // softmax scale * log2(e)
-  int R, heads, s_r, nkt, nqt, causal, n_items;
+  int R, heads, s_r, nkt, nqt, npair, causal, n_items;
   int copy, use_recv, wait;          // ring copies by the copy warps; read them; wait for them
   int n_cw;
   int inject;                        // test only: 1 = one ring piece is never counted
@@ -124,29 +135,32 @@ __device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* 
 
 // ------------------------------------------------------------------ work lists
 struct AtItem {
-  int r, h, qt, n;   // rank, head, query tile, K/V tiles to visit
+  int r, h, qp, n;   // rank, head, query-tile pair (tiles 2qp, 2qp+1), K/V tiles to visit
 };
 // Items run longest first (causal: the last rank's queries see the most keys).
 __device__ __forceinline__ AtItem at_item(const AttnParams& p, int i) {
   AtItem it;
-  const int per_r = p.heads * p.nqt;
+  const int per_r = p.heads * p.npair;
   it.r = p.R - 1 - i / per_r;
   const int rem = i - (p.R - 1 - it.r) * per_r;
-  it.h = rem / p.nqt;
-  it.qt = rem - it.h * p.nqt;
-  it.n = p.causal ? (it.qt + 1) + it.r * p.nkt : p.R * p.nkt;
+  it.h = rem / p.npair;
+  it.qp = rem - it.h * p.npair;
+  it.n = p.causal ? min(2 * it.qp + 2, p.nkt) + it.r * p.nkt : p.R * p.nkt;
   return it;
 }
 // Tile t of an item: ring step j (source rank s = r - j mod R) and key tile kt.
+// Causal: the rank's own block up to the pair's second query tile, then the
+// whole blocks of ranks r-1, r-2, ..., 0.
 __device__ __forceinline__ void at_tile(const AttnParams& p, const AtItem& it, int t, int& j, int& s, int& kt) {
   if (p.causal) {
-    if (t <= it.qt) {
+    const int own = min(2 * it.qp + 2, p.nkt);
+    if (t < own) {
       j = 0;
       s = it.r;
       kt = t;
       return;
     }
-    const int u = t - (it.qt + 1);
+    const int u = t - own;
     j = 1 + u / p.nkt;
     s = it.r - j;
     kt = u - (j - 1) * p.nkt;
@@ -164,207 +178,208 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 }
 
 // ------------------------------------------------------------------ roles
-// TMA producers: warp 0 loads the Q tile of each item and the K tiles, warp 12
-// the V tiles, each into its half of the two K/V stages.  Stage, S, P and O
-// buffer of a tile are all the parity of the CTA's running tile count n.
-// A K stage is free once S of tile n-2 is done (S full), a V stage once the
-// product of tile n-2 is done (P free).  Both land on the P-full barrier of
-// their buffer, V of tile n on the phase of tile n and K of tile n on the
-// phase of tile n-2 (six arrivals: the four softmax warps', the V load's and
-// the K load's, the loads with their bytes).  The MMA issuer's one wait per
-// tile there, before S of tile n and the product of tile n-2, then covers
-// K, P and V.  K of tiles 0 and 1, which have no tile two back, land on
-// their own barriers; after the last tile the K producer still arrives,
-// without bytes, on the two phases that no K tile follows.
-template <bool IS_V>
-__device__ void at_producer(const AttnParams& p, uint32_t bars, uint32_t base) {
-  const uint32_t EMPTY = IS_V ? B_PFREE : B_SFULL;
+// The CTA's K/V tiles, counted over all its items, form one stream u = 0, 1, ...
+// K(u) and V(u) go to stages u % AT_KST and u % AT_VST.  The MMA issuer has one
+// wait per query tile and K/V tile: GO_0 phase u, which completes on four
+// arrivals of the Q0 softmax warps (P_0(u) written), the V(u) load and the
+// K(u+1) load (both with their bytes), and GO_1 phase u (the Q1 softmax warps:
+// P_1(u) written).  K(0) lands on its own barrier.  A producer arms phase u of
+// GO_0 only once phase u-1 has completed, so no arrival can fall into an
+// earlier phase; after its last tile the K producer arrives once more, without
+// bytes, in place of the K tile that no longer follows.
+__device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, int t, bool is_v, int item,
+                                       bool& ready, int& waited_j, const CUtensorMap*& m, int& row) {
+  int j, s, kt;
+  at_tile(p, it, t, j, s, kt);
+  m = is_v ? &p.tmV[s] : &p.tmK[s];
+  row = it.h * p.s_r + kt * AT_T;
+  if (j > 0 && p.use_recv) {
+    if (p.wait && j != waited_j) {
+      if (!ready) {
+        if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, item)) return false;
+        ready = true;
+      }
+      if (!at_wait_value(p, at_counter(p, it.r, j, it.h), 2u * p.nkt, WHERE_PRODUCER, item)) return false;
+      fence_proxy_async_global();
+      waited_j = j;
+    }
+    m = is_v ? &p.tmVr[it.r] : &p.tmKr[it.r];
+    row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
+  }
+  return true;
+}
+
+// K producer (warp 0, one thread): each item's K tiles, and after the first of
+// them its Q0 and Q1 (once the previous item's last S has completed): the
+// item's first K tile completes the phase of GO_0 that the previous item's
+// last product waits for, so it goes before the wait for the query buffer.
+__device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base) {
+  uint32_t q_ph = 0, e_ph = 0;
   int stage = 0;
-  uint32_t ph = 0, q_ph = 0;
-  uint32_t count = 0;        // running tile count n of the next tile
+  uint32_t u = 0;            // stream index of the next K tile
   bool ready = false;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
-    if (!IS_V) {
-      if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) return;
-      q_ph ^= 1u;
-      const int qrow = it.h * p.s_r + it.qt * AT_T;
-      mbar_arrive_expect_tx(bars + B_QFULL, 2u * 16384u);
-      tma_load_2d(base + AT_Q, &p.tmQ[it.r], bars + B_QFULL, 0, qrow);
-      tma_load_2d(base + AT_Q + 16384u, &p.tmQ[it.r], bars + B_QFULL, 64, qrow);
-    }
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
-      int j, s, kt;
-      at_tile(p, it, t, j, s, kt);
-      if (!at_wait_bar(p, bars + EMPTY + 8u * stage, ph ^ 1u, WHERE_PRODUCER, i)) return;
-      const CUtensorMap* m = IS_V ? &p.tmV[s] : &p.tmK[s];
-      int row = it.h * p.s_r + kt * AT_T;
-      if (j > 0 && p.use_recv) {
-        if (p.wait && j != waited_j) {
-          if (!ready) {
-            if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_PRODUCER, i)) return;
-            ready = true;
-          }
-          if (!at_wait_value(p, at_counter(p, it.r, j, it.h), 2u * p.nkt, WHERE_PRODUCER, i)) return;
-          fence_proxy_async_global();
-          waited_j = j;
-        }
-        m = IS_V ? &p.tmVr[it.r] : &p.tmKr[it.r];
-        row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
+      const CUtensorMap* m;
+      int row;
+      if (!at_src(p, it, t, false, i, ready, waited_j, m, row)) return;
+      if (!at_wait_bar(p, bars + B_KEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
+      uint32_t full = bars + B_KFIRST;
+      if (u >= 1) {
+        full = bars + B_GO;   // phase u-1 of GO_0
+        if (u >= 2 && !at_wait_bar(p, full, (u - 2) & 1u, WHERE_PRODUCER, i)) return;
       }
-      const uint32_t dst = base + AT_KV + static_cast<uint32_t>(stage) * AT_KV_STAGE + (IS_V ? 32768u : 0u);
-      const uint32_t full = bars + ((IS_V || count >= 2u) ? B_PFULL : B_KFULL) + 8u * stage;
-      mbar_arrive_expect_tx(full, 32768u);
-      if (IS_V) {
-        tma_load_3d(dst, m, full, 0, row, 0);
-        tma_load_3d(dst + 16384u, m, full, 0, row + 64, 0);
-      } else {
-        tma_load_2d(dst, m, full, 0, row);
-        tma_load_2d(dst + 16384u, m, full, 64, row);
-      }
-      ++count;
-      if (++stage == 2) {
+      const uint32_t dst = base + AT_K + static_cast<uint32_t>(stage) * AT_TILE;
+      mbar_arrive_expect_tx(full, AT_TILE);
+      tma_load_2d(dst, m, full, 0, row);
+      tma_load_2d(dst + 16384u, m, full, 64, row);
+      ++u;
+      if (++stage == AT_KST) {
         stage = 0;
-        ph ^= 1u;
+        e_ph ^= 1u;
+      }
+      if (t == 0) {   // the item's query tiles
+        if (!at_wait_bar(p, bars + B_QEMPTY, q_ph ^ 1u, WHERE_PRODUCER, i)) return;
+        q_ph ^= 1u;
+        const int qrow = it.h * p.s_r + 2 * it.qp * AT_T;
+        mbar_arrive_expect_tx(bars + B_QFULL, 2u * AT_TILE);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          tma_load_2d(base + AT_Q + q * AT_TILE, &p.tmQ[it.r], bars + B_QFULL, 0, qrow + q * AT_T);
+          tma_load_2d(base + AT_Q + q * AT_TILE + 16384u, &p.tmQ[it.r], bars + B_QFULL, 64, qrow + q * AT_T);
+        }
       }
     }
   }
-  if (!IS_V) {
-    // the phases of the last two tiles count a K arrival too: made once S of
-    // those tiles is done, as a K load for the tiles after them would be
-    for (uint32_t n = count; n < count + 2u; ++n) {
-      if (n >= 2u) {
-        if (!at_wait_bar(p, bars + B_SFULL + 8u * stage, ph ^ 1u, WHERE_PRODUCER, 0)) return;
-        mbar_arrive(bars + B_PFULL + 8u * stage);
-      }
-      if (++stage == 2) {
+  // GO_0's last phase (u-1) expects a K arrival too: made without bytes
+  if (u >= 1) {
+    if (u >= 2 && !at_wait_bar(p, bars + B_GO, (u - 2) & 1u, WHERE_PRODUCER, 0)) return;
+    mbar_arrive(bars + B_GO);
+  }
+}
+
+// V producer (warp 12, one thread): V(u) lands on phase u of GO_0.
+__device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base) {
+  uint32_t e_ph = 0;
+  int stage = 0;
+  uint32_t u = 0;
+  bool ready = false;
+  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+    const AtItem it = at_item(p, i);
+    int waited_j = 0;
+    for (int t = 0; t < it.n; ++t) {
+      const CUtensorMap* m;
+      int row;
+      if (!at_src(p, it, t, true, i, ready, waited_j, m, row)) return;
+      if (!at_wait_bar(p, bars + B_VEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
+      if (u >= 1 && !at_wait_bar(p, bars + B_GO, (u - 1) & 1u, WHERE_PRODUCER, i)) return;
+      const uint32_t dst = base + AT_V + static_cast<uint32_t>(stage) * AT_TILE;
+      mbar_arrive_expect_tx(bars + B_GO, AT_TILE);
+      tma_load_3d(dst, m, bars + B_GO, 0, row, 0);
+      tma_load_3d(dst + 16384u, m, bars + B_GO, 0, row + 64, 0);
+      ++u;
+      if (++stage == AT_VST) {
         stage = 0;
-        ph ^= 1u;
+        e_ph ^= 1u;
       }
     }
   }
 }
 
-// MMA issuer.  The CTA's n-th tile (counted over all its items) uses K/V
-// stage, S, P and O buffers n & 1: the softmax of the even ones (warps 2-5)
-// and of the odd ones (warps 6-9) each keep their own running maximum, sum
-// and O for the item; they are merged when the item ends.
-//
-// Issue order: when the softmax of running tile n-2 has published P (one
-// wait, which also covers V of that tile and frees S buffer n & 1), the
-// issuer starts S of tile n first and then the product of tile n-2, so the
-// softmax group's next S is not queued behind a product.  Per tile one
-// mbarrier wait besides the K tile and two commits: S full (which also frees
-// the K stage) and P free (which also frees the V stage and marks O
-// updated).  Every wait and commit in this thread stalls the tensor pipe's
-// short queue, so there are no others.
-__device__ __forceinline__ void at_pv(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, int pb,
-                                      int tile) {
-  const uint32_t vb = base + AT_KV + static_cast<uint32_t>(pb) * AT_KV_STAGE + 32768u;
-  const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(pb);
-  const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(pb) * AT_T;
+// S_i = Q_i K(u)^T into S_i (columns 128 i): 8 MMAs of K = 16.
+__device__ __forceinline__ void at_s(uint32_t base, uint32_t tmem, int i, int kstage) {
+  const uint32_t qb = base + AT_Q + static_cast<uint32_t>(i) * AT_TILE;
+  const uint32_t kb = base + AT_K + static_cast<uint32_t>(kstage) * AT_TILE;
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint64_t ad = sdesc_swz(pbase + 16384u * a + 32u * k, 16u, 1024u, 2u);
-      const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
-      // the first product of each O buffer in an item (tiles 0 and 1) overwrites it
-      tc_mma_bf16(obuf, ad, bd, IDESC_PV, (tile >= 2 || a || k) ? 1u : 0u);
+      const uint64_t ad = sdesc_swz(qb + 16384u * a + 32u * k, 16u, 1024u, 2u);
+      const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
+      tc_mma_bf16(tmem + static_cast<uint32_t>(i) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
     }
-  tc_commit(bars + B_PFREE + 8u * pb);   // P buffer and V stage free; O[pb] holds this product
+}
+// O_i (+)= P_i V(u): P_i (keys 2c, 2c+1 in column c of S_i) from tensor memory, V MN-major
+// (two 64-column atoms 8 KB apart, 8-key groups 1024 B apart).
+__device__ __forceinline__ void at_pv(uint32_t base, uint32_t tmem, int i, int vstage, bool first) {
+  const uint32_t vb = base + AT_V + static_cast<uint32_t>(vstage) * AT_TILE;
+  const uint32_t pcol = tmem + static_cast<uint32_t>(i) * AT_T;
+  const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(i) * AT_T;
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
+      tc_mma_bf16_ts(obuf, pcol + 32u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
+    }
 }
 
+// MMA issuer (warp 1, one thread).  Iteration u: [GO_0 phase u-1] PV_0(u-1),
+// S_0(u), [GO_1 phase u-1] PV_1(u-1), S_1(u).  A product of tile u-1 is issued
+// before the S of tile u that overwrites its P: the tensor pipe runs a
+// thread's MMAs in issue order.  Commits: S_i full after each S_i (for S_1 also
+// the K stage free), V stage free after PV_1, the query tiles free after an
+// item's last S_1, O_i full after an item's last PV_i.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, of_ph = 0;
-  uint32_t pf_ph = 0;        // phase bits of the P-full barriers, bit b for buffer b
-  int stage = 0;
-  // products not yet issued: the tile two back (pend2) and one back (pend1),
-  // as their tile index within their item (-1: none)
-  int pend2 = -1, pend1 = -1;
+  uint32_t q_ph = 0, go_ph = 0;
+  uint32_t u = 0;
+  int kst = 0, vst = 0;
+  bool prev_first = false, prev_last = false;   // the pending tile u-1 opens / closes its item
   int item = -1;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
     item = i;
-    if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
-    q_ph ^= 1u;
-    for (int t = 0; t < it.n; ++t) {
-      const int b = stage;
-      if (pend2 >= 0) {
-        // P and V of the tile two back (same buffer; S buffer b is free too)
-        // and K of this tile
-        if (!at_wait_bar(p, bars + B_PFULL + 8u * b, (pf_ph >> b) & 1u, WHERE_MMA, i)) goto done;
-        pf_ph ^= 1u << b;
-        if (pend2 == 0) {   // first product of an item: the previous item's O has been read out
-          if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, i)) goto done;
-          of_ph ^= 1u;
-        }
+    for (int t = 0; t < it.n; ++t, ++u) {
+      if (u == 0) {
+        if (!at_wait_bar(p, bars + B_KFIRST, 0u, WHERE_MMA, i)) goto done;
       } else {
-        // the CTA's first two tiles: K on its own barrier
-        if (!at_wait_bar(p, bars + B_KFULL + 8u * b, 0u, WHERE_MMA, i)) goto done;
+        // P_0(u-1), V(u-1) and K(u) are ready
+        if (!at_wait_bar(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+        tc_fence_after();
+        at_pv(base, tmem, 0, vst, prev_first);
+        if (prev_last) tc_commit(bars + B_OFULL);
+      }
+      if (t == 0) {
+        if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
+        q_ph ^= 1u;
       }
       tc_fence_after();
-      {
-        const uint32_t kb = base + AT_KV + static_cast<uint32_t>(b) * AT_KV_STAGE;
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_swz(base + AT_Q + 16384u * a + 32u * k, 16u, 1024u, 2u);
-            const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
-            tc_mma_bf16(tmem + static_cast<uint32_t>(b) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
-          }
-        tc_commit(bars + B_SFULL + 8u * b);              // S ready; this K stage may be refilled
-        if (t == it.n - 1) tc_commit(bars + B_QEMPTY);   // Q is read by no later MMA of this item
+      at_s(base, tmem, 0, kst);
+      tc_commit(bars + B_SFULL);
+      if (u >= 1) {
+        if (!at_wait_bar(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
+        go_ph ^= 1u;
+        tc_fence_after();
+        at_pv(base, tmem, 1, vst, prev_first);
+        tc_commit(bars + B_VEMPTY + 8u * vst);   // V(u-1) read by both products
+        if (prev_last) tc_commit(bars + B_OFULL + 8u);
+        if (++vst == AT_VST) vst = 0;
       }
-      if (pend2 >= 0) at_pv(p, bars, base, tmem, b, pend2);
-      pend2 = pend1;
-      pend1 = t;
-      if (++stage == 2) stage = 0;
+      at_s(base, tmem, 1, kst);
+      tc_commit(bars + B_SFULL + 8u);
+      tc_commit(bars + B_KEMPTY + 8u * kst);     // K(u) read by both S
+      if (t == it.n - 1) tc_commit(bars + B_QEMPTY);
+      if (++kst == AT_KST) kst = 0;
+      prev_first = (t == 0);
+      prev_last = (t == it.n - 1);
     }
   }
-  // the last two products (tiles two back and one back of the running count)
-  for (int r = 0; r < 2; ++r) {
-    if (pend2 >= 0) {
-      const int b = stage;
-      if (!at_wait_bar(p, bars + B_PFULL + 8u * b, (pf_ph >> b) & 1u, WHERE_MMA, item)) goto done;
-      pf_ph ^= 1u << b;
-      if (pend2 == 0) {
-        if (!at_wait_bar(p, bars + B_OFREE, of_ph ^ 1u, WHERE_MMA, item)) goto done;
-        of_ph ^= 1u;
-      }
-      tc_fence_after();
-      at_pv(p, bars, base, tmem, b, pend2);
-    }
-    pend2 = pend1;
-    pend1 = -1;
-    if (++stage == 2) stage = 0;
+  if (u >= 1) {   // the products of the last tile
+    if (!at_wait_bar(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
+    tc_fence_after();
+    at_pv(base, tmem, 0, vst, prev_first);
+    tc_commit(bars + B_OFULL);
+    if (!at_wait_bar(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
+    tc_fence_after();
+    at_pv(base, tmem, 1, vst, prev_first);
+    tc_commit(bars + B_VEMPTY + 8u * vst);
+    tc_commit(bars + B_OFULL + 8u);
   }
 done:
   tc_commit(bars + B_DRAIN);
   at_wait_bar(p, bars + B_DRAIN, 0, WHERE_DRAIN, 0, false);
-}
-
-// P tile element (row, key): K-major, 128-byte swizzle, two 64-key atoms.
-__device__ __forceinline__ uint32_t p_chunk_addr(uint32_t pbase, int row, int kchunk) {
-  // kchunk: 8-key group 0..15
-  const int atom = kchunk >> 3, c = kchunk & 7;
-  return pbase + static_cast<uint32_t>(atom) * 16384u + static_cast<uint32_t>(row >> 3) * 1024u +
-         static_cast<uint32_t>(row & 7) * 128u + static_cast<uint32_t>((c ^ (row & 7)) << 4);
-}
-
-// Softmax warps 2-9: warp w handles TMEM lanes 32*(w%4) .. +31 (query rows)
-// and half (w-2)/4 of the 128 columns (keys of S, head dims of O).  The two
-// warps of a row quarter exchange their row maxima and, at the end, their row
-// sums through shared memory, meeting at a two-arrival mbarrier (a bounded
-// wait, so that one warp leaving on an abort cannot strand the other).
-__device__ __forceinline__ bool pair_sync(const AttnParams& p, uint32_t bar, uint32_t& ph, int item) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const int ok = at_wait_bar(p, bar, ph, WHERE_EPILOGUE, item) ? 1 : 0;
-  ph ^= 1u;
-  return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // 2^x for x <= 0 or -inf (the hardware approximation, flushing subnormals).
@@ -398,35 +413,56 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-__device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem, float* xch) {
+// Two values of 2^x on the FMA pipe, for -125 <= x <= 64 (smaller x are clamped:
+// the result, <= 2^-125, is below anything a row keeps).  Range reduction:
+// x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low mantissa
+// bits) and |f| <= 1/2, then 2^f by a cubic 1 + f (c1 + f (c2 + f c3)) fitted to
+// 2^f on [-1/2, 1/2] (relative error below 1.3e-4, far under bf16's 2^-9), and
+// n added to the exponent field: the bits of 1.5 * 2^23 + n shifted left by 23
+// are n << 23, since the constant's low nine bits are zero.
+__device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& y1) {
+  constexpr float SHIFT = 12582912.f;            // 1.5 * 2^23
+  const uint64_t xs = f2pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
+  const uint64_t t = f2add(xs, f2pack(SHIFT, SHIFT));
+  const uint64_t n = f2add(t, f2pack(-SHIFT, -SHIFT));
+  const uint64_t f = f2fma(n, f2pack(-1.f, -1.f), xs);   // exact: x - round(x)
+  uint64_t q = f2fma(f, f2pack(0.05533514f, 0.05533514f), f2pack(0.24229739f, 0.24229739f));
+  q = f2fma(q, f, f2pack(0.69322545f, 0.69322545f));
+  q = f2fma(q, f, f2pack(1.f, 1.f));
+  float q0, q1, t0, t1;
+  f2unpack(q, q0, q1);
+  f2unpack(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
+// Softmax of query tile g (warps 2-5: g = 0, warps 6-9: g = 1): warp w handles
+// TMEM lanes 32 (w % 4) .. +31, one query row per thread, all 128 columns.
+__device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int grp = (warp - 2) >> 2;                           // 0: even tiles, 1: odd tiles (running count)
+  const int g = (warp - 2) >> 2;                             // query tile of the pair
   const int row = quarter * 32 + lane;                       // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t pbar = bars + B_PAIR + 8u * quarter;
-  const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(grp) * AT_T;
-  const uint32_t obase = tmem + lane_off + AT_O_COL;
-  const uint32_t pbase = base + AT_P + 32768u * static_cast<uint32_t>(grp);
+  const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(g) * AT_T;
+  const uint32_t obase = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(g) * AT_T;
+  const uint32_t sfull = bars + B_SFULL + 8u * g, go = bars + B_GO + 8u * g, ofull = bars + B_OFULL + 8u * g;
   const float c = p.scale_log2;
-  uint32_t pair_ph = 0, sf_ph = 0, uses = 0;
-  uint32_t count = 0;                                        // tiles of the CTA's earlier items
+  uint32_t sf_ph = 0, of_ph = 0;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
-    const int qpos = it.qt * AT_T + row;                     // position within rank r's block
-    const int par = static_cast<int>(count & 1u);
-    const int t0 = grp ^ par;                                // this group's first tile of the item
-    count += static_cast<uint32_t>(it.n);
+    const int qt = 2 * it.qp + g;
+    const int qpos = qt * AT_T + row;                        // position within rank r's block
     float m_run = -INFINITY, l_run = 0.f;
-    for (int t = t0; t < it.n; t += 2) {
+    for (int t = 0; t < it.n; ++t) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
       const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
-      const bool diag = p.causal && j == 0 && kt == it.qt;   // keys after the query are masked
-      const int lim = diag ? min(valid, row + 1) : valid;
+      int lim = valid;
+      if (p.causal && j == 0) lim = (kt > qt) ? 0 : (kt == qt ? min(valid, row + 1) : valid);
       const bool masked = __any_sync(0xffffffffu, lim < AT_T);
       {
-        int ok = at_wait_bar(p, bars + B_SFULL + 8u * grp, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
+        const int ok = at_wait_bar(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
         if (!__all_sync(0xffffffffu, ok)) return;
       }
       sf_ph ^= 1u;
@@ -455,13 +491,10 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         }
       }
       const float m_new = fmaxf(m_run, mx * c);
-      // the product that last read this P buffer (and wrote this O) has completed
-      if (uses > 0u) {
-        int ok = at_wait_bar(p, bars + B_PFREE + 8u * grp, (uses - 1u) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, ok)) return;
-      }
+      // S_i(u) complete implies the product of tile u-1 complete (issued before
+      // it): O_i is settled until this group publishes P_i(u)
       float factor = 1.f;
-      if (t == t0) {
+      if (t == 0) {
         m_run = m_new;
       } else if (m_new > m_run + RESCALE_LOG2) {
         factor = ex2(m_run - m_new);
@@ -469,21 +502,18 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         l_run *= factor;
       }
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        tc_fence_after();
-        const uint32_t ob = obase + static_cast<uint32_t>(grp) * AT_T;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t v[32];
-          tc_ld_32x32b_x32(ob + 32u * cc, v);
+          tc_ld_32x32b_x32(obase + 32u * cc, v);
           tc_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
-          tc_st_32x32b_x32(ob + 32u * cc, v);
+          tc_st_32x32b_x32(obase + 32u * cc, v);
         }
-        tc_wait_st();
       }
-      // pass 2: P = 2^(c*s - m), the running sum, P as bf16 into shared memory
-      // (two lanes per packed fp32 fused multiply-add / add)
+      // pass 2: P = 2^(c*s - m), the running sum, P as bf16 pairs into columns
+      // 16cc .. 16cc+15 of S_i (S columns 0 .. 32cc+31 have been read by then)
       const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_run, -m_run);
       uint64_t l2 = f2pack(0.f, 0.f);
 #pragma unroll 1
@@ -491,88 +521,65 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t base, ui
         uint32_t v[32];
         tc_ld_32x32b_x32(sbase + 32u * cc, v);
         tc_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {   // 8 keys per 16-byte chunk
-          uint32_t pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int kk = 32 * cc + 8 * k8 + 2 * q;
-            float e0, e1;
-            f2unpack(f2fma(f2pack(__uint_as_float(v[8 * k8 + 2 * q]), __uint_as_float(v[8 * k8 + 2 * q + 1])), c2,
-                           nm2),
-                     e0, e1);
-            float p0 = ex2(e0), p1 = ex2(e1);
-            if (masked) {
-              p0 = (kk < lim) ? p0 : 0.f;
-              p1 = (kk + 1 < lim) ? p1 : 0.f;
-            }
-            l2 = f2add(l2, f2pack(p0, p1));
-            pk[q] = pack_bf16x2(p0, p1);
+        for (int q = 0; q < 16; ++q) {
+          const int kk = 32 * cc + 2 * q;
+          float e0, e1, p0, p1;
+          f2unpack(f2fma(f2pack(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1])), c2, nm2), e0, e1);
+          if ((q & 7) < (POLY_PAIRS >> 1) + ((q >> 3) < (POLY_PAIRS & 1) ? 1 : 0)) {
+            ex2_poly2(e0, e1, p0, p1);
+          } else {
+            p0 = ex2(e0);
+            p1 = ex2(e1);
           }
-          const uint32_t a = p_chunk_addr(pbase, row, 4 * cc + k8);
-          asm volatile("st.shared::cta.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
-                       "r"(pk[2]), "r"(pk[3])
-                       : "memory");
+          if (masked) {
+            p0 = (kk < lim) ? p0 : 0.f;
+            p1 = (kk + 1 < lim) ? p1 : 0.f;
+          }
+          l2 = f2add(l2, f2pack(p0, p1));
+          pk[q] = pack_bf16x2(p0, p1);
         }
+        tc_st_32x32b_x16(sbase + 16u * cc, pk);
       }
       {
         float la, lb;
         f2unpack(l2, la, lb);
         l_run += la + lb;
       }
-      // S read out: the MMA may overwrite it; P written: the product may read it
-      fence_proxy_async_smem();
+      // P_i(u) (and any rescaled O_i) written: the products may read them
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bars + B_PFULL + 8u * grp);
-      }
-      ++uses;
+      if (lane == 0) mbar_arrive(go);
     }
-    // item done: this group's last product has completed
-    if (t0 < it.n) {
-      int ok = at_wait_bar(p, bars + B_PFREE + 8u * grp, (uses - 1u) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
+    // item done: the last product into O_i has completed
+    {
+      const int ok = at_wait_bar(p, ofull, of_ph, WHERE_EPILOGUE, i) ? 1 : 0;
       if (!__all_sync(0xffffffffu, ok)) return;
     }
-    // merge the two groups' (maximum, sum, O): exchange maxima, then scaled sums
-    xch[grp * AT_T + row] = m_run;
-    if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const float m0 = xch[row], m1 = xch[AT_T + row];
-    if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const bool h0 = par < it.n, h1 = (par ^ 1) < it.n;       // the group had tiles of this item
-    const float m = h0 ? (h1 ? fmaxf(m0, m1) : m0) : m1;
-    const float f0 = h0 ? ex2(m0 - m) : 0.f, f1 = h1 ? ex2(m1 - m) : 0.f;
-    xch[grp * AT_T + row] = l_run * (grp ? f1 : f0);
-    if (!pair_sync(p, pbar, pair_ph, i)) return;
-    const float l_all = (h0 ? xch[row] : 0.f) + (h1 ? xch[AT_T + row] : 0.f);
-    if (!pair_sync(p, pbar, pair_ph, i)) return;
+    of_ph ^= 1u;
     tc_fence_after();
-    const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
+    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
     const bool row_ok = qpos < p.s_r;
-    const int c0 = 64 * grp;                                 // this group writes output columns c0 .. c0+63
-    uint8_t* orow = p.out[it.r] + ((static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D + c0) * 2;
+    uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2;
 #pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-      uint32_t v0[32], v1[32];
-      tc_ld_32x32b_x32(obase + static_cast<uint32_t>(c0 + 32 * cc), v0);
-      tc_ld_32x32b_x32(obase + AT_T + static_cast<uint32_t>(c0 + 32 * cc), v1);
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[32];
+      tc_ld_32x32b_x32(obase + 32u * cc, v);
       tc_wait_ld();
       if (!row_ok) continue;
-      float o[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q)
-        o[q] = (h0 ? (h1 ? fmaf(__uint_as_float(v0[q]), f0, __uint_as_float(v1[q]) * f1)
-                         : __uint_as_float(v0[q]) * f0)
-                   : __uint_as_float(v1[q]) * f1) * inv;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        st_global_v4(orow + (32 * cc + 8 * q) * 2, pack_bf16x2(o[8 * q], o[8 * q + 1]),
-                     pack_bf16x2(o[8 * q + 2], o[8 * q + 3]), pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
-                     pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+        st_global_v4(orow + (32 * cc + 8 * q) * 2,
+                     pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
     }
+    // O_i read out: the next item's first product may overwrite it once this
+    // group has published that item's first P (the wait before that product)
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + B_OFREE);
   }
 }
 
@@ -660,17 +667,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   if (warp == 0 && lane == 0) {
     mbar_init(bars + B_QFULL, 1);
     mbar_init(bars + B_QEMPTY, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bars + B_KFULL + 8u * s, 1);
-      mbar_init(bars + B_SFULL + 8u * s, 1);
+    mbar_init(bars + B_KFIRST, 1);
+    for (int s = 0; s < AT_KST; ++s) mbar_init(bars + B_KEMPTY + 8u * s, 1);
+    for (int s = 0; s < AT_VST; ++s) mbar_init(bars + B_VEMPTY + 8u * s, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bars + B_SFULL + 8u * g, 1);
+      mbar_init(bars + B_OFULL + 8u * g, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + B_PFULL + 8u * b, 6);   // four softmax warps, the V load, the K load
-      mbar_init(bars + B_PFREE + 8u * b, 1);
-    }
-    mbar_init(bars + B_OFREE, 8);
+    mbar_init(bars + B_GO, 6);          // Q0 softmax warps, the V load, the next K load
+    mbar_init(bars + B_GO + 8u, 4);     // Q1 softmax warps
     mbar_init(bars + B_DRAIN, 1);       // MMA drain
-    for (int qq = 0; qq < 4; ++qq) mbar_init(bars + B_PAIR + 8u * qq, 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -683,15 +689,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   const uint32_t tmem = *tmem_slot;
   if (warp == 0 || warp == 12) {
     if (lane == 0) {
-      if (warp == 0) at_producer<false>(p, bars, base);
-      else at_producer<true>(p, bars, base);
+      if (warp == 0) at_producer_k(p, bars, base);
+      else at_producer_v(p, bars, base);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) at_mma(p, bars, base, tmem);
     __syncwarp();
   } else if (warp <= 9) {
-    at_softmax(p, bars, base, tmem, reinterpret_cast<float*>(smem + AT_XCH));
+    at_softmax(p, bars, tmem);
     __syncwarp();
   } else if (warp <= 11 && p.copy) {
     at_copy(p);
@@ -791,6 +797,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
   p.s_r = static_cast<int>(s_r);
   p.nkt = L.nkt;
   p.nqt = L.nqt;
+  p.npair = (L.nqt + 1) / 2;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.cnt_off);
@@ -816,7 +823,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
         return MK_ERR_CUDA;
     }
   }
-  const int n_items = R * heads * L.nqt;
+  const int n_items = R * heads * p.npair;
   const int grid = std::max(1, std::min(sms, n_items));
   if (mode == MK_MODE_GEMM_ONLY || R == 1) {   // K/V read from the source ranks: no ring
     p.n_items = n_items;

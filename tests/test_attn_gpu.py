@@ -141,3 +141,19 @@ def test_ring_attention_full_size_row_sample(causal):
     for r in range(w.R):
         got = gpu_values(out[r][:, torch.from_numpy(rows[r]).cuda()])
         assert _err(got, exact[r].astype(np.float64), vmax) <= ATT_TOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_attention_large_scores(causal):
+    # scale 1 instead of 1/sqrt(d): scores with a standard deviation near 11, so the
+    # running maximum grows by more than 2^8 within a row (O rescaled) and most
+    # exponentials fall far below 2^-100 (the clamped end of the polynomial)
+    w = I.AttnWorkload("t", R=2, heads=2, s_r=384, causal=causal, q_seed=56, k_seed=66, v_seed=76)
+    q, k, v = I.attn_inputs(w)
+    out = mk.ring_attention(dev(q), dev(k), dev(v), causal=causal, scale=1.0)
+    _ok()
+    exact = O.ring_attention([I.bits(t) for t in q], [I.bits(t) for t in k], [I.bits(t) for t in v],
+                             causal, 1.0, out="f32")
+    vmax = max(float(t.float().abs().max()) for t in v)
+    for r in range(w.R):
+        assert _err(gpu_values(out[r]), exact[r].astype(np.float64), vmax) <= ATT_TOL
