@@ -4,25 +4,25 @@
 // while each rank attends its queries to every block that has arrived,
 // merging the partial softmax results.
 //
-// One persistent launch of 416 threads per CTA, one CTA per SM.  A work item
+// One persistent launch of 384 threads per CTA, one CTA per SM.  A work item
 // is a pair of 128-query tiles (Q0, Q1) of one (rank, head), so that every
 // K/V tile brought into shared memory serves 256 query rows:
 //   * warp 0 (TMA): the item's two Q tiles, then the K tiles, 128 keys each,
 //     in ring order -- the rank's own block, then the blocks of ranks r-1,
-//     r-2, ... as they land in its receive buffer; warp 12 (TMA): the V tiles;
+//     r-2, ... as they land in its receive buffer; warp 11 (TMA): the V tiles;
 //   * warp 1 (MMA): per K/V tile, S_i = Q_i K^T (i = 0, 1) into tensor memory,
 //     and O_i += P_i V with P_i read from tensor memory (tcgen05, bf16 ->
 //     fp32), in the order PV_0(u-1), S_0(u), PV_1(u-1), S_1(u), so that the
 //     product of one query tile runs while the other's softmax works;
 //   * warps 2-5 / 6-9 (softmax of Q0 / Q1): online softmax over the rows of
-//     their query tile, P = 2^(scale * log2(e) * s - m) written as bf16 over
-//     the first 64 columns of S_i in tensor memory (the columns of S already
-//     read); O_i is rescaled only when the maximum grows by more than 2^8
+//     their query tile, each thread one row held in registers, P = 2^(scale *
+//     log2(e) * s - m) written as bf16 over the first 64 columns of S_i in
+//     tensor memory; O_i is rescaled only when the maximum grows by more than 2^8
 //     (the final division uses the same stale maximum for O and the sum, so
 //     the result is unchanged); part of the exponentials run as a polynomial
 //     on the FMA pipe beside the hardware ex2; at the end of an item the
 //     group scales O_i by 1 / sum and stores it;
-//   * warps 10-11 (copy): the ring's transfers -- rank r receives the block
+//   * warp 10 (copy): the ring's transfers -- rank r receives the block
 //     of rank (r - j) mod R at step j -- as row copies into its receive
 //     buffer, one counter per (rank, step, head).
 // Causal attention skips the tiles after each query pair (and, in ring order,
@@ -40,7 +40,8 @@ namespace {
 
 constexpr int AT_D = 128;                    // head dimension
 constexpr int AT_T = 128;                    // query rows / keys per tile
-constexpr int AT_THREADS = 416;              // 13 warps: see the role list above
+constexpr int AT_THREADS = 384;              // 12 warps: see the role list above
+constexpr int AT_WARP_COPY = 10, AT_WARP_V = 11;
 constexpr int AT_MAX_R = 8;
 constexpr int AT_KST = 2;                    // K stages
 constexpr int AT_VST = 2;                    // V stages
@@ -62,13 +63,21 @@ constexpr uint32_t AT_O_COL = 256;           // O_i at AT_O_COL + 128 i; S_i (an
 constexpr uint32_t IDESC_S = idesc_bf16_f32(AT_T, AT_T, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(AT_T, AT_D, false, true);
 constexpr float RESCALE_LOG2 = 8.f;          // rescale O when the maximum grows by more than 2^8
-// Of every 16 pairs of exponentials in a 32-key chunk, this many are computed by
-// the polynomial on the FMA pipe, the rest by the hardware ex2 (MUFU).
+// Of every 16 pairs of exponentials in a row, this many are computed by the
+// polynomial on the FMA pipe, the rest by the hardware ex2 (MUFU).
 #ifndef MK_ATTN_POLY_PAIRS
-#define MK_ATTN_POLY_PAIRS 6
+#define MK_ATTN_POLY_PAIRS 0
 #endif
 constexpr int POLY_PAIRS = MK_ATTN_POLY_PAIRS;
-static_assert(POLY_PAIRS >= 0 && POLY_PAIRS <= 16, "pairs per chunk");
+// How P becomes bf16: 0 = cvt.rn.bf16x2.f32 (round to nearest even, on the
+// conversion pipe); 1 = the exponentials are taken 2^-9 high (log2(1 + 2^-9)
+// added to the argument), the two upper halves kept by one byte permute (which
+// then rounds to within half a bf16 unit), and the row sum divided by the same
+// 1 + 2^-9 at the end.
+#ifndef MK_ATTN_PACK
+#define MK_ATTN_PACK 0
+#endif
+static_assert(POLY_PAIRS >= 0 && POLY_PAIRS <= 16, "pairs per 16");
 
 struct AttnParams {
   CUtensorMap tmQ[AT_MAX_R], tmK[AT_MAX_R], tmV[AT_MAX_R], tmKr[AT_MAX_R], tmVr[AT_MAX_R];
@@ -99,14 +108,16 @@ __device__ __noinline__ void at_error(const AttnParams& p, int where, int item) 
   __threadfence();
   atomicExch(&p.hdr[HDR_ABORT], p.epoch);
 }
-__device__ __noinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
-                                         bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The bounded wait loop.  SPIN: poll with the non-blocking test (the MMA
+// issuer and the softmax warps, whose waits sit on the critical path).
+template <bool SPIN>
+__device__ __noinline__ bool at_wait_loop(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
+                                          bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++it & 31u) == 0) {
+    if (SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if ((++it & (SPIN ? 255u : 31u)) == 0) {
       if (honor_abort && at_aborted(p)) return false;
       if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
         at_error(p, where, item);
@@ -114,6 +125,14 @@ __device__ __noinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, uint
       }
     }
   }
+}
+// Bounded mbarrier wait.  The first test is inline: a call into the loop costs
+// the issuing thread a few hundred cycles even when the phase has completed.
+template <bool SPIN = false>
+__device__ __forceinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
+                                            bool honor_abort = true) {
+  if (SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return at_wait_loop<SPIN>(p, bar, parity, where, item, honor_abort);
 }
 __device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* f, uint32_t want, int where,
                                            int item) {
@@ -260,7 +279,7 @@ __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base)
   }
 }
 
-// V producer (warp 12, one thread): V(u) lands on phase u of GO_0.
+// V producer (warp 11, one thread): V(u) lands on phase u of GO_0.
 __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base) {
   uint32_t e_ph = 0;
   int stage = 0;
@@ -292,12 +311,14 @@ __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base)
 __device__ __forceinline__ void at_s(uint32_t base, uint32_t tmem, int i, int kstage) {
   const uint32_t qb = base + AT_Q + static_cast<uint32_t>(i) * AT_TILE;
   const uint32_t kb = base + AT_K + static_cast<uint32_t>(kstage) * AT_TILE;
+  // descriptors differ only in the start address field (address >> 4, low bits)
+  const uint64_t dq = sdesc_swz(qb, 16u, 1024u, 2u), dk = sdesc_swz(kb, 16u, 1024u, 2u);
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint64_t ad = sdesc_swz(qb + 16384u * a + 32u * k, 16u, 1024u, 2u);
-      const uint64_t bd = sdesc_swz(kb + 16384u * a + 32u * k, 16u, 1024u, 2u);
+      const uint64_t ad = dq + ((16384u * a + 32u * k) >> 4);
+      const uint64_t bd = dk + ((16384u * a + 32u * k) >> 4);
       tc_mma_bf16(tmem + static_cast<uint32_t>(i) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
     }
 }
@@ -307,11 +328,12 @@ __device__ __forceinline__ void at_pv(uint32_t base, uint32_t tmem, int i, int v
   const uint32_t vb = base + AT_V + static_cast<uint32_t>(vstage) * AT_TILE;
   const uint32_t pcol = tmem + static_cast<uint32_t>(i) * AT_T;
   const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(i) * AT_T;
+  const uint64_t dv = sdesc_sw128(vb, 8192u, 1024u);
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint64_t bd = sdesc_sw128(vb + 16384u * a + 2048u * k, 8192u, 1024u);
+      const uint64_t bd = dv + ((16384u * a + 2048u * k) >> 4);
       tc_mma_bf16_ts(obuf, pcol + 32u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
     }
 }
@@ -336,7 +358,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
         if (!at_wait_bar(p, bars + B_KFIRST, 0u, WHERE_MMA, i)) goto done;
       } else {
         // P_0(u-1), V(u-1) and K(u) are ready
-        if (!at_wait_bar(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_bar<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
         tc_fence_after();
         at_pv(base, tmem, 0, vst, prev_first);
         if (prev_last) tc_commit(bars + B_OFULL);
@@ -349,7 +371,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       at_s(base, tmem, 0, kst);
       tc_commit(bars + B_SFULL);
       if (u >= 1) {
-        if (!at_wait_bar(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_bar<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
         go_ph ^= 1u;
         tc_fence_after();
         at_pv(base, tmem, 1, vst, prev_first);
@@ -367,11 +389,11 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     }
   }
   if (u >= 1) {   // the products of the last tile
-    if (!at_wait_bar(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_bar<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 0, vst, prev_first);
     tc_commit(bars + B_OFULL);
-    if (!at_wait_bar(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_bar<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 1, vst, prev_first);
     tc_commit(bars + B_VEMPTY + 8u * vst);
@@ -432,12 +454,16 @@ __device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& 
   float q0, q1, t0, t1;
   f2unpack(q, q0, q1);
   f2unpack(t, t0, t1);
-  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+  uint32_t r0, r1;
+  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r0) : "r"(__float_as_uint(t0)), "r"(__float_as_uint(q0)));
+  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r1) : "r"(__float_as_uint(t1)), "r"(__float_as_uint(q1)));
+  y0 = __uint_as_float(r0);
+  y1 = __uint_as_float(r1);
 }
 
 // Softmax of query tile g (warps 2-5: g = 0, warps 6-9: g = 1): warp w handles
-// TMEM lanes 32 (w % 4) .. +31, one query row per thread, all 128 columns.
+// TMEM lanes 32 (w % 4) .. +31, one query row per thread, all 128 columns held
+// in registers (four loads of 32 columns, one wait).
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -462,37 +488,40 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
       if (p.causal && j == 0) lim = (kt > qt) ? 0 : (kt == qt ? min(valid, row + 1) : valid);
       const bool masked = __any_sync(0xffffffffu, lim < AT_T);
       {
-        const int ok = at_wait_bar(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
+        const int ok = at_wait_bar<true>(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
         if (!__all_sync(0xffffffffu, ok)) return;
       }
       sf_ph ^= 1u;
       tc_fence_after();
-      // pass 1: the row maximum (scale > 0 keeps the order: taken unscaled); the
-      // next 32 columns load while these are reduced
-      float mx = -INFINITY;
-      {
-        uint32_t va[32], vb[32];
-        tc_ld_32x32b_x32(sbase, va);
-        tc_wait_ld_regs(va);
+      uint32_t sv[4][32];
+      tc_ld_32x32b_x32(sbase, sv[0]);
+      tc_ld_32x32b_x32(sbase + 32u, sv[1]);
+      tc_ld_32x32b_x32(sbase + 64u, sv[2]);
+      tc_ld_32x32b_x32(sbase + 96u, sv[3]);
+      tc_wait_ld_regs(sv[0]);
+      reg_fence(sv[1]);
+      reg_fence(sv[2]);
+      reg_fence(sv[3]);
+      // the row maximum (scale > 0 keeps the order: taken unscaled), four
+      // partial maxima so that the dependent chain is a quarter as long
+      float mx;
+      if (masked) {
+        mx = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t (&cur)[32] = (cc & 1) ? vb : va;
-          uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
-          if (cc < 3) tc_ld_32x32b_x32(sbase + 32u * (cc + 1), nxt);
-          if (masked) {
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(cur[q]));
-          } else {
+          for (int q = 0; q < 32; ++q)
+            if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(sv[cc][q]));
+      } else {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int q = 0; q < 32; q += 2) mx = fmax3(mx, __uint_as_float(cur[q]), __uint_as_float(cur[q + 1]));
-          }
-          if (cc < 3) tc_wait_ld_regs(nxt);
-        }
+        for (int q = 0; q < 32; q += 2)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            m4[cc] = fmax3(m4[cc], __uint_as_float(sv[cc][q]), __uint_as_float(sv[cc][q + 1]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       const float m_new = fmaxf(m_run, mx * c);
-      // S_i(u) complete implies the product of tile u-1 complete (issued before
-      // it): O_i is settled until this group publishes P_i(u)
       float factor = 1.f;
       if (t == 0) {
         m_run = m_new;
@@ -501,6 +530,54 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
         m_run = m_new;
         l_run *= factor;
       }
+      // P = 2^(c*s - m), four partial sums, P as bf16 pairs (keys 2q, 2q+1 in
+      // column q) over columns 0 .. 63 of S_i
+#if MK_ATTN_PACK
+      constexpr float PACK_BIAS = 0.0028150156f;   // log2(1 + 2^-9)
+      const float m_arg = m_run - PACK_BIAS;
+#else
+      const float m_arg = m_run;
+#endif
+      const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_arg, -m_arg);
+      uint64_t l4[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          const int q = 8 * h8 + qq;
+          const int kk = 32 * cc + 2 * q;
+          float e0, e1, p0, p1;
+          f2unpack(f2fma(f2pack(__uint_as_float(sv[cc][2 * q]), __uint_as_float(sv[cc][2 * q + 1])), c2, nm2),
+                   e0, e1);
+          if (((16 * cc + q) & 15) < POLY_PAIRS) {
+            ex2_poly2(e0, e1, p0, p1);
+          } else {
+            p0 = ex2(e0);
+            p1 = ex2(e1);
+          }
+          if (masked) {
+            p0 = (kk < lim) ? p0 : 0.f;
+            p1 = (kk + 1 < lim) ? p1 : 0.f;
+          }
+          l4[q & 1] = f2add(l4[q & 1], f2pack(p0, p1));
+#if MK_ATTN_PACK
+          pk[qq] = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x7632);
+#else
+          pk[qq] = pack_bf16x2(p0, p1);
+#endif
+        }
+        tc_st_32x32b_x8(sbase + 16u * cc + 8u * h8, pk);
+      }
+      {
+        float la, lb;
+        f2unpack(f2add(l4[0], l4[1]), la, lb);
+        l_run += la + lb;
+      }
+      // S_i(u) complete implies the product of tile u-1 complete (issued before
+      // it): O_i is settled until this group publishes P_i(u)
       if (__any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -511,41 +588,6 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
           for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
           tc_st_32x32b_x32(obase + 32u * cc, v);
         }
-      }
-      // pass 2: P = 2^(c*s - m), the running sum, P as bf16 pairs into columns
-      // 16cc .. 16cc+15 of S_i (S columns 0 .. 32cc+31 have been read by then)
-      const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_run, -m_run);
-      uint64_t l2 = f2pack(0.f, 0.f);
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(sbase + 32u * cc, v);
-        tc_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int kk = 32 * cc + 2 * q;
-          float e0, e1, p0, p1;
-          f2unpack(f2fma(f2pack(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1])), c2, nm2), e0, e1);
-          if ((q & 7) < (POLY_PAIRS >> 1) + ((q >> 3) < (POLY_PAIRS & 1) ? 1 : 0)) {
-            ex2_poly2(e0, e1, p0, p1);
-          } else {
-            p0 = ex2(e0);
-            p1 = ex2(e1);
-          }
-          if (masked) {
-            p0 = (kk < lim) ? p0 : 0.f;
-            p1 = (kk + 1 < lim) ? p1 : 0.f;
-          }
-          l2 = f2add(l2, f2pack(p0, p1));
-          pk[q] = pack_bf16x2(p0, p1);
-        }
-        tc_st_32x32b_x16(sbase + 16u * cc, pk);
-      }
-      {
-        float la, lb;
-        f2unpack(l2, la, lb);
-        l_run += la + lb;
       }
       // P_i(u) (and any rescaled O_i) written: the products may read them
       tc_wait_st();
@@ -560,7 +602,11 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
     }
     of_ph ^= 1u;
     tc_fence_after();
+#if MK_ATTN_PACK
+    const float inv = (l_run > 0.f) ? 1.001953125f / l_run : 0.f;   // (1 + 2^-9) / sum
+#else
     const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#endif
     const bool row_ok = qpos < p.s_r;
     uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2;
 #pragma unroll 1
@@ -590,7 +636,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
 // and lane 0 counts it in its (rank, step, head) counter.
 __device__ void at_copy(const AttnParams& p) {
   const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 10;
+  const int cw = (threadIdx.x >> 5) - AT_WARP_COPY;
   if (cw >= p.n_cw) return;
   const int worker = blockIdx.x * p.n_cw + cw;
   const int n_workers = gridDim.x * p.n_cw;
@@ -687,7 +733,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp == 0 || warp == 12) {
+  if (warp == 0 || warp == AT_WARP_V) {
     if (lane == 0) {
       if (warp == 0) at_producer_k(p, bars, base);
       else at_producer_v(p, bars, base);
@@ -699,7 +745,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   } else if (warp <= 9) {
     at_softmax(p, bars, tmem);
     __syncwarp();
-  } else if (warp <= 11 && p.copy) {
+  } else if (warp == AT_WARP_COPY && p.copy) {
     at_copy(p);
     __syncwarp();
   }
@@ -805,7 +851,7 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();
-  p.n_cw = 2;   // warps 10-11
+  p.n_cw = 1;   // warp 10
   const uint64_t rows = static_cast<uint64_t>(heads) * s_r;
   for (int r = 0; r < R; ++r) {
     p.out[r] = static_cast<uint8_t*>(out[r]);
