@@ -86,60 +86,89 @@ _lib = None
 _lib_lock = threading.Lock()
 
 
+LIB_DEBUG_PATH = os.path.join(_HERE, "libmk_debug.so")
+
+
 def lib() -> ctypes.CDLL:
     """Load libmk.so (built in-tree by build.py).  Raises if it is missing."""
     global _lib
     with _lib_lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is not built; run comm_gemm_tile_gb300/build.py "
-                               "(or __graft_entry__.build())")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, sz, ll, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong, ctypes.c_int
-        P = ctypes.POINTER
-        L.mk_version.restype = i
-        L.mk_device_sm_count.restype = i
-        L.mk_status_string.restype = ctypes.c_char_p
-        L.mk_status_string.argtypes = [i]
-        L.mk_workspace_size.restype = sz
-        L.mk_workspace_size.argtypes = [i, i, ll, ll, ll, P(_Cfg)]
-        L.mk_trace_entries.restype = sz
-        L.mk_trace_entries.argtypes = [i, i, ll, ll, ll, P(_Cfg), P(sz)]
-        L.mk_moe_trace_entries.restype = sz
-        L.mk_moe_trace_entries.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg), P(sz)]
-        L.mk_moe_workspace_size.restype = sz
-        L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
-        L.mk_get_device_status.restype = i
-        L.mk_get_device_status.argtypes = [vp, vp, P(ll)]
-        L.mk_ag_gemm.restype = i
-        L.mk_ag_gemm.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
-        for name in ("mk_gemm_rs", "mk_gemm_ar"):
-            f = getattr(L, name)
-            f.restype = i
-            f.argtypes = [P(vp), P(vp), P(vp), i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
-        L.mk_ag_gemm_noalloc.restype = i
-        L.mk_ag_gemm_noalloc.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, P(_Cfg), vp]
-        L.mk_moe_combine_workspace_size.restype = sz
-        L.mk_moe_combine_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
-        L.mk_moe_combine.restype = i
-        L.mk_moe_combine.argtypes = [P(vp), P(vp), P(vp), P(vp), vp, i, i, i, ll, ll, ll, ll,
-                                     P(vp), P(vp), vp, sz, P(_Cfg), vp]
-        L.mk_mlp_workspace_size.restype = sz
-        L.mk_mlp_workspace_size.argtypes = [i, ll, ll, ll, P(_Cfg)]
-        L.mk_mlp_ag_rs.restype = i
-        L.mk_mlp_ag_rs.argtypes = [P(vp), P(vp), P(vp), i, ll, ll, ll, vp, P(vp), P(vp), vp, sz,
-                                   P(_Cfg), vp]
-        L.mk_ring_attention_workspace_size.restype = sz
-        L.mk_ring_attention_workspace_size.argtypes = [i, i, ll, i, i, P(_Cfg)]
-        L.mk_ring_attention.restype = i
-        L.mk_ring_attention.argtypes = [P(vp), P(vp), P(vp), i, i, ll, i, i, ctypes.c_float, P(vp),
-                                        P(vp), P(vp), vp, sz, P(_Cfg), vp]
-        L.mk_moe_dispatch_gemm.restype = i
-        L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
-                                           P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
-        _lib = L
-        return L
+        _lib = load_library(LIB_PATH)
+        return _lib
+
+
+class use_library:
+    """Context manager: every op of this module calls the given library (for
+    example the bounds-checking LIB_DEBUG_PATH) instead of libmk.so."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.prev = lib()
+        with _lib_lock:
+            _lib = load_library(self.path)
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lib_lock:
+            _lib = self.prev
+        return False
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library and declare its C ABI."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run comm_gemm_tile_gb300/build.py "
+                           "(or __graft_entry__.build())")
+    L = ctypes.CDLL(path)
+    vp, sz, ll, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong, ctypes.c_int
+    P = ctypes.POINTER
+    L.mk_version.restype = i
+    L.mk_device_sm_count.restype = i
+    L.mk_status_string.restype = ctypes.c_char_p
+    L.mk_status_string.argtypes = [i]
+    L.mk_workspace_size.restype = sz
+    L.mk_workspace_size.argtypes = [i, i, ll, ll, ll, P(_Cfg)]
+    L.mk_trace_entries.restype = sz
+    L.mk_trace_entries.argtypes = [i, i, ll, ll, ll, P(_Cfg), P(sz)]
+    L.mk_moe_trace_entries.restype = sz
+    L.mk_moe_trace_entries.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg), P(sz)]
+    L.mk_moe_workspace_size.restype = sz
+    L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
+    L.mk_get_device_status.restype = i
+    L.mk_get_device_status.argtypes = [vp, vp, P(ll)]
+    L.mk_ag_gemm.restype = i
+    L.mk_ag_gemm.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
+    for name in ("mk_gemm_rs", "mk_gemm_ar"):
+        f = getattr(L, name)
+        f.restype = i
+        f.argtypes = [P(vp), P(vp), P(vp), i, i, ll, ll, ll, vp, sz, P(_Cfg), vp]
+    L.mk_ag_gemm_noalloc.restype = i
+    L.mk_ag_gemm_noalloc.argtypes = [P(vp), vp, vp, vp, i, i, i, ll, ll, ll, vp, P(_Cfg), vp]
+    L.mk_moe_combine_workspace_size.restype = sz
+    L.mk_moe_combine_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
+    L.mk_moe_combine.restype = i
+    L.mk_moe_combine.argtypes = [P(vp), P(vp), P(vp), P(vp), vp, i, i, i, ll, ll, ll, ll,
+                                 P(vp), P(vp), vp, sz, P(_Cfg), vp]
+    L.mk_mlp_workspace_size.restype = sz
+    L.mk_mlp_workspace_size.argtypes = [i, ll, ll, ll, P(_Cfg)]
+    L.mk_mlp_ag_rs.restype = i
+    L.mk_mlp_ag_rs.argtypes = [P(vp), P(vp), P(vp), i, ll, ll, ll, vp, P(vp), P(vp), vp, sz,
+                               P(_Cfg), vp]
+    L.mk_ring_attention_workspace_size.restype = sz
+    L.mk_ring_attention_workspace_size.argtypes = [i, i, ll, i, i, P(_Cfg)]
+    L.mk_ring_attention.restype = i
+    L.mk_ring_attention.argtypes = [P(vp), P(vp), P(vp), i, i, ll, i, i, ctypes.c_float, P(vp),
+                                    P(vp), P(vp), vp, sz, P(_Cfg), vp]
+    L.mk_moe_dispatch_gemm.restype = i
+    L.mk_moe_dispatch_gemm.argtypes = [P(vp), P(vp), P(vp), i, i, i, ll, ll, ll, ll, vp, vp,
+                                       P(vp), vp, P(vp), P(vp), vp, sz, P(_Cfg), vp]
+    return L
 
 
 def status_string(s: int) -> str:

@@ -339,7 +339,11 @@ static void set_items(FusedParams& p, int per, int mlp_phases) {
 }
 
 static mk_status launch_compute(FusedParams& p, bool pair, int sms, cudaStream_t s, int mlp_phases = 3) {
-  const int per = (p.op == OP_AG || p.mode == MK_MODE_GEMM_ONLY) ? 1 : p.P;
+  // AR GEMM-only: one item per (tile, rank) (see decode); other GEMM-only
+  // launches sum every rank of a tile in one item
+  const int per = (p.op == OP_AG) ? 1
+                  : (p.mode == MK_MODE_GEMM_ONLY) ? (p.op == OP_AR ? p.R : 1)
+                                                  : p.P;
   if (pair && p.op != OP_MOE) {
     const int clusters = std::min(max_pair_clusters(), sms / 2);
     {

@@ -101,12 +101,24 @@ struct AttnParams {
 __device__ __forceinline__ bool at_aborted(const AttnParams& p) {
   return ld_volatile(&p.hdr[HDR_ABORT]) == p.epoch;
 }
-__device__ __noinline__ void at_error(const AttnParams& p, int where, int item) {
+__device__ __noinline__ void at_error(const AttnParams& p, int where, int item, int code = MK_ERR_TIMEOUT) {
   int* st = reinterpret_cast<int*>(&p.hdr[HDR_STATUS]);
-  if (atomicCAS(st, 0, MK_ERR_TIMEOUT) == 0)
+  if (atomicCAS(st, 0, code) == 0)
     atomicExch(reinterpret_cast<int*>(&p.hdr[HDR_DETAIL]), where * 1000000 + (item % 1000000));
   __threadfence();
   atomicExch(&p.hdr[HDR_ABORT], p.epoch);
+}
+// Bounds check of the MK_DEBUG_BOUNDS build (compiled to true otherwise).
+__device__ __forceinline__ bool at_bounds_ok(const AttnParams& p, bool cond, int code, long long index) {
+#if MK_DEBUG_BOUNDS
+  if (!cond) {
+    at_error(p, WHERE_BOUNDS, code * 10000 + static_cast<int>(index % 10000), MK_ERR_INVALID);
+    return false;
+  }
+#else
+  (void)p; (void)cond; (void)code; (void)index;
+#endif
+  return true;
 }
 // The bounded wait loop.  SPIN: poll with the non-blocking test (the MMA
 // issuer and the softmax warps, whose waits sit on the critical path).
@@ -210,6 +222,10 @@ __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, in
                                        bool& ready, int& waited_j, const CUtensorMap*& m, int& row) {
   int j, s, kt;
   at_tile(p, it, t, j, s, kt);
+  if (!at_bounds_ok(p, j >= 0 && j < p.R && s >= 0 && s < p.R && kt >= 0 && kt < p.nkt && it.h >= 0 &&
+                           it.h < p.heads && it.r >= 0 && it.r < p.R && 2 * it.qp < p.nqt,
+                    BC_ATTN_TILE, item))
+    return false;
   m = is_v ? &p.tmV[s] : &p.tmK[s];
   row = it.h * p.s_r + kt * AT_T;
   if (j > 0 && p.use_recv) {
@@ -664,6 +680,12 @@ __device__ void at_copy(const AttnParams& p) {
     if (lane == 0) stop = at_aborted(p) ? 1 : 0;
     if (__shfl_sync(0xffffffffu, stop, 0)) return;
     const int rows = min(AT_T, p.s_r - kt * AT_T);
+    {
+      const int ok = at_bounds_ok(p, r >= 0 && r < p.R && j >= 1 && j < p.R && s >= 0 && s < p.R && h < p.heads &&
+                                         kt < p.nkt && rows > 0,
+                                  BC_ATTN_COPY, q) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, ok)) return;
+    }
     const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
     const size_t dst_off =
         ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;

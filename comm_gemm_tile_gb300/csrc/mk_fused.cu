@@ -46,11 +46,26 @@ __device__ __noinline__ void raise_error(const FusedParams& p, int code, int whe
   atomicExch(&p.hdr[HDR_ABORT], p.epoch);
 }
 
+// Bounds check of the MK_DEBUG_BOUNDS build (true when the check passes; the
+// default build compiles it to true).
+__device__ __forceinline__ bool bounds_ok(const FusedParams& p, bool cond, int code, long long index) {
+#if MK_DEBUG_BOUNDS
+  if (!cond) {
+    raise_error(p, MK_ERR_INVALID, WHERE_BOUNDS, code * 10000 + static_cast<int>(index % 10000));
+    return false;
+  }
+#else
+  (void)p; (void)cond; (void)code; (void)index;
+#endif
+  return true;
+}
+
 // Bounded mbarrier wait.  honor_abort = false is used only to drain copies
-// that are known to be in flight (they complete on their own).
-__device__ __noinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
-                                      int item, bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+// that are known to be in flight (they complete on their own).  The first
+// test is inline (wait_bar below): a call into this loop costs the calling
+// thread a few hundred cycles even when the phase has already completed.
+__device__ __noinline__ bool wait_bar_loop(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
+                                           int item, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (true) {
@@ -65,9 +80,15 @@ __device__ __noinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32
   }
 }
 
-// Bounded wait until *f == epoch (acquire, gpu scope).  Single thread.
-__device__ __noinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, int where, int item) {
-  if (ld_acquire_gpu(f) == p.epoch) return true;
+__device__ __forceinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
+                                         int item, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_loop(p, bar, parity, where, item, honor_abort);
+}
+
+// Bounded wait until *f == epoch (acquire, gpu scope).  Single thread.  The
+// first load is inline (wait_flag below).
+__device__ __noinline__ bool wait_flag_loop(const FusedParams& p, const uint32_t* f, int where, int item) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (ld_acquire_gpu(f) != p.epoch) {
@@ -83,6 +104,11 @@ __device__ __noinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, 
   return true;
 }
 
+__device__ __forceinline__ bool wait_flag(const FusedParams& p, const uint32_t* f, int where, int item) {
+  if (ld_acquire_gpu(f) == p.epoch) return true;
+  return wait_flag_loop(p, f, where, item);
+}
+
 // AG copy warps: chunk mb is ready when its piece counter (the first word of
 // the chunk's flag slot) reaches pieces(mb).  The CTA with ticket 0 zeroes
 // the counters at kernel start and then releases hdr[HDR_READY] = epoch;
@@ -94,9 +120,9 @@ __device__ __forceinline__ int chunk_pieces(const FusedParams& p, int mb) {
   const int rows = min(BM, p.M - mb * BM);
   return (rows + p.copy_rows - 1) / p.copy_rows;
 }
-// Bounded wait until the counter *c reaches `want` (single thread).
-__device__ __noinline__ bool wait_count(const FusedParams& p, const uint32_t* c, uint32_t want, int item) {
-  if (ld_acquire_gpu(c) == want) return true;
+// Bounded wait until the counter *c reaches `want` (single thread); the first
+// load is inline (wait_count below).
+__device__ __noinline__ bool wait_count_loop(const FusedParams& p, const uint32_t* c, uint32_t want, int item) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (ld_acquire_gpu(c) != want) {
@@ -110,6 +136,10 @@ __device__ __noinline__ bool wait_count(const FusedParams& p, const uint32_t* c,
     __nanosleep(64);
   }
   return true;
+}
+__device__ __forceinline__ bool wait_count(const FusedParams& p, const uint32_t* c, uint32_t want, int item) {
+  if (ld_acquire_gpu(c) == want) return true;
+  return wait_count_loop(p, c, want, item);
 }
 __device__ __forceinline__ bool wait_chunk_count(const FusedParams& p, int mb, int item) {
   return wait_count(p, chunk_counter(p, mb), static_cast<uint32_t>(chunk_pieces(p, mb)), item);
@@ -129,6 +159,7 @@ struct Item {
   int out_row0;     // output row of tile row 0
   int phase;        // chained MLP: 1 = up-projection tile (of rank hid_r), 2 = down-projection; else 0
   int hid_r;
+  int rep;          // AR GEMM-only: the one replica this item stores (-1: all of them)
 };
 
 // Grouped raster over (m-position, n-block): group_m m-positions per group,
@@ -196,6 +227,7 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
   it.row_hi = BM;
   it.phase = 0;
   it.hid_r = 0;
+  it.rep = -1;
   if (p.op == OP_MLP && i < p.mlp_n1) {
     // up-projection of every rank, row-block major so that a block of H_r
     // completes early: item = (m-position, rank, n-block), n-block innermost
@@ -249,7 +281,21 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
     return true;
   }
   if (p.op == OP_RS || p.op == OP_AR || p.op == OP_MLP) {
-    if (p.mode == MK_MODE_GEMM_ONLY) {
+    if (p.mode == MK_MODE_GEMM_ONLY && p.op == OP_AR) {
+      // AR baseline split over ranks, so that its few output tiles still fill
+      // the chip: item (tile, rank) = that rank's product for the tile, in the
+      // fused schedule's order, stored to that rank's replica (no reduction)
+      const int G = p.group_tiles;
+      const int g = i / (G * p.R);
+      const int Gg = min(G, p.n_sched - g * G);
+      const int iin = i - g * G * p.R;
+      const int r = iin / Gg;
+      raster(p, g * G + (iin - r * Gg), it.mb, it.nb);
+      if (p.pair) it.mb = 2 * it.mb + rank;
+      it.amap = r;
+      it.bmap = r;
+      it.rep = r;
+    } else if (p.mode == MK_MODE_GEMM_ONLY) {
       raster(p, i, it.mb, it.nb);
       it.nseg = p.R;
       if (p.pair) it.mb = 2 * it.mb + rank;
@@ -408,6 +454,22 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
       trace_put(p, i, rank, 0, globaltimer_ns());
       trace_put(p, i, rank, 5, clock64());
     }
+    // the tile lies inside the output and the operands' k-blocks (MoE: inside
+    // the receive buffer of a valid destination rank)
+    if (!bounds_ok(p, it.row_hi >= 0 && it.row_hi <= BM && it.out_row0 >= 0 && it.arow >= 0 &&
+                          (it.row_hi == 0 || it.out_row0 + it.row_hi <= p.M) && it.nb >= 0 &&
+                          it.nb < (it.phase == 1 ? p.mlp_nb1 : p.n_nblk),
+                   BC_TILE, i))
+      goto done;
+    if (!bounds_ok(p, it.kb0 >= 0 && it.nkb >= 0 && it.kb0 + it.nkb <= (it.phase == 1 ? p.mlp_kb1 : p.n_kblk) &&
+                          it.amap >= 0 && it.amap + it.nseg <= MK_MAX_RANKS && it.bmap >= 0 &&
+                          it.bmap + it.nseg <= MK_MAX_RANKS,
+                   BC_KRANGE, i))
+      goto done;
+    if ((p.op == OP_MOE || p.op == OP_MOE_COMBINE) &&
+        !bounds_ok(p, it.amap < p.R && it.bz >= 0 && (it.row_hi == 0 || it.arow + it.row_hi <= p.M),
+                   BC_MOE_TILE, i))
+      goto done;
     if (p.op == OP_MOE && p.mode == MK_MODE_FUSED && it.row_hi > 0) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       // (an empty pair half covers no rows and waits for nothing)
@@ -963,6 +1025,17 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     // warp-uniform outcome: the tcgen05.ld below needs every lane of the warp
     const int landed = wait_bar(p, S.tfull(buf), acc_phase, WHERE_EPILOGUE, i) ? 1 : 0;
     if (!__all_sync(0xffffffffu, landed)) return;
+#if MK_DEBUG_BOUNDS
+    // the owner block of an RS / MLP output row exists (warp-uniform: the
+    // tcgen05.ld below needs every lane)
+    if ((p.op == OP_RS || p.op == OP_MLP) && it.phase != 1) {
+      int ok = 1;
+      if (lane == 0)
+        ok = bounds_ok(p, it.row_hi == 0 || (it.out_row0 + it.row_hi - 1) / p.rows_per_owner < p.R, BC_OWNER, i)
+                 ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+#endif
     if (p.trace != nullptr && warp == 2 && lane == 0) {
       trace_put(p, i, rank, 3, globaltimer_ns());
       trace_put(p, i, rank, 6, clock64());
@@ -1212,6 +1285,9 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
           const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
           uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
           store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
+        } else if (it.rep >= 0) {   // AR baseline: this rank's product to its replica
+          uint8_t* base = reinterpret_cast<uint8_t*>(p.out[it.rep]);
+          store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
         } else {  // OP_AR: the same bits to every replica
           for (int o = 0; o < p.R; ++o) {
             uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
@@ -1284,6 +1360,11 @@ constexpr int CW_UNROLL = MK_CW_UNROLL;
 #define MK_MOE_CW_UNROLL MK_CW_UNROLL
 #endif
 constexpr int MOE_CW_UNROLL = MK_MOE_CW_UNROLL;   // 16-byte loads in flight per lane (MoE rows)
+// MK_MOE_CW_HINT = 1: the dispatch copy reads token rows with an L2 evict_first
+// policy and writes received rows with evict_last (the GEMM reads them next).
+#ifndef MK_MOE_CW_HINT
+#define MK_MOE_CW_HINT 0
+#endif
 // MK_CW_HINT = 1: shard reads marked L2 evict_first, gathered-A writes evict_last;
 // 2: both evict_first.
 #ifndef MK_CW_HINT
@@ -1323,6 +1404,13 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
     long long run_hi;
     int s;
     while (copy_run(p, row, hi, run_hi, s)) {
+      {
+        const int ok = bounds_ok(p, row >= 0 && run_hi <= p.M && s >= 0 && s < p.R &&
+                                        row >= static_cast<long long>(s) * p.m_r &&
+                                        run_hi <= static_cast<long long>(s + 1) * p.m_r,
+                                 BC_AG_COPY, row) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
       const uint8_t* src = p.shard[s] + static_cast<size_t>(row - static_cast<long long>(s) * p.m_r) * rb;
       uint8_t* dst = p.gathered + static_cast<size_t>(row) * rb;
       const size_t n16 = static_cast<size_t>(run_hi - row) * rb / 16;
@@ -1380,6 +1468,11 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const size_t rb = static_cast<size_t>(p.K) * 2;
   const size_t n16 = rb / 16;
   bool skip_first = (p.inject == 1 && worker == 0);
+#if MK_MOE_CW_HINT
+  // token rows are read once per slot; received rows are read again by the GEMM
+  const uint64_t pol_src = l2_policy_evict_first();
+  const uint64_t pol_dst = l2_policy_evict_last();
+#endif
   for (long long q = worker; q < total; q += n_workers) {
     int d = 0;
     long long j = q;
@@ -1391,8 +1484,16 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
     }
     const int row0 = static_cast<int>(j) * pr;
     const int rows = min(pr, rc - row0);
+    {
+      const int ok = bounds_ok(p, d < p.R && row0 >= 0 && row0 + rows <= p.M, BC_MOE_COPY, q) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, ok)) return;
+    }
     for (int rr = 0; rr < rows; ++rr) {
       const int src = p.moe_src[d][row0 + rr];
+      {
+        const int ok = bounds_ok(p, src >= 0 && src < p.R * p.moe_T * p.moe_topk, BC_MOE_SRC, row0 + rr) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
       const int g = src / p.moe_topk;
       const int r = g / p.moe_T, t = g - r * p.moe_T;
       const uint8_t* sp = p.shard[r] + static_cast<size_t>(t) * rb;
@@ -1402,12 +1503,20 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
 #pragma unroll
         for (int u = 0; u < MOE_CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
+#if MK_MOE_CW_HINT
+          if (idx < n16) v[u] = ld_nc_v4_pol(sp + idx * 16, pol_src);
+#else
           if (idx < n16) v[u] = ld_nc_v4(sp + idx * 16);
+#endif
         }
 #pragma unroll
         for (int u = 0; u < MOE_CW_UNROLL; ++u) {
           const size_t idx = i0 + static_cast<size_t>(u) * 32;
+#if MK_MOE_CW_HINT
+          if (idx < n16) st_global_v4_pol(dp + idx * 16, v[u], pol_dst);
+#else
           if (idx < n16) st_global_v4(dp + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+#endif
         }
       }
     }

@@ -60,7 +60,19 @@ enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3, OP_MOE_COMBINE = 4, OP_ML
 
 // Role codes used in the error detail word.
 enum { WHERE_PRODUCER = 1, WHERE_MMA = 2, WHERE_EPILOGUE = 3, WHERE_COPY = 4, WHERE_REDUCE = 5,
-       WHERE_DRAIN = 6, WHERE_MOE = 7 };
+       WHERE_DRAIN = 6, WHERE_MOE = 7, WHERE_BOUNDS = 8 };
+
+// Bounds-checking build (MK_DEBUG_BOUNDS=1, built beside the library as
+// libmk_debug.so): device-side index checks on tile coordinates, copy rows,
+// MoE slots and received-row sources.  A failed check records MK_ERR_INVALID
+// with detail WHERE_BOUNDS * 1e6 + check code * 1e4 + (index % 1e4), raises the
+// abort word, skips the access and lets the kernel wind down like a timeout;
+// it never traps.  With 0 (the default build) the checks compile to nothing.
+#ifndef MK_DEBUG_BOUNDS
+#define MK_DEBUG_BOUNDS 0
+#endif
+enum { BC_TILE = 1, BC_KRANGE = 2, BC_AG_COPY = 3, BC_MOE_COPY = 4, BC_MOE_SRC = 5, BC_MOE_TILE = 6,
+       BC_OWNER = 7, BC_MOE_SCATTER = 8, BC_ATTN_TILE = 9, BC_ATTN_COPY = 10 };
 
 struct FusedParams {
   CUtensorMap tmA[MK_MAX_RANKS];   // AG: [0] local shard, [1] gathered A; RS/AR: A_r; MoE: recv_x[d]

@@ -26,7 +26,7 @@
 #include "mk_ptx.cuh"
 
 #ifndef MK_MOE_COPY_WARPS
-#define MK_MOE_COPY_WARPS 6   // copy warps per compute CTA for the MoE dispatch
+#define MK_MOE_COPY_WARPS 3   // copy warps per compute CTA for the fused MoE dispatch
 #endif
 
 namespace mk {
@@ -58,6 +58,17 @@ struct MoeArgs {
   int tile_rows;      // rows per tile-table entry: 128, or 256 for CTA pairs
   long long cap;
 };
+
+#if MK_DEBUG_BOUNDS
+// Bounds-checking build: a failed check records MK_ERR_INVALID with its detail
+// (the first failure wins) and the caller skips the access.
+__device__ __noinline__ void bounds_fail(const MoeArgs& a, int code, long long index) {
+  int* st = reinterpret_cast<int*>(&a.hdr[HDR_STATUS]);
+  if (atomicCAS(st, 0, MK_ERR_INVALID) == 0)
+    atomicExch(reinterpret_cast<int*>(&a.hdr[HDR_DETAIL]),
+               WHERE_BOUNDS * 1000000 + code * 10000 + static_cast<int>(index % 10000));
+}
+#endif
 
 __device__ __forceinline__ bool better(float v, int e, float ov, int oe) {
   // (ov, oe) beats (v, e): larger logit, ties to the lower expert id; e < 0 = none
@@ -210,10 +221,22 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
     const int aa = static_cast<int>(ai - static_cast<long long>(r) * T * K);
     const int t = aa / K, j = aa - t * K;
     const int e = a.topk_idx[ai];
+#if MK_DEBUG_BOUNDS
+    if (e < 0 || e >= E) {   // bounds-checking build: record and skip
+      bounds_fail(a, BC_MOE_SCATTER, ai);
+      continue;
+    }
+#endif
     const int d = e / El, l = e - d * El;
     const int c = t / RR_TOKENS;
     const int row = a.segoff[d * (El + 1) + l] + a.base[r * E + e] +
                     a.hist[(static_cast<size_t>(r) * a.C + c) * E + e] + a.pos[ai];
+#if MK_DEBUG_BOUNDS
+    if (row < 0 || row >= a.cap) {
+      bounds_fail(a, BC_MOE_SCATTER, ai);
+      continue;
+    }
+#endif
     a.recv_src[d][row] = (r * T + t) * K + j;
   }
   const int ntiles = static_cast<int>(a.misc[MISC_NTILES]);
@@ -410,8 +433,10 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   int pr = 1;
   while (pr < BM && static_cast<long long>(pr) * 2 * H * 2 <= 32768) pr *= 2;
   p.moe_rows_per_piece = pr;
-  // the dispatch moves 4x the bytes of the AG copy-in: every copy warp takes part
-  // (MK_MOE_COPY_WARPS < 6 paces the copy; two warps starved the tiles)
+  // Fused: three copy warps per CTA move the rows at about the rate the tiles
+  // consume them (measured: 6 warps front-load the copy and slow the tiles
+  // that run beside it; 2 starve the tiles).  The unfused baseline's copy
+  // launch runs alone and uses every copy warp.
   p.n_cw = std::max(1, std::min(MK_MOE_COPY_WARPS, N_COPY_WARPS));
   p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
@@ -447,6 +472,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   if (mode == MK_MODE_UNFUSED) {
     // host-ordered baseline: the dispatch copy as one launch, then the grouped GEMM
     p.mode = MK_MODE_UNFUSED;
+    p.n_cw = N_COPY_WARPS;
     if (launch_fused(p, grid, s) != cudaSuccess) return MK_ERR_CUDA;
     p.mode = MK_MODE_GEMM_ONLY;
   } else if (mode == MK_MODE_GEMM_ONLY) {

@@ -81,7 +81,9 @@ typedef enum { MK_OP_AG_GEMM = 0, MK_OP_GEMM_RS = 1, MK_OP_GEMM_AR = 2, MK_OP_MO
 typedef enum {
   MK_MODE_FUSED = 0,     /* one persistent launch: copy/reduce roles overlap the GEMM tiles */
   MK_MODE_GEMM_ONLY = 1, /* the same FLOPs with no data movement: AG reads a_gathered as
-                            already filled; RS/AR accumulate all ranks in tensor memory      */
+                            already filled; RS accumulates all ranks in tensor memory; AR
+                            (few output tiles) runs one item per (tile, rank) and writes
+                            rank r's own product A_r @ B_r to replica r (no reduction)    */
   MK_MODE_UNFUSED = 2    /* host-ordered: a copy launch then a GEMM launch (AG), or a
                             partial-GEMM launch then a reduce launch (RS/AR)               */
 } mk_mode;

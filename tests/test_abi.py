@@ -31,6 +31,15 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
+def test_bounds_build_exports_the_same_symbols():
+    # libmk_debug.so: the same sources with MK_DEBUG_BOUNDS=1 (device-side index checks)
+    mkbuild.build(debug=True)
+    D = mk.load_library(mk.LIB_DEBUG_PATH)
+    for n in declared_functions():
+        assert hasattr(D, n), n
+    assert D.mk_version() == 1
+
+
 def test_version_and_status_strings(L):
     assert L.mk_version() == 1
     assert "timed out" in mk.status_string(mk.MK_ERR_TIMEOUT)
