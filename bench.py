@@ -404,9 +404,17 @@ def main():
     ap.add_argument("--only", choices=["rs", "ar", "moe", "combine", "mlp", "ring", "ring_small", "ag_fp8"],
                     default=None,
                     help="time only this secondary workload (profiling aid) and print its entry")
+    ap.add_argument("--profile", choices=list(PROFILE_WORKLOADS), default=None,
+                    help="profiling aid: make the workload's inputs and run --calls untimed fused calls "
+                         "back to back (for an ncu capture of one of them); prints the device status")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--scale", choices=["full", "small"], default="full",
+                    help="--profile: the bench workload, or a reduced case (inputs still larger than L2)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     if args.only:
         return run_only(args)
 
@@ -602,6 +610,85 @@ def main():
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+PROFILE_WORKLOADS = ("ag", "rs", "ar", "moe", "combine", "mlp", "ring")
+
+
+def run_profile(args):
+    """Untimed fused calls of one workload (profiling aid: ncu captures one of
+    them).  --scale small shrinks the row / token / position counts, keeping the
+    inputs larger than L2, so that multi-pass captures stay small."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import comm_gemm_tile_gb300 as mk
+    from comm_gemm_tile_gb300 import build as mkbuild
+    mkbuild.build()
+    small = args.scale == "small"
+    ws = mk.Workspace(device)
+    name = args.profile
+    if name in ("ag", "rs", "ar"):
+        w = {"ag": I.AG_R8_TP8_UP, "rs": I.RS_R8_TP8_DOWN, "ar": I.AR_R8_DECODE}[name]
+        if small and name != "ar":
+            w = I.GemmWorkload(w.name + "_small", w.op, R=w.R, m=w.m // 4, n=w.n, k=w.k, out=w.out,
+                               a_seed=w.a_seed, b_seed=w.b_seed, b_std=w.b_std)
+        if name == "ag":
+            a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r, device) for r in range(w.R)]
+            b = dev_normal((w.k, w.n), w.b_std, w.b_seed, device)
+            g = torch.empty((w.R * w.m, w.k), dtype=torch.bfloat16, device=device)
+            c = torch.empty((w.R * w.m, w.n), dtype=torch.bfloat16, device=device)
+            call = lambda: mk.ag_gemm(a, b, a_gathered=g, c=c, workspace=ws)  # noqa: E731
+        else:
+            a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r, device) for r in range(w.R)]
+            b = [dev_normal((w.k, w.n), w.b_std, w.b_seed + r, device) for r in range(w.R)]
+            rows = w.m // w.R if name == "rs" else w.m
+            o = [torch.empty((rows, w.n), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+            fn = mk.gemm_rs if name == "rs" else mk.gemm_ar
+            key = "c_blocks" if name == "rs" else "c_replicas"
+            call = lambda: fn(a, b, workspace=ws, **{key: o})  # noqa: E731
+    elif name in ("moe", "combine"):
+        wd = I.MOE_R8_E64
+        T = wd.T // 4 if small else wd.T
+        x = [dev_normal((T, wd.H), 1.0, wd.x_seed + r, device) for r in range(wd.R)]
+        lg = [I.zipf_logits(T, wd.E, wd.logit_seed + r).to(device) for r in range(wd.R)]
+        we = [dev_normal((wd.E_loc, wd.H, wd.N), 0.02, wd.w_seed + d, device) for d in range(wd.R)]
+        cap = 2 * T * wd.R
+        disp = mk.moe_dispatch_gemm(x, lg, we, E_loc=wd.E_loc, topk=wd.topk, cap_rows=cap, workspace=ws)
+        if name == "moe":
+            call = lambda: mk.moe_dispatch_gemm(x, lg, we, E_loc=wd.E_loc, topk=wd.topk,  # noqa: E731
+                                                cap_rows=cap, out=disp, workspace=ws)
+        else:
+            w = I.MOE_COMBINE_R8_E64
+            h = [dev_normal((cap, w.N), 1.0, w.h_seed + d, device) for d in range(w.R)]
+            w2 = [dev_normal((w.E_loc, w.N, w.H), 0.02, w.w2_seed + d, device) for d in range(w.R)]
+            gates = [torch.full((T, w.topk), 0.5, device=device) for _ in range(w.R)]
+            del x, we
+            outs = mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"], E_loc=w.E_loc,
+                                  topk=w.topk, cap_rows=cap, workspace=ws)
+            call = lambda: mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"],  # noqa: E731
+                                          E_loc=w.E_loc, topk=w.topk, cap_rows=cap, out=outs,
+                                          workspace=ws)
+    elif name == "mlp":
+        w = I.MLP_R8_TP8
+        m = w.m // 4 if small else w.m
+        x = [dev_normal((m, w.h), 1.0, w.x_seed + r, device) for r in range(w.R)]
+        w1 = [dev_normal((w.h, w.f_r), w.w_std, w.w1_seed + r, device) for r in range(w.R)]
+        w2 = [dev_normal((w.f_r, w.h), w.w_std, w.w2_seed + r, device) for r in range(w.R)]
+        call = lambda: mk.mlp_ag_rs(x, w1, w2, workspace=ws)  # noqa: E731
+    else:  # ring
+        w = I.RING_R8_H8_S4096
+        s_r = w.s_r // 4 if small else w.s_r
+        shape = (w.heads, s_r, w.d)
+        q, k, v = ([dev_normal(shape, 1.0, seed + r, device) for r in range(w.R)]
+                   for seed in (w.q_seed, w.k_seed, w.v_seed))
+        call = lambda: mk.ring_attention(q, k, v, workspace=ws)  # noqa: E731
+    for _ in range(args.calls):
+        call()
+    torch.cuda.synchronize()
+    st, detail = mk.device_status(ws)
+    print(json.dumps({"profile": name, "scale": args.scale, "calls": args.calls,
+                      "status": mk.status_string(st), "detail": detail}), flush=True)
+    return 0 if st == mk.MK_OK else 1
 
 
 def run_only(args):

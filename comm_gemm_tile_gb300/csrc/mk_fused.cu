@@ -214,6 +214,9 @@ __device__ __forceinline__ void empty_half(Item& it, int mb) {
   it.row_hi = 0;
 }
 
+// Chained MLP up-projection: m-positions per raster group (see decode).
+constexpr int MLP_GROUP_M = 8;
+
 __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, int rank = 0) {
   it.bz = -1;
   it.slot = -1;
@@ -229,13 +232,18 @@ __device__ __forceinline__ bool decode(const FusedParams& p, int i, Item& it, in
   it.hid_r = 0;
   it.rep = -1;
   if (p.op == OP_MLP && i < p.mlp_n1) {
-    // up-projection of every rank, row-block major so that a block of H_r
-    // completes early: item = (m-position, rank, n-block), n-block innermost
+    // up-projection of every rank in groups of MLP_GROUP_M m-positions: inside
+    // a group rank-major, then n-block, then the group's m-positions, so that
+    // a panel of W1_r is read once per group and reused from L2 by the group's
+    // row blocks (row-block-major order streamed all of W1 once per row block)
     const int per_m = p.R * p.mlp_nb1;
-    int pos = i / per_m;
-    const int rem = i - pos * per_m;
-    it.hid_r = rem / p.mlp_nb1;
-    it.nb = rem - it.hid_r * p.mlp_nb1;
+    const int g = i / (MLP_GROUP_M * per_m);
+    const int Gg = min(MLP_GROUP_M, p.n_mrow - g * MLP_GROUP_M);
+    const int iin = i - g * MLP_GROUP_M * per_m;
+    it.hid_r = iin / (Gg * p.mlp_nb1);
+    const int rem = iin - it.hid_r * Gg * p.mlp_nb1;
+    it.nb = rem / Gg;
+    int pos = g * MLP_GROUP_M + (rem - it.nb * Gg);
     it.phase = 1;
     it.amap = 0;
     it.bmap = it.hid_r;

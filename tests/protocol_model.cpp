@@ -526,10 +526,15 @@ int run_mlp(int argc, char** argv) {
   };
   L.decode = [&](int i, int half) {
     Item it;
-    if (i < n1) {   // up-projection: (m-position, rank, n-block), n-block innermost
-      const int per_m = R * f_nblk;
-      int pos = i / per_m;
-      const int r = (i % per_m) / f_nblk, nb = i % f_nblk;
+    if (i < n1) {   // up-projection: groups of 8 m-positions; inside one rank, n-block, m-position
+      const int GM = 8, per_m = R * f_nblk;
+      const int g = i / (GM * per_m);
+      const int Gg = std::min(GM, n_mrow - g * GM);
+      const int iin = i - g * GM * per_m;
+      const int r = iin / (Gg * f_nblk);
+      const int rem = iin - r * Gg * f_nblk;
+      const int nb = rem / Gg;
+      int pos = g * GM + (rem - nb * Gg);
       if (pair) pos = 2 * pos + half;
       if (pos >= n_mblk) {
         it.empty = true;
