@@ -78,23 +78,28 @@ def whole_job_rate(units_per_rank: float, world: int, t_max_ms: float) -> float:
 FUSED_KERNEL_SOURCES = ("mk_api.cu", "mk_fused.cu", "mk_internal.h", "mk_ptx.cuh")
 
 
-def kernel_source_sha256() -> str:
-    """Hash of mk_fused_kernel's sources, to tell whether recorded ncu counters still apply."""
+ATTN_KERNEL_SOURCES = ("mk_attn.cu", "mk_internal.h", "mk_ptx.cuh")
+
+
+def kernel_source_sha256(files=FUSED_KERNEL_SOURCES) -> str:
+    """Hash of a kernel's sources, to tell whether recorded ncu counters still apply."""
     import hashlib
     root = os.path.join(ROOT, "comm_gemm_tile_gb300", "csrc")
     h = hashlib.sha256()
-    for f in FUSED_KERNEL_SOURCES:
+    for f in files:
         h.update(f.encode())
         h.update(open(os.path.join(root, f), "rb").read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str, key: str = "fused_dram_bytes"):
-    """DRAM bytes per launch from the committed ncu record, or None when the
-    kernel sources changed since it was taken."""
+def recorded_traffic(workload: str, key: str = "fused_dram_bytes", kernel: str = "mk_fused_kernel"):
+    """DRAM bytes per launch from the committed ncu record of `kernel`
+    (mk_fused_kernel or mk_ring_attn_kernel), or None when the kernel sources
+    changed since it was taken."""
+    files = FUSED_KERNEL_SOURCES if kernel == "mk_fused_kernel" else ATTN_KERNEL_SOURCES
     try:
-        rec = json.load(open(os.path.join(ROOT, "profiles", "mk_fused_kernel_traffic.json")))
-        if rec.get("source_sha256") != kernel_source_sha256():
+        rec = json.load(open(os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")))
+        if rec.get("source_sha256") != kernel_source_sha256(files):
             return None
         return rec[workload][key]
     except Exception:
@@ -907,6 +912,7 @@ def bench_moe_combine(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak
             "pct_of_peak": 100 * fused_tf / bf16_peak, "algorithmic_bytes": hbm_bytes,
             "roofline_ms": 1e3 * max(t_tensor, t_hbm),
             "roofline_frac": 1e3 * max(t_tensor, t_hbm) / res["fused"],
+            "traffic": recorded_traffic(w.name),
             "status": mk.status_string(st)}
 
 
@@ -935,7 +941,9 @@ def bench_mlp(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_pe
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12
     return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
             "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
-            "pct_of_peak": 100 * fused_tf / bf16_peak, "status": mk.status_string(st)}
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "bound": "tensor",
+            "roofline_frac": fused_tf / bf16_peak, "traffic": recorded_traffic(w.name),
+            "status": mk.status_string(st)}
 
 
 def bench_ag_fp8(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_peak):
@@ -996,7 +1004,10 @@ def bench_ring(mk, device, stream, dist, steps, seed_off, tmax, bf16_peak, hbm_p
     fused_tf = flops / (res["fused"] * 1e-3) / 1e12
     return {"fused_ms": res["fused"], "gemm_only_ms": res["gemm_only"], "unfused_ms": res["unfused"],
             "exposed_ms": res["fused"] - res["gemm_only"], "fused_tflops": fused_tf,
-            "pct_of_peak": 100 * fused_tf / bf16_peak, "status": mk.status_string(st)}
+            "pct_of_peak": 100 * fused_tf / bf16_peak, "bound": "tensor",
+            "roofline_frac": fused_tf / bf16_peak,
+            "traffic": recorded_traffic(w.name, kernel="mk_ring_attn_kernel"),
+            "status": mk.status_string(st)}
 
 
 if __name__ == "__main__":
