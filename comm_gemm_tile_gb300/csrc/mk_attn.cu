@@ -10,7 +10,7 @@
 //   * warp 0 (TMA): the item's two Q tiles, then the K tiles, 128 keys each,
 //     in ring order -- the rank's own block, then the blocks of ranks r-1,
 //     r-2, ... as they land in its receive buffer; warp 11 (TMA): the V tiles;
-//   * warp 1 (MMA): per K/V tile, S_i = Q_i K^T (i = 0, 1) into tensor memory,
+//   * warp 1 (MMA, one elected lane issuing): per K/V tile, S_i = Q_i K^T (i = 0, 1) into tensor memory,
 //     and O_i += P_i V with P_i read from tensor memory (tcgen05, bf16 ->
 //     fp32), in the order PV_0(u-1), S_0(u), PV_1(u-1), S_1(u), so that the
 //     product of one query tile runs while the other's softmax works;
@@ -43,7 +43,10 @@ constexpr int AT_T = 128;                    // query rows / keys per tile
 constexpr int AT_THREADS = 384;              // 12 warps: see the role list above
 constexpr int AT_WARP_COPY = 10, AT_WARP_V = 11;
 constexpr int AT_MAX_R = 8;
-constexpr int AT_KST = 2;                    // K stages
+#ifndef MK_ATTN_KST
+#define MK_ATTN_KST 3
+#endif
+constexpr int AT_KST = MK_ATTN_KST;          // K stages
 constexpr int AT_VST = 2;                    // V stages
 // shared memory (from the 1024-aligned base)
 constexpr uint32_t AT_TILE = 32768;          // one 128 x 128 bf16 tile: 2 K-major atoms of [128 rows x 128 B]
@@ -52,8 +55,10 @@ constexpr uint32_t AT_K = 2 * AT_TILE;       // K stages
 constexpr uint32_t AT_V = AT_K + AT_KST * AT_TILE;   // V stages
 constexpr uint32_t AT_BARS = AT_V + AT_VST * AT_TILE;
 constexpr int AT_SMEM = 1024 + AT_BARS + 256;
+static_assert(AT_SMEM <= 232448, "dynamic shared memory per block");
 // barriers (byte offsets in the barrier block)
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFIRST = 16, B_KEMPTY = 24, B_VEMPTY = B_KEMPTY + 8 * AT_KST,
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_KEMPTY = B_KFULL + 8 * AT_KST,
+                   B_VFULL = B_KEMPTY + 8 * AT_KST, B_VEMPTY = B_VFULL + 8 * AT_VST,
                    B_SFULL = B_VEMPTY + 8 * AT_VST, B_GO = B_SFULL + 16, B_OFULL = B_GO + 16,
                    B_DRAIN = B_OFULL + 16, B_TMEM = B_DRAIN + 8;
 static_assert(B_TMEM + 4 <= 256, "barrier block");
@@ -146,6 +151,15 @@ __device__ __forceinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, u
   if (SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   return at_wait_loop<SPIN>(p, bar, parity, where, item, honor_abort);
 }
+// The MMA warp's waits: lane 0 polls, the other lanes wait at the shuffle, and
+// every lane returns lane 0's result, so the warp stays converged.
+template <bool SPIN = false>
+__device__ __forceinline__ bool at_wait_warp(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
+                                             bool honor_abort = true) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = at_wait_bar<SPIN>(p, bar, parity, where, item, honor_abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
 __device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* f, uint32_t want, int where,
                                            int item) {
   if (ld_acquire_gpu(f) == want) return true;
@@ -210,14 +224,10 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 
 // ------------------------------------------------------------------ roles
 // The CTA's K/V tiles, counted over all its items, form one stream u = 0, 1, ...
-// K(u) and V(u) go to stages u % AT_KST and u % AT_VST.  The MMA issuer has one
-// wait per query tile and K/V tile: GO_0 phase u, which completes on four
-// arrivals of the Q0 softmax warps (P_0(u) written), the V(u) load and the
-// K(u+1) load (both with their bytes), and GO_1 phase u (the Q1 softmax warps:
-// P_1(u) written).  K(0) lands on its own barrier.  A producer arms phase u of
-// GO_0 only once phase u-1 has completed, so no arrival can fall into an
-// earlier phase; after its last tile the K producer arrives once more, without
-// bytes, in place of the K tile that no longer follows.
+// K(u) and V(u) go to stages u % AT_KST and u % AT_VST, each stage with a full
+// barrier (the TMA bytes) and an empty barrier (the MMAs that read it), so a
+// load is issued as soon as its stage is free.  GO_i phase u completes on the
+// four arrivals of query tile i's softmax warps (P_i(u) written).
 __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, int t, bool is_v, int item,
                                        bool& ready, int& waited_j, const CUtensorMap*& m, int& row) {
   int j, s, kt;
@@ -245,13 +255,10 @@ __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, in
 }
 
 // K producer (warp 0, one thread): each item's K tiles, and after the first of
-// them its Q0 and Q1 (once the previous item's last S has completed): the
-// item's first K tile completes the phase of GO_0 that the previous item's
-// last product waits for, so it goes before the wait for the query buffer.
+// them its Q0 and Q1 (once the previous item's last S has completed).
 __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base) {
   uint32_t q_ph = 0, e_ph = 0;
   int stage = 0;
-  uint32_t u = 0;            // stream index of the next K tile
   bool ready = false;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
@@ -261,16 +268,11 @@ __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base)
       int row;
       if (!at_src(p, it, t, false, i, ready, waited_j, m, row)) return;
       if (!at_wait_bar(p, bars + B_KEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
-      uint32_t full = bars + B_KFIRST;
-      if (u >= 1) {
-        full = bars + B_GO;   // phase u-1 of GO_0
-        if (u >= 2 && !at_wait_bar(p, full, (u - 2) & 1u, WHERE_PRODUCER, i)) return;
-      }
+      const uint32_t full = bars + B_KFULL + 8u * stage;
       const uint32_t dst = base + AT_K + static_cast<uint32_t>(stage) * AT_TILE;
       mbar_arrive_expect_tx(full, AT_TILE);
       tma_load_2d(dst, m, full, 0, row);
       tma_load_2d(dst + 16384u, m, full, 64, row);
-      ++u;
       if (++stage == AT_KST) {
         stage = 0;
         e_ph ^= 1u;
@@ -288,18 +290,12 @@ __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base)
       }
     }
   }
-  // GO_0's last phase (u-1) expects a K arrival too: made without bytes
-  if (u >= 1) {
-    if (u >= 2 && !at_wait_bar(p, bars + B_GO, (u - 2) & 1u, WHERE_PRODUCER, 0)) return;
-    mbar_arrive(bars + B_GO);
-  }
 }
 
-// V producer (warp 11, one thread): V(u) lands on phase u of GO_0.
+// V producer (warp 11, one thread).
 __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base) {
   uint32_t e_ph = 0;
   int stage = 0;
-  uint32_t u = 0;
   bool ready = false;
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
@@ -309,12 +305,11 @@ __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base)
       int row;
       if (!at_src(p, it, t, true, i, ready, waited_j, m, row)) return;
       if (!at_wait_bar(p, bars + B_VEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
-      if (u >= 1 && !at_wait_bar(p, bars + B_GO, (u - 1) & 1u, WHERE_PRODUCER, i)) return;
+      const uint32_t full = bars + B_VFULL + 8u * stage;
       const uint32_t dst = base + AT_V + static_cast<uint32_t>(stage) * AT_TILE;
-      mbar_arrive_expect_tx(bars + B_GO, AT_TILE);
-      tma_load_3d(dst, m, bars + B_GO, 0, row, 0);
-      tma_load_3d(dst + 16384u, m, bars + B_GO, 0, row + 64, 0);
-      ++u;
+      mbar_arrive_expect_tx(full, AT_TILE);
+      tma_load_3d(dst, m, full, 0, row, 0);
+      tma_load_3d(dst + 16384u, m, full, 0, row + 64, 0);
       if (++stage == AT_VST) {
         stage = 0;
         e_ph ^= 1u;
@@ -329,14 +324,17 @@ __device__ __forceinline__ void at_s(uint32_t base, uint32_t tmem, int i, int ks
   const uint32_t kb = base + AT_K + static_cast<uint32_t>(kstage) * AT_TILE;
   // descriptors differ only in the start address field (address >> 4, low bits)
   const uint64_t dq = sdesc_swz(qb, 16u, 1024u, 2u), dk = sdesc_swz(kb, 16u, 1024u, 2u);
+  if (elect_one_sync()) {
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint64_t ad = dq + ((16384u * a + 32u * k) >> 4);
-      const uint64_t bd = dk + ((16384u * a + 32u * k) >> 4);
-      tc_mma_bf16(tmem + static_cast<uint32_t>(i) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
-    }
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t ad = dq + ((16384u * a + 32u * k) >> 4);
+        const uint64_t bd = dk + ((16384u * a + 32u * k) >> 4);
+        tc_mma_bf16(tmem + static_cast<uint32_t>(i) * AT_T, ad, bd, IDESC_S, (a | k) ? 1u : 0u);
+      }
+  }
+  __syncwarp();
 }
 // O_i (+)= P_i V(u): P_i (keys 2c, 2c+1 in column c of S_i) from tensor memory, V MN-major
 // (two 64-column atoms 8 KB apart, 8-key groups 1024 B apart).
@@ -345,23 +343,34 @@ __device__ __forceinline__ void at_pv(uint32_t base, uint32_t tmem, int i, int v
   const uint32_t pcol = tmem + static_cast<uint32_t>(i) * AT_T;
   const uint32_t obuf = tmem + AT_O_COL + static_cast<uint32_t>(i) * AT_T;
   const uint64_t dv = sdesc_sw128(vb, 8192u, 1024u);
+  if (elect_one_sync()) {
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint64_t bd = dv + ((16384u * a + 2048u * k) >> 4);
-      tc_mma_bf16_ts(obuf, pcol + 32u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
-    }
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t bd = dv + ((16384u * a + 2048u * k) >> 4);
+        tc_mma_bf16_ts(obuf, pcol + 32u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
+      }
+  }
+  __syncwarp();
+}
+// tcgen05.commit from the lane that issued the MMAs (elect.sync over the full
+// warp chooses the same lane each time).
+__device__ __forceinline__ void at_commit(uint32_t bar) {
+  if (elect_one_sync()) tc_commit(bar);
+  __syncwarp();
 }
 
-// MMA issuer (warp 1, one thread).  Iteration u: [GO_0 phase u-1] PV_0(u-1),
-// S_0(u), [GO_1 phase u-1] PV_1(u-1), S_1(u).  A product of tile u-1 is issued
-// before the S of tile u that overwrites its P: the tensor pipe runs a
-// thread's MMAs in issue order.  Commits: S_i full after each S_i (for S_1 also
-// the K stage free), V stage free after PV_1, the query tiles free after an
-// item's last S_1, O_i full after an item's last PV_i.
+// MMA issuer (warp 1, converged: lane 0 waits, one elected lane issues the
+// MMAs and commits, the descriptors are computed by the whole warp).
+// Iteration u: [GO_0 phase u-1, V(u-1) landed] PV_0(u-1), [K(u) landed]
+// S_0(u), [GO_1 phase u-1] PV_1(u-1), S_1(u).  A product of tile u-1 is
+// issued before the S of tile u that overwrites its P: the tensor pipe runs a
+// thread's MMAs in issue order.  Commits: S_i full after each S_i (for S_1
+// also the K stage free), V stage free after PV_1, the query tiles free after
+// an item's last S_1, O_i full after an item's last PV_i.
 __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32_t tmem) {
-  uint32_t q_ph = 0, go_ph = 0;
+  uint32_t q_ph = 0, go_ph = 0, k_ph = 0, v_ph = 0;
   uint32_t u = 0;
   int kst = 0, vst = 0;
   bool prev_first = false, prev_last = false;   // the pending tile u-1 opens / closes its item
@@ -370,54 +379,61 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     const AtItem it = at_item(p, i);
     item = i;
     for (int t = 0; t < it.n; ++t, ++u) {
-      if (u == 0) {
-        if (!at_wait_bar(p, bars + B_KFIRST, 0u, WHERE_MMA, i)) goto done;
-      } else {
-        // P_0(u-1), V(u-1) and K(u) are ready
-        if (!at_wait_bar<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+      if (u >= 1) {
+        // P_0(u-1) written and V(u-1) landed
+        if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, i)) goto done;
         tc_fence_after();
         at_pv(base, tmem, 0, vst, prev_first);
-        if (prev_last) tc_commit(bars + B_OFULL);
+        if (prev_last) at_commit(bars + B_OFULL);
       }
       if (t == 0) {
-        if (!at_wait_bar(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
         q_ph ^= 1u;
       }
+      if (!at_wait_warp<true>(p, bars + B_KFULL + 8u * kst, k_ph, WHERE_MMA, i)) goto done;
       tc_fence_after();
       at_s(base, tmem, 0, kst);
-      tc_commit(bars + B_SFULL);
+      at_commit(bars + B_SFULL);
       if (u >= 1) {
-        if (!at_wait_bar<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
         go_ph ^= 1u;
         tc_fence_after();
         at_pv(base, tmem, 1, vst, prev_first);
-        tc_commit(bars + B_VEMPTY + 8u * vst);   // V(u-1) read by both products
-        if (prev_last) tc_commit(bars + B_OFULL + 8u);
-        if (++vst == AT_VST) vst = 0;
+        at_commit(bars + B_VEMPTY + 8u * vst);   // V(u-1) read by both products
+        if (prev_last) at_commit(bars + B_OFULL + 8u);
+        if (++vst == AT_VST) {
+          vst = 0;
+          v_ph ^= 1u;
+        }
       }
       at_s(base, tmem, 1, kst);
-      tc_commit(bars + B_SFULL + 8u);
-      tc_commit(bars + B_KEMPTY + 8u * kst);     // K(u) read by both S
-      if (t == it.n - 1) tc_commit(bars + B_QEMPTY);
-      if (++kst == AT_KST) kst = 0;
+      at_commit(bars + B_SFULL + 8u);
+      at_commit(bars + B_KEMPTY + 8u * kst);     // K(u) read by both S
+      if (t == it.n - 1) at_commit(bars + B_QEMPTY);
+      if (++kst == AT_KST) {
+        kst = 0;
+        k_ph ^= 1u;
+      }
       prev_first = (t == 0);
       prev_last = (t == it.n - 1);
     }
   }
   if (u >= 1) {   // the products of the last tile
-    if (!at_wait_bar<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 0, vst, prev_first);
-    tc_commit(bars + B_OFULL);
-    if (!at_wait_bar<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
+    at_commit(bars + B_OFULL);
+    if (!at_wait_warp<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 1, vst, prev_first);
-    tc_commit(bars + B_VEMPTY + 8u * vst);
-    tc_commit(bars + B_OFULL + 8u);
+    at_commit(bars + B_VEMPTY + 8u * vst);
+    at_commit(bars + B_OFULL + 8u);
   }
 done:
-  tc_commit(bars + B_DRAIN);
-  at_wait_bar(p, bars + B_DRAIN, 0, WHERE_DRAIN, 0, false);
+  at_commit(bars + B_DRAIN);
+  at_wait_warp(p, bars + B_DRAIN, 0, WHERE_DRAIN, 0, false);
 }
 
 // 2^x for x <= 0 or -inf (the hardware approximation, flushing subnormals).
@@ -477,6 +493,72 @@ __device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& 
   y1 = __uint_as_float(r1);
 }
 
+// Row maximum of the 128 raw scores: four partial maxima, so that the
+// dependent chain is a quarter as long.
+__device__ __forceinline__ float at_row_max(const uint32_t (&sv)[4][32]) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int q = 0; q < 32; q += 2)
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      m4[cc] = fmax3(m4[cc], __uint_as_float(sv[cc][q]), __uint_as_float(sv[cc][q + 1]));
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+// The reference the exponentials are taken against for running maximum m.
+__device__ __forceinline__ float at_p_ref(float m) {
+#if MK_ATTN_PACK
+  return m - 0.0028150156f;   // log2(1 + 2^-9): the exponentials 2^-9 high
+#else
+  return m;
+#endif
+}
+// P = 2^(c*s - m_ref) of this thread's row (keys >= lim set to 0 when masked),
+// stored as bf16 pairs (keys 2q, 2q+1 in column q) over columns 0 .. 63 of S_i;
+// returns the row's sum of P.  MAX: also the maximum of the raw scores into mx.
+template <bool MAX>
+__device__ __forceinline__ float at_emit_p(const uint32_t (&sv)[4][32], uint32_t sbase, float c, float m_ref,
+                                           bool masked, int lim, float& mx) {
+  const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_ref, -m_ref);
+  uint64_t l4[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) {
+        const int q = 8 * h8 + qq;
+        const int kk = 32 * cc + 2 * q;
+        const float s0 = __uint_as_float(sv[cc][2 * q]), s1 = __uint_as_float(sv[cc][2 * q + 1]);
+        if (MAX) m4[cc] = fmax3(m4[cc], s0, s1);
+        float e0, e1, p0, p1;
+        f2unpack(f2fma(f2pack(s0, s1), c2, nm2), e0, e1);
+        if (((16 * cc + q) & 15) < POLY_PAIRS) {
+          ex2_poly2(e0, e1, p0, p1);
+        } else {
+          p0 = ex2(e0);
+          p1 = ex2(e1);
+        }
+        if (masked) {
+          p0 = (kk < lim) ? p0 : 0.f;
+          p1 = (kk + 1 < lim) ? p1 : 0.f;
+        }
+        l4[q & 1] = f2add(l4[q & 1], f2pack(p0, p1));
+#if MK_ATTN_PACK
+        pk[qq] = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x7632);
+#else
+        pk[qq] = pack_bf16x2(p0, p1);
+#endif
+      }
+      tc_st_32x32b_x8(sbase + 16u * cc + 8u * h8, pk);
+    }
+  if (MAX) mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  float la, lb;
+  f2unpack(f2add(l4[0], l4[1]), la, lb);
+  return la + lb;
+}
+
 // Softmax of query tile g (warps 2-5: g = 0, warps 6-9: g = 1): warp w handles
 // TMEM lanes 32 (w % 4) .. +31, one query row per thread, all 128 columns held
 // in registers (four loads of 32 columns, one wait).
@@ -504,7 +586,7 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
       if (p.causal && j == 0) lim = (kt > qt) ? 0 : (kt == qt ? min(valid, row + 1) : valid);
       const bool masked = __any_sync(0xffffffffu, lim < AT_T);
       {
-        const int ok = at_wait_bar<true>(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
+        const int ok = at_wait_bar(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
         if (!__all_sync(0xffffffffu, ok)) return;
       }
       sf_ph ^= 1u;
@@ -518,80 +600,46 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
       reg_fence(sv[1]);
       reg_fence(sv[2]);
       reg_fence(sv[3]);
-      // the row maximum (scale > 0 keeps the order: taken unscaled), four
-      // partial maxima so that the dependent chain is a quarter as long
-      float mx;
-      if (masked) {
-        mx = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(sv[cc][q]));
+      float factor = 1.f, lsum, mx;
+      if (t > 0 && !masked) {
+        // P against the running maximum, the tile's maximum taken alongside:
+        // the maximum moves only when it grows by more than 2^8, which the
+        // check below catches (then the tile is done again)
+        lsum = at_emit_p<true>(sv, sbase, c, at_p_ref(m_run), false, AT_T, mx);
+        const float m_new = fmaxf(m_run, mx * c);
+        const bool grow = m_new > m_run + RESCALE_LOG2;
+        if (__any_sync(0xffffffffu, grow)) {
+          if (grow) {
+            factor = ex2(m_run - m_new);
+            m_run = m_new;
+            l_run *= factor;
+          }
+          tc_wait_st();
+          lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run), false, AT_T, mx);
+        }
       } else {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int q = 0; q < 32; q += 2)
+        // the row maximum first (scale > 0 keeps the order: taken unscaled)
+        if (masked) {
+          mx = -INFINITY;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
-            m4[cc] = fmax3(m4[cc], __uint_as_float(sv[cc][q]), __uint_as_float(sv[cc][q + 1]));
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      const float m_new = fmaxf(m_run, mx * c);
-      float factor = 1.f;
-      if (t == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + RESCALE_LOG2) {
-        factor = ex2(m_run - m_new);
-        m_run = m_new;
-        l_run *= factor;
-      }
-      // P = 2^(c*s - m), four partial sums, P as bf16 pairs (keys 2q, 2q+1 in
-      // column q) over columns 0 .. 63 of S_i
-#if MK_ATTN_PACK
-      constexpr float PACK_BIAS = 0.0028150156f;   // log2(1 + 2^-9)
-      const float m_arg = m_run - PACK_BIAS;
-#else
-      const float m_arg = m_run;
-#endif
-      const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_arg, -m_arg);
-      uint64_t l4[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-        uint32_t pk[8];
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          const int q = 8 * h8 + qq;
-          const int kk = 32 * cc + 2 * q;
-          float e0, e1, p0, p1;
-          f2unpack(f2fma(f2pack(__uint_as_float(sv[cc][2 * q]), __uint_as_float(sv[cc][2 * q + 1])), c2, nm2),
-                   e0, e1);
-          if (((16 * cc + q) & 15) < POLY_PAIRS) {
-            ex2_poly2(e0, e1, p0, p1);
-          } else {
-            p0 = ex2(e0);
-            p1 = ex2(e1);
-          }
-          if (masked) {
-            p0 = (kk < lim) ? p0 : 0.f;
-            p1 = (kk + 1 < lim) ? p1 : 0.f;
-          }
-          l4[q & 1] = f2add(l4[q & 1], f2pack(p0, p1));
-#if MK_ATTN_PACK
-          pk[qq] = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x7632);
-#else
-          pk[qq] = pack_bf16x2(p0, p1);
-#endif
+            for (int q = 0; q < 32; ++q)
+              if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(sv[cc][q]));
+        } else {
+          mx = at_row_max(sv);
         }
-        tc_st_32x32b_x8(sbase + 16u * cc + 8u * h8, pk);
+        const float m_new = fmaxf(m_run, mx * c);
+        if (t == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + RESCALE_LOG2) {
+          factor = ex2(m_run - m_new);
+          m_run = m_new;
+          l_run *= factor;
+        }
+        lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run), masked, lim, mx);
       }
-      {
-        float la, lb;
-        f2unpack(f2add(l4[0], l4[1]), la, lb);
-        l_run += la + lb;
-      }
+      l_run += lsum;
       // S_i(u) complete implies the product of tile u-1 complete (issued before
       // it): O_i is settled until this group publishes P_i(u)
       if (__any_sync(0xffffffffu, factor != 1.f)) {
@@ -735,14 +783,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
   if (warp == 0 && lane == 0) {
     mbar_init(bars + B_QFULL, 1);
     mbar_init(bars + B_QEMPTY, 1);
-    mbar_init(bars + B_KFIRST, 1);
-    for (int s = 0; s < AT_KST; ++s) mbar_init(bars + B_KEMPTY + 8u * s, 1);
-    for (int s = 0; s < AT_VST; ++s) mbar_init(bars + B_VEMPTY + 8u * s, 1);
+    for (int s = 0; s < AT_KST; ++s) {
+      mbar_init(bars + B_KFULL + 8u * s, 1);
+      mbar_init(bars + B_KEMPTY + 8u * s, 1);
+    }
+    for (int s = 0; s < AT_VST; ++s) {
+      mbar_init(bars + B_VFULL + 8u * s, 1);
+      mbar_init(bars + B_VEMPTY + 8u * s, 1);
+    }
     for (int g = 0; g < 2; ++g) {
       mbar_init(bars + B_SFULL + 8u * g, 1);
       mbar_init(bars + B_OFULL + 8u * g, 1);
     }
-    mbar_init(bars + B_GO, 6);          // Q0 softmax warps, the V load, the next K load
+    mbar_init(bars + B_GO, 4);          // Q0 softmax warps
     mbar_init(bars + B_GO + 8u, 4);     // Q1 softmax warps
     mbar_init(bars + B_DRAIN, 1);       // MMA drain
     fence_mbar_init();
@@ -762,7 +815,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) at_mma(p, bars, base, tmem);
+    at_mma(p, bars, base, tmem);
     __syncwarp();
   } else if (warp <= 9) {
     at_softmax(p, bars, tmem);
