@@ -10,18 +10,19 @@
 //   * warp 0 (TMA): the item's two Q tiles, then the K tiles, 128 keys each,
 //     in ring order -- the rank's own block, then the blocks of ranks r-1,
 //     r-2, ... as they land in its receive buffer; warp 11 (TMA): the V tiles;
-//   * warp 1 (MMA, one elected lane issuing): per K/V tile, S_i = Q_i K^T (i = 0, 1) into tensor memory,
-//     and O_i += P_i V with P_i read from tensor memory (tcgen05, bf16 ->
-//     fp32), in the order PV_0(u-1), S_0(u), PV_1(u-1), S_1(u), so that the
-//     product of one query tile runs while the other's softmax works;
-//   * warps 2-5 / 6-9 (softmax of Q0 / Q1): online softmax over the rows of
-//     their query tile, each thread one row held in registers, P = 2^(scale *
-//     log2(e) * s - m) written as bf16 over the first 64 columns of S_i in
-//     tensor memory; O_i is rescaled only when the maximum grows by more than 2^8
-//     (the final division uses the same stale maximum for O and the sum, so
-//     the result is unchanged); part of the exponentials run as a polynomial
-//     on the FMA pipe beside the hardware ex2; at the end of an item the
-//     group scales O_i by 1 / sum and stores it;
+//   * warp 1 (MMA, one elected lane issuing): per K/V tile, S_i = Q_i K^T
+//     (i = 0, 1) into tensor memory, and O_i += P_i V with P_i read from
+//     tensor memory (tcgen05, bf16 -> fp32), in the order PV_0(u-1), S_0(u),
+//     PV_1(u-1), S_1(u), so that the product of one query tile runs while
+//     the softmax works on the other;
+//   * warps 2-9 (softmax): all eight on every S tile, S_0 then S_1; each
+//     warp holds 16 query rows, each thread half a row (64 keys) in
+//     registers; P = 2^(scale * log2(e) * s - m) is written as bf16 into
+//     the row half's own columns of S_i; the exponentials are taken against
+//     the running maximum, which moves only when it grows by more than 2^8
+//     (O_i is then rescaled; the final division uses the same maximum for O
+//     and the sum, so the result is unchanged); at the end of an item the
+//     warps scale O_0 and O_1 by 1 / sum and store them;
 //   * warp 10 (copy): the ring's transfers -- rank r receives the block
 //     of rank (r - j) mod R at step j -- as row copies into its receive
 //     buffer, one counter per (rank, step, head).
@@ -151,14 +152,35 @@ __device__ __forceinline__ bool at_wait_bar(const AttnParams& p, uint32_t bar, u
   if (SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   return at_wait_loop<SPIN>(p, bar, parity, where, item, honor_abort);
 }
-// The MMA warp's waits: lane 0 polls, the other lanes wait at the shuffle, and
-// every lane returns lane 0's result, so the warp stays converged.
+// The MMA warp's waits: every lane polls the barrier (one instruction for the
+// warp, and no divergence: a lane-0 poll with a shuffle costs about four times
+// as long) and the warp agrees by vote; lane 0 reports a timeout.
+template <bool SPIN>
+__device__ __noinline__ bool at_wait_warp_loop(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
+                                               bool honor_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) return true;
+    if ((++it & (SPIN ? 255u : 31u)) == 0) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (honor_abort && at_aborted(p)) {
+          stop = 1;
+        } else if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+          at_error(p, where, item);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0) != 0) return false;
+    }
+  }
+}
 template <bool SPIN = false>
 __device__ __forceinline__ bool at_wait_warp(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
                                              bool honor_abort = true) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = at_wait_bar<SPIN>(p, bar, parity, where, item, honor_abort) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  if (__all_sync(0xffffffffu, SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) return true;
+  return at_wait_warp_loop<SPIN>(p, bar, parity, where, item, honor_abort);
 }
 __device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* f, uint32_t want, int where,
                                            int item) {
@@ -227,7 +249,7 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 // K(u) and V(u) go to stages u % AT_KST and u % AT_VST, each stage with a full
 // barrier (the TMA bytes) and an empty barrier (the MMAs that read it), so a
 // load is issued as soon as its stage is free.  GO_i phase u completes on the
-// four arrivals of query tile i's softmax warps (P_i(u) written).
+// arrivals of the eight softmax warps once P_i(u) is written.
 __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, int t, bool is_v, int item,
                                        bool& ready, int& waited_j, const CUtensorMap*& m, int& row) {
   int j, s, kt;
@@ -336,7 +358,8 @@ __device__ __forceinline__ void at_s(uint32_t base, uint32_t tmem, int i, int ks
   }
   __syncwarp();
 }
-// O_i (+)= P_i V(u): P_i (keys 2c, 2c+1 in column c of S_i) from tensor memory, V MN-major
+// O_i (+)= P_i V(u): P_i from tensor memory (keys 2c, 2c+1 in column c for c < 32, keys
+// 64 + 2c, 65 + 2c in column 64 + c), V MN-major
 // (two 64-column atoms 8 KB apart, 8-key groups 1024 B apart).
 __device__ __forceinline__ void at_pv(uint32_t base, uint32_t tmem, int i, int vstage, bool first) {
   const uint32_t vb = base + AT_V + static_cast<uint32_t>(vstage) * AT_TILE;
@@ -349,7 +372,7 @@ __device__ __forceinline__ void at_pv(uint32_t base, uint32_t tmem, int i, int v
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint64_t bd = dv + ((16384u * a + 2048u * k) >> 4);
-        tc_mma_bf16_ts(obuf, pcol + 32u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
+        tc_mma_bf16_ts(obuf, pcol + 64u * a + 8u * k, bd, IDESC_PV, (!first || a || k) ? 1u : 0u);
       }
   }
   __syncwarp();
@@ -363,8 +386,8 @@ __device__ __forceinline__ void at_commit(uint32_t bar) {
 
 // MMA issuer (warp 1, converged: lane 0 waits, one elected lane issues the
 // MMAs and commits, the descriptors are computed by the whole warp).
-// Iteration u: [GO_0 phase u-1, V(u-1) landed] PV_0(u-1), [K(u) landed]
-// S_0(u), [GO_1 phase u-1] PV_1(u-1), S_1(u).  A product of tile u-1 is
+// Iteration u: [K(u), V(u-1) landed, GO_0 phase u-1] PV_0(u-1), S_0(u),
+// [GO_1 phase u-1] PV_1(u-1), S_1(u).  A product of tile u-1 is
 // issued before the S of tile u that overwrites its P: the tensor pipe runs a
 // thread's MMAs in issue order.  Commits: S_i full after each S_i (for S_1
 // also the K stage free), V stage free after PV_1, the query tiles free after
@@ -379,19 +402,21 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     const AtItem it = at_item(p, i);
     item = i;
     for (int t = 0; t < it.n; ++t, ++u) {
-      if (u >= 1) {
-        // P_0(u-1) written and V(u-1) landed
-        if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
-        if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, i)) goto done;
-        tc_fence_after();
-        at_pv(base, tmem, 0, vst, prev_first);
-        if (prev_last) at_commit(bars + B_OFULL);
-      }
+      // the loads first (they have usually landed long before): every wait
+      // costs the issuer time, and P_0(u-1) is the one the chain waits for
       if (t == 0) {
         if (!at_wait_warp(p, bars + B_QFULL, q_ph, WHERE_MMA, i)) goto done;
         q_ph ^= 1u;
       }
       if (!at_wait_warp<true>(p, bars + B_KFULL + 8u * kst, k_ph, WHERE_MMA, i)) goto done;
+      if (u >= 1) {
+        // V(u-1) landed and P_0(u-1) written
+        if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+        tc_fence_after();
+        at_pv(base, tmem, 0, vst, prev_first);
+        if (prev_last) at_commit(bars + B_OFULL);
+      }
       tc_fence_after();
       at_s(base, tmem, 0, kst);
       at_commit(bars + B_SFULL);
@@ -420,8 +445,8 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
     }
   }
   if (u >= 1) {   // the products of the last tile
-    if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
     if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 0, vst, prev_first);
     at_commit(bars + B_OFULL);
@@ -493,17 +518,6 @@ __device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& 
   y1 = __uint_as_float(r1);
 }
 
-// Row maximum of the 128 raw scores: four partial maxima, so that the
-// dependent chain is a quarter as long.
-__device__ __forceinline__ float at_row_max(const uint32_t (&sv)[4][32]) {
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int q = 0; q < 32; q += 2)
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-      m4[cc] = fmax3(m4[cc], __uint_as_float(sv[cc][q]), __uint_as_float(sv[cc][q + 1]));
-  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-}
 // The reference the exponentials are taken against for running maximum m.
 __device__ __forceinline__ float at_p_ref(float m) {
 #if MK_ATTN_PACK
@@ -512,26 +526,36 @@ __device__ __forceinline__ float at_p_ref(float m) {
   return m;
 #endif
 }
-// P = 2^(c*s - m_ref) of this thread's row (keys >= lim set to 0 when masked),
-// stored as bf16 pairs (keys 2q, 2q+1 in column q) over columns 0 .. 63 of S_i;
-// returns the row's sum of P.  MAX: also the maximum of the raw scores into mx.
+// Half a row: this thread's 64 keys of S_i (keys 64 kh + 0 .. 63, kh = the
+// thread's half).  P = 2^(c*s - m_ref) (keys >= lim set to 0 when masked) is
+// stored as bf16 pairs, keys 2q, 2q+1 (q = 0 .. 31 within the half) in
+// column 64 kh + q of S_i, i.e. inside the half's own score columns; returns
+// the half's sum of P.  MAX: also the maximum of the half's raw scores (of the
+// keys below lim) into mx.
 template <bool MAX>
-__device__ __forceinline__ float at_emit_p(const uint32_t (&sv)[4][32], uint32_t sbase, float c, float m_ref,
-                                           bool masked, int lim, float& mx) {
+__device__ __forceinline__ float at_emit_p(const uint32_t (&sv)[2][32], uint32_t sbase, float c, float m_ref,
+                                           bool masked, int lim, int key0, float& mx) {
   const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_ref, -m_ref);
   uint64_t l4[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float m4[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc)
+  for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
     for (int h8 = 0; h8 < 2; ++h8) {
       uint32_t pk[8];
 #pragma unroll
       for (int qq = 0; qq < 8; ++qq) {
         const int q = 8 * h8 + qq;
-        const int kk = 32 * cc + 2 * q;
+        const int kk = key0 + 32 * cc + 2 * q;
         const float s0 = __uint_as_float(sv[cc][2 * q]), s1 = __uint_as_float(sv[cc][2 * q + 1]);
-        if (MAX) m4[cc] = fmax3(m4[cc], s0, s1);
+        if (MAX) {
+          if (masked) {
+            if (kk < lim) m4[cc] = fmaxf(m4[cc], s0);
+            if (kk + 1 < lim) m4[cc] = fmaxf(m4[cc], s1);
+          } else {
+            m4[cc] = fmax3(m4[cc], s0, s1);
+          }
+        }
         float e0, e1, p0, p1;
         f2unpack(f2fma(f2pack(s0, s1), c2, nm2), e0, e1);
         if (((16 * cc + q) & 15) < POLY_PAIRS) {
@@ -551,144 +575,149 @@ __device__ __forceinline__ float at_emit_p(const uint32_t (&sv)[4][32], uint32_t
         pk[qq] = pack_bf16x2(p0, p1);
 #endif
       }
-      tc_st_32x32b_x8(sbase + 16u * cc + 8u * h8, pk);
+      tc_st_16x32bx2_x8_h64(sbase + 16u * cc + 8u * h8, pk);
     }
-  if (MAX) mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  if (MAX) mx = fmaxf(m4[0], m4[1]);
   float la, lb;
   f2unpack(f2add(l4[0], l4[1]), la, lb);
   return la + lb;
 }
 
-// Softmax of query tile g (warps 2-5: g = 0, warps 6-9: g = 1): warp w handles
-// TMEM lanes 32 (w % 4) .. +31, one query row per thread, all 128 columns held
-// in registers (four loads of 32 columns, one wait).
+// Softmax (warps 2-9): all eight warps work on every S tile, S_0 then S_1 of
+// each K/V tile.  Warp w takes 16 of the 32 TMEM lanes of its quarter (w % 4):
+// lanes 32 (w % 4) + 16 ((w - 2) / 4) + 0 .. 15, one query row each; a row is
+// split between threads t and t + 16 (keys 0 .. 63 and 64 .. 127), which
+// combine its maximum and sum by one shuffle, so both halves of a row always
+// hold the same running maximum.
 __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int g = (warp - 2) >> 2;                             // query tile of the pair
-  const int row = quarter * 32 + lane;                       // query row within the tile
-  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(g) * AT_T;
-  const uint32_t obase = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(g) * AT_T;
-  const uint32_t sfull = bars + B_SFULL + 8u * g, go = bars + B_GO + 8u * g, ofull = bars + B_OFULL + 8u * g;
+  const int lane16 = 32 * quarter + 16 * ((warp - 2) >> 2);  // first TMEM lane of this warp
+  const int row = lane16 + (lane & 15);                      // query row within a tile
+  const int kh = lane >> 4;                                  // which half of the row's keys
+  const int key0 = 64 * kh;
+  const uint32_t lane_off = static_cast<uint32_t>(lane16) << 16;
   const float c = p.scale_log2;
-  uint32_t sf_ph = 0, of_ph = 0;
+  uint32_t sf_ph = 0, of_ph = 0;                             // bit g: query tile g
   for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
     const AtItem it = at_item(p, i);
-    const int qt = 2 * it.qp + g;
-    const int qpos = qt * AT_T + row;                        // position within rank r's block
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     for (int t = 0; t < it.n; ++t) {
       int j, s, kt;
       at_tile(p, it, t, j, s, kt);
       const int valid = min(AT_T, p.s_r - kt * AT_T);       // keys of this tile inside the block
-      int lim = valid;
-      if (p.causal && j == 0) lim = (kt > qt) ? 0 : (kt == qt ? min(valid, row + 1) : valid);
-      const bool masked = __any_sync(0xffffffffu, lim < AT_T);
-      {
-        const int ok = at_wait_bar(p, sfull, sf_ph, WHERE_EPILOGUE, i) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, ok)) return;
-      }
-      sf_ph ^= 1u;
-      tc_fence_after();
-      uint32_t sv[4][32];
-      tc_ld_32x32b_x32(sbase, sv[0]);
-      tc_ld_32x32b_x32(sbase + 32u, sv[1]);
-      tc_ld_32x32b_x32(sbase + 64u, sv[2]);
-      tc_ld_32x32b_x32(sbase + 96u, sv[3]);
-      tc_wait_ld_regs(sv[0]);
-      reg_fence(sv[1]);
-      reg_fence(sv[2]);
-      reg_fence(sv[3]);
-      float factor = 1.f, lsum, mx;
-      if (t > 0 && !masked) {
-        // P against the running maximum, the tile's maximum taken alongside:
-        // the maximum moves only when it grows by more than 2^8, which the
-        // check below catches (then the tile is done again)
-        lsum = at_emit_p<true>(sv, sbase, c, at_p_ref(m_run), false, AT_T, mx);
-        const float m_new = fmaxf(m_run, mx * c);
-        const bool grow = m_new > m_run + RESCALE_LOG2;
-        if (__any_sync(0xffffffffu, grow)) {
-          if (grow) {
-            factor = ex2(m_run - m_new);
-            m_run = m_new;
-            l_run *= factor;
-          }
-          tc_wait_st();
-          lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run), false, AT_T, mx);
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int qt = 2 * it.qp + g;
+        const uint32_t sbase = tmem + lane_off + static_cast<uint32_t>(g) * AT_T;
+        int lim = valid;
+        if (p.causal && j == 0) lim = (kt > qt) ? 0 : (kt == qt ? min(valid, row + 1) : valid);
+        const bool masked = __any_sync(0xffffffffu, lim < AT_T);
+        {
+          const int ok = at_wait_bar(p, bars + B_SFULL + 8u * g, (sf_ph >> g) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
+          if (!__all_sync(0xffffffffu, ok)) return;
         }
-      } else {
-        // the row maximum first (scale > 0 keeps the order: taken unscaled)
-        if (masked) {
+        sf_ph ^= 1u << g;
+        tc_fence_after();
+        uint32_t sv[2][32];
+        tc_ld_16x32bx2_x32_h64(sbase, sv[0]);
+        tc_ld_16x32bx2_x32_h64(sbase + 32u, sv[1]);
+        tc_wait_ld_regs(sv[0]);
+        reg_fence(sv[1]);
+        float factor = 1.f, lsum, mx;
+        if (t > 0 && !masked) {
+          // P against the running maximum, the tile's maximum taken alongside:
+          // the maximum moves only when it grows by more than 2^8, which the
+          // check below catches (then the tile is done again)
+          lsum = at_emit_p<true>(sv, sbase, c, at_p_ref(m_run[g]), false, AT_T, key0, mx);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[g], mx * c);
+          const bool grow = m_new > m_run[g] + RESCALE_LOG2;
+          if (__any_sync(0xffffffffu, grow)) {
+            if (grow) {
+              factor = ex2(m_run[g] - m_new);
+              m_run[g] = m_new;
+              l_run[g] *= factor;
+            }
+            tc_wait_st();
+            lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run[g]), false, AT_T, key0, mx);
+          }
+        } else {
+          // the row maximum first (scale > 0 keeps the order: taken unscaled)
           mx = -INFINITY;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-              if (32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(sv[cc][q]));
-        } else {
-          mx = at_row_max(sv);
+              if (!masked || key0 + 32 * cc + q < lim) mx = fmaxf(mx, __uint_as_float(sv[cc][q]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[g], mx * c);
+          if (t == 0) {
+            m_run[g] = m_new;
+          } else if (m_new > m_run[g] + RESCALE_LOG2) {
+            factor = ex2(m_run[g] - m_new);
+            m_run[g] = m_new;
+            l_run[g] *= factor;
+          }
+          lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run[g]), masked, lim, key0, mx);
         }
-        const float m_new = fmaxf(m_run, mx * c);
-        if (t == 0) {
-          m_run = m_new;
-        } else if (m_new > m_run + RESCALE_LOG2) {
-          factor = ex2(m_run - m_new);
-          m_run = m_new;
-          l_run *= factor;
-        }
-        lsum = at_emit_p<false>(sv, sbase, c, at_p_ref(m_run), masked, lim, mx);
-      }
-      l_run += lsum;
-      // S_i(u) complete implies the product of tile u-1 complete (issued before
-      // it): O_i is settled until this group publishes P_i(u)
-      if (__any_sync(0xffffffffu, factor != 1.f)) {
+        l_run[g] += lsum;
+        // S_g(u) complete implies the product of tile u-1 complete (issued
+        // before it): O_g is settled until P_g(u) is published
+        if (__any_sync(0xffffffffu, factor != 1.f)) {
+          const uint32_t obase = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(g) * AT_T;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          tc_ld_32x32b_x32(obase + 32u * cc, v);
-          tc_wait_ld();
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+            tc_ld_16x32bx2_x32_h64(obase + 32u * cc, v);
+            tc_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
-          tc_st_32x32b_x32(obase + 32u * cc, v);
+            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * factor);
+            tc_st_16x32bx2_x32_h64(obase + 32u * cc, v);
+          }
         }
+        // P_g(u) (and any rescaled O_g) written: the products may read them
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + B_GO + 8u * g);
       }
-      // P_i(u) (and any rescaled O_i) written: the products may read them
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(go);
     }
-    // item done: the last product into O_i has completed
-    {
-      const int ok = at_wait_bar(p, ofull, of_ph, WHERE_EPILOGUE, i) ? 1 : 0;
-      if (!__all_sync(0xffffffffu, ok)) return;
-    }
-    of_ph ^= 1u;
-    tc_fence_after();
+    // item done: the last product into each O_g has completed
+    for (int g = 0; g < 2; ++g) {
+      {
+        const int ok = at_wait_bar(p, bars + B_OFULL + 8u * g, (of_ph >> g) & 1u, WHERE_EPILOGUE, i) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
+      of_ph ^= 1u << g;
+      tc_fence_after();
+      const float l = l_run[g] + __shfl_xor_sync(0xffffffffu, l_run[g], 16);
 #if MK_ATTN_PACK
-    const float inv = (l_run > 0.f) ? 1.001953125f / l_run : 0.f;   // (1 + 2^-9) / sum
+      const float inv = (l > 0.f) ? 1.001953125f / l : 0.f;   // (1 + 2^-9) / sum
 #else
-    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #endif
-    const bool row_ok = qpos < p.s_r;
-    uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2;
+      const int qpos = (2 * it.qp + g) * AT_T + row;          // position within rank r's block
+      const bool row_ok = qpos < p.s_r;
+      uint8_t* orow = p.out[it.r] + (static_cast<size_t>(it.h) * p.s_r + qpos) * AT_D * 2 + key0 * 2;
+      const uint32_t obase = tmem + lane_off + AT_O_COL + static_cast<uint32_t>(g) * AT_T;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      uint32_t v[32];
-      tc_ld_32x32b_x32(obase + 32u * cc, v);
-      tc_wait_ld();
-      if (!row_ok) continue;
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        tc_ld_16x32bx2_x32_h64(obase + 32u * cc, v);
+        tc_wait_ld();
+        if (!row_ok) continue;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_global_v4(orow + (32 * cc + 8 * q) * 2,
-                     pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                     pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+        for (int q = 0; q < 4; ++q)
+          st_global_v4(orow + (32 * cc + 8 * q) * 2,
+                       pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+      }
     }
-    // O_i read out: the next item's first product may overwrite it once this
-    // group has published that item's first P (the wait before that product)
+    // O read out: the next item's first products may overwrite it once P of
+    // that item's first tile is published (the waits before those products)
     tc_fence_before();
   }
 }
@@ -795,8 +824,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
       mbar_init(bars + B_SFULL + 8u * g, 1);
       mbar_init(bars + B_OFULL + 8u * g, 1);
     }
-    mbar_init(bars + B_GO, 4);          // Q0 softmax warps
-    mbar_init(bars + B_GO + 8u, 4);     // Q1 softmax warps
+    mbar_init(bars + B_GO, 8);          // the softmax warps, for Q0
+    mbar_init(bars + B_GO + 8u, 8);     // and for Q1
     mbar_init(bars + B_DRAIN, 1);       // MMA drain
     fence_mbar_init();
   }
