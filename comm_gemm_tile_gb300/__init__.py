@@ -23,7 +23,7 @@ MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_CUDA, MK_ERR_TIMEOUT, MK_ERR_C
 MK_BF16, MK_F32 = 0, 1
 OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR, OP_MOE = 0, 1, 2, 3
 MODE_FUSED, MODE_GEMM_ONLY, MODE_UNFUSED = 0, 1, 2
-REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL, REDUCE_ATOMIC = 0, 1, 2, 3
+REDUCE_AUTO, REDUCE_RUNNING_SUM, REDUCE_LAST_ARRIVAL, REDUCE_ATOMIC, REDUCE_SLICED = 0, 1, 2, 3, 4
 WIRE_F32, WIRE_BF16 = 0, 1
 OPERAND_BF16, OPERAND_FP8 = 0, 1
 FP8 = torch.float8_e4m3fn

@@ -158,11 +158,13 @@ struct Plan {
   int n_mblk, n_nblk, n_kblk, n_tiles;
   int split_k, kps, P;
   int group_m;
-  int chain, last, atomic, wire, fp8;
+  int chain, last, sliced, atomic, wire, fp8;
+  int ar_single;   // AR small enough for the sliced reduction: single CTAs by default
   size_t flags_off, n_flags, staging_off, staging_bytes, total;
   size_t trace_off, trace_n;   // in-kernel trace records (8 x u64 each) at the end, or none
 };
 constexpr int ZFLAG_WORDS = 1024;   // atomic reduction: one zero-done word per CTA
+constexpr long long SLICED_MAX_PARTIAL_TILES = 2048;   // 256 MiB of staged fp32 partial tiles
 
 static bool plan_gemm(int op, int R, long long m, long long n, long long k, const mk_config* cfg,
                       Plan& pl) {
@@ -193,11 +195,13 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
   pl.staging_bytes = 0;
   pl.chain = 0;
   pl.last = 0;
+  pl.sliced = 0;
+  pl.ar_single = 0;
   pl.atomic = 0;
   pl.wire = 0;
   const int want_reduce = cfg ? cfg->reduce : 0;
   const int want_wire = cfg ? cfg->wire : 0;
-  if (want_reduce < 0 || want_reduce > 3 || want_wire < 0 || want_wire > 1) return false;
+  if (want_reduce < 0 || want_reduce > 4 || want_wire < 0 || want_wire > 1) return false;
   // fp8 operands: 128-element k-blocks, and every row a whole number of 16-byte units
   pl.fp8 = cfg ? cfg->operand : 0;
   if (pl.fp8 < 0 || pl.fp8 > 1) return false;
@@ -211,16 +215,28 @@ static bool plan_gemm(int op, int R, long long m, long long n, long long k, cons
     // n_reduce_ctas > 0, or in the unfused baseline, every partial is staged
     // in its own slot and reduce-role CTAs sum them (at most MAX_PARTIALS).
     // Without reduce-role CTAs the fused path reduces in the epilogues, either
-    // as a running sum (the default: measured fastest for both RS and AR) or by
-    // last arrival (the warp that completes a tile quarter sums all partials).
+    // as a running sum (the default for RS and large AllReduces), by slices
+    // (below: the default for small AllReduces) or by last arrival (the warp
+    // that completes a tile quarter sums all partials).
     // Two variants of the in-epilogue reduction trade the fixed rank order for
     // less partial traffic: the running sum forwarded in bf16 (wire = 1), and
     // red.global.add of every partial into one fp32 tile per output tile
     // (reduce = 3), converted by the warp that completes it.
     const bool in_epilogue = (mode == MK_MODE_FUSED && !(cfg && cfg->n_reduce_ctas > 0));
-    const int want = want_reduce;
-    pl.chain = (in_epilogue && want != 2 && want != 3) ? 1 : 0;
-    pl.last = (in_epilogue && want == 2) ? 1 : 0;
+    // An AllReduce whose R partials per output tile fit in SLICED_MAX_PARTIAL_TILES
+    // staged tiles (the decode shape: few output tiles) reduces by slices by
+    // default: every part stages its partial without waiting, and once their own
+    // tiles are done all epilogue warps sum 32-row x 64-column slices in rank
+    // order -- the running sum's serial chain of R steps was the tail of the
+    // launch.  Such AllReduces also run one CTA per tile by default (in every
+    // mode, so the GEMM-only baseline has the same tiles): a pair's 256-row
+    // tile is half empty at m = 128.
+    pl.ar_single = (op == OP_AR && static_cast<long long>(pl.n_tiles) * R <= SLICED_MAX_PARTIAL_TILES) ? 1 : 0;
+    int want = want_reduce;
+    if (want == 0 && pl.ar_single && in_epilogue && want_wire == 0 && !(cfg && cfg->split_k > 1)) want = 4;
+    pl.chain = (in_epilogue && want != 2 && want != 3 && want != 4) ? 1 : 0;
+    pl.last = (in_epilogue && (want == 2 || want == 4)) ? 1 : 0;
+    pl.sliced = (in_epilogue && want == 4) ? 1 : 0;
     pl.atomic = (in_epilogue && want == 3) ? 1 : 0;
     pl.wire = (pl.chain && want_wire == 1) ? 1 : 0;
     const int max_parts = in_epilogue ? MAX_CHAIN_PARTIALS : MAX_PARTIALS;
@@ -289,6 +305,7 @@ static void fill_common(FusedParams& p, const Plan& pl, uint8_t* ws, const mk_co
   p.P = pl.P;
   p.chain = pl.chain;
   p.last_arrival = pl.last;
+  p.sliced = pl.sliced;
   p.atomic = pl.atomic;
   p.wire_bf16 = pl.wire;
   p.fp8 = pl.fp8;
@@ -576,7 +593,8 @@ static mk_status rs_ar_common(int op, const void* const* a, const void* const* b
   if (op == OP_AR) p.rows_per_owner = static_cast<int>(m);
   p.b_one_box = (n % 64 == 0) ? 1 : 0;
   // CTA pairs for every compute-only launch (not with reduce-role CTAs).
-  const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last || pl.atomic);
+  const bool pair = use_pair(cfg, sms) && (pl.mode != MK_MODE_FUSED || pl.chain || pl.last || pl.atomic) &&
+                    !(pl.ar_single && !(cfg && cfg->cta_pair == 2));
   for (int r = 0; r < R; ++r) {
     p.out[r] = outs[r];
     if (pl.fp8) {   // A_r [m x k] and B_r^T [n x k], bytes

@@ -250,8 +250,14 @@ __device__ __forceinline__ uint32_t* at_counter(const AttnParams& p, int r, int 
 // barrier (the TMA bytes) and an empty barrier (the MMAs that read it), so a
 // load is issued as soon as its stage is free.  GO_i phase u completes on the
 // arrivals of the eight softmax warps once P_i(u) is written.
+// The K / V maps have the block as their outer coordinate (head h of a
+// rank's own K_r / V_r, or block (j-1) * heads + h of a receive buffer) and
+// rows 0 .. s_r-1 inside it, so the rows of a ragged last tile past s_r read
+// as zeros: never another block's rows, which in a receive buffer may not
+// have arrived yet (and whatever they hold would enter P V even with P = 0,
+// as 0 * NaN).
 __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, int t, bool is_v, int item,
-                                       bool& ready, int& waited_j, const CUtensorMap*& m, int& row) {
+                                       bool& ready, int& waited_j, const CUtensorMap*& m, int& row, int& blk) {
   int j, s, kt;
   at_tile(p, it, t, j, s, kt);
   if (!at_bounds_ok(p, j >= 0 && j < p.R && s >= 0 && s < p.R && kt >= 0 && kt < p.nkt && it.h >= 0 &&
@@ -259,7 +265,8 @@ __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, in
                     BC_ATTN_TILE, item))
     return false;
   m = is_v ? &p.tmV[s] : &p.tmK[s];
-  row = it.h * p.s_r + kt * AT_T;
+  row = kt * AT_T;
+  blk = it.h;
   if (j > 0 && p.use_recv) {
     if (p.wait && j != waited_j) {
       if (!ready) {
@@ -271,7 +278,7 @@ __device__ __forceinline__ bool at_src(const AttnParams& p, const AtItem& it, in
       waited_j = j;
     }
     m = is_v ? &p.tmVr[it.r] : &p.tmKr[it.r];
-    row = ((j - 1) * p.heads + it.h) * p.s_r + kt * AT_T;
+    blk = (j - 1) * p.heads + it.h;
   }
   return true;
 }
@@ -287,14 +294,14 @@ __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base)
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
       const CUtensorMap* m;
-      int row;
-      if (!at_src(p, it, t, false, i, ready, waited_j, m, row)) return;
+      int row, blk;
+      if (!at_src(p, it, t, false, i, ready, waited_j, m, row, blk)) return;
       if (!at_wait_bar(p, bars + B_KEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
       const uint32_t full = bars + B_KFULL + 8u * stage;
       const uint32_t dst = base + AT_K + static_cast<uint32_t>(stage) * AT_TILE;
       mbar_arrive_expect_tx(full, AT_TILE);
-      tma_load_2d(dst, m, full, 0, row);
-      tma_load_2d(dst + 16384u, m, full, 64, row);
+      tma_load_3d(dst, m, full, 0, row, blk);
+      tma_load_3d(dst + 16384u, m, full, 64, row, blk);
       if (++stage == AT_KST) {
         stage = 0;
         e_ph ^= 1u;
@@ -324,14 +331,14 @@ __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base)
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
       const CUtensorMap* m;
-      int row;
-      if (!at_src(p, it, t, true, i, ready, waited_j, m, row)) return;
+      int row, blk;
+      if (!at_src(p, it, t, true, i, ready, waited_j, m, row, blk)) return;
       if (!at_wait_bar(p, bars + B_VEMPTY + 8u * stage, e_ph ^ 1u, WHERE_PRODUCER, i)) return;
       const uint32_t full = bars + B_VFULL + 8u * stage;
       const uint32_t dst = base + AT_V + static_cast<uint32_t>(stage) * AT_TILE;
       mbar_arrive_expect_tx(full, AT_TILE);
-      tma_load_3d(dst, m, full, 0, row, 0);
-      tma_load_3d(dst + 16384u, m, full, 0, row + 64, 0);
+      tma_load_4d(dst, m, full, 0, row, 0, blk);
+      tma_load_4d(dst + 16384u, m, full, 0, row + 64, 0, blk);
       if (++stage == AT_VST) {
         stage = 0;
         e_ph ^= 1u;
@@ -961,15 +968,20 @@ mk_status mk_ring_attention(const void* const* q, const void* const* k, const vo
     p.out[r] = static_cast<uint8_t*>(out[r]);
     p.ksrc[r] = static_cast<const uint8_t*>(k[r]);
     p.vsrc[r] = static_cast<const uint8_t*>(v[r]);
-    if (!make_map_a(&p.tmQ[r], q[r], AT_D, rows, AT_D * 2) || !make_map_a(&p.tmK[r], k[r], AT_D, rows, AT_D * 2) ||
-        !make_map_b_chunks(&p.tmV[r], v[r], rows, AT_D, 2))
+    // K: [d, s_r, heads], boxes of 64 d x 128 rows; V: [64 d, s_r, 2 d halves,
+    // heads], boxes of 64 rows x both halves (MN-major for P V)
+    if (!make_map_a(&p.tmQ[r], q[r], AT_D, rows, AT_D * 2) ||
+        !make_map_3d(&p.tmK[r], k[r], AT_D, s_r, heads, AT_D * 2, static_cast<uint64_t>(s_r) * AT_D * 2, 64, AT_T,
+                     1) ||
+        !make_map_w_chunks(&p.tmV[r], v[r], s_r, AT_D, heads, 2))
       return MK_ERR_CUDA;
     if (need_recv) {
       p.krecv[r] = static_cast<uint8_t*>(k_recv[r]);
       p.vrecv[r] = static_cast<uint8_t*>(v_recv[r]);
-      const uint64_t rrows = rows * (R - 1);
-      if (!make_map_a(&p.tmKr[r], k_recv[r], AT_D, rrows, AT_D * 2) ||
-          !make_map_b_chunks(&p.tmVr[r], v_recv[r], rrows, AT_D, 2))
+      const uint64_t blocks = static_cast<uint64_t>(heads) * (R - 1);
+      if (!make_map_3d(&p.tmKr[r], k_recv[r], AT_D, s_r, blocks, AT_D * 2, static_cast<uint64_t>(s_r) * AT_D * 2, 64,
+                       AT_T, 1) ||
+          !make_map_w_chunks(&p.tmVr[r], v_recv[r], s_r, AT_D, blocks, 2))
         return MK_ERR_CUDA;
     }
   }

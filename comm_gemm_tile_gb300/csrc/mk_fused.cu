@@ -383,6 +383,7 @@ struct ComputeSmem {
   uint32_t bars;  // smem address of the barrier block
   uint32_t cq;    // smem address of the MoE combine queue block
   uint32_t* cq_ctl;   // the same block, generic pointer (control words)
+  uint32_t epi;   // smem address of the epilogue staging (EPI_WARP_BYTES per epilogue warp)
   __device__ __forceinline__ uint32_t full(int s) const { return bars + BAR_FULL + 8u * s; }
   __device__ __forceinline__ uint32_t empty(int s) const { return bars + BAR_EMPTY + 8u * s; }
   __device__ __forceinline__ uint32_t tfull(int b) const { return bars + BAR_TFULL + 8u * b; }
@@ -769,6 +770,173 @@ __device__ void reduce_quarter(const FusedParams& p, const Item& it, const float
   }
 }
 
+// Final stores through the warp's staging: this lane's row piece (32 columns:
+// 128 bytes of fp32 or 64 bytes of bf16, at byte `off` of the staged 128-byte
+// row segment) goes to shared memory; flush_staged then writes the warp's 32
+// rows x 128 bytes with lane l taking 16 bytes of row 4k + l/8, so each store
+// instruction covers four whole 128-byte row segments (a lane per row would
+// make 32 separate 16-byte writes of one instruction).
+__device__ __forceinline__ void stage_piece(uint32_t stage, int lane, int off, const uint32_t (&r)[32], bool f32) {
+  const uint32_t a = stage + static_cast<uint32_t>(lane * EPI_ROW_STRIDE + off);
+  if (f32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16u * q), "r"(r[4 * q]), "r"(r[4 * q + 1]),
+                   "r"(r[4 * q + 2]), "r"(r[4 * q + 3]) : "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16u * q),
+                   "r"(pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]))),
+                   "r"(pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]))),
+                   "r"(pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]))),
+                   "r"(pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])))
+                   : "memory");
+  }
+}
+// The staged segment (columns col0 .. col0 + 128/esz - 1 of the warp's 32 rows,
+// tile rows 32 quarter + 0 .. 31) to the output: every replica (AR) or the
+// owner's row block (RS, the chained MLP).  Rows outside [row_lo, row_hi) and
+// columns at or past N are skipped.
+__device__ __forceinline__ void flush_staged(const FusedParams& p, const Item& it, uint32_t stage, int lane,
+                                             int quarter, int col0) {
+  const int esz = p.out_f32 ? 4 : 2;
+  const int pc = col0 + (lane & 7) * (16 / esz);   // first column of this lane's 16-byte piece
+  const bool col_ok = pc + 16 / esz <= p.N;
+#pragma unroll 1
+  for (int k = 0; k < 8; ++k) {
+    const int row = 4 * k + (lane >> 3);
+    const int trow = quarter * 32 + row;
+    uint32_t v0, v1, v2, v3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                 : "r"(stage + static_cast<uint32_t>(row * EPI_ROW_STRIDE + (lane & 7) * 16))
+                 : "memory");
+    if (!col_ok || trow < it.row_lo || trow >= it.row_hi) continue;
+    const int grow = it.out_row0 + trow;
+    if (p.op == OP_AR) {
+      for (int o = 0; o < p.R; ++o)
+        st_global_v4(reinterpret_cast<uint8_t*>(p.out[o]) + (static_cast<size_t>(grow) * p.N + pc) * esz, v0, v1,
+                     v2, v3);
+    } else {
+      const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
+      st_global_v4(reinterpret_cast<uint8_t*>(p.out[o]) + (static_cast<size_t>(lr) * p.N + pc) * esz, v0, v1, v2,
+                   v3);
+    }
+  }
+}
+
+// Sliced reduction (reduce = 4), after the warp's own tiles: job j = (tile,
+// 32-row quarter, 64-column group), taken by epilogue warps j, j + n_warps, ...
+// Once the quarter's arrival count shows all P partials staged, the warp sums
+// its slice of them in rank order 0..P-1 (the running sum's order, so the
+// result is the same bits) and writes it through its staging to every replica
+// (AR) or the owner's block (RS).  The waits come after all of this CTA's own
+// tiles, which wait for nothing, so every count is reached.
+__device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_t epi, int gw, int n_warps,
+                                bool& counters_ready) {
+  const int lane = threadIdx.x & 31;
+  constexpr int GROUPS = BN / 64;
+  const int n_jobs = p.n_tiles * 4 * GROUPS;
+  for (int j = gw; j < n_jobs; j += n_warps) {
+    const int tile = j / (4 * GROUPS), q = (j / GROUPS) % 4, g = j % GROUPS;
+    const int mb = tile / p.n_nblk, nb = tile - mb * p.n_nblk;
+    const int rows = min(BM, p.M - mb * BM);
+    if (32 * q >= rows) continue;                   // no row of this quarter is an output row
+    int ok = 1;
+    if (lane == 0) {
+      if (!counters_ready) {
+        if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_REDUCE, j)) ok = 0;
+        counters_ready = true;
+      }
+      const uint32_t* cnt = p.flags + static_cast<size_t>(tile) * 4 + q;
+      if (ok && ld_acquire_gpu(cnt) != static_cast<uint32_t>(p.P)) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t it = 0;
+        while (ld_acquire_gpu(cnt) != static_cast<uint32_t>(p.P)) {
+          if ((++it & 7u) == 0) {
+            if (aborted(p)) {
+              ok = 0;
+              break;
+            }
+            if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+              raise_error(p, MK_ERR_TIMEOUT, WHERE_REDUCE, j);
+              ok = 0;
+              break;
+            }
+          }
+          __nanosleep(64);
+        }
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    const int trow = 32 * q + lane;
+    const float* base = p.staging + static_cast<size_t>(tile) * p.P * TILE_F32;
+    Item it = proto;
+    it.row_lo = 0;
+    it.row_hi = rows;
+    it.out_row0 = mb * BM;
+    const int per = p.out_f32 ? 1 : 2;   // 32-column chunks per 128-byte staged segment
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * g + cc;
+      float4 acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        acc[u] = ld_global_cg_f4(base + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+      // two partials' loads in flight at a time, added in rank order
+      int part = 1;
+#pragma unroll 1
+      for (; part + 1 < p.P; part += 2) {
+        const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
+        const float* s1 = s0 + TILE_F32;
+        float4 v0[8], v1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          v0[u] = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+          v1[u] = ld_global_cg_f4(s1 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[u].x += v0[u].x;
+          acc[u].y += v0[u].y;
+          acc[u].z += v0[u].z;
+          acc[u].w += v0[u].w;
+          acc[u].x += v1[u].x;
+          acc[u].y += v1[u].y;
+          acc[u].z += v1[u].z;
+          acc[u].w += v1[u].w;
+        }
+      }
+      if (part < p.P) {
+        const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 v = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+          acc[u].x += v.x;
+          acc[u].y += v.y;
+          acc[u].z += v.z;
+          acc[u].w += v.w;
+        }
+      }
+      uint32_t r[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        r[4 * u + 0] = __float_as_uint(acc[u].x);
+        r[4 * u + 1] = __float_as_uint(acc[u].y);
+        r[4 * u + 2] = __float_as_uint(acc[u].z);
+        r[4 * u + 3] = __float_as_uint(acc[u].w);
+      }
+      stage_piece(epi, lane, (c % per) * 64, r, p.out_f32);
+      if (c % per == per - 1) {
+        __syncwarp();
+        flush_staged(p, it, epi, lane, q, nb * BN + 32 * (c - per + 1));
+        __syncwarp();
+      }
+    }
+  }
+}
+
 // An epilogue warp is done reading TMEM buffer `buf`: arrive on the barrier
 // that lets the MMA issuer overwrite it (the leader's, with pairs: it counts
 // the four epilogue warps of both CTAs).
@@ -1021,6 +1189,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
   const int trow = quarter * 32 + lane;
   const size_t esz = p.out_f32 ? 4 : 2;
+  const uint32_t epi = S.epi + static_cast<uint32_t>((warp - 2) * EPI_WARP_BYTES);   // this warp's staging
   int buf = 0;
   uint32_t acc_phase = 0;
   uint32_t pd_par = 0;           // phase bit of pdone(b) in bit b
@@ -1129,20 +1298,14 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
             st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
           }
         } else {
-          const int col = n0 + 32 * c;
-          const int nvalid = max(0, min(32, p.N - col));
-          if (row_ok && nvalid > 0) {
-            if (p.op != OP_AR) {   // RS and the chained MLP: the owner's row block
-              const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
-              uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
-              store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
-            } else {
-              for (int o = 0; o < p.R; ++o) {
-                uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
-                store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid,
-                                p.out_f32);
-              }
-            }
+          // the final sum: through the warp's staging, as whole 128-byte row
+          // segments (two 32-column chunks of bf16, one of fp32)
+          const int per = p.out_f32 ? 1 : 2;
+          stage_piece(epi, lane, (c % per) * 64, r, p.out_f32);
+          if (c % per == per - 1) {
+            __syncwarp();
+            flush_staged(p, it, epi, lane, quarter, n0 + 32 * (c - per + 1));
+            __syncwarp();
           }
         }
       }
@@ -1229,7 +1392,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last < 0) return;
-      if (last) {
+      if (last && !p.sliced) {
         __threadfence();   // the other partials' stores happened before their counts
         reduce_quarter(p, it, p.staging + static_cast<size_t>(tile) * p.P * TILE_F32, p.P, trow, row_ok, grow);
       }
@@ -1335,6 +1498,12 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       buf = 0;
       acc_phase ^= 1u;
     }
+  }
+  if (p.sliced) {
+    const int cta = PAIR ? 2 * cid + static_cast<int>(rank) : cid;
+    const int n_ctas = (PAIR ? 2 : 1) * p.n_compute;
+    Item proto{};
+    finalize_slices(p, proto, epi, cta * 4 + (warp - 2), n_ctas * 4, counters_ready);
   }
 }
 
@@ -1568,6 +1737,7 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
   S.bars = smem_u32(smem + RING_BYTES);
   S.cq = smem_u32(smem + RING_BYTES + BAR_BYTES);
   S.cq_ctl = reinterpret_cast<uint32_t*>(smem + RING_BYTES + BAR_BYTES);
+  S.epi = smem_u32(smem + RING_BYTES + BAR_BYTES + CQ_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RING_BYTES + TMEM_SLOT);
   if (p.op == OP_MOE_COMBINE) {
     // queue: control words zero, entry i free for slot i (sequence word 2i)

@@ -45,7 +45,15 @@ constexpr int BAR_BYTES = 256;
 // (16-byte entries after a 64-byte control block), placed after the barriers.
 constexpr int CQ_CAP = 512;
 constexpr int CQ_BYTES = 64 + 16 * CQ_CAP;
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + CQ_BYTES;
+// Epilogue staging (after the combine ring): per epilogue warp 32 rows of 128
+// bytes (rows 144 bytes apart, so that neither the row-wise writes nor the
+// piece-wise reads of a quarter warp meet in a bank), used to turn the final
+// output stores of the running-sum reduction into full 128-byte row segments.
+constexpr int EPI_ROW_STRIDE = 144;
+constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_STRIDE;
+constexpr int EPI_STAGE_BYTES = 4 * EPI_WARP_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + CQ_BYTES + EPI_STAGE_BYTES;
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per block");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int TILE_F32 = BM * BN;              // floats in one partial tile
 constexpr int MAX_PARTIALS = 16;               // staged partial tiles reduced per output tile
@@ -106,6 +114,9 @@ struct FusedParams {
                        //        forwarded tile by tile); 0 = staged partials + reduce-role CTAs
   int last_arrival;    // RS/AR: 1 = staged partials, the epilogue warp that completes a tile
                        //        quarter (32 rows) sums its partials (with chain = 0)
+  int sliced;          // RS/AR with last_arrival: nobody sums on arrival; once its own tiles
+                       //        are done, every epilogue warp sums 32-row x 64-column slices of
+                       //        tiles whose partials have all arrived
   int atomic;          // RS/AR: 1 = every partial added into one fp32 tile per output tile with
                        //        red.global.add; the warp that completes a quarter converts it
   int wire_bf16;       // RS/AR running sum: 1 = the sum forwarded between parts is bf16

@@ -9,7 +9,7 @@ records give when the AllGather copy-in started and ended and its rate.
 
 Run as a module on one GPU to trace a bench workload:
 
-    python -m comm_gemm_tile_gb300.trace ag|rs|ar|moe [--mode fused|gemm] [--calls N]
+    python -m comm_gemm_tile_gb300.trace ag|rs|ar|moe [--mode fused|gemm] [--calls N] [--pair auto|off|on]
 
 It makes the workload's inputs (seeded normal bf16, drawn on the device), runs N
 untraced calls back to back to reach a steady clock and power state, then one
@@ -151,7 +151,7 @@ def _trace_moe(mode: str, calls: int, dev) -> str:
     return format_summary(summarize(rec), f"{w.name}, {mode}, after {calls} untraced calls")
 
 
-def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0") -> str:
+def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0", pair: int = 0) -> str:
     from comm_gemm_tile_gb300 import build
     from comm_gemm_tile_gb300 import inputs as I
     build.build()
@@ -189,9 +189,9 @@ def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0
     if op == "ag" and m_mode == mk.MODE_GEMM_ONLY:
         for i in range(nsets):           # GEMM-only reads the gathered A as it stands
             call(i, mk.Config())
-    cfg = mk.Config(mode=m_mode, trace=1)
+    cfg = mk.Config(mode=m_mode, trace=1, cta_pair=pair)
     for i in range(calls):
-        call(i, mk.Config(mode=m_mode))
+        call(i, mk.Config(mode=m_mode, cta_pair=pair))
     call(calls, cfg)
     st, detail = mk.device_status(ws)
     if st != mk.MK_OK:
@@ -206,8 +206,11 @@ def main():
     ap.add_argument("op", choices=["ag", "rs", "ar", "moe"])
     ap.add_argument("--mode", choices=["fused", "gemm"], default="fused")
     ap.add_argument("--calls", type=int, default=30)
+    ap.add_argument("--pair", choices=["auto", "off", "on"], default="auto",
+                    help="CTA pairs for AG / RS / AR (mk_config.cta_pair)")
     args = ap.parse_args()
-    print(trace_workload(args.op, args.mode, args.calls))
+    pair = {"auto": mk.PAIR_AUTO, "off": mk.PAIR_OFF, "on": mk.PAIR_ON}[args.pair]
+    print(trace_workload(args.op, args.mode, args.calls, pair=pair))
 
 
 if __name__ == "__main__":

@@ -99,17 +99,26 @@ typedef struct {
   long long wait_limit_ns;  /* bound on every device-side wait (default 2e9 ns)        */
   int inject;               /* test only: 1 = one copy-in chunk never signals ready;
                                2 = one partial tile never signals ready                */
-  int reduce;               /* RS / AR with n_reduce_ctas == 0: 0 = default (running sum),
+  int reduce;               /* RS / AR with n_reduce_ctas == 0: 0 = default: 4 for an AR
+                                   with at most 2048 partial tiles (output tiles x R, i.e.
+                                   256 MiB of staging) when wire == 0 and split_k <= 1,
+                                   else 1,
                                1 = running sum forwarded in rank order by the epilogues,
                                2 = last arrival: every partial staged, the epilogue that
                                    completes a tile sums all of them in rank order,
+                               4 = sliced: every partial staged without waiting; once
+                                   their own tiles are done, all epilogues sum 32-row x
+                                   64-column slices of the tiles whose partials have all
+                                   arrived, in rank order (the same bits as 1 and 2),
                                3 = atomic: every partial added into one fp32 tile per
                                    output tile (red.global.add), the epilogue that
                                    completes a tile converts it.  The fp32 summation
                                    order is not fixed: results agree with the other
                                    modes within rounding (exactly when every partial
                                    sum is exact in fp32).                              */
-  int cta_pair;             /* GEMM tiles: 0 = default, 1 = one CTA per 128 x 256 tile,
+  int cta_pair;             /* GEMM tiles: 0 = default (pairs, except for an AR within the
+                                   reduce = 4 size limit: one CTA per tile, in every mode),
+                               1 = one CTA per 128 x 256 tile,
                                2 = CTA pairs (clusters of two SMs sharing a 256 x 256 tile
                                    through tcgen05 cta_group::2).  Pairs serve every launch
                                    without copy-role or reduce-role CTAs (MoE: 256-row

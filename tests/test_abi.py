@@ -61,8 +61,22 @@ def test_workspace_sizes(L):
     assert 2048 * 128 * 256 * 4 <= sz < 2048 * 128 * 256 * 4 + (1 << 20)
     # bf16 wire: the same staging (half of each tile used)
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(wire=mk.WIRE_BF16)) > 0
+    # sliced reduction: every partial staged (8 fp32 partial tiles per output tile)
+    sz = mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=mk.REDUCE_SLICED))
+    assert 2048 * 8 * 128 * 256 * 4 <= sz < 2048 * 8 * 128 * 256 * 4 + (1 << 20)
+    # AR defaults: the decode shape (32 output tiles x 8 partials <= 2048) reduces by
+    # slices (all partials staged); a large AR keeps one running-sum tile per output tile
+    sz = mk.workspace_size(mk.OP_GEMM_AR, 8, 128, 8192, 3584)
+    assert 32 * 8 * 128 * 256 * 4 <= sz < 32 * 8 * 128 * 256 * 4 + (1 << 20)
+    assert sz == mk.workspace_size(mk.OP_GEMM_AR, 8, 128, 8192, 3584, mk.Config(reduce=mk.REDUCE_SLICED))
+    sz = mk.workspace_size(mk.OP_GEMM_AR, 8, 8192, 8192, 3584)
+    assert 2048 * 128 * 256 * 4 <= sz < 2048 * 128 * 256 * 4 + (1 << 20)
+    # the running sum chosen explicitly, or with the bf16 wire: one tile per output tile
+    for cfg in (mk.Config(reduce=mk.REDUCE_RUNNING_SUM), mk.Config(wire=mk.WIRE_BF16)):
+        sz = mk.workspace_size(mk.OP_GEMM_AR, 8, 128, 8192, 3584, cfg)
+        assert 32 * 128 * 256 * 4 <= sz < 32 * 128 * 256 * 4 + (1 << 20)
     # out-of-range reduce / wire -> 0
-    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=4)) == 0
+    assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(reduce=5)) == 0
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(wire=2)) == 0
     # fp8 operands: k must be a multiple of 16 (rows of whole 16-byte units)
     assert mk.workspace_size(mk.OP_AG_GEMM, 8, 1024, 3584, 8192, mk.Config(operand=mk.OPERAND_FP8)) > 0

@@ -7,7 +7,8 @@ each output row is the mean of the visible values; with integer values and a
 power-of-two key count that mean is exact in fp32 and must match bit for bit.
 The receive buffers must hold bit copies of the ring's blocks.  Shapes cover
 ragged blocks (positions not a multiple of 128), one rank, several heads,
-causal and full attention, all three modes and a missing ring piece.
+causal and full attention, all three modes, a missing ring piece and receive
+buffers that start as NaN (rows past a ragged block must read as zeros).
 """
 import numpy as np
 import pytest
@@ -157,3 +158,23 @@ def test_ring_attention_large_scores(causal):
     vmax = max(float(t.float().abs().max()) for t in v)
     for r in range(w.R):
         assert _err(gpu_values(out[r]), exact[r].astype(np.float64), vmax) <= ATT_TOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mode", [mk.MODE_FUSED, mk.MODE_UNFUSED])
+def test_ring_attention_stale_receive_rows_do_not_leak(mode, causal):
+    # Ragged blocks (200 positions: the second key tile has 72 keys).  The
+    # receive buffers start as NaN, so rows a tile would read past its block
+    # (the next block, which may not have arrived) poison P V unless they read
+    # as zeros; the result must be the GEMM-only mode's bits, which reads the
+    # source blocks directly.
+    wa = I.AttnWorkload("t", R=4, heads=2, s_r=200, causal=causal, q_seed=511, k_seed=512, v_seed=513)
+    q, k, v = (dev(t) for t in I.attn_inputs(wa))
+    want = mk.ring_attention(q, k, v, causal=causal, cfg=mk.Config(mode=mk.MODE_GEMM_ONLY))
+    nan = lambda: [torch.full((3 * 2, 200, 128), float("nan"), dtype=torch.bfloat16, device="cuda")  # noqa: E731
+                   for _ in range(4)]
+    got = mk.ring_attention(q, k, v, causal=causal, k_recv=nan(), v_recv=nan(), cfg=mk.Config(mode=mode))
+    _ok()
+    for g, w in zip(got, want):
+        assert not torch.isnan(g).any()
+        assert torch.equal(g, w)

@@ -137,3 +137,41 @@ def test_few_ctas_atomic_and_wire():
         _ok()
         want = O.running_sum_bf16_wire(O.rank_partials([I.bits(x) for x in a], [I.bits(x) for x in b]), "bf16")
         np.testing.assert_array_equal(gpu_bits(got), want)
+
+
+# Sliced reduction (reduce = 4): every partial staged, then slices summed in
+# rank order by all epilogue warps.  The order is the running sum's, so on any
+# inputs the result must be the same bits as reduce = 1 (fp32 addition of the
+# same values in the same order); with integer inputs it equals the oracle.
+@pytest.mark.parametrize("pair", PAIRS)
+@pytest.mark.parametrize("op,R,m,n,k", SHAPES)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_sliced_same_bits_as_running_sum(op, R, m, n, k, pair, out):
+    a, b = _inputs(op, R, m, n, k, False, 171)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    chain = _run(op, a, b, mk.Config(cta_pair=pair, reduce=mk.REDUCE_RUNNING_SUM), dt)
+    sliced = _run(op, a, b, mk.Config(cta_pair=pair, reduce=mk.REDUCE_SLICED), dt)
+    _ok()
+    assert torch.equal(chain, sliced)
+
+
+@pytest.mark.parametrize("op,R,m,n,k", SHAPES)
+def test_sliced_integer_bit_exact_few_ctas(op, R, m, n, k):
+    # three CTAs: every epilogue warp takes several slices after its tiles
+    a, b = _inputs(op, R, m, n, k, True, 181)
+    exact = O.sum_over_ranks([I.bits(x) for x in a], [I.bits(x) for x in b])
+    got = _run(op, a, b, mk.Config(reduce=mk.REDUCE_SLICED, cta_pair=mk.PAIR_OFF, max_ctas=3))
+    _ok()
+    np.testing.assert_array_equal(gpu_bits(got), oracle_bits(exact, "bf16"))
+
+
+def test_sliced_is_the_small_allreduce_default_and_repeats():
+    # the decode-like AR (few output tiles) takes the sliced reduction by default;
+    # repeated calls on one workspace (counters zeroed by each call) agree
+    a, b = _inputs("ar", 8, 128, 1024, 512, False, 191)
+    ws = mk.Workspace()
+    base = _run("ar", a, b, mk.Config(reduce=mk.REDUCE_RUNNING_SUM), ws=ws)
+    for _ in range(3):
+        got = _run("ar", a, b, mk.Config(), ws=ws)
+        _ok(ws)
+        assert torch.equal(got, base)
