@@ -106,16 +106,16 @@ typedef struct {
                                1 = running sum forwarded in rank order by the epilogues,
                                2 = last arrival: every partial staged, the epilogue that
                                    completes a tile sums all of them in rank order,
-                               4 = sliced: every partial staged without waiting; once
-                                   their own tiles are done, all epilogues sum 32-row x
-                                   64-column slices of the tiles whose partials have all
-                                   arrived, in rank order (the same bits as 1 and 2),
                                3 = atomic: every partial added into one fp32 tile per
                                    output tile (red.global.add), the epilogue that
                                    completes a tile converts it.  The fp32 summation
                                    order is not fixed: results agree with the other
                                    modes within rounding (exactly when every partial
-                                   sum is exact in fp32).                              */
+                                   sum is exact in fp32),
+                               4 = sliced: every partial staged without waiting; once
+                                   their own tiles are done, all epilogues sum 32-row x
+                                   64-column slices of the tiles whose partials have all
+                                   arrived, in rank order (the same bits as 1 and 2).  */
   int cta_pair;             /* GEMM tiles: 0 = default (pairs, except for an AR within the
                                    reduce = 4 size limit: one CTA per tile, in every mode),
                                1 = one CTA per 128 x 256 tile,
