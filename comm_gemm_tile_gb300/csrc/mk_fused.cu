@@ -86,6 +86,36 @@ __device__ __forceinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uin
   return wait_bar_loop(p, bar, parity, where, item, honor_abort);
 }
 
+// The same wait by a whole warp that stays converged (the MMA warp): every
+// lane tests the barrier and the warp agrees by vote -- cheaper for the issuing
+// warp than one lane polling while the others wait -- and lane 0 reports a
+// timeout.  Called by all 32 lanes.
+__device__ __noinline__ bool wait_bar_warp_loop(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
+                                                int item, bool honor_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if ((++it & 31u) == 0) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (honor_abort && aborted(p)) {
+          stop = 1;
+        } else if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.wait_ns)) {
+          raise_error(p, MK_ERR_TIMEOUT, where, item);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0) != 0) return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bar_warp(const FusedParams& p, uint32_t bar, uint32_t parity, int where,
+                                              int item, bool honor_abort = true) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return wait_bar_warp_loop(p, bar, parity, where, item, honor_abort);
+}
+
 // Bounded wait until *f == epoch (acquire, gpu scope).  Single thread.  The
 // first load is inline (wait_flag below).
 __device__ __noinline__ bool wait_flag_loop(const FusedParams& p, const uint32_t* f, int where, int item) {
@@ -617,7 +647,7 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it);
-    if (!wait_bar(p, S.tempty(buf), acc_phase ^ 1u, WHERE_MMA, i)) goto done;
+    if (!wait_bar_warp(p, S.tempty(buf), acc_phase ^ 1u, WHERE_MMA, i)) goto done;
     tc_fence_after();
     {
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
@@ -625,40 +655,43 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
       for (int seg = 0; seg < it.nseg; ++seg) {
         for (int kb0 = 0; kb0 < it.nkb; kb0 += Ring<PAIR>::kps) {
           const int nk = min(Ring<PAIR>::kps, it.nkb - kb0);   // k-blocks in this stage
-          if (!wait_bar(p, S.full(stage), phase, WHERE_MMA, i)) goto done;
+          if (!wait_bar_warp(p, S.full(stage), phase, WHERE_MMA, i)) goto done;
           tc_fence_after();
-          for (int h = 0; h < nk; ++h) {
-            const uint32_t a_addr =
-                S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * Ring<PAIR>::kb_bytes;
-            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
-            if constexpr (F8) {
-              // fp8: four K = 32 steps of 32 bytes; A and B^T both K-major, 128-byte
-              // swizzle, 8-row groups 1024 B apart
+          if (elect_one_sync()) {
+            for (int h = 0; h < nk; ++h) {
+              const uint32_t a_addr =
+                  S.ring + static_cast<uint32_t>(stage) * SB + static_cast<uint32_t>(h) * Ring<PAIR>::kb_bytes;
+              const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+              if constexpr (F8) {
+                // fp8: four K = 32 steps of 32 bytes; A and B^T both K-major, 128-byte
+                // swizzle, 8-row groups 1024 B apart
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 1024u, 2u);
-                const uint64_t bd = sdesc_swz(b_addr + 32u * k, 16u, 1024u, 2u);
-                if constexpr (PAIR) tc_mma_f8_pair(d_tmem, ad, bd, IDESC_F8_PAIR, acc);
-                else tc_mma_f8(d_tmem, ad, bd, IDESC_F8, acc);
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 1024u, 2u);
+                  const uint64_t bd = sdesc_swz(b_addr + 32u * k, 16u, 1024u, 2u);
+                  if constexpr (PAIR) tc_mma_f8_pair(d_tmem, ad, bd, IDESC_F8_PAIR, acc);
+                  else tc_mma_f8(d_tmem, ad, bd, IDESC_F8, acc);
+                  acc = 1;
+                }
+                continue;
+              }
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
+                const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 8u * A_SWIZZLE_BYTES,
+                                              A_SWIZZLE_BYTES == 128 ? 2u : 4u);
+                // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
+                // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
+                const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
+                if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, acc);
+                else tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
                 acc = 1;
               }
-              continue;
             }
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              // A: K-major, BK*2-byte swizzle, 8-row atoms 8*BK*2 B apart; +32 B per 16-wide K step.
-              const uint64_t ad = sdesc_swz(a_addr + 32u * k, 16u, 8u * A_SWIZZLE_BYTES,
-                                            A_SWIZZLE_BYTES == 128 ? 2u : 4u);
-              // B: MN-major, 128-B swizzle; 64-column atoms 8 KiB apart (LBO),
-              // 8-row K groups 1024 B apart (SBO); +2048 B per 16-row K step.
-              const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, static_cast<uint32_t>(B_BOX_BYTES), 1024u);
-              if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, acc);
-              else tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
-              acc = 1;
-            }
+            if constexpr (PAIR) tc_commit_pair(S.empty(stage), 3);
+            else tc_commit(S.empty(stage));
           }
-          if constexpr (PAIR) tc_commit_pair(S.empty(stage), 3);
-          else tc_commit(S.empty(stage));
+          __syncwarp();
           if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
@@ -666,8 +699,11 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
         }
       }
     }
-    if constexpr (PAIR) tc_commit_pair(S.tfull(buf), 3);
-    else tc_commit(S.tfull(buf));
+    if (elect_one_sync()) {
+      if constexpr (PAIR) tc_commit_pair(S.tfull(buf), 3);
+      else tc_commit(S.tfull(buf));
+    }
+    __syncwarp();
     if (++buf == 2) {
       buf = 0;
       acc_phase ^= 1u;
@@ -675,9 +711,12 @@ __device__ void mma_issuer(const FusedParams& p, const ComputeSmem& S, uint32_t 
   }
 done:
   // Every MMA issued must have completed before tensor memory is freed.
-  if constexpr (PAIR) tc_commit_pair(S.drain(), 1);
-  else tc_commit(S.drain());
-  wait_bar(p, S.drain(), 0, WHERE_DRAIN, 0, /*honor_abort=*/false);
+  if (elect_one_sync()) {
+    if constexpr (PAIR) tc_commit_pair(S.drain(), 1);
+    else tc_commit(S.drain());
+  }
+  __syncwarp();
+  wait_bar_warp(p, S.drain(), 0, WHERE_DRAIN, 0, /*honor_abort=*/false);
 }
 
 __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&r)[32], int ncols_valid,
@@ -1783,8 +1822,9 @@ __device__ void compute_role(const FusedParams& p, uint8_t* smem, int cid) {
     if (lane == 0) producer<PAIR>(p, S, cid, rank);
     __syncwarp();
   } else if (warp == 1) {
-    // the operand type picks the MMA loop once (the issuing thread's loop stays branch-free)
-    if (lane == 0 && rank == 0) {
+    // the operand type picks the MMA loop once (the issuing warp's loop stays branch-free);
+    // the warp runs it converged and one elected lane issues
+    if (rank == 0) {
       if (p.fp8) mma_issuer<PAIR, true>(p, S, tmem_base, cid);
       else mma_issuer<PAIR, false>(p, S, tmem_base, cid);
     }
