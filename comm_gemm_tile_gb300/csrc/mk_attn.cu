@@ -24,8 +24,11 @@
 //     and the sum, so the result is unchanged); at the end of an item the
 //     warps scale O_0 and O_1 by 1 / sum and store them;
 //   * warp 10 (copy): the ring's transfers -- rank r receives the block
-//     of rank (r - j) mod R at step j -- as row copies into its receive
-//     buffer, one counter per (rank, step, head).
+//     of rank (r - j) mod R at step j -- moved by the bulk-copy engine
+//     through shared memory into its receive buffer, one counter per
+//     (rank, step, head).
+// Items run rank by rank, causal ones longest first, dealt to the CTAs in
+// alternating directions so that every CTA's share of tiles is about equal.
 // Causal attention skips the tiles after each query pair (and, in ring order,
 // every block of a later rank: those blocks are not moved either).
 #include <algorithm>
@@ -45,7 +48,7 @@ constexpr int AT_THREADS = 384;              // 12 warps: see the role list abov
 constexpr int AT_WARP_COPY = 10, AT_WARP_V = 11;
 constexpr int AT_MAX_R = 8;
 #ifndef MK_ATTN_KST
-#define MK_ATTN_KST 3
+#define MK_ATTN_KST 2
 #endif
 constexpr int AT_KST = MK_ATTN_KST;          // K stages
 constexpr int AT_VST = 2;                    // V stages
@@ -54,14 +57,16 @@ constexpr uint32_t AT_TILE = 32768;          // one 128 x 128 bf16 tile: 2 K-maj
 constexpr uint32_t AT_Q = 0;                 // Q0, Q1
 constexpr uint32_t AT_K = 2 * AT_TILE;       // K stages
 constexpr uint32_t AT_V = AT_K + AT_KST * AT_TILE;   // V stages
-constexpr uint32_t AT_BARS = AT_V + AT_VST * AT_TILE;
+constexpr uint32_t AT_CHUNK = 16384;         // the ring copy's staging: two buffers of this size
+constexpr uint32_t AT_CBUF = AT_V + AT_VST * AT_TILE;
+constexpr uint32_t AT_BARS = AT_CBUF + 2 * AT_CHUNK;
 constexpr int AT_SMEM = 1024 + AT_BARS + 256;
 static_assert(AT_SMEM <= 232448, "dynamic shared memory per block");
 // barriers (byte offsets in the barrier block)
 constexpr uint32_t B_QFULL = 0, B_QEMPTY = 8, B_KFULL = 16, B_KEMPTY = B_KFULL + 8 * AT_KST,
                    B_VFULL = B_KEMPTY + 8 * AT_KST, B_VEMPTY = B_VFULL + 8 * AT_VST,
                    B_SFULL = B_VEMPTY + 8 * AT_VST, B_GO = B_SFULL + 16, B_OFULL = B_GO + 16,
-                   B_DRAIN = B_OFULL + 16, B_TMEM = B_DRAIN + 8;
+                   B_DRAIN = B_OFULL + 16, B_CFULL = B_DRAIN + 8, B_TMEM = B_CFULL + 16;
 static_assert(B_TMEM + 4 <= 256, "barrier block");
 constexpr uint32_t AT_TMEM_COLS = 512;       // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t AT_O_COL = 256;           // O_i at AT_O_COL + 128 i; S_i (and P_i) at 128 i
@@ -204,16 +209,35 @@ __device__ __noinline__ bool at_wait_value(const AttnParams& p, const uint32_t* 
 struct AtItem {
   int r, h, qp, n;   // rank, head, query-tile pair (tiles 2qp, 2qp+1), K/V tiles to visit
 };
-// Items run longest first (causal: the last rank's queries see the most keys).
+// Items run rank by rank, the last rank first.  Causal items run longest first:
+// a rank's later query pairs see more of its own block, so inside a rank the
+// pairs go in descending order, the heads inside each pair (full attention:
+// every item has the same length; heads outer, pairs inner).
 __device__ __forceinline__ AtItem at_item(const AttnParams& p, int i) {
   AtItem it;
   const int per_r = p.heads * p.npair;
   it.r = p.R - 1 - i / per_r;
   const int rem = i - (p.R - 1 - it.r) * per_r;
-  it.h = rem / p.npair;
-  it.qp = rem - it.h * p.npair;
+  if (p.causal) {
+    const int k = rem / p.heads;
+    it.h = rem - k * p.heads;
+    it.qp = p.npair - 1 - k;
+  } else {
+    it.h = rem / p.npair;
+    it.qp = rem - it.h * p.npair;
+  }
   it.n = p.causal ? min(2 * it.qp + 2, p.nkt) + it.r * p.nkt : p.R * p.nkt;
   return it;
+}
+// The CTA's round-j item: rounds of gridDim.x items, dealt in CTA order in even
+// rounds and in reverse in odd ones, so that with items longest first every
+// CTA's total stays near the mean (causal, 8 ranks x 4096 positions: the
+// busiest CTA 2 % above it, against 17 % when every round is dealt in order).
+// n_items or more: no item for this CTA in round j.  Every role walks the
+// same sequence: for (j = 0; j * gridDim.x < n_items; ++j).
+__device__ __forceinline__ int at_deal(int j) {
+  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  return j * g + ((j & 1) ? g - 1 - b : b);
 }
 // Tile t of an item: ring step j (source rank s = r - j mod R) and key tile kt.
 // Causal: the rank's own block up to the pair's second query tile, then the
@@ -289,7 +313,9 @@ __device__ void at_producer_k(const AttnParams& p, uint32_t bars, uint32_t base)
   uint32_t q_ph = 0, e_ph = 0;
   int stage = 0;
   bool ready = false;
-  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+  for (int j = 0; j * static_cast<int>(gridDim.x) < p.n_items; ++j) {
+    const int i = at_deal(j);
+    if (i >= p.n_items) continue;
     const AtItem it = at_item(p, i);
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
@@ -326,7 +352,9 @@ __device__ void at_producer_v(const AttnParams& p, uint32_t bars, uint32_t base)
   uint32_t e_ph = 0;
   int stage = 0;
   bool ready = false;
-  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+  for (int j = 0; j * static_cast<int>(gridDim.x) < p.n_items; ++j) {
+    const int i = at_deal(j);
+    if (i >= p.n_items) continue;
     const AtItem it = at_item(p, i);
     int waited_j = 0;
     for (int t = 0; t < it.n; ++t) {
@@ -405,7 +433,9 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
   int kst = 0, vst = 0;
   bool prev_first = false, prev_last = false;   // the pending tile u-1 opens / closes its item
   int item = -1;
-  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+  for (int j = 0; j * static_cast<int>(gridDim.x) < p.n_items; ++j) {
+    const int i = at_deal(j);
+    if (i >= p.n_items) continue;
     const AtItem it = at_item(p, i);
     item = i;
     for (int t = 0; t < it.n; ++t, ++u) {
@@ -606,7 +636,9 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
   const uint32_t lane_off = static_cast<uint32_t>(lane16) << 16;
   const float c = p.scale_log2;
   uint32_t sf_ph = 0, of_ph = 0;                             // bit g: query tile g
-  for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+  for (int j = 0; j * static_cast<int>(gridDim.x) < p.n_items; ++j) {
+    const int i = at_deal(j);
+    if (i >= p.n_items) continue;
     const AtItem it = at_item(p, i);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     for (int t = 0; t < it.n; ++t) {
@@ -731,23 +763,47 @@ __device__ void at_softmax(const AttnParams& p, uint32_t bars, uint32_t tmem) {
 
 // The ring's transfers: piece = (rank r, step j >= 1, head h, key tile kt, K or V),
 // in the order the work list needs them (ranks as the items run, then step,
-// head, tile).  Copy warp w takes pieces w, w + n_workers, ...; each lane
-// streams 16-byte vectors, 16 loads in flight; after a piece every lane fences
-// and lane 0 counts it in its (rank, step, head) counter.
-__device__ void at_copy(const AttnParams& p) {
+// head, tile).  Copy warp w takes pieces w, w + n_workers, ...  Lane 0 moves
+// a piece with the bulk-copy engine in chunks of up to 16 KB through two
+// shared-memory buffers (global -> shared on a barrier, shared -> global as a
+// bulk group), the next chunk's load in flight while the current one is
+// stored; once a piece's stores have completed it counts the piece in its
+// (rank, step, head) counter.  (Row copies through registers cost the
+// softmax and MMA warps more: their load/store stream competes with the
+// barrier and tensor-memory traffic.)
+__device__ void at_copy(const AttnParams& p, uint32_t bars, uint32_t base) {
   const int lane = threadIdx.x & 31;
   const int cw = (threadIdx.x >> 5) - AT_WARP_COPY;
-  if (cw >= p.n_cw) return;
+  if (cw >= p.n_cw || lane != 0) return;
   const int worker = blockIdx.x * p.n_cw + cw;
   const int n_workers = gridDim.x * p.n_cw;
-  {
-    int ok = 1;
-    if (lane == 0) ok = at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, worker) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-  }
+  if (!at_wait_value(p, &p.hdr[HDR_READY], p.epoch, WHERE_COPY, worker)) return;
   const long long per_r = static_cast<long long>(p.heads) * (p.R - 1) * p.nkt * 2;
   const long long total = per_r * p.R;
   bool skip_first = (p.inject == 1 && worker == 0);
+  uint32_t n = 0;   // chunks whose load has been issued; chunk c uses buffer c & 1
+  // the newest chunk: loaded (or landing) but not yet stored
+  bool pend = false, pend_last = false;
+  uint8_t* pend_dst = nullptr;
+  uint32_t pend_bytes = 0;
+  uint32_t* pend_counter = nullptr;
+  // Store chunk n-1 once it has landed; after the last chunk of a piece, wait
+  // until the piece's stores have completed and count it.
+  auto store_pending = [&]() -> bool {
+    const uint32_t pb = (n - 1) & 1u;
+    if (!at_wait_bar(p, bars + B_CFULL + 8u * pb, ((n - 1) >> 1) & 1u, WHERE_COPY, worker)) return false;
+    bulk_s2g(pend_dst, base + AT_CBUF + pb * AT_CHUNK, pend_bytes);
+    bulk_commit();
+    pend = false;
+    if (pend_last) {
+      bulk_wait<0>();
+      fence_proxy_async_global();
+      __threadfence();
+      if (skip_first) skip_first = false;
+      else atomicAdd(pend_counter, 1u);
+    }
+    return true;
+  };
   for (long long q = worker; q < total; q += n_workers) {
     const int rr = static_cast<int>(q / per_r);
     long long rem = q - rr * per_r;
@@ -760,44 +816,38 @@ __device__ void at_copy(const AttnParams& p) {
     const int kt = static_cast<int>(rem / 2), isv = static_cast<int>(rem & 1);
     const int s = (r - j + p.R) % p.R;
     if (p.causal && s > r) continue;            // a later rank's keys: never read
-    int stop = 0;
-    if (lane == 0) stop = at_aborted(p) ? 1 : 0;
-    if (__shfl_sync(0xffffffffu, stop, 0)) return;
+    if (at_aborted(p)) break;
     const int rows = min(AT_T, p.s_r - kt * AT_T);
-    {
-      const int ok = at_bounds_ok(p, r >= 0 && r < p.R && j >= 1 && j < p.R && s >= 0 && s < p.R && h < p.heads &&
-                                         kt < p.nkt && rows > 0,
-                                  BC_ATTN_COPY, q) ? 1 : 0;
-      if (!__all_sync(0xffffffffu, ok)) return;
-    }
+    if (!at_bounds_ok(p, r >= 0 && r < p.R && j >= 1 && j < p.R && s >= 0 && s < p.R && h < p.heads && kt < p.nkt &&
+                             rows > 0,
+                      BC_ATTN_COPY, q))
+      break;
     const size_t src_off = (static_cast<size_t>(h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
     const size_t dst_off =
         ((static_cast<size_t>(j - 1) * p.heads + h) * p.s_r + static_cast<size_t>(kt) * AT_T) * AT_D * 2;
     const uint8_t* src = (isv ? p.vsrc[s] : p.ksrc[s]) + src_off;
     uint8_t* dst = (isv ? p.vrecv[r] : p.krecv[r]) + dst_off;
-    const size_t n16 = static_cast<size_t>(rows) * AT_D * 2 / 16;
-    constexpr int U = 16;
-    for (size_t i0 = lane; i0 < n16; i0 += 32 * U) {
-      uint4 v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t idx = i0 + static_cast<size_t>(u) * 32;
-        if (idx < n16) v[u] = ld_nc_v4(src + idx * 16);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t idx = i0 + static_cast<size_t>(u) * 32;
-        if (idx < n16) st_global_v4(dst + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
-      }
+    const uint32_t bytes = static_cast<uint32_t>(rows) * AT_D * 2;   // a multiple of 256
+    for (uint32_t off = 0; off < bytes; off += AT_CHUNK) {
+      if (pend && !store_pending()) goto out;
+      const uint32_t cb = min(AT_CHUNK, bytes - off);
+      const uint32_t b = n & 1u;
+      // buffer b was last read by the store of chunk n-2: only the newest
+      // store (chunk n-1) may still be reading shared memory
+      bulk_wait_read<1>();
+      mbar_arrive_expect_tx(bars + B_CFULL + 8u * b, cb);
+      bulk_g2s(base + AT_CBUF + b * AT_CHUNK, src + off, cb, bars + B_CFULL + 8u * b);
+      ++n;
+      pend = true;
+      pend_dst = dst + off;
+      pend_bytes = cb;
+      pend_last = (off + cb >= bytes);
+      pend_counter = at_counter(p, r, j, h);
     }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-      if (skip_first) skip_first = false;
-      else atomicAdd(at_counter(p, r, j, h), 1u);
-    }
-    __syncwarp();
   }
+  if (pend) store_pending();
+out:
+  bulk_wait<0>();   // no store may still read shared memory when the CTA exits
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __grid_constant__ AttnParams p) {
@@ -834,6 +884,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     mbar_init(bars + B_GO, 8);          // the softmax warps, for Q0
     mbar_init(bars + B_GO + 8u, 8);     // and for Q1
     mbar_init(bars + B_DRAIN, 1);       // MMA drain
+    mbar_init(bars + B_CFULL, 1);       // the ring copy's two staging buffers
+    mbar_init(bars + B_CFULL + 8u, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -857,7 +909,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) mk_ring_attn_kernel(const __gri
     at_softmax(p, bars, tmem);
     __syncwarp();
   } else if (warp == AT_WARP_COPY && p.copy) {
-    at_copy(p);
+    at_copy(p, bars, base);
     __syncwarp();
   }
   tc_fence_before();
