@@ -132,7 +132,11 @@ __device__ __forceinline__ bool at_bounds_ok(const AttnParams& p, bool cond, int
   return true;
 }
 // The bounded wait loop.  SPIN: poll with the non-blocking test (the MMA
-// issuer and the softmax warps, whose waits sit on the critical path).
+// warp's waits for K and V, which have almost always landed); otherwise
+// try_wait, which suspends the warp until the phase completes or a time limit
+// passes and leaves its issue slots to the other warps (the MMA warp's wait for
+// the softmax: spinning there slowed the two softmax warps that share its SM
+// sub-partition, and the slowest softmax warp sets the pace).
 template <bool SPIN>
 __device__ __noinline__ bool at_wait_loop(const AttnParams& p, uint32_t bar, uint32_t parity, int where, int item,
                                           bool honor_abort) {
@@ -449,7 +453,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       if (u >= 1) {
         // V(u-1) landed and P_0(u-1) written
         if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, i)) goto done;
-        if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp<false>(p, bars + B_GO, go_ph, WHERE_MMA, i)) goto done;
         tc_fence_after();
         at_pv(base, tmem, 0, vst, prev_first);
         if (prev_last) at_commit(bars + B_OFULL);
@@ -458,7 +462,7 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
       at_s(base, tmem, 0, kst);
       at_commit(bars + B_SFULL);
       if (u >= 1) {
-        if (!at_wait_warp<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
+        if (!at_wait_warp<false>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, i)) goto done;
         go_ph ^= 1u;
         tc_fence_after();
         at_pv(base, tmem, 1, vst, prev_first);
@@ -483,11 +487,11 @@ __device__ void at_mma(const AttnParams& p, uint32_t bars, uint32_t base, uint32
   }
   if (u >= 1) {   // the products of the last tile
     if (!at_wait_warp<true>(p, bars + B_VFULL + 8u * vst, v_ph, WHERE_MMA, item)) goto done;
-    if (!at_wait_warp<true>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_warp<false>(p, bars + B_GO, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 0, vst, prev_first);
     at_commit(bars + B_OFULL);
-    if (!at_wait_warp<true>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
+    if (!at_wait_warp<false>(p, bars + B_GO + 8u, go_ph, WHERE_MMA, item)) goto done;
     tc_fence_after();
     at_pv(base, tmem, 1, vst, prev_first);
     at_commit(bars + B_VEMPTY + 8u * vst);
