@@ -21,7 +21,7 @@ def L():
 def valid(op, R, m, n, k, c):
     if not (1 <= R <= mk.MAX_RANKS) or min(m, n, k) < 0 or n % 8 or k % 8:
         return False
-    if not (0 <= c.mode <= 2) or not (0 <= c.reduce <= 3) or not (0 <= c.wire <= 1):
+    if not (0 <= c.mode <= 2) or not (0 <= c.reduce <= 4) or not (0 <= c.wire <= 1):
         return False
     if not (0 <= c.operand <= 1) or c.trace not in (0, 1):
         return False
@@ -41,7 +41,7 @@ dims = st.one_of(st.integers(0, 4096), st.sampled_from([8, 16, 128, 136, 1 << 31
 @hyp.settings(max_examples=400, deadline=None)
 @hyp.given(op=st.sampled_from([mk.OP_AG_GEMM, mk.OP_GEMM_RS, mk.OP_GEMM_AR]),
            R=st.integers(-1, 18), m=dims, n=dims, k=dims,
-           mode=st.integers(-1, 3), reduce=st.integers(-1, 4), wire=st.integers(-1, 2),
+           mode=st.integers(-1, 3), reduce=st.integers(-1, 5), wire=st.integers(-1, 2),
            operand=st.integers(-1, 2), trace=st.integers(-1, 2), split_k=st.integers(0, 9),
            n_reduce=st.sampled_from([0, 0, 4]))
 def test_workspace_size_matches_validity(L, op, R, m, n, k, mode, reduce, wire, operand, trace,
