@@ -2217,6 +2217,9 @@ __device__ void reduce_role(const FusedParams& p, uint8_t* smem, int rid) {
 // all tcgen05 work of the launch uses cta_group::2.
 template <bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_constant__ FusedParams p) {
+  // With p.pdl the launch overlaps the previous kernel's end (the MoE
+  // bookkeeping); nothing here runs before that kernel's results are visible.
+  griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -2273,23 +2276,29 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  if (!p.pair) {
-    mk_fused_kernel<false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (p.pair) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  if (p.pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mk_fused_kernel<true>, p);
+  cfg.numAttrs = n_attr;
+  if (p.pair) return cudaLaunchKernelEx(&cfg, mk_fused_kernel<true>, p);
+  return cudaLaunchKernelEx(&cfg, mk_fused_kernel<false>, p);
 }
 
 int max_pair_clusters() {

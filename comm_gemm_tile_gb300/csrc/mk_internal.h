@@ -117,6 +117,7 @@ struct FusedParams {
   int sliced;          // RS/AR with last_arrival: nobody sums on arrival; once its own tiles
                        //        are done, every epilogue warp sums 32-row x 64-column slices of
                        //        tiles whose partials have all arrived
+  int pdl;             // launched as a programmatic dependent of the previous kernel on the stream
   int atomic;          // RS/AR: 1 = every partial added into one fp32 tile per output tile with
                        //        red.global.add; the warp that completes a quarter converts it
   int wire_bf16;       // RS/AR running sum: 1 = the sum forwarded between parts is bf16

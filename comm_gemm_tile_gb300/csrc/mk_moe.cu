@@ -4,7 +4,8 @@
 // tokens processed on arrival).
 //
 // Four launches on the caller's stream:
-//   1. route + rank (one CTA per chunk of 64 tokens of a source rank): top-k
+//   1. route + rank (one CTA per chunk of 128 tokens of a source rank, one
+//      thread per token): top-k
 //      experts of every token, and for every (token, slot) its position among
 //      the chunk's rows routed to the same expert (a stable block-level
 //      multisplit), plus the chunk's per-expert counts;
@@ -17,6 +18,9 @@
 //   4. the persistent fused kernel: copy warps move token rows into recv_x in
 //      destination order and count them per 128-row block; compute CTAs run
 //      the tiles of each expert as soon as their blocks are complete.
+// Launches 2-4 are programmatic dependents of the launch before them: each
+// starts while its predecessor finishes and waits (griddepcontrol.wait) for
+// its results before it reads them.
 // Row order inside a destination rank d: local expert, then global token
 // g = r*T + t; every (token, slot) pair is one row.
 #include <algorithm>
@@ -33,9 +37,13 @@ namespace mk {
 
 namespace {
 
-constexpr int RR_THREADS = 256;
-constexpr int RR_TOKENS = 64;   // tokens per route/rank CTA
+constexpr int RR_TOKENS = 128;                 // tokens per route/rank CTA, one thread each
+constexpr int RR_THREADS = RR_TOKENS;
 constexpr int RR_WARPS = RR_THREADS / 32;
+constexpr int RR_COLS = 64;                    // experts staged in shared memory at a time
+constexpr int RR_PITCH = RR_COLS + 1;          // padded row of the staged logits
+constexpr int OF_THREADS = 1024;               // the offsets kernel's CTA
+constexpr int OF_BATCH = 16;                   // chunk counts a thread loads at once
 enum { MISC_NTILES = 0, MISC_OK = 1, MISC_WORDS = 64 };
 
 struct MoeArgs {
@@ -70,67 +78,83 @@ __device__ __noinline__ void bounds_fail(const MoeArgs& a, int code, long long i
 }
 #endif
 
-__device__ __forceinline__ bool better(float v, int e, float ov, int oe) {
-  // (ov, oe) beats (v, e): larger logit, ties to the lower expert id; e < 0 = none
-  if (oe < 0) return false;
-  if (e < 0) return true;
-  return ov > v || (ov == v && oe < e);
-}
-
 // Grid (C chunks, R ranks): CTA (c, r) routes tokens [c*RR_TOKENS, ...) of
-// rank r and ranks their (token, slot) pairs per expert inside the chunk.
+// rank r, one thread per token, and ranks their (token, slot) pairs per expert
+// inside the chunk.  The chunk's logits pass through shared memory in blocks
+// of RR_COLS experts: copied row-contiguously (coalesced, all copies of a
+// block in flight together by cp.async), then read by row
+// (one token per thread; the padded pitch keeps the column reads conflict
+// free).  A thread keeps its token's best KMAX (>= topk) experts as a list
+// sorted by (logit descending, expert id ascending), branch free.
+template <int KMAX>
 __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid_constant__ MoeArgs a) {
+  griddep_launch_dependents();
   const int c = blockIdx.x, r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, T = a.T, K = a.topk;
-  const int t0 = c * RR_TOKENS, t1 = min(T, t0 + RR_TOKENS);
-  const float* lg = a.logits[r];
+  const int t0 = c * RR_TOKENS, t1 = min(T, t0 + RR_TOKENS), nt = t1 - t0;
+  const float* lg = a.logits[r] + static_cast<size_t>(t0) * E;
   int* idx = a.topk_idx + static_cast<size_t>(r) * T * K;
-  // ---- top-k per token, one warp per token
-  for (int t = t0 + warp; t < t1; t += RR_WARPS) {
-    float v[MOE_MAX_E / 32];
-#pragma unroll
-    for (int i = 0; i < MOE_MAX_E / 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? lg[static_cast<size_t>(t) * E + e] : 0.f;
-    }
-    uint32_t taken = 0;
-    for (int j = 0; j < K; ++j) {
-      float bv = 0.f;
-      int be = -1;
-#pragma unroll
-      for (int i = 0; i < MOE_MAX_E / 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && better(bv, be, v[i], e)) {
-          bv = v[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (better(bv, be, ov, oe)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) idx[static_cast<size_t>(t) * K + j] = be;
-    }
-  }
-  __syncthreads();
-  // ---- stable multisplit of the chunk's (token, slot) list by expert
+  __shared__ float s_lg[RR_TOKENS * RR_PITCH];
+  __shared__ int s_idx[RR_TOKENS * MOE_MAX_TOPK];
   __shared__ int wcnt[RR_WARPS * MOE_MAX_E];
   __shared__ int run[MOE_MAX_E];
+  // ---- top-k per token.  Key of (logit v, expert e): the order-preserving
+  // bits of v (-0 made +0, so that it ties with +0) above ~e, so that a larger
+  // key is a larger logit or, on a tie, the lower expert id; 0 = empty.
+  unsigned long long best[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) best[j] = 0ull;
+  for (int e0 = 0; e0 < E; e0 += RR_COLS) {
+    const int w = min(RR_COLS, E - e0);
+    if (e0 > 0) __syncthreads();   // the previous block has been read
+    {   // every copy of the block in flight at once
+      const int ee = tid % RR_COLS;
+      if (ee < w) {
+        for (int tt = tid / RR_COLS; tt < nt; tt += RR_THREADS / RR_COLS)
+          cp_async_4(smem_u32(&s_lg[tt * RR_PITCH + ee]), lg + static_cast<size_t>(tt) * E + e0 + ee);
+      }
+      cp_async_wait_all();
+    }
+    __syncthreads();
+    if (tid < nt) {
+#pragma unroll 8
+      for (int ee = 0; ee < w; ++ee) {
+        const float v = s_lg[tid * RR_PITCH + ee];
+        const uint32_t b = __float_as_uint(v);
+        const uint32_t u = (b << 1) == 0u ? 0u : b;   // -0 -> +0
+        const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        unsigned long long key = (static_cast<unsigned long long>(ord) << 32) | ~static_cast<uint32_t>(e0 + ee);
+        // insert into the descending list: each slot keeps the larger key and
+        // passes the smaller one on
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          const unsigned long long hi = key > best[j] ? key : best[j];
+          key = key > best[j] ? best[j] : key;
+          best[j] = hi;
+        }
+      }
+    }
+  }
+  if (tid < nt) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < K) {
+        const int be = static_cast<int>(~static_cast<uint32_t>(best[j]));
+        idx[static_cast<size_t>(t0 + tid) * K + j] = be;
+        s_idx[tid * K + j] = be;
+      }
+  }
   for (int e = tid; e < E; e += RR_THREADS) run[e] = 0;
-  const int a0 = t0 * K, n = (t1 - t0) * K;
+  __syncthreads();
+  // ---- stable multisplit of the chunk's (token, slot) list by expert
+  const int n = nt * K;
   const uint32_t lt = (1u << lane) - 1u;
   for (int b0 = 0; b0 < n; b0 += RR_THREADS) {
     for (int x = tid; x < RR_WARPS * E; x += RR_THREADS) wcnt[x] = 0;
     __syncthreads();
     const int ai = b0 + tid;
-    const int e = (ai < n) ? idx[a0 + ai] : -1 - lane;   // distinct sentinels never group
+    const int e = (ai < n) ? s_idx[ai] : -1 - lane;   // distinct sentinels never group
     const uint32_t mask = __match_any_sync(0xffffffffu, e);
     const int rank_w = __popc(mask & lt);
     if (ai < n && (__ffs(mask) - 1) == lane) wcnt[warp * E + e] = __popc(mask);
@@ -145,73 +169,143 @@ __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid
       run[ee] = acc;
     }
     __syncthreads();
-    if (ai < n) a.pos[static_cast<size_t>(r) * T * K + a0 + ai] = wcnt[warp * E + e] + rank_w;
+    if (ai < n) a.pos[static_cast<size_t>(r) * T * K + static_cast<size_t>(t0) * K + ai] = wcnt[warp * E + e] + rank_w;
     __syncthreads();
   }
   for (int e = tid; e < E; e += RR_THREADS)
     a.hist[(static_cast<size_t>(r) * a.C + c) * E + e] = run[e];
 }
 
-__global__ void __launch_bounds__(256) moe_offsets_kernel(const __grid_constant__ MoeArgs a) {
-  const int tid = threadIdx.x;
-  const int R = a.R, E = a.E, El = a.E_loc;
-  // per (rank, expert): exclusive prefix over chunks (in place), and the count
-  for (int x = tid; x < R * E; x += 256) {
-    const int r = x / E, e = x - r * E;
-    int* h = a.hist + static_cast<size_t>(r) * a.C * E + e;
-    int acc = 0;
-    for (int c0 = 0; c0 < a.C; c0 += 8) {   // 8 loads in flight per thread
-      int v[8];
+// Exclusive scan by one warp of f(0) .. f(n-1): lane L takes a run of
+// ceil(n/32) consecutive values, the runs' sums are scanned with shuffles, and
+// put(k, prefix) receives every prefix.  Returns the total (in every lane).
+template <class F, class Put>
+__device__ int warp_exclusive_scan(int n, F f, Put put) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int lo = min(n, lane * per), hi = min(n, lo + per);
+  int s = 0;
+  for (int k = lo; k < hi; ++k) s += f(k);
+  int incl = s;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = (c0 + u < a.C) ? h[static_cast<size_t>(c0 + u) * E] : 0;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  int acc = incl - s;
+  for (int k = lo; k < hi; ++k) {
+    put(k, acc);
+    acc += f(k);
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// One CTA.  Step 1: for every (rank r, expert e), the exclusive prefix of the
+// chunk counts hist[r][c][e] over the chunks c (in place) and counts[r][e].
+// A team of G threads shares a pair (G a power of two, G*R*E <= OF_THREADS):
+// member m takes the m-th run of consecutive chunks, and consecutive threads
+// take consecutive experts, so each load of a warp is one coalesced request and
+// a thread has a whole batch of loads in flight.  Step 2 works in shared
+// memory: expert totals, per-(rank, expert) bases, per-destination segment
+// offsets, received-row counts, the capacity check and the tile-table prefix.
+__global__ void __launch_bounds__(OF_THREADS) moe_offsets_kernel(const __grid_constant__ MoeArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int s_cnt[MK_MAX_RANKS * MOE_MAX_E];
+  __shared__ int s_part[OF_THREADS];
+  __shared__ int s_tot[MOE_MAX_E];
+  __shared__ int s_rc[MK_MAX_RANKS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.R, E = a.E, El = a.E_loc, C = a.C;
+  const int P = R * E;
+  int G = 1;
+  while (2 * G * P <= OF_THREADS) G *= 2;
+  const int span = (C + G - 1) / G;
+  for (int x0 = 0; x0 < P * G; x0 += OF_THREADS) {   // more than one round only when G = 1
+    const int x = x0 + tid;
+    const bool act = x < P * G;
+    const int pr = act ? x % P : 0, m = act ? x / P : 0;
+    const int rr = pr / E, e = pr - rr * E;
+    int* h = a.hist + static_cast<size_t>(rr) * C * E + e;
+    const int c_lo = min(C, m * span), c_hi = act ? min(C, c_lo + span) : c_lo;
+    int v[OF_BATCH];
+    int sum = 0;
+    for (int cb = c_lo; cb < c_hi; cb += OF_BATCH) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (c0 + u < a.C) {
-          h[static_cast<size_t>(c0 + u) * E] = acc;
+      for (int u = 0; u < OF_BATCH; ++u) v[u] = (cb + u < c_hi) ? h[static_cast<size_t>(cb + u) * E] : 0;
+#pragma unroll
+      for (int u = 0; u < OF_BATCH; ++u) sum += v[u];
+    }
+    s_part[tid] = sum;
+    __syncthreads();
+    int acc = 0;   // the team's earlier members (G >= 2 means a single round, x0 = 0)
+    for (int q = 0; q < m; ++q) acc += s_part[pr + q * P];
+    if (act && m == G - 1) s_cnt[pr] = acc + sum;
+    if (c_hi - c_lo <= OF_BATCH) {   // the run is still in registers
+#pragma unroll
+      for (int u = 0; u < OF_BATCH; ++u)
+        if (c_lo + u < c_hi) {
+          h[static_cast<size_t>(c_lo + u) * E] = acc;
           acc += v[u];
         }
+    } else {
+      for (int cb = c_lo; cb < c_hi; cb += OF_BATCH) {
+#pragma unroll
+        for (int u = 0; u < OF_BATCH; ++u) v[u] = (cb + u < c_hi) ? h[static_cast<size_t>(cb + u) * E] : 0;
+#pragma unroll
+        for (int u = 0; u < OF_BATCH; ++u)
+          if (cb + u < c_hi) {
+            h[static_cast<size_t>(cb + u) * E] = acc;
+            acc += v[u];
+          }
+      }
     }
-    a.counts[r * E + e] = acc;
+    __syncthreads();   // s_part is rewritten by the next round
   }
-  __syncthreads();
-  for (int e = tid; e < E; e += 256) {
+  for (int x = tid; x < P; x += OF_THREADS) a.counts[x] = s_cnt[x];
+  for (int e = tid; e < E; e += OF_THREADS) {
     int acc = 0;
     for (int r = 0; r < R; ++r) {
       a.base[r * E + e] = acc;
-      acc += a.counts[r * E + e];
+      acc += s_cnt[r * E + e];
     }
+    s_tot[e] = acc;
     a.totals[e] = acc;
   }
   __syncthreads();
-  if (tid < R) {
-    const int d = tid;
-    int acc = 0;
-    for (int l = 0; l < El; ++l) {
-      a.segoff[d * (El + 1) + l] = acc;
-      acc += a.totals[d * El + l];
+  // warp d: segment offsets of destination d's local experts, and its received rows
+  for (int d = warp; d < R; d += OF_THREADS / 32) {
+    int* seg = a.segoff + d * (El + 1);
+    const int tot = warp_exclusive_scan(
+        El, [&](int l) { return s_tot[d * El + l]; }, [&](int l, int pre) { seg[l] = pre; });
+    if (lane == 0) {
+      seg[El] = tot;
+      a.recv_counts[d] = tot;
+      s_rc[d] = tot;
     }
-    a.segoff[d * (El + 1) + El] = acc;
-    a.recv_counts[d] = acc;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {
     int ok = 1;
     for (int d = 0; d < R; ++d)
-      if (a.recv_counts[d] > a.cap) ok = 0;
-    int acc = 0;
-    for (int k = 0; k < R * El; ++k) {
-      a.tprefix[k] = acc;
-      if (ok) acc += ((a.totals[k] + a.tile_rows - 1) / a.tile_rows) * a.n_nblk;
+      if (s_rc[d] > a.cap) ok = 0;
+    const int tr = a.tile_rows, nn = a.n_nblk;
+    const int acc = warp_exclusive_scan(
+        E, [&](int k) { return ok ? ((s_tot[k] + tr - 1) / tr) * nn : 0; },
+        [&](int k, int pre) { a.tprefix[k] = pre; });
+    if (lane == 0) {
+      a.tprefix[E] = acc;
+      a.misc[MISC_NTILES] = static_cast<uint32_t>(acc);
+      a.misc[MISC_OK] = static_cast<uint32_t>(ok);
+      if (!ok) atomicCAS(reinterpret_cast<int*>(&a.hdr[HDR_STATUS]), 0, MK_ERR_CAPACITY);
     }
-    a.tprefix[R * El] = acc;
-    a.misc[MISC_NTILES] = static_cast<uint32_t>(acc);
-    a.misc[MISC_OK] = static_cast<uint32_t>(ok);
-    if (!ok) atomicCAS(reinterpret_cast<int*>(&a.hdr[HDR_STATUS]), 0, MK_ERR_CAPACITY);
   }
-  for (int x = tid; x < R * a.nblk; x += 256) a.blocks[x] = 0u;
+  for (int x = tid; x < R * a.nblk; x += OF_THREADS) a.blocks[x] = 0u;
 }
 
 __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant__ MoeArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int El = a.E_loc, E = a.E, K = a.topk, T = a.T;
   if (a.misc[MISC_OK] == 0u) return;
   const long long n = static_cast<long long>(a.R) * T * K;
@@ -308,6 +402,19 @@ bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long 
   return true;
 }
 
+cudaError_t launch_dependent(void (*kernel)(MoeArgs), dim3 grid, dim3 block, cudaStream_t s, const MoeArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool okp(const void* p, long long elems, unsigned align) {
   if (elems > 0 && !p) return false;
@@ -397,14 +504,18 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   a.cap = cap_rows;
   a.tile_rows = pair ? 2 * BM : BM;
 
-  moe_route_rank_kernel<<<dim3(L.C, R), RR_THREADS, 0, s>>>(a);
+  const dim3 rgrid(L.C, R);
+  if (topk <= 2) moe_route_rank_kernel<2><<<rgrid, RR_THREADS, 0, s>>>(a);
+  else moe_route_rank_kernel<MOE_MAX_TOPK><<<rgrid, RR_THREADS, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
-  moe_offsets_kernel<<<1, 256, 0, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  // offsets, scatter and the fused kernel launch as programmatic dependents of
+  // the kernel before them: each waits (griddepcontrol.wait) for its
+  // predecessor's results, and its launch overlaps the predecessor's end.
+  if (launch_dependent(moe_offsets_kernel, dim3(1), dim3(OF_THREADS), s, a) != cudaSuccess) return MK_ERR_CUDA;
   const long long work = std::max(rows, static_cast<long long>(L.max_tiles));
   const int sgrid = static_cast<int>(std::min<long long>(ceil_div_ll(work, 256), 4LL * sms));
-  moe_scatter_kernel<<<std::max(1, sgrid), 256, 0, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  if (launch_dependent(moe_scatter_kernel, dim3(std::max(1, sgrid)), dim3(256), s, a) != cudaSuccess)
+    return MK_ERR_CUDA;
   if (H == 0 || N == 0 || cap_rows == 0) return MK_OK;
 
   // ---- the persistent dispatch + grouped GEMM kernel
@@ -441,6 +552,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
   p.hdr = a.hdr;
+  p.pdl = 1;
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();

@@ -124,6 +124,38 @@ def test_moe_routing_ties_and_golden():
     np.testing.assert_array_equal(res["topk_idx"].cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("R,E_loc,T,topk", [
+    (2, 80, 300, 5),     # experts in three staging blocks, the last one partial
+    (4, 64, 129, 8),     # E = 256, the largest expert set; topk = 8
+    (16, 16, 200, 2),    # the most ranks
+    (3, 7, 1000, 3),     # E = 21 (one partial block), many chunks
+    (1, 1, 50, 1),
+])
+def test_moe_routing_bookkeeping_shapes(R, E_loc, T, topk):
+    # routing, counts and the dispatch permutation alone (N = 0: no GEMM launch),
+    # on logits with many ties, including -0 against +0 (a tie: lower id wins)
+    E = R * E_loc
+    lg = []
+    for r in range(R):
+        v = np.round(np.random.default_rng(90 + r).standard_normal((T, E)) * 1.2).astype(np.float32)
+        v[::7, ::3] = -0.0
+        lg.append(torch.from_numpy(v))
+    x = [torch.zeros((T, 8), dtype=torch.bfloat16).cuda() for _ in range(R)]
+    wexp = [torch.zeros((E_loc, 8, 0), dtype=torch.bfloat16).cuda() for _ in range(R)]
+    ws = mk.Workspace()
+    res = mk.moe_dispatch_gemm(x, [t.cuda() for t in lg], wexp, E_loc=E_loc, topk=topk, workspace=ws)
+    st, _ = mk.device_status(ws)
+    assert st == mk.MK_OK
+    idx = [O.moe_route(t.numpy(), topk) for t in lg]
+    np.testing.assert_array_equal(res["topk_idx"].cpu().numpy(), np.concatenate(idx, 0))
+    np.testing.assert_array_equal(res["counts"].cpu().numpy(), O.moe_counts(idx, E))
+    recv_src, _ = O.moe_dispatch(idx, E_loc)
+    rc = res["recv_counts"].cpu().numpy()
+    for d in range(R):
+        assert rc[d] == len(recv_src[d])
+        np.testing.assert_array_equal(res["recv_src"][d][:rc[d]].cpu().numpy(), recv_src[d])
+
+
 def test_moe_capacity_overflow_reports_and_dispatches_nothing():
     w = I.MoeWorkload("t", R=2, E_loc=2, T=128, H=64, N=256, integer=True, cap_rows=64)
     x, logits, wexp = I.moe_inputs(w)
