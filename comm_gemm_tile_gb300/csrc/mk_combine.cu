@@ -39,43 +39,51 @@ struct CombineArgs {
   long long cap;
 };
 
+// One CTA: expert totals, segment offsets, the capacity check and the
+// tile-table prefix, with the small tables in shared memory and the prefixes
+// taken by warp scans.
 __global__ void __launch_bounds__(256) combine_plan_kernel(const __grid_constant__ CombineArgs a) {
-  const int tid = threadIdx.x;
+  griddep_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.R, El = a.E_loc, E = a.E;
+  __shared__ int s_tot[MOE_MAX_E];
   __shared__ int s_ok;
   if (tid == 0) s_ok = 1;
   for (int e = tid; e < E; e += 256) {
     int acc = 0;
     for (int r = 0; r < R; ++r) acc += a.counts[r * E + e];
+    s_tot[e] = acc;
     a.totals[e] = acc;
   }
   __syncthreads();
-  if (tid < R) {
-    const int d = tid;
-    long long acc = 0;
-    for (int l = 0; l < El; ++l) {
-      a.segoff[d * (El + 1) + l] = static_cast<int>(acc);
-      acc += a.totals[d * El + l];
+  for (int d = warp; d < R; d += 256 / 32) {   // warp d: destination d's segments
+    int* seg = a.segoff + d * (El + 1);
+    const int tot = warp_exclusive_scan(
+        El, [&](int l) { return s_tot[d * El + l]; }, [&](int l, int pre) { seg[l] = pre; });
+    if (lane == 0) {
+      seg[El] = tot;
+      if (tot > a.cap) atomicExch(&s_ok, 0);
     }
-    a.segoff[d * (El + 1) + El] = static_cast<int>(acc);
-    if (acc > a.cap) atomicExch(&s_ok, 0);
   }
   __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {
     const int ok = s_ok;
-    int acc = 0;
-    for (int k = 0; k < E; ++k) {
-      a.tprefix[k] = acc;
-      if (ok) acc += ((a.totals[k] + a.tile_rows - 1) / a.tile_rows) * a.n_nblk;
+    const int tr = a.tile_rows, nn = a.n_nblk;
+    const int acc = warp_exclusive_scan(
+        E, [&](int k) { return ok ? ((s_tot[k] + tr - 1) / tr) * nn : 0; },
+        [&](int k, int pre) { a.tprefix[k] = pre; });
+    if (lane == 0) {
+      a.tprefix[E] = acc;
+      a.misc[CMISC_NTILES] = static_cast<uint32_t>(acc);
+      a.misc[CMISC_OK] = static_cast<uint32_t>(ok);
+      if (!ok) atomicCAS(reinterpret_cast<int*>(&a.hdr[HDR_STATUS]), 0, MK_ERR_CAPACITY);
     }
-    a.tprefix[E] = acc;
-    a.misc[CMISC_NTILES] = static_cast<uint32_t>(acc);
-    a.misc[CMISC_OK] = static_cast<uint32_t>(ok);
-    if (!ok) atomicCAS(reinterpret_cast<int*>(&a.hdr[HDR_STATUS]), 0, MK_ERR_CAPACITY);
   }
 }
 
 __global__ void __launch_bounds__(256) combine_tiles_kernel(const __grid_constant__ CombineArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long ncnt = static_cast<long long>(a.R) * a.T * a.n_nblk;
@@ -248,8 +256,10 @@ mk_status mk_moe_combine(const void* const* h, const void* const* w2, const floa
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
   const long long work = std::max(static_cast<long long>(R) * T * L.n_nblk, static_cast<long long>(L.max_tiles));
   const int tgrid = static_cast<int>(std::min<long long>(ceil_div_ll(work, 256), 4LL * device_sm_count()));
-  combine_tiles_kernel<<<std::max(1, tgrid), 256, 0, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+  // the tile kernel and the fused kernel launch as programmatic dependents of
+  // the launch before them (each waits for its predecessor's results)
+  if (launch_dependent(combine_tiles_kernel, dim3(std::max(1, tgrid)), dim3(256), s, a) != cudaSuccess)
+    return MK_ERR_CUDA;
 
   FusedParams p;
   std::memset(&p, 0, sizeof(p));
@@ -274,6 +284,7 @@ mk_status mk_moe_combine(const void* const* h, const void* const* w2, const floa
   p.moe_cnt = a.cnt;
   p.b_one_box = (H % 64 == 0) ? 1 : 0;
   p.hdr = a.hdr;
+  p.pdl = 1;
   p.wait_ns = default_wait_ns(cfg);
   p.inject = cfg ? cfg->inject : 0;
   p.epoch = next_epoch();

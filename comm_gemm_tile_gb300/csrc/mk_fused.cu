@@ -474,6 +474,28 @@ __device__ __forceinline__ void trace_end(const FusedParams& p, int i, uint32_t 
                                (static_cast<unsigned long long>(blockIdx.x) << 1) | rank);
 }
 
+// MoE dispatch: whether every row of the item has landed, from one round trip
+// of relaxed loads (its block counters and the rank's row count, all in flight
+// together, where acquire loads would go one after another); when they have,
+// the acquire fence and the proxy fence that order the item's TMA loads after
+// them are taken here.  false: not yet (or an entry out of range: the caller's
+// bounds checks and bounded waits take over).
+__device__ bool moe_rows_ready(const FusedParams& p, const Item& it) {
+  const int d = it.amap;
+  if (d < 0 || d >= p.R || it.arow < 0 || it.row_hi <= 0 || it.row_hi > BM || it.arow + it.row_hi > p.M) return false;
+  const int b0 = it.arow / BM, b1 = (it.arow + it.row_hi - 1) / BM;   // b1 <= b0 + 1
+  const uint32_t* cnt = p.flags + static_cast<size_t>(d) * p.moe_nblk;
+  const uint32_t v0 = ld_relaxed_gpu(cnt + b0);
+  const uint32_t v1 = (b1 > b0) ? ld_relaxed_gpu(cnt + b1) : 0u;
+  const int rc = p.moe_recv_counts[d];
+  const uint32_t w0 = static_cast<uint32_t>(min(BM, rc - b0 * BM));
+  const uint32_t w1 = (b1 > b0) ? static_cast<uint32_t>(min(BM, rc - b1 * BM)) : 0u;
+  if (v0 != w0 || v1 != w1) return false;
+  fence_acq_rel_gpu();
+  fence_proxy_async_global();
+  return true;
+}
+
 // TMA producer (one thread).  With pairs each CTA loads its own 128 rows of A
 // and its 128 of the tile's 256 B columns into its own ring, completing on
 // the leader's full barrier, which the leader arms with both CTAs' bytes.
@@ -486,9 +508,16 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
   uint32_t issued_mask = 0, issued_par = 0;
   const int n_items = n_items_for(p);
   bool counters_ready = false;
+  const bool moe_wait = (p.op == OP_MOE && p.mode == MK_MODE_FUSED);
   for (int i = cid; i < n_items; i += p.n_compute) {
     Item it;
     decode(p, i, it, static_cast<int>(rank));
+    // the next item's tile-table entry (written by the routing kernels) into L1
+    // while this item's loads are issued
+    if ((p.op == OP_MOE || p.op == OP_MOE_COMBINE) && i + p.n_compute < n_items) {
+      prefetch_l1(p.moe_tiles + 5 * (i + p.n_compute));
+      prefetch_l1(p.moe_tiles + 5 * (i + p.n_compute) + 4);
+    }
     if (p.trace != nullptr) {
       trace_put(p, i, rank, 0, globaltimer_ns());
       trace_put(p, i, rank, 5, clock64());
@@ -509,7 +538,7 @@ __device__ void producer(const FusedParams& p, const ComputeSmem& S, int cid, ui
         !bounds_ok(p, it.amap < p.R && it.bz >= 0 && (it.row_hi == 0 || it.arow + it.row_hi <= p.M),
                    BC_MOE_TILE, i))
       goto done;
-    if (p.op == OP_MOE && p.mode == MK_MODE_FUSED && it.row_hi > 0) {
+    if (moe_wait && it.row_hi > 0 && !moe_rows_ready(p, it)) {
       // the tile's rows must have landed: every 128-row block of recv_x[d] it covers
       // (an empty pair half covers no rows and waits for nothing)
       const int d = it.amap;
@@ -1667,29 +1696,53 @@ __device__ void copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
 }
 
 // MoE dispatch by the copy warps of every compute CTA: destination rows of all
-// ranks, rank-major, in pieces of moe_rows_per_piece rows inside one 128-row
-// block; row `row` of rank d is a bit copy of token g = recv_src[d][row] / topk
-// (rank g / T, token g % T).  After a piece every lane fences and lane 0 adds
-// the piece's rows to the block's counter (zeroed by the offsets kernel).
+// ranks, rank-major (the dispatch order), in pieces of moe_rows_per_piece rows
+// inside one 128-row block; row `row` of rank d is a bit copy of token
+// g = recv_src[d][row] / topk (rank g / T, token g % T).  A token is read once:
+// the copy of its slot that comes first in the dispatch order also writes the
+// rows of its other slots (all later) and counts them in their blocks; the
+// later rows are then skipped.  After a piece every lane fences and lane 0 adds
+// the piece's own copied rows to the block's counter (zeroed by the offsets
+// kernel), and the lanes holding forwarded rows add one each to theirs.
 __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
   const int lane = threadIdx.x & 31;
-  if ((threadIdx.x >> 5) - 6 >= p.n_cw) return;
-  const int worker = cta * p.n_cw + ((threadIdx.x >> 5) - 6);
-  const int n_workers = n_ctas * p.n_cw;
+  const int wid = (threadIdx.x >> 5) - 6;   // copy warp of this CTA
+  if (wid < 0 || wid >= N_COPY_WARPS) return;
   if (p.mode == MK_MODE_GEMM_ONLY) return;   // baseline: recv_x is already filled
   if (*reinterpret_cast<const volatile int*>(p.moe_ok) == 0) return;
   const int pr = p.moe_rows_per_piece;
+  const int K = p.moe_topk;
   long long total = 0;
   for (int d = 0; d < p.R; ++d) total += (p.moe_recv_counts[d] + pr - 1) / pr;
+  // The pieces of the first moe_boost_waves waves' tiles go to every copy warp
+  // (those tiles wait for nothing else); the rest to the first n_cw warps of
+  // every CTA, which keep ahead of the tiles without crowding out their loads.
+  long long q_boost = 0;
+  if (p.moe_boost_waves > 0) {
+    const int nt = min(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p.moe_ntiles)),
+                       static_cast<uint32_t>(p.n_items));
+    const int ib = min(nt, p.moe_boost_waves * p.n_compute) - 1;
+    if (ib >= 0) {
+      const int* e = p.moe_tiles + 5 * ib;
+      const int db = e[0], last = e[2] + e[3] - 1;   // the entry's destination rank and last row
+      if (db >= 0 && db < p.R && last >= 0) {
+        for (int d = 0; d < db; ++d) q_boost += (p.moe_recv_counts[d] + pr - 1) / pr;
+        q_boost = min(total, q_boost + last / pr + 1);
+      }
+    }
+  }
   const size_t rb = static_cast<size_t>(p.K) * 2;
   const size_t n16 = rb / 16;
-  bool skip_first = (p.inject == 1 && worker == 0);
+  bool skip_first = (p.inject == 1 && cta == 0 && wid == 0);
 #if MK_MOE_CW_HINT
   // token rows are read once per slot; received rows are read again by the GEMM
   const uint64_t pol_src = l2_policy_evict_first();
   const uint64_t pol_dst = l2_policy_evict_last();
 #endif
-  for (long long q = worker; q < total; q += n_workers) {
+  uint32_t* pend_w = nullptr;   // lane j < n_pend: block counter of the j-th forwarded row
+  int n_pend = 0;
+  // piece q of the dispatch order; false: stop (a bounds failure or an abort)
+  auto copy_piece = [&](long long q) -> bool {
     int d = 0;
     long long j = q;
     int rc = p.moe_recv_counts[0];
@@ -1702,15 +1755,40 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
     const int rows = min(pr, rc - row0);
     {
       const int ok = bounds_ok(p, d < p.R && row0 >= 0 && row0 + rows <= p.M, BC_MOE_COPY, q) ? 1 : 0;
-      if (!__all_sync(0xffffffffu, ok)) return;
+      if (!__all_sync(0xffffffffu, ok)) return false;
     }
+    const int base_d = static_cast<int>(p.moe_rbase[d]);
+    int written = 0;
     for (int rr = 0; rr < rows; ++rr) {
       const int src = p.moe_src[d][row0 + rr];
       {
-        const int ok = bounds_ok(p, src >= 0 && src < p.R * p.moe_T * p.moe_topk, BC_MOE_SRC, row0 + rr) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, ok)) return;
+        const int ok = bounds_ok(p, src >= 0 && src < p.R * p.moe_T * K, BC_MOE_SRC, row0 + rr) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, ok)) return false;
       }
-      const int g = src / p.moe_topk;
+      const int g = src / K, slot = src - g * K;
+      // dispatch-order positions of the token's other slots (lane l: slot l)
+      const int self = base_d + row0 + rr;
+      int pos = INT_MAX;
+      if (lane < K && lane != slot) pos = p.moe_fwd[static_cast<size_t>(g) * K + lane];
+      if (__any_sync(0xffffffffu, pos < self)) continue;   // copied and counted with an earlier slot
+      uint8_t* xp = nullptr;    // lane l: slot l's destination row and its block counter
+      uint32_t* xw = nullptr;
+      int okx = 1;
+      if (pos != INT_MAX) {
+        int dd = 0;
+        while (dd + 1 < p.R && static_cast<int>(p.moe_rbase[dd + 1]) <= pos) ++dd;
+        const int rw = pos - static_cast<int>(p.moe_rbase[dd]);
+        okx = bounds_ok(p, rw >= 0 && rw < p.moe_recv_counts[dd] && rw < p.M, BC_MOE_SRC, pos) ? 1 : 0;
+        xp = p.moe_recv_x[dd] + static_cast<size_t>(rw) * rb;
+        xw = p.flags + static_cast<size_t>(dd) * p.moe_nblk + rw / BM;
+      }
+      if (!__all_sync(0xffffffffu, okx)) return false;
+      const uint32_t xmask = __ballot_sync(0xffffffffu, pos != INT_MAX);
+      uint8_t* xd[MOE_MAX_TOPK];
+#pragma unroll
+      for (int l = 0; l < MOE_MAX_TOPK; ++l)
+        xd[l] = reinterpret_cast<uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(xp), l));
       const int r = g / p.moe_T, t = g - r * p.moe_T;
       const uint8_t* sp = p.shard[r] + static_cast<size_t>(t) * rb;
       uint8_t* dp = p.moe_recv_x[d] + static_cast<size_t>(row0 + rr) * rb;
@@ -1734,19 +1812,53 @@ __device__ void moe_copy_warps_role(const FusedParams& p, int cta, int n_ctas) {
           if (idx < n16) st_global_v4(dp + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
 #endif
         }
+#pragma unroll
+        for (int l = 0; l < MOE_MAX_TOPK; ++l) {
+          if (!((xmask >> l) & 1u)) continue;
+#pragma unroll
+          for (int u = 0; u < MOE_CW_UNROLL; ++u) {
+            const size_t idx = i0 + static_cast<size_t>(u) * 32;
+            if (idx < n16) st_global_v4(xd[l] + idx * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+          }
+        }
+      }
+      ++written;
+      // queue one count for each forwarded row (flushed with the piece's fence)
+      for (uint32_t m = xmask; m != 0u; m &= m - 1u) {
+        const int l = __ffs(m) - 1;
+        uint32_t* w = reinterpret_cast<uint32_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(xw), l));
+        if (n_pend == 32) {
+          __threadfence();
+          __syncwarp();
+          atomicAdd(pend_w, 1u);
+          n_pend = 0;
+          __syncwarp();
+        }
+        if (lane == n_pend) pend_w = w;
+        ++n_pend;
       }
     }
     __threadfence();
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0 && written > 0) {
       if (skip_first) skip_first = false;
-      else atomicAdd(p.flags + static_cast<size_t>(d) * p.moe_nblk + row0 / BM, static_cast<uint32_t>(rows));
+      else atomicAdd(p.flags + static_cast<size_t>(d) * p.moe_nblk + row0 / BM, static_cast<uint32_t>(written));
     }
+    if (lane < n_pend) atomicAdd(pend_w, 1u);
+    n_pend = 0;
     __syncwarp();
     int stop = 0;
     if (lane == 0) stop = aborted(p) ? 1 : 0;
-    if (__shfl_sync(0xffffffffu, stop, 0)) return;
-  }
+    return __shfl_sync(0xffffffffu, stop, 0) == 0;
+  };
+  for (long long q = static_cast<long long>(cta) * N_COPY_WARPS + wid; q < q_boost;
+       q += static_cast<long long>(n_ctas) * N_COPY_WARPS)
+    if (!copy_piece(q)) return;
+  if (wid >= p.n_cw) return;
+  for (long long q = q_boost + static_cast<long long>(cta) * p.n_cw + wid; q < total;
+       q += static_cast<long long>(n_ctas) * p.n_cw)
+    if (!copy_piece(q)) return;
 }
 
 // Compute CTA (cid = compute index; with pairs, the pair index).

@@ -138,9 +138,12 @@ struct FusedParams {
   uint8_t* moe_recv_x[MK_MAX_RANKS];     // destination rows, [cap x H] per rank
   const int* moe_src[MK_MAX_RANKS];      // recv_src per rank: g*topk + slot of each row
   const int* moe_recv_counts;            // [R] rows received per rank
+  const int* moe_fwd;                    // [R*T*topk] dispatch-order position of each (token, slot)
+  const uint32_t* moe_rbase;             // [R] dispatch-order position of each rank's row 0
   const int* moe_ok;                     // 1 when no rank exceeds its capacity
   int moe_T, moe_topk, moe_nblk;         // tokens per rank, slots, 128-row blocks per rank
   int moe_rows_per_piece;                // destination rows per copy piece (divides 128)
+  int moe_boost_waves;                   // waves of tiles whose rows every copy warp moves first
   // MoE combine (out[r] = combined rows of source rank r)
   uint8_t* moe_ret[MK_MAX_RANKS];        // [T x topk x N] bf16 returned expert rows per source rank
   const float* moe_gates[MK_MAX_RANKS];  // [T x topk] gate weights per source rank
@@ -196,5 +199,22 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uin
                  uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
                  uint32_t b2);
 long long default_wait_ns(const mk_config* cfg);
+
+// Launches kernel(a) as a programmatic dependent of the previous launch on s:
+// the kernel must wait (griddepcontrol.wait) before it reads that launch's
+// results, and its own launch overlaps that launch's end.
+template <class Args>
+cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s, const Args& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 }  // namespace mk

@@ -29,6 +29,9 @@
 #include "mk_internal.h"
 #include "mk_ptx.cuh"
 
+#ifndef MK_MOE_BOOST_WAVES
+#define MK_MOE_BOOST_WAVES 2   // waves of tiles whose rows all copy warps move first
+#endif
 #ifndef MK_MOE_COPY_WARPS
 #define MK_MOE_COPY_WARPS 3   // copy warps per compute CTA for the fused MoE dispatch
 #endif
@@ -44,7 +47,8 @@ constexpr int RR_COLS = 64;                    // experts staged in shared memor
 constexpr int RR_PITCH = RR_COLS + 1;          // padded row of the staged logits
 constexpr int OF_THREADS = 1024;               // the offsets kernel's CTA
 constexpr int OF_BATCH = 16;                   // chunk counts a thread loads at once
-enum { MISC_NTILES = 0, MISC_OK = 1, MISC_WORDS = 64 };
+enum { MISC_NTILES = 0, MISC_OK = 1, MISC_RBASE = 16, MISC_WORDS = 64 };   // RBASE: R words
+static_assert(MISC_RBASE + MK_MAX_RANKS <= MISC_WORDS, "misc words");
 
 struct MoeArgs {
   const float* logits[MK_MAX_RANKS];
@@ -53,6 +57,7 @@ struct MoeArgs {
   int* counts;        // [R x E]
   int* recv_counts;   // [R]
   int* pos;           // [R*T*topk] position among the chunk's rows of the same expert
+  int* fwd;           // [R*T*topk] position of each (token, slot) row in the dispatch order
   int* hist;          // [R x C x E] per-chunk expert counts, turned into chunk prefixes
   int* base;          // [R x E]  rows of expert e from ranks before r
   int* totals;        // [E]
@@ -176,30 +181,6 @@ __global__ void __launch_bounds__(RR_THREADS) moe_route_rank_kernel(const __grid
     a.hist[(static_cast<size_t>(r) * a.C + c) * E + e] = run[e];
 }
 
-// Exclusive scan by one warp of f(0) .. f(n-1): lane L takes a run of
-// ceil(n/32) consecutive values, the runs' sums are scanned with shuffles, and
-// put(k, prefix) receives every prefix.  Returns the total (in every lane).
-template <class F, class Put>
-__device__ int warp_exclusive_scan(int n, F f, Put put) {
-  const int lane = threadIdx.x & 31;
-  const int per = (n + 31) / 32;
-  const int lo = min(n, lane * per), hi = min(n, lo + per);
-  int s = 0;
-  for (int k = lo; k < hi; ++k) s += f(k);
-  int incl = s;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  int acc = incl - s;
-  for (int k = lo; k < hi; ++k) {
-    put(k, acc);
-    acc += f(k);
-  }
-  return __shfl_sync(0xffffffffu, incl, 31);
-}
-
 // One CTA.  Step 1: for every (rank r, expert e), the exclusive prefix of the
 // chunk counts hist[r][c][e] over the chunks c (in place) and counts[r][e].
 // A team of G threads shares a pair (G a power of two, G*R*E <= OF_THREADS):
@@ -294,6 +275,11 @@ __global__ void __launch_bounds__(OF_THREADS) moe_offsets_kernel(const __grid_co
         E, [&](int k) { return ok ? ((s_tot[k] + tr - 1) / tr) * nn : 0; },
         [&](int k, int pre) { a.tprefix[k] = pre; });
     if (lane == 0) {
+      int rb = 0;   // first position of each destination's rows in the dispatch order
+      for (int d = 0; d < R; ++d) {
+        a.misc[MISC_RBASE + d] = static_cast<uint32_t>(rb);
+        rb += s_rc[d];
+      }
       a.tprefix[E] = acc;
       a.misc[MISC_NTILES] = static_cast<uint32_t>(acc);
       a.misc[MISC_OK] = static_cast<uint32_t>(ok);
@@ -332,6 +318,7 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
     }
 #endif
     a.recv_src[d][row] = (r * T + t) * K + j;
+    a.fwd[ai] = static_cast<int>(a.misc[MISC_RBASE + d]) + row;
   }
   const int ntiles = static_cast<int>(a.misc[MISC_NTILES]);
   const int npairs = a.R * El;
@@ -356,7 +343,7 @@ __global__ void __launch_bounds__(256) moe_scatter_kernel(const __grid_constant_
 }
 
 struct MoeLayout {
-  size_t blocks_off, misc_off, pos_off, hist_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
+  size_t blocks_off, misc_off, pos_off, fwd_off, hist_off, base_off, totals_off, segoff_off, tprefix_off, tiles_off;
   size_t trace_off, trace_n;   // in-kernel trace: item records (8 x u64), then copy-warp records
   size_t total;
   int nblk, n_nblk, max_tiles, C;
@@ -384,6 +371,7 @@ bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long 
   L.blocks_off = off;  off = al(off + static_cast<size_t>(R) * L.nblk * 4);
   L.misc_off = off;    off = al(off + MISC_WORDS * 4);
   L.pos_off = off;     off = al(off + static_cast<size_t>(rows) * 4);
+  L.fwd_off = off;     off = al(off + static_cast<size_t>(rows) * 4);
   L.C = static_cast<int>(ceil_div_ll(std::max(T, 1LL), RR_TOKENS));
   L.hist_off = off;    off = al(off + static_cast<size_t>(R) * L.C * E * 4);
   L.base_off = off;    off = al(off + static_cast<size_t>(E) * R * 4);
@@ -400,19 +388,6 @@ bool moe_layout(int R, int E_loc, int topk, long long T, long long H, long long 
   }
   L.total = off;
   return true;
-}
-
-cudaError_t launch_dependent(void (*kernel)(MoeArgs), dim3 grid, dim3 block, cudaStream_t s, const MoeArgs& a) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -484,6 +459,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   a.counts = counts;
   a.recv_counts = recv_counts;
   a.pos = reinterpret_cast<int*>(ws + L.pos_off);
+  a.fwd = reinterpret_cast<int*>(ws + L.fwd_off);
   a.hist = reinterpret_cast<int*>(ws + L.hist_off);
   a.C = L.C;
   a.base = reinterpret_cast<int*>(ws + L.base_off);
@@ -538,6 +514,8 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   p.moe_ntiles = reinterpret_cast<const int*>(a.misc + MISC_NTILES);
   p.moe_ok = reinterpret_cast<const int*>(a.misc + MISC_OK);
   p.moe_recv_counts = recv_counts;
+  p.moe_fwd = a.fwd;
+  p.moe_rbase = a.misc + MISC_RBASE;
   p.moe_T = static_cast<int>(T);
   p.moe_topk = topk;
   p.moe_nblk = L.nblk;
@@ -549,6 +527,7 @@ mk_status mk_moe_dispatch_gemm(const void* const* x, const float* const* logits,
   // that run beside it; 2 starve the tiles).  The unfused baseline's copy
   // launch runs alone and uses every copy warp.
   p.n_cw = std::max(1, std::min(MK_MOE_COPY_WARPS, N_COPY_WARPS));
+  p.moe_boost_waves = MK_MOE_BOOST_WAVES;
   p.b_one_box = (N % 64 == 0) ? 1 : 0;
   p.flags = a.blocks;
   p.hdr = a.hdr;

@@ -79,6 +79,30 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Exclusive scan by one warp of f(0) .. f(n-1): lane L takes a run of
+// ceil(n/32) consecutive values, the runs' sums are scanned with shuffles, and
+// put(k, prefix) receives every prefix.  Returns the total (in every lane).
+template <class F, class Put>
+__device__ int warp_exclusive_scan(int n, F f, Put put) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int lo = min(n, lane * per), hi = min(n, lo + per);
+  int s = 0;
+  for (int k = lo; k < hi; ++k) s += f(k);
+  int incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  int acc = incl - s;
+  for (int k = lo; k < hi; ++k) {
+    put(k, acc);
+    acc += f(k);
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 // ---------------------------------------------------------------- TMA (tensor memory access)
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -203,6 +227,19 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Relaxed load: several may be in flight at once (an acquire load orders
+// every later access after it); pair with fence_acq_rel_gpu() once the values
+// show that the data they guard is complete.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Brings a line into L1 ahead of a plain load of data no one writes during the kernel.
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ uint32_t ld_volatile(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
