@@ -79,6 +79,23 @@ def test_moe_integer_bit_exact(R, E_loc, T, H, N, pair):
         np.testing.assert_array_equal(gpu_bits(res["y"][d][:len(recv_src[d])]), want)
 
 
+@pytest.mark.parametrize("mode", [mk.MODE_FUSED, mk.MODE_UNFUSED])
+@pytest.mark.parametrize("R,E_loc,T,topk", [(2, 3, 200, 1), (4, 2, 150, 3), (2, 4, 130, 8), (8, 4, 64, 5)])
+def test_moe_topk_bit_exact(R, E_loc, T, topk, mode):
+    # the dispatch copy reads a token once and writes the rows of all its slots
+    # (the first slot in dispatch order forwards to the others): every top-k
+    w = I.MoeWorkload("t", R=R, E_loc=E_loc, T=T, H=136, N=256, topk=topk, integer=True,
+                      x_seed=33, logit_seed=43, w_seed=53)
+    x, logits, wexp, res, st, detail = run_both(w, cfg=mk.Config(mode=mode))
+    assert st == mk.MK_OK, (mk.status_string(st), detail)
+    recv_src, seg = check_dispatch(w, x, logits, res)
+    xb = [I.bits(t) for t in x]
+    for d in range(R):
+        rx = O.moe_gather_rows(xb, recv_src[d], w.topk)
+        want = O.moe_expert_gemm(rx, seg[d], I.bits(wexp[d]), out="bf16")
+        np.testing.assert_array_equal(gpu_bits(res["y"][d][:len(recv_src[d])]), want)
+
+
 @pytest.mark.parametrize("R,E_loc,T,H,N", SMALL)
 def test_moe_float_within_tolerance(R, E_loc, T, H, N):
     w = I.MoeWorkload("t", R=R, E_loc=E_loc, T=T, H=H, N=N, x_seed=61, logit_seed=71, w_seed=81)
