@@ -138,6 +138,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.mk_trace_entries.argtypes = [i, i, ll, ll, ll, P(_Cfg), P(sz)]
     L.mk_moe_trace_entries.restype = sz
     L.mk_moe_trace_entries.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg), P(sz)]
+    L.mk_mlp_trace_entries.restype = sz
+    L.mk_mlp_trace_entries.argtypes = [i, ll, ll, ll, P(_Cfg), P(sz)]
     L.mk_moe_workspace_size.restype = sz
     L.mk_moe_workspace_size.argtypes = [i, i, i, ll, ll, ll, ll, P(_Cfg)]
     L.mk_get_device_status.restype = i
@@ -357,6 +359,22 @@ def moe_trace_records(workspace: Workspace, R, E_loc, topk, T, H, N, cap_rows, c
     off = ctypes.c_size_t(0)
     n_rec = int(lib().mk_moe_trace_entries(R, E_loc, topk, T, H, N, cap_rows, _cfgp(cfg),
                                            ctypes.byref(off)))
+    if n_rec == 0:
+        z = torch.zeros((0, TRACE_WORDS), dtype=torch.int64)
+        return z, z
+    o = int(off.value)
+    nb = (n_rec + TRACE_COPY_RECORDS) * TRACE_WORDS * 8
+    raw = workspace.get(o + nb)[o:o + nb].view(torch.int64).view(-1, TRACE_WORDS).cpu()
+    return raw[:n_rec], raw[n_rec:]
+
+
+def mlp_trace_records(workspace: Workspace, R, m, h, f_r, cfg: Config):
+    """The in-kernel trace of the last chained MLP call made on `workspace` with
+    cfg.trace = 1 and these arguments: (item records, copy-warp records), int64 with
+    the words of trace_records; item i < R * row tiles * f_r column tiles is an
+    up-projection tile, the rest are down-projection items."""
+    off = ctypes.c_size_t(0)
+    n_rec = int(lib().mk_mlp_trace_entries(R, m, h, f_r, _cfgp(cfg), ctypes.byref(off)))
     if n_rec == 0:
         z = torch.zeros((0, TRACE_WORDS), dtype=torch.int64)
         return z, z

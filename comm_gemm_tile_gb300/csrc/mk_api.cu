@@ -647,14 +647,17 @@ namespace {
 struct MlpLayout {
   Plan pl;
   size_t chunk_off, cnt_off, flags_off, staging_off, total;
+  size_t trace_off, trace_n;   // in-kernel trace records at the end (cfg->trace = 1), or none
 };
 
 bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* cfg, MlpLayout& L) {
   if (R < 1 || R > MK_MLP_MAX_RANKS || m < 0 || h < 0 || f_r < 0) return false;
   if ((h % 8) || (f_r % 8)) return false;
-  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->operand != 0 || cfg->trace != 0 ||
+  if (cfg && (cfg->reduce >= 2 || cfg->wire != 0 || cfg->operand != 0 || cfg->trace < 0 || cfg->trace > 1 ||
               cfg->n_reduce_ctas > 0 || cfg->split_k > 1))
     return false;
+  // the trace covers one launch: the fused call or its GEMM-only baseline
+  if (cfg && cfg->trace && cfg->mode == MK_MODE_UNFUSED) return false;
   if (!plan_gemm(OP_RS, R, static_cast<long long>(R) * m, h, f_r, cfg, L.pl)) return false;
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   size_t off = WS_HDR_BYTES;
@@ -664,6 +667,19 @@ bool mlp_plan(int R, long long m, long long h, long long f_r, const mk_config* c
   off = (off + 1023) & ~static_cast<size_t>(1023);
   L.staging_off = off;
   L.total = off + L.pl.staging_bytes;
+  L.trace_off = 0;
+  L.trace_n = 0;
+  if (cfg && cfg->trace) {
+    // two records (the CTAs of a pair) per item, items counted for single CTAs
+    // (the larger count): up-projection tiles of every rank, then down-projection
+    // (tile, rank) parts
+    const long long nb1 = ceil_div_ll(f_r, BN);
+    const long long items = static_cast<long long>(L.pl.n_mblk) * R * nb1 +
+                            static_cast<long long>(L.pl.n_mblk) * L.pl.n_nblk * R;
+    L.trace_n = static_cast<size_t>(std::max(items, 1LL)) * 2;
+    L.trace_off = al(L.total);
+    L.total = L.trace_off + (L.trace_n + MK_TRACE_COPY_RECORDS) * 64;
+  }
   return true;
 }
 
@@ -676,6 +692,15 @@ size_t mk_mlp_workspace_size(int R, long long m, long long h, long long f_r, con
   MlpLayout L;
   if (!mlp_plan(R, m, h, f_r, cfg, L)) return 0;
   return L.total;
+}
+
+size_t mk_mlp_trace_entries(int R, long long m, long long h, long long f_r, const mk_config* cfg,
+                            size_t* offset) {
+  if (offset) *offset = 0;
+  MlpLayout L;
+  if (!mlp_plan(R, m, h, f_r, cfg, L)) return 0;
+  if (offset) *offset = L.trace_off;
+  return L.trace_n;
 }
 
 mk_status mk_mlp_ag_rs(const void* const* x_shards, const void* const* w1, const void* const* w2, int R,
@@ -712,6 +737,8 @@ mk_status mk_mlp_ag_rs(const void* const* x_shards, const void* const* w1, const
   FusedParams p;
   fill_common(p, pl, ws, cfg, MK_BF16);
   p.op = OP_MLP;
+  p.trace = L.trace_n ? reinterpret_cast<unsigned long long*>(ws + L.trace_off) : nullptr;
+  p.trace_cap = static_cast<int>(L.trace_n);
   p.flags = reinterpret_cast<uint32_t*>(ws + L.flags_off);
   p.staging = reinterpret_cast<float*>(ws + L.staging_off);
   p.chunk_cnt = reinterpret_cast<uint32_t*>(ws + L.chunk_off);

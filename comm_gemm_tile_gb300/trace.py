@@ -1,4 +1,4 @@
-"""Summaries of the in-kernel trace (mk_config.trace = 1) of one AG / RS / AR / MoE call.
+"""Summaries of the in-kernel trace (mk_config.trace = 1) of one AG / RS / AR / MoE / MLP call.
 
 `summarize(records, copy_records)` reduces the records of the newest call to
 per-wave figures: wave w is the w-th work item of every CTA.  For each wave it
@@ -9,7 +9,7 @@ records give when the AllGather copy-in started and ended and its rate.
 
 Run as a module on one GPU to trace a bench workload:
 
-    python -m comm_gemm_tile_gb300.trace ag|rs|ar|moe [--mode fused|gemm] [--calls N] [--pair auto|off|on]
+    python -m comm_gemm_tile_gb300.trace ag|rs|ar|moe|mlp [--mode fused|gemm] [--calls N] [--pair auto|off|on]
 
 It makes the workload's inputs (seeded normal bf16, drawn on the device), runs N
 untraced calls back to back to reach a steady clock and power state, then one
@@ -36,8 +36,13 @@ def _med(xs):
     return statistics.median(xs) if xs else float("nan")
 
 
-def summarize(rec: torch.Tensor, copy_rec: torch.Tensor | None = None, max_rows: int = 12) -> dict:
+def summarize(rec: torch.Tensor, copy_rec: torch.Tensor | None = None, max_rows: int = 12,
+              items: tuple | None = None) -> dict:
+    """items = (lo, hi): only work items lo <= i < hi (waves counted inside that range)."""
     idx = _newest(rec)
+    if items is not None:
+        it_ = idx // 2
+        idx = idx[(it_ >= items[0]) & (it_ < items[1])]
     r = rec[idx]
     t0i = int(r[:, mk.TRACE_START].min())
     # differences in int64 first: the stamps are ~1e18 ns, beyond a double's integer range
@@ -151,6 +156,43 @@ def _trace_moe(mode: str, calls: int, dev) -> str:
     return format_summary(summarize(rec), f"{w.name}, {mode}, after {calls} untraced calls")
 
 
+def _trace_mlp(mode: str, calls: int, dev) -> str:
+    """The chained MLP: the up-projection tiles and the down-projection items
+    summarised apart (item order: every up-projection tile first)."""
+    from comm_gemm_tile_gb300 import inputs as I
+    w = I.MLP_R8_TP8
+    m_mode = {"fused": mk.MODE_FUSED, "gemm": mk.MODE_GEMM_ONLY}[mode]
+    sets = []
+    for s in range(2):
+        x = [_dev_normal((w.m, w.h), 1.0, 40 + r + 1000 * s, dev) for r in range(w.R)]
+        w1 = [_dev_normal((w.h, w.f_r), 0.02, 50 + r + 1000 * s, dev) for r in range(w.R)]
+        w2 = [_dev_normal((w.f_r, w.h), 0.02, 60 + r + 1000 * s, dev) for r in range(w.R)]
+        sets.append((x, w1, w2))
+    ws = mk.Workspace(dev)
+    xg, hid, y = mk.mlp_ag_rs(*sets[0], workspace=ws)
+
+    def call(i, cfg):
+        mk.mlp_ag_rs(*sets[i % 2], x_gathered=xg, hid=hid, y_blocks=y, cfg=cfg, workspace=ws)
+
+    cfg = mk.Config(mode=m_mode, trace=1)
+    for i in range(calls):
+        call(i, mk.Config(mode=m_mode))
+    # the traced call on a zero-filled workspace of its own: the fused call's
+    # staging, where GEMM-only's records go, holds running sums
+    ws = mk.Workspace(dev)
+    call(calls, cfg)
+    st, detail = mk.device_status(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"traced call reported {mk.status_string(st)} ({detail})")
+    rec, crec = mk.mlp_trace_records(ws, w.R, w.m, w.h, w.f_r, cfg)
+    rows = w.R * w.m
+    n1 = w.R * (-(-rows // 256)) * (-(-w.f_r // 256))   # up-projection items on CTA pairs
+    t = f"{w.name}, {mode}, after {calls} untraced calls"
+    return "\n".join([format_summary(summarize(rec, crec, items=(0, n1)), t + ": up-projection tiles"),
+                      format_summary(summarize(rec, items=(n1, rec.shape[0] // 2)),
+                                     t + ": down-projection items")])
+
+
 def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0", pair: int = 0) -> str:
     from comm_gemm_tile_gb300 import build
     from comm_gemm_tile_gb300 import inputs as I
@@ -158,6 +200,8 @@ def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0
     dev = torch.device(device)
     if op == "moe":
         return _trace_moe(mode, calls, dev)
+    if op == "mlp":
+        return _trace_mlp(mode, calls, dev)
     w = {"ag": I.AG_R8_TP8_UP, "rs": I.RS_R8_TP8_DOWN, "ar": I.AR_R8_DECODE}[op]
     m_mode = {"fused": mk.MODE_FUSED, "gemm": mk.MODE_GEMM_ONLY}[mode]
     nsets = 2
@@ -203,7 +247,7 @@ def trace_workload(op: str, mode: str = "fused", calls: int = 30, device="cuda:0
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("op", choices=["ag", "rs", "ar", "moe"])
+    ap.add_argument("op", choices=["ag", "rs", "ar", "moe", "mlp"])
     ap.add_argument("--mode", choices=["fused", "gemm"], default="fused")
     ap.add_argument("--calls", type=int, default=30)
     ap.add_argument("--pair", choices=["auto", "off", "on"], default="auto",

@@ -137,9 +137,10 @@ typedef struct {
                                fp32 accumulation, bf16 / fp32 output as for bf16.  The
                                gathered A of AG is fp8 too.  MoE, combine, the MLP and
                                ring attention take bf16 only (MK_ERR_INVALID).           */
-  int trace;                /* AG / RS / AR / MoE dispatch: 1 = record per-item timestamps
-                               into a region at the end of the workspace (see
-                               mk_trace_entries, mk_moe_trace_entries); 0 = off. */
+  int trace;                /* AG / RS / AR / MoE dispatch / chained MLP (fused or
+                               GEMM-only): 1 = record per-item timestamps into a region
+                               at the end of the workspace (see mk_trace_entries,
+                               mk_moe_trace_entries, mk_mlp_trace_entries); 0 = off. */
 } mk_config;
 
 /* Bytes of workspace an op needs for this shape and config (0 on bad args).
@@ -384,6 +385,16 @@ size_t mk_trace_entries(int op, int R, long long m, long long n, long long k, co
  * copy writes none). */
 size_t mk_moe_trace_entries(int R, int E_loc, int topk, long long T, long long H, long long N,
                             long long cap_rows, const mk_config *cfg, size_t *offset);
+
+/* The same for a chained MLP call (arguments as for mk_mlp_workspace_size;
+ * MK_MODE_FUSED or MK_MODE_GEMM_ONLY): record 2*i + c belongs to work item i,
+ * the up-projection tiles of every rank first, then the down-projection
+ * items, with the words of mk_trace_entries ([1]: an up-projection tile's
+ * gathered rows have landed; for a down-projection item, when its rows of
+ * H_r are complete).  The copy-warp records that follow are those of the
+ * AllGather copy-in. */
+size_t mk_mlp_trace_entries(int R, long long m, long long h, long long f_r, const mk_config *cfg,
+                            size_t *offset);
 
 /* Synchronises `stream`, then reads and clears the device status word of a
  * workspace: MK_OK, MK_ERR_TIMEOUT or MK_ERR_CAPACITY (or MK_ERR_CUDA if the

@@ -189,7 +189,15 @@ def test_trace_layout(L):
     n = L.mk_trace_entries(mk.OP_AG_GEMM, 8, 1024, 3584, 8192, ctypes.byref(cfg_on.c()), ctypes.byref(off))
     assert n == 64 * 14 * 2
     assert mk.workspace_size(mk.OP_GEMM_RS, 8, 8192, 8192, 3584, mk.Config(trace=2)) == 0
-    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1)) == 0
+    # the chained MLP: two records per up-projection tile (64 row tiles x 8 ranks x 14
+    # column tiles) and per down-projection (tile, rank) part (64 x 32 tiles x 8 ranks)
+    n = L.mk_mlp_trace_entries(8, 1024, 8192, 3584, ctypes.byref(cfg_on.c()), ctypes.byref(off))
+    assert n == 2 * (64 * 8 * 14 + 64 * 32 * 8) and off.value % 256 == 0
+    assert off.value >= mk.mlp_workspace_size(8, 1024, 8192, 3584)
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1)) == \
+        off.value + (n + mk.TRACE_COPY_RECORDS) * 64
+    assert L.mk_mlp_trace_entries(8, 1024, 8192, 3584, ctypes.byref(cfg_off.c()), ctypes.byref(off)) == 0
+    assert mk.mlp_workspace_size(8, 1024, 8192, 3584, mk.Config(trace=1, mode=mk.MODE_UNFUSED)) == 0
 
 
 def test_moe_trace_layout(L):

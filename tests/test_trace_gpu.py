@@ -153,3 +153,42 @@ def test_moe_trace_records(pair):
         assert bool((r[:, a_] <= r[:, b_]).all()), (a_, b_)
     assert crec.shape == (mk.TRACE_COPY_RECORDS, mk.TRACE_WORDS)
     assert not bool(((crec[:, mk.TRACE_ID] >> 32) == e).any())   # the dispatch writes none
+
+
+@pytest.mark.parametrize("mode", [mk.MODE_FUSED, mk.MODE_GEMM_ONLY])
+@pytest.mark.parametrize("pair", [mk.PAIR_OFF, mk.PAIR_ON])
+def test_mlp_trace_records(pair, mode):
+    # the chained MLP: every up-projection tile and down-projection item of the
+    # traced launch leaves ordered stamps; results unchanged by tracing
+    w = I.MlpWorkload("t", R=4, m=200, h=264, f_r=520, integer=True)
+    x, w1, w2 = I.mlp_inputs(w)
+    args = (dev(x), dev(w1), dev(w2))
+    ws0 = mk.Workspace()
+    xg, hid, y0 = mk.mlp_ag_rs(*args, workspace=ws0)    # fills x_gathered for GEMM-only
+    plain = mk.mlp_ag_rs(*args, x_gathered=xg, cfg=mk.Config(cta_pair=pair, mode=mode), workspace=ws0)[2]
+    cfg = mk.Config(cta_pair=pair, mode=mode, trace=1)
+    ws = mk.Workspace()
+    got = mk.mlp_ag_rs(*args, x_gathered=xg, cfg=cfg, workspace=ws)[2]
+    st, detail = mk.device_status(ws)
+    assert st == mk.MK_OK, (mk.status_string(st), detail)
+    for a_, b_ in zip(got, plain):
+        assert torch.equal(a_, b_)
+    rec, crec = mk.mlp_trace_records(ws, w.R, w.m, w.h, w.f_r, cfg)
+    e, sel = _latest(rec)
+    idx = torch.nonzero(sel).flatten()
+    items = sorted({int(j) // 2 for j in idx})
+    assert items and items == list(range(len(items)))
+    # up-projection tiles (R ranks x row tiles x column tiles of f_r) come first
+    rows = w.R * w.m
+    rt = -(-rows // (256 if pair == mk.PAIR_ON else 128))
+    n1 = w.R * rt * -(-w.f_r // 256)
+    assert len(items) > n1
+    r = rec[idx]
+    for a_, b_ in ((mk.TRACE_START, mk.TRACE_INPUTS), (mk.TRACE_INPUTS, mk.TRACE_ISSUED),
+                   (mk.TRACE_START, mk.TRACE_READY), (mk.TRACE_READY, mk.TRACE_END)):
+        assert bool((r[:, a_] <= r[:, b_]).all()), (a_, b_)
+    mine = crec[(crec[:, mk.TRACE_ID] >> 32) == e]
+    if mode == mk.MODE_FUSED:   # the AllGather copy-in by copy warps moved every gathered row
+        assert mine.shape[0] > 0 and int(mine[:, 3].sum()) >= (w.R - 1) * w.m * w.h * 2
+    else:
+        assert mine.shape[0] == 0
