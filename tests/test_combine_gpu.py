@@ -181,3 +181,33 @@ def test_combine_repeated_calls_and_empty_contraction():
     st, _ = mk.device_status(ws)
     assert st == mk.MK_OK
     assert all(float(t.float().abs().max()) == 0.0 for t in res["ret"] + res["out"])
+
+
+def _random_case(seed):
+    g = np.random.default_rng(seed)
+    R = int(g.integers(1, 17))                      # up to 16 ranks
+    E_loc = int(g.integers(1, 256 // R + 1 if R > 1 else 9))
+    E_loc = min(E_loc, 256 // R)
+    topk = int(g.integers(1, min(8, R * E_loc) + 1))
+    T = int(g.integers(1, 200))
+    N = 8 * int(g.integers(1, 40))
+    H = 8 * int(g.integers(1, 70))
+    pair = [mk.PAIR_OFF, mk.PAIR_ON][int(g.integers(0, 2))]
+    return R, E_loc, topk, T, N, H, pair
+
+
+@pytest.mark.parametrize("seed", list(range(8)))
+def test_combine_random_shapes_bit_exact(seed):
+    # seeded random shapes: up to 16 ranks and 256 experts (the plan kernel's
+    # shared-memory tables and warp scans), top-k 1..8, CTA pairs on and off
+    R, E_loc, topk, T, N, H, pair = _random_case(9000 + seed)
+    w = I.MoeCombineWorkload("t", R=R, E_loc=E_loc, T=T, N=N, H=H, topk=topk, integer=True,
+                             logit_seed=300 + seed, h_seed=310 + seed, w2_seed=320 + seed,
+                             gate_seed=330 + seed)
+    (logits, h, w2, gates), (counts, recv_src), res, st, detail = run(w, mk.Config(cta_pair=pair))
+    assert st == mk.MK_OK, (mk.status_string(st), detail, (R, E_loc, topk, T, N, H, pair))
+    want = O.moe_combine([I.bits(t) for t in h], recv_src, counts, [I.bits(t) for t in w2],
+                         [g.numpy() for g in gates], w.E_loc, w.topk, w.T)
+    for r in range(R):
+        np.testing.assert_array_equal(I.bits(res["ret"][r]), want["ret"][r])
+        np.testing.assert_array_equal(I.bits(res["out"][r]), want["out"][r])
