@@ -28,8 +28,8 @@ def built():
 
 def _case(seed):
     g = np.random.default_rng(seed)
-    R = int(g.integers(1, 9))
-    E_loc = int(g.integers(1, 7))
+    R = int(g.integers(1, 17))                      # up to 16 ranks
+    E_loc = int(g.integers(1, min(6, 256 // R) + 1))
     topk = int(g.integers(1, min(8, R * E_loc) + 1))
     T = int(g.integers(1, 400))
     H = 8 * int(g.integers(1, 40))
