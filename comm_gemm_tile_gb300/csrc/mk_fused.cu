@@ -894,18 +894,30 @@ __device__ __forceinline__ void flush_staged(const FusedParams& p, const Item& i
   }
 }
 
+// fp32 load through L2 (not L1) with an L2 eviction policy.
+__device__ __forceinline__ float4 ld_cg_f4_pol(const float* ptr, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
 // Sliced reduction (reduce = 4), after the warp's own tiles: job j = (tile,
 // 32-row quarter, 64-column group), taken by epilogue warps j, j + n_warps, ...
 // Once the quarter's arrival count shows all P partials staged, the warp sums
 // its slice of them in rank order 0..P-1 (the running sum's order, so the
 // result is the same bits) and writes it through its staging to every replica
 // (AR) or the owner's block (RS).  The waits come after all of this CTA's own
-// tiles, which wait for nothing, so every count is reached.
+// tiles, which wait for nothing, so every count is reached.  The partials were
+// staged with an L2 evict_last policy (they stay in L2 while the operands
+// stream past) and are read here with evict_first (each is read once).
 __device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_t epi, int gw, int n_warps,
                                 bool& counters_ready) {
   const int lane = threadIdx.x & 31;
   constexpr int GROUPS = BN / 64;
   const int n_jobs = p.n_tiles * 4 * GROUPS;
+  const uint64_t pol_once = l2_policy_evict_first();
   for (int j = gw; j < n_jobs; j += n_warps) {
     const int tile = j / (4 * GROUPS), q = (j / GROUPS) % 4, g = j % GROUPS;
     const int mb = tile / p.n_nblk, nb = tile - mb * p.n_nblk;
@@ -951,7 +963,7 @@ __device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_
       float4 acc[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        acc[u] = ld_global_cg_f4(base + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+        acc[u] = ld_cg_f4_pol(base + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4, pol_once);
       // two partials' loads in flight at a time, added in rank order
       int part = 1;
 #pragma unroll 1
@@ -961,8 +973,8 @@ __device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_
         float4 v0[8], v1[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          v0[u] = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
-          v1[u] = ld_global_cg_f4(s1 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+          v0[u] = ld_cg_f4_pol(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4, pol_once);
+          v1[u] = ld_cg_f4_pol(s1 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4, pol_once);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -980,7 +992,7 @@ __device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_
         const float* s0 = base + static_cast<size_t>(part) * TILE_F32;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 v = ld_global_cg_f4(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4);
+          const float4 v = ld_cg_f4_pol(s0 + (static_cast<size_t>((c * 8 + u) * BM + trow)) * 4, pol_once);
           acc[u].x += v.x;
           acc[u].y += v.y;
           acc[u].z += v.z;
@@ -1430,7 +1442,10 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     } else if (it.slot >= 0 && p.last_arrival) {
       // Stage this partial, then the warp whose store completes its 32-row
       // quarter of the tile (the P-th arrival) sums all P partials in order.
+      // Sliced: staged with L2 evict_last, so that they are still in L2 when
+      // the slices are summed (measured: decode AR 0.1015 -> 0.0955 ms).
       float* slot = p.staging + static_cast<size_t>(it.slot) * TILE_F32;
+      const uint64_t pol_keep = l2_policy_evict_last();
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -1439,7 +1454,8 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float* d = slot + (static_cast<size_t>((c * 8 + q) * BM + trow)) * 4;
-          st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+          if (p.sliced) st_global_v4_pol(d, make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]), pol_keep);
+          else st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         }
       }
       tc_fence_before();
