@@ -904,31 +904,45 @@ __device__ __forceinline__ float4 ld_cg_f4_pol(const float* ptr, uint64_t pol) {
 }
 
 // Sliced reduction (reduce = 4), after the warp's own tiles: job j = (tile,
-// 32-row quarter, 64-column group), taken by epilogue warps j, j + n_warps, ...
-// Once the quarter's arrival count shows all P partials staged, the warp sums
-// its slice of them in rank order 0..P-1 (the running sum's order, so the
-// result is the same bits) and writes it through its staging to every replica
-// (AR) or the owner's block (RS).  The waits come after all of this CTA's own
+// 32-row quarter, 64-column group).  An epilogue warp that has finished its own
+// tiles claims the next job from a counter in the header, so the jobs go out
+// in tile order (the order the tiles' partials complete in) to whichever warps
+// are free first: warps of CTAs with fewer items sum the first tiles while the
+// last wave still runs.  Once the quarter's arrival count shows all P partials
+// staged, the warp sums its slice of them in rank order 0..P-1 (the running
+// sum's order, so the result is the same bits) and writes it through its
+// staging to every replica (AR) or the owner's block (RS).  The waits come after all of this CTA's own
 // tiles, which wait for nothing, so every count is reached.  The partials were
 // staged with an L2 evict_last policy (they stay in L2 while the operands
 // stream past) and are read here with evict_first (each is read once).
-__device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_t epi, int gw, int n_warps,
+__device__ void finalize_slices(const FusedParams& p, const Item& proto, uint32_t epi, int gw,
                                 bool& counters_ready) {
   const int lane = threadIdx.x & 31;
   constexpr int GROUPS = BN / 64;
   const int n_jobs = p.n_tiles * 4 * GROUPS;
   const uint64_t pol_once = l2_policy_evict_first();
-  for (int j = gw; j < n_jobs; j += n_warps) {
+  while (true) {
+    int j = 0;
+    {
+      int ok = 1;
+      if (lane == 0) {
+        // the claim counter is zeroed at kernel start, with the counts
+        if (!counters_ready) {
+          if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_REDUCE, gw)) ok = 0;
+          counters_ready = true;
+        }
+        if (ok) j = static_cast<int>(atomicAdd(&p.hdr[HDR_CLAIM], 1u));
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+      j = __shfl_sync(0xffffffffu, j, 0);
+    }
+    if (j >= n_jobs) break;
     const int tile = j / (4 * GROUPS), q = (j / GROUPS) % 4, g = j % GROUPS;
     const int mb = tile / p.n_nblk, nb = tile - mb * p.n_nblk;
     const int rows = min(BM, p.M - mb * BM);
     if (32 * q >= rows) continue;                   // no row of this quarter is an output row
     int ok = 1;
     if (lane == 0) {
-      if (!counters_ready) {
-        if (!wait_flag(p, &p.hdr[HDR_READY], WHERE_REDUCE, j)) ok = 0;
-        counters_ready = true;
-      }
       const uint32_t* cnt = p.flags + static_cast<size_t>(tile) * 4 + q;
       if (ok && ld_acquire_gpu(cnt) != static_cast<uint32_t>(p.P)) {
         const uint64_t t0 = globaltimer_ns();
@@ -1585,9 +1599,8 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
   }
   if (p.sliced) {
     const int cta = PAIR ? 2 * cid + static_cast<int>(rank) : cid;
-    const int n_ctas = (PAIR ? 2 : 1) * p.n_compute;
     Item proto{};
-    finalize_slices(p, proto, epi, cta * 4 + (warp - 2), n_ctas * 4, counters_ready);
+    finalize_slices(p, proto, epi, cta * 4 + (warp - 2), counters_ready);
   }
 }
 
@@ -2374,6 +2387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_fused_kernel(const __grid_cons
       for (int x = threadIdx.x; x < p.R * p.n_mblk; x += NTHREADS) p.mlp_cnt[x] = 0u;
     } else {
       for (int x = threadIdx.x; x < p.n_tiles * 4; x += NTHREADS) p.flags[x] = 0u;
+      if (threadIdx.x == 0) p.hdr[HDR_CLAIM] = 0u;   // the sliced reduction's next job
     }
     __threadfence();
     __syncthreads();

@@ -61,7 +61,7 @@ constexpr int MAX_CHAIN_PARTIALS = 128;        // partials per tile of the runni
 constexpr int COPY_SUB_MAX = 16;               // AG flag stride per 128-row chunk
 
 // Workspace header words (uint32 each).
-enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_READY = 4, HDR_WORDS = 64 };
+enum { HDR_TICKET = 0, HDR_ABORT = 1, HDR_STATUS = 2, HDR_DETAIL = 3, HDR_READY = 4, HDR_CLAIM = 5, HDR_WORDS = 64 };
 constexpr size_t WS_HDR_BYTES = 256;
 
 enum Op { OP_AG = 0, OP_RS = 1, OP_AR = 2, OP_MOE = 3, OP_MOE_COMBINE = 4, OP_MLP = 5 };
