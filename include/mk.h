@@ -337,9 +337,7 @@ mk_status mk_ring_attention(const void *const *q, const void *const *k, const vo
  *     128 gathered rows, i.e. R*m_r up to 130560 rows) are rejected with
  *     MK_ERR_INVALID before anything is enqueued.
  *   - The first call on a device looks up the array's device address and
- *     zero-fills it on `stream`.  That set-up may not run while a stream is
- *     being captured, so make the first call on each device outside any
- *     stream capture.
+ *     zero-fills it on `stream` before its kernel.
  *   - Every call shares the one array and it keeps the previous call's
  *     contents; each call clears the part that must start at zero.  Two calls
  *     whose GPU work can overlap (different streams without ordering, or
