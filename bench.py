@@ -412,6 +412,10 @@ def main():
     ap.add_argument("--profile", choices=list(PROFILE_WORKLOADS), default=None,
                     help="profiling aid: make the workload's inputs and run --calls untimed fused calls "
                          "back to back (for an ncu capture of one of them); prints the device status")
+    ap.add_argument("--energy", choices=list(PROFILE_WORKLOADS), default=None,
+                    help="energy per call (NVML counter) of the workload's fused, GEMM-only and unfused "
+                         "modes")
+    ap.add_argument("--energy-secs", type=float, default=3.0)
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--scale", choices=["full", "small"], default="full",
                     help="--profile: the bench workload, or a reduced case (inputs still larger than L2)")
@@ -420,6 +424,8 @@ def main():
         return run_reference(args)
     if args.profile:
         return run_profile(args)
+    if args.energy:
+        return run_energy(args)
     if args.only:
         return run_only(args)
 
@@ -620,18 +626,10 @@ def main():
 PROFILE_WORKLOADS = ("ag", "rs", "ar", "moe", "combine", "mlp", "ring")
 
 
-def run_profile(args):
-    """Untimed fused calls of one workload (profiling aid: ncu captures one of
-    them).  --scale small shrinks the row / token / position counts, keeping the
-    inputs larger than L2, so that multi-pass captures stay small."""
-    torch.cuda.set_device(0)
-    device = torch.device("cuda", 0)
-    import comm_gemm_tile_gb300 as mk
-    from comm_gemm_tile_gb300 import build as mkbuild
-    mkbuild.build()
-    small = args.scale == "small"
-    ws = mk.Workspace(device)
-    name = args.profile
+def profile_call(mk, name, small, device, ws):
+    """One workload's inputs and a call(cfg=None) that runs it once (fused by
+    default; a Config picks GEMM-only or unfused).  small: the reduced case,
+    inputs still larger than L2."""
     if name in ("ag", "rs", "ar"):
         w = {"ag": I.AG_R8_TP8_UP, "rs": I.RS_R8_TP8_DOWN, "ar": I.AR_R8_DECODE}[name]
         if small and name != "ar":
@@ -642,16 +640,15 @@ def run_profile(args):
             b = dev_normal((w.k, w.n), w.b_std, w.b_seed, device)
             g = torch.empty((w.R * w.m, w.k), dtype=torch.bfloat16, device=device)
             c = torch.empty((w.R * w.m, w.n), dtype=torch.bfloat16, device=device)
-            call = lambda: mk.ag_gemm(a, b, a_gathered=g, c=c, workspace=ws)  # noqa: E731
-        else:
-            a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r, device) for r in range(w.R)]
-            b = [dev_normal((w.k, w.n), w.b_std, w.b_seed + r, device) for r in range(w.R)]
-            rows = w.m // w.R if name == "rs" else w.m
-            o = [torch.empty((rows, w.n), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
-            fn = mk.gemm_rs if name == "rs" else mk.gemm_ar
-            key = "c_blocks" if name == "rs" else "c_replicas"
-            call = lambda: fn(a, b, workspace=ws, **{key: o})  # noqa: E731
-    elif name in ("moe", "combine"):
+            return lambda cfg=None: mk.ag_gemm(a, b, a_gathered=g, c=c, cfg=cfg, workspace=ws)
+        a = [dev_normal((w.m, w.k), 1.0, w.a_seed + r, device) for r in range(w.R)]
+        b = [dev_normal((w.k, w.n), w.b_std, w.b_seed + r, device) for r in range(w.R)]
+        rows = w.m // w.R if name == "rs" else w.m
+        o = [torch.empty((rows, w.n), dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+        fn = mk.gemm_rs if name == "rs" else mk.gemm_ar
+        key = "c_blocks" if name == "rs" else "c_replicas"
+        return lambda cfg=None: fn(a, b, cfg=cfg, workspace=ws, **{key: o})
+    if name in ("moe", "combine"):
         wd = I.MOE_R8_E64
         T = wd.T // 4 if small else wd.T
         x = [dev_normal((T, wd.H), 1.0, wd.x_seed + r, device) for r in range(wd.R)]
@@ -660,33 +657,151 @@ def run_profile(args):
         cap = 2 * T * wd.R
         disp = mk.moe_dispatch_gemm(x, lg, we, E_loc=wd.E_loc, topk=wd.topk, cap_rows=cap, workspace=ws)
         if name == "moe":
-            call = lambda: mk.moe_dispatch_gemm(x, lg, we, E_loc=wd.E_loc, topk=wd.topk,  # noqa: E731
-                                                cap_rows=cap, out=disp, workspace=ws)
-        else:
-            w = I.MOE_COMBINE_R8_E64
-            h = [dev_normal((cap, w.N), 1.0, w.h_seed + d, device) for d in range(w.R)]
-            w2 = [dev_normal((w.E_loc, w.N, w.H), 0.02, w.w2_seed + d, device) for d in range(w.R)]
-            gates = [torch.full((T, w.topk), 0.5, device=device) for _ in range(w.R)]
-            del x, we
-            outs = mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"], E_loc=w.E_loc,
-                                  topk=w.topk, cap_rows=cap, workspace=ws)
-            call = lambda: mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"],  # noqa: E731
-                                          E_loc=w.E_loc, topk=w.topk, cap_rows=cap, out=outs,
-                                          workspace=ws)
-    elif name == "mlp":
+            return lambda cfg=None: mk.moe_dispatch_gemm(x, lg, we, E_loc=wd.E_loc, topk=wd.topk,
+                                                         cap_rows=cap, out=disp, cfg=cfg, workspace=ws)
+        w = I.MOE_COMBINE_R8_E64
+        h = [dev_normal((cap, w.N), 1.0, w.h_seed + d, device) for d in range(w.R)]
+        w2 = [dev_normal((w.E_loc, w.N, w.H), 0.02, w.w2_seed + d, device) for d in range(w.R)]
+        gates = [torch.full((T, w.topk), 0.5, device=device) for _ in range(w.R)]
+        del x, we
+        outs = mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"], E_loc=w.E_loc,
+                              topk=w.topk, cap_rows=cap, workspace=ws)
+        return lambda cfg=None: mk.moe_combine(h, w2, gates, disp["recv_src"], disp["counts"],
+                                               E_loc=w.E_loc, topk=w.topk, cap_rows=cap, out=outs,
+                                               cfg=cfg, workspace=ws)
+    if name == "mlp":
         w = I.MLP_R8_TP8
         m = w.m // 4 if small else w.m
         x = [dev_normal((m, w.h), 1.0, w.x_seed + r, device) for r in range(w.R)]
         w1 = [dev_normal((w.h, w.f_r), w.w_std, w.w1_seed + r, device) for r in range(w.R)]
         w2 = [dev_normal((w.f_r, w.h), w.w_std, w.w2_seed + r, device) for r in range(w.R)]
-        call = lambda: mk.mlp_ag_rs(x, w1, w2, workspace=ws)  # noqa: E731
-    else:  # ring
-        w = I.RING_R8_H8_S4096
-        s_r = w.s_r // 4 if small else w.s_r
-        shape = (w.heads, s_r, w.d)
-        q, k, v = ([dev_normal(shape, 1.0, seed + r, device) for r in range(w.R)]
-                   for seed in (w.q_seed, w.k_seed, w.v_seed))
-        call = lambda: mk.ring_attention(q, k, v, workspace=ws)  # noqa: E731
+        xg, hid, y = mk.mlp_ag_rs(x, w1, w2, workspace=ws)
+        return lambda cfg=None: mk.mlp_ag_rs(x, w1, w2, x_gathered=xg, hid=hid, y_blocks=y, cfg=cfg,
+                                             workspace=ws)
+    w = I.RING_R8_H8_S4096
+    s_r = w.s_r // 4 if small else w.s_r
+    shape = (w.heads, s_r, w.d)
+    q, k, v = ([dev_normal(shape, 1.0, seed + r, device) for r in range(w.R)]
+               for seed in (w.q_seed, w.k_seed, w.v_seed))
+    out = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(w.R)]
+    return lambda cfg=None: mk.ring_attention(q, k, v, out=out, cfg=cfg, workspace=ws)
+
+
+class Nvml:
+    """Read-only NVML queries through the driver's own library (no Python
+    bindings needed): the total-energy counter (mJ), the SM clock and the
+    enforced power limit of the GPU that CUDA device `idx` is."""
+
+    def __init__(self, idx: int = 0):
+        import ctypes
+        self.ct = ctypes
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        cnt = ctypes.c_uint()
+        self.nv.nvmlDeviceGetCount_v2(ctypes.byref(cnt))
+        self.h = ctypes.c_void_p()
+        pick = 0
+        if cnt.value > 1:
+            want = str(getattr(torch.cuda.get_device_properties(idx), "uuid", ""))
+            buf = ctypes.create_string_buffer(96)
+            pick = -1
+            for i in range(cnt.value):
+                self.nv.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(self.h))
+                self.nv.nvmlDeviceGetUUID(self.h, buf, 96)
+                if want and want in buf.value.decode():
+                    pick = i
+                    break
+            if pick < 0:
+                raise RuntimeError("cannot match the CUDA device to an NVML device")
+        if self.nv.nvmlDeviceGetHandleByIndex_v2(pick, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+
+    def _u(self, fn, *args, ull=False):
+        v = self.ct.c_ulonglong() if ull else self.ct.c_uint()
+        if fn(self.h, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError(f"{fn.__name__} failed")
+        return v.value
+
+    def energy_mj(self) -> int:
+        return self._u(self.nv.nvmlDeviceGetTotalEnergyConsumption, ull=True)
+
+    def sm_mhz(self) -> int:
+        return self._u(self.nv.nvmlDeviceGetClockInfo, 1)   # NVML_CLOCK_SM
+
+    def power_limit_w(self) -> float:
+        return self._u(self.nv.nvmlDeviceGetEnforcedPowerLimit) / 1000.0
+
+
+def run_energy(args):
+    """Energy per call of one workload in its fused, GEMM-only and unfused
+    modes: NVML's total-energy counter read around ~3 s of back-to-back calls
+    per mode, modes interleaved over three rounds, medians reported.  Under
+    the power limit the fused call's extra time over GEMM-only follows its
+    extra energy: exposed time ~ extra energy / power."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import comm_gemm_tile_gb300 as mk
+    from comm_gemm_tile_gb300 import build as mkbuild
+    mkbuild.build()
+    nv = Nvml(0)
+    ws = mk.Workspace(device)
+    call = profile_call(mk, args.energy, args.scale == "small", device, ws)
+    modes = {"fused": None, "gemm_only": mk.Config(mode=mk.MODE_GEMM_ONLY),
+             "unfused": mk.Config(mode=mk.MODE_UNFUSED)}
+    res: dict = {m: [] for m in modes}
+    for _ in range(3):
+        for m, cfg in modes.items():
+            for _ in range(5):
+                call(cfg)
+            torch.cuda.synchronize()
+            t = time.time()
+            n = 0
+            while time.time() - t < 0.3:
+                call(cfg)
+                n += 1
+            torch.cuda.synchronize()
+            n = max(10, int(args.energy_secs / ((time.time() - t) / n)))
+            clk = []
+            e0, t0 = nv.energy_mj(), time.time()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record()
+            last = t0
+            for _ in range(n):
+                call(cfg)
+                if time.time() - last > 0.05:
+                    clk.append(nv.sm_mhz())
+                    last = time.time()
+            ev1.record()
+            torch.cuda.synchronize()
+            e1, t1 = nv.energy_mj(), time.time()
+            res[m].append({"us": ev0.elapsed_time(ev1) / n * 1e3, "mj": (e1 - e0) / n,
+                           "w": (e1 - e0) / (t1 - t0) / 1e3,
+                           "sm_mhz": statistics.median(clk) if clk else None})
+    st, detail = mk.device_status(ws)
+    med = {m: {k: statistics.median(r[k] for r in v) if v[0][k] is not None else None
+               for k in ("us", "mj", "w", "sm_mhz")} for m, v in res.items()}
+    de = med["fused"]["mj"] - med["gemm_only"]["mj"]
+    print(json.dumps({"energy": args.energy, "scale": args.scale, "power_limit_w": nv.power_limit_w(),
+                      "modes": med, "exposed_us": med["fused"]["us"] - med["gemm_only"]["us"],
+                      "extra_energy_mj": de,
+                      "extra_energy_us_at_fused_power": de / med["fused"]["w"] * 1e3,
+                      "status": mk.status_string(st), "detail": detail}), flush=True)
+    return 0 if st == mk.MK_OK else 1
+
+
+def run_profile(args):
+    """Untimed fused calls of one workload (profiling aid: ncu captures one of
+    them).  --scale small shrinks the row / token / position counts, keeping the
+    inputs larger than L2, so that multi-pass captures stay small."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import comm_gemm_tile_gb300 as mk
+    from comm_gemm_tile_gb300 import build as mkbuild
+    mkbuild.build()
+    ws = mk.Workspace(device)
+    name = args.profile
+    call = profile_call(mk, name, args.scale == "small", device, ws)
     for _ in range(args.calls):
         call()
     torch.cuda.synchronize()
