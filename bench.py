@@ -688,9 +688,10 @@ def profile_call(mk, name, small, device, ws):
 
 
 class Nvml:
-    """Read-only NVML queries through the driver's own library (no Python
-    bindings needed): the total-energy counter (mJ), the SM clock and the
-    enforced power limit of the GPU that CUDA device `idx` is."""
+    """Read-only NVML queries through NVIDIA's management library,
+    libnvidia-ml (no Python bindings needed): the total-energy counter (mJ),
+    the SM clock and the enforced power limit of the GPU that CUDA device
+    `idx` is."""
 
     def __init__(self, idx: int = 0):
         import ctypes

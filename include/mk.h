@@ -65,7 +65,7 @@ typedef struct CUstream_st *mk_stream_t;
 typedef enum {
   MK_OK = 0,
   MK_ERR_INVALID = 1,      /* bad argument (NULL pointer, bad size, misaligned, R out of range) */
-  MK_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (e.g. no sm_103a device)   */
+  MK_ERR_UNSUPPORTED = 2,  /* valid request the library cannot serve (e.g. no sm_103a device) */
   MK_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                                 */
   MK_ERR_TIMEOUT = 4,      /* device: a bounded wait gave up (missing flag / stalled pipeline)  */
   MK_ERR_CAPACITY = 5      /* device: MoE rows for a rank exceeded cap_rows                     */
