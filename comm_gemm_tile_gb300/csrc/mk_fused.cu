@@ -894,6 +894,36 @@ __device__ __forceinline__ void flush_staged(const FusedParams& p, const Item& i
   }
 }
 
+// One 32-column chunk of the warp's 32 rows stored through its staging: lane
+// l's piece goes to shared memory, and once a 128-byte segment of every row
+// is staged (two bf16 chunks, one fp32 chunk) the warp writes it out, lane l
+// taking 16 bytes of row 4j + l/8, so each store instruction covers four whole
+// 128-byte row segments instead of 32 separate 16-byte pieces.  row_ptr: this
+// lane's row (byte address of column 0), 0 to skip the row; columns at or
+// past ncols are skipped.  Called by all 32 lanes, chunks c = 0, 1, ... in order.
+__device__ __forceinline__ void staged_chunk(uint32_t stage, int lane, int c, const uint32_t (&r)[32], bool f32,
+                                             unsigned long long row_ptr, int n0, int ncols) {
+  const int per = f32 ? 1 : 2;   // chunks per staged 128-byte segment
+  stage_piece(stage, lane, (c % per) * 64, r, f32);
+  if (c % per != per - 1) return;
+  __syncwarp();
+  const int esz = f32 ? 4 : 2;
+  const int pc = n0 + 32 * (c - per + 1) + (lane & 7) * (16 / esz);   // first column of this lane's piece
+#pragma unroll 1
+  for (int j = 0; j < 8; ++j) {
+    const int row = 4 * j + (lane >> 3);
+    const unsigned long long dst = __shfl_sync(0xffffffffu, row_ptr, row);
+    uint32_t v0, v1, v2, v3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                 : "r"(stage + static_cast<uint32_t>(row * EPI_ROW_STRIDE + (lane & 7) * 16))
+                 : "memory");
+    if (dst != 0ull && pc + 16 / esz <= ncols)
+      st_global_v4(reinterpret_cast<uint8_t*>(dst) + static_cast<size_t>(pc) * esz, v0, v1, v2, v3);
+  }
+  __syncwarp();
+}
+
 // fp32 load through L2 (not L1) with an L2 eviction policy.
 __device__ __forceinline__ float4 ld_cg_f4_pol(const float* ptr, uint64_t pol) {
   float4 v;
@@ -1052,7 +1082,7 @@ __device__ __forceinline__ void release_tmem(const ComputeSmem& S, int buf, uint
 template <bool PAIR>
 __device__ __forceinline__ void combine_epilogue(const FusedParams& p, const ComputeSmem& S, const Item& it,
                                                  uint32_t taddr, int buf, uint32_t rank, int lane, int trow,
-                                                 bool row_ok, int grow) {
+                                                 bool row_ok, int grow, uint32_t epi) {
   const int topk = p.moe_topk, T = p.moe_T;
   const int n0 = it.nb * BN;
   int r = 0, t = 0, k = 0;
@@ -1069,14 +1099,13 @@ __device__ __forceinline__ void combine_epilogue(const FusedParams& p, const Com
     }
   }
   uint8_t* slot_row = p.moe_ret[r] + (static_cast<size_t>(t) * topk + k) * p.N * 2;
+  const unsigned long long my_row = row_ok ? reinterpret_cast<unsigned long long>(slot_row) : 0ull;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t v[32];
     tc_ld_32x32b_x32(taddr + 32u * c, v);
     tc_wait_ld();
-    const int col = n0 + 32 * c;
-    const int nvalid = max(0, min(32, p.N - col));
-    if (row_ok && nvalid > 0) store_row_chunk(slot_row + static_cast<size_t>(col) * 2, v, nvalid, false);
+    staged_chunk(epi, lane, c, v, false, my_row, n0, p.N);
   }
   tc_fence_before();
   __syncwarp();
@@ -1501,7 +1530,7 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
       }
       continue;
     } else if (p.op == OP_MOE_COMBINE) {
-      combine_epilogue<PAIR>(p, S, it, taddr, buf, rank, lane, trow, row_ok, grow);
+      combine_epilogue<PAIR>(p, S, it, taddr, buf, rank, lane, trow, row_ok, grow, epi);
       __syncwarp();   // lanes that handed a row over rejoin before the next tcgen05.ld
       if (++buf == 2) {
         buf = 0;
@@ -1511,17 +1540,15 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
     } else if (it.phase == 1) {
       // chained MLP up-projection: H_r = bf16(ReLU(acc)) into rank hid_r's hidden buffer
       uint8_t* hrow = p.mlp_hid[it.hid_r] + static_cast<size_t>(grow) * p.mlp_f * 2;
+      const unsigned long long hptr = row_ok ? reinterpret_cast<unsigned long long>(hrow) : 0ull;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tc_ld_32x32b_x32(taddr + 32u * c, r);
         tc_wait_ld();
-        const int col = n0 + 32 * c;
-        const int nvalid = max(0, min(32, p.mlp_f - col));
-        if (!row_ok || nvalid == 0) continue;
 #pragma unroll
         for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(fmaxf(__uint_as_float(r[q]), 0.f));
-        store_row_chunk(hrow + static_cast<size_t>(col) * 2, r, nvalid, false);
+        staged_chunk(epi, lane, c, r, false, hptr, n0, p.mlp_f);
       }
     } else if (it.slot >= 0) {
       // Partial tile -> staging slot.  Layout: float4 (row, column group cg)
@@ -1538,6 +1565,29 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
           st_global_v4(d, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         }
       }
+    } else if (p.op != OP_AR || it.rep >= 0) {
+      // one destination row per lane: staged stores
+      uint8_t* base;
+      size_t orow;
+      if (p.op == OP_AG || p.op == OP_MOE) {
+        base = reinterpret_cast<uint8_t*>(p.out[p.op == OP_MOE ? it.mb : 0]);
+        orow = static_cast<size_t>(grow);
+      } else if (p.op == OP_RS || p.op == OP_MLP) {
+        const int o = row_ok ? grow / p.rows_per_owner : 0;
+        base = reinterpret_cast<uint8_t*>(p.out[o]);
+        orow = static_cast<size_t>(row_ok ? grow - o * p.rows_per_owner : 0);
+      } else {   // AR baseline: this rank's product to its replica
+        base = reinterpret_cast<uint8_t*>(p.out[it.rep]);
+        orow = static_cast<size_t>(grow);
+      }
+      const unsigned long long optr = row_ok ? reinterpret_cast<unsigned long long>(base + orow * p.N * esz) : 0ull;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr + 32u * c, r);
+        tc_wait_ld();
+        staged_chunk(epi, lane, c, r, p.out_f32 != 0, optr, n0, p.N);
+      }
     } else {
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -1547,21 +1597,9 @@ __device__ void epilogue(const FusedParams& p, const ComputeSmem& S, uint32_t tm
         const int col = n0 + 32 * c;
         const int nvalid = max(0, min(32, p.N - col));
         if (!row_ok || nvalid == 0) continue;
-        if (p.op == OP_AG || p.op == OP_MOE) {
-          uint8_t* base = reinterpret_cast<uint8_t*>(p.out[p.op == OP_MOE ? it.mb : 0]);
-          store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
-        } else if (p.op == OP_RS || p.op == OP_MLP) {
-          const int o = grow / p.rows_per_owner, lr = grow - o * p.rows_per_owner;
+        for (int o = 0; o < p.R; ++o) {   // AR: the same bits to every replica
           uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
-          store_row_chunk(base + (static_cast<size_t>(lr) * p.N + col) * esz, r, nvalid, p.out_f32);
-        } else if (it.rep >= 0) {   // AR baseline: this rank's product to its replica
-          uint8_t* base = reinterpret_cast<uint8_t*>(p.out[it.rep]);
           store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
-        } else {  // OP_AR: the same bits to every replica
-          for (int o = 0; o < p.R; ++o) {
-            uint8_t* base = reinterpret_cast<uint8_t*>(p.out[o]);
-            store_row_chunk(base + (static_cast<size_t>(grow) * p.N + col) * esz, r, nvalid, p.out_f32);
-          }
         }
       }
     }
